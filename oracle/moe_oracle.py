@@ -1,0 +1,391 @@
+"""Plain CPU oracle for the forward pass of one sparse Mixture-of-Experts layer.
+
+TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
+module. The CUDA product path never imports, calls or links anything here, and
+nothing here imports the product package.
+
+Every step follows the pages literally, in their order, and is written for a
+reader to check by eye rather than for speed:
+
+  router logits -> softmax / top-k gates -> counts, capacity, aux loss
+  -> dispatch (group rows by expert) -> expert FFN per group
+  -> combine (gate-weighted sum per token) + shared expert + residual.
+
+Precision. The router logits are fp32 with one fixed summation order (see
+``router_logits.c``), because the top-k decision is an integer result that the
+CUDA router must reproduce bit for bit; the decision is therefore taken in the
+kernel's precision on identical values. Everything after the logits (softmax,
+gates, aux loss, expert FFNs, combine) is float64 on the exact values of the
+(bf16 or fp32) inputs.
+
+Page references used below:
+  [MoE glossary]   "Mixture of Experts (MoE)" glossary page (inferensys.com)
+  [Switch]         "Switch Transformers: Mixture of Experts explained" (thelatentdaily.com)
+  [Noisy top-k]    "Noise Top-k Gating" glossary page (inferensys.com)
+  [Choosing MLPs]  "MoE: Choosing Which MLPs to Use for Each Token" (llm-systems-engineering)
+  [DeepSeekMoE eq] "Mixture-of-Experts (MoE)" ml-notes page, the MoE-layer equation
+                   h_t = sum_i g_{i,t} FFN_i(u_t) + u_t quoted from DeepSeekMoE.
+
+Readings where the pages are silent (each also listed in the design doc):
+  * top-k selects by logit, descending, lower expert index first on equal values;
+  * softmax-then-top-k gates are not renormalised (DeepSeekMoE eq.);
+  * capacity C = ceil(T * cf / N); priority is slot-major (all first choices in
+    token order, then all second choices, ...); a dropped slot contributes 0 and
+    the remaining gates are not renormalised;
+  * kept rows are grouped by expert ascending, token ascending inside a group;
+  * aux loss is reported in two forms (Switch form and the variance form);
+  * expert FFNs have no biases; SiLU(z) = z / (1 + exp(-z)).
+
+Parity pins: the aux-loss *form* has no printed formula on the pages, so which
+of the two values "the" auxiliary loss is stays parity unpinned; the
+arithmetic of both forms is pinned by closed-form cases in tests/test_oracle.py.
+"""
+from __future__ import annotations
+
+import ctypes
+import pathlib
+import subprocess
+
+import numpy as np
+
+_HERE = pathlib.Path(__file__).resolve().parent
+_SO = _HERE / "_liboracle.so"
+_SRC = _HERE / "router_logits.c"
+_lib = None
+
+GATING_SOFTMAX_THEN_TOPK = "softmax_then_topk"
+GATING_TOPK_THEN_SOFTMAX = "topk_then_softmax"
+
+
+def build(force: bool = False) -> pathlib.Path:
+    """Compile the C part of the oracle (plain gcc, no GPU headers)."""
+    if force or not _SO.exists() or _SO.stat().st_mtime < _SRC.stat().st_mtime:
+        # -mfma makes fmaf a single instruction; its result is the correctly
+        # rounded fused multiply-add either way (libm's fmaf is exact too).
+        cmd = ["gcc", "-O3", "-mfma", "-fno-fast-math", "-ffp-contract=off",
+               "-shared", "-fPIC", "-o", str(_SO), str(_SRC), "-lm"]
+        subprocess.run(cmd, check=True)
+    return _SO
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(str(_SO))
+        lib.oracle_router_logits.restype = None
+        lib.oracle_router_logits.argtypes = [ctypes.c_long] * 3 + [ctypes.c_void_p] * 4
+        _lib = lib
+    return _lib
+
+
+# --------------------------------------------------------------------------- router
+
+def router_logits(x: np.ndarray, w_r: np.ndarray, b: np.ndarray | None = None) -> np.ndarray:
+    """fp32 logits L[t, e] = sum_i x[t, i] * W_r[i, e] (+ b[e]).
+
+    [Noisy top-k] router paragraph (one linear layer to one logit per expert);
+    [Choosing MLPs] section "Router: Selecting Experts and Computing Weights",
+    Figure 2 (W_r is d x N); [DeepSeekMoE eq] the affinity u_t^T e_i; [Switch]
+    section "Making it work" (the router runs in higher precision).
+    Summation order: fused multiply-add per feature in increasing index (C code).
+    """
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    w_r = np.ascontiguousarray(w_r, dtype=np.float32)
+    T, d = x.shape
+    d2, N = w_r.shape
+    assert d == d2
+    assert np.isfinite(x).all() and np.isfinite(w_r).all(), "router inputs must be finite"
+    out = np.empty((T, N), dtype=np.float32)
+    bp = None
+    if b is not None:
+        b = np.ascontiguousarray(b, dtype=np.float32)
+        assert b.shape == (N,)
+        bp = b.ctypes.data
+    _load().oracle_router_logits(T, d, N, x.ctypes.data, w_r.ctypes.data, bp, out.ctypes.data)
+    return out
+
+
+def select_topk(logits: np.ndarray, k: int) -> np.ndarray:
+    """Indices of the k largest logits per token, largest first.
+
+    [MoE glossary] top-k gating bullet (the k experts with the highest scores
+    process the token); [Choosing MLPs] section "Router: Selecting Experts and
+    Computing Weights" (top-2 keeps the two largest scores); [DeepSeekMoE eq]
+    the Topk(., K) set. Softmax is monotone, so selecting on logits is
+    the same set as selecting on the affinities s in exact arithmetic.
+    Equal logits: the lower expert index comes first (a stable sort of -logit;
+    -0.0 and +0.0 compare equal).
+    """
+    order = np.argsort(-logits, axis=1, kind="stable")
+    return order[:, :k].astype(np.int64)
+
+
+def softmax_all(logits: np.ndarray) -> np.ndarray:
+    """p[t, e] = exp(L[t, e] - max_e L) / sum_e' exp(L[t, e'] - max_e L), float64.
+
+    [MoE glossary] gating-network paragraph (a softmax turns the router output
+    into a probability vector over every expert); [DeepSeekMoE eq]
+    s_{i,t} = Softmax_i(u_t^T e_i).
+    """
+    L = logits.astype(np.float64)
+    z = np.exp(L - L.max(axis=1, keepdims=True))
+    return z / z.sum(axis=1, keepdims=True)
+
+
+def gates(logits: np.ndarray, idx: np.ndarray, gating: str) -> np.ndarray:
+    """Gate weight per selected slot, float64 [T][k].
+
+    softmax_then_topk: g = s at the selected experts, not renormalised
+      ([DeepSeekMoE eq]: g_{i,t} = s_{i,t} if s_{i,t} in Topk, else 0).
+    topk_then_softmax: softmax over the k selected logits only
+      ([Choosing MLPs] section "Router: Selecting Experts and Computing
+      Weights": the softmax runs over the two selected scores only, so the
+      weights add up to 1).
+    """
+    if gating == GATING_SOFTMAX_THEN_TOPK:
+        p = softmax_all(logits)
+        return np.take_along_axis(p, idx, axis=1)
+    if gating == GATING_TOPK_THEN_SOFTMAX:
+        sel = np.take_along_axis(logits, idx, axis=1).astype(np.float64)
+        z = np.exp(sel - sel.max(axis=1, keepdims=True))
+        return z / z.sum(axis=1, keepdims=True)
+    raise ValueError(gating)
+
+
+# --------------------------------------------------------------- counts, capacity, aux
+
+def counts_routed(idx: np.ndarray, N: int) -> np.ndarray:
+    """Number of (token, slot) selections per expert, before any capacity drop."""
+    return np.bincount(idx.reshape(-1), minlength=N).astype(np.int64)
+
+
+def capacity(T: int, N: int, capacity_factor) -> int | None:
+    """Expert capacity C = (tokens_per_batch / num_experts) * capacity_factor,
+    rounded up ([MoE glossary] capacity-factor paragraph). None: no limit."""
+    if capacity_factor is None:
+        return None
+    num, den = capacity_factor
+    return (T * num + N * den - 1) // (N * den)
+
+
+def keep_within_capacity(idx: np.ndarray, N: int, C: int | None) -> np.ndarray:
+    """kept[t, j]: slot j of token t is processed by its expert.
+
+    [MoE glossary] capacity-factor paragraph: assignments beyond an expert's
+    capacity are dropped and the token passes through the residual; [Switch]
+    section "Making it work": tokens over the limit bypass the layer. Priority
+    (a reading): slot-major, i.e. every token's first choice in token order,
+    then every second choice, and so on.
+    """
+    T, k = idx.shape
+    kept = np.ones((T, k), dtype=bool)
+    if C is None:
+        return kept
+    used = [0] * N
+    for j in range(k):
+        for t in range(T):
+            e = int(idx[t, j])
+            if used[e] < C:
+                used[e] += 1
+            else:
+                kept[t, j] = False
+    return kept
+
+
+def group_by_expert(idx: np.ndarray, kept: np.ndarray, N: int):
+    """Dispatch: group the kept (token, slot) pairs by expert.
+
+    [Choosing MLPs] section "From Router to Combine", Figure 3: dispatch collects,
+    for each expert, the tokens that chose it (E1 gets x1 and x3, E2 gets x2, E3
+    gets x1, x2 and x3, E4 gets nothing). Rows are ordered by expert, then by
+    token, the order in which the figure lists them.
+
+    Returns counts_kept [N], expert_offsets [N+1], perm_token [R] (token of each
+    row), slot_row [T][k] (row of each slot, -1 when dropped).
+    """
+    T, k = idx.shape
+    groups = [[] for _ in range(N)]
+    for t in range(T):
+        for j in range(k):
+            if kept[t, j]:
+                groups[int(idx[t, j])].append((t, j))
+    counts_kept = np.array([len(g) for g in groups], dtype=np.int64)
+    offsets = np.zeros(N + 1, dtype=np.int64)
+    offsets[1:] = np.cumsum(counts_kept)
+    perm_token = np.empty(int(offsets[-1]), dtype=np.int64)
+    slot_row = np.full((T, k), -1, dtype=np.int64)
+    for e in range(N):
+        for r, (t, j) in enumerate(groups[e]):
+            perm_token[offsets[e] + r] = t
+            slot_row[t, j] = offsets[e] + r
+    return counts_kept, offsets, perm_token, slot_row
+
+
+def aux_losses(p: np.ndarray, routed: np.ndarray, k: int):
+    """Auxiliary load-balancing loss, two forms (the pages print no formula).
+
+    P_e = mean over tokens of the full softmax p[t, e]; f_e = routed_e / (T k)
+    (selections before capacity drops).
+      form 0 (Switch form):  N * sum_e f_e P_e   ([Switch] section "Making it
+              work" names a load-balancing loss that pushes the router toward an
+              even spread; the expression itself is a reading, not printed)
+      form 1 (variance form): (1/N) sum_e (P_e - 1/N)^2  ([Noisy top-k] load-
+              balancing bullets and [MoE glossary] auxiliary-loss paragraph: the
+              loss penalises how unevenly the routing probability is spread over
+              the experts, measured as a variance)
+    """
+    T, N = p.shape
+    P = p.mean(axis=0)
+    f = routed.astype(np.float64) / float(T * k)
+    return float(N * np.sum(f * P)), float(np.mean((P - 1.0 / N) ** 2))
+
+
+# ------------------------------------------------------------------------- experts
+
+def silu(z: np.ndarray) -> np.ndarray:
+    """SiLU(z) = z / (1 + exp(-z))."""
+    with np.errstate(over="ignore"):
+        return z / (1.0 + np.exp(-z))
+
+
+def expert_ffn(xr: np.ndarray, w_a, w_b, w_out, act: str) -> np.ndarray:
+    """One expert applied to each row of xr independently, float64.
+
+    act="silu_gated": W_down (SiLU(W_gate x) * (W_up x)) — a gated MLP with
+      separate gate, up and down projections per expert ([Choosing MLPs]
+      section "Dense MLP and MoE", Figure 1; [MoE glossary]: experts are
+      independent feed-forward networks).
+    act="relu": W2 max(0, W1 x) — the plain FFN of [DeepSeekMoE eq]'s text.
+    Weights use the [out][in] layout: w_a/w_b [h][d], w_out [d][h].
+    """
+    xr = np.asarray(xr, dtype=np.float64)
+    wa = np.asarray(w_a, dtype=np.float64)
+    wo = np.asarray(w_out, dtype=np.float64)
+    if act == "silu_gated":
+        wb = np.asarray(w_b, dtype=np.float64)
+        hid = silu(xr @ wa.T) * (xr @ wb.T)
+    elif act == "relu":
+        hid = np.maximum(xr @ wa.T, 0.0)
+    else:
+        raise ValueError(act)
+    return hid @ wo.T
+
+
+# ------------------------------------------------------------------------- layer
+
+def route(cfg, x, w_r, b_r=None) -> dict:
+    """Router, gates, counts, capacity, aux loss and dispatch order for all tokens."""
+    L = router_logits(x, w_r, b_r)
+    idx = select_topk(L, cfg.k)
+    g = gates(L, idx, cfg.gating)
+    p = softmax_all(L)
+    routed = counts_routed(idx, cfg.N)
+    C = capacity(cfg.T, cfg.N, cfg.capacity_factor)
+    kept = keep_within_capacity(idx, cfg.N, C)
+    counts_kept, offsets, perm_token, slot_row = group_by_expert(idx, kept, cfg.N)
+    aux = aux_losses(p, routed, cfg.k)
+    return dict(logits=L, topk_idx=idx, topk_gate=g, p=p, counts_routed=routed,
+                capacity=C, kept=kept, counts_kept=counts_kept, expert_offsets=offsets,
+                perm_token=perm_token, slot_row=slot_row, aux=aux)
+
+
+def shared_expert(xr, sw_gate, sw_up, sw_down) -> np.ndarray:
+    """Always-on shared expert S(x), a gated MLP applied to every token
+    ([Choosing MLPs] "Shared Expert: A Transformation Applied to Every Token",
+    Figure 4: y = S(x) + R(x))."""
+    return expert_ffn(xr, sw_gate, sw_up, sw_down, "silu_gated")
+
+
+def layer_output(cfg, x, rt: dict, w_gate, w_up, w_down,
+                 sw_gate=None, sw_up=None, sw_down=None, tokens=None) -> np.ndarray:
+    """Layer output y for `tokens` (all tokens when None), float64 [len(tokens)][d].
+
+    Dispatch -> expert computation -> combine ([Choosing MLPs] "From Router to
+    Combine", Figure 3), then the shared expert ([Choosing MLPs] Figure 4) and the
+    residual ([DeepSeekMoE eq]: + u_t; [MoE glossary]: dropped overflow keeps the
+    residual). Only the dispatched rows whose token is requested are computed.
+    """
+    T = cfg.T
+    tokens = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    want = np.zeros(T, dtype=bool)
+    want[tokens] = True
+    perm_token, offsets = rt["perm_token"], rt["expert_offsets"]
+    R = len(perm_token)
+    y_perm = {}                                    # row -> expert output (float64 [d])
+    for e in range(cfg.N):
+        rows = [r for r in range(int(offsets[e]), int(offsets[e + 1])) if want[perm_token[r]]]
+        if not rows:
+            continue
+        xe = np.asarray(x[perm_token[rows]], dtype=np.float64)   # dispatch: gather rows
+        ye = expert_ffn(xe, w_gate[e], None if w_up is None else w_up[e], w_down[e], cfg.act)
+        for i, r in enumerate(rows):
+            y_perm[r] = ye[i]
+    assert all(0 <= r < R for r in y_perm)
+    xt = np.asarray(x[tokens], dtype=np.float64)
+    out = np.zeros_like(xt)
+    for n, t in enumerate(tokens):                 # combine: weighted sum per token
+        for j in range(cfg.k):
+            r = int(rt["slot_row"][t, j])
+            if r >= 0:
+                out[n] += rt["topk_gate"][t, j] * y_perm[r]
+    if cfg.h_shared:
+        out += shared_expert(xt, sw_gate, sw_up, sw_down)
+    return out + xt
+
+
+def forward(cfg, inp: dict, tokens=None) -> dict:
+    """Whole layer: routing for all tokens, outputs for `tokens` (default all)."""
+    rt = route(cfg, inp["x"], inp["w_r"], inp.get("b_r"))
+    rt["y"] = layer_output(cfg, inp["x"], rt, inp["w_gate"], inp.get("w_up"), inp["w_down"],
+                           inp.get("shared_w_gate"), inp.get("shared_w_up"),
+                           inp.get("shared_w_down"), tokens)
+    return rt
+
+
+def forward_dense(cfg, inp: dict) -> np.ndarray:
+    """Brute-force dense evaluation of the DeepSeekMoE equation on tiny inputs.
+
+    h_t = sum_{i=1..N} g_{i,t} FFN_i(u_t) + u_t with g the dense N-vector (the
+    gate at kept selected experts, 0 elsewhere); every expert is computed for
+    every token and then masked. Plus S(u_t) when a shared expert is present.
+    """
+    rt = route(cfg, inp["x"], inp["w_r"], inp.get("b_r"))
+    x = np.asarray(inp["x"], dtype=np.float64)
+    G = np.zeros((cfg.T, cfg.N))
+    for t in range(cfg.T):
+        for j in range(cfg.k):
+            if rt["kept"][t, j]:
+                G[t, rt["topk_idx"][t, j]] = rt["topk_gate"][t, j]
+    y = x.copy()
+    for i in range(cfg.N):
+        wu = None if inp.get("w_up") is None else inp["w_up"][i]
+        y += G[:, i:i + 1] * expert_ffn(x, inp["w_gate"][i], wu, inp["w_down"][i], cfg.act)
+    if cfg.h_shared:
+        y += shared_expert(x, inp["shared_w_gate"], inp["shared_w_up"], inp["shared_w_down"])
+    return y
+
+
+def config_from(T, d, N, k, h, h_shared=0, gating=GATING_TOPK_THEN_SOFTMAX,
+                act="silu_gated", capacity_factor=None):
+    """A plain attribute bag with the fields the oracle reads."""
+    class _Cfg:
+        pass
+    c = _Cfg()
+    c.T, c.d, c.N, c.k, c.h, c.h_shared = T, d, N, k, h, h_shared
+    c.gating, c.act, c.capacity_factor = gating, act, capacity_factor
+    return c
+
+
+def tokens_per_second_sample(cfg, inp: dict, tokens) -> float:
+    """Time the oracle on a token sample (routing for all tokens, outputs for the
+    sample); returns sample tokens per second."""
+    import time
+    t0 = time.perf_counter()
+    forward(cfg, inp, tokens=tokens)
+    return len(tokens) / (time.perf_counter() - t0)
+
+
+__all__ = [n for n in dir() if not n.startswith("_") and n not in ("ctypes", "np", "pathlib",
+                                                                   "subprocess")]

@@ -1,0 +1,464 @@
+"""Pins for the CPU oracle: each checks it against something other than itself.
+
+The pins are the pages' worked examples (fixtures under tests/golden/), closed
+forms, invariants, textbook/library routines on special cases and brute force on
+tiny inputs. The last group plants plausible mistakes in the oracle and checks
+that some pin catches each of them.
+"""
+import math
+import os
+import random
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+from oracle import moe_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_fixture(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                rows.append(line.split())
+    return rows
+
+
+def _kv(rows):
+    out = {}
+    for r in rows:
+        out.setdefault(r[0], []).append(r[1:])
+    return out
+
+
+# ----------------------------------------------------------------- exact arithmetic
+
+def _round_f32(v: Fraction) -> float:
+    """Round a rational to the nearest binary32 value, ties to even (IEEE 754)."""
+    if v == 0:
+        return 0.0
+    s = -1 if v < 0 else 1
+    a = abs(v)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    ulp = Fraction(2) ** (max(e, -126) - 23)
+    q = a / ulp
+    n = q.numerator // q.denominator
+    rem = q - n
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    return float(np.float32(s * n * ulp))
+
+
+def _fma_f32(a, b, c):
+    return _round_f32(Fraction(float(a)) * Fraction(float(b)) + Fraction(float(c)))
+
+
+def pin_router_logits_exact(O):
+    """Each logit equals the fp32 chain acc = fma(x_i, w_i, acc), i increasing,
+    evaluated here with exact rationals and IEEE round-to-nearest-even."""
+    rng = np.random.default_rng(7)
+    T, d, N = 3, 24, 5
+    x = rng.standard_normal((T, d)).astype(np.float32) * np.float32(3.0)
+    w = rng.standard_normal((d, N)).astype(np.float32)
+    b = rng.standard_normal(N).astype(np.float32)
+    L = O.router_logits(x, w, b)
+    for t in range(T):
+        for e in range(N):
+            acc = 0.0
+            for i in range(d):
+                acc = _fma_f32(x[t, i], w[i, e], acc)
+            acc = _round_f32(Fraction(acc) + Fraction(float(b[e])))
+            assert L[t, e] == np.float32(acc), (t, e, L[t, e], acc)
+
+
+def pin_router_logits_error_bound(O):
+    """|fp32 logit - exact dot| <= gamma_d * sum |x_i w_i| (+ one rounding for b)."""
+    rng = np.random.default_rng(11)
+    for (T, d, N) in [(5, 64, 4), (3, 768, 8), (2, 1000, 7)]:
+        x = rng.standard_normal((T, d)).astype(np.float32)
+        w = (rng.standard_normal((d, N)) / math.sqrt(d)).astype(np.float32)
+        L = O.router_logits(x, w)
+        exact = x.astype(np.float64) @ w.astype(np.float64)
+        mag = np.abs(x.astype(np.float64)) @ np.abs(w.astype(np.float64))
+        u = 2.0 ** -24
+        gamma = d * u / (1 - d * u)
+        assert np.all(np.abs(L - exact) <= gamma * mag + 1e-30)
+
+
+def pin_topk_brute_force(O):
+    """Top-k equals a brute-force ordering by (value descending, index ascending),
+    including exact ties and signed zeros."""
+    rng = random.Random(3)
+    for _ in range(200):
+        N = rng.randint(1, 12)
+        k = rng.randint(1, N)
+        vals = [rng.choice([-2.0, -1.0, -0.0, 0.0, 0.5, 1.0, 3.0]) for _ in range(N)]
+        L = np.array([vals], dtype=np.float32)
+        want = sorted(range(N), key=lambda e: (-vals[e], e))[:k]
+        got = O.select_topk(L, k)[0].tolist()
+        assert got == want, (vals, k, got, want)
+
+
+def pin_worked_example(O):
+    """Fixture: the pages' d=8, four-expert, top-2 router example."""
+    kv = _kv(_read_fixture("router_worked_example.txt"))
+    d, N, k = int(kv["d"][0][0]), int(kv["N"][0][0]), int(kv["k"][0][0])
+    scores = [float(v) for v in kv["scores"][0]]
+    sel = [int(v) - 1 for v in kv["selected"][0]]
+    wts = [float(v) for v in kv["weights"][0]]
+    tol = float(kv["tolerance"][0][0])
+    x = np.zeros((1, d), np.float32)
+    x[0, 0] = 1.0                                 # x = e_1, so the scores are W_r row 0
+    w_r = np.zeros((d, N), np.float32)
+    w_r[0] = scores
+    L = O.router_logits(x, w_r)
+    assert L[0].tolist() == scores
+    idx = O.select_topk(L, k)
+    assert idx[0].tolist() == sel
+    g = O.gates(L, idx, O.GATING_TOPK_THEN_SOFTMAX)
+    assert np.allclose(g[0], wts, atol=tol)
+    # closed form: e^2 / (e^1 + e^2) = 1 / (1 + e^-1)
+    assert abs(g[0, 0] - 1.0 / (1.0 + math.exp(-1.0))) < 1e-12
+    assert abs(g[0, 1] - 1.0 / (1.0 + math.exp(1.0))) < 1e-12
+    assert abs(g[0].sum() - 1.0) < 1e-12
+
+
+def _three_token_setup():
+    kv = _kv(_read_fixture("dispatch_three_tokens.txt"))
+    T, d, N, k = (int(kv[n][0][0]) for n in ("tokens", "d", "N", "k"))
+    w = {(int(a), int(b)): float(c) for a, b, c in kv["weight"]}
+    # Scores chosen so that each token's top-2 and softmax weights are the page's:
+    # a gap ln(w / (1 - w)) between the two selected experts, others far below.
+    scores = np.full((T, N), -8.0)
+    scores[0, 0], scores[0, 2] = 0.0, math.log(w[(1, 3)] / w[(1, 1)])
+    scores[1, 1], scores[1, 2] = 0.0, 0.25
+    scores[2, 0], scores[2, 2] = math.log(w[(3, 1)] / (1 - w[(3, 1)])), 0.0
+    x = np.zeros((T, d), np.float32)
+    w_r = np.zeros((d, N), np.float32)
+    for t in range(T):
+        x[t, t] = 1.0
+        w_r[t] = scores[t].astype(np.float32)
+    return kv, T, d, N, k, w, x, w_r
+
+
+def pin_three_token_dispatch(O):
+    """Fixture: the pages' three-token Router -> Dispatch -> Combine example."""
+    kv, T, d, N, k, w, x, w_r = _three_token_setup()
+    cfg = O.config_from(T=T, d=d, N=N, k=k, h=8)
+    rt = O.route(cfg, x, w_r)
+    for tok, a, b in kv["select"]:
+        assert sorted((rt["topk_idx"][int(tok) - 1] + 1).tolist()) == [int(a), int(b)]
+    tol = float(kv["tolerance"][0][0])
+    for (tok, e), val in w.items():
+        j = rt["topk_idx"][tok - 1].tolist().index(e - 1)
+        assert abs(rt["topk_gate"][tok - 1, j] - val) <= tol
+    groups = {int(g[0]): [int(v) - 1 for v in g[1:]] for g in kv["group"]}
+    counts = [len(groups[e + 1]) for e in range(N)]
+    assert rt["counts_kept"].tolist() == counts == [2, 1, 3, 0]
+    assert rt["expert_offsets"].tolist() == [0, 2, 3, 6, 6]
+    perm = sum((groups[e + 1] for e in range(N)), [])
+    assert rt["perm_token"].tolist() == perm == [0, 2, 1, 0, 1, 2]
+    # every slot points at a row holding its own token
+    for t in range(T):
+        for j in range(k):
+            assert rt["perm_token"][rt["slot_row"][t, j]] == t
+
+
+def pin_softmax_library(O):
+    """Full softmax equals scipy's softmax; softmax-then-top-k gates are p at the
+    selected experts, sum to <= 1, and to 1 when k = N."""
+    rng = np.random.default_rng(5)
+    L = rng.standard_normal((50, 9)).astype(np.float32) * 4
+    p = O.softmax_all(L)
+    assert np.allclose(p, scipy.special.softmax(L.astype(np.float64), axis=1), rtol=1e-13, atol=0)
+    for k in (1, 3, 9):
+        idx = O.select_topk(L, k)
+        g = O.gates(L, idx, O.GATING_SOFTMAX_THEN_TOPK)
+        assert np.all(g.sum(axis=1) <= 1 + 1e-12)
+        assert np.allclose(g, scipy.special.softmax(L.astype(np.float64), axis=1)[
+            np.arange(50)[:, None], idx], rtol=1e-13)
+        if k == 9:
+            assert np.allclose(g.sum(axis=1), 1.0, atol=1e-12)
+        g2 = O.gates(L, idx, O.GATING_TOPK_THEN_SOFTMAX)
+        assert np.allclose(g2.sum(axis=1), 1.0, atol=1e-12)
+        # top-k-then-softmax is the full softmax restricted to k and renormalised
+        assert np.allclose(g2, g / g.sum(axis=1, keepdims=True), rtol=1e-12)
+
+
+def pin_aux_closed_forms(O):
+    """Aux loss: W_r = 0 gives form0 = 1, form1 = 0; balanced counts give form0 = 1;
+    a two-expert hand case gives 1.5 and 0.0625."""
+    T, d, N, k = 12, 8, 4, 2
+    cfg = O.config_from(T=T, d=d, N=N, k=k, h=8)
+    x = np.random.default_rng(0).standard_normal((T, d)).astype(np.float32)
+    rt = O.route(cfg, x, np.zeros((d, N), np.float32))
+    assert rt["topk_idx"].tolist() == [[0, 1]] * T      # ties -> lowest indices
+    a0, a1 = rt["aux"]
+    assert a0 == 1.0 and a1 == 0.0
+    # balanced: token t picks expert t mod N (k = 1), one-hot inputs
+    T2 = 8
+    x2 = np.zeros((T2, d), np.float32)
+    w2 = np.zeros((d, N), np.float32)
+    for t in range(T2):
+        x2[t, t] = 1.0
+        w2[t, t % N] = 2.0
+    rt2 = O.route(O.config_from(T=T2, d=d, N=N, k=1, h=8), x2, w2)
+    assert rt2["counts_routed"].tolist() == [2, 2, 2, 2]
+    assert abs(rt2["aux"][0] - 1.0) < 1e-12
+    # hand case: 2 tokens, 2 experts, logits [ln 3, 0] for both -> p = [.75, .25]
+    x3 = np.ones((2, 1), np.float32)
+    w3 = np.array([[math.log(3.0), 0.0]], np.float32)
+    rt3 = O.route(O.config_from(T=2, d=1, N=2, k=1, h=8), x3, w3)
+    assert np.allclose(rt3["p"][:, 0], 0.75, atol=1e-7)
+    assert abs(rt3["aux"][0] - 1.5) < 1e-6
+    assert abs(rt3["aux"][1] - 0.0625) < 1e-6
+
+
+def pin_capacity(O):
+    """Capacity: C = ceil(T cf / N); kept_e = min(routed_e, C); kept + dropped = T k;
+    all-tied routing keeps tokens 0..C-1; slot-major priority for k = 2."""
+    assert O.capacity(4096, 8, (5, 4)) == 640
+    assert O.capacity(10, 4, (1, 1)) == 3
+    assert O.capacity(10, 4, None) is None
+    T, d, N = 10, 4, 4
+    x = np.random.default_rng(1).standard_normal((T, d)).astype(np.float32)
+    cfg = O.config_from(T=T, d=d, N=N, k=1, h=8, capacity_factor=(1, 1))
+    rt = O.route(cfg, x, np.zeros((d, N), np.float32))
+    assert rt["capacity"] == 3
+    assert rt["kept"][:, 0].tolist() == [True] * 3 + [False] * 7
+    assert rt["perm_token"].tolist() == [0, 1, 2]
+    assert rt["slot_row"][:, 0].tolist() == [0, 1, 2] + [-1] * 7
+    rng = np.random.default_rng(2)
+    for _ in range(20):
+        T, N, k = 40, 5, 2
+        L = rng.standard_normal((T, N)).astype(np.float32)
+        L[:, 0] += 2.0                                   # overload expert 0
+        idx = O.select_topk(L, k)
+        C = O.capacity(T, N, (1, 1))
+        kept = O.keep_within_capacity(idx, N, C)
+        routed = O.counts_routed(idx, N)
+        ck, off, perm, sr = O.group_by_expert(idx, kept, N)
+        assert ck.tolist() == np.minimum(routed, C).tolist()
+        assert int(ck.sum()) + int((~kept).sum()) == T * k
+        # slot-major: a dropped first choice implies the expert was already full
+        # with first choices of earlier tokens
+        for t in range(T):
+            if not kept[t, 0]:
+                e = idx[t, 0]
+                assert int(np.sum(idx[:t, 0] == e)) >= C
+            if kept[t, 1]:
+                e = idx[t, 1]
+                assert int(np.sum(idx[:, 0] == e)) + int(np.sum(idx[:t, 1] == e)) < C
+
+
+def _rand_layer(rng, T, d, N, k, h, hs=0, act="silu_gated", gating=O.GATING_TOPK_THEN_SOFTMAX,
+                cf=None, bias=False):
+    cfg = O.config_from(T=T, d=d, N=N, k=k, h=h, h_shared=hs, gating=gating, act=act,
+                        capacity_factor=cf)
+    inp = dict(x=rng.standard_normal((T, d)).astype(np.float32),
+               w_r=(rng.standard_normal((d, N)) / math.sqrt(d)).astype(np.float32),
+               b_r=rng.standard_normal(N).astype(np.float32) if bias else None,
+               w_gate=rng.standard_normal((N, h, d)) / math.sqrt(d),
+               w_up=(rng.standard_normal((N, h, d)) / math.sqrt(d)) if act == "silu_gated" else None,
+               w_down=rng.standard_normal((N, d, h)) / math.sqrt(h))
+    if hs:
+        inp.update(shared_w_gate=rng.standard_normal((hs, d)) / math.sqrt(d),
+                   shared_w_up=rng.standard_normal((hs, d)) / math.sqrt(d),
+                   shared_w_down=rng.standard_normal((d, hs)) / math.sqrt(hs))
+    return cfg, inp
+
+
+def _torch_mlp(x, wg, wu, wd):
+    F = torch.nn.functional
+    xt = torch.as_tensor(np.asarray(x, np.float64))
+    return F.linear(F.silu(F.linear(xt, torch.as_tensor(wg))) * F.linear(xt, torch.as_tensor(wu)),
+                    torch.as_tensor(wd)).numpy()
+
+
+def pin_single_expert_is_dense_mlp(O):
+    """N = 1, k = 1 (top-k then softmax: gate 1) reduces to x + MLP(x), checked
+    against torch's own linear/SiLU; ReLU variant against torch's relu; SiLU(1)."""
+    rng = np.random.default_rng(4)
+    cfg, inp = _rand_layer(rng, T=7, d=16, N=1, k=1, h=24)
+    y = O.forward(cfg, inp)["y"]
+    ref = inp["x"].astype(np.float64) + _torch_mlp(inp["x"], inp["w_gate"][0], inp["w_up"][0],
+                                                   inp["w_down"][0])
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-12)
+    cfg, inp = _rand_layer(rng, T=7, d=16, N=1, k=1, h=24, act="relu")
+    y = O.forward(cfg, inp)["y"]
+    F = torch.nn.functional
+    xt = torch.as_tensor(inp["x"].astype(np.float64))
+    ref = xt + F.linear(F.relu(F.linear(xt, torch.as_tensor(inp["w_gate"][0]))),
+                        torch.as_tensor(inp["w_down"][0]))
+    assert np.allclose(y, ref.numpy(), rtol=1e-12, atol=1e-12)
+    assert abs(O.silu(np.array([1.0]))[0] - 1.0 / (1.0 + math.exp(-1.0))) < 1e-15
+    assert O.silu(np.array([0.0]))[0] == 0.0
+
+
+def pin_identical_experts(O):
+    """With identical experts, y = x + (sum of gates) * FFN(x) whatever the routing."""
+    rng = np.random.default_rng(6)
+    for gating in (O.GATING_TOPK_THEN_SOFTMAX, O.GATING_SOFTMAX_THEN_TOPK):
+        cfg, inp = _rand_layer(rng, T=9, d=8, N=5, k=3, h=12, gating=gating)
+        for name in ("w_gate", "w_up", "w_down"):
+            inp[name] = np.repeat(inp[name][:1], 5, axis=0)
+        rt = O.forward(cfg, inp)
+        ffn = _torch_mlp(inp["x"], inp["w_gate"][0], inp["w_up"][0], inp["w_down"][0])
+        ref = inp["x"].astype(np.float64) + rt["topk_gate"].sum(axis=1, keepdims=True) * ffn
+        assert np.allclose(rt["y"], ref, rtol=1e-12, atol=1e-12)
+
+
+def pin_dense_brute_force(O):
+    """Sparse path (dispatch, grouped experts, combine) equals the dense sum of the
+    DeepSeekMoE equation with every expert computed and masked."""
+    rng = np.random.default_rng(8)
+    cases = [dict(T=11, d=8, N=4, k=2, h=6),
+             dict(T=13, d=8, N=5, k=3, h=6, gating=O.GATING_SOFTMAX_THEN_TOPK, hs=5),
+             dict(T=16, d=8, N=3, k=1, h=4, act="relu", gating=O.GATING_SOFTMAX_THEN_TOPK,
+                  cf=(1, 1), bias=True),
+             dict(T=17, d=8, N=4, k=2, h=4, cf=(1, 2))]
+    for c in cases:
+        cfg, inp = _rand_layer(rng, **c)
+        y = O.forward(cfg, inp)["y"]
+        yd = O.forward_dense(cfg, inp)
+        assert np.allclose(y, yd, rtol=1e-12, atol=1e-12)
+        sub = [0, 3, cfg.T - 1]                       # the token-sample path agrees too
+        assert np.allclose(O.forward(cfg, inp, tokens=sub)["y"], yd[sub], rtol=1e-12, atol=1e-12)
+
+
+def pin_dropped_tokens_are_residual(O):
+    """A token with every slot dropped leaves the layer as exactly x (no shared
+    expert) and as x + S(x) with a shared expert."""
+    rng = np.random.default_rng(9)
+    cfg, inp = _rand_layer(rng, T=12, d=8, N=4, k=1, h=6, cf=(1, 2))
+    inp["w_r"] = np.zeros_like(inp["w_r"])            # everyone ties onto expert 0
+    rt = O.forward(cfg, inp)
+    dropped = ~rt["kept"].any(axis=1)
+    assert dropped.sum() == cfg.T - rt["capacity"]
+    assert np.array_equal(rt["y"][dropped], inp["x"][dropped].astype(np.float64))
+    cfg, inp = _rand_layer(rng, T=12, d=8, N=4, k=1, h=6, cf=(1, 2), hs=7)
+    inp["w_r"] = np.zeros_like(inp["w_r"])
+    rt = O.forward(cfg, inp)
+    dropped = ~rt["kept"].any(axis=1)
+    s = _torch_mlp(inp["x"], inp["shared_w_gate"], inp["shared_w_up"], inp["shared_w_down"])
+    assert np.allclose(rt["y"][dropped], inp["x"][dropped] + s[dropped], rtol=1e-12, atol=1e-12)
+
+
+PINS = [pin_router_logits_exact, pin_router_logits_error_bound, pin_topk_brute_force,
+        pin_worked_example, pin_three_token_dispatch, pin_softmax_library, pin_aux_closed_forms,
+        pin_capacity, pin_single_expert_is_dense_mlp, pin_identical_experts,
+        pin_dense_brute_force, pin_dropped_tokens_are_residual]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_oracle_pin(pin):
+    pin(O)
+
+
+# ----------------------------------------------------------- planted mistakes
+
+def _mut_tie_high_index(mp):
+    mp.setattr(O, "select_topk", lambda L, k: (L.shape[1] - 1 - np.argsort(
+        -L[:, ::-1], axis=1, kind="stable"))[:, :k])
+
+
+def _mut_swap_gating(mp):
+    real = O.gates
+    mp.setattr(O, "gates", lambda L, idx, g: real(
+        L, idx, O.GATING_SOFTMAX_THEN_TOPK if g == O.GATING_TOPK_THEN_SOFTMAX
+        else O.GATING_TOPK_THEN_SOFTMAX))
+
+
+def _mut_token_major_rows(mp):
+    def grp(idx, kept, N):
+        ck, off, perm, sr = real(idx, kept, N)
+        order = np.argsort(perm, kind="stable")       # rows by token instead of expert
+        inv = np.empty_like(order)
+        inv[order] = np.arange(len(order))
+        sr2 = np.where(sr >= 0, inv[np.maximum(sr, 0)], -1)
+        return ck, off, perm[order], sr2
+    real = O.group_by_expert
+    mp.setattr(O, "group_by_expert", grp)
+
+
+def _mut_no_residual(mp):
+    real = O.layer_output
+
+    def lo(cfg, x, rt, *a, **kw):
+        toks = a[6] if len(a) > 6 else kw.get("tokens")
+        xs = np.asarray(x, np.float64)
+        return real(cfg, x, rt, *a, **kw) - (xs if toks is None else xs[toks])
+    mp.setattr(O, "layer_output", lo)
+
+
+def _mut_sigmoid_act(mp):
+    mp.setattr(O, "silu", lambda z: 1.0 / (1.0 + np.exp(-z)))
+
+
+def _mut_dropped_term(mp):
+    real = O.router_logits
+    mp.setattr(O, "router_logits", lambda x, w, b=None: real(
+        np.ascontiguousarray(np.asarray(x, np.float32)[:, 1:]),
+        np.ascontiguousarray(np.asarray(w, np.float32)[1:]), b))
+
+
+def _mut_mul_then_add(mp):
+    def logits(x, w, b=None):
+        x = np.asarray(x, np.float32)
+        w = np.asarray(w, np.float32)
+        acc = np.zeros((x.shape[0], w.shape[1]), np.float32)
+        for i in range(x.shape[1]):
+            acc = acc + x[:, i:i + 1] * w[i:i + 1]       # two roundings per term
+        return acc if b is None else acc + np.asarray(b, np.float32)
+    mp.setattr(O, "router_logits", logits)
+
+
+def _mut_reverse_order(mp):
+    real = O.router_logits
+    mp.setattr(O, "router_logits", lambda x, w, b=None: real(
+        np.ascontiguousarray(np.asarray(x, np.float32)[:, ::-1]),
+        np.ascontiguousarray(np.asarray(w, np.float32)[::-1]), b))
+
+
+def _mut_capacity_floor(mp):
+    mp.setattr(O, "capacity", lambda T, N, cf: None if cf is None else (T * cf[0]) // (N * cf[1]))
+
+
+def _mut_renormalise_softmax_gates(mp):
+    real = O.gates
+    def g(L, idx, gating):
+        out = real(L, idx, gating)
+        return out / out.sum(axis=1, keepdims=True)
+    mp.setattr(O, "gates", g)
+
+
+MUTATIONS = [
+    (_mut_tie_high_index, pin_topk_brute_force),
+    (_mut_swap_gating, pin_worked_example),
+    (_mut_token_major_rows, pin_three_token_dispatch),
+    (_mut_no_residual, pin_dropped_tokens_are_residual),
+    (_mut_sigmoid_act, pin_single_expert_is_dense_mlp),
+    (_mut_dropped_term, pin_router_logits_error_bound),
+    (_mut_mul_then_add, pin_router_logits_exact),
+    (_mut_reverse_order, pin_router_logits_exact),
+    (_mut_capacity_floor, pin_capacity),
+    (_mut_renormalise_softmax_gates, pin_softmax_library),
+]
+
+
+@pytest.mark.parametrize("mut,pin", MUTATIONS, ids=[m.__name__ for m, _ in MUTATIONS])
+def test_planted_mistake_is_caught(mut, pin, monkeypatch):
+    with monkeypatch.context() as mp:
+        mut(mp)
+        with pytest.raises(AssertionError):
+            pin(O)
