@@ -1,0 +1,429 @@
+#!/usr/bin/env python
+"""Benchmark: sparse MoE layer forward, tokens/s on B300, against its roofline.
+
+Default workload: the Mixtral-shaped prefill layer (T=4096, d=4096, 8 experts,
+SiLU-gated hidden 14336, top-2, top-k then softmax; bf16 activations and experts,
+fp32 router). One step = one moe_forward over the whole batch: router, gating,
+counts and aux loss, dispatch, both expert products on tensor cores, combine.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+  python bench.py --impl reference ...   (the CPU oracle, timed on host cores)
+
+Multi-GPU (torchrun, one process per GPU): every rank runs an independent replica
+of the layer on its own batch (the layer needs no exchange between replicas);
+the time is the max over ranks and `value` counts the tokens of all ranks.
+
+Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+L2_BYTES = 126 * 1024 * 1024
+METRIC = "MoE layer tokens/s on 1 B300 and % of roofline (BF16 TC peak / HBM BW)"
+UNIT = "tokens/s"
+STAGES = ["router", "dispatch", "expert_product_1", "expert_product_2", "combine"]
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="mixtral_prefill", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--cpu-sample", type=int, default=256,
+                    help="tokens whose outputs the CPU oracle computes for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------- helpers
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not torch.distributed.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        torch.distributed.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def _barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def _max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    dev = "cuda" if torch.cuda.is_available() and torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weight_bytes_hit(w, counts_kept=None) -> int:
+    """Bytes of the expert weights a forward reads: every expert that received a
+    row, plus the shared expert and the router weight."""
+    es = 2 if w.dtype == "bf16" else 4
+    m = 3 if w.act == "silu_gated" else 2
+    per_expert = m * w.d * w.h * es
+    hit = w.N if counts_kept is None else int(sum(1 for c in counts_kept if c > 0))
+    shared = 3 * w.d * w.h_shared * es if w.h_shared else 0
+    return hit * per_expert + shared + 4 * w.d * w.N
+
+
+def algorithmic(w, rows: int, counts_kept=None) -> dict:
+    """Algorithmic FLOPs and bytes of one layer forward and of its expert products."""
+    es = 2 if w.dtype == "bf16" else 4
+    m = 3 if w.act == "silu_gated" else 2
+    p1 = 2 * (m - 1) * rows * w.d * w.h + (2 * 2 * w.T * w.d * w.h_shared if w.h_shared else 0)
+    p2 = 2 * rows * w.d * w.h + (2 * w.T * w.d * w.h_shared if w.h_shared else 0)
+    bytes_ = weight_bytes_hit(w, counts_kept) + 2 * w.T * w.d * es
+    return {"flops": p1 + p2, "flops_p1": p1, "flops_p2": p2, "bytes": bytes_,
+            "router_flops": 2 * w.T * w.d * w.N}
+
+
+def launches_per_forward(w) -> int:
+    """Kernels one moe_forward launches: router (logits+gating, expert scan, slot
+    assignment), dispatch, expert product 1 (two launches for ReLU experts with a
+    shared expert), expert product 2, combine."""
+    p1 = 2 if (w.act == "relu" and w.h_shared) else 1
+    return 3 + 1 + p1 + 1 + 1
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm": float(p["hbm_gbs"]), "bf16": float(p["bf16_tflops"]),
+                "bf16_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm": 6400.0, "bf16": 1800.0, "bf16_sustained": 1400.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int, enabled: bool = True):
+        self.idx = device_index
+        self.proc = None
+        self.file = None
+        if enabled:
+            try:
+                self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.Q}",
+                     "--format=csv,noheader,nounits", "-lms", "100"],
+                    stdout=self.file, stderr=subprocess.DEVNULL)
+                time.sleep(0.3)
+            except OSError:
+                self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                clk, cmax = float(r[1]), float(r[2])
+            except (ValueError, IndexError):
+                continue
+            mx = max(mx, cmax)
+            sm.append(clk)
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        loaded = [c for c in sm if c > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else 1
+    except Exception:
+        return 1
+
+
+# ------------------------------------------------------------------ CPU oracle legs
+
+class _HostExperts:
+    def __init__(self, t):
+        self.t = t.float().cpu().numpy()
+
+    def __getitem__(self, e):
+        return self.t[e]
+
+
+def _oracle_inputs(inp):
+    out = {"x": inp["x"].float().cpu().numpy(), "w_r": inp["w_r"].cpu().numpy(),
+           "b_r": None if inp["b_r"] is None else inp["b_r"].cpu().numpy()}
+    for n in ("w_gate", "w_up", "w_down"):
+        out[n] = None if inp[n] is None else _HostExperts(inp[n])
+    for n in ("shared_w_gate", "shared_w_up", "shared_w_down"):
+        out[n] = None if inp[n] is None else inp[n].float().cpu().numpy()
+    return out
+
+
+def time_oracle(w, host_inp, sample: int, seed: int) -> tuple[float, float]:
+    """One oracle pass: routing for all T tokens, outputs for `sample` tokens.
+    Returns (seconds, tokens of output computed)."""
+    import numpy as np
+    from oracle import moe_oracle as O
+    rng = np.random.default_rng(seed)
+    n = min(sample, w.T)
+    toks = np.sort(rng.choice(w.T, size=n, replace=False))
+    t0 = time.perf_counter()
+    O.forward(w, host_inp, tokens=toks)
+    return time.perf_counter() - t0, n
+
+
+def run_reference(a, w, world, rank):
+    """The reference arm: the CPU oracle as it stands, on the host cores."""
+    if rank != 0:
+        return
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = W.make_inputs(w, device=dev)
+    host_inp = _oracle_inputs(inp)
+    del inp
+    sample = max(1, min(a.cpu_sample, w.T) // 4)
+    for i in range(a.warmup):
+        time_oracle(w, host_inp, sample, 100 + i)
+    secs, toks = 0.0, 0
+    for i in range(a.steps):
+        s, n = time_oracle(w, host_inp, sample, 1000 + i)
+        secs += s
+        toks += n
+    value = toks / secs
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": 1000 * secs / a.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": w.name, "T": w.T, "d": w.d, "N": w.N, "k": w.k, "h": w.h,
+                       "h_shared": w.h_shared, "gating": w.gating, "act": w.act},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": _blas_threads(),
+                             "kind": "oracle",
+                             "sample": f"per step: routing of all {w.T} tokens + layer outputs "
+                                       f"of {sample} random tokens (fp32 router, float64 rest)"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------ GPU arm
+
+def run_ours(a, w, world, rank, local):
+    import sparse_mixture_experts_64_b300 as moe
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    inp = W.make_inputs(w, device=dev)
+    cfg = moe.make_config(T=w.T, d=w.d, N=w.N, k=w.k, h=w.h, h_shared=w.h_shared, dtype=w.dtype,
+                          gating=w.gating, act=w.act, capacity_factor=w.capacity_factor,
+                          router_bias=w.router_bias)
+    ws = moe.workspace(cfg, device=dev)
+    T, k, N, d = w.T, w.k, w.N, w.d
+    y = torch.empty((T, d), dtype=inp["x"].dtype, device=dev)
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    gate = torch.empty((T, k), dtype=torch.float32, device=dev)
+    routed = torch.empty(N, dtype=torch.int32, device=dev)
+    kept = torch.empty(N, dtype=torch.int32, device=dev)
+    aux = torch.empty(2, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def fwd(x=None):
+        moe.moe_forward(cfg, inp["x"] if x is None else x, inp["w_r"], inp["b_r"], inp["w_gate"],
+                        inp["w_up"], inp["w_down"], inp["shared_w_gate"], inp["shared_w_up"],
+                        inp["shared_w_down"], y, idx, gate, routed, kept, aux, ws, stream)
+
+    # L2: weights larger than L2 stream from HBM every step; otherwise flush.
+    wbytes = weight_bytes_hit(w)
+    flush = None
+    if wbytes < 2 * L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    l2_mode = ("inputs larger than L2 (%.2f GB of expert weights)" % (wbytes / 1e9) if flush is None
+               else "L2 flushed between steps (256 MB write, outside the timed events)")
+
+    for _ in range(max(3, a.warmup)):
+        fwd()
+    torch.cuda.synchronize(dev)
+    st = moe.moe_check_error(ws, stream)
+    if st != moe.MOE_OK:
+        raise RuntimeError("device error word: " + moe.status_str(st))
+    counts_kept = kept.cpu().tolist()
+    rows = int(sum(counts_kept))
+
+    # ---- timed region: K forwards, per-step CUDA events on the launching stream
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps)]
+    clocks = ClockSampler(local, enabled=not a.no_clocks)
+    _barrier(world)
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    for i in range(a.steps):
+        if flush is not None:
+            flush.zero_()
+        starts[i].record(stream)
+        fwd()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    _barrier(world)
+    clk = clocks.stop()
+    ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / a.steps
+    ms_max = _max_over_ranks(ms, world)
+    value = world * T / (ms_max / 1e3)
+
+    # ---- per-stage durations (same launches, events between the stages)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    for ev in evs:
+        ev.record(stream)
+    stage_ms = [0.0] * 5
+    nprof = max(10, a.steps // 2)
+    for i in range(nprof):
+        if flush is not None:
+            flush.zero_()
+        moe.moe_forward_profiled(cfg, inp["x"], inp["w_r"], inp["b_r"], inp["w_gate"], inp["w_up"],
+                                 inp["w_down"], inp["shared_w_gate"], inp["shared_w_up"],
+                                 inp["shared_w_down"], y, idx, gate, routed, kept, aux, ws, evs,
+                                 stream)
+        evs[-1].synchronize()
+        for j in range(5):
+            stage_ms[j] += evs[j].elapsed_time(evs[j + 1]) / nprof
+
+    # ---- end to end: pinned host x -> device, forward, y -> pinned host
+    x_host = inp["x"].cpu().pin_memory()
+    y_host = torch.empty_like(y, device="cpu").pin_memory()
+    x_dev = torch.empty_like(inp["x"])
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(3):
+        x_dev.copy_(x_host, non_blocking=True)
+        fwd(x_dev)
+        y_host.copy_(y, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    ne2e = max(10, a.steps // 2)
+    e0.record(stream)
+    for _ in range(ne2e):
+        x_dev.copy_(x_host, non_blocking=True)
+        fwd(x_dev)
+        y_host.copy_(y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = _max_over_ranks(e0.elapsed_time(e1) / ne2e, world)
+    e2e_value = world * T / (e2e_ms / 1e3)
+    st = moe.moe_check_error(ws, stream)
+    if st != moe.MOE_OK:
+        raise RuntimeError("device error word: " + moe.status_str(st))
+
+    # ---- roofline of the dominant kernel
+    alg = algorithmic(w, rows, counts_kept)
+    peaks = _peaks()
+    stage = dict(zip(STAGES, stage_ms))
+    if w.dtype == "bf16":
+        dom = max(("expert_product_1", "expert_product_2"), key=lambda s: stage[s])
+        flops = alg["flops_p1"] if dom == "expert_product_1" else alg["flops_p2"]
+        achieved = flops / (stage[dom] / 1e3) / 1e12
+        roof = {"kernel": "k_ffn_tc<gated>" if dom == "expert_product_1" else "k_ffn_tc<plain>",
+                "bound": "tensor", "achieved": achieved, "peak": peaks["bf16"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16"], "traffic": None,
+                "peak_source": peaks["source"] + " bf16 burst",
+                "algorithmic_flops_per_launch": flops, "avg_launch_ms": stage[dom]}
+    else:
+        dom = "expert_product_1"
+        flops = alg["flops_p1"]
+        achieved = flops / (stage[dom] / 1e3) / 1e12
+        fp32_peak = 148 * 128 * 2 * 2.032e9 / 1e12
+        roof = {"kernel": "k_ffn_simt<gated>", "bound": "alu", "achieved": achieved,
+                "peak": fp32_peak, "unit": "TFLOP/s", "frac": achieved / fp32_peak,
+                "traffic": None, "peak_source": "148 SMs x 128 FP32 lanes x 2 x 2032 MHz",
+                "algorithmic_flops_per_launch": flops, "avg_launch_ms": stage[dom]}
+    layer_roof_ms = max(alg["flops"] / (peaks["bf16"] * 1e12), alg["bytes"] / (peaks["hbm"] * 1e9)) * 1e3
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded normal inputs and weights)",
+        "config": {"workload": w.name, "T": T, "d": d, "N": N, "k": k, "h": w.h,
+                   "h_shared": w.h_shared, "gating": w.gating, "act": w.act,
+                   "capacity_factor": w.capacity_factor, "router": "fp32",
+                   "global_batch_tokens": world * T, "parallelism": f"replicas x{world}",
+                   "l2": l2_mode},
+        "roofline": roof,
+        "layer_roofline": {"roofline_ms": layer_roof_ms, "frac": layer_roof_ms / ms_max,
+                           "algorithmic_flops": alg["flops"], "algorithmic_bytes": alg["bytes"],
+                           "router_flops_fp32": alg["router_flops"],
+                           "peaks": f"{peaks['source']}: bf16 {peaks['bf16']} TFLOP/s, "
+                                    f"HBM {peaks['hbm']} GB/s"},
+        "stages_ms": stage, "rows_dispatched": rows,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
+                "d2h_bytes_per_step": y_host.numel() * y_host.element_size()},
+        "gpu_launches": launches_per_forward(w) * a.steps,
+        "clocks": clk, "wall_s_timed": wall,
+    }
+
+    # ---- CPU oracle baseline (rank 0, single process only)
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        host_inp = _oracle_inputs(inp)
+        secs, n = time_oracle(w, host_inp, a.cpu_sample, 7)
+        line["cpu_baseline"] = {
+            "value": n / secs, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
+            "sample": f"routing of all {T} tokens + layer outputs of {n} random tokens, "
+                      f"{secs:.1f} s (fp32 router in C, float64 numpy elsewhere)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    a = _args()
+    world, rank, local = _dist()
+    w = W.WORKLOADS[a.config]
+    if a.impl == "reference":
+        run_reference(a, w, world, rank)
+    else:
+        run_ours(a, w, world, rank, local)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

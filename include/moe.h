@@ -1,0 +1,229 @@
+/*
+ * moe.h — C ABI of libmoe.so: the forward pass of one sparse Mixture-of-Experts
+ * layer on one B300 GPU (sm_103a).
+ *
+ * The layer computes, for every token t with hidden state x_t (the pages' u_t):
+ *
+ *     y_t = x_t + S(x_t) + sum_{j < k, slot j kept} g_{t,j} * FFN_{e_{t,j}}(x_t)
+ *
+ * "Mixture-of-Experts (MoE)" ml-notes page (DeepSeekMoE layer equation: a sum of
+ * gated expert FFNs plus the residual, with s = softmax over all N affinities and
+ * Topk); "MoE: Choosing Which MLPs to Use for Each Token" (sections "Router:
+ * Selecting Experts and Computing Weights", "From Router to Combine", "Shared
+ * Expert"); "Mixture of Experts (MoE)" glossary (top-k gating, expert capacity
+ * with residual bypass of overflow, auxiliary load-balancing loss); "Switch
+ * Transformers ... explained" (top-1 routing, capacity, router in higher
+ * precision).
+ *
+ * The calls follow the pages' Router -> Dispatch -> Expert computation ->
+ * Combine sequence; moe_forward runs all of them.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Every pointer argument is a DEVICE pointer unless stated otherwise; the
+ *    config is a HOST pointer. The caller owns all memory. The library never
+ *    allocates, frees or synchronises (moe_check_error excepted): every call
+ *    enqueues kernels on `stream` and returns.
+ *  - Layouts are row-major. Activations x, x_perm, y_perm, y: [rows][d].
+ *    Router weight w_r: [d][N] fp32; router bias b_r: [N] fp32.
+ *    Expert weights use the [out][in] (nn.Linear) layout:
+ *      SiLU-gated experts: w_gate, w_up [N][h][d], w_down [N][d][h];
+ *      ReLU experts:       w1 (passed as w_gate) [N][h][d], w_up NULL, w2 (as w_down) [N][d][h];
+ *      shared expert:      shared_w_gate, shared_w_up [h_shared][d], shared_w_down [d][h_shared].
+ *  - Element type of activations and expert weights: cfg->dtype (fp32 or bf16).
+ *    Router math is fp32 in both cases; gates are fp32.
+ *  - Worst-case row count of the dispatched buffers x_perm / y_perm:
+ *      R_max = T*k                      without a capacity limit,
+ *      R_max = min(T*k, N*C)            with capacity C = ceil(T*cap_num / (N*cap_den)).
+ *    The actual row count R = expert_offsets[N] stays on the device.
+ *  - Workspace: `ws` is a device buffer of at least moe_workspace_size(cfg)
+ *    bytes, 256-byte aligned, owned by the caller, reused across calls. It holds
+ *    intermediate arrays and the device error word. Concurrent calls on different
+ *    streams must use different workspaces.
+ *  - Errors: host-side validation returns a status before anything is enqueued.
+ *    A failed launch returns MOE_ERR_CUDA. Faults detected on the device (index
+ *    out of range, bounded waits that ran out) are recorded in the workspace's
+ *    error word and reported by moe_check_error.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* null pointer, size out of range, bad enum value      */
+    MOE_ERR_UNSUPPORTED = 2,   /* valid layer, but a shape/dtype this build does not run */
+    MOE_ERR_WORKSPACE = 3,     /* workspace missing, too small or misaligned            */
+    MOE_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed           */
+    MOE_ERR_TIMEOUT = 5,       /* a bounded wait inside a kernel ran out                */
+    MOE_ERR_DEVICE_FAULT = 6   /* a kernel saw an out-of-range index and skipped it     */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+/* Gating convention.
+ * MOE_SOFTMAX_THEN_TOPK: softmax over all N logits, keep the top-k probabilities
+ *   as gates without renormalising (DeepSeekMoE layer equation; glossary's
+ *   gating-network paragraph; Switch top-1 uses this with k = 1).
+ * MOE_TOPK_THEN_SOFTMAX: keep the k largest logits, softmax over those k only
+ *   (the worked example in "Router: Selecting Experts and Computing Weights"). */
+typedef enum { MOE_SOFTMAX_THEN_TOPK = 0, MOE_TOPK_THEN_SOFTMAX = 1 } moe_gating;
+
+/* Expert FFN. SILU_GATED: W_down (SiLU(W_gate x) * (W_up x)); RELU: W2 max(0, W1 x). */
+typedef enum { MOE_ACT_SILU_GATED = 0, MOE_ACT_RELU = 1 } moe_act;
+
+typedef struct {
+    int32_t T;                /* tokens, 1..65536                                    */
+    int32_t d;                /* model dim: multiple of 8 (fp32) or of 64 (bf16)    */
+    int32_t N;                /* routed experts, 1..256                              */
+    int32_t k;                /* experts per token, 1..min(N, 8)                     */
+    int32_t h;                /* routed expert hidden size, same multiple rule as d  */
+    int32_t h_shared;         /* shared expert hidden size, 0 = no shared expert     */
+    int32_t dtype;            /* moe_dtype                                           */
+    int32_t gating;           /* moe_gating                                          */
+    int32_t act;              /* moe_act (the shared expert is always SiLU-gated)    */
+    int32_t cap_num, cap_den; /* capacity factor cap_num/cap_den; 0/0 = no limit     */
+    int32_t has_router_bias;  /* 1: b_r is read and added to the logits              */
+    int32_t debug_flags;      /* MOE_DEBUG_* bits, 0 in normal use                   */
+} moe_config;
+
+/* debug_flags bits */
+#define MOE_DEBUG_FORCE_SIMT_FFN 1u  /* run the expert FFN on the CUDA-core kernel even for bf16 */
+
+/* Validate a config on the host. No CUDA call is made. */
+moe_status moe_validate_config(const moe_config *cfg);
+
+/* Bytes of workspace every call below needs for `cfg` (the maximum over calls);
+ * 0 when the config is invalid. No CUDA call is made. */
+size_t moe_workspace_size(const moe_config *cfg);
+
+/* Worst-case dispatched row count R_max for `cfg` (see above); 0 if invalid. */
+int64_t moe_max_rows(const moe_config *cfg);
+
+/* Expert capacity C for `cfg`, or 0 when no capacity limit is set / invalid. */
+int32_t moe_capacity(const moe_config *cfg);
+
+/*
+ * Router: logits, gating, counts, capacity and dispatch order.
+ *
+ * logits L[t][e] = sum_i x[t][i] * w_r[i][e] (+ b_r[e]) in fp32, accumulated from
+ * 0 with one fused multiply-add per feature i in increasing order ("Noise Top-k
+ * Gating" router paragraph; "Router: Selecting Experts ..." Figure 2; Switch
+ * explainer "Making it work" for the fp32 router). Top-k by logit, largest first,
+ * lower expert index first on equal logits. Gates per cfg->gating.
+ * Capacity (glossary capacity paragraph; Switch "Making it work"): when set, an
+ * expert keeps at most C slots, chosen slot-major (every token's first choice in
+ * token order, then every second choice, ...); dropped slots get slot_row = -1
+ * and contribute nothing (the token keeps its residual).
+ * Kept rows are grouped by expert ascending, token ascending within an expert
+ * ("From Router to Combine", Figure 3).
+ *
+ * Inputs:  x [T][d] (cfg->dtype), w_r [d][N] fp32, b_r [N] fp32 (NULL unless
+ *          cfg->has_router_bias).
+ * Outputs (device, caller-owned):
+ *   topk_idx       int32 [T][k]   selected experts, slot order = descending logit
+ *   topk_gate      fp32  [T][k]   gate of each slot
+ *   counts_routed  int32 [N]      selections per expert before capacity
+ *   counts_kept    int32 [N]      kept slots per expert (= min(routed, C))
+ *   expert_offsets int32 [N+1]    exclusive scan of counts_kept; R = offsets[N]
+ *   slot_row       int32 [T][k]   row of each slot in the dispatched order, -1 if dropped
+ *   perm_token     int32 [R_max]  token of each dispatched row (rows >= R untouched)
+ *   aux            fp32  [2]      aux[0] = N * sum_e f_e P_e, aux[1] = mean_e (P_e - 1/N)^2
+ *                                 with P_e = mean_t softmax_e, f_e = routed_e / (T k).
+ * Any output pointer except topk_idx, topk_gate, slot_row, perm_token and
+ * expert_offsets may be NULL (not written).
+ */
+moe_status moe_router_topk(const moe_config *cfg, const void *x, const float *w_r,
+                           const float *b_r, int32_t *topk_idx, float *topk_gate,
+                           int32_t *counts_routed, int32_t *counts_kept,
+                           int32_t *expert_offsets, int32_t *slot_row, int32_t *perm_token,
+                           float *aux, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Dispatch: x_perm[r] = x[perm_token[r]] for r < expert_offsets[N]
+ * ("From Router to Combine": the original token vectors are sent to the experts
+ * that chose them). x [T][d], x_perm [R_max][d] in cfg->dtype. Rows r >= R are
+ * not written. A perm_token entry outside [0, T) is skipped and recorded as
+ * MOE_ERR_DEVICE_FAULT in the error word (ws may be NULL: no record).
+ */
+moe_status moe_dispatch(const moe_config *cfg, const void *x, const int32_t *perm_token,
+                        const int32_t *expert_offsets, void *x_perm, void *ws,
+                        size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Expert computation: each expert e applies its FFN to its rows
+ * [expert_offsets[e], expert_offsets[e+1]) of x_perm, independently per row
+ * ("From Router to Combine"; glossary: experts are independent FFNs):
+ *   SILU_GATED: y_perm[r] = W_down[e] (SiLU(W_gate[e] x_perm[r]) * (W_up[e] x_perm[r]))
+ *   RELU:       y_perm[r] = W2[e] max(0, W1[e] x_perm[r])
+ * fp32 accumulation; for bf16 the hidden activation is rounded to bf16 between
+ * the two products and y_perm is bf16. Rows >= R are not written. The bf16 path
+ * runs on tcgen05 tensor cores; fp32 runs on CUDA cores.
+ */
+moe_status moe_grouped_ffn(const moe_config *cfg, const void *x_perm,
+                           const int32_t *expert_offsets, const void *w_gate_or_w1,
+                           const void *w_up, const void *w_down, void *y_perm, void *ws,
+                           size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Combine: y[t] = x[t] + S(x[t]) + sum_{j: slot_row[t][j] >= 0} topk_gate[t][j] * y_perm[slot_row[t][j]]
+ * ("From Router to Combine": weighted sum per original token; "Shared Expert":
+ * y = S(x) + R(x); DeepSeekMoE equation: + u_t). The expert terms are summed in
+ * fp32 in slot order, then S, then x. S is computed here (SiLU-gated, hidden
+ * cfg->h_shared) when cfg->h_shared > 0; the shared_* pointers are then required.
+ * A token whose slots were all dropped gets y = x + S(x) (exactly x without a
+ * shared expert). y [T][d] in cfg->dtype.
+ */
+moe_status moe_combine(const moe_config *cfg, const void *x, const void *y_perm,
+                       const int32_t *slot_row, const float *topk_gate,
+                       const void *shared_w_gate, const void *shared_w_up,
+                       const void *shared_w_down, void *y, void *ws, size_t ws_bytes,
+                       cudaStream_t stream);
+
+/*
+ * Whole layer: router -> dispatch -> experts (+ shared expert) -> combine.
+ * Same inputs as above; outputs y [T][d] and, when non-NULL, topk_idx, topk_gate,
+ * counts_routed, counts_kept (as in moe_router_topk) and aux [2]. The dispatch
+ * order, x_perm, hidden activations and y_perm live in the workspace.
+ */
+moe_status moe_forward(const moe_config *cfg, const void *x, const float *w_r,
+                       const float *b_r, const void *w_gate_or_w1, const void *w_up,
+                       const void *w_down, const void *shared_w_gate,
+                       const void *shared_w_up, const void *shared_w_down, void *y,
+                       int32_t *topk_idx, float *topk_gate, int32_t *counts_routed,
+                       int32_t *counts_kept, float *aux, void *ws, size_t ws_bytes,
+                       cudaStream_t stream);
+
+/*
+ * moe_forward with timing instrumentation: the same launches and results, plus
+ * events[0..5] recorded on `stream` before the router, after the router, after
+ * dispatch, after the first expert product (hidden activations), after the second
+ * expert product (expert outputs) and after combine. `events` is a host array of
+ * n_events == 6 caller-created CUDA events. Not part of the layer's math.
+ */
+moe_status moe_forward_profiled(const moe_config *cfg, const void *x, const float *w_r,
+                                const float *b_r, const void *w_gate_or_w1, const void *w_up,
+                                const void *w_down, const void *shared_w_gate,
+                                const void *shared_w_up, const void *shared_w_down, void *y,
+                                int32_t *topk_idx, float *topk_gate, int32_t *counts_routed,
+                                int32_t *counts_kept, float *aux, void *ws, size_t ws_bytes,
+                                cudaStream_t stream, cudaEvent_t *events, int32_t n_events);
+
+/* Synchronise `stream`, read and clear the device error word in `ws`.
+ * Returns MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_FAULT or MOE_ERR_CUDA. */
+moe_status moe_check_error(void *ws, cudaStream_t stream);
+
+/* Static string naming a status. */
+const char *moe_status_str(moe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H_ */

@@ -1,0 +1,498 @@
+// Grouped expert FFN on tcgen05 tensor cores (bf16 in, fp32 accumulate in TMEM).
+//
+// Each expert is an independent FFN applied to the rows dispatched to it
+// ("Mixture of Experts (MoE)" glossary; "MoE: Choosing Which MLPs to Use for Each
+// Token", sections "Dense MLP and MoE" and "From Router to Combine"; DeepSeekMoE
+// layer equation, FFN_i). Product 1 computes the hidden activation — for gated
+// experts SiLU(X W_gateᵀ) ⊙ (X W_upᵀ) fused in the epilogue from two accumulators
+// of one MMA, for ReLU experts max(0, X W1ᵀ) — and product 2 the output H W_downᵀ.
+// A shared expert ("Shared Expert" section, Figure 4) is one more segment of the
+// same launch, with its own operands.
+//
+// Kernel structure (one persistent CTA per SM, 192 threads):
+//   warp 0   TMA producer: A tile 128x64 and B tile 256x64 (bf16, 128-byte
+//            swizzle) per k-block into a 4-stage shared-memory ring;
+//   warp 1   owns the TMEM allocation (2 accumulators x 256 fp32 columns) and
+//            issues tcgen05.mma 128x256x16 from one thread;
+//   warps 2-5 epilogue: tcgen05.ld of the accumulator, activation, bf16 rows
+//            stored straight to global memory; overlaps the next tile's MMAs.
+// Tiles are enumerated on the device from the expert offsets (segment, then
+// n-tile, then m-tile fastest, so CTAs running together share weight tiles in
+// L2); row counts never travel to the host. Rows past a segment's end are
+// computed on whatever the A rows hold and never stored. Every wait is bounded:
+// after kTimeoutNs the kernel records MOE_ERR_TIMEOUT, drains its own copies and
+// MMAs, frees TMEM and returns.
+#include <algorithm>
+#include <cstring>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace {
+
+using namespace tc;
+
+constexpr int BM = 128, BK = 64, STAGES = 4;
+constexpr int BN_MMA = 256;
+constexpr uint32_t A_BYTES = BM * BK * 2;
+constexpr uint32_t B_BYTES = BN_MMA * BK * 2;
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int ACC_COLS = 256;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int NUM_THREADS = 192;
+constexpr int MAX_SEG = 257;
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + 1024;
+
+enum { KIND_GATED = 0, KIND_RELU = 1, KIND_PLAIN = 2 };
+
+struct TcParams {
+    CUtensorMap tmA, tmA_sh;       // [rows][K], box 64 x 128
+    CUtensorMap tmB0, tmB1;        // routed weights [n_seg][n_out][K], box 64 x (128|256) x 1
+    CUtensorMap tmB0_sh, tmB1_sh;  // shared weights [n_out_sh][K_sh], box 64 x (128|256)
+    const int32_t *offsets;
+    int n_seg, sh_rows;
+    int a_rows;                    // rows of the routed buffers; offsets are clamped to it
+    int n_out, K, n_out_sh, K_sh;
+    __nv_bfloat16 *C, *C_sh;
+    uint32_t *err;
+};
+
+struct Smem {
+    uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], drain;
+    uint32_t tmem_base;
+    int abort_flag;
+    int base[MAX_SEG + 1];  // first tile of each segment; base[nseg] = total
+    int mt[MAX_SEG];        // m-tiles per segment
+    int row0[MAX_SEG];      // first A row of each segment
+    int rows[MAX_SEG];      // rows per segment
+};
+
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                         uint32_t *err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > kTimeoutNs) {
+            *abort_flag = 1;
+            record_error(err, kErrTimeout);
+            return false;
+        }
+    }
+}
+
+// Wait without honouring the abort flag (used to drain work already in flight).
+__device__ __forceinline__ void drain_bar(uint64_t *bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer_ns() - t0 > kTimeoutNs) break;
+}
+
+struct TileInfo {
+    int seg, m, n;
+    bool shared;
+};
+
+__device__ __forceinline__ TileInfo decode_tile(const Smem &s, int nseg, int tile) {
+    int lo = 0, hi = nseg - 1;  // largest g with base[g] <= tile
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s.base[mid] <= tile) lo = mid;
+        else hi = mid - 1;
+    }
+    TileInfo ti;
+    ti.seg = lo;
+    const int local = tile - s.base[lo];
+    ti.m = local % s.mt[lo];
+    ti.n = local / s.mt[lo];
+    return ti;
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(NUM_THREADS, 1) k_ffn_tc(const __grid_constant__ TcParams p) {
+    constexpr int BN_OUT = KIND == KIND_GATED ? 128 : 256;
+    __shared__ Smem s;
+    extern __shared__ uint8_t dyn_smem[];
+    const uint32_t dyn_base = smem_u32(dyn_smem);
+    uint8_t *tiles = dyn_smem + (((dyn_base + 1023u) & ~1023u) - dyn_base);
+    auto smA = [&](int st) { return tiles + (size_t)st * STAGE_BYTES; };
+    auto smB = [&](int st) { return tiles + (size_t)st * STAGE_BYTES + A_BYTES; };
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nseg = p.n_seg + (p.sh_rows > 0 ? 1 : 0);
+    const int nt_routed = (p.n_out + BN_OUT - 1) / BN_OUT;
+    const int nt_sh = (p.n_out_sh + BN_OUT - 1) / BN_OUT;
+
+    // ---- tile table (warp 0) and barriers (thread 0) ----
+    if (warp == 0) {
+        constexpr int PER = (MAX_SEG + 31) / 32;
+        int cnt[PER];
+        int sum = 0;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int g = lane * PER + i;
+            int tiles_g = 0;
+            if (g < nseg) {
+                int r0, rows, nt;
+                if (g < p.n_seg) {
+                    r0 = min(max(p.offsets[g], 0), p.a_rows);
+                    rows = min(max(p.offsets[g + 1], r0), p.a_rows) - r0;
+                    nt = nt_routed;
+                } else {
+                    r0 = 0;
+                    rows = p.sh_rows;
+                    nt = nt_sh;
+                }
+                rows = max(rows, 0);
+                const int mt = (rows + BM - 1) / BM;
+                s.mt[g] = max(mt, 1);
+                s.row0[g] = r0;
+                s.rows[g] = rows;
+                tiles_g = mt * nt;
+            }
+            cnt[i] = tiles_g;
+            sum += tiles_g;
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += u;
+        }
+        int run = incl - sum;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int g = lane * PER + i;
+            if (g < nseg) s.base[g] = run;
+            run += cnt[i];
+        }
+        if (lane == 31) s.base[nseg] = incl;
+        if (lane == 0) {
+            for (int i = 0; i < STAGES; ++i) {
+                mbar_init(&s.full[i], 1);
+                mbar_init(&s.empty[i], 1);
+            }
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(&s.tfull[i], 1);
+                mbar_init(&s.tempty[i], 128);
+            }
+            mbar_init(&s.drain, 1);
+            s.abort_flag = 0;
+            fence_mbar_init();
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc(&s.tmem_base, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = s.tmem_base;
+    const int total = s.base[nseg];
+    volatile int *abort_flag = &s.abort_flag;
+
+    if (warp == 0) {
+        // ================= TMA producer =================
+        if (lane == 0) {
+            int st = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            uint32_t issued_mask = 0, issued_par = 0;  // last issue per stage
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                const TileInfo ti = decode_tile(s, nseg, tile);
+                const bool sh = ti.seg >= p.n_seg;
+                const int K = sh ? p.K_sh : p.K;
+                const int arow = s.row0[ti.seg] + ti.m * BM;
+                const CUtensorMap *ta = sh ? &p.tmA_sh : &p.tmA;
+                for (int kb = 0; kb < K / BK; ++kb) {
+                    if (!wait_bar(&s.empty[st], ph ^ 1, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&s.full[st], STAGE_BYTES);
+                    const int kc = kb * BK;
+                    tma_load_2d(smA(st), ta, kc, arow, &s.full[st]);
+                    if (KIND == KIND_GATED) {
+                        if (sh) {
+                            tma_load_2d(smB(st), &p.tmB0_sh, kc, ti.n * 128, &s.full[st]);
+                            tma_load_2d(smB(st) + B_BYTES / 2, &p.tmB1_sh, kc, ti.n * 128, &s.full[st]);
+                        } else {
+                            tma_load_3d(smB(st), &p.tmB0, kc, ti.n * 128, ti.seg, &s.full[st]);
+                            tma_load_3d(smB(st) + B_BYTES / 2, &p.tmB1, kc, ti.n * 128, ti.seg, &s.full[st]);
+                        }
+                    } else {
+                        if (sh) tma_load_2d(smB(st), &p.tmB0_sh, kc, ti.n * 256, &s.full[st]);
+                        else tma_load_3d(smB(st), &p.tmB0, kc, ti.n * 256, ti.seg, &s.full[st]);
+                    }
+                    issued_mask |= 1u << st;
+                    issued_par = (issued_par & ~(1u << st)) | (ph << st);
+                    if (++st == STAGES) {
+                        st = 0;
+                        ph ^= 1;
+                    }
+                }
+            }
+            // every load issued has landed before the CTA exits (immediate unless aborted)
+            for (int i = 0; i < STAGES; ++i)
+                if (issued_mask & (1u << i)) drain_bar(&s.full[i], (issued_par >> i) & 1u);
+        }
+    } else if (warp == 1) {
+        // ================= MMA issuer =================
+        if (lane == 0) {
+            constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN_MMA);
+            int st = 0, acc = 0;
+            uint32_t ph = 0, aph = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                const TileInfo ti = decode_tile(s, nseg, tile);
+                const int K = ti.seg >= p.n_seg ? p.K_sh : p.K;
+                if (!wait_bar(&s.tempty[acc], aph ^ 1, abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * ACC_COLS);
+                for (int kb = 0; kb < K / BK; ++kb) {
+                    if (!wait_bar(&s.full[st], ph, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = desc_sw128(smem_u32(smA(st)));
+                    const uint64_t bd = desc_sw128(smem_u32(smB(st)));
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        umma_bf16(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), IDESC,
+                                  (kb | kk) != 0 ? 1u : 0u);
+                    umma_commit(&s.empty[st]);
+                    if (++st == STAGES) {
+                        st = 0;
+                        ph ^= 1;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(&s.tfull[acc]);
+                if (++acc == 2) {
+                    acc = 0;
+                    aph ^= 1;
+                }
+            }
+            // all MMAs issued by this thread complete before TMEM is released
+            umma_commit(&s.drain);
+            drain_bar(&s.drain, 0);
+        }
+    } else {
+        // ================= epilogue (warps 2..5) =================
+        const int quarter = warp & 3;  // TMEM lanes this warp may access
+        const int r_in_tile = quarter * 32 + lane;
+        int acc = 0;
+        uint32_t aph = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+            const TileInfo ti = decode_tile(s, nseg, tile);
+            const bool sh = ti.seg >= p.n_seg;
+            if (!wait_bar(&s.tfull[acc], aph, abort_flag, p.err)) break;
+            tc_fence_after();
+            const int rows = s.rows[ti.seg] - ti.m * BM;
+            const bool row_ok = r_in_tile < rows;
+            const int64_t orow = (int64_t)s.row0[ti.seg] + ti.m * BM + r_in_tile;
+            const int n_out = sh ? p.n_out_sh : p.n_out;
+            __nv_bfloat16 *crow = (sh ? p.C_sh : p.C) + orow * n_out;
+            const uint32_t tbase = tmem_base + (uint32_t)(acc * ACC_COLS) + ((uint32_t)(quarter * 32) << 16);
+            if constexpr (KIND == KIND_GATED) {
+#pragma unroll 1
+                for (int c = 0; c < 128; c += 32) {
+                    uint32_t g[32], u[32];
+                    tmem_ld32(tbase + c, g);
+                    tmem_ld32(tbase + 128 + c, u);
+                    tmem_ld_wait();
+                    const int col = ti.n * 128 + c;
+                    if (row_ok && col < n_out) {
+                        uint32_t packed[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float h0 = silu_f32(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
+                            const float h1 =
+                                silu_f32(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
+                            __nv_bfloat162 b = __floats2bfloat162_rn(h0, h1);
+                            packed[i] = *reinterpret_cast<uint32_t *>(&b);
+                        }
+                        uint4 *dst = reinterpret_cast<uint4 *>(crow + col);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+                    }
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < 256; c += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(tbase + c, v);
+                    tmem_ld_wait();
+                    const int col = ti.n * 256 + c;
+                    if (row_ok && col < n_out) {
+                        uint32_t packed[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            float h0 = __uint_as_float(v[2 * i]), h1 = __uint_as_float(v[2 * i + 1]);
+                            if (KIND == KIND_RELU) {
+                                h0 = fmaxf(h0, 0.0f);
+                                h1 = fmaxf(h1, 0.0f);
+                            }
+                            __nv_bfloat162 b = __floats2bfloat162_rn(h0, h1);
+                            packed[i] = *reinterpret_cast<uint32_t *>(&b);
+                        }
+                        uint4 *dst = reinterpret_cast<uint4 *>(crow + col);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&s.tempty[acc]);
+            if (++acc == 2) {
+                acc = 0;
+                aph ^= 1;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// 2D bf16 [outer][inner] map, box inner 64 x box_outer, 128-byte swizzle.
+bool encode_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {inner * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)BK, box_outer};
+    const cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3D bf16 [n_exp][outer][inner] map, box 64 x box_outer x 1.
+bool encode_3d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t n_exp,
+               uint32_t box_outer) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {inner, outer, n_exp};
+    const cuuint64_t strides[2] = {inner * 2, inner * outer * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)BK, box_outer, 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int KIND>
+cudaError_t launch_kind(const TcParams &p, int64_t max_tiles, cudaStream_t s) {
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t e =
+            cudaFuncSetAttribute(k_ffn_tc<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(max_tiles, device_sm_count()));
+    k_ffn_tc<KIND><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(p);
+    return cudaGetLastError();
+}
+
+// One product over the routed segments and/or the shared segment.
+//   a / a_sh: A operands ([a_rows][K] / [sh_rows][K_sh]);
+//   b0,b1 / b0_sh,b1_sh: weights ([n_seg][n_out][K] / [n_out_sh][K_sh]);
+//   out / out_sh: outputs ([a_rows][n_out] / [sh_rows][n_out_sh]).
+template <int KIND>
+cudaError_t product(const int32_t *offsets, int n_seg, int64_t a_rows, const void *a, const void *b0,
+                    const void *b1, int K, int n_out, void *out, int sh_rows, const void *a_sh,
+                    const void *b0_sh, const void *b1_sh, int K_sh, int n_out_sh, void *out_sh,
+                    uint32_t *err, cudaStream_t s) {
+    constexpr int BN_OUT = KIND == KIND_GATED ? 128 : 256;
+    constexpr uint32_t BOX_B = KIND == KIND_GATED ? 128 : 256;
+    TcParams p;
+    memset(&p, 0, sizeof(p));
+    p.offsets = offsets;
+    p.n_seg = n_seg;
+    p.sh_rows = sh_rows;
+    p.a_rows = (int)a_rows;
+    p.n_out = n_out;
+    p.K = K;
+    p.n_out_sh = n_out_sh;
+    p.K_sh = K_sh;
+    p.C = static_cast<__nv_bfloat16 *>(out);
+    p.C_sh = static_cast<__nv_bfloat16 *>(out_sh);
+    p.err = err;
+    int64_t max_tiles = 0;
+    if (n_seg > 0) {
+        if (!encode_2d(&p.tmA, a, K, a_rows, BM)) return cudaErrorInvalidValue;
+        if (!encode_3d(&p.tmB0, b0, K, n_out, n_seg, BOX_B)) return cudaErrorInvalidValue;
+        if (KIND == KIND_GATED && !encode_3d(&p.tmB1, b1, K, n_out, n_seg, BOX_B)) return cudaErrorInvalidValue;
+        max_tiles += ((a_rows + BM - 1) / BM + n_seg) * ((n_out + BN_OUT - 1) / BN_OUT);
+    }
+    if (sh_rows > 0) {
+        if (!encode_2d(&p.tmA_sh, a_sh, K_sh, sh_rows, BM)) return cudaErrorInvalidValue;
+        if (!encode_2d(&p.tmB0_sh, b0_sh, K_sh, n_out_sh, BOX_B)) return cudaErrorInvalidValue;
+        if (KIND == KIND_GATED && !encode_2d(&p.tmB1_sh, b1_sh, K_sh, n_out_sh, BOX_B))
+            return cudaErrorInvalidValue;
+        max_tiles += ((int64_t)(sh_rows + BM - 1) / BM) * ((n_out_sh + BN_OUT - 1) / BN_OUT);
+    }
+    if (max_tiles == 0) return cudaSuccess;
+    return launch_kind<KIND>(p, max_tiles, s);
+}
+
+}  // namespace
+
+cudaError_t launch_ffn_tc(const moe_config &c, const FfnGroup &g, uint32_t *err, cudaStream_t s) {
+    cudaError_t e;
+    // product 1: hidden activations
+    if (g.act == MOE_ACT_SILU_GATED) {
+        e = product<KIND_GATED>(g.offsets, g.n_seg, g.a_rows, g.a, g.w_a, g.w_b, c.d, g.h, g.hid, g.sh_rows,
+                                g.sh_a, g.sh_w_gate, g.sh_w_up, c.d, g.h_sh, g.sh_hid, err, s);
+    } else {
+        e = product<KIND_RELU>(g.offsets, g.n_seg, g.a_rows, g.a, g.w_a, nullptr, c.d, g.h, g.hid, 0, nullptr,
+                               nullptr, nullptr, 0, 0, nullptr, err, s);
+        if (e == cudaSuccess && g.sh_rows > 0)
+            e = product<KIND_GATED>(nullptr, 0, 0, nullptr, nullptr, nullptr, 0, 0, nullptr, g.sh_rows, g.sh_a,
+                                    g.sh_w_gate, g.sh_w_up, c.d, g.h_sh, g.sh_hid, err, s);
+    }
+    if (e != cudaSuccess) return e;
+    if (g.mid_event && (e = cudaEventRecord(g.mid_event, s)) != cudaSuccess) return e;
+    // product 2: outputs
+    return product<KIND_PLAIN>(g.offsets, g.n_seg, g.a_rows, g.hid, g.w_out, nullptr, g.h, c.d, g.out,
+                               g.sh_rows, g.sh_hid, g.sh_w_down, nullptr, g.h_sh, c.d, g.sh_out, err, s);
+}
+
+}  // namespace moe

@@ -1,0 +1,94 @@
+// Host-side internals shared by the translation units of libmoe.so:
+// workspace layout, launcher declarations and tiling constants.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime_api.h>
+#include "../../include/moe.h"
+
+namespace moe {
+
+// Device error word bits (the word lives at the start of the workspace).
+constexpr uint32_t kErrFault = 1u;    // an out-of-range index was seen and skipped
+constexpr uint32_t kErrTimeout = 2u;  // a bounded wait gave up
+
+// The router kernel handles tokens in tiles of 8 * router_warps(cfg) tokens.
+// The tile size is a pure function of the config (no device query) so that the
+// workspace size can be computed without a GPU; 148 is the B300 SM count.
+constexpr int kSmCountForTiling = 148;
+int router_warps(const moe_config &c);
+inline int router_tile_tokens(const moe_config &c) { return 8 * router_warps(c); }
+inline int router_tiles(const moe_config &c) {
+    int tt = router_tile_tokens(c);
+    return (c.T + tt - 1) / tt;
+}
+
+int64_t max_rows(const moe_config &c);     // R_max
+int32_t capacity_of(const moe_config &c);  // C, 0 = no limit
+size_t dtype_size(const moe_config &c);
+
+// Byte offsets of every workspace region (each 256-byte aligned).
+struct WsLayout {
+    size_t err;                  // uint32 error word
+    size_t cnt, pre;             // int32 [N][k][tiles]
+    size_t kpre;                 // int32 [N][tiles]
+    size_t psum;                 // f32   [N][tiles]
+    size_t pmean;                // f32   [N]
+    size_t routed, kept;         // int32 [N] (used when the caller passes NULL)
+    size_t offsets;              // int32 [N+1]
+    size_t topk_idx, topk_gate;  // [T][k]
+    size_t slot_row;             // int32 [T][k]
+    size_t perm_token;           // int32 [R_max]
+    size_t aux;                  // f32 [2]
+    size_t x_perm, y_perm;       // [R_max][d]
+    size_t hid;                  // [R_max][h]
+    size_t hid_sh;               // [T][h_shared]
+    size_t s_out;                // [T][d]  shared expert output
+    size_t total;
+};
+WsLayout ws_layout(const moe_config &c);
+
+// ---- launchers (return cudaGetLastError() after the launch) ----
+struct RouterOut {
+    int32_t *topk_idx;
+    float *topk_gate;
+    int32_t *counts_routed, *counts_kept, *expert_offsets, *slot_row, *perm_token;
+    float *aux;
+};
+cudaError_t launch_router(const moe_config &c, const void *x, const float *w_r, const float *b_r,
+                          const RouterOut &o, uint8_t *ws, cudaStream_t s);
+
+cudaError_t launch_dispatch(const moe_config &c, const void *x, const int32_t *perm_token,
+                            const int32_t *offsets, void *x_perm, uint32_t *err, cudaStream_t s);
+
+cudaError_t launch_combine(const moe_config &c, const void *x, const void *y_perm,
+                           const void *s_out, const int32_t *slot_row, const float *gate,
+                           void *y, uint32_t *err, cudaStream_t s);
+
+// One grouped FFN problem: routed segments given by offsets (n_seg experts,
+// rows [offsets[e], offsets[e+1]) of A) plus an optional shared segment of
+// sh_rows rows with its own A and weights.
+struct FfnGroup {
+    const int32_t *offsets;  // device, [n_seg + 1]; may be null when n_seg == 0
+    int n_seg;
+    int64_t a_rows;          // rows allocated in the routed A / hidden / output buffers
+    const void *a;           // routed A [a_rows][d]
+    const void *w_a, *w_b, *w_out;  // routed weights (w_b null for ReLU)
+    void *hid;               // routed hidden [a_rows][h]
+    void *out;               // routed output [a_rows][d]
+    int h;
+    int act;
+    int sh_rows;             // 0: no shared segment
+    const void *sh_a;        // [sh_rows][d]
+    const void *sh_w_gate, *sh_w_up, *sh_w_down;
+    void *sh_hid;            // [sh_rows][h_shared]
+    void *sh_out;            // [sh_rows][d]
+    int h_sh;
+    cudaEvent_t mid_event;   // if set: recorded between the two products
+};
+cudaError_t launch_ffn_simt(const moe_config &c, const FfnGroup &g, uint32_t *err, cudaStream_t s);
+cudaError_t launch_ffn_tc(const moe_config &c, const FfnGroup &g, uint32_t *err, cudaStream_t s);
+
+int device_sm_count();
+
+}  // namespace moe

@@ -1,0 +1,356 @@
+// C ABI of libmoe.so: host-side validation, workspace layout and the launch
+// sequence of the sparse MoE layer forward (router -> dispatch -> experts ->
+// combine). The calls and their order follow "MoE: Choosing Which MLPs to Use for
+// Each Token", section "From Router to Combine"; see include/moe.h for each
+// call's contract.
+#include <algorithm>
+#include <cstring>
+
+#include "internal.h"
+
+namespace moe {
+
+int64_t max_rows(const moe_config &c) {
+    const int64_t tk = (int64_t)c.T * c.k;
+    const int32_t C = capacity_of(c);
+    return C > 0 ? std::min<int64_t>(tk, (int64_t)c.N * C) : tk;
+}
+
+int32_t capacity_of(const moe_config &c) {
+    if (c.cap_num <= 0 || c.cap_den <= 0) return 0;
+    const int64_t num = (int64_t)c.T * c.cap_num, den = (int64_t)c.N * c.cap_den;
+    const int64_t C = (num + den - 1) / den;
+    return (int32_t)std::min<int64_t>(C, INT32_MAX);
+}
+
+size_t dtype_size(const moe_config &c) { return c.dtype == MOE_BF16 ? 2 : 4; }
+
+static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+WsLayout ws_layout(const moe_config &c) {
+    WsLayout L;
+    const size_t tiles = (size_t)router_tiles(c);
+    const size_t N = c.N, k = c.k, T = c.T, es = dtype_size(c);
+    const size_t rmax = (size_t)max_rows(c);
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = align256(o + std::max<size_t>(bytes, 1));
+        return at;
+    };
+    // router scratch first: moe_router_topk needs only this prefix
+    L.err = take(4);
+    L.cnt = take(N * k * tiles * 4);
+    L.pre = take(N * k * tiles * 4);
+    L.kpre = take(N * tiles * 4);
+    L.psum = take(N * tiles * 4);
+    L.pmean = take(N * 4);
+    L.routed = take(N * 4);
+    L.kept = take(N * 4);
+    // expert / shared-expert buffers
+    L.hid = take(rmax * c.h * es);
+    L.hid_sh = take(c.h_shared ? T * c.h_shared * es : 0);
+    L.s_out = take(c.h_shared ? T * c.d * es : 0);
+    // moe_forward only
+    L.offsets = take((N + 1) * 4);
+    L.topk_idx = take(T * k * 4);
+    L.topk_gate = take(T * k * 4);
+    L.slot_row = take(T * k * 4);
+    L.perm_token = take(rmax * 4);
+    L.aux = take(2 * 4);
+    L.x_perm = take(rmax * c.d * es);
+    L.y_perm = take(rmax * c.d * es);
+    L.total = o;
+    return L;
+}
+
+int device_sm_count() {
+    static int count = 0;
+    if (count == 0) {
+        int dev = 0, v = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+            count = v;
+        else
+            return kSmCountForTiling;
+    }
+    return count;
+}
+
+static bool dim_ok(int32_t v, int dtype) {
+    if (v < 8 || v > 65536) return false;
+    return dtype == MOE_BF16 ? v % 64 == 0 : v % 8 == 0;
+}
+
+static moe_status validate(const moe_config *c) {
+    if (!c) return MOE_ERR_INVALID_ARG;
+    if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+    if (c->gating != MOE_SOFTMAX_THEN_TOPK && c->gating != MOE_TOPK_THEN_SOFTMAX) return MOE_ERR_INVALID_ARG;
+    if (c->act != MOE_ACT_SILU_GATED && c->act != MOE_ACT_RELU) return MOE_ERR_INVALID_ARG;
+    if (c->T < 1 || c->T > 65536) return MOE_ERR_INVALID_ARG;
+    if (c->N < 1 || c->N > 256) return MOE_ERR_INVALID_ARG;
+    if (c->k < 1 || c->k > c->N || c->k > 8) return MOE_ERR_INVALID_ARG;
+    if (c->d < 1 || c->h < 1 || c->h_shared < 0) return MOE_ERR_INVALID_ARG;
+    if ((c->cap_num == 0) != (c->cap_den == 0) || c->cap_num < 0 || c->cap_den < 0) return MOE_ERR_INVALID_ARG;
+    if (c->has_router_bias != 0 && c->has_router_bias != 1) return MOE_ERR_INVALID_ARG;
+    if (!dim_ok(c->d, c->dtype) || !dim_ok(c->h, c->dtype)) return MOE_ERR_UNSUPPORTED;
+    if (c->h_shared && !dim_ok(c->h_shared, c->dtype)) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+static moe_status check_ws(const void *ws, size_t ws_bytes, size_t need) {
+    if (!ws) return MOE_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(ws) % 256 != 0) return MOE_ERR_WORKSPACE;
+    if (ws_bytes < need) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+static bool aligned16(const void *p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
+
+static moe_status to_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+static cudaError_t run_ffn(const moe_config &c, const FfnGroup &g, uint32_t *err, cudaStream_t s) {
+    const bool simt = c.dtype == MOE_F32 || (c.debug_flags & MOE_DEBUG_FORCE_SIMT_FFN);
+    return simt ? launch_ffn_simt(c, g, err, s) : launch_ffn_tc(c, g, err, s);
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+moe_status moe_validate_config(const moe_config *cfg) { return validate(cfg); }
+
+size_t moe_workspace_size(const moe_config *cfg) {
+    if (validate(cfg) != MOE_OK) return 0;
+    return ws_layout(*cfg).total;
+}
+
+int64_t moe_max_rows(const moe_config *cfg) {
+    if (validate(cfg) != MOE_OK) return 0;
+    return max_rows(*cfg);
+}
+
+int32_t moe_capacity(const moe_config *cfg) {
+    if (validate(cfg) != MOE_OK) return 0;
+    return capacity_of(*cfg);
+}
+
+moe_status moe_router_topk(const moe_config *cfg, const void *x, const float *w_r, const float *b_r,
+                           int32_t *topk_idx, float *topk_gate, int32_t *counts_routed,
+                           int32_t *counts_kept, int32_t *expert_offsets, int32_t *slot_row,
+                           int32_t *perm_token, float *aux, void *ws, size_t ws_bytes,
+                           cudaStream_t stream) {
+    moe_status st = validate(cfg);
+    if (st != MOE_OK) return st;
+    const moe_config &c = *cfg;
+    if (!x || !w_r || !topk_idx || !topk_gate || !expert_offsets || !slot_row || !perm_token)
+        return MOE_ERR_INVALID_ARG;
+    if (c.has_router_bias && !b_r) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w_r)) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(c);
+    if ((st = check_ws(ws, ws_bytes, L.hid)) != MOE_OK) return st;
+    RouterOut o{topk_idx, topk_gate, counts_routed, counts_kept, expert_offsets, slot_row, perm_token, aux};
+    return to_status(launch_router(c, x, w_r, c.has_router_bias ? b_r : nullptr, o,
+                                   static_cast<uint8_t *>(ws), stream));
+}
+
+moe_status moe_dispatch(const moe_config *cfg, const void *x, const int32_t *perm_token,
+                        const int32_t *expert_offsets, void *x_perm, void *ws, size_t ws_bytes,
+                        cudaStream_t stream) {
+    moe_status st = validate(cfg);
+    if (st != MOE_OK) return st;
+    if (!x || !perm_token || !expert_offsets || !x_perm) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(x_perm)) return MOE_ERR_INVALID_ARG;
+    uint32_t *err = nullptr;
+    if (ws) {
+        if ((st = check_ws(ws, ws_bytes, 4)) != MOE_OK) return st;
+        err = static_cast<uint32_t *>(ws);
+    }
+    return to_status(launch_dispatch(*cfg, x, perm_token, expert_offsets, x_perm, err, stream));
+}
+
+moe_status moe_grouped_ffn(const moe_config *cfg, const void *x_perm, const int32_t *expert_offsets,
+                           const void *w_gate_or_w1, const void *w_up, const void *w_down, void *y_perm,
+                           void *ws, size_t ws_bytes, cudaStream_t stream) {
+    moe_status st = validate(cfg);
+    if (st != MOE_OK) return st;
+    const moe_config &c = *cfg;
+    if (!x_perm || !expert_offsets || !w_gate_or_w1 || !w_down || !y_perm) return MOE_ERR_INVALID_ARG;
+    if (c.act == MOE_ACT_SILU_GATED && !w_up) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x_perm) || !aligned16(w_gate_or_w1) || !aligned16(w_down) || !aligned16(y_perm) ||
+        (w_up && !aligned16(w_up)))
+        return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(c);
+    if ((st = check_ws(ws, ws_bytes, L.hid_sh)) != MOE_OK) return st;
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    FfnGroup g{};
+    g.offsets = expert_offsets;
+    g.n_seg = c.N;
+    g.a_rows = max_rows(c);
+    g.a = x_perm;
+    g.w_a = w_gate_or_w1;
+    g.w_b = c.act == MOE_ACT_SILU_GATED ? w_up : nullptr;
+    g.w_out = w_down;
+    g.hid = w + L.hid;
+    g.out = y_perm;
+    g.h = c.h;
+    g.act = c.act;
+    return to_status(run_ffn(c, g, reinterpret_cast<uint32_t *>(w + L.err), stream));
+}
+
+moe_status moe_combine(const moe_config *cfg, const void *x, const void *y_perm, const int32_t *slot_row,
+                       const float *topk_gate, const void *shared_w_gate, const void *shared_w_up,
+                       const void *shared_w_down, void *y, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    moe_status st = validate(cfg);
+    if (st != MOE_OK) return st;
+    const moe_config &c = *cfg;
+    if (!x || !y_perm || !slot_row || !topk_gate || !y) return MOE_ERR_INVALID_ARG;
+    if (c.h_shared && (!shared_w_gate || !shared_w_up || !shared_w_down)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(y_perm) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(c);
+    if ((st = check_ws(ws, ws_bytes, L.offsets)) != MOE_OK) return st;
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    uint32_t *err = reinterpret_cast<uint32_t *>(w + L.err);
+    const void *s_out = nullptr;
+    if (c.h_shared) {
+        FfnGroup g{};
+        g.n_seg = 0;
+        g.act = MOE_ACT_SILU_GATED;
+        g.h = c.h;
+        g.sh_rows = c.T;
+        g.sh_a = x;
+        g.sh_w_gate = shared_w_gate;
+        g.sh_w_up = shared_w_up;
+        g.sh_w_down = shared_w_down;
+        g.sh_hid = w + L.hid_sh;
+        g.sh_out = w + L.s_out;
+        g.h_sh = c.h_shared;
+        cudaError_t e = run_ffn(c, g, err, stream);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+        s_out = w + L.s_out;
+    }
+    return to_status(launch_combine(c, x, y_perm, s_out, slot_row, topk_gate, y, err, stream));
+}
+
+static moe_status forward_impl(const moe_config *cfg, const void *x, const float *w_r, const float *b_r,
+                               const void *w_gate_or_w1, const void *w_up, const void *w_down,
+                               const void *shared_w_gate, const void *shared_w_up,
+                               const void *shared_w_down, void *y, int32_t *topk_idx, float *topk_gate,
+                               int32_t *counts_routed, int32_t *counts_kept, float *aux, void *ws,
+                               size_t ws_bytes, cudaStream_t stream, cudaEvent_t *ev) {
+    moe_status st = validate(cfg);
+    if (st != MOE_OK) return st;
+    const moe_config &c = *cfg;
+    if (!x || !w_r || !w_gate_or_w1 || !w_down || !y) return MOE_ERR_INVALID_ARG;
+    if (c.act == MOE_ACT_SILU_GATED && !w_up) return MOE_ERR_INVALID_ARG;
+    if (c.has_router_bias && !b_r) return MOE_ERR_INVALID_ARG;
+    if (c.h_shared && (!shared_w_gate || !shared_w_up || !shared_w_down)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w_r) || !aligned16(w_gate_or_w1) || !aligned16(w_down) ||
+        !aligned16(y) || (w_up && !aligned16(w_up)))
+        return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(c);
+    if ((st = check_ws(ws, ws_bytes, L.total)) != MOE_OK) return st;
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    uint32_t *err = reinterpret_cast<uint32_t *>(w + L.err);
+    auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], stream) : cudaSuccess; };
+
+    RouterOut o;
+    o.topk_idx = topk_idx ? topk_idx : reinterpret_cast<int32_t *>(w + L.topk_idx);
+    o.topk_gate = topk_gate ? topk_gate : reinterpret_cast<float *>(w + L.topk_gate);
+    o.counts_routed = counts_routed;
+    o.counts_kept = counts_kept;
+    o.expert_offsets = reinterpret_cast<int32_t *>(w + L.offsets);
+    o.slot_row = reinterpret_cast<int32_t *>(w + L.slot_row);
+    o.perm_token = reinterpret_cast<int32_t *>(w + L.perm_token);
+    o.aux = aux ? aux : reinterpret_cast<float *>(w + L.aux);
+    if (mark(0) != cudaSuccess) return MOE_ERR_CUDA;
+    cudaError_t e = launch_router(c, x, w_r, c.has_router_bias ? b_r : nullptr, o, w, stream);
+    if (e != cudaSuccess || mark(1) != cudaSuccess) return MOE_ERR_CUDA;
+
+    void *x_perm = w + L.x_perm, *y_perm = w + L.y_perm;
+    e = launch_dispatch(c, x, o.perm_token, o.expert_offsets, x_perm, err, stream);
+    if (e != cudaSuccess || mark(2) != cudaSuccess) return MOE_ERR_CUDA;
+
+    FfnGroup g{};
+    g.offsets = o.expert_offsets;
+    g.n_seg = c.N;
+    g.a_rows = max_rows(c);
+    g.a = x_perm;
+    g.w_a = w_gate_or_w1;
+    g.w_b = c.act == MOE_ACT_SILU_GATED ? w_up : nullptr;
+    g.w_out = w_down;
+    g.hid = w + L.hid;
+    g.out = y_perm;
+    g.h = c.h;
+    g.act = c.act;
+    g.mid_event = ev ? ev[3] : nullptr;
+    if (c.h_shared) {
+        g.sh_rows = c.T;
+        g.sh_a = x;
+        g.sh_w_gate = shared_w_gate;
+        g.sh_w_up = shared_w_up;
+        g.sh_w_down = shared_w_down;
+        g.sh_hid = w + L.hid_sh;
+        g.sh_out = w + L.s_out;
+        g.h_sh = c.h_shared;
+    }
+    e = run_ffn(c, g, err, stream);
+    if (e != cudaSuccess || mark(4) != cudaSuccess) return MOE_ERR_CUDA;
+
+    e = launch_combine(c, x, y_perm, c.h_shared ? w + L.s_out : nullptr, o.slot_row, o.topk_gate, y, err,
+                       stream);
+    if (e != cudaSuccess || mark(5) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+moe_status moe_forward(const moe_config *cfg, const void *x, const float *w_r, const float *b_r,
+                       const void *w_gate_or_w1, const void *w_up, const void *w_down,
+                       const void *shared_w_gate, const void *shared_w_up, const void *shared_w_down,
+                       void *y, int32_t *topk_idx, float *topk_gate, int32_t *counts_routed,
+                       int32_t *counts_kept, float *aux, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    return forward_impl(cfg, x, w_r, b_r, w_gate_or_w1, w_up, w_down, shared_w_gate, shared_w_up,
+                        shared_w_down, y, topk_idx, topk_gate, counts_routed, counts_kept, aux, ws, ws_bytes,
+                        stream, nullptr);
+}
+
+moe_status moe_forward_profiled(const moe_config *cfg, const void *x, const float *w_r, const float *b_r,
+                                const void *w_gate_or_w1, const void *w_up, const void *w_down,
+                                const void *shared_w_gate, const void *shared_w_up,
+                                const void *shared_w_down, void *y, int32_t *topk_idx, float *topk_gate,
+                                int32_t *counts_routed, int32_t *counts_kept, float *aux, void *ws,
+                                size_t ws_bytes, cudaStream_t stream, cudaEvent_t *events, int32_t n_events) {
+    if (!events || n_events != 6) return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i < 6; ++i)
+        if (!events[i]) return MOE_ERR_INVALID_ARG;
+    return forward_impl(cfg, x, w_r, b_r, w_gate_or_w1, w_up, w_down, shared_w_gate, shared_w_up,
+                        shared_w_down, y, topk_idx, topk_gate, counts_routed, counts_kept, aux, ws, ws_bytes,
+                        stream, events);
+}
+
+moe_status moe_check_error(void *ws, cudaStream_t stream) {
+    if (!ws) return MOE_ERR_WORKSPACE;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+    uint32_t word = 0;
+    if (cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    if (word && cudaMemset(ws, 0, sizeof(word)) != cudaSuccess) return MOE_ERR_CUDA;
+    if (word & kErrTimeout) return MOE_ERR_TIMEOUT;
+    if (word & kErrFault) return MOE_ERR_DEVICE_FAULT;
+    return MOE_OK;
+}
+
+const char *moe_status_str(moe_status s) {
+    switch (s) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+        case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+        case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+        case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+        case MOE_ERR_DEVICE_FAULT: return "MOE_ERR_DEVICE_FAULT";
+    }
+    return "MOE_ERR_UNKNOWN";
+}
+
+}  // extern "C"

@@ -1,0 +1,137 @@
+"""Host-side checks of libmoe.so that need no GPU: the library loads, exports
+every function include/moe.h declares, and rejects bad arguments with a status
+before anything is enqueued (no CUDA call is made on these paths)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparse_mixture_experts_64_b300 as moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = []
+    with open(os.path.join(ROOT, "include", "moe.h")) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    for m in re.finditer(r"^\s*(?:const\s+)?\w+\s*\*?\s*(moe_\w+)\s*\(", src, flags=re.M):
+        names.append(m.group(1))
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported():
+    names = _declared()
+    assert set(moe.EXPORTED) <= set(names) and len(names) >= 11
+    lib = ctypes.CDLL(moe.library_path())
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def _cfg(**kw):
+    base = dict(T=64, d=128, N=8, k=2, h=256, dtype="bf16")
+    base.update(kw)
+    return moe.make_config(**base)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(T=0), moe.MOE_ERR_INVALID_ARG),
+    (dict(T=65537), moe.MOE_ERR_INVALID_ARG),
+    (dict(N=0), moe.MOE_ERR_INVALID_ARG),
+    (dict(N=257, k=2), moe.MOE_ERR_INVALID_ARG),
+    (dict(k=0), moe.MOE_ERR_INVALID_ARG),
+    (dict(k=9, N=16), moe.MOE_ERR_INVALID_ARG),
+    (dict(k=3, N=2), moe.MOE_ERR_INVALID_ARG),
+    (dict(d=96), moe.MOE_ERR_UNSUPPORTED),            # bf16 needs multiples of 64
+    (dict(h=100), moe.MOE_ERR_UNSUPPORTED),
+    (dict(h_shared=32), moe.MOE_ERR_UNSUPPORTED),
+    (dict(d=12, dtype="f32"), moe.MOE_ERR_UNSUPPORTED),  # fp32 needs multiples of 8
+    (dict(capacity_factor=(1, 0)), moe.MOE_ERR_INVALID_ARG),
+    (dict(dtype=7), moe.MOE_ERR_INVALID_ARG),
+    (dict(gating=5), moe.MOE_ERR_INVALID_ARG),
+    (dict(act=3), moe.MOE_ERR_INVALID_ARG),
+])
+def test_config_validation(kw, status):
+    c = _cfg(**kw)
+    assert moe.moe_validate_config(c) == status
+    assert moe.moe_workspace_size(c) == 0
+
+
+def test_valid_configs_and_sizes():
+    c = _cfg()
+    assert moe.moe_validate_config(c) == moe.MOE_OK
+    assert moe.moe_workspace_size(c) > 0
+    assert moe.moe_max_rows(c) == 64 * 2
+    assert moe.moe_capacity(c) == 0
+    sw = moe.make_config(T=4096, d=768, N=8, k=1, h=3072, act="relu", gating="softmax_then_topk",
+                         capacity_factor=(5, 4), router_bias=True)
+    assert moe.moe_capacity(sw) == 640
+    assert moe.moe_max_rows(sw) == 4096
+    sw2 = moe.make_config(T=4096, d=768, N=8, k=2, h=3072, capacity_factor=(1, 2))
+    assert moe.moe_capacity(sw2) == 256 and moe.moe_max_rows(sw2) == 8 * 256
+    tiny = moe.make_config(T=256, d=64, N=4, k=2, h=128, dtype="f32")
+    assert moe.moe_validate_config(tiny) == moe.MOE_OK
+    assert moe.status_str(moe.MOE_ERR_TIMEOUT) == "MOE_ERR_TIMEOUT"
+
+
+FAKE = 1 << 20          # a 256-aligned address that is never dereferenced on these paths
+
+
+def _raw(fn, *args):
+    return getattr(moe._lib, fn)(*args)
+
+
+def test_null_pointers_rejected_before_launch():
+    c = _cfg()
+    cp = ctypes.byref(c)
+    ws = moe.moe_workspace_size(c)
+    # forward: x missing
+    st = _raw("moe_forward", cp, None, FAKE, None, FAKE, FAKE, FAKE, None, None, None, FAKE,
+              None, None, None, None, None, FAKE, ws, None)
+    assert st == moe.MOE_ERR_INVALID_ARG
+    # forward: gated experts need w_up
+    st = _raw("moe_forward", cp, FAKE, FAKE, None, FAKE, None, FAKE, None, None, None, FAKE,
+              None, None, None, None, None, FAKE, ws, None)
+    assert st == moe.MOE_ERR_INVALID_ARG
+    # router: bias declared but missing
+    cb = _cfg(router_bias=True)
+    st = _raw("moe_router_topk", ctypes.byref(cb), FAKE, FAKE, None, FAKE, FAKE, None, None,
+              FAKE, FAKE, FAKE, None, FAKE, moe.moe_workspace_size(cb), None)
+    assert st == moe.MOE_ERR_INVALID_ARG
+    # combine: shared expert declared but weights missing
+    cs = _cfg(h_shared=128)
+    st = _raw("moe_combine", ctypes.byref(cs), FAKE, FAKE, FAKE, FAKE, None, None, None, FAKE,
+              FAKE, moe.moe_workspace_size(cs), None)
+    assert st == moe.MOE_ERR_INVALID_ARG
+    # misaligned activation pointer
+    st = _raw("moe_dispatch", cp, FAKE + 2, FAKE, FAKE, FAKE, None, 0, None)
+    assert st == moe.MOE_ERR_INVALID_ARG
+
+
+def test_workspace_checks_before_launch():
+    c = _cfg()
+    cp = ctypes.byref(c)
+    ws = moe.moe_workspace_size(c)
+    args = [FAKE, FAKE, None, FAKE, FAKE, FAKE, None, None, None, FAKE, None, None, None, None,
+            None]
+    assert _raw("moe_forward", cp, *args, None, ws, None) == moe.MOE_ERR_WORKSPACE
+    assert _raw("moe_forward", cp, *args, FAKE, ws - 1, None) == moe.MOE_ERR_WORKSPACE
+    assert _raw("moe_forward", cp, *args, FAKE + 16, ws, None) == moe.MOE_ERR_WORKSPACE
+    assert _raw("moe_router_topk", cp, FAKE, FAKE, None, FAKE, FAKE, None, None, FAKE, FAKE, FAKE,
+                None, FAKE, 16, None) == moe.MOE_ERR_WORKSPACE
+    assert _raw("moe_check_error", None, None) == moe.MOE_ERR_WORKSPACE
+
+
+def test_product_path_has_no_cpu_fallback():
+    """The binding only marshals arguments: it imports nothing from the oracle."""
+    import inspect
+    src = inspect.getsource(moe)
+    assert "oracle" not in src.replace("no Python or CPU fallback", "")
+    pkg = os.path.dirname(moe.__file__)
+    for name in os.listdir(pkg):
+        if name.endswith(".py"):
+            with open(os.path.join(pkg, name)) as f:
+                assert "import oracle" not in f.read() and "from oracle" not in open(
+                    os.path.join(pkg, name)).read()

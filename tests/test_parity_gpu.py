@@ -1,0 +1,194 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Small and ragged shapes are compared element by element on every output; the
+full-size workloads are compared bit-exactly on all routing outputs and on the
+layer output of a seeded token sample."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import moe_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import sparse_mixture_experts_64_b300 as moe
+    from moe_harness import (cfg_of, check_output, check_routing, host, oracle_inputs,
+                             rel_max_err, run_forward, run_separate)
+
+
+def _small(name, **kw):
+    return W.WORKLOADS[name].replace(name=name + "_" + "_".join(f"{a}{b}" for a, b in kw.items()),
+                                     **kw)
+
+
+SMALL = [
+    W.WORKLOADS["tiny_fp32"],
+    _small("tiny_fp32", T=77),
+    _small("tiny_fp32", T=33, N=1, k=1, d=16, h=24),
+    _small("tiny_fp32", T=50, N=5, k=5, d=24, h=40, h_shared=16,
+           gating="softmax_then_topk"),
+    _small("switch_top1", T=640, d=256, h=512),
+    W.WORKLOADS["switch_top1"],
+    _small("switch_top1", T=333, d=128, h=256, k=2, capacity_factor=(1, 2), act="silu_gated"),
+    _small("mixtral_prefill", T=300, d=256, h=384),
+    _small("mixtral_prefill", T=1, d=128, h=128),
+    _small("mixtral_prefill", T=129, d=192, h=320, N=3, k=3),
+    _small("deepseek_fine", T=200, d=256, N=16, k=4, h=128, h_shared=128),
+    _small("deepseek_fine", T=130, d=128, N=256, k=8, h=128, h_shared=192),
+    _small("deepseek_fine", T=96, d=128, N=100, k=6, h=192, h_shared=0,
+           gating="topk_then_softmax"),
+]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    torch.cuda.init()
+    yield
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("w", SMALL, ids=[w.name for w in SMALL])
+def test_small_parity(w):
+    inp = W.make_inputs(w, device="cuda")
+    cfg = cfg_of(w)
+    ws = moe.workspace(cfg)
+    sep = host(run_separate(cfg, inp, ws))
+    fwd = host(run_forward(cfg, inp, ws))
+    assert moe.moe_check_error(ws) == moe.MOE_OK
+    rt = O.forward(w, oracle_inputs(inp))
+    check_routing(sep, rt, sep=True)
+    check_routing(fwd, rt, sep=False)
+    check_output(sep["y"], rt["y"], w.dtype)
+    # the fused call runs the same kernels: identical bits
+    assert np.array_equal(fwd["y"], sep["y"])
+    # dropped tokens keep exactly their residual when there is no shared expert
+    dropped = ~rt["kept"].any(axis=1)
+    if dropped.any() and not w.h_shared:
+        assert np.array_equal(sep["y"][dropped], inp["x"].float().cpu().numpy()[dropped])
+
+
+@pytest.mark.parametrize("name", ["mixtral_prefill", "deepseek_fine"])
+def test_simt_and_tensor_core_ffn_agree(name):
+    w = _small(name, T=160, d=256, h=256, N=8, k=2, h_shared=128 if name == "deepseek_fine" else 0)
+    inp = W.make_inputs(w, device="cuda")
+    ws = moe.workspace(cfg_of(w))
+    tc = host(run_forward(cfg_of(w), inp, ws))
+    simt = host(run_forward(cfg_of(w, debug_flags=moe.MOE_DEBUG_FORCE_SIMT_FFN), inp, ws))
+    assert np.array_equal(tc["topk_idx"], simt["topk_idx"])
+    assert rel_max_err(tc["y"], simt["y"]) <= 2e-2
+
+
+def test_worked_example_on_gpu():
+    """The pages' d=8, four-expert, top-2 router example through moe_router_topk."""
+    w = W.Workload("worked", 1, T=1, d=8, N=4, k=2, h=8, dtype="f32")
+    x = torch.zeros((1, 8), dtype=torch.float32, device="cuda")
+    x[0, 0] = 1.0
+    w_r = torch.zeros((8, 4), dtype=torch.float32, device="cuda")
+    w_r[0] = torch.tensor([1.0, 0.0, 2.0, -1.0])
+    cfg = cfg_of(w)
+    ws = moe.workspace(cfg)
+    idx = torch.empty((1, 2), dtype=torch.int32, device="cuda")
+    gate = torch.empty((1, 2), dtype=torch.float32, device="cuda")
+    off = torch.empty(5, dtype=torch.int32, device="cuda")
+    sr = torch.empty((1, 2), dtype=torch.int32, device="cuda")
+    perm = torch.empty(2, dtype=torch.int32, device="cuda")
+    moe.moe_router_topk(cfg, x, w_r, None, idx, gate, None, None, off, sr, perm, None, ws)
+    assert idx.cpu().tolist() == [[2, 0]]
+    g = gate.cpu().numpy()[0]
+    assert abs(g[0] - 1 / (1 + np.exp(-1.0))) < 1e-6 and abs(g[1] - 1 / (1 + np.exp(1.0))) < 1e-6
+    assert off.cpu().tolist() == [0, 1, 1, 2, 2]
+    assert perm.cpu().tolist() == [0, 0]
+    assert sr.cpu().tolist() == [[1, 0]]
+
+
+def test_three_token_example_on_gpu():
+    """The pages' three-token dispatch example: groups E1{1,3}, E2{2}, E3{1,2,3}, E4{}."""
+    import math
+    scores = np.full((3, 4), -8.0, np.float32)
+    scores[0, 0], scores[0, 2] = 0.0, math.log(0.73 / 0.27)
+    scores[1, 1], scores[1, 2] = 0.0, 0.25
+    scores[2, 0], scores[2, 2] = math.log(0.88 / 0.12), 0.0
+    x = torch.zeros((3, 8), dtype=torch.float32, device="cuda")
+    w_r = torch.zeros((8, 4), dtype=torch.float32, device="cuda")
+    for t in range(3):
+        x[t, t] = 1.0
+        w_r[t] = torch.from_numpy(scores[t])
+    w = W.Workload("three", 1, T=3, d=8, N=4, k=2, h=8, dtype="f32")
+    cfg = cfg_of(w)
+    ws = moe.workspace(cfg)
+    rmax = moe.moe_max_rows(cfg)
+    o = {n: torch.empty(s, dtype=torch.int32, device="cuda") for n, s in
+         [("idx", (3, 2)), ("off", (5,)), ("sr", (3, 2)), ("perm", (rmax,)), ("cr", (4,)),
+          ("ck", (4,))]}
+    gate = torch.empty((3, 2), dtype=torch.float32, device="cuda")
+    moe.moe_router_topk(cfg, x, w_r, None, o["idx"], gate, o["cr"], o["ck"], o["off"], o["sr"],
+                        o["perm"], None, ws)
+    assert o["ck"].cpu().tolist() == [2, 1, 3, 0]
+    assert o["off"].cpu().tolist() == [0, 2, 3, 6, 6]
+    assert o["perm"].cpu().tolist()[:6] == [0, 2, 1, 0, 1, 2]
+    g = gate.cpu().numpy()
+    i = o["idx"].cpu().numpy()
+    assert abs(g[0][list(i[0]).index(0)] - 0.27) < 0.005
+    assert abs(g[2][list(i[2]).index(0)] - 0.88) < 0.005
+
+
+def test_run_to_run_determinism():
+    w = _small("deepseek_fine", T=256, d=256, N=32, k=4, h=128, h_shared=128)
+    inp = W.make_inputs(w, device="cuda")
+    cfg = cfg_of(w)
+    ws = moe.workspace(cfg)
+    first = host(run_forward(cfg, inp, ws))
+    for _ in range(5):
+        again = host(run_forward(cfg, inp, ws))
+        for k in first:
+            assert np.array_equal(first[k], again[k]), k
+
+
+def test_dispatch_rejects_out_of_range_token():
+    """A perm_token entry outside [0, T) is skipped and reported, never followed."""
+    w = _small("mixtral_prefill", T=64, d=128, h=128)
+    cfg = cfg_of(w)
+    ws = moe.workspace(cfg)
+    x = torch.randn((64, 128), device="cuda").to(torch.bfloat16)
+    rmax = moe.moe_max_rows(cfg)
+    perm = torch.arange(rmax, dtype=torch.int32, device="cuda") % 64
+    perm[5] = 64
+    perm[9] = -3
+    off = torch.tensor([0] * 8 + [rmax], dtype=torch.int32, device="cuda")
+    x_perm = torch.zeros((rmax + 1, 128), dtype=torch.bfloat16, device="cuda")
+    moe.moe_dispatch(cfg, x, perm, off, x_perm, ws)
+    assert moe.moe_check_error(ws) == moe.MOE_ERR_DEVICE_FAULT
+    assert moe.moe_check_error(ws) == moe.MOE_OK          # the word was cleared
+    xp = x_perm.float().cpu()
+    xs = x.float().cpu()
+    assert torch.equal(xp[0], xs[0]) and torch.equal(xp[6], xs[6])
+    assert torch.all(xp[5] == 0) and torch.all(xp[9] == 0) and torch.all(xp[rmax] == 0)
+
+
+# ------------------------------------------------------------ full-size workloads
+
+FULL = [("switch_top1", None), ("mixtral_decode_16", None), ("mixtral_decode_128", 24),
+        ("mixtral_prefill", 16), ("deepseek_fine", 8)]
+
+
+@pytest.mark.parametrize("name,sample", FULL, ids=[n for n, _ in FULL])
+def test_full_size_parity(name, sample):
+    """Full-size layer as the benchmark runs it (moe_forward, one call): routing,
+    counts and aux bit-exact / toleranced over all tokens; outputs on a sample."""
+    w = W.WORKLOADS[name]
+    inp = W.make_inputs(w, device="cuda")
+    cfg = cfg_of(w)
+    ws = moe.workspace(cfg)
+    fwd = host(run_forward(cfg, inp, ws))
+    sep = host(run_separate(cfg, inp, ws))
+    assert moe.moe_check_error(ws) == moe.MOE_OK
+    rng = np.random.default_rng(1234)
+    tokens = None if sample is None else np.sort(rng.choice(w.T, size=sample, replace=False))
+    rt = O.forward(w, oracle_inputs(inp), tokens=tokens)
+    check_routing(sep, rt, sep=True)
+    check_routing(fwd, rt, sep=False)
+    ysel = fwd["y"] if tokens is None else fwd["y"][tokens]
+    check_output(ysel, rt["y"], w.dtype)
+    assert np.array_equal(fwd["y"], sep["y"])
