@@ -47,7 +47,10 @@ def _args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="mixtral_prefill", choices=sorted(W.WORKLOADS))
-    ap.add_argument("--cpu-sample", type=int, default=256,
+    ap.add_argument("--tokens", type=int, default=None, help="override T (profiling variants)")
+    ap.add_argument("--experts", type=int, default=None, help="override N (profiling variants)")
+    ap.add_argument("--hidden", type=int, default=None, help="override h (profiling variants)")
+    ap.add_argument("--cpu-sample", type=int, default=1024,
                     help="tokens whose outputs the CPU oracle computes for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
@@ -177,8 +180,10 @@ class ClockSampler:
 
 
 def _blas_threads() -> int:
+    """Threads the oracle's float64 BLAS calls use (its C router is single-threaded)."""
     try:
         from threadpoolctl import threadpool_info
+        import numpy  # noqa: F401  (loads the BLAS so that it is listed)
         n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
         return max(n) if n else 1
     except Exception:
@@ -188,20 +193,28 @@ def _blas_threads() -> int:
 # ------------------------------------------------------------------ CPU oracle legs
 
 class _HostExperts:
-    def __init__(self, t):
-        self.t = t.float().cpu().numpy()
+    """Host copy of a [N][...] weight stack, indexed per expert by the oracle."""
+
+    def __init__(self, t, dtype):
+        self.t = t.float().cpu().numpy().astype(dtype, copy=False)
 
     def __getitem__(self, e):
         return self.t[e]
 
 
-def _oracle_inputs(inp):
+def _oracle_inputs(inp, w):
+    """Host arrays for the oracle, prepared once outside any timed region. The
+    expert weights are handed over as float64 (the oracle's own precision) when
+    they fit in 32 GB of host memory, else as float32 (converted per call)."""
+    import numpy as np
+    es = 8 if weight_bytes_hit(w) // (2 if w.dtype == "bf16" else 4) * 8 <= 32 * 2**30 else 4
+    dt = np.float64 if es == 8 else np.float32
     out = {"x": inp["x"].float().cpu().numpy(), "w_r": inp["w_r"].cpu().numpy(),
            "b_r": None if inp["b_r"] is None else inp["b_r"].cpu().numpy()}
     for n in ("w_gate", "w_up", "w_down"):
-        out[n] = None if inp[n] is None else _HostExperts(inp[n])
+        out[n] = None if inp[n] is None else _HostExperts(inp[n], dt)
     for n in ("shared_w_gate", "shared_w_up", "shared_w_down"):
-        out[n] = None if inp[n] is None else inp[n].float().cpu().numpy()
+        out[n] = None if inp[n] is None else inp[n].float().cpu().numpy().astype(dt)
     return out
 
 
@@ -224,7 +237,7 @@ def run_reference(a, w, world, rank):
         return
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     inp = W.make_inputs(w, device=dev)
-    host_inp = _oracle_inputs(inp)
+    host_inp = _oracle_inputs(inp, w)
     del inp
     sample = max(1, min(a.cpu_sample, w.T) // 4)
     for i in range(a.warmup):
@@ -403,7 +416,7 @@ def run_ours(a, w, world, rank, local):
 
     # ---- CPU oracle baseline (rank 0, single process only)
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
-        host_inp = _oracle_inputs(inp)
+        host_inp = _oracle_inputs(inp, w)
         secs, n = time_oracle(w, host_inp, a.cpu_sample, 7)
         line["cpu_baseline"] = {
             "value": n / secs, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
@@ -417,6 +430,9 @@ def main():
     a = _args()
     world, rank, local = _dist()
     w = W.WORKLOADS[a.config]
+    over = {k: v for k, v in (("T", a.tokens), ("N", a.experts), ("h", a.hidden)) if v}
+    if over:
+        w = w.replace(name=w.name + "_" + "_".join(f"{k}{v}" for k, v in over.items()), **over)
     if a.impl == "reference":
         run_reference(a, w, world, rank)
     else:

@@ -27,6 +27,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc_ptx.cuh"
 
 namespace moe {
 
@@ -41,14 +42,13 @@ int router_warps(const moe_config &c) {
 
 namespace {
 
-constexpr int KC = 32;  // features staged per chunk
-
 struct RouterArgs {
     int T, d, N, k, gating, tiles, has_bias;
     int32_t *topk_idx;
     float *topk_gate;
     int32_t *cnt;   // [N][k][tiles]
     float *psum;    // [N][tiles]
+    uint32_t *err;  // device error word (bounded waits)
 };
 
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
@@ -86,119 +86,46 @@ __device__ __forceinline__ float warp_sum_bcast(float v) {
     return __shfl_sync(0xffffffffu, v, 0);
 }
 
-// Thread tile: TPT tokens x EPT experts; a warp is (32/LE) token groups x LE
-// expert groups = 8 tokens x LE*EPT experts; warps stack along tokens.
-template <typename XT, int LE, int EPT, int TPT, bool NALIGN4>
-__global__ void __launch_bounds__(256) k_router(const XT *__restrict__ x, const float *__restrict__ w_r,
-                                                const float *__restrict__ b_r, RouterArgs a) {
+// Expert of accumulator j of a thread in expert group le. With EPT >= 4 the
+// experts come in runs of 4 interleaved across the LE groups, so one 128-bit
+// shared load per run covers LE*16 contiguous bytes (no bank conflicts).
+template <int LE, int EPT>
+__device__ __forceinline__ int expert_of(int le, int j) {
+    if constexpr (EPT >= 4) return (j / 4) * (LE * 4) + le * 4 + (j % 4);
+    else return le * EPT + j;
+}
+
+template <int LE, int EPT, bool VEC>
+__device__ __forceinline__ void load_w(const float *row, int le, float *wv) {
+    if constexpr (VEC && EPT >= 4) {
+#pragma unroll
+        for (int g = 0; g < EPT / 4; ++g) lds<4>(row + g * LE * 4 + le * 4, wv + 4 * g);
+    } else if constexpr (VEC) {
+        lds<EPT>(row + le * EPT, wv);
+    } else {
+#pragma unroll
+        for (int j = 0; j < EPT; ++j) wv[j] = row[expert_of<LE, EPT>(le, j)];
+    }
+}
+
+// Logits -> gating -> per-tile statistics, shared by both router kernels.
+// acc holds this thread's logits (TPT tokens x EPT experts, expert_of mapping);
+// smem must hold TT*N + TT*8 words and be free (all staging consumed).
+template <int LE, int EPT, int TPT>
+__device__ __forceinline__ void router_tail(float (&acc)[TPT][EPT], float *smem, const float *__restrict__ b_r,
+                                            const RouterArgs &a, int TT, int tok_base, int le) {
     constexpr int NP = LE * EPT;
     constexpr int QMAX = (NP + 31) / 32;
-    constexpr int VX = 16 / sizeof(XT);         // x elements per 16-byte load
-    constexpr int XPAIRS = (KC / VX) * 8 / 32;  // (token, 16B) pairs per thread
-    static_assert((32 / LE) * TPT == 8, "a warp covers 8 tokens");
-    extern __shared__ __align__(16) float smem[];
-
-    const int nthreads = blockDim.x;
-    const int nwarps = nthreads / 32;
-    const int TT = nwarps * 8;
-    const int N = a.N, d = a.d, T = a.T;
-    const int wbuf = KC * N + NP;  // W chunk [KC][N] + padding read by lanes with e >= N
-    float *Ws = smem;
-    float *Xs = smem + 2 * wbuf;   // [2][KC][TT], transposed, fp32
+    const int N = a.N, T = a.T;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int le = lane % LE, lt = lane / LE;
+    const int nthreads = blockDim.x, nwarps = nthreads / 32;
     const int t0 = blockIdx.x * TT;
-    const int tok_base = warp * 8 + lt * TPT;
-    const int e_base = le * EPT;
-
-    float acc[TPT][EPT];
-#pragma unroll
-    for (int i = 0; i < TPT; ++i)
-#pragma unroll
-        for (int j = 0; j < EPT; ++j) acc[i][j] = 0.0f;
-
-    const int nchunks = (d + KC - 1) / KC;
-    float xr[XPAIRS][VX];
-
-    auto load_x = [&](int c) {
-#pragma unroll
-        for (int p = 0; p < XPAIRS; ++p) {
-            const int pi = tid + p * nthreads;
-            const int tok = pi / (KC / VX), kq = pi % (KC / VX);
-            const int t = t0 + tok, kf = c * KC + kq * VX;
-            if (t < T && kf < d) {
-                Vec16<XT>::load(x + (size_t)t * d + kf, xr[p]);
-            } else {
-#pragma unroll
-                for (int i = 0; i < VX; ++i) xr[p][i] = 0.0f;
-            }
-        }
-    };
-    auto store_x = [&](int buf) {
-        float *xb = Xs + buf * KC * TT;
-#pragma unroll
-        for (int p = 0; p < XPAIRS; ++p) {
-            const int pi = tid + p * nthreads;
-            const int tok = pi / (KC / VX), kq = pi % (KC / VX);
-#pragma unroll
-            for (int i = 0; i < VX; ++i) xb[(kq * VX + i) * TT + tok] = xr[p][i];
-        }
-    };
-    auto issue_w = [&](int c, int buf) {
-        const int k0 = c * KC;
-        const int kc = min(KC, d - k0);
-        const float *src = w_r + (size_t)k0 * N;
-        float *dst = Ws + buf * wbuf;
-        if constexpr (NALIGN4) {
-            const int nvec = kc * N / 4;
-            for (int v = tid; v < nvec; v += nthreads) cp_async16(dst + 4 * v, src + 4 * v);
-        } else {
-            const int n = kc * N;
-            for (int v = tid; v < n; v += nthreads) cp_async4(dst + v, src + v);
-        }
-        cp_async_commit();
-    };
-
-    load_x(0);
-    issue_w(0, 0);
-    for (int c = 0; c < nchunks; ++c) {
-        const int buf = c & 1;
-        store_x(buf);
-        if (c + 1 < nchunks) {
-            issue_w(c + 1, buf ^ 1);
-            load_x(c + 1);
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
-        }
-        __syncthreads();
-        const float *wb = Ws + buf * wbuf + e_base;
-        const float *xb = Xs + buf * KC * TT + tok_base;
-        const int kc = min(KC, d - c * KC);
-#pragma unroll 8
-        for (int kk = 0; kk < kc; ++kk) {
-            float xv[TPT], wv[EPT];
-            lds<TPT>(xb + kk * TT, xv);
-            if constexpr (NALIGN4) {
-                lds<EPT>(wb + kk * N, wv);
-            } else {
-#pragma unroll
-                for (int j = 0; j < EPT; ++j) wv[j] = wb[kk * N + j];
-            }
-#pragma unroll
-            for (int i = 0; i < TPT; ++i)
-#pragma unroll
-                for (int j = 0; j < EPT; ++j) acc[i][j] = __fmaf_rn(xv[i], wv[j], acc[i][j]);
-        }
-        __syncthreads();
-    }
-
     // ---- logits to shared memory: Ls[TT][N]; Is[TT][8] behind it ----
     float *Ls = smem;
     int *Is = reinterpret_cast<int *>(smem + TT * N);
 #pragma unroll
     for (int j = 0; j < EPT; ++j) {
-        const int e = e_base + j;
+        const int e = expert_of<LE, EPT>(le, j);
         if (e < N) {
             const float bj = a.has_bias ? b_r[e] : 0.0f;
 #pragma unroll
@@ -299,6 +226,431 @@ __global__ void __launch_bounds__(256) k_router(const XT *__restrict__ x, const 
         for (int j = 0; j < 8; ++j)
             if (j < k) a.cnt[((size_t)e * k + j) * a.tiles + blockIdx.x] = cj[j];
     }
+}
+
+// Gating tail for few experts (N <= 32): one thread per token (no shuffles),
+// then per-tile statistics. Same rules as router_tail: top-k by logit, lower
+// index first on ties, softmax over all N in fp32, gates per convention.
+template <int LE, int EPT, int TPT>
+__device__ __forceinline__ void router_tail_small(float (&acc)[TPT][EPT], float *smem,
+                                                  const float *__restrict__ b_r, const RouterArgs &a, int TT,
+                                                  int tok_base, int le) {
+    const int N = a.N, T = a.T, k = a.k;
+    const int tid = threadIdx.x, nthreads = blockDim.x;
+    const int t0 = blockIdx.x * TT;
+    float *Ls = smem;                                   // [TT][N] logits, then p
+    int *Is = reinterpret_cast<int *>(smem + TT * N);   // [TT][8]
+#pragma unroll
+    for (int j = 0; j < EPT; ++j) {
+        const int e = expert_of<LE, EPT>(le, j);
+        if (e < N) {
+            const float bj = a.has_bias ? b_r[e] : 0.0f;
+#pragma unroll
+            for (int i = 0; i < TPT; ++i) {
+                float v = acc[i][j];
+                if (a.has_bias) v = __fadd_rn(v, bj);
+                Ls[(tok_base + i) * N + e] = v;
+            }
+        }
+    }
+    __syncthreads();
+    constexpr int NP = LE * EPT;  // <= 32: one token's logits fit in registers
+    for (int tok = tid; tok < TT; tok += nthreads) {
+        float *L = Ls + tok * N;
+        const int t = t0 + tok;
+        if (t >= T) {
+            for (int e = 0; e < N; ++e) L[e] = 0.0f;
+            for (int j = 0; j < 8; ++j) Is[tok * 8 + j] = -1;
+            continue;
+        }
+        float Lr[NP];
+#pragma unroll
+        for (int e = 0; e < NP; ++e) Lr[e] = e < N ? L[e] : 0.0f;
+        uint32_t taken = 0;
+        float vmax = 0.0f, den = 0.0f;
+        for (int s = 0; s < k; ++s) {
+            float bv = -INFINITY;
+            int bi = -1;
+#pragma unroll
+            for (int e = 0; e < NP; ++e)  // ascending e, strict '>': lowest index wins ties
+                if (e < N && !((taken >> e) & 1u) && (bi < 0 || Lr[e] > bv)) {
+                    bv = Lr[e];
+                    bi = e;
+                }
+            taken |= 1u << bi;
+            if (s == 0) vmax = bv;
+            Is[tok * 8 + s] = bi;
+        }
+        float sum = 0.0f;
+#pragma unroll
+        for (int e = 0; e < NP; ++e) {
+            Lr[e] = e < N ? expf(Lr[e] - vmax) : 0.0f;
+            sum += Lr[e];
+        }
+        // exp of a selected expert's logit, picked without dynamic register indexing
+        auto pick = [&](int e) {
+            float v = 0.0f;
+#pragma unroll
+            for (int q = 0; q < NP; ++q) v = q == e ? Lr[q] : v;
+            return v;
+        };
+        if (a.gating != MOE_SOFTMAX_THEN_TOPK)
+            for (int s = 0; s < k; ++s) den += pick(Is[tok * 8 + s]);
+        for (int s = 0; s < k; ++s) {
+            const int e = Is[tok * 8 + s];
+            const float ex = pick(e);
+            a.topk_idx[(size_t)t * k + s] = e;
+            a.topk_gate[(size_t)t * k + s] = a.gating == MOE_SOFTMAX_THEN_TOPK ? ex / sum : ex / den;
+        }
+        for (int s = k; s < 8; ++s) Is[tok * 8 + s] = -1;
+#pragma unroll
+        for (int e = 0; e < NP; ++e)
+            if (e < N) L[e] = Lr[e] / sum;
+    }
+    __syncthreads();
+    for (int e = tid; e < N; e += nthreads) {
+        float ps = 0.0f;
+        int cj[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        for (int tok = 0; tok < TT; ++tok) {
+            ps += Ls[tok * N + e];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (j < k && Is[tok * 8 + j] == e) ++cj[j];
+        }
+        a.psum[(size_t)e * a.tiles + blockIdx.x] = ps;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (j < k) a.cnt[((size_t)e * k + j) * a.tiles + blockIdx.x] = cj[j];
+    }
+}
+
+// Shared-memory plan of the logits loop: a ring of STAGES chunks, each holding
+// KC features of the router weight ([KC][N] fp32) and of the tile's token rows
+// ([TT][KC] input type, rows padded by 16 bytes), filled by cp.async; plus one
+// fp32 transposed copy of the current chunk's token values ([KC][TT]).
+template <typename XT, int KC>
+struct RouterSmem {
+    static constexpr int STAGES = 4;
+    static constexpr int XROW = KC * (int)sizeof(XT) + 16;  // bytes per staged token row
+    static __host__ __device__ size_t w_bytes(int N) { return (size_t)KC * N * 4; }
+    static __host__ __device__ size_t x_bytes(int TT) { return (size_t)TT * XROW; }
+    static __host__ __device__ size_t stage_bytes(int N, int TT) { return w_bytes(N) + x_bytes(TT); }
+    static __host__ __device__ size_t xf_offset(int N, int TT) { return STAGES * stage_bytes(N, TT); }
+    // + NP floats of padding: lanes whose experts are >= N read (and discard) past the last row
+    static __host__ __device__ size_t loop_bytes(int N, int TT, int NP) {
+        return xf_offset(N, TT) + (size_t)KC * TT * 4 + (size_t)NP * 4;
+    }
+};
+
+// Thread tile: TPT tokens x EPT experts; a warp is (32/LE) token groups x LE
+// expert groups = 8 tokens x LE*EPT experts; warps stack along tokens.
+template <typename XT, int LE, int EPT, int TPT, int KC, bool NALIGN4>
+__global__ void __launch_bounds__(256) k_router(const XT *__restrict__ x, const float *__restrict__ w_r,
+                                                const float *__restrict__ b_r, RouterArgs a) {
+    using SM = RouterSmem<XT, KC>;
+    constexpr int STAGES = SM::STAGES;
+    constexpr int NP = LE * EPT;
+    constexpr int VX = 16 / sizeof(XT);  // input elements per 16 bytes
+    static_assert((32 / LE) * TPT == 8, "a warp covers 8 tokens");
+    static_assert(KC % 8 == 0, "chunks hold whole 16-byte pieces");
+    extern __shared__ __align__(16) float smem[];
+    uint8_t *sbytes = reinterpret_cast<uint8_t *>(smem);
+
+    const int nthreads = blockDim.x;
+    const int nwarps = nthreads / 32;
+    const int TT = nwarps * 8;
+    const int N = a.N, d = a.d, T = a.T;
+    const size_t stage_b = SM::stage_bytes(N, TT);
+    const size_t wb_b = SM::w_bytes(N);
+    float *Xf = reinterpret_cast<float *>(sbytes + SM::xf_offset(N, TT));  // [KC][TT]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int le = lane % LE, lt = lane / LE;
+    const int t0 = blockIdx.x * TT;
+    const int tok_base = warp * 8 + lt * TPT;
+
+    float acc[TPT][EPT];
+#pragma unroll
+    for (int i = 0; i < TPT; ++i)
+#pragma unroll
+        for (int j = 0; j < EPT; ++j) acc[i][j] = 0.0f;
+
+    const int nchunks = (d + KC - 1) / KC;
+
+    // Copy chunk c into ring slot c % STAGES (one commit group per call, even if empty).
+    auto issue = [&](int c) {
+        if (c < nchunks) {
+            const int k0 = c * KC;
+            const int kc = min(KC, d - k0);
+            uint8_t *slot = sbytes + (size_t)(c % STAGES) * stage_b;
+            float *wdst = reinterpret_cast<float *>(slot);
+            const float *wsrc = w_r + (size_t)k0 * N;
+            if constexpr (NALIGN4) {
+                const int nvec = kc * N / 4;
+                for (int v = tid; v < nvec; v += nthreads) cp_async16(wdst + 4 * v, wsrc + 4 * v);
+            } else {
+                const int n = kc * N;
+                for (int v = tid; v < n; v += nthreads) cp_async4(wdst + v, wsrc + v);
+            }
+            uint8_t *xdst = slot + wb_b;
+            const int pieces = kc / VX;  // 16-byte pieces per token row in this chunk
+            for (int v = tid; v < TT * pieces; v += nthreads) {
+                const int tok = v / pieces, q = v % pieces;
+                const int t = t0 + tok;
+                if (t < T) cp_async16(xdst + (size_t)tok * SM::XROW + q * 16, x + (size_t)t * d + k0 + q * VX);
+            }
+        }
+        cp_async_commit();
+    };
+
+#pragma unroll
+    for (int c = 0; c < STAGES - 1; ++c) issue(c);
+
+    for (int c = 0; c < nchunks; ++c) {
+        cp_async_wait<STAGES - 2>();  // this thread's copies of chunk c have landed
+        __syncthreads();              // ... everyone's; and chunk c-1 is fully consumed
+        issue(c + STAGES - 1);        // into the slot chunk c-1 used
+        const uint8_t *slot = sbytes + (size_t)(c % STAGES) * stage_b;
+        const int kc = min(KC, d - c * KC);
+        // token values of this chunk -> fp32, transposed to [KC][TT]
+        {
+            const uint8_t *xs = slot + wb_b;
+            const int pieces = kc / VX;
+            for (int v = tid; v < TT * pieces; v += nthreads) {
+                const int q = v / TT, tok = v % TT;
+                float f[VX];
+                if (t0 + tok < T) {
+                    Vec16<XT>::load(reinterpret_cast<const XT *>(xs + (size_t)tok * SM::XROW + q * 16), f);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < VX; ++i) f[i] = 0.0f;
+                }
+#pragma unroll
+                for (int i = 0; i < VX; ++i) Xf[(q * VX + i) * TT + tok] = f[i];
+            }
+        }
+        __syncthreads();
+        const float *wb = reinterpret_cast<const float *>(slot);
+        const float *xb = Xf + tok_base;
+        if constexpr (TPT * EPT <= 8) {
+            // Few accumulators: the FMA chains are the critical path, so load the
+            // operands of the next 8 features while the current 8 are consumed.
+            float xa[8][TPT], wa[8][EPT], xn[8][TPT], wn[8][EPT];
+            auto load8 = [&](int k0, float (*xv)[TPT], float (*wv)[EPT]) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    lds<TPT>(xb + (k0 + q) * TT, xv[q]);
+                    load_w<LE, EPT, NALIGN4>(wb + (k0 + q) * N, le, wv[q]);
+                }
+            };
+            auto fma8 = [&](float (*xv)[TPT], float (*wv)[EPT]) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+#pragma unroll
+                    for (int i = 0; i < TPT; ++i)
+#pragma unroll
+                        for (int j = 0; j < EPT; ++j) acc[i][j] = __fmaf_rn(xv[q][i], wv[q][j], acc[i][j]);
+            };
+            load8(0, xa, wa);
+            for (int k8 = 0; k8 < kc; k8 += 16) {
+                if (k8 + 8 < kc) load8(k8 + 8, xn, wn);
+                fma8(xa, wa);
+                if (k8 + 8 < kc) {
+                    if (k8 + 16 < kc) load8(k8 + 16, xa, wa);
+                    fma8(xn, wn);
+                }
+            }
+        } else {
+#pragma unroll 4
+            for (int kk = 0; kk < kc; ++kk) {
+                float xv[TPT], wv[EPT];
+                lds<TPT>(xb + kk * TT, xv);
+                load_w<LE, EPT, NALIGN4>(wb + kk * N, le, wv);
+#pragma unroll
+                for (int i = 0; i < TPT; ++i)
+#pragma unroll
+                    for (int j = 0; j < EPT; ++j) acc[i][j] = __fmaf_rn(xv[i], wv[j], acc[i][j]);
+            }
+        }
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+
+    router_tail<LE, EPT, TPT>(acc, smem, b_r, a, TT, tok_base, le);
+}
+
+// Router for few experts (LE*EPT <= 32). Here every logit's FMA chain over d is
+// the critical path, so the loop is shaped for latency: the tile shape is fixed
+// at compile time (NW warps, 8*NW tokens), the weight chunk is staged with row
+// stride NP so every shared load uses an immediate offset, the token rows stay in
+// their input type and are converted in registers (8 features per 128-bit load),
+// and one barrier per chunk recycles the ring slot used two chunks earlier.
+template <typename XT, int LE, int EPT, int NW, int KC, bool BULK>
+__global__ void __launch_bounds__(NW * 32) k_router_small(const XT *__restrict__ x, const float *__restrict__ w_r,
+                                                         const float *__restrict__ b_r, RouterArgs a) {
+    constexpr int NP = LE * EPT;
+    constexpr int TT = NW * 8;
+    constexpr int TPT = 8 * LE / 32;
+    constexpr int STAGES = 4;
+    constexpr int ES = (int)sizeof(XT);
+    constexpr int VX = 16 / ES;
+    constexpr int XROW = KC * ES + 16;                       // bytes per staged token row
+    constexpr int W_BYTES = KC * NP * 4;
+    constexpr int STAGE = W_BYTES + TT * XROW;
+    static_assert(NP <= 32 && (32 / LE) * TPT == 8, "small-N tile");
+    static_assert(KC % 8 == 0 && (W_BYTES % 16) == 0, "16-byte pieces");
+    static_assert(TT <= 31, "one token row per lane of warp 0");
+    extern __shared__ __align__(16) float smem[];
+    __shared__ uint64_t full[STAGES];
+    __shared__ int abort_flag;
+    uint8_t *sb = reinterpret_cast<uint8_t *>(smem);
+
+    const int N = a.N, d = a.d, T = a.T;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int le = lane % LE, lt = lane / LE;
+    const int t0 = blockIdx.x * TT;
+    const int tok_base = warp * 8 + lt * TPT;
+    const int nchunks = (d + KC - 1) / KC;
+    const int ntok = min(TT, T - t0);
+
+    float acc[TPT][EPT];
+#pragma unroll
+    for (int i = 0; i < TPT; ++i)
+#pragma unroll
+        for (int j = 0; j < EPT; ++j) acc[i][j] = 0.0f;
+
+    if (tid == 0) {
+        abort_flag = 0;
+        if constexpr (BULK) {
+            for (int i = 0; i < STAGES; ++i) tc::mbar_init(&full[i], 1);
+            tc::fence_mbar_init();
+        }
+    }
+    __syncthreads();
+
+    // Stage chunk c into ring slot c % STAGES. BULK: one thread issues one bulk
+    // copy for the weight rows (contiguous, N == NP) and one per token row, all
+    // completing on the slot's mbarrier. Otherwise every thread issues cp.async.
+    auto issue = [&](int c) {
+        if constexpr (BULK) {
+            // warp 0: lane 0 arms the barrier, then lane 0 copies the weight rows
+            // and lanes 1..ntok one token row each (TT <= 31)
+            if (warp == 0 && c < nchunks) {
+                const int k0 = c * KC, kc = min(KC, d - k0);
+                uint8_t *slot = sb + (c % STAGES) * STAGE;
+                const uint32_t wbytes = (uint32_t)(kc * N * 4), xbytes = (uint32_t)(kc * ES);
+                uint64_t *bar = &full[c % STAGES];
+                if (lane == 0) tc::mbar_arrive_expect_tx(bar, wbytes + xbytes * (uint32_t)ntok);
+                __syncwarp();
+                if (lane == 0) tc::bulk_copy_g2s(slot, w_r + (size_t)k0 * N, wbytes, bar);
+                else if (lane <= ntok)
+                    tc::bulk_copy_g2s(slot + W_BYTES + (lane - 1) * XROW, x + (size_t)(t0 + lane - 1) * d + k0,
+                                      xbytes, bar);
+            }
+        } else {
+            if (c < nchunks) {
+                const int k0 = c * KC, kc = min(KC, d - k0);
+                uint8_t *slot = sb + (c % STAGES) * STAGE;
+                float *wdst = reinterpret_cast<float *>(slot);
+                const float *wsrc = w_r + (size_t)k0 * N;
+                for (int v = tid; v < kc * N; v += NW * 32) {
+                    const int r = v / N, e = v - r * N;
+                    cp_async4(wdst + r * NP + e, wsrc + v);
+                }
+                uint8_t *xdst = slot + W_BYTES;
+                const int pieces = kc / VX;
+                for (int v = tid; v < ntok * pieces; v += NW * 32) {
+                    const int tok = v / pieces, q = v - tok * pieces;
+                    cp_async16(xdst + tok * XROW + q * 16, x + (size_t)(t0 + tok) * d + k0 + q * VX);
+                }
+            }
+            cp_async_commit();
+        }
+    };
+    // Wait until chunk c has landed; false if the wait ran out (error recorded).
+    auto wait_chunk = [&](int c) -> bool {
+        if constexpr (BULK) {
+            uint64_t *bar = &full[c % STAGES];
+            const uint32_t par = (uint32_t)((c / STAGES) & 1);
+            if (!tc::mbar_try_wait(bar, par)) {
+                const uint64_t ts = tc::globaltimer_ns();
+                while (!tc::mbar_try_wait(bar, par)) {
+                    if (*(volatile int *)&abort_flag) return false;
+                    if (tc::globaltimer_ns() - ts > 1000000000ull) {
+                        *(volatile int *)&abort_flag = 1;
+                        record_error(a.err, kErrTimeout);
+                        return false;
+                    }
+                }
+            }
+            return true;
+        } else {
+            cp_async_wait<STAGES - 2>();
+            return true;
+        }
+    };
+
+    auto load_x8 = [&](const uint8_t *xs, int k8, float (*xv)[TPT]) {
+#pragma unroll
+        for (int i = 0; i < TPT; ++i) {
+            float f[8];
+            const XT *p = reinterpret_cast<const XT *>(xs + (tok_base + i) * XROW) + k8;
+            Vec16<XT>::load(p, f);
+            if constexpr (VX == 4) Vec16<XT>::load(p + 4, f + 4);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) xv[q][i] = f[q];
+        }
+    };
+    auto step8 = [&](const float *ws, const uint8_t *xs, int k8) {
+        float xv[8][TPT], wv[8][EPT];
+        load_x8(xs, k8, xv);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) lds<EPT>(ws + (k8 + q) * NP + le * EPT, wv[q]);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+#pragma unroll
+            for (int i = 0; i < TPT; ++i)
+#pragma unroll
+                for (int j = 0; j < EPT; ++j) acc[i][j] = __fmaf_rn(xv[q][i], wv[q][j], acc[i][j]);
+    };
+
+#pragma unroll
+    for (int c = 0; c < STAGES - 1; ++c) issue(c);
+    int issued = STAGES - 1;
+    bool ok = true;
+    for (int c = 0; c < nchunks; ++c) {
+        ok = wait_chunk(c);
+        __syncthreads();
+        if (!ok || *(volatile int *)&abort_flag) {
+            ok = false;
+            break;
+        }
+        issue(c + STAGES - 1);
+        ++issued;
+        const uint8_t *slot = sb + (c % STAGES) * STAGE;
+        const float *ws = reinterpret_cast<const float *>(slot);
+        const uint8_t *xs = slot + W_BYTES;
+        const int kc = min(KC, d - c * KC);
+        if (kc == KC) {
+#pragma unroll
+            for (int k8 = 0; k8 < KC; k8 += 8) step8(ws, xs, k8);
+        } else {
+            for (int k8 = 0; k8 < kc; k8 += 8) step8(ws, xs, k8);
+        }
+    }
+    if constexpr (BULK) {
+        // every copy issued lands before shared memory is reused or the CTA exits
+        if (tid == 0)
+            for (int c = max(0, issued - STAGES); c < min(issued, nchunks); ++c) {
+                const uint64_t ts = tc::globaltimer_ns();
+                while (!tc::mbar_try_wait(&full[c % STAGES], (uint32_t)((c / STAGES) & 1)))
+                    if (tc::globaltimer_ns() - ts > 1000000000ull) break;
+            }
+    } else {
+        cp_async_wait<0>();
+    }
+    __syncthreads();
+    if (!ok) return;
+    router_tail_small<LE, EPT, TPT>(acc, smem, b_r, a, TT, tok_base, le);
 }
 
 // Block-wide exclusive scan of one int per thread; returns the exclusive prefix
@@ -508,36 +860,54 @@ __global__ void __launch_bounds__(256) k_assign(AssignArgs a) {
     }
 }
 
-template <typename XT, int LE, int EPT, int TPT, bool A4>
+template <typename XT, int LE, int EPT, int TPT, int KC, bool A4>
 cudaError_t launch_router_t(const moe_config &c, const XT *x, const float *w_r, const float *b_r,
                             RouterArgs ra, int warps, cudaStream_t s) {
     constexpr int NP = LE * EPT;
     const int TT = warps * 8;
-    const size_t wbuf = (size_t)KC * c.N + NP;
-    const size_t stage = 2 * wbuf + 2 * (size_t)KC * TT;
-    const size_t gate = (size_t)TT * c.N + (size_t)TT * 8;
-    const size_t bytes = std::max(stage, gate) * sizeof(float);
-    auto kern = k_router<XT, LE, EPT, TPT, A4>;
+    const size_t loop = RouterSmem<XT, KC>::loop_bytes(c.N, TT, NP);
+    const size_t gate = ((size_t)TT * c.N + (size_t)TT * 8) * sizeof(float);
+    const size_t bytes = std::max(loop, gate);
+    auto kern = k_router<XT, LE, EPT, TPT, KC, A4>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
     if (e != cudaSuccess) return e;
     kern<<<ra.tiles, warps * 32, bytes, s>>>(x, w_r, b_r, ra);
     return cudaGetLastError();
 }
 
+// Many experts: chunks of 32 features so that four stages of [KC][N] weights fit.
 template <typename XT, int LE, int EPT, int TPT>
 cudaError_t launch_router_a(const moe_config &c, const XT *x, const float *w_r, const float *b_r,
                             RouterArgs ra, int warps, cudaStream_t s) {
-    if (c.N % 4 == 0) return launch_router_t<XT, LE, EPT, TPT, true>(c, x, w_r, b_r, ra, warps, s);
-    return launch_router_t<XT, LE, EPT, TPT, false>(c, x, w_r, b_r, ra, warps, s);
+    constexpr int KC = 32;
+    if (c.N % 4 == 0) return launch_router_t<XT, LE, EPT, TPT, KC, true>(c, x, w_r, b_r, ra, warps, s);
+    return launch_router_t<XT, LE, EPT, TPT, KC, false>(c, x, w_r, b_r, ra, warps, s);
+}
+
+// Few experts: 2 warps (16 tokens) per CTA, chunks of 256 features; bulk copies
+// when the weight chunk is one contiguous block of whole 16-byte pieces.
+template <typename XT, int LE, int EPT>
+cudaError_t launch_router_small(const moe_config &c, const XT *x, const float *w_r, const float *b_r,
+                                RouterArgs ra, cudaStream_t s) {
+    constexpr int NW = 2, KC = 256, TT = NW * 8;
+    constexpr size_t stage = (size_t)KC * LE * EPT * 4 + (size_t)TT * (KC * sizeof(XT) + 16);
+    const size_t gate = ((size_t)TT * c.N + (size_t)TT * 8) * sizeof(float);
+    const size_t bytes = std::max(4 * stage, gate);
+    const bool bulk = c.N == LE * EPT && c.N % 4 == 0;
+    auto kern = bulk ? k_router_small<XT, LE, EPT, NW, KC, true> : k_router_small<XT, LE, EPT, NW, KC, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e != cudaSuccess) return e;
+    kern<<<ra.tiles, NW * 32, bytes, s>>>(x, w_r, b_r, ra);
+    return cudaGetLastError();
 }
 
 template <typename XT>
 cudaError_t launch_router_x(const moe_config &c, const XT *x, const float *w_r, const float *b_r,
                             RouterArgs ra, int warps, cudaStream_t s) {
-    if (c.N <= 4) return launch_router_a<XT, 4, 1, 1>(c, x, w_r, b_r, ra, warps, s);
-    if (c.N <= 8) return launch_router_a<XT, 4, 2, 1>(c, x, w_r, b_r, ra, warps, s);
-    if (c.N <= 16) return launch_router_a<XT, 8, 2, 2>(c, x, w_r, b_r, ra, warps, s);
-    if (c.N <= 32) return launch_router_a<XT, 16, 2, 4>(c, x, w_r, b_r, ra, warps, s);
+    if (c.N <= 4) return launch_router_small<XT, 4, 1>(c, x, w_r, b_r, ra, s);
+    if (c.N <= 8) return launch_router_small<XT, 4, 2>(c, x, w_r, b_r, ra, s);
+    if (c.N <= 16) return launch_router_small<XT, 8, 2>(c, x, w_r, b_r, ra, s);
+    if (c.N <= 32) return launch_router_small<XT, 16, 2>(c, x, w_r, b_r, ra, s);
     if (c.N <= 64) return launch_router_a<XT, 32, 2, 8>(c, x, w_r, b_r, ra, warps, s);
     if (c.N <= 128) return launch_router_a<XT, 32, 4, 8>(c, x, w_r, b_r, ra, warps, s);
     return launch_router_a<XT, 32, 8, 8>(c, x, w_r, b_r, ra, warps, s);
@@ -560,7 +930,7 @@ cudaError_t launch_router(const moe_config &c, const void *x, const float *w_r, 
     int32_t *kept = o.counts_kept ? o.counts_kept : reinterpret_cast<int32_t *>(ws + L.kept);
 
     RouterArgs ra{c.T, c.d, c.N, c.k, c.gating, tiles, c.has_router_bias ? 1 : 0,
-                  o.topk_idx, o.topk_gate, cnt, psum};
+                  o.topk_idx, o.topk_gate, cnt, psum, err};
     cudaError_t e;
     if (c.dtype == MOE_BF16)
         e = launch_router_x<__nv_bfloat16>(c, static_cast<const __nv_bfloat16 *>(x), w_r, b_r, ra, warps, s);
