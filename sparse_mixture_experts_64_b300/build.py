@@ -1,6 +1,7 @@
 """Build libmoe.so (the CUDA kernels and the C ABI) in-tree for sm_103a.
 
-Usage: python -m sparse_mixture_experts_64_b300.build [--force] [--verbose]
+Usage: python sparse_mixture_experts_64_b300/build.py [--force] [--verbose] [--ptxas-info]
+(run it as a script: importing the package loads the library being built)
 """
 from __future__ import annotations
 
