@@ -147,6 +147,30 @@ moe_status moe_router_topk(const moe_config *cfg, const void *x, const float *w_
                            float *aux, void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * moe_router_topk for callers that cannot allocate device memory. The paper has
+ * no counterpart to this call; it exists for hosts that forbid allocation after
+ * start-up (engines that plan all device memory ahead and call plugins from an
+ * enqueue path, services with a fixed memory budget), which cannot hand over a
+ * workspace on demand.
+ * Same computation, arguments and outputs as moe_router_topk, without the
+ * workspace: the router's scratch lives in one static 8 MiB device array of the
+ * library, held by every GPU that loads it until the process exits. Configs whose
+ * router scratch would exceed 8 MiB are rejected with MOE_ERR_UNSUPPORTED before
+ * anything is enqueued (the five reference workloads all fit). Nothing is
+ * allocated and no allocating routine is called.
+ * The first call on a device looks up the array's device address (make that first
+ * call before any stream capture). All calls share the array: the error word in
+ * it is cleared at the start of each call and is not readable through
+ * moe_check_error; calls that overlap on the GPU race on the array and must be
+ * serialised by the caller.
+ */
+moe_status moe_router_topk_noalloc(const moe_config *cfg, const void *x, const float *w_r,
+                                   const float *b_r, int32_t *topk_idx, float *topk_gate,
+                                   int32_t *counts_routed, int32_t *counts_kept,
+                                   int32_t *expert_offsets, int32_t *slot_row,
+                                   int32_t *perm_token, float *aux, cudaStream_t stream);
+
+/*
  * Dispatch: x_perm[r] = x[perm_token[r]] for r < expert_offsets[N]
  * ("From Router to Combine": the original token vectors are sent to the experts
  * that chose them). x [T][d], x_perm [R_max][d] in cfg->dtype. Rows r >= R are

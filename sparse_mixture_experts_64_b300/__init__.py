@@ -26,7 +26,7 @@ MOE_DEBUG_FORCE_SIMT_FFN = 1
 
 EXPORTED = ("moe_validate_config", "moe_workspace_size", "moe_max_rows", "moe_capacity",
             "moe_router_topk", "moe_dispatch", "moe_grouped_ffn", "moe_combine", "moe_forward",
-            "moe_forward_profiled", "moe_check_error", "moe_status_str")
+            "moe_forward_profiled", "moe_check_error", "moe_status_str", "moe_router_topk_noalloc")
 
 
 class moe_config(ctypes.Structure):
@@ -55,6 +55,7 @@ def _load() -> ctypes.CDLL:
         "moe_max_rows": (I64, [cfgp]),
         "moe_capacity": (I32, [cfgp]),
         "moe_router_topk": (I32, [cfgp] + [P] * 11 + [P, SZ, P]),
+        "moe_router_topk_noalloc": (I32, [cfgp] + [P] * 11 + [P]),
         "moe_dispatch": (I32, [cfgp, P, P, P, P, P, SZ, P]),
         "moe_grouped_ffn": (I32, [cfgp, P, P, P, P, P, P, P, SZ, P]),
         "moe_combine": (I32, [cfgp, P, P, P, P, P, P, P, P, P, SZ, P]),
@@ -149,6 +150,16 @@ def moe_router_topk(cfg, x, w_r, b_r, topk_idx, topk_gate, counts_routed, counts
                                 _p(expert_offsets), _p(slot_row), _p(perm_token), _p(aux),
                                 _p(ws), ws.numel() if ws is not None else 0, _stream(stream)),
            "moe_router_topk")
+
+
+def moe_router_topk_noalloc(cfg, x, w_r, b_r, topk_idx, topk_gate, counts_routed, counts_kept,
+                            expert_offsets, slot_row, perm_token, aux, stream=None):
+    """moe_router_topk without a workspace, for callers that cannot allocate device
+    memory: the router scratch is a static array inside libmoe.so (8 MiB limit)."""
+    _check(_lib.moe_router_topk_noalloc(ctypes.byref(cfg), _p(x), _p(w_r), _p(b_r), _p(topk_idx),
+                                        _p(topk_gate), _p(counts_routed), _p(counts_kept),
+                                        _p(expert_offsets), _p(slot_row), _p(perm_token), _p(aux),
+                                        _stream(stream)), "moe_router_topk_noalloc")
 
 
 def moe_dispatch(cfg, x, perm_token, expert_offsets, x_perm, ws=None, stream=None):

@@ -1,0 +1,70 @@
+// moe_router_topk_noalloc: the router call for callers that cannot allocate
+// device memory — for example a host engine that plans all device memory when it
+// starts and then calls its plugins from an enqueue path where allocation is not
+// allowed, or a service that runs inside a fixed device-memory budget. Such a
+// caller has no way to provide moe_router_topk's workspace on demand.
+//
+// The router's scratch (per-tile counts and probability sums, their scans and
+// the device error word) lives here instead, in one file-scope device array of
+// kNoAllocScratchBytes. Every GPU that loads libmoe.so holds that array until the
+// process exits. The caller still passes every input and output buffer.
+//
+// Set-up: the first call on a device looks up the array's device address with
+// that device current (cudaGetSymbolAddress) and caches it per device; make that
+// first call before any stream capture. All calls share the one array and it keeps
+// the previous call's contents: the error word is cleared at the start of every
+// call and every other scratch region is fully rewritten before it is read. Calls
+// that overlap on the GPU (different streams, or different host threads) race on
+// the array and must be serialised by the caller.
+#include <mutex>
+
+#include "internal.h"
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB
+constexpr int kMaxDevices = 64;
+
+__device__ __align__(256) uint8_t g_router_scratch[kNoAllocScratchBytes];
+
+void *g_scratch_addr[kMaxDevices];  // device address of g_router_scratch, per device
+std::mutex g_scratch_mu;
+
+moe_status scratch_of_current_device(uint8_t **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_router_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
+        g_scratch_addr[dev] = p;
+    }
+    *out = static_cast<uint8_t *>(g_scratch_addr[dev]);
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" moe_status moe_router_topk_noalloc(const moe_config *cfg, const void *x, const float *w_r,
+                                              const float *b_r, int32_t *topk_idx, float *topk_gate,
+                                              int32_t *counts_routed, int32_t *counts_kept,
+                                              int32_t *expert_offsets, int32_t *slot_row, int32_t *perm_token,
+                                              float *aux, cudaStream_t stream) {
+    moe_status st = moe_validate_config(cfg);
+    if (st != MOE_OK) return st;
+    const moe_config &c = *cfg;
+    if (!x || !w_r || !topk_idx || !topk_gate || !expert_offsets || !slot_row || !perm_token)
+        return MOE_ERR_INVALID_ARG;
+    if (c.has_router_bias && !b_r) return MOE_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(x) % 16 || reinterpret_cast<uintptr_t>(w_r) % 16) return MOE_ERR_INVALID_ARG;
+    // the router's scratch is the workspace prefix that ends where the hidden buffer starts
+    const size_t need = moe::ws_layout(c).hid;
+    if (need > kNoAllocScratchBytes) return MOE_ERR_UNSUPPORTED;
+    uint8_t *scratch = nullptr;
+    if ((st = scratch_of_current_device(&scratch)) != MOE_OK) return st;
+    if (cudaMemsetAsync(scratch + moe::ws_layout(c).err, 0, sizeof(uint32_t), stream) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    moe::RouterOut o{topk_idx, topk_gate, counts_routed, counts_kept, expert_offsets, slot_row, perm_token, aux};
+    const cudaError_t e = moe::launch_router(c, x, w_r, c.has_router_bias ? b_r : nullptr, o, scratch, stream);
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
