@@ -153,9 +153,9 @@ moe_status moe_router_topk(const moe_config *cfg, const void *x, const float *w_
  * enqueue path, services with a fixed memory budget), which cannot hand over a
  * workspace on demand.
  * Same computation, arguments and outputs as moe_router_topk, without the
- * workspace: the router's scratch lives in one static 8 MiB device array of the
+ * workspace: the router's scratch lives in one static 32 MiB device array of the
  * library, held by every GPU that loads it until the process exits. Configs whose
- * router scratch would exceed 8 MiB are rejected with MOE_ERR_UNSUPPORTED before
+ * router scratch would exceed 32 MiB are rejected with MOE_ERR_UNSUPPORTED before
  * anything is enqueued (the five reference workloads all fit). Nothing is
  * allocated and no allocating routine is called.
  * The first call on a device looks up the array's device address (make that first

@@ -13,7 +13,7 @@ reader to check by eye rather than for speed:
   -> combine (gate-weighted sum per token) + shared expert + residual.
 
 Precision. The router logits are fp32 with one fixed summation order (see
-``router_logits.c``), because the top-k decision is an integer result that the
+``router_logits.c``: 32 blocked fma partials and a pairwise combine), because the top-k decision is an integer result that the
 CUDA router must reproduce bit for bit; the decision is therefore taken in the
 kernel's precision on identical values. Everything after the logits (softmax,
 gates, aux loss, expert FFNs, combine) is float64 on the exact values of the
@@ -89,7 +89,8 @@ def router_logits(x: np.ndarray, w_r: np.ndarray, b: np.ndarray | None = None) -
     [Choosing MLPs] section "Router: Selecting Experts and Computing Weights",
     Figure 2 (W_r is d x N); [DeepSeekMoE eq] the affinity u_t^T e_i; [Switch]
     section "Making it work" (the router runs in higher precision).
-    Summation order: fused multiply-add per feature in increasing index (C code).
+    Summation order (C code): 8-feature blocks dealt round-robin to 32 fma partial
+    sums, combined by five pairwise rounds (xor distance 16, 8, 4, 2, 1), then + b.
     """
     x = np.ascontiguousarray(x, dtype=np.float32)
     w_r = np.ascontiguousarray(w_r, dtype=np.float32)

@@ -155,7 +155,7 @@ def moe_router_topk(cfg, x, w_r, b_r, topk_idx, topk_gate, counts_routed, counts
 def moe_router_topk_noalloc(cfg, x, w_r, b_r, topk_idx, topk_gate, counts_routed, counts_kept,
                             expert_offsets, slot_row, perm_token, aux, stream=None):
     """moe_router_topk without a workspace, for callers that cannot allocate device
-    memory: the router scratch is a static array inside libmoe.so (8 MiB limit)."""
+    memory: the router scratch is a static array inside libmoe.so (32 MiB limit)."""
     _check(_lib.moe_router_topk_noalloc(ctypes.byref(cfg), _p(x), _p(w_r), _p(b_r), _p(topk_idx),
                                         _p(topk_gate), _p(counts_routed), _p(counts_kept),
                                         _p(expert_offsets), _p(slot_row), _p(perm_token), _p(aux),

@@ -12,14 +12,12 @@ namespace moe {
 constexpr uint32_t kErrFault = 1u;    // an out-of-range index was seen and skipped
 constexpr uint32_t kErrTimeout = 2u;  // a bounded wait gave up
 
-// The router kernel handles tokens in tiles of 8 * router_warps(cfg) tokens.
-// The tile size is a pure function of the config (no device query) so that the
-// workspace size can be computed without a GPU; 148 is the B300 SM count.
-constexpr int kSmCountForTiling = 148;
-int router_warps(const moe_config &c);
-inline int router_tile_tokens(const moe_config &c) { return 8 * router_warps(c); }
+// The router writes its per-expert statistics per tile of router_tile_tokens(cfg)
+// tokens; the tile is a pure function of the config (no device query), so the
+// workspace size can be computed without a GPU.
+int router_tile_tokens(const moe_config &c);
 inline int router_tiles(const moe_config &c) {
-    int tt = router_tile_tokens(c);
+    const int tt = router_tile_tokens(c);
     return (c.T + tt - 1) / tt;
 }
 
@@ -35,6 +33,8 @@ struct WsLayout {
     size_t psum;                 // f32   [N][tiles]
     size_t pmean;                // f32   [N]
     size_t routed, kept;         // int32 [N] (used when the caller passes NULL)
+    size_t logits;               // f32   [T][N]  (N > 32 only)
+    size_t w_t;                  // f32   [N][d]  router weight transposed (N > 32 only)
     size_t offsets;              // int32 [N+1]
     size_t topk_idx, topk_gate;  // [T][k]
     size_t slot_row;             // int32 [T][k]

@@ -47,6 +47,8 @@ WsLayout ws_layout(const moe_config &c) {
     L.pmean = take(N * 4);
     L.routed = take(N * 4);
     L.kept = take(N * 4);
+    L.logits = take(c.N > 32 ? T * N * 4 : 0);
+    L.w_t = take(c.N > 32 ? N * (size_t)c.d * 4 : 0);
     // expert / shared-expert buffers
     L.hid = take(rmax * c.h * es);
     L.hid_sh = take(c.h_shared ? T * c.h_shared * es : 0);
@@ -72,7 +74,7 @@ int device_sm_count() {
             cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
             count = v;
         else
-            return kSmCountForTiling;
+            return 148;  // B300
     }
     return count;
 }

@@ -22,7 +22,7 @@
 
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB
 constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) uint8_t g_router_scratch[kNoAllocScratchBytes];

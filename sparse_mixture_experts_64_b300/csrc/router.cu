@@ -11,16 +11,27 @@
 // Transformers ... explained", section "Making it work" (router in higher
 // precision, capacity with overflow skipping the layer).
 //
-// Three kernels, no atomics, deterministic:
-//   k_router       one CTA per tile of 8*warps tokens: logits (fp32 FMA chain over
-//                  d in increasing order), top-k, gates, full softmax; writes per
-//                  tile, per expert: routed counts per slot and the sum of p.
-//   k_expert_scan  one CTA per expert: priority-order prefix of the tile counts
-//                  (slot-major, token order), capacity clamp, kept-per-tile prefix,
-//                  routed/kept totals, mean routing probability P_e.
-//   k_assign       one CTA per tile: expert offsets, keep/drop per slot, row of
-//                  each kept slot (expert ascending, token ascending), perm_token;
-//                  CTA 0 also writes expert_offsets and the aux losses.
+// Logit summation order (the pages fix none; routing must be bit-exact, so one
+// order is specified): features in blocks of 8; lane l of a warp accumulates
+// blocks l, l+32, l+64, ... with one fp32 fma per feature in increasing order,
+// starting from 0; the 32 lane partials are combined by five xor-butterfly
+// rounds v = v + shfl_xor(v, o), o = 16, 8, 4, 2, 1, and lane 0's value is the
+// logit; the bias is added last. Every kernel below keeps exactly this order.
+//
+// Kernels (no atomics, deterministic):
+//   k_router_small   N <= 32: one CTA per tile of tokens; each lane holds every
+//                    expert's partial for its tokens; gating fused (one thread per
+//                    token). Per-tile routed counts per slot and sums of p.
+//   k_transpose_wr   N > 32: router weight [d][N] -> [N][d] (workspace), so that a
+//                    lane's 8 features of one expert are contiguous.
+//   k_logits_large   N > 32: 16 tokens x 32 experts per CTA -> logits [T][N].
+//   k_gate           N > 32: one warp per token: top-k, softmax, gates; per-tile stats.
+//   k_expert_scan    one CTA per expert: priority-order prefix of the tile counts
+//                    (slot-major, token order), capacity clamp, kept-per-tile
+//                    prefix, routed/kept totals, mean routing probability P_e.
+//   k_assign         one CTA per tile: keep/drop per slot, row of each kept slot
+//                    (expert ascending, token ascending), perm_token; CTA 0 also
+//                    writes expert_offsets and the aux losses.
 #include <algorithm>
 #include <climits>
 #include <cmath>
@@ -31,16 +42,17 @@
 
 namespace moe {
 
-int router_warps(const moe_config &c) {
-    if (c.N > 32) {
-        const int warp_tiles = (c.T + 7) / 8;
-        const int w = (warp_tiles + kSmCountForTiling - 1) / kSmCountForTiling;
-        return std::min(8, std::max(1, w));
-    }
-    return 2;
+// Experts per lane register row of the small kernel: 4, 8, 16 or 32.
+static int router_np(int N) { return N <= 4 ? 4 : N <= 8 ? 8 : N <= 16 ? 16 : 32; }
+
+int router_tile_tokens(const moe_config &c) {
+    if (c.N > 32) return 64;           // k_gate: 8 warps x 8 tokens
+    return 4 * (32 / router_np(c.N));  // k_router_small: 4 warps x (32 / NP) tokens
 }
 
 namespace {
+
+constexpr uint64_t kWaitNs = 1000000000ull;  // bound of every mbarrier wait (1 s)
 
 struct RouterArgs {
     int T, d, N, k, gating, tiles, has_bias;
@@ -48,35 +60,135 @@ struct RouterArgs {
     float *topk_gate;
     int32_t *cnt;   // [N][k][tiles]
     float *psum;    // [N][tiles]
-    uint32_t *err;  // device error word (bounded waits)
+    uint32_t *err;  // device error word
 };
 
-__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
-    uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
-    uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int n> __device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;\n" ::"n"(n) : "memory");
+// 8 consecutive features of one token as fp32 (16 bytes of bf16, 32 of fp32).
+template <typename XT>
+__device__ __forceinline__ void load8(const uint8_t *p, float *f) {
+    Vec16<XT>::load(reinterpret_cast<const XT *>(p), f);
+    if constexpr (sizeof(XT) == 4) Vec16<XT>::load(reinterpret_cast<const XT *>(p) + 4, f + 4);
 }
 
 template <int n> __device__ __forceinline__ void lds(const float *p, float *v) {
-    if constexpr (n % 4 == 0) {
 #pragma unroll
-        for (int i = 0; i < n; i += 4) {
-            float4 q = *reinterpret_cast<const float4 *>(p + i);
-            v[i] = q.x; v[i + 1] = q.y; v[i + 2] = q.z; v[i + 3] = q.w;
+    for (int i = 0; i < n; i += 4) {
+        const float4 q = *reinterpret_cast<const float4 *>(p + i);
+        v[i] = q.x; v[i + 1] = q.y; v[i + 2] = q.z; v[i + 3] = q.w;
+    }
+}
+
+// v <- v + shfl_xor(v, o) for o = 16 .. 1; lane 0 then holds the specified sum.
+__device__ __forceinline__ float butterfly32(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Bounded wait for phase `par` of `bar`; on expiry sets *abort_flag and records
+// MOE_ERR_TIMEOUT. Returns false if the wait ran out or another thread aborted.
+__device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t par, int *abort_flag, uint32_t *err) {
+    if (tc::mbar_try_wait(bar, par)) return true;
+    const uint64_t t0 = tc::globaltimer_ns();
+    while (!tc::mbar_try_wait(bar, par)) {
+        if (*(volatile int *)abort_flag) return false;
+        if (tc::globaltimer_ns() - t0 > kWaitNs) {
+            *(volatile int *)abort_flag = 1;
+            record_error(err, kErrTimeout);
+            return false;
         }
-    } else if constexpr (n == 2) {
-        float2 q = *reinterpret_cast<const float2 *>(p);
-        v[0] = q.x; v[1] = q.y;
-    } else {
+    }
+    return true;
+}
+
+// Stride (in floats) of one staged block of 8 router-weight rows [8][N] in the
+// small kernel: room for reads up to column NP-1 and == 4 (mod 32) words, so the
+// 32 lanes reading 32 different blocks spread over the banks.
+__host__ __device__ inline int wblock_stride(int N, int NP) {
+    int s = 8 * N + (NP > N ? NP - N : 0);
+    s = (s + 3) & ~3;
+    s += ((4 - (s & 31)) + 32) & 31;
+    return s;
+}
+
+// ------------------------------------------------------------------ gating
+
+// Per-tile statistics from p (Ls) and the selections (Is): per expert, the sum of
+// p over the tile's tokens and the number of tokens choosing it in each slot.
+__device__ __forceinline__ void tile_stats(const float *Ls, const int *Is, const RouterArgs &a, int TT) {
+    const int N = a.N, k = a.k;
+    for (int e = threadIdx.x; e < N; e += blockDim.x) {
+        float ps = 0.0f;
+        int cj[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        for (int tok = 0; tok < TT; ++tok) {
+            ps += Ls[tok * N + e];
 #pragma unroll
-        for (int i = 0; i < n; ++i) v[i] = p[i];
+            for (int j = 0; j < 8; ++j)
+                if (j < k && Is[tok * 8 + j] == e) ++cj[j];
+        }
+        a.psum[(size_t)e * a.tiles + blockIdx.x] = ps;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (j < k) a.cnt[((size_t)e * k + j) * a.tiles + blockIdx.x] = cj[j];
+    }
+}
+
+// Gating for N <= NP <= 32 experts, one thread per token. Ls [TT][N] holds the
+// logits on entry and p on exit; Is [TT][8] receives the selections.
+template <int NP>
+__device__ __forceinline__ void gate_tokens_thread(float *Ls, int *Is, const RouterArgs &a, int TT) {
+    const int N = a.N, T = a.T, k = a.k;
+    const int t0 = blockIdx.x * TT;
+    for (int tok = threadIdx.x; tok < TT; tok += blockDim.x) {
+        float *L = Ls + tok * N;
+        const int t = t0 + tok;
+        if (t >= T) {
+            for (int e = 0; e < N; ++e) L[e] = 0.0f;
+            for (int j = 0; j < 8; ++j) Is[tok * 8 + j] = -1;
+            continue;
+        }
+        float Lr[NP];
+#pragma unroll
+        for (int e = 0; e < NP; ++e) Lr[e] = e < N ? L[e] : 0.0f;
+        uint32_t taken = 0;
+        float vmax = 0.0f, den = 0.0f;
+        for (int s = 0; s < k; ++s) {
+            float bv = -INFINITY;
+            int bi = -1;
+#pragma unroll
+            for (int e = 0; e < NP; ++e)  // ascending e, strict '>': lowest index wins ties
+                if (e < N && !((taken >> e) & 1u) && (bi < 0 || Lr[e] > bv)) {
+                    bv = Lr[e];
+                    bi = e;
+                }
+            taken |= 1u << bi;
+            if (s == 0) vmax = bv;
+            Is[tok * 8 + s] = bi;
+        }
+        float sum = 0.0f;
+#pragma unroll
+        for (int e = 0; e < NP; ++e) {
+            Lr[e] = e < N ? expf(Lr[e] - vmax) : 0.0f;
+            sum += Lr[e];
+        }
+        auto pick = [&](int e) {  // Lr[e] without dynamic register indexing
+            float v = 0.0f;
+#pragma unroll
+            for (int q = 0; q < NP; ++q) v = q == e ? Lr[q] : v;
+            return v;
+        };
+        if (a.gating != MOE_SOFTMAX_THEN_TOPK)
+            for (int s = 0; s < k; ++s) den += pick(Is[tok * 8 + s]);
+        for (int s = 0; s < k; ++s) {
+            const int e = Is[tok * 8 + s];
+            const float ex = pick(e);
+            a.topk_idx[(size_t)t * k + s] = e;
+            a.topk_gate[(size_t)t * k + s] = a.gating == MOE_SOFTMAX_THEN_TOPK ? ex / sum : ex / den;
+        }
+        for (int s = k; s < 8; ++s) Is[tok * 8 + s] = -1;
+#pragma unroll
+        for (int e = 0; e < NP; ++e)
+            if (e < N) L[e] = Lr[e] / sum;
     }
 }
 
@@ -86,60 +198,12 @@ __device__ __forceinline__ float warp_sum_bcast(float v) {
     return __shfl_sync(0xffffffffu, v, 0);
 }
 
-// Expert of accumulator j of a thread in expert group le. With EPT >= 4 the
-// experts come in runs of 4 interleaved across the LE groups, so one 128-bit
-// shared load per run covers LE*16 contiguous bytes (no bank conflicts).
-template <int LE, int EPT>
-__device__ __forceinline__ int expert_of(int le, int j) {
-    if constexpr (EPT >= 4) return (j / 4) * (LE * 4) + le * 4 + (j % 4);
-    else return le * EPT + j;
-}
-
-template <int LE, int EPT, bool VEC>
-__device__ __forceinline__ void load_w(const float *row, int le, float *wv) {
-    if constexpr (VEC && EPT >= 4) {
-#pragma unroll
-        for (int g = 0; g < EPT / 4; ++g) lds<4>(row + g * LE * 4 + le * 4, wv + 4 * g);
-    } else if constexpr (VEC) {
-        lds<EPT>(row + le * EPT, wv);
-    } else {
-#pragma unroll
-        for (int j = 0; j < EPT; ++j) wv[j] = row[expert_of<LE, EPT>(le, j)];
-    }
-}
-
-// Logits -> gating -> per-tile statistics, shared by both router kernels.
-// acc holds this thread's logits (TPT tokens x EPT experts, expert_of mapping);
-// smem must hold TT*N + TT*8 words and be free (all staging consumed).
-template <int LE, int EPT, int TPT>
-__device__ __forceinline__ void router_tail(float (&acc)[TPT][EPT], float *smem, const float *__restrict__ b_r,
-                                            const RouterArgs &a, int TT, int tok_base, int le) {
-    constexpr int NP = LE * EPT;
-    constexpr int QMAX = (NP + 31) / 32;
-    const int N = a.N, T = a.T;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int nthreads = blockDim.x, nwarps = nthreads / 32;
+// Gating for any N <= 256, one warp per token (lane holds experts lane + 32q).
+__device__ __forceinline__ void gate_tokens_warp(float *Ls, int *Is, const RouterArgs &a, int TT) {
+    constexpr int QMAX = 8;
+    const int N = a.N, T = a.T, k = a.k;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
     const int t0 = blockIdx.x * TT;
-    // ---- logits to shared memory: Ls[TT][N]; Is[TT][8] behind it ----
-    float *Ls = smem;
-    int *Is = reinterpret_cast<int *>(smem + TT * N);
-#pragma unroll
-    for (int j = 0; j < EPT; ++j) {
-        const int e = expert_of<LE, EPT>(le, j);
-        if (e < N) {
-            const float bj = a.has_bias ? b_r[e] : 0.0f;
-#pragma unroll
-            for (int i = 0; i < TPT; ++i) {
-                float v = acc[i][j];
-                if (a.has_bias) v = __fadd_rn(v, bj);
-                Ls[(tok_base + i) * N + e] = v;
-            }
-        }
-    }
-    __syncthreads();
-
-    // ---- gating: one warp per token ----
-    const int k = a.k;
     for (int tok = warp; tok < TT; tok += nwarps) {
         const int t = t0 + tok;
         if (t >= T) {
@@ -209,448 +273,263 @@ __device__ __forceinline__ void router_tail(float (&acc)[TPT][EPT], float *smem,
         }
         if (lane < 8) Is[tok * 8 + lane] = lane < k ? my_e : -1;
     }
-    __syncthreads();
-
-    // ---- per-expert statistics of this tile ----
-    for (int e = tid; e < N; e += nthreads) {
-        float ps = 0.0f;
-        int cj[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        for (int tok = 0; tok < TT; ++tok) {
-            ps += Ls[tok * N + e];
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (j < k && Is[tok * 8 + j] == e) ++cj[j];
-        }
-        a.psum[(size_t)e * a.tiles + blockIdx.x] = ps;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            if (j < k) a.cnt[((size_t)e * k + j) * a.tiles + blockIdx.x] = cj[j];
-    }
 }
 
-// Gating tail for few experts (N <= 32): one thread per token (no shuffles),
-// then per-tile statistics. Same rules as router_tail: top-k by logit, lower
-// index first on ties, softmax over all N in fp32, gates per convention.
-template <int LE, int EPT, int TPT>
-__device__ __forceinline__ void router_tail_small(float (&acc)[TPT][EPT], float *smem,
-                                                  const float *__restrict__ b_r, const RouterArgs &a, int TT,
-                                                  int tok_base, int le) {
-    const int N = a.N, T = a.T, k = a.k;
-    const int tid = threadIdx.x, nthreads = blockDim.x;
-    const int t0 = blockIdx.x * TT;
-    float *Ls = smem;                                   // [TT][N] logits, then p
-    int *Is = reinterpret_cast<int *>(smem + TT * N);   // [TT][8]
-#pragma unroll
-    for (int j = 0; j < EPT; ++j) {
-        const int e = expert_of<LE, EPT>(le, j);
-        if (e < N) {
-            const float bj = a.has_bias ? b_r[e] : 0.0f;
-#pragma unroll
-            for (int i = 0; i < TPT; ++i) {
-                float v = acc[i][j];
-                if (a.has_bias) v = __fadd_rn(v, bj);
-                Ls[(tok_base + i) * N + e] = v;
-            }
-        }
-    }
-    __syncthreads();
-    constexpr int NP = LE * EPT;  // <= 32: one token's logits fit in registers
-    for (int tok = tid; tok < TT; tok += nthreads) {
-        float *L = Ls + tok * N;
-        const int t = t0 + tok;
-        if (t >= T) {
-            for (int e = 0; e < N; ++e) L[e] = 0.0f;
-            for (int j = 0; j < 8; ++j) Is[tok * 8 + j] = -1;
-            continue;
-        }
-        float Lr[NP];
-#pragma unroll
-        for (int e = 0; e < NP; ++e) Lr[e] = e < N ? L[e] : 0.0f;
-        uint32_t taken = 0;
-        float vmax = 0.0f, den = 0.0f;
-        for (int s = 0; s < k; ++s) {
-            float bv = -INFINITY;
-            int bi = -1;
-#pragma unroll
-            for (int e = 0; e < NP; ++e)  // ascending e, strict '>': lowest index wins ties
-                if (e < N && !((taken >> e) & 1u) && (bi < 0 || Lr[e] > bv)) {
-                    bv = Lr[e];
-                    bi = e;
-                }
-            taken |= 1u << bi;
-            if (s == 0) vmax = bv;
-            Is[tok * 8 + s] = bi;
-        }
-        float sum = 0.0f;
-#pragma unroll
-        for (int e = 0; e < NP; ++e) {
-            Lr[e] = e < N ? expf(Lr[e] - vmax) : 0.0f;
-            sum += Lr[e];
-        }
-        // exp of a selected expert's logit, picked without dynamic register indexing
-        auto pick = [&](int e) {
-            float v = 0.0f;
-#pragma unroll
-            for (int q = 0; q < NP; ++q) v = q == e ? Lr[q] : v;
-            return v;
-        };
-        if (a.gating != MOE_SOFTMAX_THEN_TOPK)
-            for (int s = 0; s < k; ++s) den += pick(Is[tok * 8 + s]);
-        for (int s = 0; s < k; ++s) {
-            const int e = Is[tok * 8 + s];
-            const float ex = pick(e);
-            a.topk_idx[(size_t)t * k + s] = e;
-            a.topk_gate[(size_t)t * k + s] = a.gating == MOE_SOFTMAX_THEN_TOPK ? ex / sum : ex / den;
-        }
-        for (int s = k; s < 8; ++s) Is[tok * 8 + s] = -1;
-#pragma unroll
-        for (int e = 0; e < NP; ++e)
-            if (e < N) L[e] = Lr[e] / sum;
-    }
-    __syncthreads();
-    for (int e = tid; e < N; e += nthreads) {
-        float ps = 0.0f;
-        int cj[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        for (int tok = 0; tok < TT; ++tok) {
-            ps += Ls[tok * N + e];
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (j < k && Is[tok * 8 + j] == e) ++cj[j];
-        }
-        a.psum[(size_t)e * a.tiles + blockIdx.x] = ps;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            if (j < k) a.cnt[((size_t)e * k + j) * a.tiles + blockIdx.x] = cj[j];
-    }
-}
+// ------------------------------------------------------------------ N <= 32
 
-// Shared-memory plan of the logits loop: a ring of STAGES chunks, each holding
-// KC features of the router weight ([KC][N] fp32) and of the tile's token rows
-// ([TT][KC] input type, rows padded by 16 bytes), filled by cp.async; plus one
-// fp32 transposed copy of the current chunk's token values ([KC][TT]).
-template <typename XT, int KC>
-struct RouterSmem {
-    static constexpr int STAGES = 4;
-    static constexpr int XROW = KC * (int)sizeof(XT) + 16;  // bytes per staged token row
-    static __host__ __device__ size_t w_bytes(int N) { return (size_t)KC * N * 4; }
-    static __host__ __device__ size_t x_bytes(int TT) { return (size_t)TT * XROW; }
-    static __host__ __device__ size_t stage_bytes(int N, int TT) { return w_bytes(N) + x_bytes(TT); }
-    static __host__ __device__ size_t xf_offset(int N, int TT) { return STAGES * stage_bytes(N, TT); }
-    // + NP floats of padding: lanes whose experts are >= N read (and discard) past the last row
-    static __host__ __device__ size_t loop_bytes(int N, int TT, int NP) {
-        return xf_offset(N, TT) + (size_t)KC * TT * 4 + (size_t)NP * 4;
-    }
-};
-
-// Thread tile: TPT tokens x EPT experts; a warp is (32/LE) token groups x LE
-// expert groups = 8 tokens x LE*EPT experts; warps stack along tokens.
-template <typename XT, int LE, int EPT, int TPT, int KC, bool NALIGN4>
-__global__ void __launch_bounds__(256) k_router(const XT *__restrict__ x, const float *__restrict__ w_r,
-                                                const float *__restrict__ b_r, RouterArgs a) {
-    using SM = RouterSmem<XT, KC>;
-    constexpr int STAGES = SM::STAGES;
-    constexpr int NP = LE * EPT;
-    constexpr int VX = 16 / sizeof(XT);  // input elements per 16 bytes
-    static_assert((32 / LE) * TPT == 8, "a warp covers 8 tokens");
-    static_assert(KC % 8 == 0, "chunks hold whole 16-byte pieces");
-    extern __shared__ __align__(16) float smem[];
-    uint8_t *sbytes = reinterpret_cast<uint8_t *>(smem);
-
-    const int nthreads = blockDim.x;
-    const int nwarps = nthreads / 32;
-    const int TT = nwarps * 8;
-    const int N = a.N, d = a.d, T = a.T;
-    const size_t stage_b = SM::stage_bytes(N, TT);
-    const size_t wb_b = SM::w_bytes(N);
-    float *Xf = reinterpret_cast<float *>(sbytes + SM::xf_offset(N, TT));  // [KC][TT]
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int le = lane % LE, lt = lane / LE;
-    const int t0 = blockIdx.x * TT;
-    const int tok_base = warp * 8 + lt * TPT;
-
-    float acc[TPT][EPT];
-#pragma unroll
-    for (int i = 0; i < TPT; ++i)
-#pragma unroll
-        for (int j = 0; j < EPT; ++j) acc[i][j] = 0.0f;
-
-    const int nchunks = (d + KC - 1) / KC;
-
-    // Copy chunk c into ring slot c % STAGES (one commit group per call, even if empty).
-    auto issue = [&](int c) {
-        if (c < nchunks) {
-            const int k0 = c * KC;
-            const int kc = min(KC, d - k0);
-            uint8_t *slot = sbytes + (size_t)(c % STAGES) * stage_b;
-            float *wdst = reinterpret_cast<float *>(slot);
-            const float *wsrc = w_r + (size_t)k0 * N;
-            if constexpr (NALIGN4) {
-                const int nvec = kc * N / 4;
-                for (int v = tid; v < nvec; v += nthreads) cp_async16(wdst + 4 * v, wsrc + 4 * v);
-            } else {
-                const int n = kc * N;
-                for (int v = tid; v < n; v += nthreads) cp_async4(wdst + v, wsrc + v);
-            }
-            uint8_t *xdst = slot + wb_b;
-            const int pieces = kc / VX;  // 16-byte pieces per token row in this chunk
-            for (int v = tid; v < TT * pieces; v += nthreads) {
-                const int tok = v / pieces, q = v % pieces;
-                const int t = t0 + tok;
-                if (t < T) cp_async16(xdst + (size_t)tok * SM::XROW + q * 16, x + (size_t)t * d + k0 + q * VX);
-            }
-        }
-        cp_async_commit();
-    };
-
-#pragma unroll
-    for (int c = 0; c < STAGES - 1; ++c) issue(c);
-
-    for (int c = 0; c < nchunks; ++c) {
-        cp_async_wait<STAGES - 2>();  // this thread's copies of chunk c have landed
-        __syncthreads();              // ... everyone's; and chunk c-1 is fully consumed
-        issue(c + STAGES - 1);        // into the slot chunk c-1 used
-        const uint8_t *slot = sbytes + (size_t)(c % STAGES) * stage_b;
-        const int kc = min(KC, d - c * KC);
-        // token values of this chunk -> fp32, transposed to [KC][TT]
-        {
-            const uint8_t *xs = slot + wb_b;
-            const int pieces = kc / VX;
-            for (int v = tid; v < TT * pieces; v += nthreads) {
-                const int q = v / TT, tok = v % TT;
-                float f[VX];
-                if (t0 + tok < T) {
-                    Vec16<XT>::load(reinterpret_cast<const XT *>(xs + (size_t)tok * SM::XROW + q * 16), f);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < VX; ++i) f[i] = 0.0f;
-                }
-#pragma unroll
-                for (int i = 0; i < VX; ++i) Xf[(q * VX + i) * TT + tok] = f[i];
-            }
-        }
-        __syncthreads();
-        const float *wb = reinterpret_cast<const float *>(slot);
-        const float *xb = Xf + tok_base;
-        if constexpr (TPT * EPT <= 8) {
-            // Few accumulators: the FMA chains are the critical path, so load the
-            // operands of the next 8 features while the current 8 are consumed.
-            float xa[8][TPT], wa[8][EPT], xn[8][TPT], wn[8][EPT];
-            auto load8 = [&](int k0, float (*xv)[TPT], float (*wv)[EPT]) {
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    lds<TPT>(xb + (k0 + q) * TT, xv[q]);
-                    load_w<LE, EPT, NALIGN4>(wb + (k0 + q) * N, le, wv[q]);
-                }
-            };
-            auto fma8 = [&](float (*xv)[TPT], float (*wv)[EPT]) {
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-#pragma unroll
-                    for (int i = 0; i < TPT; ++i)
-#pragma unroll
-                        for (int j = 0; j < EPT; ++j) acc[i][j] = __fmaf_rn(xv[q][i], wv[q][j], acc[i][j]);
-            };
-            load8(0, xa, wa);
-            for (int k8 = 0; k8 < kc; k8 += 16) {
-                if (k8 + 8 < kc) load8(k8 + 8, xn, wn);
-                fma8(xa, wa);
-                if (k8 + 8 < kc) {
-                    if (k8 + 16 < kc) load8(k8 + 16, xa, wa);
-                    fma8(xn, wn);
-                }
-            }
-        } else {
-#pragma unroll 4
-            for (int kk = 0; kk < kc; ++kk) {
-                float xv[TPT], wv[EPT];
-                lds<TPT>(xb + kk * TT, xv);
-                load_w<LE, EPT, NALIGN4>(wb + kk * N, le, wv);
-#pragma unroll
-                for (int i = 0; i < TPT; ++i)
-#pragma unroll
-                    for (int j = 0; j < EPT; ++j) acc[i][j] = __fmaf_rn(xv[i], wv[j], acc[i][j]);
-            }
-        }
-    }
-    cp_async_wait<0>();
-    __syncthreads();
-
-    router_tail<LE, EPT, TPT>(acc, smem, b_r, a, TT, tok_base, le);
-}
-
-// Router for few experts (LE*EPT <= 32). Here every logit's FMA chain over d is
-// the critical path, so the loop is shaped for latency: the tile shape is fixed
-// at compile time (NW warps, 8*NW tokens), the weight chunk is staged with row
-// stride NP so every shared load uses an immediate offset, the token rows stay in
-// their input type and are converted in registers (8 features per 128-bit load),
-// and one barrier per chunk recycles the ring slot used two chunks earlier.
-template <typename XT, int LE, int EPT, int NW, int KC, bool BULK>
-__global__ void __launch_bounds__(NW * 32) k_router_small(const XT *__restrict__ x, const float *__restrict__ w_r,
-                                                         const float *__restrict__ b_r, RouterArgs a) {
-    constexpr int NP = LE * EPT;
-    constexpr int TT = NW * 8;
-    constexpr int TPT = 8 * LE / 32;
-    constexpr int STAGES = 4;
+// One CTA = 4 warps; warp w owns TO = 32/NP tokens and all NP experts; lane l
+// owns partial l. Chunks of 256 features (one 8-feature block per lane) are
+// staged by bulk copies issued from warp 0 (lane j copies weight block j and
+// token row j) into a 6-slot ring, each slot completing on its own mbarrier.
+template <typename XT, int NP, bool VEC>
+__global__ void __launch_bounds__(128) k_router_small(const XT *__restrict__ x, const float *__restrict__ w_r,
+                                                     const float *__restrict__ b_r, RouterArgs a) {
+    constexpr int NW = 4, TO = 32 / NP, TT = NW * TO;
+    constexpr int KC = 256, NBLK = KC / 8;
+    constexpr int STAGES = 6;
     constexpr int ES = (int)sizeof(XT);
-    constexpr int VX = 16 / ES;
-    constexpr int XROW = KC * ES + 16;                       // bytes per staged token row
-    constexpr int W_BYTES = KC * NP * 4;
-    constexpr int STAGE = W_BYTES + TT * XROW;
-    static_assert(NP <= 32 && (32 / LE) * TPT == 8, "small-N tile");
-    static_assert(KC % 8 == 0 && (W_BYTES % 16) == 0, "16-byte pieces");
-    static_assert(TT <= 31, "one token row per lane of warp 0");
+    constexpr int XROW = KC * ES + 16;
+    static_assert(TT <= 32, "one token row per lane of warp 0");
     extern __shared__ __align__(16) float smem[];
     __shared__ uint64_t full[STAGES];
     __shared__ int abort_flag;
     uint8_t *sb = reinterpret_cast<uint8_t *>(smem);
 
     const int N = a.N, d = a.d, T = a.T;
+    const int BST = wblock_stride(N, NP);
+    const int W_BYTES = NBLK * BST * 4;
+    const int STAGE = W_BYTES + TT * XROW;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int le = lane % LE, lt = lane / LE;
     const int t0 = blockIdx.x * TT;
-    const int tok_base = warp * 8 + lt * TPT;
-    const int nchunks = (d + KC - 1) / KC;
     const int ntok = min(TT, T - t0);
-
-    float acc[TPT][EPT];
-#pragma unroll
-    for (int i = 0; i < TPT; ++i)
-#pragma unroll
-        for (int j = 0; j < EPT; ++j) acc[i][j] = 0.0f;
+    const int nblocks = d / 8;
+    const int nchunks = (nblocks + NBLK - 1) / NBLK;
 
     if (tid == 0) {
         abort_flag = 0;
-        if constexpr (BULK) {
-            for (int i = 0; i < STAGES; ++i) tc::mbar_init(&full[i], 1);
-            tc::fence_mbar_init();
-        }
+        for (int i = 0; i < STAGES; ++i) tc::mbar_init(&full[i], 1);
+        tc::fence_mbar_init();
     }
     __syncthreads();
 
-    // Stage chunk c into ring slot c % STAGES. BULK: one thread issues one bulk
-    // copy for the weight rows (contiguous, N == NP) and one per token row, all
-    // completing on the slot's mbarrier. Otherwise every thread issues cp.async.
     auto issue = [&](int c) {
-        if constexpr (BULK) {
-            // warp 0: lane 0 arms the barrier, then lane 0 copies the weight rows
-            // and lanes 1..ntok one token row each (TT <= 31)
-            if (warp == 0 && c < nchunks) {
-                const int k0 = c * KC, kc = min(KC, d - k0);
-                uint8_t *slot = sb + (c % STAGES) * STAGE;
-                const uint32_t wbytes = (uint32_t)(kc * N * 4), xbytes = (uint32_t)(kc * ES);
-                uint64_t *bar = &full[c % STAGES];
-                if (lane == 0) tc::mbar_arrive_expect_tx(bar, wbytes + xbytes * (uint32_t)ntok);
-                __syncwarp();
-                if (lane == 0) tc::bulk_copy_g2s(slot, w_r + (size_t)k0 * N, wbytes, bar);
-                else if (lane <= ntok)
-                    tc::bulk_copy_g2s(slot + W_BYTES + (lane - 1) * XROW, x + (size_t)(t0 + lane - 1) * d + k0,
-                                      xbytes, bar);
-            }
-        } else {
-            if (c < nchunks) {
-                const int k0 = c * KC, kc = min(KC, d - k0);
-                uint8_t *slot = sb + (c % STAGES) * STAGE;
-                float *wdst = reinterpret_cast<float *>(slot);
-                const float *wsrc = w_r + (size_t)k0 * N;
-                for (int v = tid; v < kc * N; v += NW * 32) {
-                    const int r = v / N, e = v - r * N;
-                    cp_async4(wdst + r * NP + e, wsrc + v);
-                }
-                uint8_t *xdst = slot + W_BYTES;
-                const int pieces = kc / VX;
-                for (int v = tid; v < ntok * pieces; v += NW * 32) {
-                    const int tok = v / pieces, q = v - tok * pieces;
-                    cp_async16(xdst + tok * XROW + q * 16, x + (size_t)(t0 + tok) * d + k0 + q * VX);
-                }
-            }
-            cp_async_commit();
-        }
-    };
-    // Wait until chunk c has landed; false if the wait ran out (error recorded).
-    auto wait_chunk = [&](int c) -> bool {
-        if constexpr (BULK) {
-            uint64_t *bar = &full[c % STAGES];
-            const uint32_t par = (uint32_t)((c / STAGES) & 1);
-            if (!tc::mbar_try_wait(bar, par)) {
-                const uint64_t ts = tc::globaltimer_ns();
-                while (!tc::mbar_try_wait(bar, par)) {
-                    if (*(volatile int *)&abort_flag) return false;
-                    if (tc::globaltimer_ns() - ts > 1000000000ull) {
-                        *(volatile int *)&abort_flag = 1;
-                        record_error(a.err, kErrTimeout);
-                        return false;
-                    }
-                }
-            }
-            return true;
-        } else {
-            cp_async_wait<STAGES - 2>();
-            return true;
-        }
+        if (warp != 0 || c >= nchunks) return;
+        const int b0 = c * NBLK, nb = min(NBLK, nblocks - b0);
+        uint8_t *slot = sb + (size_t)(c % STAGES) * STAGE;
+        uint64_t *bar = &full[c % STAGES];
+        const uint32_t wb = (uint32_t)(8 * N * 4), xb = (uint32_t)(nb * 8 * ES);
+        if (lane == 0) tc::mbar_arrive_expect_tx(bar, (uint32_t)nb * wb + (uint32_t)ntok * xb);
+        __syncwarp();
+        if (lane < nb) tc::bulk_copy_g2s(slot + lane * BST * 4, w_r + (size_t)(b0 + lane) * 8 * N, wb, bar);
+        if (lane < ntok)
+            tc::bulk_copy_g2s(slot + W_BYTES + lane * XROW, x + (size_t)(t0 + lane) * d + (size_t)b0 * 8, xb, bar);
     };
 
-    auto load_x8 = [&](const uint8_t *xs, int k8, float (*xv)[TPT]) {
+    float acc[TO][NP];
 #pragma unroll
-        for (int i = 0; i < TPT; ++i) {
-            float f[8];
-            const XT *p = reinterpret_cast<const XT *>(xs + (tok_base + i) * XROW) + k8;
-            Vec16<XT>::load(p, f);
-            if constexpr (VX == 4) Vec16<XT>::load(p + 4, f + 4);
+    for (int i = 0; i < TO; ++i)
 #pragma unroll
-            for (int q = 0; q < 8; ++q) xv[q][i] = f[q];
-        }
-    };
-    auto step8 = [&](const float *ws, const uint8_t *xs, int k8) {
-        float xv[8][TPT], wv[8][EPT];
-        load_x8(xs, k8, xv);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) lds<EPT>(ws + (k8 + q) * NP + le * EPT, wv[q]);
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-#pragma unroll
-            for (int i = 0; i < TPT; ++i)
-#pragma unroll
-                for (int j = 0; j < EPT; ++j) acc[i][j] = __fmaf_rn(xv[q][i], wv[q][j], acc[i][j]);
-    };
+        for (int e = 0; e < NP; ++e) acc[i][e] = 0.0f;
 
 #pragma unroll
     for (int c = 0; c < STAGES - 1; ++c) issue(c);
-    int issued = STAGES - 1;
     bool ok = true;
+    int issued = min(STAGES - 1, nchunks);
     for (int c = 0; c < nchunks; ++c) {
-        ok = wait_chunk(c);
+        const bool mine = wait_phase(&full[c % STAGES], (uint32_t)((c / STAGES) & 1), &abort_flag, a.err);
         __syncthreads();
-        if (!ok || *(volatile int *)&abort_flag) {
+        if (!mine || *(volatile int *)&abort_flag) {
             ok = false;
             break;
         }
         issue(c + STAGES - 1);
-        ++issued;
-        const uint8_t *slot = sb + (c % STAGES) * STAGE;
-        const float *ws = reinterpret_cast<const float *>(slot);
-        const uint8_t *xs = slot + W_BYTES;
-        const int kc = min(KC, d - c * KC);
-        if (kc == KC) {
+        if (c + STAGES - 1 < nchunks) ++issued;
+        const uint8_t *slot = sb + (size_t)(c % STAGES) * STAGE;
+        if (c * NBLK + lane < nblocks) {
+            const float *wbk = reinterpret_cast<const float *>(slot) + lane * BST;
+            float xf[TO][8];
 #pragma unroll
-            for (int k8 = 0; k8 < KC; k8 += 8) step8(ws, xs, k8);
-        } else {
-            for (int k8 = 0; k8 < kc; k8 += 8) step8(ws, xs, k8);
+            for (int i = 0; i < TO; ++i) load8<XT>(slot + W_BYTES + (warp * TO + i) * XROW + lane * 8 * ES, xf[i]);
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                float wv[NP];
+                if constexpr (VEC) {
+                    lds<NP>(wbk + r * N, wv);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < NP; ++e) wv[e] = wbk[r * N + e];
+                }
+#pragma unroll
+                for (int i = 0; i < TO; ++i)
+#pragma unroll
+                    for (int e = 0; e < NP; ++e) acc[i][e] = __fmaf_rn(xf[i][r], wv[e], acc[i][e]);
+            }
         }
     }
-    if constexpr (BULK) {
-        // every copy issued lands before shared memory is reused or the CTA exits
-        if (tid == 0)
-            for (int c = max(0, issued - STAGES); c < min(issued, nchunks); ++c) {
-                const uint64_t ts = tc::globaltimer_ns();
-                while (!tc::mbar_try_wait(&full[c % STAGES], (uint32_t)((c / STAGES) & 1)))
-                    if (tc::globaltimer_ns() - ts > 1000000000ull) break;
-            }
-    } else {
-        cp_async_wait<0>();
-    }
+    // every copy issued has landed before shared memory is reused or the CTA exits
+    if (tid == 0)
+        for (int c = max(0, issued - STAGES); c < issued; ++c) {
+            const uint64_t ts = tc::globaltimer_ns();
+            while (!tc::mbar_try_wait(&full[c % STAGES], (uint32_t)((c / STAGES) & 1)))
+                if (tc::globaltimer_ns() - ts > kWaitNs) break;
+        }
     __syncthreads();
     if (!ok) return;
-    router_tail_small<LE, EPT, TPT>(acc, smem, b_r, a, TT, tok_base, le);
+
+    float *Ls = smem;                                    // [TT][N]
+    int *Is = reinterpret_cast<int *>(smem + TT * N);    // [TT][8]
+#pragma unroll
+    for (int i = 0; i < TO; ++i)
+#pragma unroll
+        for (int e = 0; e < NP; ++e) {
+            const float v = butterfly32(acc[i][e]);
+            if (lane == 0 && e < N) Ls[(warp * TO + i) * N + e] = a.has_bias ? __fadd_rn(v, b_r[e]) : v;
+        }
+    __syncthreads();
+    gate_tokens_thread<NP>(Ls, Is, a, TT);
+    __syncthreads();
+    tile_stats(Ls, Is, a, TT);
+}
+
+// ------------------------------------------------------------------ N > 32
+
+__global__ void __launch_bounds__(256) k_transpose_wr(const float *__restrict__ w_r, float *__restrict__ w_t,
+                                                      int d, int N) {
+    __shared__ float tile[32][33];
+    const int i0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    for (int r = ty; r < 32; r += 8)
+        if (i0 + r < d && e0 + tx < N) tile[r][tx] = w_r[(size_t)(i0 + r) * N + e0 + tx];
+    __syncthreads();
+    for (int r = ty; r < 32; r += 8)
+        if (e0 + r < N && i0 + tx < d) w_t[(size_t)(e0 + r) * d + i0 + tx] = tile[tx][r];
+}
+
+struct LogitsArgs {
+    int T, d, N, has_bias;
+    float *logits;  // [T][N]
+    uint32_t *err;
+};
+
+// One CTA = 16 warps = 4 token groups x 4 expert groups; warp tile 4 tokens x 8
+// experts, lane l = partial l. Tile 16 tokens x 32 experts; chunks of 256 features:
+// token rows and transposed weight rows ([expert][feature], so a lane's 8 features
+// of one expert are one 32-byte run) by bulk copies into a 4-slot ring.
+template <typename XT>
+__global__ void __launch_bounds__(512, 1) k_logits_large(const XT *__restrict__ x, const float *__restrict__ w_t,
+                                                        const float *__restrict__ b_r, LogitsArgs a) {
+    constexpr int TOK = 16, EXP = 32, TO = 4, EO = 8;
+    constexpr int KC = 256, NBLK = KC / 8, STAGES = 4;
+    constexpr int ES = (int)sizeof(XT);
+    constexpr int XROW = KC * ES + 16;
+    constexpr int WROW = KC * 4 + 16;
+    constexpr int X_BYTES = TOK * XROW;
+    constexpr int STAGE = X_BYTES + EXP * WROW;
+    extern __shared__ __align__(16) float smem[];
+    __shared__ uint64_t full[STAGES];
+    __shared__ int abort_flag;
+    uint8_t *sb = reinterpret_cast<uint8_t *>(smem);
+
+    const int T = a.T, d = a.d, N = a.N;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tg = warp >> 2, eg = warp & 3;
+    const int t0 = blockIdx.x * TOK, e0 = blockIdx.y * EXP;
+    const int ntok = min(TOK, T - t0), nexp = min(EXP, N - e0);
+    const int nblocks = d / 8;
+    const int nchunks = (nblocks + NBLK - 1) / NBLK;
+
+    if (tid == 0) {
+        abort_flag = 0;
+        for (int i = 0; i < STAGES; ++i) tc::mbar_init(&full[i], 1);
+        tc::fence_mbar_init();
+    }
+    __syncthreads();
+
+    auto issue = [&](int c) {
+        if (warp != 0 || c >= nchunks) return;
+        const int b0 = c * NBLK, nb = min(NBLK, nblocks - b0);
+        uint8_t *slot = sb + (size_t)(c % STAGES) * STAGE;
+        uint64_t *bar = &full[c % STAGES];
+        const uint32_t xb = (uint32_t)(nb * 8 * ES), wb = (uint32_t)(nb * 8 * 4);
+        if (lane == 0) tc::mbar_arrive_expect_tx(bar, (uint32_t)ntok * xb + (uint32_t)nexp * wb);
+        __syncwarp();
+        if (lane < ntok)
+            tc::bulk_copy_g2s(slot + lane * XROW, x + (size_t)(t0 + lane) * d + (size_t)b0 * 8, xb, bar);
+        if (lane < nexp)
+            tc::bulk_copy_g2s(slot + X_BYTES + lane * WROW, w_t + (size_t)(e0 + lane) * d + (size_t)b0 * 8, wb, bar);
+    };
+
+    float acc[TO][EO];
+#pragma unroll
+    for (int i = 0; i < TO; ++i)
+#pragma unroll
+        for (int j = 0; j < EO; ++j) acc[i][j] = 0.0f;
+
+#pragma unroll
+    for (int c = 0; c < STAGES - 1; ++c) issue(c);
+    bool ok = true;
+    int issued = min(STAGES - 1, nchunks);
+    for (int c = 0; c < nchunks; ++c) {
+        const bool mine = wait_phase(&full[c % STAGES], (uint32_t)((c / STAGES) & 1), &abort_flag, a.err);
+        __syncthreads();
+        if (!mine || *(volatile int *)&abort_flag) {
+            ok = false;
+            break;
+        }
+        issue(c + STAGES - 1);
+        if (c + STAGES - 1 < nchunks) ++issued;
+        const uint8_t *slot = sb + (size_t)(c % STAGES) * STAGE;
+        if (c * NBLK + lane < nblocks) {
+            float xf[TO][8];
+#pragma unroll
+            for (int i = 0; i < TO; ++i) load8<XT>(slot + (tg * TO + i) * XROW + lane * 8 * ES, xf[i]);
+            const float *wl = reinterpret_cast<const float *>(slot + X_BYTES) + lane * 8;
+#pragma unroll
+            for (int jp = 0; jp < EO; jp += 2) {
+                float w0[8], w1[8];
+                lds<8>(wl + (eg * EO + jp) * (WROW / 4), w0);
+                lds<8>(wl + (eg * EO + jp + 1) * (WROW / 4), w1);
+#pragma unroll
+                for (int r = 0; r < 8; ++r)
+#pragma unroll
+                    for (int i = 0; i < TO; ++i) {
+                        acc[i][jp] = __fmaf_rn(xf[i][r], w0[r], acc[i][jp]);
+                        acc[i][jp + 1] = __fmaf_rn(xf[i][r], w1[r], acc[i][jp + 1]);
+                    }
+            }
+        }
+    }
+    if (tid == 0)
+        for (int c = max(0, issued - STAGES); c < issued; ++c) {
+            const uint64_t ts = tc::globaltimer_ns();
+            while (!tc::mbar_try_wait(&full[c % STAGES], (uint32_t)((c / STAGES) & 1)))
+                if (tc::globaltimer_ns() - ts > kWaitNs) break;
+        }
+    __syncthreads();
+    if (!ok) return;
+#pragma unroll
+    for (int i = 0; i < TO; ++i)
+#pragma unroll
+        for (int j = 0; j < EO; ++j) {
+            const float v = butterfly32(acc[i][j]);
+            const int t = t0 + tg * TO + i, e = e0 + eg * EO + j;
+            if (lane == 0 && t < T && e < N) a.logits[(size_t)t * N + e] = a.has_bias ? __fadd_rn(v, b_r[e]) : v;
+        }
+}
+
+// One CTA = 8 warps, 64 tokens: logits tile -> shared memory -> gating -> stats.
+__global__ void __launch_bounds__(256) k_gate(const float *__restrict__ logits, RouterArgs a) {
+    constexpr int TT = 64;
+    extern __shared__ __align__(16) float smem[];
+    float *Ls = smem;                                    // [TT][N]
+    int *Is = reinterpret_cast<int *>(smem + TT * a.N);  // [TT][8]
+    const int t0 = blockIdx.x * TT;
+    const int nrows = min(TT, a.T - t0);
+    for (int i = threadIdx.x; i < nrows * a.N; i += blockDim.x) Ls[i] = logits[(size_t)t0 * a.N + i];
+    __syncthreads();
+    gate_tokens_warp(Ls, Is, a, TT);
+    __syncthreads();
+    tile_stats(Ls, Is, a, TT);
 }
 
 // Block-wide exclusive scan of one int per thread; returns the exclusive prefix
@@ -860,57 +739,47 @@ __global__ void __launch_bounds__(256) k_assign(AssignArgs a) {
     }
 }
 
-template <typename XT, int LE, int EPT, int TPT, int KC, bool A4>
-cudaError_t launch_router_t(const moe_config &c, const XT *x, const float *w_r, const float *b_r,
-                            RouterArgs ra, int warps, cudaStream_t s) {
-    constexpr int NP = LE * EPT;
-    const int TT = warps * 8;
-    const size_t loop = RouterSmem<XT, KC>::loop_bytes(c.N, TT, NP);
+template <typename XT, int NP>
+cudaError_t launch_small(const moe_config &c, const XT *x, const float *w_r, const float *b_r, RouterArgs ra,
+                         cudaStream_t s) {
+    constexpr int TT = 4 * (32 / NP);
+    const size_t stage = (size_t)32 * wblock_stride(c.N, NP) * 4 + (size_t)TT * (256 * sizeof(XT) + 16);
     const size_t gate = ((size_t)TT * c.N + (size_t)TT * 8) * sizeof(float);
-    const size_t bytes = std::max(loop, gate);
-    auto kern = k_router<XT, LE, EPT, TPT, KC, A4>;
+    const size_t bytes = std::max(6 * stage, gate);
+    auto kern = c.N % 4 == 0 ? k_router_small<XT, NP, true> : k_router_small<XT, NP, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
     if (e != cudaSuccess) return e;
-    kern<<<ra.tiles, warps * 32, bytes, s>>>(x, w_r, b_r, ra);
-    return cudaGetLastError();
-}
-
-// Many experts: chunks of 32 features so that four stages of [KC][N] weights fit.
-template <typename XT, int LE, int EPT, int TPT>
-cudaError_t launch_router_a(const moe_config &c, const XT *x, const float *w_r, const float *b_r,
-                            RouterArgs ra, int warps, cudaStream_t s) {
-    constexpr int KC = 32;
-    if (c.N % 4 == 0) return launch_router_t<XT, LE, EPT, TPT, KC, true>(c, x, w_r, b_r, ra, warps, s);
-    return launch_router_t<XT, LE, EPT, TPT, KC, false>(c, x, w_r, b_r, ra, warps, s);
-}
-
-// Few experts: 2 warps (16 tokens) per CTA, chunks of 256 features; bulk copies
-// when the weight chunk is one contiguous block of whole 16-byte pieces.
-template <typename XT, int LE, int EPT>
-cudaError_t launch_router_small(const moe_config &c, const XT *x, const float *w_r, const float *b_r,
-                                RouterArgs ra, cudaStream_t s) {
-    constexpr int NW = 2, KC = 256, TT = NW * 8;
-    constexpr size_t stage = (size_t)KC * LE * EPT * 4 + (size_t)TT * (KC * sizeof(XT) + 16);
-    const size_t gate = ((size_t)TT * c.N + (size_t)TT * 8) * sizeof(float);
-    const size_t bytes = std::max(4 * stage, gate);
-    const bool bulk = c.N == LE * EPT && c.N % 4 == 0;
-    auto kern = bulk ? k_router_small<XT, LE, EPT, NW, KC, true> : k_router_small<XT, LE, EPT, NW, KC, false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-    if (e != cudaSuccess) return e;
-    kern<<<ra.tiles, NW * 32, bytes, s>>>(x, w_r, b_r, ra);
+    kern<<<ra.tiles, 128, bytes, s>>>(x, w_r, b_r, ra);
     return cudaGetLastError();
 }
 
 template <typename XT>
-cudaError_t launch_router_x(const moe_config &c, const XT *x, const float *w_r, const float *b_r,
-                            RouterArgs ra, int warps, cudaStream_t s) {
-    if (c.N <= 4) return launch_router_small<XT, 4, 1>(c, x, w_r, b_r, ra, s);
-    if (c.N <= 8) return launch_router_small<XT, 4, 2>(c, x, w_r, b_r, ra, s);
-    if (c.N <= 16) return launch_router_small<XT, 8, 2>(c, x, w_r, b_r, ra, s);
-    if (c.N <= 32) return launch_router_small<XT, 16, 2>(c, x, w_r, b_r, ra, s);
-    if (c.N <= 64) return launch_router_a<XT, 32, 2, 8>(c, x, w_r, b_r, ra, warps, s);
-    if (c.N <= 128) return launch_router_a<XT, 32, 4, 8>(c, x, w_r, b_r, ra, warps, s);
-    return launch_router_a<XT, 32, 8, 8>(c, x, w_r, b_r, ra, warps, s);
+cudaError_t launch_large(const moe_config &c, const XT *x, const float *w_r, const float *b_r, RouterArgs ra,
+                         float *logits, float *w_t, cudaStream_t s) {
+    k_transpose_wr<<<dim3((c.d + 31) / 32, (c.N + 31) / 32), 256, 0, s>>>(w_r, w_t, c.d, c.N);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    LogitsArgs la{c.T, c.d, c.N, ra.has_bias, logits, ra.err};
+    const size_t lbytes = 4 * (size_t)(16 * (256 * sizeof(XT) + 16) + 32 * (256 * 4 + 16));
+    e = cudaFuncSetAttribute(k_logits_large<XT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lbytes);
+    if (e != cudaSuccess) return e;
+    k_logits_large<XT><<<dim3((c.T + 15) / 16, (c.N + 31) / 32), 512, lbytes, s>>>(x, w_t, b_r, la);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const size_t gbytes = ((size_t)64 * c.N + 64 * 8) * sizeof(float);
+    e = cudaFuncSetAttribute(k_gate, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gbytes);
+    if (e != cudaSuccess) return e;
+    k_gate<<<ra.tiles, 256, gbytes, s>>>(logits, ra);
+    return cudaGetLastError();
+}
+
+template <typename XT>
+cudaError_t launch_logits_gate(const moe_config &c, const XT *x, const float *w_r, const float *b_r, RouterArgs ra,
+                               float *logits, float *w_t, cudaStream_t s) {
+    if (c.N <= 4) return launch_small<XT, 4>(c, x, w_r, b_r, ra, s);
+    if (c.N <= 8) return launch_small<XT, 8>(c, x, w_r, b_r, ra, s);
+    if (c.N <= 16) return launch_small<XT, 16>(c, x, w_r, b_r, ra, s);
+    if (c.N <= 32) return launch_small<XT, 32>(c, x, w_r, b_r, ra, s);
+    return launch_large<XT>(c, x, w_r, b_r, ra, logits, w_t, s);
 }
 
 }  // namespace
@@ -918,7 +787,6 @@ cudaError_t launch_router_x(const moe_config &c, const XT *x, const float *w_r, 
 cudaError_t launch_router(const moe_config &c, const void *x, const float *w_r, const float *b_r,
                           const RouterOut &o, uint8_t *ws, cudaStream_t s) {
     const WsLayout L = ws_layout(c);
-    const int warps = router_warps(c);
     const int tiles = router_tiles(c);
     uint32_t *err = reinterpret_cast<uint32_t *>(ws + L.err);
     int32_t *cnt = reinterpret_cast<int32_t *>(ws + L.cnt);
@@ -926,6 +794,8 @@ cudaError_t launch_router(const moe_config &c, const void *x, const float *w_r, 
     int32_t *kpre = reinterpret_cast<int32_t *>(ws + L.kpre);
     float *psum = reinterpret_cast<float *>(ws + L.psum);
     float *pmean = reinterpret_cast<float *>(ws + L.pmean);
+    float *logits = reinterpret_cast<float *>(ws + L.logits);
+    float *w_t = reinterpret_cast<float *>(ws + L.w_t);
     int32_t *routed = o.counts_routed ? o.counts_routed : reinterpret_cast<int32_t *>(ws + L.routed);
     int32_t *kept = o.counts_kept ? o.counts_kept : reinterpret_cast<int32_t *>(ws + L.kept);
 
@@ -933,9 +803,9 @@ cudaError_t launch_router(const moe_config &c, const void *x, const float *w_r, 
                   o.topk_idx, o.topk_gate, cnt, psum, err};
     cudaError_t e;
     if (c.dtype == MOE_BF16)
-        e = launch_router_x<__nv_bfloat16>(c, static_cast<const __nv_bfloat16 *>(x), w_r, b_r, ra, warps, s);
+        e = launch_logits_gate<__nv_bfloat16>(c, static_cast<const __nv_bfloat16 *>(x), w_r, b_r, ra, logits, w_t, s);
     else
-        e = launch_router_x<float>(c, static_cast<const float *>(x), w_r, b_r, ra, warps, s);
+        e = launch_logits_gate<float>(c, static_cast<const float *>(x), w_r, b_r, ra, logits, w_t, s);
     if (e != cudaSuccess) return e;
 
     const int cap = capacity_of(c);

@@ -63,22 +63,44 @@ def _fma_f32(a, b, c):
     return _round_f32(Fraction(float(a)) * Fraction(float(b)) + Fraction(float(c)))
 
 
+def _logit_exact(xrow, wcol, b=None):
+    """The specified fp32 order, evaluated with exact rationals and IEEE
+    round-to-nearest-even at every step: 32 partials over 8-feature blocks
+    (block b -> partial b mod 32, features in increasing order, one fma each),
+    five pairwise rounds p_l <- p_l + p_(l^o) for o = 16, 8, 4, 2, 1, take p_0,
+    then add the bias."""
+    part = [0.0] * 32
+    for i in range(len(xrow)):
+        lane = (i // 8) % 32
+        part[lane] = _fma_f32(xrow[i], wcol[i], part[lane])
+    for o in (16, 8, 4, 2, 1):
+        part = [_round_f32(Fraction(part[lane]) + Fraction(part[lane ^ o])) for lane in range(32)]
+    acc = part[0]
+    if b is not None:
+        acc = _round_f32(Fraction(acc) + Fraction(float(b)))
+    return np.float32(acc)
+
+
 def pin_router_logits_exact(O):
-    """Each logit equals the fp32 chain acc = fma(x_i, w_i, acc), i increasing,
-    evaluated here with exact rationals and IEEE round-to-nearest-even."""
+    """Each logit equals the specified fp32 summation, re-evaluated exactly: 8-feature
+    blocks dealt round-robin to 32 fma partials, a five-round pairwise combine, bias."""
     rng = np.random.default_rng(7)
-    T, d, N = 3, 24, 5
+    T, d, N = 2, 8 * 32 * 2 + 24, 3          # two full passes over the 32 partials + a tail
     x = rng.standard_normal((T, d)).astype(np.float32) * np.float32(3.0)
     w = rng.standard_normal((d, N)).astype(np.float32)
     b = rng.standard_normal(N).astype(np.float32)
     L = O.router_logits(x, w, b)
     for t in range(T):
         for e in range(N):
-            acc = 0.0
-            for i in range(d):
-                acc = _fma_f32(x[t, i], w[i, e], acc)
-            acc = _round_f32(Fraction(acc) + Fraction(float(b[e])))
-            assert L[t, e] == np.float32(acc), (t, e, L[t, e], acc)
+            want = _logit_exact(x[t], w[:, e], b[e])
+            assert L[t, e] == want, (t, e, L[t, e], want)
+    # short inputs leave most partials at zero
+    x2 = rng.standard_normal((3, 24)).astype(np.float32)
+    w2 = rng.standard_normal((24, 4)).astype(np.float32)
+    L2 = O.router_logits(x2, w2)
+    for t in range(3):
+        for e in range(4):
+            assert L2[t, e] == _logit_exact(x2[t], w2[:, e])
 
 
 def pin_router_logits_error_bound(O):
@@ -430,6 +452,43 @@ def _mut_reverse_order(mp):
         np.ascontiguousarray(np.asarray(w, np.float32)[::-1]), b))
 
 
+def _mut_sequential_order(mp):
+    def logits(x, w, b=None):
+        x = np.asarray(x, np.float32)
+        w = np.asarray(w, np.float32)
+        out = np.zeros((x.shape[0], w.shape[1]), np.float32)
+        for t in range(x.shape[0]):
+            for e in range(w.shape[1]):
+                acc = 0.0
+                for i in range(x.shape[1]):
+                    acc = _fma_f32(x[t, i], w[i, e], acc)
+                if b is not None:
+                    acc = _round_f32(Fraction(acc) + Fraction(float(b[e])))
+                out[t, e] = acc
+        return out
+    mp.setattr(O, "router_logits", logits)
+
+
+def _mut_butterfly_ascending(mp):
+    def logits(x, w, b=None):
+        x = np.asarray(x, np.float32)
+        w = np.asarray(w, np.float32)
+        out = np.zeros((x.shape[0], w.shape[1]), np.float32)
+        for t in range(x.shape[0]):
+            for e in range(w.shape[1]):
+                part = [0.0] * 32
+                for i in range(x.shape[1]):
+                    part[(i // 8) % 32] = _fma_f32(x[t, i], w[i, e], part[(i // 8) % 32])
+                for o in (1, 2, 4, 8, 16):
+                    part = [_round_f32(Fraction(part[q]) + Fraction(part[q ^ o])) for q in range(32)]
+                acc = part[0]
+                if b is not None:
+                    acc = _round_f32(Fraction(acc) + Fraction(float(b[e])))
+                out[t, e] = acc
+        return out
+    mp.setattr(O, "router_logits", logits)
+
+
 def _mut_capacity_floor(mp):
     mp.setattr(O, "capacity", lambda T, N, cf: None if cf is None else (T * cf[0]) // (N * cf[1]))
 
@@ -451,6 +510,8 @@ MUTATIONS = [
     (_mut_dropped_term, pin_router_logits_error_bound),
     (_mut_mul_then_add, pin_router_logits_exact),
     (_mut_reverse_order, pin_router_logits_exact),
+    (_mut_sequential_order, pin_router_logits_exact),
+    (_mut_butterfly_ascending, pin_router_logits_exact),
     (_mut_capacity_floor, pin_capacity),
     (_mut_renormalise_softmax_gates, pin_softmax_library),
 ]
