@@ -3,6 +3,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime_api.h>
 #include "../../include/moe.h"
 
@@ -34,7 +35,7 @@ struct WsLayout {
     size_t pmean;                // f32   [N]
     size_t routed, kept;         // int32 [N] (used when the caller passes NULL)
     size_t logits;               // f32   [T][N]  (N > 32 only)
-    size_t w_t;                  // f32   [N][d]  router weight transposed (N > 32 only)
+    size_t w_t;                  // f32   [ceil(d/256)][N][256]  router weight, re-laid out
     size_t offsets;              // int32 [N+1]
     size_t topk_idx, topk_gate;  // [T][k]
     size_t slot_row;             // int32 [T][k]
@@ -90,5 +91,10 @@ cudaError_t launch_ffn_simt(const moe_config &c, const FfnGroup &g, uint32_t *er
 cudaError_t launch_ffn_tc(const moe_config &c, const FfnGroup &g, uint32_t *err, cudaStream_t s);
 
 int device_sm_count();
+
+// TMA tensor map of a `rank`-dimensional array (dims innermost first, strides in
+// bytes for dims 1..rank-1, box in elements). false if the driver refuses it.
+bool encode_tmap(CUtensorMap *m, CUtensorMapDataType dt, int rank, const void *base, const uint64_t *dims,
+                 const uint64_t *strides_bytes, const uint32_t *box, CUtensorMapSwizzle swizzle);
 
 }  // namespace moe

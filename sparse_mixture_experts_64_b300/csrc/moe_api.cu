@@ -48,7 +48,7 @@ WsLayout ws_layout(const moe_config &c) {
     L.routed = take(N * 4);
     L.kept = take(N * 4);
     L.logits = take(c.N > 32 ? T * N * 4 : 0);
-    L.w_t = take(c.N > 32 ? N * (size_t)c.d * 4 : 0);
+    L.w_t = take((size_t)((c.d + 255) / 256) * 256 * N * 4);
     // expert / shared-expert buffers
     L.hid = take(rmax * c.h * es);
     L.hid_sh = take(c.h_shared ? T * c.h_shared * es : 0);

@@ -101,16 +101,6 @@ __device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t par, int *abo
     return true;
 }
 
-// Stride (in floats) of one staged block of 8 router-weight rows [8][N] in the
-// small kernel: room for reads up to column NP-1 and == 4 (mod 32) words, so the
-// 32 lanes reading 32 different blocks spread over the banks.
-__host__ __device__ inline int wblock_stride(int N, int NP) {
-    int s = 8 * N + (NP > N ? NP - N : 0);
-    s = (s + 3) & ~3;
-    s += ((4 - (s & 31)) + 32) & 31;
-    return s;
-}
-
 // ------------------------------------------------------------------ gating
 
 // Per-tile statistics from p (Ls) and the selections (Is): per expert, the sum of
@@ -275,123 +265,64 @@ __device__ __forceinline__ void gate_tokens_warp(float *Ls, int *Is, const Route
     }
 }
 
-// ------------------------------------------------------------------ N <= 32
+// ------------------------------------------------------------------ pipeline
 
-// One CTA = 4 warps; warp w owns TO = 32/NP tokens and all NP experts; lane l
-// owns partial l. Chunks of 256 features (one 8-feature block per lane) are
-// staged by bulk copies issued from warp 0 (lane j copies weight block j and
-// token row j) into a 6-slot ring, each slot completing on its own mbarrier.
-template <typename XT, int NP, bool VEC>
-__global__ void __launch_bounds__(128) k_router_small(const XT *__restrict__ x, const float *__restrict__ w_r,
-                                                     const float *__restrict__ b_r, RouterArgs a) {
-    constexpr int NW = 4, TO = 32 / NP, TT = NW * TO;
-    constexpr int KC = 256, NBLK = KC / 8;
-    constexpr int STAGES = 6;
-    constexpr int ES = (int)sizeof(XT);
-    constexpr int XROW = KC * ES + 16;
-    static_assert(TT <= 32, "one token row per lane of warp 0");
-    extern __shared__ __align__(16) float smem[];
-    __shared__ uint64_t full[STAGES];
-    __shared__ int abort_flag;
-    uint8_t *sb = reinterpret_cast<uint8_t *>(smem);
+// Ring of STAGES staging slots between one producer warp (bulk copies) and NC
+// consumer warps. full[s]: the copies of the chunk in slot s have landed (one
+// arrival + transaction bytes); empty[s]: all NC consumer warps are done with it.
+template <int STAGES>
+struct Ring {
+    uint64_t full[STAGES], empty[STAGES];
+    int abort_flag;
 
-    const int N = a.N, d = a.d, T = a.T;
-    const int BST = wblock_stride(N, NP);
-    const int W_BYTES = NBLK * BST * 4;
-    const int STAGE = W_BYTES + TT * XROW;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int t0 = blockIdx.x * TT;
-    const int ntok = min(TT, T - t0);
-    const int nblocks = d / 8;
-    const int nchunks = (nblocks + NBLK - 1) / NBLK;
-
-    if (tid == 0) {
+    __device__ void init(int nc) {
         abort_flag = 0;
-        for (int i = 0; i < STAGES; ++i) tc::mbar_init(&full[i], 1);
+        for (int i = 0; i < STAGES; ++i) {
+            tc::mbar_init(&full[i], 1);
+            tc::mbar_init(&empty[i], (uint32_t)nc);
+        }
         tc::fence_mbar_init();
     }
-    __syncthreads();
-
-    auto issue = [&](int c) {
-        if (warp != 0 || c >= nchunks) return;
-        const int b0 = c * NBLK, nb = min(NBLK, nblocks - b0);
-        uint8_t *slot = sb + (size_t)(c % STAGES) * STAGE;
-        uint64_t *bar = &full[c % STAGES];
-        const uint32_t wb = (uint32_t)(8 * N * 4), xb = (uint32_t)(nb * 8 * ES);
-        if (lane == 0) tc::mbar_arrive_expect_tx(bar, (uint32_t)nb * wb + (uint32_t)ntok * xb);
-        __syncwarp();
-        if (lane < nb) tc::bulk_copy_g2s(slot + lane * BST * 4, w_r + (size_t)(b0 + lane) * 8 * N, wb, bar);
-        if (lane < ntok)
-            tc::bulk_copy_g2s(slot + W_BYTES + lane * XROW, x + (size_t)(t0 + lane) * d + (size_t)b0 * 8, xb, bar);
-    };
-
-    float acc[TO][NP];
-#pragma unroll
-    for (int i = 0; i < TO; ++i)
-#pragma unroll
-        for (int e = 0; e < NP; ++e) acc[i][e] = 0.0f;
-
-#pragma unroll
-    for (int c = 0; c < STAGES - 1; ++c) issue(c);
-    bool ok = true;
-    int issued = min(STAGES - 1, nchunks);
-    for (int c = 0; c < nchunks; ++c) {
-        const bool mine = wait_phase(&full[c % STAGES], (uint32_t)((c / STAGES) & 1), &abort_flag, a.err);
-        __syncthreads();
-        if (!mine || *(volatile int *)&abort_flag) {
-            ok = false;
-            break;
-        }
-        issue(c + STAGES - 1);
-        if (c + STAGES - 1 < nchunks) ++issued;
-        const uint8_t *slot = sb + (size_t)(c % STAGES) * STAGE;
-        if (c * NBLK + lane < nblocks) {
-            const float *wbk = reinterpret_cast<const float *>(slot) + lane * BST;
-            float xf[TO][8];
-#pragma unroll
-            for (int i = 0; i < TO; ++i) load8<XT>(slot + W_BYTES + (warp * TO + i) * XROW + lane * 8 * ES, xf[i]);
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                float wv[NP];
-                if constexpr (VEC) {
-                    lds<NP>(wbk + r * N, wv);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < NP; ++e) wv[e] = wbk[r * N + e];
-                }
-#pragma unroll
-                for (int i = 0; i < TO; ++i)
-#pragma unroll
-                    for (int e = 0; e < NP; ++e) acc[i][e] = __fmaf_rn(xf[i][r], wv[e], acc[i][e]);
-            }
-        }
+    __device__ bool aborted() { return *(volatile int *)&abort_flag != 0; }
+    // producer: wait until slot c % STAGES may be refilled with chunk c
+    __device__ bool acquire(int c, uint32_t *err) {
+        if (c < STAGES) return !aborted();
+        return wait_phase(&empty[c % STAGES], (uint32_t)((c / STAGES - 1) & 1), &abort_flag, err);
     }
-    // every copy issued has landed before shared memory is reused or the CTA exits
-    if (tid == 0)
+    // consumer: wait until chunk c has landed
+    __device__ bool ready(int c, uint32_t *err) {
+        return wait_phase(&full[c % STAGES], (uint32_t)((c / STAGES) & 1), &abort_flag, err);
+    }
+    // consumer warp: done reading chunk c
+    __device__ void release(int c) {
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) tc::mbar_arrive(&empty[c % STAGES]);
+    }
+    // producer lane 0: every chunk issued lands before the CTA moves on
+    __device__ void drain(int issued) {
         for (int c = max(0, issued - STAGES); c < issued; ++c) {
             const uint64_t ts = tc::globaltimer_ns();
             while (!tc::mbar_try_wait(&full[c % STAGES], (uint32_t)((c / STAGES) & 1)))
                 if (tc::globaltimer_ns() - ts > kWaitNs) break;
         }
-    __syncthreads();
-    if (!ok) return;
+    }
+};
 
-    float *Ls = smem;                                    // [TT][N]
-    int *Is = reinterpret_cast<int *>(smem + TT * N);    // [TT][8]
-#pragma unroll
-    for (int i = 0; i < TO; ++i)
-#pragma unroll
-        for (int e = 0; e < NP; ++e) {
-            const float v = butterfly32(acc[i][e]);
-            if (lane == 0 && e < N) Ls[(warp * TO + i) * N + e] = a.has_bias ? __fadd_rn(v, b_r[e]) : v;
-        }
-    __syncthreads();
-    gate_tokens_thread<NP>(Ls, Is, a, TT);
-    __syncthreads();
-    tile_stats(Ls, Is, a, TT);
+// ------------------------------------------------------------------ weight layout
+
+// The router weight is re-laid out once per call (k_transpose_wr) as
+// [chunk of 256 features][expert][256 positions]: one chunk of every expert is
+// one contiguous run (a single bulk copy), and inside an expert's 256 positions
+// features 0-3 of every 8-feature block come first (block after block), then
+// features 4-7, so lane l's two 16-byte halves of block l sit at 16*l and
+// 16*(nb + l) bytes (nb = blocks in the chunk): every half-load of a warp reads
+// one contiguous 512-byte run.
+__device__ __forceinline__ size_t wt_index(int i, int e, int d, int N) {
+    const int c = i >> 8, p = i & 255;
+    const int nb = min(32, (d - (c << 8)) >> 3);
+    const int l = p >> 3, r = p & 7;
+    return ((size_t)c * N + e) * 256 + (r >> 2) * (nb * 4) + l * 4 + (r & 3);
 }
-
-// ------------------------------------------------------------------ N > 32
 
 __global__ void __launch_bounds__(256) k_transpose_wr(const float *__restrict__ w_r, float *__restrict__ w_t,
                                                       int d, int N) {
@@ -402,8 +333,111 @@ __global__ void __launch_bounds__(256) k_transpose_wr(const float *__restrict__ 
         if (i0 + r < d && e0 + tx < N) tile[r][tx] = w_r[(size_t)(i0 + r) * N + e0 + tx];
     __syncthreads();
     for (int r = ty; r < 32; r += 8)
-        if (e0 + r < N && i0 + tx < d) w_t[(size_t)(e0 + r) * d + i0 + tx] = tile[tx][r];
+        if (e0 + r < N && i0 + tx < d) w_t[wt_index(i0 + tx, e0 + r, d, N)] = tile[tx][r];
 }
+
+// 8 weights of expert row `row` (256 floats of one chunk) for lane's block.
+__device__ __forceinline__ void load_w8(const float *row, int lane, int nb, float *w) {
+    lds<4>(row + lane * 4, w);
+    lds<4>(row + nb * 4 + lane * 4, w + 4);
+}
+
+// ------------------------------------------------------------------ N <= 32
+
+// One CTA = 4 consumer warps + 1 producer warp. Consumer warp w owns TO = 32/NP
+// tokens and all NP experts; lane l owns partial l. Per chunk of 256 features the
+// producer issues one 2D TMA copy of the token tile ([TT][256]) and one bulk copy
+// of the weight chunk ([N][256]) into a 6-slot ring.
+template <typename XT, int NP>
+__global__ void __launch_bounds__(160) k_router_small(const __grid_constant__ CUtensorMap tmx,
+                                                     const float *__restrict__ w_t, const float *__restrict__ b_r,
+                                                     RouterArgs a) {
+    constexpr int NW = 4, TO = 32 / NP, TT = NW * TO;
+    constexpr int KC = 256, NBLK = KC / 8;
+    constexpr int STAGES = 6;
+    constexpr int ES = (int)sizeof(XT);
+    constexpr int X_BYTES = TT * KC * ES;
+    constexpr int STAGE = (X_BYTES + NP * KC * 4 + 1023) & ~1023;
+    extern __shared__ __align__(1024) uint8_t router_smem[];
+    __shared__ Ring<STAGES> ring;
+    uint8_t *sb = router_smem + ((1024 - (tc::smem_u32(router_smem) & 1023)) & 1023);
+
+    const int N = a.N, d = a.d;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int t0 = blockIdx.x * TT;
+    const int nblocks = d / 8;
+    const int nchunks = (nblocks + NBLK - 1) / NBLK;
+
+    if (tid == 0) ring.init(NW);
+    __syncthreads();
+
+    float acc[TO][NP];
+#pragma unroll
+    for (int i = 0; i < TO; ++i)
+#pragma unroll
+        for (int e = 0; e < NP; ++e) acc[i][e] = 0.0f;
+
+    if (warp == NW) {
+        // ---- producer (lane 0)
+        if (lane == 0) {
+            int issued = 0;
+            for (int c = 0; c < nchunks; ++c) {
+                if (!ring.acquire(c, a.err)) break;
+                uint8_t *slot = sb + (size_t)(c % STAGES) * STAGE;
+                uint64_t *bar = &ring.full[c % STAGES];
+                const uint32_t wbytes = (uint32_t)(N * KC * 4);
+                tc::mbar_arrive_expect_tx(bar, (uint32_t)X_BYTES + wbytes);
+                tc::tma_load_2d(slot, &tmx, c * KC, t0, bar);
+                tc::bulk_copy_g2s(slot + X_BYTES, w_t + (size_t)c * N * KC, wbytes, bar);
+                issued = c + 1;
+            }
+            ring.drain(issued);
+        }
+    } else {
+        // ---- consumers
+        for (int c = 0; c < nchunks; ++c) {
+            if (!ring.ready(c, a.err)) break;
+            const uint8_t *slot = sb + (size_t)(c % STAGES) * STAGE;
+            const int nb = min(NBLK, nblocks - c * NBLK);
+            if (lane < nb) {
+                const float *wl = reinterpret_cast<const float *>(slot + X_BYTES);
+                float xf[TO][8];
+#pragma unroll
+                for (int i = 0; i < TO; ++i) load8<XT>(slot + ((warp * TO + i) * KC + lane * 8) * ES, xf[i]);
+#pragma unroll
+                for (int e = 0; e < NP; ++e) {
+                    float w[8];
+                    load_w8(wl + e * KC, lane, nb, w);
+#pragma unroll
+                    for (int r = 0; r < 8; ++r)
+#pragma unroll
+                        for (int i = 0; i < TO; ++i) acc[i][e] = __fmaf_rn(xf[i][r], w[r], acc[i][e]);
+                }
+            }
+            ring.release(c);
+        }
+    }
+    __syncthreads();
+    if (ring.aborted()) return;
+
+    float *Ls = reinterpret_cast<float *>(sb);            // [TT][N]
+    int *Is = reinterpret_cast<int *>(Ls + TT * N);       // [TT][8]
+    if (warp < NW) {
+#pragma unroll
+        for (int i = 0; i < TO; ++i)
+#pragma unroll
+            for (int e = 0; e < NP; ++e) {
+                const float v = butterfly32(acc[i][e]);
+                if (lane == 0 && e < N) Ls[(warp * TO + i) * N + e] = a.has_bias ? __fadd_rn(v, b_r[e]) : v;
+            }
+    }
+    __syncthreads();
+    gate_tokens_thread<NP>(Ls, Is, a, TT);
+    __syncthreads();
+    tile_stats(Ls, Is, a, TT);
+}
+
+// ------------------------------------------------------------------ N > 32
 
 struct LogitsArgs {
     int T, d, N, has_bias;
@@ -411,53 +445,33 @@ struct LogitsArgs {
     uint32_t *err;
 };
 
-// One CTA = 16 warps = 4 token groups x 4 expert groups; warp tile 4 tokens x 8
-// experts, lane l = partial l. Tile 16 tokens x 32 experts; chunks of 256 features:
-// token rows and transposed weight rows ([expert][feature], so a lane's 8 features
-// of one expert are one 32-byte run) by bulk copies into a 4-slot ring.
+// One CTA = 16 consumer warps (4 token groups x 4 expert groups, warp tile 4
+// tokens x 8 experts, lane l = partial l) + 1 producer warp. Tile 16 tokens x 32
+// experts; per chunk of 256 features one 2D TMA copy of the token tile and one
+// bulk copy of the 32 experts' weight rows, into a 4-slot ring.
 template <typename XT>
-__global__ void __launch_bounds__(512, 1) k_logits_large(const XT *__restrict__ x, const float *__restrict__ w_t,
-                                                        const float *__restrict__ b_r, LogitsArgs a) {
-    constexpr int TOK = 16, EXP = 32, TO = 4, EO = 8;
+__global__ void __launch_bounds__(544, 1) k_logits_large(const __grid_constant__ CUtensorMap tmx,
+                                                        const float *__restrict__ w_t, const float *__restrict__ b_r,
+                                                        LogitsArgs a) {
+    constexpr int NC = 16, TOK = 16, EXP = 32, TO = 4, EO = 8;
     constexpr int KC = 256, NBLK = KC / 8, STAGES = 4;
     constexpr int ES = (int)sizeof(XT);
-    constexpr int XROW = KC * ES + 16;
-    constexpr int WROW = KC * 4 + 16;
-    constexpr int X_BYTES = TOK * XROW;
-    constexpr int STAGE = X_BYTES + EXP * WROW;
-    extern __shared__ __align__(16) float smem[];
-    __shared__ uint64_t full[STAGES];
-    __shared__ int abort_flag;
-    uint8_t *sb = reinterpret_cast<uint8_t *>(smem);
+    constexpr int X_BYTES = TOK * KC * ES;
+    constexpr int STAGE = (X_BYTES + EXP * KC * 4 + 1023) & ~1023;
+    extern __shared__ __align__(1024) uint8_t router_smem[];
+    __shared__ Ring<STAGES> ring;
+    uint8_t *sb = router_smem + ((1024 - (tc::smem_u32(router_smem) & 1023)) & 1023);
 
     const int T = a.T, d = a.d, N = a.N;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int tg = warp >> 2, eg = warp & 3;
-    const int t0 = blockIdx.x * TOK, e0 = blockIdx.y * EXP;
-    const int ntok = min(TOK, T - t0), nexp = min(EXP, N - e0);
+    const int e0 = blockIdx.x * EXP, t0 = blockIdx.y * TOK;   // experts fastest: CTAs sharing a token tile run together
+    const int nexp = min(EXP, N - e0);
     const int nblocks = d / 8;
     const int nchunks = (nblocks + NBLK - 1) / NBLK;
 
-    if (tid == 0) {
-        abort_flag = 0;
-        for (int i = 0; i < STAGES; ++i) tc::mbar_init(&full[i], 1);
-        tc::fence_mbar_init();
-    }
+    if (tid == 0) ring.init(NC);
     __syncthreads();
-
-    auto issue = [&](int c) {
-        if (warp != 0 || c >= nchunks) return;
-        const int b0 = c * NBLK, nb = min(NBLK, nblocks - b0);
-        uint8_t *slot = sb + (size_t)(c % STAGES) * STAGE;
-        uint64_t *bar = &full[c % STAGES];
-        const uint32_t xb = (uint32_t)(nb * 8 * ES), wb = (uint32_t)(nb * 8 * 4);
-        if (lane == 0) tc::mbar_arrive_expect_tx(bar, (uint32_t)ntok * xb + (uint32_t)nexp * wb);
-        __syncwarp();
-        if (lane < ntok)
-            tc::bulk_copy_g2s(slot + lane * XROW, x + (size_t)(t0 + lane) * d + (size_t)b0 * 8, xb, bar);
-        if (lane < nexp)
-            tc::bulk_copy_g2s(slot + X_BYTES + lane * WROW, w_t + (size_t)(e0 + lane) * d + (size_t)b0 * 8, wb, bar);
-    };
 
     float acc[TO][EO];
 #pragma unroll
@@ -465,48 +479,50 @@ __global__ void __launch_bounds__(512, 1) k_logits_large(const XT *__restrict__ 
 #pragma unroll
         for (int j = 0; j < EO; ++j) acc[i][j] = 0.0f;
 
-#pragma unroll
-    for (int c = 0; c < STAGES - 1; ++c) issue(c);
-    bool ok = true;
-    int issued = min(STAGES - 1, nchunks);
-    for (int c = 0; c < nchunks; ++c) {
-        const bool mine = wait_phase(&full[c % STAGES], (uint32_t)((c / STAGES) & 1), &abort_flag, a.err);
-        __syncthreads();
-        if (!mine || *(volatile int *)&abort_flag) {
-            ok = false;
-            break;
-        }
-        issue(c + STAGES - 1);
-        if (c + STAGES - 1 < nchunks) ++issued;
-        const uint8_t *slot = sb + (size_t)(c % STAGES) * STAGE;
-        if (c * NBLK + lane < nblocks) {
-            float xf[TO][8];
-#pragma unroll
-            for (int i = 0; i < TO; ++i) load8<XT>(slot + (tg * TO + i) * XROW + lane * 8 * ES, xf[i]);
-            const float *wl = reinterpret_cast<const float *>(slot + X_BYTES) + lane * 8;
-#pragma unroll
-            for (int jp = 0; jp < EO; jp += 2) {
-                float w0[8], w1[8];
-                lds<8>(wl + (eg * EO + jp) * (WROW / 4), w0);
-                lds<8>(wl + (eg * EO + jp + 1) * (WROW / 4), w1);
-#pragma unroll
-                for (int r = 0; r < 8; ++r)
-#pragma unroll
-                    for (int i = 0; i < TO; ++i) {
-                        acc[i][jp] = __fmaf_rn(xf[i][r], w0[r], acc[i][jp]);
-                        acc[i][jp + 1] = __fmaf_rn(xf[i][r], w1[r], acc[i][jp + 1]);
-                    }
+    if (warp == NC) {
+        if (lane == 0) {
+            int issued = 0;
+            for (int c = 0; c < nchunks; ++c) {
+                if (!ring.acquire(c, a.err)) break;
+                uint8_t *slot = sb + (size_t)(c % STAGES) * STAGE;
+                uint64_t *bar = &ring.full[c % STAGES];
+                const uint32_t wbytes = (uint32_t)(nexp * KC * 4);
+                tc::mbar_arrive_expect_tx(bar, (uint32_t)X_BYTES + wbytes);
+                tc::tma_load_2d(slot, &tmx, c * KC, t0, bar);
+                tc::bulk_copy_g2s(slot + X_BYTES, w_t + ((size_t)c * N + e0) * KC, wbytes, bar);
+                issued = c + 1;
             }
+            ring.drain(issued);
+        }
+    } else {
+        for (int c = 0; c < nchunks; ++c) {
+            if (!ring.ready(c, a.err)) break;
+            const uint8_t *slot = sb + (size_t)(c % STAGES) * STAGE;
+            const int nb = min(NBLK, nblocks - c * NBLK);
+            if (lane < nb) {
+                float xf[TO][8];
+#pragma unroll
+                for (int i = 0; i < TO; ++i) load8<XT>(slot + ((tg * TO + i) * KC + lane * 8) * ES, xf[i]);
+                const float *wl = reinterpret_cast<const float *>(slot + X_BYTES) + (eg * EO) * KC;
+#pragma unroll
+                for (int jp = 0; jp < EO; jp += 2) {
+                    float w0[8], w1[8];
+                    load_w8(wl + jp * KC, lane, nb, w0);
+                    load_w8(wl + (jp + 1) * KC, lane, nb, w1);
+#pragma unroll
+                    for (int r = 0; r < 8; ++r)
+#pragma unroll
+                        for (int i = 0; i < TO; ++i) {
+                            acc[i][jp] = __fmaf_rn(xf[i][r], w0[r], acc[i][jp]);
+                            acc[i][jp + 1] = __fmaf_rn(xf[i][r], w1[r], acc[i][jp + 1]);
+                        }
+                }
+            }
+            ring.release(c);
         }
     }
-    if (tid == 0)
-        for (int c = max(0, issued - STAGES); c < issued; ++c) {
-            const uint64_t ts = tc::globaltimer_ns();
-            while (!tc::mbar_try_wait(&full[c % STAGES], (uint32_t)((c / STAGES) & 1)))
-                if (tc::globaltimer_ns() - ts > kWaitNs) break;
-        }
     __syncthreads();
-    if (!ok) return;
+    if (ring.aborted() || warp == NC) return;
 #pragma unroll
     for (int i = 0; i < TO; ++i)
 #pragma unroll
@@ -739,31 +755,44 @@ __global__ void __launch_bounds__(256) k_assign(AssignArgs a) {
     }
 }
 
+// 2D map of the token activations [T][d], box 256 features x `rows` tokens.
+template <typename XT>
+bool token_map(CUtensorMap *m, const XT *x, int T, int d, int rows) {
+    const uint64_t dims[2] = {(uint64_t)d, (uint64_t)T};
+    const uint64_t strides[1] = {(uint64_t)d * sizeof(XT)};
+    const uint32_t box[2] = {256u, (uint32_t)rows};
+    const CUtensorMapDataType dt =
+        sizeof(XT) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    return encode_tmap(m, dt, 2, x, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 template <typename XT, int NP>
-cudaError_t launch_small(const moe_config &c, const XT *x, const float *w_r, const float *b_r, RouterArgs ra,
+cudaError_t launch_small(const moe_config &c, const XT *x, const float *w_t, const float *b_r, RouterArgs ra,
                          cudaStream_t s) {
     constexpr int TT = 4 * (32 / NP);
-    const size_t stage = (size_t)32 * wblock_stride(c.N, NP) * 4 + (size_t)TT * (256 * sizeof(XT) + 16);
+    CUtensorMap tmx;
+    if (!token_map<XT>(&tmx, x, c.T, c.d, TT)) return cudaErrorInvalidValue;
+    const size_t stage = ((size_t)TT * 256 * sizeof(XT) + (size_t)NP * 256 * 4 + 1023) & ~(size_t)1023;
     const size_t gate = ((size_t)TT * c.N + (size_t)TT * 8) * sizeof(float);
-    const size_t bytes = std::max(6 * stage, gate);
-    auto kern = c.N % 4 == 0 ? k_router_small<XT, NP, true> : k_router_small<XT, NP, false>;
+    const size_t bytes = std::max(6 * stage, gate) + 1024;
+    auto kern = k_router_small<XT, NP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
     if (e != cudaSuccess) return e;
-    kern<<<ra.tiles, 128, bytes, s>>>(x, w_r, b_r, ra);
+    kern<<<ra.tiles, 160, bytes, s>>>(tmx, w_t, b_r, ra);
     return cudaGetLastError();
 }
 
 template <typename XT>
-cudaError_t launch_large(const moe_config &c, const XT *x, const float *w_r, const float *b_r, RouterArgs ra,
-                         float *logits, float *w_t, cudaStream_t s) {
-    k_transpose_wr<<<dim3((c.d + 31) / 32, (c.N + 31) / 32), 256, 0, s>>>(w_r, w_t, c.d, c.N);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+cudaError_t launch_large(const moe_config &c, const XT *x, const float *w_t, const float *b_r, RouterArgs ra,
+                         float *logits, cudaStream_t s) {
+    CUtensorMap tmx;
+    if (!token_map<XT>(&tmx, x, c.T, c.d, 16)) return cudaErrorInvalidValue;
     LogitsArgs la{c.T, c.d, c.N, ra.has_bias, logits, ra.err};
-    const size_t lbytes = 4 * (size_t)(16 * (256 * sizeof(XT) + 16) + 32 * (256 * 4 + 16));
-    e = cudaFuncSetAttribute(k_logits_large<XT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lbytes);
+    const size_t stage = ((size_t)16 * 256 * sizeof(XT) + (size_t)32 * 256 * 4 + 1023) & ~(size_t)1023;
+    const size_t lbytes = 4 * stage + 1024;
+    cudaError_t e = cudaFuncSetAttribute(k_logits_large<XT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lbytes);
     if (e != cudaSuccess) return e;
-    k_logits_large<XT><<<dim3((c.T + 15) / 16, (c.N + 31) / 32), 512, lbytes, s>>>(x, w_t, b_r, la);
+    k_logits_large<XT><<<dim3((c.N + 31) / 32, (c.T + 15) / 16), 544, lbytes, s>>>(tmx, w_t, b_r, la);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const size_t gbytes = ((size_t)64 * c.N + 64 * 8) * sizeof(float);
     e = cudaFuncSetAttribute(k_gate, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gbytes);
@@ -775,11 +804,14 @@ cudaError_t launch_large(const moe_config &c, const XT *x, const float *w_r, con
 template <typename XT>
 cudaError_t launch_logits_gate(const moe_config &c, const XT *x, const float *w_r, const float *b_r, RouterArgs ra,
                                float *logits, float *w_t, cudaStream_t s) {
-    if (c.N <= 4) return launch_small<XT, 4>(c, x, w_r, b_r, ra, s);
-    if (c.N <= 8) return launch_small<XT, 8>(c, x, w_r, b_r, ra, s);
-    if (c.N <= 16) return launch_small<XT, 16>(c, x, w_r, b_r, ra, s);
-    if (c.N <= 32) return launch_small<XT, 32>(c, x, w_r, b_r, ra, s);
-    return launch_large<XT>(c, x, w_r, b_r, ra, logits, w_t, s);
+    k_transpose_wr<<<dim3((c.d + 31) / 32, (c.N + 31) / 32), 256, 0, s>>>(w_r, w_t, c.d, c.N);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (c.N <= 4) return launch_small<XT, 4>(c, x, w_t, b_r, ra, s);
+    if (c.N <= 8) return launch_small<XT, 8>(c, x, w_t, b_r, ra, s);
+    if (c.N <= 16) return launch_small<XT, 16>(c, x, w_t, b_r, ra, s);
+    if (c.N <= 32) return launch_small<XT, 32>(c, x, w_t, b_r, ra, s);
+    return launch_large<XT>(c, x, w_t, b_r, ra, logits, s);
 }
 
 }  // namespace
