@@ -96,6 +96,8 @@ typedef struct {
 
 /* debug_flags bits */
 #define MOE_DEBUG_FORCE_SIMT_FFN 1u  /* run the expert FFN on the CUDA-core kernel even for bf16 */
+#define MOE_DEBUG_FFN_PAIR 2u        /* bf16: always use the CTA-pair tensor-core kernel   */
+#define MOE_DEBUG_FFN_SINGLE 4u      /* bf16: always use the single-CTA tensor-core kernel */
 
 /* Validate a config on the host. No CUDA call is made. */
 moe_status moe_validate_config(const moe_config *cfg);

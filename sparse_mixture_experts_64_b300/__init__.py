@@ -23,6 +23,8 @@ MOE_F32, MOE_BF16 = 0, 1
 MOE_SOFTMAX_THEN_TOPK, MOE_TOPK_THEN_SOFTMAX = 0, 1
 MOE_ACT_SILU_GATED, MOE_ACT_RELU = 0, 1
 MOE_DEBUG_FORCE_SIMT_FFN = 1
+MOE_DEBUG_FFN_PAIR = 2
+MOE_DEBUG_FFN_SINGLE = 4
 
 EXPORTED = ("moe_validate_config", "moe_workspace_size", "moe_max_rows", "moe_capacity",
             "moe_router_topk", "moe_dispatch", "moe_grouped_ffn", "moe_combine", "moe_forward",

@@ -97,7 +97,8 @@ struct TileInfo {
     bool shared;
 };
 
-__device__ __forceinline__ TileInfo decode_tile(const Smem &s, int nseg, int tile) {
+template <typename S>
+__device__ __forceinline__ TileInfo decode_tile(const S &s, int nseg, int tile) {
     int lo = 0, hi = nseg - 1;  // largest g with base[g] <= tile
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -110,6 +111,61 @@ __device__ __forceinline__ TileInfo decode_tile(const Smem &s, int nseg, int til
     ti.m = local % s.mt[lo];
     ti.n = local / s.mt[lo];
     return ti;
+}
+
+// Epilogue of one accumulator row (this thread's TMEM lane): activation, bf16,
+// 16-byte stores of the output columns [col0, col0 + BN_OUT) when row_ok.
+template <int KIND>
+__device__ __forceinline__ void epilogue_row(uint32_t tbase, __nv_bfloat16 *crow, int col0, int n_out, bool row_ok) {
+    if constexpr (KIND == KIND_GATED) {
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 32) {
+            uint32_t g[32], u[32];
+            tmem_ld32(tbase + c, g);
+            tmem_ld32(tbase + 128 + c, u);
+            tmem_ld_wait();
+            const int col = col0 + c;
+            if (row_ok && col < n_out) {
+                uint32_t packed[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float h0 = silu_f32(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
+                    const float h1 = silu_f32(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
+                    __nv_bfloat162 b = __floats2bfloat162_rn(h0, h1);
+                    packed[i] = *reinterpret_cast<uint32_t *>(&b);
+                }
+                uint4 *dst = reinterpret_cast<uint4 *>(crow + col);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+            }
+        }
+    } else {
+#pragma unroll 1
+        for (int c = 0; c < 256; c += 32) {
+            uint32_t v[32];
+            tmem_ld32(tbase + c, v);
+            tmem_ld_wait();
+            const int col = col0 + c;
+            if (row_ok && col < n_out) {
+                uint32_t packed[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float h0 = __uint_as_float(v[2 * i]), h1 = __uint_as_float(v[2 * i + 1]);
+                    if (KIND == KIND_RELU) {
+                        h0 = fmaxf(h0, 0.0f);
+                        h1 = fmaxf(h1, 0.0f);
+                    }
+                    __nv_bfloat162 b = __floats2bfloat162_rn(h0, h1);
+                    packed[i] = *reinterpret_cast<uint32_t *>(&b);
+                }
+                uint4 *dst = reinterpret_cast<uint4 *>(crow + col);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+            }
+        }
+    }
 }
 
 template <int KIND>
@@ -303,56 +359,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_ffn_tc(const __grid_constant
             const int n_out = sh ? p.n_out_sh : p.n_out;
             __nv_bfloat16 *crow = (sh ? p.C_sh : p.C) + orow * n_out;
             const uint32_t tbase = tmem_base + (uint32_t)(acc * ACC_COLS) + ((uint32_t)(quarter * 32) << 16);
-            if constexpr (KIND == KIND_GATED) {
-#pragma unroll 1
-                for (int c = 0; c < 128; c += 32) {
-                    uint32_t g[32], u[32];
-                    tmem_ld32(tbase + c, g);
-                    tmem_ld32(tbase + 128 + c, u);
-                    tmem_ld_wait();
-                    const int col = ti.n * 128 + c;
-                    if (row_ok && col < n_out) {
-                        uint32_t packed[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const float h0 = silu_f32(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
-                            const float h1 =
-                                silu_f32(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
-                            __nv_bfloat162 b = __floats2bfloat162_rn(h0, h1);
-                            packed[i] = *reinterpret_cast<uint32_t *>(&b);
-                        }
-                        uint4 *dst = reinterpret_cast<uint4 *>(crow + col);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
-                    }
-                }
-            } else {
-#pragma unroll 1
-                for (int c = 0; c < 256; c += 32) {
-                    uint32_t v[32];
-                    tmem_ld32(tbase + c, v);
-                    tmem_ld_wait();
-                    const int col = ti.n * 256 + c;
-                    if (row_ok && col < n_out) {
-                        uint32_t packed[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            float h0 = __uint_as_float(v[2 * i]), h1 = __uint_as_float(v[2 * i + 1]);
-                            if (KIND == KIND_RELU) {
-                                h0 = fmaxf(h0, 0.0f);
-                                h1 = fmaxf(h1, 0.0f);
-                            }
-                            __nv_bfloat162 b = __floats2bfloat162_rn(h0, h1);
-                            packed[i] = *reinterpret_cast<uint32_t *>(&b);
-                        }
-                        uint4 *dst = reinterpret_cast<uint4 *>(crow + col);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
-                    }
-                }
-            }
+            epilogue_row<KIND>(tbase, crow, ti.n * BN_OUT, n_out, row_ok);
             tc_fence_before();
             mbar_arrive(&s.tempty[acc]);
             if (++acc == 2) {
@@ -367,6 +374,266 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_ffn_tc(const __grid_constant
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ CTA-pair kernel
+//
+// Same computation with 2-CTA (cta_group::2) MMAs: a cluster of two CTAs on two
+// SMs computes a 256 x 256 tile per MMA 256x256x16. Each CTA stages its own 128
+// rows of A and 128 of the 256 B rows (gated: gate rows in the even CTA, up rows in
+// the odd CTA), so each SM moves a third less operand data per FLOP than the
+// single-CTA kernel and six 32 KB stages fit in shared memory. Both CTAs' loads
+// complete on the even CTA's stage barrier, and the even CTA issues the MMAs;
+// each CTA's TMEM holds its own 128 accumulator rows and its epilogue stores them.
+// Commits arrive on both CTAs' barriers (multicast). Tiles cover 256 rows of one
+// segment, so this kernel is chosen when experts receive many rows.
+constexpr int STAGES2 = 6;
+constexpr uint32_t HALF_BYTES = 128 * BK * 2;            // 16 KB: 128 rows x 64 bf16
+constexpr uint32_t STAGE2_BYTES = 2 * HALF_BYTES;
+constexpr size_t SMEM2_BYTES = (size_t)STAGES2 * STAGE2_BYTES + 1024;
+
+struct Smem2 {
+    uint64_t full[STAGES2], empty[STAGES2], tfull[2], tempty[2], drain;
+    uint32_t tmem_base;
+    int abort_flag;
+    int base[MAX_SEG + 1];
+    int mt[MAX_SEG];
+    int row0[MAX_SEG];
+    int rows[MAX_SEG];
+};
+
+template <int KIND, int NACC>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    k_ffn_tc2(const __grid_constant__ TcParams p) {
+    constexpr int BN_OUT = KIND == KIND_GATED ? 128 : 256;
+    constexpr uint32_t TMEM_COLS2 = NACC * ACC_COLS;
+    __shared__ Smem2 s;
+    extern __shared__ uint8_t dyn_smem[];
+    const uint32_t dyn_base = smem_u32(dyn_smem);
+    uint8_t *tiles = dyn_smem + (((dyn_base + 1023u) & ~1023u) - dyn_base);
+    auto smA = [&](int st) { return tiles + (size_t)st * STAGE2_BYTES; };
+    auto smB = [&](int st) { return tiles + (size_t)st * STAGE2_BYTES + HALF_BYTES; };
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+    const int nseg = p.n_seg + (p.sh_rows > 0 ? 1 : 0);
+    const int nt_routed = (p.n_out + BN_OUT - 1) / BN_OUT;
+    const int nt_sh = (p.n_out_sh + BN_OUT - 1) / BN_OUT;
+
+    // ---- tile table (pair tiles of 256 rows) and barriers ----
+    if (warp == 0) {
+        constexpr int PER = (MAX_SEG + 31) / 32;
+        int cnt[PER];
+        int sum = 0;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int g = lane * PER + i;
+            int tiles_g = 0;
+            if (g < nseg) {
+                int r0, rows, nt;
+                if (g < p.n_seg) {
+                    r0 = min(max(p.offsets[g], 0), p.a_rows);
+                    rows = min(max(p.offsets[g + 1], r0), p.a_rows) - r0;
+                    nt = nt_routed;
+                } else {
+                    r0 = 0;
+                    rows = p.sh_rows;
+                    nt = nt_sh;
+                }
+                rows = max(rows, 0);
+                const int mt = (rows + 2 * BM - 1) / (2 * BM);
+                s.mt[g] = max(mt, 1);
+                s.row0[g] = r0;
+                s.rows[g] = rows;
+                tiles_g = mt * nt;
+            }
+            cnt[i] = tiles_g;
+            sum += tiles_g;
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += u;
+        }
+        int run = incl - sum;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int g = lane * PER + i;
+            if (g < nseg) s.base[g] = run;
+            run += cnt[i];
+        }
+        if (lane == 31) s.base[nseg] = incl;
+        if (lane == 0) {
+            for (int i = 0; i < STAGES2; ++i) {
+                mbar_init(&s.full[i], 1);
+                mbar_init(&s.empty[i], 1);
+            }
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(&s.tfull[i], 1);
+                mbar_init(&s.tempty[i], 8);  // 4 epilogue warps of each CTA
+            }
+            mbar_init(&s.drain, 1);
+            s.abort_flag = 0;
+            fence_mbar_init();
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(&s.tmem_base, TMEM_COLS2);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // both CTAs' barriers initialised and TMEM allocated
+    tc_fence_after();
+    const uint32_t tmem_base = s.tmem_base;
+    if (tid == 0) {
+        // the pair MMA writes the same TMEM address in both CTAs
+        const uint32_t other = ld_shared_cluster_u32(map_to_rank(smem_u32(&s.tmem_base), rank ^ 1u));
+        if (other != tmem_base) {
+            s.abort_flag = 1;
+            record_error(p.err, kErrFault);
+        }
+    }
+    __syncthreads();
+    const bool run = s.abort_flag == 0;
+    const int total = s.base[nseg];
+    volatile int *abort_flag = &s.abort_flag;
+    const uint32_t lead_tempty = map_to_rank(smem_u32(&s.tempty[0]), 0);
+
+    if (warp == 0) {
+        // ================= TMA producer (both CTAs) =================
+        // Both CTAs' loads complete on the even CTA's full[] barrier, which the even
+        // CTA's producer arms with the bytes of both halves.
+        if (lane == 0 && run) {
+            int st = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            uint32_t issued_mask = 0, issued_par = 0;
+            const uint32_t lead_full = map_to_rank(smem_u32(&s.full[0]), 0);
+            for (int tile = cluster; tile < total && ok; tile += nclusters) {
+                const TileInfo ti = decode_tile(s, nseg, tile);
+                const bool sh = ti.seg >= p.n_seg;
+                const int K = sh ? p.K_sh : p.K;
+                const int arow = s.row0[ti.seg] + ti.m * 2 * BM + (int)rank * BM;
+                const CUtensorMap *ta = sh ? &p.tmA_sh : &p.tmA;
+                for (int kb = 0; kb < K / BK; ++kb) {
+                    if (!wait_bar(&s.empty[st], ph ^ 1, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = lead_full + 8u * (uint32_t)st;
+                    if (leader) mbar_arrive_expect_tx(&s.full[st], 2 * STAGE2_BYTES);
+                    const int kc = kb * BK;
+                    tma_load_2d_pair(smA(st), ta, kc, arow, fb);
+                    if (KIND == KIND_GATED) {
+                        // even CTA: gate rows, odd CTA: up rows -> accumulator columns 0-127 / 128-255
+                        if (sh) tma_load_2d_pair(smB(st), rank == 0 ? &p.tmB0_sh : &p.tmB1_sh, kc, ti.n * 128, fb);
+                        else tma_load_3d_pair(smB(st), rank == 0 ? &p.tmB0 : &p.tmB1, kc, ti.n * 128, ti.seg, fb);
+                    } else {
+                        const int brow = ti.n * 256 + (int)rank * 128;
+                        if (sh) tma_load_2d_pair(smB(st), &p.tmB0_sh, kc, brow, fb);
+                        else tma_load_3d_pair(smB(st), &p.tmB0, kc, brow, ti.seg, fb);
+                    }
+                    issued_mask |= 1u << st;
+                    issued_par = (issued_par & ~(1u << st)) | (ph << st);
+                    if (++st == STAGES2) {
+                        st = 0;
+                        ph ^= 1;
+                    }
+                }
+            }
+            // loads in flight land before the CTA exits (the even CTA waits for both halves)
+            if (leader)
+                for (int i = 0; i < STAGES2; ++i)
+                    if (issued_mask & (1u << i)) drain_bar(&s.full[i], (issued_par >> i) & 1u);
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && run) {
+            int st = 0, acc = 0;
+            uint32_t ph = 0, aph = 0;
+            bool ok = true;
+            if (leader) {
+                // ================= MMA issuer (even CTA) =================
+                constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, BN_MMA);
+                for (int tile = cluster; tile < total && ok; tile += nclusters) {
+                    const TileInfo ti = decode_tile(s, nseg, tile);
+                    const int K = ti.seg >= p.n_seg ? p.K_sh : p.K;
+                    if (!wait_bar(&s.tempty[acc], aph ^ 1, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + (uint32_t)(acc * ACC_COLS);
+                    for (int kb = 0; kb < K / BK; ++kb) {
+                        if (!wait_bar(&s.full[st], ph, abort_flag, p.err)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t ad = desc_sw128(smem_u32(smA(st)));
+                        const uint64_t bd = desc_sw128(smem_u32(smB(st)));
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk)
+                            umma_bf16_pair(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), IDESC,
+                                           (kb | kk) != 0 ? 1u : 0u);
+                        umma_commit_pair_mc(&s.empty[st], 0x3);
+                        if (++st == STAGES2) {
+                            st = 0;
+                            ph ^= 1;
+                        }
+                    }
+                    if (!ok) break;
+                    umma_commit_pair_mc(&s.tfull[acc], 0x3);
+                    if (++acc == NACC) {
+                        acc = 0;
+                        aph ^= 1;
+                    }
+                }
+                umma_commit_pair_mc(&s.drain, 0x1);
+                drain_bar(&s.drain, 0);
+            }
+        }
+    } else if (run) {
+        // ================= epilogue (warps 2..5 of both CTAs) =================
+        const int quarter = warp & 3;
+        const int r_in_tile = quarter * 32 + lane;
+        int acc = 0;
+        uint32_t aph = 0;
+        for (int tile = cluster; tile < total; tile += nclusters) {
+            const TileInfo ti = decode_tile(s, nseg, tile);
+            const bool sh = ti.seg >= p.n_seg;
+            if (!wait_bar(&s.tfull[acc], aph, abort_flag, p.err)) break;
+            tc_fence_after();
+            const int r_seg = ti.m * 2 * BM + (int)rank * BM + r_in_tile;  // row within the segment
+            const bool row_ok = r_seg < s.rows[ti.seg];
+            const int64_t orow = (int64_t)s.row0[ti.seg] + r_seg;
+            const int n_out = sh ? p.n_out_sh : p.n_out;
+            __nv_bfloat16 *crow = (sh ? p.C_sh : p.C) + orow * n_out;
+            const uint32_t tbase = tmem_base + (uint32_t)(acc * ACC_COLS) + ((uint32_t)(quarter * 32) << 16);
+            epilogue_row<KIND>(tbase, crow, ti.n * BN_OUT, n_out, row_ok);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (leader) mbar_arrive(&s.tempty[acc]);
+                else mbar_arrive_remote(lead_tempty + 8u * (uint32_t)acc);
+            }
+            if (++acc == NACC) {
+                acc = 0;
+                aph ^= 1;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // the pair's MMAs and both epilogues are done with TMEM
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, TMEM_COLS2);
     }
 }
 
@@ -403,17 +670,36 @@ cudaError_t launch_kind(const TcParams &p, int64_t max_tiles, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// Accumulator buffers of the pair kernel (TMEM columns = 256 per buffer).
+constexpr int PAIR_NACC = 2;
+
+template <int KIND>
+cudaError_t launch_kind2(const TcParams &p, int64_t max_tiles, cudaStream_t s) {
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(k_ffn_tc2<KIND, PAIR_NACC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)SMEM2_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    const int clusters = (int)std::max<int64_t>(1, std::min<int64_t>(max_tiles, device_sm_count() / 2));
+    k_ffn_tc2<KIND, PAIR_NACC><<<2 * clusters, NUM_THREADS, SMEM2_BYTES, s>>>(p);
+    return cudaGetLastError();
+}
+
 // One product over the routed segments and/or the shared segment.
 //   a / a_sh: A operands ([a_rows][K] / [sh_rows][K_sh]);
 //   b0,b1 / b0_sh,b1_sh: weights ([n_seg][n_out][K] / [n_out_sh][K_sh]);
 //   out / out_sh: outputs ([a_rows][n_out] / [sh_rows][n_out_sh]).
+// pair: run the CTA-pair kernel (256-row tiles) instead of the single-CTA one.
 template <int KIND>
 cudaError_t product(const int32_t *offsets, int n_seg, int64_t a_rows, const void *a, const void *b0,
                     const void *b1, int K, int n_out, void *out, int sh_rows, const void *a_sh,
                     const void *b0_sh, const void *b1_sh, int K_sh, int n_out_sh, void *out_sh,
-                    uint32_t *err, cudaStream_t s) {
+                    uint32_t *err, cudaStream_t s, bool pair) {
     constexpr int BN_OUT = KIND == KIND_GATED ? 128 : 256;
-    constexpr uint32_t BOX_B = KIND == KIND_GATED ? 128 : 256;
+    const uint32_t box_b = (KIND == KIND_GATED || pair) ? 128 : 256;
+    const int64_t tm = pair ? 2 * BM : BM;
     TcParams p;
     memset(&p, 0, sizeof(p));
     p.offsets = offsets;
@@ -430,41 +716,47 @@ cudaError_t product(const int32_t *offsets, int n_seg, int64_t a_rows, const voi
     int64_t max_tiles = 0;
     if (n_seg > 0) {
         if (!encode_2d(&p.tmA, a, K, a_rows, BM)) return cudaErrorInvalidValue;
-        if (!encode_3d(&p.tmB0, b0, K, n_out, n_seg, BOX_B)) return cudaErrorInvalidValue;
-        if (KIND == KIND_GATED && !encode_3d(&p.tmB1, b1, K, n_out, n_seg, BOX_B)) return cudaErrorInvalidValue;
-        max_tiles += ((a_rows + BM - 1) / BM + n_seg) * ((n_out + BN_OUT - 1) / BN_OUT);
+        if (!encode_3d(&p.tmB0, b0, K, n_out, n_seg, box_b)) return cudaErrorInvalidValue;
+        if (KIND == KIND_GATED && !encode_3d(&p.tmB1, b1, K, n_out, n_seg, box_b)) return cudaErrorInvalidValue;
+        max_tiles += ((a_rows + tm - 1) / tm + n_seg) * ((n_out + BN_OUT - 1) / BN_OUT);
     }
     if (sh_rows > 0) {
         if (!encode_2d(&p.tmA_sh, a_sh, K_sh, sh_rows, BM)) return cudaErrorInvalidValue;
-        if (!encode_2d(&p.tmB0_sh, b0_sh, K_sh, n_out_sh, BOX_B)) return cudaErrorInvalidValue;
-        if (KIND == KIND_GATED && !encode_2d(&p.tmB1_sh, b1_sh, K_sh, n_out_sh, BOX_B))
+        if (!encode_2d(&p.tmB0_sh, b0_sh, K_sh, n_out_sh, box_b)) return cudaErrorInvalidValue;
+        if (KIND == KIND_GATED && !encode_2d(&p.tmB1_sh, b1_sh, K_sh, n_out_sh, box_b))
             return cudaErrorInvalidValue;
-        max_tiles += ((int64_t)(sh_rows + BM - 1) / BM) * ((n_out_sh + BN_OUT - 1) / BN_OUT);
+        max_tiles += ((int64_t)(sh_rows + tm - 1) / tm) * ((n_out_sh + BN_OUT - 1) / BN_OUT);
     }
     if (max_tiles == 0) return cudaSuccess;
-    return launch_kind<KIND>(p, max_tiles, s);
+    return pair ? launch_kind2<KIND>(p, max_tiles, s) : launch_kind<KIND>(p, max_tiles, s);
 }
 
 }  // namespace
 
 cudaError_t launch_ffn_tc(const moe_config &c, const FfnGroup &g, uint32_t *err, cudaStream_t s) {
+    // CTA-pair tiles hold 256 rows of one segment: worth it when experts receive
+    // many rows (at least 512 on average), otherwise the last tile of each
+    // segment wastes too much.
+    bool pair = g.n_seg > 0 && g.a_rows >= 512LL * g.n_seg;
+    if (c.debug_flags & MOE_DEBUG_FFN_PAIR) pair = true;
+    if (c.debug_flags & MOE_DEBUG_FFN_SINGLE) pair = false;
     cudaError_t e;
     // product 1: hidden activations
     if (g.act == MOE_ACT_SILU_GATED) {
         e = product<KIND_GATED>(g.offsets, g.n_seg, g.a_rows, g.a, g.w_a, g.w_b, c.d, g.h, g.hid, g.sh_rows,
-                                g.sh_a, g.sh_w_gate, g.sh_w_up, c.d, g.h_sh, g.sh_hid, err, s);
+                                g.sh_a, g.sh_w_gate, g.sh_w_up, c.d, g.h_sh, g.sh_hid, err, s, pair);
     } else {
         e = product<KIND_RELU>(g.offsets, g.n_seg, g.a_rows, g.a, g.w_a, nullptr, c.d, g.h, g.hid, 0, nullptr,
-                               nullptr, nullptr, 0, 0, nullptr, err, s);
+                               nullptr, nullptr, 0, 0, nullptr, err, s, pair);
         if (e == cudaSuccess && g.sh_rows > 0)
             e = product<KIND_GATED>(nullptr, 0, 0, nullptr, nullptr, nullptr, 0, 0, nullptr, g.sh_rows, g.sh_a,
-                                    g.sh_w_gate, g.sh_w_up, c.d, g.h_sh, g.sh_hid, err, s);
+                                    g.sh_w_gate, g.sh_w_up, c.d, g.h_sh, g.sh_hid, err, s, false);
     }
     if (e != cudaSuccess) return e;
     if (g.mid_event && (e = cudaEventRecord(g.mid_event, s)) != cudaSuccess) return e;
     // product 2: outputs
     return product<KIND_PLAIN>(g.offsets, g.n_seg, g.a_rows, g.hid, g.w_out, nullptr, g.h, c.d, g.out,
-                               g.sh_rows, g.sh_hid, g.sh_w_down, nullptr, g.h_sh, c.d, g.sh_out, err, s);
+                               g.sh_rows, g.sh_hid, g.sh_w_down, nullptr, g.h_sh, c.d, g.sh_out, err, s, pair);
 }
 
 }  // namespace moe

@@ -69,6 +69,30 @@ def test_small_parity(w):
         assert np.array_equal(sep["y"][dropped], inp["x"].float().cpu().numpy()[dropped])
 
 
+PAIR = [
+    _small("mixtral_prefill", T=300, d=256, h=384),
+    _small("switch_top1", T=640, d=256, h=512),
+    _small("deepseek_fine", T=200, d=256, N=16, k=4, h=128, h_shared=192),
+    _small("mixtral_prefill", T=1100, d=128, h=256, N=2, k=1),
+]
+
+
+@pytest.mark.parametrize("w", PAIR, ids=[w.name for w in PAIR])
+def test_pair_and_single_cta_ffn_kernels(w):
+    """Both tensor-core kernels (CTA pair with 256-row tiles, single CTA with 128-row
+    tiles) match the oracle on the same inputs."""
+    inp = W.make_inputs(w, device="cuda")
+    ws = moe.workspace(cfg_of(w))
+    rt = O.forward(w, oracle_inputs(inp))
+    outs = {}
+    for name, flag in (("pair", moe.MOE_DEBUG_FFN_PAIR), ("single", moe.MOE_DEBUG_FFN_SINGLE)):
+        outs[name] = host(run_forward(cfg_of(w, debug_flags=flag), inp, ws))
+        assert moe.moe_check_error(ws) == moe.MOE_OK, name
+        check_routing(outs[name], rt, sep=False)
+        check_output(outs[name]["y"], rt["y"], w.dtype)
+    assert rel_max_err(outs["pair"]["y"], outs["single"]["y"]) <= 2e-2
+
+
 @pytest.mark.parametrize("name", ["mixtral_prefill", "deepseek_fine"])
 def test_simt_and_tensor_core_ffn_agree(name):
     w = _small(name, T=160, d=256, h=256, N=8, k=2, h_shared=128 if name == "deepseek_fine" else 0)
