@@ -25,6 +25,7 @@ MOE_ACT_SILU_GATED, MOE_ACT_RELU = 0, 1
 MOE_DEBUG_FORCE_SIMT_FFN = 1
 MOE_DEBUG_FFN_PAIR = 2
 MOE_DEBUG_FFN_SINGLE = 4
+MOE_DEBUG_FFN_SWAP = 8
 
 EXPORTED = ("moe_validate_config", "moe_workspace_size", "moe_max_rows", "moe_capacity",
             "moe_router_topk", "moe_dispatch", "moe_grouped_ffn", "moe_combine", "moe_forward",

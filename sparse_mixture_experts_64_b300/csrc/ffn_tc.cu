@@ -28,6 +28,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "tc_ptx.cuh"
+#include "tc_sync.cuh"
 
 namespace moe {
 namespace {
@@ -43,7 +44,6 @@ constexpr int ACC_COLS = 256;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int NUM_THREADS = 192;
 constexpr int MAX_SEG = 257;
-constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + 1024;
 
 enum { KIND_GATED = 0, KIND_RELU = 1, KIND_PLAIN = 2 };
@@ -69,28 +69,6 @@ struct Smem {
     int row0[MAX_SEG];      // first A row of each segment
     int rows[MAX_SEG];      // rows per segment
 };
-
-__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                         uint32_t *err) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > kTimeoutNs) {
-            *abort_flag = 1;
-            record_error(err, kErrTimeout);
-            return false;
-        }
-    }
-}
-
-// Wait without honouring the abort flag (used to drain work already in flight).
-__device__ __forceinline__ void drain_bar(uint64_t *bar, uint32_t parity) {
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity))
-        if (globaltimer_ns() - t0 > kTimeoutNs) break;
-}
 
 struct TileInfo {
     int seg, m, n;
@@ -361,7 +339,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_ffn_tc(const __grid_constant
             const uint32_t tbase = tmem_base + (uint32_t)(acc * ACC_COLS) + ((uint32_t)(quarter * 32) << 16);
             epilogue_row<KIND>(tbase, crow, ti.n * BN_OUT, n_out, row_ok);
             tc_fence_before();
-            mbar_arrive(&s.tempty[acc]);
+            mbar_arrive_relaxed(&s.tempty[acc]);
             if (++acc == 2) {
                 acc = 0;
                 aph ^= 1;
@@ -618,8 +596,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                if (leader) mbar_arrive(&s.tempty[acc]);
-                else mbar_arrive_remote(lead_tempty + 8u * (uint32_t)acc);
+                if (leader) mbar_arrive_relaxed(&s.tempty[acc]);
+                else mbar_arrive_remote_relaxed(lead_tempty + 8u * (uint32_t)acc);
             }
             if (++acc == NACC) {
                 acc = 0;
@@ -638,23 +616,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 }
 
 // ------------------------------------------------------------------ host side
-
-// 2D bf16 [outer][inner] map, box inner 64 x box_outer, 128-byte swizzle.
-bool encode_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
-    const uint64_t dims[2] = {inner, outer};
-    const uint64_t strides[1] = {inner * 2};
-    const uint32_t box[2] = {(uint32_t)BK, box_outer};
-    return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
-}
-
-// 3D bf16 [n_exp][outer][inner] map, box 64 x box_outer x 1.
-bool encode_3d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t n_exp,
-               uint32_t box_outer) {
-    const uint64_t dims[3] = {inner, outer, n_exp};
-    const uint64_t strides[2] = {inner * 2, inner * outer * 2};
-    const uint32_t box[3] = {(uint32_t)BK, box_outer, 1};
-    return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
-}
 
 template <int KIND>
 cudaError_t launch_kind(const TcParams &p, int64_t max_tiles, cudaStream_t s) {
@@ -715,15 +676,15 @@ cudaError_t product(const int32_t *offsets, int n_seg, int64_t a_rows, const voi
     p.err = err;
     int64_t max_tiles = 0;
     if (n_seg > 0) {
-        if (!encode_2d(&p.tmA, a, K, a_rows, BM)) return cudaErrorInvalidValue;
-        if (!encode_3d(&p.tmB0, b0, K, n_out, n_seg, box_b)) return cudaErrorInvalidValue;
-        if (KIND == KIND_GATED && !encode_3d(&p.tmB1, b1, K, n_out, n_seg, box_b)) return cudaErrorInvalidValue;
+        if (!encode_bf16_2d(&p.tmA, a, K, a_rows, BM)) return cudaErrorInvalidValue;
+        if (!encode_bf16_3d(&p.tmB0, b0, K, n_out, n_seg, box_b)) return cudaErrorInvalidValue;
+        if (KIND == KIND_GATED && !encode_bf16_3d(&p.tmB1, b1, K, n_out, n_seg, box_b)) return cudaErrorInvalidValue;
         max_tiles += ((a_rows + tm - 1) / tm + n_seg) * ((n_out + BN_OUT - 1) / BN_OUT);
     }
     if (sh_rows > 0) {
-        if (!encode_2d(&p.tmA_sh, a_sh, K_sh, sh_rows, BM)) return cudaErrorInvalidValue;
-        if (!encode_2d(&p.tmB0_sh, b0_sh, K_sh, n_out_sh, box_b)) return cudaErrorInvalidValue;
-        if (KIND == KIND_GATED && !encode_2d(&p.tmB1_sh, b1_sh, K_sh, n_out_sh, box_b))
+        if (!encode_bf16_2d(&p.tmA_sh, a_sh, K_sh, sh_rows, BM)) return cudaErrorInvalidValue;
+        if (!encode_bf16_2d(&p.tmB0_sh, b0_sh, K_sh, n_out_sh, box_b)) return cudaErrorInvalidValue;
+        if (KIND == KIND_GATED && !encode_bf16_2d(&p.tmB1_sh, b1_sh, K_sh, n_out_sh, box_b))
             return cudaErrorInvalidValue;
         max_tiles += ((int64_t)(sh_rows + tm - 1) / tm) * ((n_out_sh + BN_OUT - 1) / BN_OUT);
     }
@@ -734,10 +695,13 @@ cudaError_t product(const int32_t *offsets, int n_seg, int64_t a_rows, const voi
 }  // namespace
 
 cudaError_t launch_ffn_tc(const moe_config &c, const FfnGroup &g, uint32_t *err, cudaStream_t s) {
-    // CTA-pair tiles hold 256 rows of one segment: worth it when experts receive
-    // many rows (at least 512 on average), otherwise the last tile of each
-    // segment wastes too much.
-    bool pair = g.n_seg > 0 && g.a_rows >= 512LL * g.n_seg;
+    if (c.debug_flags & MOE_DEBUG_FFN_SWAP) return launch_ffn_sw(c, g, err, s);
+    // CTA-pair tiles hold 256 rows of one segment. Measured on B300, the pair
+    // kernel wins from about 256 rows per expert on average (DeepSeek-shaped
+    // layer: 8.70 vs 9.27 ms per forward, even with half of its last tiles
+    // empty); with a few rows per expert the single-CTA kernel's 128-row tiles
+    // waste less.
+    bool pair = g.n_seg > 0 && g.a_rows >= 224LL * g.n_seg;
     if (c.debug_flags & MOE_DEBUG_FFN_PAIR) pair = true;
     if (c.debug_flags & MOE_DEBUG_FFN_SINGLE) pair = false;
     cudaError_t e;

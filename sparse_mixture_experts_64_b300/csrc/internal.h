@@ -89,6 +89,7 @@ struct FfnGroup {
 };
 cudaError_t launch_ffn_simt(const moe_config &c, const FfnGroup &g, uint32_t *err, cudaStream_t s);
 cudaError_t launch_ffn_tc(const moe_config &c, const FfnGroup &g, uint32_t *err, cudaStream_t s);
+cudaError_t launch_ffn_sw(const moe_config &c, const FfnGroup &g, uint32_t *err, cudaStream_t s);
 
 int device_sm_count();
 
@@ -96,5 +97,10 @@ int device_sm_count();
 // bytes for dims 1..rank-1, box in elements). false if the driver refuses it.
 bool encode_tmap(CUtensorMap *m, CUtensorMapDataType dt, int rank, const void *base, const uint64_t *dims,
                  const uint64_t *strides_bytes, const uint32_t *box, CUtensorMapSwizzle swizzle);
+// bf16 K-major operand maps: [outer][inner] and [n_exp][outer][inner], box 64
+// (inner) x box_outer (x 1), 128-byte swizzle.
+bool encode_bf16_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint32_t box_outer);
+bool encode_bf16_3d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t n_exp,
+                    uint32_t box_outer);
 
 }  // namespace moe

@@ -40,4 +40,22 @@ bool encode_tmap(CUtensorMap *m, CUtensorMapDataType dt, int rank, const void *b
               swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// bf16 [outer][inner] array, box 64 (inner) x box_outer, 128-byte swizzle: the
+// K-major operand tiles of the tensor-core kernels.
+bool encode_bf16_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+    const uint64_t dims[2] = {inner, outer};
+    const uint64_t strides[1] = {inner * 2};
+    const uint32_t box[2] = {64u, box_outer};
+    return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// bf16 [n_exp][outer][inner] array, box 64 x box_outer x 1.
+bool encode_bf16_3d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t n_exp,
+                    uint32_t box_outer) {
+    const uint64_t dims[3] = {inner, outer, n_exp};
+    const uint64_t strides[2] = {inner * 2, inner * outer * 2};
+    const uint32_t box[3] = {64u, box_outer, 1};
+    return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 }  // namespace moe

@@ -74,23 +74,29 @@ PAIR = [
     _small("switch_top1", T=640, d=256, h=512),
     _small("deepseek_fine", T=200, d=256, N=16, k=4, h=128, h_shared=192),
     _small("mixtral_prefill", T=1100, d=128, h=256, N=2, k=1),
+    # hidden sizes that are not a multiple of the 128/256-wide weight blocks
+    _small("deepseek_fine", T=333, d=192, N=12, k=3, h=320, h_shared=192),
+    _small("switch_top1", T=700, d=320, h=448, N=4),
 ]
 
 
 @pytest.mark.parametrize("w", PAIR, ids=[w.name for w in PAIR])
-def test_pair_and_single_cta_ffn_kernels(w):
-    """Both tensor-core kernels (CTA pair with 256-row tiles, single CTA with 128-row
-    tiles) match the oracle on the same inputs."""
+def test_all_tensor_core_ffn_kernels(w):
+    """The three tensor-core kernels (weights-as-M CTA pair with token tiles of 32..256,
+    row-tile CTA pair with 256-row tiles, row-tile single CTA with 128-row tiles)
+    match the oracle on the same inputs."""
     inp = W.make_inputs(w, device="cuda")
     ws = moe.workspace(cfg_of(w))
     rt = O.forward(w, oracle_inputs(inp))
     outs = {}
-    for name, flag in (("pair", moe.MOE_DEBUG_FFN_PAIR), ("single", moe.MOE_DEBUG_FFN_SINGLE)):
+    for name, flag in (("swap", moe.MOE_DEBUG_FFN_SWAP), ("pair", moe.MOE_DEBUG_FFN_PAIR),
+                       ("single", moe.MOE_DEBUG_FFN_SINGLE)):
         outs[name] = host(run_forward(cfg_of(w, debug_flags=flag), inp, ws))
         assert moe.moe_check_error(ws) == moe.MOE_OK, name
         check_routing(outs[name], rt, sep=False)
         check_output(outs[name]["y"], rt["y"], w.dtype)
     assert rel_max_err(outs["pair"]["y"], outs["single"]["y"]) <= 2e-2
+    assert rel_max_err(outs["swap"]["y"], outs["single"]["y"]) <= 2e-2
 
 
 @pytest.mark.parametrize("name", ["mixtral_prefill", "deepseek_fine"])
