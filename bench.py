@@ -18,6 +18,7 @@ Prints one JSON line on rank 0.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -112,6 +113,26 @@ def algorithmic(w, rows: int, counts_kept=None) -> dict:
         + ((w.T * hs + w.T * w.d) * es if hs else 0)
     return {"flops": p1 + p2, "flops_p1": p1, "flops_p2": p2, "bytes": bytes_,
             "bytes_p1": b1, "bytes_p2": b2, "router_flops": 2 * w.T * w.d * w.N}
+
+
+def captured_traffic(workload: str, stage: str):
+    """DRAM bytes per launch of an expert-product kernel from the committed ncu
+    capture (profiles/roofline_traffic.json), or None when there is none for this
+    workload or the kernel sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "roofline_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        h = hashlib.sha256()
+        for src in rec["sources"]:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest() != rec["sources_sha256"]:
+            return None
+        k = rec["workloads"][workload][stage]
+        return int(k["dram_read"]) + int(k["dram_write"])
+    except (OSError, KeyError, ValueError):
+        return None
 
 
 def launches_per_forward(w) -> int:
@@ -385,6 +406,7 @@ def run_ours(a, w, world, rank, local):
         p = "1" if dom == "expert_product_1" else "2"
         flops, nbytes = alg["flops_p" + p], alg["bytes_p" + p]
         sec = stage[dom] / 1e3
+        traffic = captured_traffic(w.name, dom)
         kind = ("gated" if w.act == "silu_gated" else "relu") if p == "1" else "plain"
         kernel = f"expert product {p}: k_ffn_tc2<{kind}> (CTA pair) or k_ffn_tc<{kind}>"
         # the kernel's bound is whichever floor is higher: its FLOPs at the tensor
@@ -392,14 +414,15 @@ def run_ours(a, w, world, rank, local):
         if nbytes / (peaks["hbm"] * 1e9) > flops / (peaks["bf16"] * 1e12):
             achieved = nbytes / sec / 1e9
             roof = {"kernel": kernel, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm"],
-                    "unit": "GB/s", "frac": achieved / peaks["hbm"], "traffic": None,
+                    "unit": "GB/s", "frac": achieved / peaks["hbm"], "traffic": traffic,
                     "peak_source": peaks["source"] + " HBM copy"}
         else:
             achieved = flops / sec / 1e12
             roof = {"kernel": kernel, "bound": "tensor", "achieved": achieved, "peak": peaks["bf16"],
-                    "unit": "TFLOP/s", "frac": achieved / peaks["bf16"], "traffic": None,
+                    "unit": "TFLOP/s", "frac": achieved / peaks["bf16"], "traffic": traffic,
                     "peak_source": peaks["source"] + " bf16 burst"}
         roof.update({"algorithmic_flops_per_launch": flops, "algorithmic_bytes_per_launch": nbytes,
+                     "traffic_over_algorithmic": None if traffic is None else traffic / nbytes,
                      "avg_launch_ms": stage[dom]})
     else:
         dom = "expert_product_1"

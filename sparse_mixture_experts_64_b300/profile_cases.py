@@ -1,0 +1,69 @@
+"""Small launch sequences of the C-ABI calls for profiling single kernels under ncu.
+
+Usage: python sparse_mixture_experts_64_b300/profile_cases.py CASE [--config NAME] [--reps N]
+
+  router  moe_router_topk alone (router logits, gating, expert scan, slot assignment);
+  memory  moe_router_topk, moe_dispatch and moe_combine (no shared expert) with the
+          config's activation sizes: the HBM-bound kernels without the expert weights,
+          so a DeepSeek-shaped case (0.94 GB of dispatched rows) holds about 2 GB.
+
+Inputs are seeded synthetic tensors of the config's shapes (x ~ N(0,1), router
+weight ~ N(0, 1/d), y_perm ~ N(0,1)); every launch goes through the library.
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import sys
+
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import sparse_mixture_experts_64_b300 as moe  # noqa: E402
+import workloads as W  # noqa: E402
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("case", choices=("router", "memory"))
+    ap.add_argument("--config", default="deepseek_fine", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--reps", type=int, default=4)
+    a = ap.parse_args()
+    w = W.WORKLOADS[a.config]
+    if a.case == "memory":
+        w = w.replace(h_shared=0)
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    g = torch.Generator(device="cuda").manual_seed(1)
+    x = torch.randn((w.T, w.d), device="cuda", generator=g).to(dt)
+    w_r = torch.randn((w.d, w.N), device="cuda", generator=g) / w.d ** 0.5
+    b_r = torch.randn(w.N, device="cuda", generator=g) * 0.5 ** 0.5 if w.router_bias else None
+    cfg = moe.make_config(T=w.T, d=w.d, N=w.N, k=w.k, h=w.h, h_shared=w.h_shared, dtype=w.dtype,
+                          gating=w.gating, act=w.act, capacity_factor=w.capacity_factor,
+                          router_bias=w.router_bias)
+    ws = moe.workspace(cfg)
+    T, k, N, R = w.T, w.k, w.N, moe.moe_max_rows(cfg)
+    i32 = dict(dtype=torch.int32, device="cuda")
+    idx, slot_row = torch.empty((T, k), **i32), torch.empty((T, k), **i32)
+    gate = torch.empty((T, k), device="cuda")
+    routed, kept, offsets = torch.empty(N, **i32), torch.empty(N, **i32), torch.empty(N + 1, **i32)
+    perm, aux = torch.empty(R, **i32), torch.empty(2, device="cuda")
+    if a.case == "memory":
+        x_perm = torch.empty((R, w.d), dtype=dt, device="cuda")
+        y_perm = torch.randn((R, w.d), device="cuda", generator=g).to(dt)
+        y = torch.empty((T, w.d), dtype=dt, device="cuda")
+    for _ in range(a.reps):
+        moe.moe_router_topk(cfg, x, w_r, b_r, idx, gate, routed, kept, offsets, slot_row, perm, aux, ws)
+        if a.case == "memory":
+            moe.moe_dispatch(cfg, x, perm, offsets, x_perm, ws)
+            moe.moe_combine(cfg, x, y_perm, slot_row, gate, None, None, None, y, ws)
+    st = moe.moe_check_error(ws)
+    print(f"{a.case} {w.name}: status {moe.status_str(st)}, "
+          f"{torch.cuda.max_memory_allocated() / 1e9:.2f} GB allocated")
+    if st != moe.MOE_OK:
+        sys.exit(1)
+
+
+if __name__ == "__main__":
+    main()
