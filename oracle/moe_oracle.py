@@ -27,7 +27,7 @@ Page references used below:
   [DeepSeekMoE eq] "Mixture-of-Experts (MoE)" ml-notes page, the MoE-layer equation
                    h_t = sum_i g_{i,t} FFN_i(u_t) + u_t quoted from DeepSeekMoE.
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent:
   * top-k selects by logit, descending, lower expert index first on equal values;
   * softmax-then-top-k gates are not renormalised (DeepSeekMoE eq.);
   * capacity C = ceil(T * cf / N); priority is slot-major (all first choices in
@@ -278,7 +278,11 @@ def expert_ffn(xr: np.ndarray, w_a, w_b, w_out, act: str) -> np.ndarray:
 
 def route(cfg, x, w_r, b_r=None) -> dict:
     """Router, gates, counts, capacity, aux loss and dispatch order for all tokens."""
-    L = router_logits(x, w_r, b_r)
+    return route_from_logits(cfg, router_logits(x, w_r, b_r))
+
+
+def route_from_logits(cfg, L: np.ndarray) -> dict:
+    """Everything after the router's linear layer, from the fp32 logits L [T][N]."""
     idx = select_topk(L, cfg.k)
     g = gates(L, idx, cfg.gating)
     p = softmax_all(L)
@@ -290,6 +294,51 @@ def route(cfg, x, w_r, b_r=None) -> dict:
     return dict(logits=L, topk_idx=idx, topk_gate=g, p=p, counts_routed=routed,
                 capacity=C, kept=kept, counts_kept=counts_kept, expert_offsets=offsets,
                 perm_token=perm_token, slot_row=slot_row, aux=aux)
+
+
+# ------------------------------------------------------- training-time router variants
+
+def noisy_logits(logits: np.ndarray, noise: np.ndarray, noise_weight: float) -> np.ndarray:
+    """Noisy top-k: H[t, e] = L[t, e] + W_noise * n[t, e], n ~ N(0, 1).
+
+    [Noisy top-k] "Noise Top-k Gating", opening paragraphs and the parameter list:
+    Gaussian noise of a standard normal, scaled by one scalar noise weight, is added
+    to the raw router logits before the top-k choice; at inference the weight is
+    zero. The draws n are an input (the caller samples them). The sum is taken in
+    fp32 like the logits, as two correctly rounded steps: the product W_noise * n
+    rounded to fp32, then the sum rounded to fp32, so the noisy top-k decision is
+    reproducible bit for bit.
+    """
+    L = np.asarray(logits, dtype=np.float32)
+    n = np.asarray(noise, dtype=np.float32)
+    prod = (np.float32(noise_weight) * n).astype(np.float32)
+    return (L + prod).astype(np.float32)
+
+
+def z_loss(logits: np.ndarray) -> float:
+    """Router z-loss, float64: (1/T) * sum_t (log sum_e exp L[t, e])^2.
+
+    [MoE glossary], load-balancing bullets: the z-loss penalises large router
+    logits; the pages print no formula. Reading: the square of each token's
+    log-sum-exp of its logits, averaged over tokens. It is taken on the logits of
+    the router's linear layer (bias included, noise excluded).
+    """
+    L = np.asarray(logits, dtype=np.float64)
+    m = L.max(axis=1, keepdims=True)
+    lse = m[:, 0] + np.log(np.exp(L - m).sum(axis=1))
+    return float(np.mean(lse * lse))
+
+
+def route_train(cfg, x, w_r, b_r=None, noise=None, noise_weight: float = 0.0) -> dict:
+    """Training-time router: the noisy logits H drive the selection, the gates, the
+    counts, the capacity decisions and the aux loss (softmax of H); the z-loss is
+    computed on the noiseless logits L. Without noise H = L."""
+    L = router_logits(x, w_r, b_r)
+    H = L if noise is None else noisy_logits(L, noise, noise_weight)
+    rt = route_from_logits(cfg, H)
+    rt["raw_logits"] = L
+    rt["z_loss"] = z_loss(L)
+    return rt
 
 
 def shared_expert(xr, sw_gate, sw_up, sw_down) -> np.ndarray:

@@ -376,10 +376,88 @@ def pin_dropped_tokens_are_residual(O):
     assert np.allclose(rt["y"][dropped], inp["x"][dropped] + s[dropped], rtol=1e-12, atol=1e-12)
 
 
+# ------------------------------------------------- training-time router variants
+
+def pin_noisy_logits_exact(O):
+    """H = fl(L + fl(w * n)): two correctly rounded fp32 steps, checked in exact
+    rational arithmetic; w = 0 and n = 0 leave the logits unchanged."""
+    rng = np.random.default_rng(7)
+    L = rng.standard_normal((40, 50)).astype(np.float32) * np.float32(3)
+    n = rng.standard_normal((40, 50)).astype(np.float32)
+    for w in (0.37, 1.0, 2.5e-3, 13.0):
+        H = O.noisy_logits(L, n, w)
+        w32 = float(np.float32(w))
+        for t in range(L.shape[0]):
+            for e in range(L.shape[1]):
+                prod = _round_f32(Fraction(w32) * Fraction(float(n[t, e])))
+                want = _round_f32(Fraction(float(L[t, e])) + Fraction(prod))
+                assert float(H[t, e]) == want
+    assert np.array_equal(O.noisy_logits(L, n, 0.0), L)
+    assert np.array_equal(O.noisy_logits(L, np.zeros_like(n), 5.0), L)
+
+
+def pin_noisy_selection(O):
+    """With a zero router weight every logit is 0, so the noise alone decides:
+    the top-k follow the noise in descending order (brute force), and the gates of
+    top-k-then-softmax are the softmax of the selected noise values times w."""
+    rng = np.random.default_rng(11)
+    T, d, N, k = 9, 8, 6, 3
+    cfg = O.config_from(T, d, N, k, h=4)
+    x = rng.standard_normal((T, d)).astype(np.float32)
+    w_r = np.zeros((d, N), np.float32)
+    noise = rng.standard_normal((T, N)).astype(np.float32)
+    rt = O.route_train(cfg, x, w_r, None, noise, 0.5)
+    for t in range(T):
+        order = sorted(range(N), key=lambda e: (-float(noise[t, e]), e))[:k]
+        assert list(rt["topk_idx"][t]) == order
+        v = np.array([0.5 * float(noise[t, e]) for e in order])
+        g = np.exp(v - v.max()) / np.exp(v - v.max()).sum()
+        assert np.allclose(rt["topk_gate"][t], g, rtol=1e-6, atol=1e-7)
+
+
+def pin_route_train_without_noise(O):
+    """Without noise route_train selects, gates and counts exactly as route."""
+    rng = np.random.default_rng(12)
+    cfg = O.config_from(37, 16, 5, 2, h=4, capacity_factor=(1, 1))
+    x = rng.standard_normal((37, 16)).astype(np.float32)
+    w_r = rng.standard_normal((16, 5)).astype(np.float32)
+    a = O.route(cfg, x, w_r)
+    b = O.route_train(cfg, x, w_r)
+    for key in ("topk_idx", "topk_gate", "kept", "perm_token", "slot_row", "expert_offsets"):
+        assert np.array_equal(a[key], b[key]), key
+
+
+def pin_z_loss_closed_forms(O):
+    """z = mean_t (log sum_e exp L)^2: zero logits give (ln N)^2; the two-expert
+    case [0, ln 3] gives (ln 4)^2; a per-token shift c gives mean((lse0 + c)^2);
+    random logits agree with scipy's logsumexp; noise does not enter z."""
+    for N in (1, 2, 7, 256):
+        assert math.isclose(O.z_loss(np.zeros((5, N), np.float32)), math.log(N) ** 2,
+                            rel_tol=1e-14, abs_tol=1e-15)
+    assert math.isclose(O.z_loss(np.array([[0.0, math.log(3.0)]])), math.log(4.0) ** 2, rel_tol=1e-14)
+    c = np.array([[-2.0], [0.5], [30.0]])
+    L = np.zeros((3, 4)) + c
+    assert math.isclose(O.z_loss(L), float(np.mean((math.log(4.0) + c[:, 0]) ** 2)), rel_tol=1e-13)
+    rng = np.random.default_rng(13)
+    L = rng.standard_normal((50, 9)) * 4
+    want = float(np.mean(scipy.special.logsumexp(L, axis=1) ** 2))
+    assert math.isclose(O.z_loss(L), want, rel_tol=1e-12)
+    cfg = O.config_from(20, 8, 5, 2, h=4)
+    x = rng.standard_normal((20, 8)).astype(np.float32)
+    w_r = rng.standard_normal((8, 5)).astype(np.float32)
+    noise = rng.standard_normal((20, 5)).astype(np.float32)
+    plain = O.route_train(cfg, x, w_r)
+    noisy = O.route_train(cfg, x, w_r, None, noise, 3.0)
+    assert noisy["z_loss"] == plain["z_loss"]
+    assert math.isclose(plain["z_loss"], float(np.mean(
+        scipy.special.logsumexp(plain["raw_logits"].astype(np.float64), axis=1) ** 2)), rel_tol=1e-12)
+
+
 PINS = [pin_router_logits_exact, pin_router_logits_error_bound, pin_topk_brute_force,
         pin_worked_example, pin_three_token_dispatch, pin_softmax_library, pin_aux_closed_forms,
         pin_capacity, pin_single_expert_is_dense_mlp, pin_identical_experts,
-        pin_dense_brute_force, pin_dropped_tokens_are_residual]
+        pin_dense_brute_force, pin_dropped_tokens_are_residual, pin_noisy_logits_exact,
+        pin_noisy_selection, pin_route_train_without_noise, pin_z_loss_closed_forms]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -501,6 +579,35 @@ def _mut_renormalise_softmax_gates(mp):
     mp.setattr(O, "gates", g)
 
 
+def _mut_noise_subtracted(mp):
+    real = O.noisy_logits
+    mp.setattr(O, "noisy_logits", lambda L, n, w: real(L, -np.asarray(n, np.float32), w))
+
+
+def _mut_noise_one_rounding(mp):
+    mp.setattr(O, "noisy_logits", lambda L, n, w: (np.asarray(L, np.float64) + float(np.float32(w))
+                                                   * np.asarray(n, np.float64)).astype(np.float32))
+
+
+def _mut_z_not_squared(mp):
+    def z(L):
+        L = np.asarray(L, np.float64)
+        m = L.max(axis=1, keepdims=True)
+        return float(np.mean(m[:, 0] + np.log(np.exp(L - m).sum(axis=1))))
+    mp.setattr(O, "z_loss", z)
+
+
+def _mut_z_on_noisy_logits(mp):
+    def rt(cfg, x, w_r, b_r=None, noise=None, noise_weight=0.0):
+        L = O.router_logits(x, w_r, b_r)
+        H = L if noise is None else O.noisy_logits(L, noise, noise_weight)
+        out = O.route_from_logits(cfg, H)
+        out["raw_logits"] = L
+        out["z_loss"] = O.z_loss(H)
+        return out
+    mp.setattr(O, "route_train", rt)
+
+
 MUTATIONS = [
     (_mut_tie_high_index, pin_topk_brute_force),
     (_mut_swap_gating, pin_worked_example),
@@ -514,6 +621,10 @@ MUTATIONS = [
     (_mut_butterfly_ascending, pin_router_logits_exact),
     (_mut_capacity_floor, pin_capacity),
     (_mut_renormalise_softmax_gates, pin_softmax_library),
+    (_mut_noise_subtracted, pin_noisy_selection),
+    (_mut_noise_one_rounding, pin_noisy_logits_exact),
+    (_mut_z_not_squared, pin_z_loss_closed_forms),
+    (_mut_z_on_noisy_logits, pin_z_loss_closed_forms),
 ]
 
 
