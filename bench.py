@@ -55,6 +55,8 @@ def _args():
                     help="tokens whose outputs the CPU oracle computes for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip the training-router variant timing")
     return ap.parse_args()
 
 
@@ -292,6 +294,69 @@ def run_reference(a, w, world, rank):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------- router variant legs
+
+def _time_calls(fn, stream, iters: int, warmup: int = 3) -> float:
+    """Mean ms of fn() over `iters` back-to-back calls, CUDA events on `stream`."""
+    for _ in range(warmup):
+        fn()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(iters):
+        fn()
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / iters
+
+
+def measure_router_train(w, inp, cfg, ws, stream, dev, cpu_tokens: int) -> dict:
+    """Training-time router (noisy top-k + z-loss) against the inference router on
+    the same inputs: CUDA-event times, the logits' share of the fp32 FMA peak, and
+    the oracle's training router timed on a token sample of the host cores."""
+    import sparse_mixture_experts_64_b300 as moe
+    T, k, N = w.T, w.k, w.N
+    g = torch.Generator(device=dev).manual_seed(77)
+    noise = torch.randn((T, N), device=dev, generator=g)
+    i32 = dict(dtype=torch.int32, device=dev)
+    o = [torch.empty((T, k), **i32), torch.empty((T, k), device=dev), torch.empty(N, **i32),
+         torch.empty(N, **i32), torch.empty(N + 1, **i32), torch.empty((T, k), **i32),
+         torch.empty(moe.moe_max_rows(cfg), **i32), torch.empty(2, device=dev)]
+    z = torch.empty(1, device=dev)
+
+    def infer():
+        moe.moe_router_topk(cfg, inp["x"], inp["w_r"], inp["b_r"], *o, ws, stream)
+
+    def train():
+        moe.moe_router_topk_train(cfg, inp["x"], inp["w_r"], inp["b_r"], noise, 1.0, *o[:7], o[7],
+                                  z, ws, stream)
+    iters = 20
+    ms_inf = _time_calls(infer, stream, iters)
+    ms_train = _time_calls(train, stream, iters)
+    st = moe.moe_check_error(ws, stream)
+    if st != moe.MOE_OK:
+        raise RuntimeError("device error word: " + moe.status_str(st))
+    fma_peak = 148 * 128 * 2 * 2.032e9
+    flops = 2.0 * T * w.d * N
+    out = {"train_ms": ms_train, "inference_ms": ms_inf, "overhead_ms": ms_train - ms_inf,
+           "router_flops_fp32": flops, "bound": "alu",
+           "frac": flops / (ms_train / 1e3) / fma_peak,
+           "peak": "148 SMs x 128 FP32 lanes x 2 x 2032 MHz (fp32 FMA, logits only)"}
+    if cpu_tokens > 0:
+        from oracle import moe_oracle as O
+        n = min(T, cpu_tokens)
+        ws_ = w.replace(T=n)
+        xs = inp["x"][:n].float().cpu().numpy()
+        t0 = time.perf_counter()
+        O.route_train(ws_, xs, inp["w_r"].cpu().numpy(),
+                      None if inp["b_r"] is None else inp["b_r"].cpu().numpy(),
+                      noise[:n].cpu().numpy(), 1.0)
+        secs = time.perf_counter() - t0
+        out["cpu_oracle"] = {"tokens_per_s": n / secs, "sample_tokens": n, "cores": 1,
+                             "kind": "oracle"}
+    return out
+
+
 # ------------------------------------------------------------------------ GPU arm
 
 def run_ours(a, w, world, rank, local):
@@ -456,6 +521,11 @@ def run_ours(a, w, world, rank, local):
         "gpu_launches": launches_per_forward(w) * a.steps,
         "clocks": clk, "wall_s_timed": wall,
     }
+
+    # ---- training-time router variant (noisy top-k + z-loss), same inputs
+    if not a.no_variants:
+        line["variants"] = {"router_train": measure_router_train(
+            w, inp, cfg, ws, stream, dev, 0 if (a.no_cpu_baseline or rank != 0) else 512)}
 
     # ---- CPU oracle baseline (rank 0, single process only)
     if rank == 0 and world == 1 and not a.no_cpu_baseline:

@@ -152,6 +152,30 @@ moe_status moe_router_topk(const moe_config *cfg, const void *x, const float *w_
                            float *aux, void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * Training-time router: moe_router_topk with noisy top-k gating and the router
+ * z-loss ("Noise Top-k Gating" page: standard-normal noise, scaled by one scalar
+ * noise weight, is added to the raw logits before the top-k choice and is off at
+ * inference; "Mixture of Experts (MoE)" glossary: a z-loss penalises large router
+ * logits).
+ *   noise        fp32 [T][N] standard-normal draws n (sampled by the caller), or NULL
+ *                for no noise. The router then works on H = fl(L + fl(w * n)) (the
+ *                product and the sum each rounded to fp32): selection, gates,
+ *                counts, capacity and aux all use H.
+ *   noise_weight the scalar w; must be finite when noise is given.
+ *   z_loss       fp32 [1] or NULL: (1/T) sum_t (log sum_e exp L[t,e])^2 on the
+ *                noiseless logits L (bias included). The pages print no formula;
+ *                this is the reading used.
+ * Every other argument, output and error as moe_router_topk. With noise == NULL
+ * and z_loss == NULL the results are those of moe_router_topk, bit for bit.
+ */
+moe_status moe_router_topk_train(const moe_config *cfg, const void *x, const float *w_r,
+                                 const float *b_r, const float *noise, float noise_weight,
+                                 int32_t *topk_idx, float *topk_gate, int32_t *counts_routed,
+                                 int32_t *counts_kept, int32_t *expert_offsets, int32_t *slot_row,
+                                 int32_t *perm_token, float *aux, float *z_loss, void *ws,
+                                 size_t ws_bytes, cudaStream_t stream);
+
+/*
  * moe_router_topk for callers that cannot allocate device memory. The paper has
  * no counterpart to this call; it exists for hosts that forbid allocation after
  * start-up (engines that plan all device memory ahead and call plugins from an

@@ -29,7 +29,8 @@ MOE_DEBUG_FFN_SWAP = 8
 
 EXPORTED = ("moe_validate_config", "moe_workspace_size", "moe_max_rows", "moe_capacity",
             "moe_router_topk", "moe_dispatch", "moe_grouped_ffn", "moe_combine", "moe_forward",
-            "moe_forward_profiled", "moe_check_error", "moe_status_str", "moe_router_topk_noalloc")
+            "moe_forward_profiled", "moe_check_error", "moe_status_str", "moe_router_topk_noalloc",
+            "moe_router_topk_train")
 
 
 class moe_config(ctypes.Structure):
@@ -59,6 +60,7 @@ def _load() -> ctypes.CDLL:
         "moe_capacity": (I32, [cfgp]),
         "moe_router_topk": (I32, [cfgp] + [P] * 11 + [P, SZ, P]),
         "moe_router_topk_noalloc": (I32, [cfgp] + [P] * 11 + [P]),
+        "moe_router_topk_train": (I32, [cfgp, P, P, P, P, ctypes.c_float] + [P] * 9 + [P, SZ, P]),
         "moe_dispatch": (I32, [cfgp, P, P, P, P, P, SZ, P]),
         "moe_grouped_ffn": (I32, [cfgp, P, P, P, P, P, P, P, SZ, P]),
         "moe_combine": (I32, [cfgp, P, P, P, P, P, P, P, P, P, SZ, P]),
@@ -153,6 +155,20 @@ def moe_router_topk(cfg, x, w_r, b_r, topk_idx, topk_gate, counts_routed, counts
                                 _p(expert_offsets), _p(slot_row), _p(perm_token), _p(aux),
                                 _p(ws), ws.numel() if ws is not None else 0, _stream(stream)),
            "moe_router_topk")
+
+
+def moe_router_topk_train(cfg, x, w_r, b_r, noise, noise_weight, topk_idx, topk_gate,
+                          counts_routed, counts_kept, expert_offsets, slot_row, perm_token, aux,
+                          z_loss, ws, stream=None):
+    """moe_router_topk with noisy top-k gating (noise: fp32 [T][N] standard-normal
+    draws or None, scaled by noise_weight) and the router z-loss (z_loss: fp32 [1] or
+    None)."""
+    _check(_lib.moe_router_topk_train(ctypes.byref(cfg), _p(x), _p(w_r), _p(b_r), _p(noise),
+                                      float(noise_weight), _p(topk_idx), _p(topk_gate),
+                                      _p(counts_routed), _p(counts_kept), _p(expert_offsets),
+                                      _p(slot_row), _p(perm_token), _p(aux), _p(z_loss), _p(ws),
+                                      ws.numel() if ws is not None else 0, _stream(stream)),
+           "moe_router_topk_train")
 
 
 def moe_router_topk_noalloc(cfg, x, w_r, b_r, topk_idx, topk_gate, counts_routed, counts_kept,

@@ -33,6 +33,7 @@ struct WsLayout {
     size_t kpre;                 // int32 [N][tiles]
     size_t psum;                 // f32   [N][tiles]
     size_t pmean;                // f32   [N]
+    size_t zpart;                // f32   [tiles] per-tile sums of the z-loss terms
     size_t routed, kept;         // int32 [N] (used when the caller passes NULL)
     size_t logits;               // f32   [T][N]  (N > 32 only)
     size_t w_t;                  // f32   [ceil(d/256)][N][256]  router weight, re-laid out
@@ -55,6 +56,11 @@ struct RouterOut {
     float *topk_gate;
     int32_t *counts_routed, *counts_kept, *expert_offsets, *slot_row, *perm_token;
     float *aux;
+    // training-time router (null / 0 for inference): noise draws [T][N] and their
+    // weight (noisy top-k), and the z-loss output [1]
+    const float *noise = nullptr;
+    float noise_w = 0.0f;
+    float *z_loss = nullptr;
 };
 cudaError_t launch_router(const moe_config &c, const void *x, const float *w_r, const float *b_r,
                           const RouterOut &o, uint8_t *ws, cudaStream_t s);

@@ -4,6 +4,7 @@
 // Each Token", section "From Router to Combine"; see include/moe.h for each
 // call's contract.
 #include <algorithm>
+#include <cmath>
 #include <cstring>
 
 #include "internal.h"
@@ -45,6 +46,7 @@ WsLayout ws_layout(const moe_config &c) {
     L.kpre = take(N * tiles * 4);
     L.psum = take(N * tiles * 4);
     L.pmean = take(N * 4);
+    L.zpart = take(tiles * 4);
     L.routed = take(N * 4);
     L.kept = take(N * 4);
     L.logits = take(c.N > 32 ? T * N * 4 : 0);
@@ -154,6 +156,29 @@ moe_status moe_router_topk(const moe_config *cfg, const void *x, const float *w_
     const WsLayout L = ws_layout(c);
     if ((st = check_ws(ws, ws_bytes, L.hid)) != MOE_OK) return st;
     RouterOut o{topk_idx, topk_gate, counts_routed, counts_kept, expert_offsets, slot_row, perm_token, aux};
+    return to_status(launch_router(c, x, w_r, c.has_router_bias ? b_r : nullptr, o,
+                                   static_cast<uint8_t *>(ws), stream));
+}
+
+moe_status moe_router_topk_train(const moe_config *cfg, const void *x, const float *w_r, const float *b_r,
+                                 const float *noise, float noise_weight, int32_t *topk_idx, float *topk_gate,
+                                 int32_t *counts_routed, int32_t *counts_kept, int32_t *expert_offsets,
+                                 int32_t *slot_row, int32_t *perm_token, float *aux, float *z_loss, void *ws,
+                                 size_t ws_bytes, cudaStream_t stream) {
+    moe_status st = validate(cfg);
+    if (st != MOE_OK) return st;
+    const moe_config &c = *cfg;
+    if (!x || !w_r || !topk_idx || !topk_gate || !expert_offsets || !slot_row || !perm_token)
+        return MOE_ERR_INVALID_ARG;
+    if (c.has_router_bias && !b_r) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w_r)) return MOE_ERR_INVALID_ARG;
+    if (noise && !std::isfinite(noise_weight)) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(c);
+    if ((st = check_ws(ws, ws_bytes, L.hid)) != MOE_OK) return st;
+    RouterOut o{topk_idx, topk_gate, counts_routed, counts_kept, expert_offsets, slot_row, perm_token, aux};
+    o.noise = noise;
+    o.noise_w = noise ? noise_weight : 0.0f;
+    o.z_loss = z_loss;
     return to_status(launch_router(c, x, w_r, c.has_router_bias ? b_r : nullptr, o,
                                    static_cast<uint8_t *>(ws), stream));
 }

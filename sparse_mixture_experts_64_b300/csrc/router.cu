@@ -61,6 +61,11 @@ struct RouterArgs {
     int32_t *cnt;   // [N][k][tiles]
     float *psum;    // [N][tiles]
     uint32_t *err;  // device error word
+    // training-time router: noise draws [T][N] (null: none) and their weight; per-tile
+    // sums of the z-loss terms (null: no z-loss)
+    const float *noise = nullptr;
+    float noise_w = 0.0f;
+    float *zpart = nullptr;
 };
 
 // 8 consecutive features of one token as fp32 (16 bytes of bf16, 32 of fp32).
@@ -265,6 +270,48 @@ __device__ __forceinline__ void gate_tokens_warp(float *Ls, int *Is, const Route
     }
 }
 
+__device__ __forceinline__ float warp_max_bcast(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return __shfl_sync(0xffffffffu, v, 0);
+}
+
+// Training-time step between the logits and the gating ("Noise Top-k Gating":
+// noise is added to the raw logits before the top-k choice), one warp per token of
+// the tile; called by every thread of the CTA when a.noise or a.zpart is set.
+//   z-loss: the token's (log sum_e exp L)^2 on the noiseless logits; the tile's sum,
+//           in token order, goes to zpart[tile];
+//   noise:  L <- fl(L + fl(w * n)), the product and the sum each rounded to fp32.
+constexpr int kMaxTileTokens = 64;
+__device__ void train_step(float *Ls, const RouterArgs &a, int TT) {
+    __shared__ float zs[kMaxTileTokens];
+    const int N = a.N, lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int t0 = blockIdx.x * TT;
+    const int nrows = min(TT, a.T - t0);
+    for (int tok = warp; tok < nrows; tok += nw) {
+        float *L = Ls + tok * N;
+        if (a.zpart) {
+            float m = -INFINITY;
+            for (int e = lane; e < N; e += 32) m = fmaxf(m, L[e]);
+            m = warp_max_bcast(m);
+            float part = 0.0f;
+            for (int e = lane; e < N; e += 32) part += expf(L[e] - m);
+            const float lse = m + logf(warp_sum_bcast(part));
+            if (lane == 0) zs[tok] = lse * lse;
+        }
+        if (a.noise) {
+            const float *n = a.noise + (size_t)(t0 + tok) * N;
+            for (int e = lane; e < N; e += 32) L[e] = __fadd_rn(L[e], __fmul_rn(a.noise_w, n[e]));
+        }
+    }
+    __syncthreads();
+    if (a.zpart && threadIdx.x == 0) {
+        float sum = 0.0f;
+        for (int tok = 0; tok < nrows; ++tok) sum += zs[tok];
+        a.zpart[blockIdx.x] = sum;
+    }
+}
+
 // ------------------------------------------------------------------ pipeline
 
 // Ring of STAGES staging slots between one producer warp (bulk copies) and NC
@@ -432,6 +479,7 @@ __global__ void __launch_bounds__(160) k_router_small(const __grid_constant__ CU
             }
     }
     __syncthreads();
+    if (a.noise || a.zpart) train_step(Ls, a, TT);
     gate_tokens_thread<NP>(Ls, Is, a, TT);
     __syncthreads();
     tile_stats(Ls, Is, a, TT);
@@ -543,6 +591,10 @@ __global__ void __launch_bounds__(256) k_gate(const float *__restrict__ logits, 
     const int nrows = min(TT, a.T - t0);
     for (int i = threadIdx.x; i < nrows * a.N; i += blockDim.x) Ls[i] = logits[(size_t)t0 * a.N + i];
     __syncthreads();
+    if (a.noise || a.zpart) {
+        train_step(Ls, a, TT);
+        __syncthreads();
+    }
     gate_tokens_warp(Ls, Is, a, TT);
     __syncthreads();
     tile_stats(Ls, Is, a, TT);
@@ -671,6 +723,8 @@ struct AssignArgs {
     int32_t *slot_row, *perm_token;
     float *aux;            // may be null
     uint32_t *err;
+    const float *zpart = nullptr;  // [tiles] z-loss tile sums (with z_out)
+    float *z_out = nullptr;        // [1] may be null
 };
 
 __global__ void __launch_bounds__(256) k_assign(AssignArgs a) {
@@ -709,6 +763,11 @@ __global__ void __launch_bounds__(256) k_assign(AssignArgs a) {
             a.aux[0] = (float)N * s0;
             a.aux[1] = s1 * invN;
         }
+    }
+    if (tile == 0 && a.z_out && tid == 0) {
+        float z = 0.0f;  // tile sums in tile order
+        for (int tl = 0; tl < a.tiles; ++tl) z += a.zpart[tl];
+        a.z_out[0] = z / (float)a.T;
     }
 
     for (int s = tid; s < a.TT * 8; s += nt) {
@@ -831,8 +890,9 @@ cudaError_t launch_router(const moe_config &c, const void *x, const float *w_r, 
     int32_t *routed = o.counts_routed ? o.counts_routed : reinterpret_cast<int32_t *>(ws + L.routed);
     int32_t *kept = o.counts_kept ? o.counts_kept : reinterpret_cast<int32_t *>(ws + L.kept);
 
+    float *zpart = o.z_loss ? reinterpret_cast<float *>(ws + L.zpart) : nullptr;
     RouterArgs ra{c.T, c.d, c.N, c.k, c.gating, tiles, c.has_router_bias ? 1 : 0,
-                  o.topk_idx, o.topk_gate, cnt, psum, err};
+                  o.topk_idx, o.topk_gate, cnt, psum, err, o.noise, o.noise_w, zpart};
     cudaError_t e;
     if (c.dtype == MOE_BF16)
         e = launch_logits_gate<__nv_bfloat16>(c, static_cast<const __nv_bfloat16 *>(x), w_r, b_r, ra, logits, w_t, s);
@@ -847,7 +907,7 @@ cudaError_t launch_router(const moe_config &c, const void *x, const float *w_r, 
 
     const int TT = router_tile_tokens(c);
     AssignArgs aa{c.T, c.N, c.k, tiles, TT, cap, max_rows(c), o.topk_idx, pre, kpre, routed, kept,
-                  pmean, o.expert_offsets, o.slot_row, o.perm_token, o.aux, err};
+                  pmean, o.expert_offsets, o.slot_row, o.perm_token, o.aux, err, zpart, o.z_loss};
     const size_t sbytes = (size_t)(c.N + 1 + 2 * TT * 8) * sizeof(int);
     k_assign<<<tiles, 256, sbytes, s>>>(aa);
     return cudaGetLastError();

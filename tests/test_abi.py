@@ -108,6 +108,14 @@ def test_null_pointers_rejected_before_launch():
     # misaligned activation pointer
     st = _raw("moe_dispatch", cp, FAKE + 2, FAKE, FAKE, FAKE, None, 0, None)
     assert st == moe.MOE_ERR_INVALID_ARG
+    # training router: a non-finite noise weight with noise, a missing output
+    for wn in (float("nan"), float("inf")):
+        st = _raw("moe_router_topk_train", cp, FAKE, FAKE, None, FAKE, wn, FAKE, FAKE, None, None,
+                  FAKE, FAKE, FAKE, None, None, FAKE, ws, None)
+        assert st == moe.MOE_ERR_INVALID_ARG
+    st = _raw("moe_router_topk_train", cp, FAKE, FAKE, None, None, 0.0, None, FAKE, None, None,
+              FAKE, FAKE, FAKE, None, FAKE, FAKE, ws, None)
+    assert st == moe.MOE_ERR_INVALID_ARG
 
 
 def test_workspace_checks_before_launch():
@@ -121,6 +129,8 @@ def test_workspace_checks_before_launch():
     assert _raw("moe_forward", cp, *args, FAKE + 16, ws, None) == moe.MOE_ERR_WORKSPACE
     assert _raw("moe_router_topk", cp, FAKE, FAKE, None, FAKE, FAKE, None, None, FAKE, FAKE, FAKE,
                 None, FAKE, 16, None) == moe.MOE_ERR_WORKSPACE
+    assert _raw("moe_router_topk_train", cp, FAKE, FAKE, None, None, 0.0, FAKE, FAKE, None, None,
+                FAKE, FAKE, FAKE, None, FAKE, FAKE, 16, None) == moe.MOE_ERR_WORKSPACE
     assert _raw("moe_check_error", None, None) == moe.MOE_ERR_WORKSPACE
 
 

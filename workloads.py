@@ -92,8 +92,10 @@ def _normal(shape, std, seed, device, out_dtype, chunk_dim0=False):
     return out
 
 
-def make_inputs(w: Workload, device="cpu", seed_family: int | None = None) -> dict:
+def make_inputs(w: Workload, device="cpu", seed_family: int | None = None,
+                router_only: bool = False) -> dict:
     """All inputs of one layer forward for workload `w`, on `device`.
+    router_only: only x, w_r and b_r (the same values); the weight entries are None.
 
     Returns a dict of torch tensors:
       x [T][d] (dtype of w), w_r [d][N] fp32, b_r [N] fp32 or None,
@@ -109,6 +111,10 @@ def make_inputs(w: Workload, device="cpu", seed_family: int | None = None) -> di
     inp["w_r"] = _normal((w.d, w.N), 1.0 / math.sqrt(w.d), s + 1, device, torch.float32)
     inp["b_r"] = (_normal((w.N,), math.sqrt(0.5), s + 2, device, torch.float32)
                   if w.router_bias else None)
+    if router_only:
+        for n in ("w_gate", "w_up", "w_down", "shared_w_gate", "shared_w_up", "shared_w_down"):
+            inp[n] = None
+        return inp
     inp["w_gate"] = _normal((w.N, w.h, w.d), 1.0 / math.sqrt(w.d), s + 3, device, dt, True)
     inp["w_up"] = (_normal((w.N, w.h, w.d), 1.0 / math.sqrt(w.d), s + 4, device, dt, True)
                    if w.act == "silu_gated" else None)
