@@ -176,6 +176,49 @@ moe_status moe_router_topk_train(const moe_config *cfg, const void *x, const flo
                                  size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * Token-sharded router (one batch split over R ranks in token order: rank 0 holds
+ * the first tokens). The capacity rule is global ("Mixture of Experts (MoE)"
+ * glossary, capacity-factor paragraph; GShard top-2 in its sparse-MoE list): the
+ * first C selections of each expert in priority order are kept, priority being
+ * slot-major over the whole batch (every token's first choice in token order, then
+ * every second choice, ...). Each rank runs the two phases below on its own tokens
+ * with its own workspace; between them the ranks exchange, per expert and slot,
+ * their selection counts (and, for the aux loss, per expert the sums of the
+ * softmax). cfg describes this rank's shard: T = its tokens, cap_num = cap_den = 0
+ * (the global capacity is an argument of phase 2), everything else as for the
+ * whole batch.
+ *
+ * Phase 1: logits, gating (topk_idx, topk_gate as in moe_router_topk) and
+ *   slot_counts int32 [N][k]  selections of expert e in slot j on this rank;
+ *   prob_sums   fp32  [N]     sum over this rank's tokens of softmax_e, or NULL.
+ * The workspace keeps per-tile counts that phase 2 reads: pass the same ws.
+ */
+moe_status moe_router_shard_stats(const moe_config *cfg, const void *x, const float *w_r,
+                                  const float *b_r, int32_t *topk_idx, float *topk_gate,
+                                  int32_t *slot_counts, float *prob_sums, void *ws,
+                                  size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Phase 2: capacity decisions and dispatch order of this rank's selections.
+ *   slot_base        int32 [N][k] (device) global priority of this rank's first
+ *                    selection of (e, j): sum over slots j' < j of all ranks' counts
+ *                    of (e, j'), plus the counts of (e, j) on ranks before this one;
+ *   capacity         global C (0: no limit), e.g. ceil(T_global * cf / N);
+ *   global_routed    int32 [N], global_prob_sums fp32 [N], global_T: the sums over all
+ *                    ranks, for aux (both may be NULL when aux is NULL);
+ *   topk_idx         this rank's selections from phase 1.
+ * Outputs as in moe_router_topk for this rank's tokens: counts_kept (may be NULL),
+ * expert_offsets, slot_row, perm_token, and aux [2] (or NULL) computed from the
+ * global statistics, so every rank gets the batch's aux loss.
+ */
+moe_status moe_router_shard_assign(const moe_config *cfg, const int32_t *topk_idx,
+                                   const int32_t *slot_base, int32_t capacity,
+                                   const int32_t *global_routed, const float *global_prob_sums,
+                                   int64_t global_T, int32_t *counts_kept, int32_t *expert_offsets,
+                                   int32_t *slot_row, int32_t *perm_token, float *aux, void *ws,
+                                   size_t ws_bytes, cudaStream_t stream);
+
+/*
  * moe_router_topk for callers that cannot allocate device memory. The paper has
  * no counterpart to this call; it exists for hosts that forbid allocation after
  * start-up (engines that plan all device memory ahead and call plugins from an

@@ -30,7 +30,7 @@ MOE_DEBUG_FFN_SWAP = 8
 EXPORTED = ("moe_validate_config", "moe_workspace_size", "moe_max_rows", "moe_capacity",
             "moe_router_topk", "moe_dispatch", "moe_grouped_ffn", "moe_combine", "moe_forward",
             "moe_forward_profiled", "moe_check_error", "moe_status_str", "moe_router_topk_noalloc",
-            "moe_router_topk_train")
+            "moe_router_topk_train", "moe_router_shard_stats", "moe_router_shard_assign")
 
 
 class moe_config(ctypes.Structure):
@@ -61,6 +61,8 @@ def _load() -> ctypes.CDLL:
         "moe_router_topk": (I32, [cfgp] + [P] * 11 + [P, SZ, P]),
         "moe_router_topk_noalloc": (I32, [cfgp] + [P] * 11 + [P]),
         "moe_router_topk_train": (I32, [cfgp, P, P, P, P, ctypes.c_float] + [P] * 9 + [P, SZ, P]),
+        "moe_router_shard_stats": (I32, [cfgp] + [P] * 7 + [P, SZ, P]),
+        "moe_router_shard_assign": (I32, [cfgp, P, P, I32, P, P, I64] + [P] * 5 + [P, SZ, P]),
         "moe_dispatch": (I32, [cfgp, P, P, P, P, P, SZ, P]),
         "moe_grouped_ffn": (I32, [cfgp, P, P, P, P, P, P, P, SZ, P]),
         "moe_combine": (I32, [cfgp, P, P, P, P, P, P, P, P, P, SZ, P]),
@@ -169,6 +171,29 @@ def moe_router_topk_train(cfg, x, w_r, b_r, noise, noise_weight, topk_idx, topk_
                                       _p(slot_row), _p(perm_token), _p(aux), _p(z_loss), _p(ws),
                                       ws.numel() if ws is not None else 0, _stream(stream)),
            "moe_router_topk_train")
+
+
+def moe_router_shard_stats(cfg, x, w_r, b_r, topk_idx, topk_gate, slot_counts, prob_sums, ws,
+                           stream=None):
+    """Token-sharded router, phase 1 (see sharded.py): this rank's routing and its
+    per-(expert, slot) selection counts [N][k] and softmax sums [N]."""
+    _check(_lib.moe_router_shard_stats(ctypes.byref(cfg), _p(x), _p(w_r), _p(b_r), _p(topk_idx),
+                                       _p(topk_gate), _p(slot_counts), _p(prob_sums), _p(ws),
+                                       ws.numel() if ws is not None else 0, _stream(stream)),
+           "moe_router_shard_stats")
+
+
+def moe_router_shard_assign(cfg, topk_idx, slot_base, capacity, global_routed, global_prob_sums,
+                            global_T, counts_kept, expert_offsets, slot_row, perm_token, aux, ws,
+                            stream=None):
+    """Token-sharded router, phase 2: capacity decisions at the global priorities
+    slot_base [N][k], dispatch order of this rank's selections, global aux."""
+    _check(_lib.moe_router_shard_assign(ctypes.byref(cfg), _p(topk_idx), _p(slot_base),
+                                        int(capacity), _p(global_routed), _p(global_prob_sums),
+                                        int(global_T), _p(counts_kept), _p(expert_offsets),
+                                        _p(slot_row), _p(perm_token), _p(aux), _p(ws),
+                                        ws.numel() if ws is not None else 0, _stream(stream)),
+           "moe_router_shard_assign")
 
 
 def moe_router_topk_noalloc(cfg, x, w_r, b_r, topk_idx, topk_gate, counts_routed, counts_kept,

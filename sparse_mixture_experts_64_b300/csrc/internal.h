@@ -64,6 +64,16 @@ struct RouterOut {
 };
 cudaError_t launch_router(const moe_config &c, const void *x, const float *w_r, const float *b_r,
                           const RouterOut &o, uint8_t *ws, cudaStream_t s);
+// Token-sharded router, phase 1: routing of this shard and the statistics the
+// shards exchange (selections per expert and slot, sums of the softmax).
+cudaError_t launch_router_stats(const moe_config &c, const void *x, const float *w_r, const float *b_r,
+                                int32_t *topk_idx, float *topk_gate, int32_t *slot_counts, float *prob_sums,
+                                uint8_t *ws, cudaStream_t s);
+// Phase 2: capacity decisions at global priorities, dispatch order, global aux.
+cudaError_t launch_router_assign(const moe_config &c, const int32_t *topk_idx, const int32_t *slot_base, int32_t cap,
+                                 const int32_t *g_routed, const float *g_psum, float g_T, int32_t *counts_kept,
+                                 int32_t *expert_offsets, int32_t *slot_row, int32_t *perm_token, float *aux,
+                                 uint8_t *ws, cudaStream_t s);
 
 cudaError_t launch_dispatch(const moe_config &c, const void *x, const int32_t *perm_token,
                             const int32_t *offsets, void *x_perm, uint32_t *err, cudaStream_t s);

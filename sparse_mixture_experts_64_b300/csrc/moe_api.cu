@@ -183,6 +183,42 @@ moe_status moe_router_topk_train(const moe_config *cfg, const void *x, const flo
                                    static_cast<uint8_t *>(ws), stream));
 }
 
+moe_status moe_router_shard_stats(const moe_config *cfg, const void *x, const float *w_r, const float *b_r,
+                                  int32_t *topk_idx, float *topk_gate, int32_t *slot_counts, float *prob_sums,
+                                  void *ws, size_t ws_bytes, cudaStream_t stream) {
+    moe_status st = validate(cfg);
+    if (st != MOE_OK) return st;
+    const moe_config &c = *cfg;
+    if (c.cap_num != 0 || c.cap_den != 0) return MOE_ERR_INVALID_ARG;  // the capacity is global
+    if (!x || !w_r || !topk_idx || !topk_gate || !slot_counts) return MOE_ERR_INVALID_ARG;
+    if (c.has_router_bias && !b_r) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w_r)) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(c);
+    if ((st = check_ws(ws, ws_bytes, L.hid)) != MOE_OK) return st;
+    return to_status(launch_router_stats(c, x, w_r, c.has_router_bias ? b_r : nullptr, topk_idx, topk_gate,
+                                         slot_counts, prob_sums, static_cast<uint8_t *>(ws), stream));
+}
+
+moe_status moe_router_shard_assign(const moe_config *cfg, const int32_t *topk_idx, const int32_t *slot_base,
+                                   int32_t capacity, const int32_t *global_routed, const float *global_prob_sums,
+                                   int64_t global_T, int32_t *counts_kept, int32_t *expert_offsets,
+                                   int32_t *slot_row, int32_t *perm_token, float *aux, void *ws,
+                                   size_t ws_bytes, cudaStream_t stream) {
+    moe_status st = validate(cfg);
+    if (st != MOE_OK) return st;
+    const moe_config &c = *cfg;
+    if (c.cap_num != 0 || c.cap_den != 0) return MOE_ERR_INVALID_ARG;
+    if (!topk_idx || !slot_base || !expert_offsets || !slot_row || !perm_token) return MOE_ERR_INVALID_ARG;
+    if (capacity < 0 || global_T < c.T) return MOE_ERR_INVALID_ARG;
+    if (aux && (!global_routed || !global_prob_sums)) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(c);
+    if ((st = check_ws(ws, ws_bytes, L.hid)) != MOE_OK) return st;
+    return to_status(launch_router_assign(c, topk_idx, slot_base, capacity, aux ? global_routed : nullptr,
+                                          aux ? global_prob_sums : nullptr, (float)global_T, counts_kept,
+                                          expert_offsets, slot_row, perm_token, aux, static_cast<uint8_t *>(ws),
+                                          stream));
+}
+
 moe_status moe_dispatch(const moe_config *cfg, const void *x, const int32_t *perm_token,
                         const int32_t *expert_offsets, void *x_perm, void *ws, size_t ws_bytes,
                         cudaStream_t stream) {

@@ -658,6 +658,13 @@ struct ScanArgs {
     const float *psum;        // [N][tiles]
     float *pmean;             // [N]
     int32_t *routed, *kept;   // [N]
+    // token-sharded router: slot_base [N][k] = global priority of this shard's first
+    // selection of (expert, slot) (null: this batch is the whole batch); stats_only:
+    // write slot_counts [N][k] and prob_sums [N] and stop before the capacity step
+    const int32_t *slot_base = nullptr;
+    int stats_only = 0;
+    int32_t *slot_counts = nullptr;
+    float *prob_sums = nullptr;
 };
 
 __global__ void __launch_bounds__(256) k_expert_scan(ScanArgs a) {
@@ -681,6 +688,31 @@ __global__ void __launch_bounds__(256) k_expert_scan(ScanArgs a) {
         run += ce[i];
     }
     __syncthreads();
+
+    // per-slot totals (the prefix at each slot's first tile) and, for a shard, the
+    // move from this batch's priorities to the global ones
+    __shared__ int slot_first[9];
+    if (tid < a.k) slot_first[tid] = pe[tid * a.tiles];
+    if (tid == 0) slot_first[a.k] = total;
+    __syncthreads();
+    if (a.slot_counts && tid < a.k) a.slot_counts[(size_t)e * a.k + tid] = slot_first[tid + 1] - slot_first[tid];
+    if (a.stats_only) {
+        float ps = 0.0f;
+        for (int tl = tid; tl < a.tiles; tl += nt) ps += a.psum[(size_t)e * a.tiles + tl];
+        const float psum = block_sum(ps, shf);
+        if (tid == 0) {
+            a.routed[e] = total;
+            if (a.prob_sums) a.prob_sums[e] = psum;
+        }
+        return;
+    }
+    if (a.slot_base) {
+        for (int i = beg; i < end; ++i) {
+            const int j = i / a.tiles;
+            pe[i] += a.slot_base[(size_t)e * a.k + j] - slot_first[j];
+        }
+        __syncthreads();
+    }
 
     // 2) kept slots per tile, exclusive prefix over tiles
     const int per2 = (a.tiles + nt - 1) / nt;
@@ -725,6 +757,10 @@ struct AssignArgs {
     uint32_t *err;
     const float *zpart = nullptr;  // [tiles] z-loss tile sums (with z_out)
     float *z_out = nullptr;        // [1] may be null
+    // token-sharded router: aux from the global statistics of all shards
+    const int32_t *g_routed = nullptr;  // [N] selections per expert, all shards
+    const float *g_psum = nullptr;      // [N] sum over all tokens of softmax
+    float g_T = 0.0f;                   // tokens of all shards
 };
 
 __global__ void __launch_bounds__(256) k_assign(AssignArgs a) {
@@ -753,8 +789,11 @@ __global__ void __launch_bounds__(256) k_assign(AssignArgs a) {
         const float invN = 1.0f / (float)N;
         float f0 = 0.0f, f1 = 0.0f;
         if (tid < N) {
-            const float pm = a.pmean[tid];
-            f0 = ((float)a.routed[tid] / (float)((int64_t)a.T * k)) * pm;
+            const bool global = a.g_routed != nullptr;
+            const float Tg = global ? a.g_T : (float)a.T;
+            const float pm = global ? a.g_psum[tid] / Tg : a.pmean[tid];
+            const float routed = (float)(global ? a.g_routed[tid] : a.routed[tid]);
+            f0 = (routed / (Tg * (float)k)) * pm;
             f1 = (pm - invN) * (pm - invN);
         }
         const float s0 = block_sum(f0, shf);
@@ -874,6 +913,63 @@ cudaError_t launch_logits_gate(const moe_config &c, const XT *x, const float *w_
 }
 
 }  // namespace
+
+cudaError_t launch_router_stats(const moe_config &c, const void *x, const float *w_r, const float *b_r,
+                                int32_t *topk_idx, float *topk_gate, int32_t *slot_counts, float *prob_sums,
+                                uint8_t *ws, cudaStream_t s) {
+    const WsLayout L = ws_layout(c);
+    const int tiles = router_tiles(c);
+    uint32_t *err = reinterpret_cast<uint32_t *>(ws + L.err);
+    int32_t *cnt = reinterpret_cast<int32_t *>(ws + L.cnt);
+    float *psum = reinterpret_cast<float *>(ws + L.psum);
+    RouterArgs ra{c.T, c.d, c.N, c.k, c.gating, tiles, c.has_router_bias ? 1 : 0, topk_idx, topk_gate, cnt, psum, err};
+    cudaError_t e;
+    float *logits = reinterpret_cast<float *>(ws + L.logits);
+    float *w_t = reinterpret_cast<float *>(ws + L.w_t);
+    if (c.dtype == MOE_BF16)
+        e = launch_logits_gate<__nv_bfloat16>(c, static_cast<const __nv_bfloat16 *>(x), w_r, b_r, ra, logits, w_t, s);
+    else
+        e = launch_logits_gate<float>(c, static_cast<const float *>(x), w_r, b_r, ra, logits, w_t, s);
+    if (e != cudaSuccess) return e;
+    ScanArgs sa{c.T, c.N, c.k, tiles, 0, cnt, reinterpret_cast<int32_t *>(ws + L.pre),
+                reinterpret_cast<int32_t *>(ws + L.kpre), psum, reinterpret_cast<float *>(ws + L.pmean),
+                reinterpret_cast<int32_t *>(ws + L.routed), reinterpret_cast<int32_t *>(ws + L.kept)};
+    sa.stats_only = 1;
+    sa.slot_counts = slot_counts;
+    sa.prob_sums = prob_sums;
+    k_expert_scan<<<c.N, 256, 0, s>>>(sa);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_router_assign(const moe_config &c, const int32_t *topk_idx, const int32_t *slot_base, int32_t cap,
+                                 const int32_t *g_routed, const float *g_psum, float g_T, int32_t *counts_kept,
+                                 int32_t *expert_offsets, int32_t *slot_row, int32_t *perm_token, float *aux,
+                                 uint8_t *ws, cudaStream_t s) {
+    const WsLayout L = ws_layout(c);
+    const int tiles = router_tiles(c);
+    uint32_t *err = reinterpret_cast<uint32_t *>(ws + L.err);
+    int32_t *cnt = reinterpret_cast<int32_t *>(ws + L.cnt);
+    int32_t *pre = reinterpret_cast<int32_t *>(ws + L.pre);
+    int32_t *kpre = reinterpret_cast<int32_t *>(ws + L.kpre);
+    float *psum = reinterpret_cast<float *>(ws + L.psum);
+    float *pmean = reinterpret_cast<float *>(ws + L.pmean);
+    int32_t *routed = reinterpret_cast<int32_t *>(ws + L.routed);
+    int32_t *kept = counts_kept ? counts_kept : reinterpret_cast<int32_t *>(ws + L.kept);
+    ScanArgs sa{c.T, c.N, c.k, tiles, cap, cnt, pre, kpre, psum, pmean, routed, kept};
+    sa.slot_base = slot_base;
+    k_expert_scan<<<c.N, 256, 0, s>>>(sa);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int TT = router_tile_tokens(c);
+    AssignArgs aa{c.T, c.N, c.k, tiles, TT, cap, max_rows(c), topk_idx, pre, kpre, routed, kept,
+                  pmean, expert_offsets, slot_row, perm_token, aux, err};
+    aa.g_routed = g_routed;
+    aa.g_psum = g_psum;
+    aa.g_T = g_T;
+    const size_t sbytes = (size_t)(c.N + 1 + 2 * TT * 8) * sizeof(int);
+    k_assign<<<tiles, 256, sbytes, s>>>(aa);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_router(const moe_config &c, const void *x, const float *w_r, const float *b_r,
                           const RouterOut &o, uint8_t *ws, cudaStream_t s) {

@@ -116,6 +116,24 @@ def test_null_pointers_rejected_before_launch():
     st = _raw("moe_router_topk_train", cp, FAKE, FAKE, None, None, 0.0, None, FAKE, None, None,
               FAKE, FAKE, FAKE, None, FAKE, FAKE, ws, None)
     assert st == moe.MOE_ERR_INVALID_ARG
+    # sharded router: the shard's config carries no capacity (it is global), slot
+    # counts and bases are required, global_T covers at least this shard, aux needs
+    # the global sums
+    ccap = _cfg(capacity_factor=(1, 1))
+    st = _raw("moe_router_shard_stats", ctypes.byref(ccap), FAKE, FAKE, None, FAKE, FAKE, FAKE, None,
+              FAKE, moe.moe_workspace_size(ccap), None)
+    assert st == moe.MOE_ERR_INVALID_ARG
+    st = _raw("moe_router_shard_stats", cp, FAKE, FAKE, None, FAKE, FAKE, None, None, FAKE, ws, None)
+    assert st == moe.MOE_ERR_INVALID_ARG
+    st = _raw("moe_router_shard_assign", cp, FAKE, None, 0, None, None, c.T, None, FAKE, FAKE, FAKE,
+              None, FAKE, ws, None)
+    assert st == moe.MOE_ERR_INVALID_ARG
+    st = _raw("moe_router_shard_assign", cp, FAKE, FAKE, 0, None, None, c.T - 1, None, FAKE, FAKE,
+              FAKE, None, FAKE, ws, None)
+    assert st == moe.MOE_ERR_INVALID_ARG
+    st = _raw("moe_router_shard_assign", cp, FAKE, FAKE, 0, None, None, c.T, None, FAKE, FAKE, FAKE,
+              FAKE, FAKE, ws, None)
+    assert st == moe.MOE_ERR_INVALID_ARG
 
 
 def test_workspace_checks_before_launch():
