@@ -35,7 +35,13 @@ Readings where the pages are silent:
     the remaining gates are not renormalised;
   * kept rows are grouped by expert ascending, token ascending inside a group;
   * aux loss is reported in two forms (Switch form and the variance form);
-  * expert FFNs have no biases; SiLU(z) = z / (1 + exp(-z)).
+  * expert FFNs have no biases; SiLU(z) = z / (1 + exp(-z));
+  * noisy top-k: H = fl(L + fl(w n)) drives everything after the logits; the z-loss
+    is mean_t (log sum_e exp L)^2 on the noiseless logits;
+  * Expert Choice: scores = the softmax over experts in fixed fp32 steps
+    (expert_choice.c); expert e keeps the min(C, T) highest-scoring tokens, lower
+    index first on ties, C = ceil(T cf / N); gates are the scores; rows are grouped
+    by expert, tokens ascending; a token no expert chose keeps its residual.
 
 Parity pins: the aux-loss *form* has no printed formula on the pages, so which
 of the two values "the" auxiliary loss is stays parity unpinned; the
@@ -51,7 +57,7 @@ import numpy as np
 
 _HERE = pathlib.Path(__file__).resolve().parent
 _SO = _HERE / "_liboracle.so"
-_SRC = _HERE / "router_logits.c"
+_SRCS = (_HERE / "router_logits.c", _HERE / "expert_choice.c")
 _lib = None
 
 GATING_SOFTMAX_THEN_TOPK = "softmax_then_topk"
@@ -60,11 +66,11 @@ GATING_TOPK_THEN_SOFTMAX = "topk_then_softmax"
 
 def build(force: bool = False) -> pathlib.Path:
     """Compile the C part of the oracle (plain gcc, no GPU headers)."""
-    if force or not _SO.exists() or _SO.stat().st_mtime < _SRC.stat().st_mtime:
+    if force or not _SO.exists() or any(_SO.stat().st_mtime < s.stat().st_mtime for s in _SRCS):
         # -mfma makes fmaf a single instruction; its result is the correctly
         # rounded fused multiply-add either way (libm's fmaf is exact too).
         cmd = ["gcc", "-O3", "-mfma", "-fno-fast-math", "-ffp-contract=off",
-               "-shared", "-fPIC", "-o", str(_SO), str(_SRC), "-lm"]
+               "-shared", "-fPIC", "-o", str(_SO), *map(str, _SRCS), "-lm"]
         subprocess.run(cmd, check=True)
     return _SO
 
@@ -76,6 +82,10 @@ def _load():
         lib = ctypes.CDLL(str(_SO))
         lib.oracle_router_logits.restype = None
         lib.oracle_router_logits.argtypes = [ctypes.c_long] * 3 + [ctypes.c_void_p] * 4
+        lib.oracle_ec_scores.restype = None
+        lib.oracle_ec_scores.argtypes = [ctypes.c_long] * 2 + [ctypes.c_void_p] * 2
+        lib.oracle_ec_exp_array.restype = None
+        lib.oracle_ec_exp_array.argtypes = [ctypes.c_long] + [ctypes.c_void_p] * 2
         _lib = lib
     return _lib
 
@@ -338,6 +348,104 @@ def route_train(cfg, x, w_r, b_r=None, noise=None, noise_weight: float = 0.0) ->
     rt = route_from_logits(cfg, H)
     rt["raw_logits"] = L
     rt["z_loss"] = z_loss(L)
+    return rt
+
+
+# ------------------------------------------------------------- Expert Choice routing
+
+def ec_exp(x: np.ndarray) -> np.ndarray:
+    """The fp32 exponential of the Expert Choice scores (expert_choice.c: Cody-Waite
+    reduction, degree-7 Taylor polynomial, exact power-of-two scaling), elementwise."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    y = np.empty_like(x)
+    _load().oracle_ec_exp_array(x.size, x.ctypes.data, y.ctypes.data)
+    return y
+
+
+def ec_scores(logits: np.ndarray) -> np.ndarray:
+    """Expert Choice scores S[t, e], fp32: the softmax over experts of each token's
+    logits, computed in the fixed fp32 steps of expert_choice.c (max, shifted
+    exponential, sum over experts ascending, division), because the experts'
+    choices compare these values across tokens."""
+    L = np.ascontiguousarray(logits, dtype=np.float32)
+    T, N = L.shape
+    S = np.empty_like(L)
+    _load().oracle_ec_scores(T, N, L.ctypes.data, S.ctypes.data)
+    return S
+
+
+def expert_choice_select(S: np.ndarray, C: int) -> np.ndarray:
+    """chosen [N][min(C, T)]: the tokens each expert keeps, ascending token index.
+
+    [MoE glossary] sparse-MoE list: Expert Choice lets the experts select their
+    top tokens. Expert e keeps the min(C, T) tokens with the largest S[t, e]; on
+    equal scores the lower token index wins (a reading). Every expert is full, so
+    the load is balanced by construction; a token may be chosen by several experts
+    or by none.
+    """
+    T, N = S.shape
+    Ce = min(C, T)
+    chosen = np.empty((N, Ce), dtype=np.int64)
+    for e in range(N):
+        order = np.lexsort((np.arange(T), -S[:, e].astype(np.float64)))   # score desc, t asc
+        chosen[e] = np.sort(order[:Ce])
+    return chosen
+
+
+def route_expert_choice(cfg, x, w_r, b_r=None) -> dict:
+    """Expert Choice router: logits, scores, per-expert selections, dispatch order.
+
+    Capacity C = ceil(T * cf / N) (cf = the capacity factor, the average number of
+    experts per token); expert e owns rows [e * Ce, (e + 1) * Ce), Ce = min(C, T),
+    holding its tokens in ascending order. row_gate[r] = S[token, e]. For each
+    token its rows in expert order (token_rows, split by token_ptr) drive the
+    combine."""
+    L = router_logits(x, w_r, b_r)
+    S = ec_scores(L)
+    T, N = S.shape
+    C = capacity(T, N, cfg.capacity_factor)
+    assert C is not None and C > 0, "Expert Choice needs a capacity factor"
+    chosen = expert_choice_select(S, C)
+    Ce = chosen.shape[1]
+    perm_token = chosen.reshape(-1)
+    expert_of_row = np.repeat(np.arange(N), Ce)
+    row_gate = S[perm_token, expert_of_row].astype(np.float32)
+    token_rows = [[] for _ in range(T)]
+    for r in range(N * Ce):                        # rows in expert order
+        token_rows[int(perm_token[r])].append(r)
+    token_ptr = np.zeros(T + 1, dtype=np.int64)
+    token_ptr[1:] = np.cumsum([len(v) for v in token_rows])
+    return dict(logits=L, scores=S, capacity=C, chosen=chosen,
+                expert_offsets=np.arange(N + 1, dtype=np.int64) * Ce, perm_token=perm_token,
+                row_gate=row_gate, token_ptr=token_ptr,
+                token_rows=np.array([r for v in token_rows for r in v], dtype=np.int64))
+
+
+def layer_output_expert_choice(cfg, x, rt: dict, w_gate, w_up, w_down, sw_gate=None, sw_up=None,
+                               sw_down=None, tokens=None) -> np.ndarray:
+    """y_t = x_t + S(x_t) + sum over the experts that chose t (ascending) of
+    S[t, e] * FFN_e(x_t), float64; a token no expert chose keeps x_t (+ S(x_t))."""
+    x = np.asarray(x, dtype=np.float64)
+    toks = np.arange(x.shape[0]) if tokens is None else np.asarray(tokens)
+    out = np.zeros((len(toks), x.shape[1]))
+    Ce = rt["chosen"].shape[1]
+    for i, t in enumerate(toks):
+        for r in rt["token_rows"][rt["token_ptr"][t]:rt["token_ptr"][t + 1]]:
+            e = int(r) // Ce
+            wu = None if w_up is None else w_up[e]
+            f = expert_ffn(x[t:t + 1], w_gate[e], wu, w_down[e], cfg.act)[0]
+            out[i] += float(rt["row_gate"][r]) * f
+    xt = x[toks]
+    if sw_gate is not None:
+        out += shared_expert(xt, sw_gate, sw_up, sw_down)
+    return out + xt
+
+
+def forward_expert_choice(cfg, inp: dict, tokens=None) -> dict:
+    rt = route_expert_choice(cfg, inp["x"], inp["w_r"], inp.get("b_r"))
+    rt["y"] = layer_output_expert_choice(cfg, inp["x"], rt, inp["w_gate"], inp.get("w_up"),
+                                         inp["w_down"], inp.get("shared_w_gate"),
+                                         inp.get("shared_w_up"), inp.get("shared_w_down"), tokens)
     return rt
 
 

@@ -453,11 +453,131 @@ def pin_z_loss_closed_forms(O):
         scipy.special.logsumexp(plain["raw_logits"].astype(np.float64), axis=1) ** 2)), rel_tol=1e-12)
 
 
+# ------------------------------------------------------------- Expert Choice routing
+
+def _c_hex_constants():
+    import re
+    src = open(os.path.join(os.path.dirname(O.__file__), "expert_choice.c")).read()
+    return {m.group(1): float.fromhex(m.group(2))
+            for m in re.finditer(r"static const float (\w+) = (0x[0-9a-fp.+-]+)f;", src)}
+
+
+def pin_ec_exp(O):
+    """The scores' exponential: within 1 ulp of e^x on [-87, 0], exactly 1 at 0,
+    monotone; its constants are ln 2 split as Cody and Waite prescribe (high part of
+    16 significant bits, low part the fp32 remainder), log2(e) and 1/k! in fp32."""
+    from decimal import Decimal, getcontext
+    getcontext().prec = 50
+    ln2 = Decimal(2).ln()
+    c = _c_hex_constants()
+    hi = c["LN2_HI"]
+    m, e = math.frexp(hi)
+    assert m * 2 ** 16 == int(m * 2 ** 16)                      # 16 significant bits
+    assert abs(Decimal(hi) - ln2) < Decimal(2) ** -16
+    assert c["LN2_LO"] == float(np.float32(float(ln2 - Decimal(hi))))
+    assert c["LOG2E"] == float(np.float32(float(1 / ln2)))
+    for k in range(2, 8):
+        assert c[f"C{k}"] == float(np.float32(1.0 / math.factorial(k)))
+    x = np.linspace(-87.0, 0.0, 400001).astype(np.float32)
+    y = O.ec_exp(x).astype(np.float64)
+    ref = np.exp(x.astype(np.float64))
+    ulp = np.spacing(ref.astype(np.float32)).astype(np.float64)
+    assert np.max(np.abs(y - ref) / ulp) <= 1.0
+    assert float(O.ec_exp(np.zeros(1, np.float32))[0]) == 1.0
+    assert np.all(np.diff(y) >= 0)
+    assert float(O.ec_exp(np.array([-88.0, -1e30], np.float32)).max()) == 0.0
+
+
+def pin_ec_scores(O):
+    """Scores are the softmax over experts: within 4e-7 of the float64 softmax, sum
+    to 1; equal logits give 1/N exactly for N a power of two; logits [0, ln 3] give
+    [1/4, 3/4]."""
+    rng = np.random.default_rng(21)
+    L = (rng.standard_normal((60, 13)) * 3).astype(np.float32)
+    S = O.ec_scores(L).astype(np.float64)
+    ref = scipy.special.softmax(L.astype(np.float64), axis=1)
+    assert np.max(np.abs(S - ref)) <= 4e-7
+    assert np.max(np.abs(S.sum(axis=1) - 1.0)) <= 2e-6
+    for N in (1, 2, 8, 256):
+        assert np.all(O.ec_scores(np.full((3, N), 0.37, np.float32)) == np.float32(1.0 / N))
+    S2 = O.ec_scores(np.array([[0.0, math.log(3.0)]], np.float32))[0]
+    assert abs(float(S2[0]) - 0.25) <= 1e-7 and abs(float(S2[1]) - 0.75) <= 1e-7
+
+
+def pin_ec_selection_brute_force(O):
+    """Each expert keeps the min(C, T) tokens of largest score, lower index first on
+    ties, listed in token order; all-equal scores keep tokens 0 .. C-1."""
+    rng = np.random.default_rng(22)
+    for T, N, C in ((9, 3, 4), (20, 5, 7), (6, 4, 10), (31, 8, 8)):
+        L = rng.integers(-3, 4, size=(T, N)).astype(np.float32)     # many ties
+        S = O.ec_scores(L)
+        chosen = O.expert_choice_select(S, C)
+        for e in range(N):
+            want = sorted(sorted(range(T), key=lambda t: (-float(S[t, e]), t))[:min(C, T)])
+            assert chosen[e].tolist() == want
+    S = O.ec_scores(np.zeros((10, 4), np.float32))
+    assert all(O.expert_choice_select(S, 3)[e].tolist() == [0, 1, 2] for e in range(4))
+
+
+def pin_ec_dispatch_and_balance(O):
+    """Every expert owns exactly Ce = min(C, T) rows holding its tokens ascending;
+    the per-token row lists cover every row once, in expert order; row gates are the
+    chosen scores."""
+    rng = np.random.default_rng(23)
+    T, d, N = 50, 8, 6
+    cfg = O.config_from(T, d, N, 1, h=4, capacity_factor=(2, 1))
+    x = rng.standard_normal((T, d)).astype(np.float32)
+    w_r = rng.standard_normal((d, N)).astype(np.float32)
+    rt = O.route_expert_choice(cfg, x, w_r)
+    Ce = min(O.capacity(T, N, (2, 1)), T)
+    assert rt["capacity"] == math.ceil(T * 2 / N) and rt["expert_offsets"].tolist() == [e * Ce for e in range(N + 1)]
+    rows = []
+    for t in range(T):
+        rs = rt["token_rows"][rt["token_ptr"][t]:rt["token_ptr"][t + 1]].tolist()
+        assert rs == sorted(rs) and all(rt["perm_token"][r] == t for r in rs)
+        rows += rs
+    assert sorted(rows) == list(range(N * Ce))
+    for e in range(N):
+        seg = rt["perm_token"][e * Ce:(e + 1) * Ce]
+        assert np.all(np.diff(seg) > 0)
+        assert np.array_equal(rt["row_gate"][e * Ce:(e + 1) * Ce], rt["scores"][seg, e])
+
+
+def pin_ec_dense_brute_force(O):
+    """y = x + S(x) + sum_e G[t, e] FFN_e(x) with G the dense score matrix masked to
+    the chosen (token, expert) pairs, every expert computed on every token; a token
+    no expert chose is exactly its residual (no shared expert)."""
+    rng = np.random.default_rng(24)
+    for hs in (0, 5):
+        cfg, inp = _rand_layer(rng, T=14, d=8, N=4, k=1, h=6, hs=hs, cf=(1, 2))
+        rt = O.forward_expert_choice(cfg, inp)
+        # selection and gates from the float64 softmax of the logits, brute force
+        P = scipy.special.softmax(O.router_logits(inp["x"], inp["w_r"]).astype(np.float64), axis=1)
+        C = min(O.capacity(cfg.T, cfg.N, (1, 2)), cfg.T)
+        G = np.zeros((cfg.T, cfg.N))
+        for e in range(cfg.N):
+            top = sorted(range(cfg.T), key=lambda t: (-P[t, e], t))[:C]
+            G[top, e] = P[top, e]
+        x = inp["x"].astype(np.float64)
+        y = x.copy()
+        for e in range(cfg.N):
+            y += G[:, e:e + 1] * _torch_mlp(inp["x"], inp["w_gate"][e], inp["w_up"][e], inp["w_down"][e])
+        if hs:
+            y += _torch_mlp(inp["x"], inp["shared_w_gate"], inp["shared_w_up"], inp["shared_w_down"])
+        assert np.allclose(rt["y"], y, rtol=1e-6, atol=1e-6)
+        unchosen = ~np.isin(np.arange(cfg.T), rt["chosen"])
+        assert unchosen.any()
+        if not hs:
+            assert np.array_equal(rt["y"][unchosen], x[unchosen])
+
+
 PINS = [pin_router_logits_exact, pin_router_logits_error_bound, pin_topk_brute_force,
         pin_worked_example, pin_three_token_dispatch, pin_softmax_library, pin_aux_closed_forms,
         pin_capacity, pin_single_expert_is_dense_mlp, pin_identical_experts,
         pin_dense_brute_force, pin_dropped_tokens_are_residual, pin_noisy_logits_exact,
-        pin_noisy_selection, pin_route_train_without_noise, pin_z_loss_closed_forms]
+        pin_noisy_selection, pin_route_train_without_noise, pin_z_loss_closed_forms, pin_ec_exp,
+        pin_ec_scores, pin_ec_selection_brute_force, pin_ec_dispatch_and_balance,
+        pin_ec_dense_brute_force]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -608,6 +728,38 @@ def _mut_z_on_noisy_logits(mp):
     mp.setattr(O, "route_train", rt)
 
 
+def _mut_ec_tie_high_index(mp):
+    def sel(S, C):
+        T, N = S.shape
+        Ce = min(C, T)
+        return np.stack([np.sort(np.lexsort((-np.arange(T), -S[:, e].astype(np.float64)))[:Ce])
+                         for e in range(N)])
+    mp.setattr(O, "expert_choice_select", sel)
+
+
+def _mut_ec_select_by_logits(mp):
+    real = O.route_expert_choice
+
+    def route(cfg, x, w_r, b_r=None):
+        L = O.router_logits(x, w_r, b_r)
+        mp.setattr(O, "ec_scores", lambda _L: L)       # selection and gates on logits
+        return real(cfg, x, w_r, b_r)
+    mp.setattr(O, "route_expert_choice", route)
+
+
+def _mut_ec_rows_by_score(mp):
+    def sel(S, C):
+        T, N = S.shape
+        Ce = min(C, T)
+        return np.stack([np.lexsort((np.arange(T), -S[:, e].astype(np.float64)))[:Ce] for e in range(N)])
+    mp.setattr(O, "expert_choice_select", sel)
+
+
+def _mut_ec_exp_short_series(mp):
+    mp.setattr(O, "ec_exp", lambda x: (1.0 + np.asarray(x, np.float32) + np.asarray(x, np.float32) ** 2 / 2)
+               .astype(np.float32))
+
+
 MUTATIONS = [
     (_mut_tie_high_index, pin_topk_brute_force),
     (_mut_swap_gating, pin_worked_example),
@@ -625,6 +777,10 @@ MUTATIONS = [
     (_mut_noise_one_rounding, pin_noisy_logits_exact),
     (_mut_z_not_squared, pin_z_loss_closed_forms),
     (_mut_z_on_noisy_logits, pin_z_loss_closed_forms),
+    (_mut_ec_tie_high_index, pin_ec_selection_brute_force),
+    (_mut_ec_select_by_logits, pin_ec_dense_brute_force),
+    (_mut_ec_rows_by_score, pin_ec_dispatch_and_balance),
+    (_mut_ec_exp_short_series, pin_ec_exp),
 ]
 
 
