@@ -138,11 +138,18 @@ def captured_traffic(workload: str, stage: str):
 
 
 def launches_per_forward(w) -> int:
-    """Kernels one moe_forward launches: router (logits+gating, expert scan, slot
-    assignment), dispatch, expert product 1 (two launches for ReLU experts with a
-    shared expert), expert product 2, combine."""
+    """Kernels one moe_forward launches. Token choice: router weight re-layout,
+    logits with gating (one kernel for N <= 32, logits and gating kernels above),
+    expert scan, slot assignment. Expert Choice: weight re-layout, logits, scores,
+    per-expert selection, per-token list scan and fill, per-expert counts. Then
+    dispatch, expert product 1 (two launches for ReLU experts with a shared expert),
+    expert product 2 and the combine."""
+    if w.routing == "expert_choice":
+        router = 7
+    else:
+        router = 1 + (2 if w.N > 32 else 1) + 2
     p1 = 2 if (w.act == "relu" and w.h_shared) else 1
-    return 3 + 1 + p1 + 1 + 1
+    return router + 1 + p1 + 1 + 1
 
 
 def _peaks():
@@ -258,7 +265,10 @@ def time_oracle(w, host_inp, sample: int, seed: int) -> tuple[float, float]:
     n = min(sample, w.T)
     toks = np.sort(rng.choice(w.T, size=n, replace=False))
     t0 = time.perf_counter()
-    O.forward(w, host_inp, tokens=toks)
+    if w.routing == "expert_choice":
+        O.forward_expert_choice(w, host_inp, tokens=toks)
+    else:
+        O.forward(w, host_inp, tokens=toks)
     return time.perf_counter() - t0, n
 
 
@@ -284,7 +294,8 @@ def run_reference(a, w, world, rank):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
             "config": {"workload": w.name, "T": w.T, "d": w.d, "N": w.N, "k": w.k, "h": w.h,
-                       "h_shared": w.h_shared, "gating": w.gating, "act": w.act},
+                       "h_shared": w.h_shared, "gating": w.gating, "act": w.act, "routing": w.routing,
+                       "routing": w.routing},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": _blas_threads(),
                              "kind": "oracle",
                              "sample": f"per step: routing of all {w.T} tokens + layer outputs "
@@ -367,8 +378,9 @@ def run_ours(a, w, world, rank, local):
     inp = W.make_inputs(w, device=dev)
     cfg = moe.make_config(T=w.T, d=w.d, N=w.N, k=w.k, h=w.h, h_shared=w.h_shared, dtype=w.dtype,
                           gating=w.gating, act=w.act, capacity_factor=w.capacity_factor,
-                          router_bias=w.router_bias)
+                          router_bias=w.router_bias, routing=w.routing)
     ws = moe.workspace(cfg, device=dev)
+    ec = w.routing == "expert_choice"
     T, k, N, d = w.T, w.k, w.N, w.d
     y = torch.empty((T, d), dtype=inp["x"].dtype, device=dev)
     idx = torch.empty((T, k), dtype=torch.int32, device=dev)
@@ -377,6 +389,9 @@ def run_ours(a, w, world, rank, local):
     kept = torch.empty(N, dtype=torch.int32, device=dev)
     aux = torch.empty(2, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+
+    if ec:  # Expert Choice returns no token-choice outputs
+        idx = gate = aux = None
 
     def fwd(x=None):
         moe.moe_forward(cfg, inp["x"] if x is None else x, inp["w_r"], inp["b_r"], inp["w_gate"],
@@ -523,7 +538,7 @@ def run_ours(a, w, world, rank, local):
     }
 
     # ---- training-time router variant (noisy top-k + z-loss), same inputs
-    if not a.no_variants:
+    if not a.no_variants and not ec:
         line["variants"] = {"router_train": measure_router_train(
             w, inp, cfg, ws, stream, dev, 0 if (a.no_cpu_baseline or rank != 0) else 512)}
 

@@ -79,6 +79,13 @@ typedef enum { MOE_SOFTMAX_THEN_TOPK = 0, MOE_TOPK_THEN_SOFTMAX = 1 } moe_gating
 /* Expert FFN. SILU_GATED: W_down (SiLU(W_gate x) * (W_up x)); RELU: W2 max(0, W1 x). */
 typedef enum { MOE_ACT_SILU_GATED = 0, MOE_ACT_RELU = 1 } moe_act;
 
+/* Who chooses: every token its top-k experts, or every expert its top tokens
+ * ("Mixture of Experts (MoE)" glossary, sparse-MoE list: Expert Choice inverts the
+ * routing). Expert Choice needs a capacity factor cap_num/cap_den > 0 (the average
+ * number of experts per token): each expert takes min(C, T) tokens, C =
+ * ceil(T * cap_num / (N * cap_den)); k and gating are not used; T <= 16384. */
+typedef enum { MOE_ROUTING_TOKEN_CHOICE = 0, MOE_ROUTING_EXPERT_CHOICE = 1 } moe_routing;
+
 typedef struct {
     int32_t T;                /* tokens, 1..65536                                    */
     int32_t d;                /* model dim: multiple of 8 (fp32) or of 64 (bf16)    */
@@ -92,6 +99,7 @@ typedef struct {
     int32_t cap_num, cap_den; /* capacity factor cap_num/cap_den; 0/0 = no limit     */
     int32_t has_router_bias;  /* 1: b_r is read and added to the logits              */
     int32_t debug_flags;      /* MOE_DEBUG_* bits, 0 in normal use                   */
+    int32_t routing;          /* moe_routing: token choice (top-k) or Expert Choice  */
 } moe_config;
 
 /* debug_flags bits */
@@ -219,6 +227,40 @@ moe_status moe_router_shard_assign(const moe_config *cfg, const int32_t *topk_id
                                    size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * Expert Choice router (cfg->routing == MOE_ROUTING_EXPERT_CHOICE): every expert
+ * picks its top tokens ("Mixture of Experts (MoE)" glossary, sparse-MoE list).
+ * Scores S[t][e] = softmax over experts of the fp32 logits (the router's probability
+ * distribution), computed in fixed fp32 steps (max, an exponential from Cody-Waite
+ * reduction and a degree-7 Taylor series, sum over experts ascending, division) so
+ * that the choice is reproducible bit for bit. Expert e keeps the Ce = min(C, T)
+ * tokens of largest S[t][e] (lower token first on equal scores), C =
+ * ceil(T * cap_num / (N * cap_den)): every expert is full, a token may be chosen by
+ * several experts or by none. Outputs (R = N * Ce rows, moe_max_rows(cfg)):
+ *   expert_offsets int32 [N+1]  e * Ce
+ *   perm_token     int32 [R]    rows e*Ce .. e*Ce+Ce-1: expert e's tokens, ascending
+ *   row_gate       fp32  [R]    S[token][e] of each row
+ *   token_ptr      int32 [T+1]  token t's rows are token_rows[token_ptr[t] .. token_ptr[t+1])
+ *   token_rows     int32 [R]    in expert order
+ * Feed perm_token and expert_offsets to moe_dispatch and moe_grouped_ffn as usual,
+ * then moe_combine_expert_choice. The workspace must hold moe_workspace_size(cfg).
+ */
+moe_status moe_router_expert_choice(const moe_config *cfg, const void *x, const float *w_r,
+                                   const float *b_r, int32_t *expert_offsets, int32_t *perm_token,
+                                   float *row_gate, int32_t *token_ptr, int32_t *token_rows,
+                                   void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Expert Choice combine: y_t = x_t + S(x_t) + sum over token t's rows r (expert
+ * order) of row_gate[r] * y_perm[r], fp32 accumulation; a token no expert chose
+ * gets x_t (+ S(x_t)). Shared expert as in moe_combine.
+ */
+moe_status moe_combine_expert_choice(const moe_config *cfg, const void *x, const void *y_perm,
+                                     const int32_t *token_ptr, const int32_t *token_rows,
+                                     const float *row_gate, const void *shared_w_gate,
+                                     const void *shared_w_up, const void *shared_w_down, void *y,
+                                     void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
  * moe_router_topk for callers that cannot allocate device memory. The paper has
  * no counterpart to this call; it exists for hosts that forbid allocation after
  * start-up (engines that plan all device memory ahead and call plugins from an
@@ -285,6 +327,9 @@ moe_status moe_combine(const moe_config *cfg, const void *x, const void *y_perm,
 
 /*
  * Whole layer: router -> dispatch -> experts (+ shared expert) -> combine.
+ * With cfg->routing == MOE_ROUTING_EXPERT_CHOICE the router and the combine are the
+ * Expert Choice ones; topk_idx, topk_gate and aux must then be NULL and
+ * counts_routed / counts_kept (when given) receive Ce for every expert.
  * Same inputs as above; outputs y [T][d] and, when non-NULL, topk_idx, topk_gate,
  * counts_routed, counts_kept (as in moe_router_topk) and aux [2]. The dispatch
  * order, x_perm, hidden activations and y_perm live in the workspace.

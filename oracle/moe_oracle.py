@@ -429,12 +429,16 @@ def layer_output_expert_choice(cfg, x, rt: dict, w_gate, w_up, w_down, sw_gate=N
     toks = np.arange(x.shape[0]) if tokens is None else np.asarray(tokens)
     out = np.zeros((len(toks), x.shape[1]))
     Ce = rt["chosen"].shape[1]
-    for i, t in enumerate(toks):
-        for r in rt["token_rows"][rt["token_ptr"][t]:rt["token_ptr"][t + 1]]:
-            e = int(r) // Ce
-            wu = None if w_up is None else w_up[e]
-            f = expert_ffn(x[t:t + 1], w_gate[e], wu, w_down[e], cfg.act)[0]
-            out[i] += float(rt["row_gate"][r]) * f
+    N = rt["chosen"].shape[0]
+    for e in range(N):                          # experts ascending = each token's row order
+        rows = [(i, r) for i, t in enumerate(toks)
+                for r in rt["token_rows"][rt["token_ptr"][t]:rt["token_ptr"][t + 1]] if int(r) // Ce == e]
+        if not rows:
+            continue
+        wu = None if w_up is None else w_up[e]
+        f = expert_ffn(x[[toks[i] for i, _ in rows]], w_gate[e], wu, w_down[e], cfg.act)
+        for q, (i, r) in enumerate(rows):
+            out[i] += float(rt["row_gate"][r]) * f[q]
     xt = x[toks]
     if sw_gate is not None:
         out += shared_expert(xt, sw_gate, sw_up, sw_down)

@@ -22,6 +22,7 @@ MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_FAULT = 4, 5, 6
 MOE_F32, MOE_BF16 = 0, 1
 MOE_SOFTMAX_THEN_TOPK, MOE_TOPK_THEN_SOFTMAX = 0, 1
 MOE_ACT_SILU_GATED, MOE_ACT_RELU = 0, 1
+MOE_ROUTING_TOKEN_CHOICE, MOE_ROUTING_EXPERT_CHOICE = 0, 1
 MOE_DEBUG_FORCE_SIMT_FFN = 1
 MOE_DEBUG_FFN_PAIR = 2
 MOE_DEBUG_FFN_SINGLE = 4
@@ -30,14 +31,15 @@ MOE_DEBUG_FFN_SWAP = 8
 EXPORTED = ("moe_validate_config", "moe_workspace_size", "moe_max_rows", "moe_capacity",
             "moe_router_topk", "moe_dispatch", "moe_grouped_ffn", "moe_combine", "moe_forward",
             "moe_forward_profiled", "moe_check_error", "moe_status_str", "moe_router_topk_noalloc",
-            "moe_router_topk_train", "moe_router_shard_stats", "moe_router_shard_assign")
+            "moe_router_topk_train", "moe_router_shard_stats", "moe_router_shard_assign",
+            "moe_router_expert_choice", "moe_combine_expert_choice")
 
 
 class moe_config(ctypes.Structure):
     """Mirror of the C struct moe_config (all fields int32)."""
     _fields_ = [(n, ctypes.c_int32) for n in (
         "T", "d", "N", "k", "h", "h_shared", "dtype", "gating", "act", "cap_num", "cap_den",
-        "has_router_bias", "debug_flags")]
+        "has_router_bias", "debug_flags", "routing")]
 
 
 class MoeError(RuntimeError):
@@ -62,6 +64,8 @@ def _load() -> ctypes.CDLL:
         "moe_router_topk_noalloc": (I32, [cfgp] + [P] * 11 + [P]),
         "moe_router_topk_train": (I32, [cfgp, P, P, P, P, ctypes.c_float] + [P] * 9 + [P, SZ, P]),
         "moe_router_shard_stats": (I32, [cfgp] + [P] * 7 + [P, SZ, P]),
+        "moe_router_expert_choice": (I32, [cfgp] + [P] * 8 + [P, SZ, P]),
+        "moe_combine_expert_choice": (I32, [cfgp] + [P] * 9 + [P, SZ, P]),
         "moe_router_shard_assign": (I32, [cfgp, P, P, I32, P, P, I64] + [P] * 5 + [P, SZ, P]),
         "moe_dispatch": (I32, [cfgp, P, P, P, P, P, SZ, P]),
         "moe_grouped_ffn": (I32, [cfgp, P, P, P, P, P, P, P, SZ, P]),
@@ -89,7 +93,7 @@ moe_status_str = status_str
 
 def make_config(T, d, N, k, h, h_shared=0, dtype="bf16", gating="topk_then_softmax",
                 act="silu_gated", capacity_factor=None, router_bias=False, debug_flags=0,
-                **_ignored) -> moe_config:
+                routing="token_choice", **_ignored) -> moe_config:
     """Build a moe_config from plain fields (the names used by the workload table)."""
     c = moe_config()
     c.T, c.d, c.N, c.k, c.h, c.h_shared = T, d, N, k, h, h_shared
@@ -102,6 +106,8 @@ def make_config(T, d, N, k, h, h_shared=0, dtype="bf16", gating="topk_then_softm
     c.cap_num, c.cap_den = capacity_factor if capacity_factor else (0, 0)
     c.has_router_bias = 1 if router_bias else 0
     c.debug_flags = debug_flags
+    c.routing = ({"token_choice": MOE_ROUTING_TOKEN_CHOICE, "expert_choice": MOE_ROUTING_EXPERT_CHOICE}[routing]
+                 if isinstance(routing, str) else int(routing))
     return c
 
 
@@ -194,6 +200,25 @@ def moe_router_shard_assign(cfg, topk_idx, slot_base, capacity, global_routed, g
                                         _p(slot_row), _p(perm_token), _p(aux), _p(ws),
                                         ws.numel() if ws is not None else 0, _stream(stream)),
            "moe_router_shard_assign")
+
+
+def moe_router_expert_choice(cfg, x, w_r, b_r, expert_offsets, perm_token, row_gate, token_ptr,
+                             token_rows, ws, stream=None):
+    """Expert Choice router: every expert keeps its min(C, T) highest-scoring tokens."""
+    _check(_lib.moe_router_expert_choice(ctypes.byref(cfg), _p(x), _p(w_r), _p(b_r),
+                                         _p(expert_offsets), _p(perm_token), _p(row_gate),
+                                         _p(token_ptr), _p(token_rows), _p(ws),
+                                         ws.numel() if ws is not None else 0, _stream(stream)),
+           "moe_router_expert_choice")
+
+
+def moe_combine_expert_choice(cfg, x, y_perm, token_ptr, token_rows, row_gate, shared_w_gate,
+                              shared_w_up, shared_w_down, y, ws, stream=None):
+    _check(_lib.moe_combine_expert_choice(ctypes.byref(cfg), _p(x), _p(y_perm), _p(token_ptr),
+                                          _p(token_rows), _p(row_gate), _p(shared_w_gate),
+                                          _p(shared_w_up), _p(shared_w_down), _p(y), _p(ws),
+                                          ws.numel() if ws is not None else 0, _stream(stream)),
+           "moe_combine_expert_choice")
 
 
 def moe_router_topk_noalloc(cfg, x, w_r, b_r, topk_idx, topk_gate, counts_routed, counts_kept,

@@ -13,6 +13,10 @@ namespace moe {
 constexpr uint32_t kErrFault = 1u;    // an out-of-range index was seen and skipped
 constexpr uint32_t kErrTimeout = 2u;  // a bounded wait gave up
 
+// Expert Choice selects each expert's tokens by sorting all T scores of its column
+// in shared memory (8-byte keys, T rounded up to a power of two).
+constexpr int kMaxExpertChoiceTokens = 16384;
+
 // The router writes its per-expert statistics per tile of router_tile_tokens(cfg)
 // tokens; the tile is a pure function of the config (no device query), so the
 // workspace size can be computed without a GPU.
@@ -43,6 +47,10 @@ struct WsLayout {
     size_t perm_token;           // int32 [R_max]
     size_t aux;                  // f32 [2]
     size_t x_perm, y_perm;       // [R_max][d]
+    // Expert Choice: scores [N][T] f32, row of (expert, token) [N][T] int32 (-1: not
+    // chosen), per-token row counts [T], list offsets [T+1], row lists [R_max] and
+    // row gates [R_max] (used by moe_forward)
+    size_t ec_scores, ec_row, ec_tok_cnt, ec_tok_ptr, ec_tok_rows, ec_row_gate;
     size_t hid;                  // [R_max][h]
     size_t hid_sh;               // [T][h_shared]
     size_t s_out;                // [T][d]  shared expert output
@@ -64,6 +72,19 @@ struct RouterOut {
 };
 cudaError_t launch_router(const moe_config &c, const void *x, const float *w_r, const float *b_r,
                           const RouterOut &o, uint8_t *ws, cudaStream_t s);
+// Router logits [T][N] fp32 alone (the blocked summation order of every router
+// path), for any N; used by Expert Choice.
+cudaError_t launch_router_logits(const moe_config &c, const void *x, const float *w_r, const float *b_r,
+                                 float *logits, uint8_t *ws, cudaStream_t s);
+// Expert Choice: scores, per-expert selection (expert_offsets, perm_token,
+// row_gate) and per-token row lists (tok_ptr, tok_rows) from the logits.
+cudaError_t launch_expert_choice(const moe_config &c, const float *logits, int32_t *expert_offsets,
+                                 int32_t *perm_token, float *row_gate, int32_t *tok_ptr, int32_t *tok_rows,
+                                 uint8_t *ws, cudaStream_t s);
+// Expert Choice combine: y = x + [s_out] + sum over each token's rows of gate * y_perm.
+cudaError_t launch_combine_ec(const moe_config &c, const void *x, const void *y_perm, const void *s_out,
+                              const int32_t *tok_ptr, const int32_t *tok_rows, const float *row_gate, void *y,
+                              uint32_t *err, cudaStream_t s);
 // Token-sharded router, phase 1: routing of this shard and the statistics the
 // shards exchange (selections per expert and slot, sums of the softmax).
 cudaError_t launch_router_stats(const moe_config &c, const void *x, const float *w_r, const float *b_r,

@@ -12,8 +12,9 @@
 namespace moe {
 
 int64_t max_rows(const moe_config &c) {
-    const int64_t tk = (int64_t)c.T * c.k;
     const int32_t C = capacity_of(c);
+    if (c.routing == MOE_ROUTING_EXPERT_CHOICE) return (int64_t)c.N * std::min<int64_t>(C, c.T);
+    const int64_t tk = (int64_t)c.T * c.k;
     return C > 0 ? std::min<int64_t>(tk, (int64_t)c.N * C) : tk;
 }
 
@@ -49,7 +50,8 @@ WsLayout ws_layout(const moe_config &c) {
     L.zpart = take(tiles * 4);
     L.routed = take(N * 4);
     L.kept = take(N * 4);
-    L.logits = take(c.N > 32 ? T * N * 4 : 0);
+    const bool ec = c.routing == MOE_ROUTING_EXPERT_CHOICE;
+    L.logits = take(c.N > 32 || ec ? T * N * 4 : 0);
     L.w_t = take((size_t)((c.d + 255) / 256) * 256 * N * 4);
     // expert / shared-expert buffers
     L.hid = take(rmax * c.h * es);
@@ -64,6 +66,13 @@ WsLayout ws_layout(const moe_config &c) {
     L.aux = take(2 * 4);
     L.x_perm = take(rmax * c.d * es);
     L.y_perm = take(rmax * c.d * es);
+    // Expert Choice only
+    L.ec_scores = take(ec ? N * T * 4 : 0);
+    L.ec_row = take(ec ? N * T * 4 : 0);
+    L.ec_tok_cnt = take(ec ? T * 4 : 0);
+    L.ec_tok_ptr = take(ec ? (T + 1) * 4 : 0);
+    L.ec_tok_rows = take(ec ? rmax * 4 : 0);
+    L.ec_row_gate = take(ec ? rmax * 4 : 0);
     L.total = o;
     return L;
 }
@@ -99,6 +108,11 @@ static moe_status validate(const moe_config *c) {
     if (c->has_router_bias != 0 && c->has_router_bias != 1) return MOE_ERR_INVALID_ARG;
     if (!dim_ok(c->d, c->dtype) || !dim_ok(c->h, c->dtype)) return MOE_ERR_UNSUPPORTED;
     if (c->h_shared && !dim_ok(c->h_shared, c->dtype)) return MOE_ERR_UNSUPPORTED;
+    if (c->routing != MOE_ROUTING_TOKEN_CHOICE && c->routing != MOE_ROUTING_EXPERT_CHOICE) return MOE_ERR_INVALID_ARG;
+    if (c->routing == MOE_ROUTING_EXPERT_CHOICE) {
+        if (c->cap_num == 0) return MOE_ERR_INVALID_ARG;  // the experts' capacity is the routing
+        if (c->T > kMaxExpertChoiceTokens) return MOE_ERR_UNSUPPORTED;
+    }
     return MOE_OK;
 }
 
@@ -116,6 +130,25 @@ static moe_status to_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : 
 static cudaError_t run_ffn(const moe_config &c, const FfnGroup &g, uint32_t *err, cudaStream_t s) {
     const bool simt = c.dtype == MOE_F32 || (c.debug_flags & MOE_DEBUG_FORCE_SIMT_FFN);
     return simt ? launch_ffn_simt(c, g, err, s) : launch_ffn_tc(c, g, err, s);
+}
+
+// The shared expert S(x) of every token into the workspace (hidden and output).
+static cudaError_t run_shared_expert(const moe_config &c, const void *x, const void *sw_gate, const void *sw_up,
+                                     const void *sw_down, uint8_t *w, const WsLayout &L, uint32_t *err,
+                                     cudaStream_t s) {
+    FfnGroup g{};
+    g.n_seg = 0;
+    g.act = MOE_ACT_SILU_GATED;
+    g.h = c.h;
+    g.sh_rows = c.T;
+    g.sh_a = x;
+    g.sh_w_gate = sw_gate;
+    g.sh_w_up = sw_up;
+    g.sh_w_down = sw_down;
+    g.sh_hid = w + L.hid_sh;
+    g.sh_out = w + L.s_out;
+    g.h_sh = c.h_shared;
+    return run_ffn(c, g, err, s);
 }
 
 }  // namespace moe
@@ -149,6 +182,7 @@ moe_status moe_router_topk(const moe_config *cfg, const void *x, const float *w_
     moe_status st = validate(cfg);
     if (st != MOE_OK) return st;
     const moe_config &c = *cfg;
+    if (c.routing != MOE_ROUTING_TOKEN_CHOICE) return MOE_ERR_UNSUPPORTED;
     if (!x || !w_r || !topk_idx || !topk_gate || !expert_offsets || !slot_row || !perm_token)
         return MOE_ERR_INVALID_ARG;
     if (c.has_router_bias && !b_r) return MOE_ERR_INVALID_ARG;
@@ -168,6 +202,7 @@ moe_status moe_router_topk_train(const moe_config *cfg, const void *x, const flo
     moe_status st = validate(cfg);
     if (st != MOE_OK) return st;
     const moe_config &c = *cfg;
+    if (c.routing != MOE_ROUTING_TOKEN_CHOICE) return MOE_ERR_UNSUPPORTED;
     if (!x || !w_r || !topk_idx || !topk_gate || !expert_offsets || !slot_row || !perm_token)
         return MOE_ERR_INVALID_ARG;
     if (c.has_router_bias && !b_r) return MOE_ERR_INVALID_ARG;
@@ -189,6 +224,7 @@ moe_status moe_router_shard_stats(const moe_config *cfg, const void *x, const fl
     moe_status st = validate(cfg);
     if (st != MOE_OK) return st;
     const moe_config &c = *cfg;
+    if (c.routing != MOE_ROUTING_TOKEN_CHOICE) return MOE_ERR_UNSUPPORTED;
     if (c.cap_num != 0 || c.cap_den != 0) return MOE_ERR_INVALID_ARG;  // the capacity is global
     if (!x || !w_r || !topk_idx || !topk_gate || !slot_counts) return MOE_ERR_INVALID_ARG;
     if (c.has_router_bias && !b_r) return MOE_ERR_INVALID_ARG;
@@ -207,6 +243,7 @@ moe_status moe_router_shard_assign(const moe_config *cfg, const int32_t *topk_id
     moe_status st = validate(cfg);
     if (st != MOE_OK) return st;
     const moe_config &c = *cfg;
+    if (c.routing != MOE_ROUTING_TOKEN_CHOICE) return MOE_ERR_UNSUPPORTED;
     if (c.cap_num != 0 || c.cap_den != 0) return MOE_ERR_INVALID_ARG;
     if (!topk_idx || !slot_base || !expert_offsets || !slot_row || !perm_token) return MOE_ERR_INVALID_ARG;
     if (capacity < 0 || global_T < c.T) return MOE_ERR_INVALID_ARG;
@@ -217,6 +254,53 @@ moe_status moe_router_shard_assign(const moe_config *cfg, const int32_t *topk_id
                                           aux ? global_prob_sums : nullptr, (float)global_T, counts_kept,
                                           expert_offsets, slot_row, perm_token, aux, static_cast<uint8_t *>(ws),
                                           stream));
+}
+
+moe_status moe_router_expert_choice(const moe_config *cfg, const void *x, const float *w_r, const float *b_r,
+                                   int32_t *expert_offsets, int32_t *perm_token, float *row_gate,
+                                   int32_t *token_ptr, int32_t *token_rows, void *ws, size_t ws_bytes,
+                                   cudaStream_t stream) {
+    moe_status st = validate(cfg);
+    if (st != MOE_OK) return st;
+    const moe_config &c = *cfg;
+    if (c.routing != MOE_ROUTING_EXPERT_CHOICE) return MOE_ERR_UNSUPPORTED;
+    if (!x || !w_r || !expert_offsets || !perm_token || !row_gate || !token_ptr || !token_rows)
+        return MOE_ERR_INVALID_ARG;
+    if (c.has_router_bias && !b_r) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w_r)) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(c);
+    if ((st = check_ws(ws, ws_bytes, L.total)) != MOE_OK) return st;
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    float *logits = reinterpret_cast<float *>(w + L.logits);
+    cudaError_t e = launch_router_logits(c, x, w_r, c.has_router_bias ? b_r : nullptr, logits, w, stream);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    return to_status(launch_expert_choice(c, logits, expert_offsets, perm_token, row_gate, token_ptr, token_rows,
+                                          w, stream));
+}
+
+moe_status moe_combine_expert_choice(const moe_config *cfg, const void *x, const void *y_perm,
+                                     const int32_t *token_ptr, const int32_t *token_rows, const float *row_gate,
+                                     const void *shared_w_gate, const void *shared_w_up,
+                                     const void *shared_w_down, void *y, void *ws, size_t ws_bytes,
+                                     cudaStream_t stream) {
+    moe_status st = validate(cfg);
+    if (st != MOE_OK) return st;
+    const moe_config &c = *cfg;
+    if (c.routing != MOE_ROUTING_EXPERT_CHOICE) return MOE_ERR_UNSUPPORTED;
+    if (!x || !y_perm || !token_ptr || !token_rows || !row_gate || !y) return MOE_ERR_INVALID_ARG;
+    if (c.h_shared && (!shared_w_gate || !shared_w_up || !shared_w_down)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(y_perm) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(c);
+    if ((st = check_ws(ws, ws_bytes, L.offsets)) != MOE_OK) return st;
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    uint32_t *err = reinterpret_cast<uint32_t *>(w + L.err);
+    const void *s_out = nullptr;
+    if (c.h_shared) {
+        cudaError_t e = run_shared_expert(c, x, shared_w_gate, shared_w_up, shared_w_down, w, L, err, stream);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+        s_out = w + L.s_out;
+    }
+    return to_status(launch_combine_ec(c, x, y_perm, s_out, token_ptr, token_rows, row_gate, y, err, stream));
 }
 
 moe_status moe_dispatch(const moe_config *cfg, const void *x, const int32_t *perm_token,
@@ -269,6 +353,7 @@ moe_status moe_combine(const moe_config *cfg, const void *x, const void *y_perm,
     moe_status st = validate(cfg);
     if (st != MOE_OK) return st;
     const moe_config &c = *cfg;
+    if (c.routing != MOE_ROUTING_TOKEN_CHOICE) return MOE_ERR_UNSUPPORTED;
     if (!x || !y_perm || !slot_row || !topk_gate || !y) return MOE_ERR_INVALID_ARG;
     if (c.h_shared && (!shared_w_gate || !shared_w_up || !shared_w_down)) return MOE_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(y_perm) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
@@ -278,23 +363,25 @@ moe_status moe_combine(const moe_config *cfg, const void *x, const void *y_perm,
     uint32_t *err = reinterpret_cast<uint32_t *>(w + L.err);
     const void *s_out = nullptr;
     if (c.h_shared) {
-        FfnGroup g{};
-        g.n_seg = 0;
-        g.act = MOE_ACT_SILU_GATED;
-        g.h = c.h;
-        g.sh_rows = c.T;
-        g.sh_a = x;
-        g.sh_w_gate = shared_w_gate;
-        g.sh_w_up = shared_w_up;
-        g.sh_w_down = shared_w_down;
-        g.sh_hid = w + L.hid_sh;
-        g.sh_out = w + L.s_out;
-        g.h_sh = c.h_shared;
-        cudaError_t e = run_ffn(c, g, err, stream);
+        cudaError_t e = run_shared_expert(c, x, shared_w_gate, shared_w_up, shared_w_down, w, L, err, stream);
         if (e != cudaSuccess) return MOE_ERR_CUDA;
         s_out = w + L.s_out;
     }
     return to_status(launch_combine(c, x, y_perm, s_out, slot_row, topk_gate, y, err, stream));
+}
+
+// Expert Choice: every expert takes Ce = min(C, T) tokens.
+__global__ void k_fill_counts(int32_t *a, int32_t *b, int n, int32_t v) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) {
+        if (a) a[i] = v;
+        if (b) b[i] = v;
+    }
+}
+
+static cudaError_t fill_counts(const moe_config &c, int32_t *routed, int32_t *kept, cudaStream_t s) {
+    k_fill_counts<<<(c.N + 255) / 256, 256, 0, s>>>(routed, kept, c.N, (int32_t)(max_rows(c) / c.N));
+    return cudaGetLastError();
 }
 
 static moe_status forward_impl(const moe_config *cfg, const void *x, const float *w_r, const float *b_r,
@@ -319,6 +406,8 @@ static moe_status forward_impl(const moe_config *cfg, const void *x, const float
     uint32_t *err = reinterpret_cast<uint32_t *>(w + L.err);
     auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], stream) : cudaSuccess; };
 
+    const bool ec = c.routing == MOE_ROUTING_EXPERT_CHOICE;
+    if (ec && (topk_idx || topk_gate || aux)) return MOE_ERR_INVALID_ARG;  // token-choice outputs
     RouterOut o;
     o.topk_idx = topk_idx ? topk_idx : reinterpret_cast<int32_t *>(w + L.topk_idx);
     o.topk_gate = topk_gate ? topk_gate : reinterpret_cast<float *>(w + L.topk_gate);
@@ -328,8 +417,22 @@ static moe_status forward_impl(const moe_config *cfg, const void *x, const float
     o.slot_row = reinterpret_cast<int32_t *>(w + L.slot_row);
     o.perm_token = reinterpret_cast<int32_t *>(w + L.perm_token);
     o.aux = aux ? aux : reinterpret_cast<float *>(w + L.aux);
+    int32_t *ec_tok_ptr = reinterpret_cast<int32_t *>(w + L.ec_tok_ptr);
+    int32_t *ec_tok_rows = reinterpret_cast<int32_t *>(w + L.ec_tok_rows);
+    float *ec_row_gate = reinterpret_cast<float *>(w + L.ec_row_gate);
     if (mark(0) != cudaSuccess) return MOE_ERR_CUDA;
-    cudaError_t e = launch_router(c, x, w_r, c.has_router_bias ? b_r : nullptr, o, w, stream);
+    cudaError_t e;
+    if (ec) {
+        float *logits = reinterpret_cast<float *>(w + L.logits);
+        e = launch_router_logits(c, x, w_r, c.has_router_bias ? b_r : nullptr, logits, w, stream);
+        if (e == cudaSuccess)
+            e = launch_expert_choice(c, logits, o.expert_offsets, o.perm_token, ec_row_gate, ec_tok_ptr, ec_tok_rows,
+                                     w, stream);
+        if (e == cudaSuccess && (counts_routed || counts_kept))
+            e = fill_counts(c, counts_routed, counts_kept, stream);
+    } else {
+        e = launch_router(c, x, w_r, c.has_router_bias ? b_r : nullptr, o, w, stream);
+    }
     if (e != cudaSuccess || mark(1) != cudaSuccess) return MOE_ERR_CUDA;
 
     void *x_perm = w + L.x_perm, *y_perm = w + L.y_perm;
@@ -362,8 +465,12 @@ static moe_status forward_impl(const moe_config *cfg, const void *x, const float
     e = run_ffn(c, g, err, stream);
     if (e != cudaSuccess || mark(4) != cudaSuccess) return MOE_ERR_CUDA;
 
-    e = launch_combine(c, x, y_perm, c.h_shared ? w + L.s_out : nullptr, o.slot_row, o.topk_gate, y, err,
-                       stream);
+    if (ec)
+        e = launch_combine_ec(c, x, y_perm, c.h_shared ? w + L.s_out : nullptr, ec_tok_ptr, ec_tok_rows, ec_row_gate,
+                              y, err, stream);
+    else
+        e = launch_combine(c, x, y_perm, c.h_shared ? w + L.s_out : nullptr, o.slot_row, o.topk_gate, y, err,
+                           stream);
     if (e != cudaSuccess || mark(5) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
 }

@@ -53,6 +53,7 @@ extern "C" moe_status moe_router_topk_noalloc(const moe_config *cfg, const void 
     moe_status st = moe_validate_config(cfg);
     if (st != MOE_OK) return st;
     const moe_config &c = *cfg;
+    if (c.routing != MOE_ROUTING_TOKEN_CHOICE) return MOE_ERR_UNSUPPORTED;
     if (!x || !w_r || !topk_idx || !topk_gate || !expert_offsets || !slot_row || !perm_token)
         return MOE_ERR_INVALID_ARG;
     if (c.has_router_bias && !b_r) return MOE_ERR_INVALID_ARG;

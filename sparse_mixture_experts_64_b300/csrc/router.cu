@@ -881,17 +881,24 @@ cudaError_t launch_small(const moe_config &c, const XT *x, const float *w_t, con
 }
 
 template <typename XT>
-cudaError_t launch_large(const moe_config &c, const XT *x, const float *w_t, const float *b_r, RouterArgs ra,
-                         float *logits, cudaStream_t s) {
+cudaError_t launch_logits_only(const moe_config &c, const XT *x, const float *w_t, const float *b_r, int has_bias,
+                               float *logits, uint32_t *err, cudaStream_t s) {
     CUtensorMap tmx;
     if (!token_map<XT>(&tmx, x, c.T, c.d, 16)) return cudaErrorInvalidValue;
-    LogitsArgs la{c.T, c.d, c.N, ra.has_bias, logits, ra.err};
+    LogitsArgs la{c.T, c.d, c.N, has_bias, logits, err};
     const size_t stage = ((size_t)16 * 256 * sizeof(XT) + (size_t)32 * 256 * 4 + 1023) & ~(size_t)1023;
     const size_t lbytes = 4 * stage + 1024;
     cudaError_t e = cudaFuncSetAttribute(k_logits_large<XT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lbytes);
     if (e != cudaSuccess) return e;
     k_logits_large<XT><<<dim3((c.N + 31) / 32, (c.T + 15) / 16), 544, lbytes, s>>>(tmx, w_t, b_r, la);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+template <typename XT>
+cudaError_t launch_large(const moe_config &c, const XT *x, const float *w_t, const float *b_r, RouterArgs ra,
+                         float *logits, cudaStream_t s) {
+    cudaError_t e = launch_logits_only<XT>(c, x, w_t, b_r, ra.has_bias, logits, ra.err, s);
+    if (e != cudaSuccess) return e;
     const size_t gbytes = ((size_t)64 * c.N + 64 * 8) * sizeof(float);
     e = cudaFuncSetAttribute(k_gate, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gbytes);
     if (e != cudaSuccess) return e;
@@ -913,6 +920,20 @@ cudaError_t launch_logits_gate(const moe_config &c, const XT *x, const float *w_
 }
 
 }  // namespace
+
+cudaError_t launch_router_logits(const moe_config &c, const void *x, const float *w_r, const float *b_r,
+                                 float *logits, uint8_t *ws, cudaStream_t s) {
+    const WsLayout L = ws_layout(c);
+    uint32_t *err = reinterpret_cast<uint32_t *>(ws + L.err);
+    float *w_t = reinterpret_cast<float *>(ws + L.w_t);
+    k_transpose_wr<<<dim3((c.d + 31) / 32, (c.N + 31) / 32), 256, 0, s>>>(w_r, w_t, c.d, c.N);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int hb = c.has_router_bias && b_r ? 1 : 0;
+    if (c.dtype == MOE_BF16)
+        return launch_logits_only<__nv_bfloat16>(c, static_cast<const __nv_bfloat16 *>(x), w_t, b_r, hb, logits, err, s);
+    return launch_logits_only<float>(c, static_cast<const float *>(x), w_t, b_r, hb, logits, err, s);
+}
 
 cudaError_t launch_router_stats(const moe_config &c, const void *x, const float *w_r, const float *b_r,
                                 int32_t *topk_idx, float *topk_gate, int32_t *slot_counts, float *prob_sums,

@@ -136,6 +136,39 @@ def test_null_pointers_rejected_before_launch():
     assert st == moe.MOE_ERR_INVALID_ARG
 
 
+def test_expert_choice_config_rules():
+    """Expert Choice needs a capacity factor and T <= 16384; its rows are N * min(C, T);
+    the token-choice calls refuse it and its forward takes no token-choice outputs."""
+    assert moe.moe_validate_config(_cfg(routing="expert_choice")) == moe.MOE_ERR_INVALID_ARG
+    ec = _cfg(routing="expert_choice", capacity_factor=(2, 1))
+    assert moe.moe_validate_config(ec) == moe.MOE_OK
+    assert moe.moe_max_rows(ec) == 8 * 16                            # N * ceil(64 * 2 / 8)
+    big = _cfg(routing="expert_choice", capacity_factor=(1, 1), T=16385)
+    assert moe.moe_validate_config(big) == moe.MOE_ERR_UNSUPPORTED
+    whole = _cfg(routing="expert_choice", capacity_factor=(64, 1))  # C >= T: every token
+    assert moe.moe_max_rows(whole) == 8 * 64
+    bad = _cfg(routing=7)
+    assert moe.moe_validate_config(bad) == moe.MOE_ERR_INVALID_ARG
+    cp = ctypes.byref(ec)
+    ws = moe.moe_workspace_size(ec)
+    assert _raw("moe_router_topk", cp, FAKE, FAKE, None, FAKE, FAKE, None, None, FAKE, FAKE, FAKE,
+                None, FAKE, ws, None) == moe.MOE_ERR_UNSUPPORTED
+    assert _raw("moe_combine", cp, FAKE, FAKE, FAKE, FAKE, None, None, None, FAKE, FAKE, ws,
+                None) == moe.MOE_ERR_UNSUPPORTED
+    assert _raw("moe_router_topk_noalloc", cp, FAKE, FAKE, None, FAKE, FAKE, None, None, FAKE,
+                FAKE, FAKE, None, None) == moe.MOE_ERR_UNSUPPORTED
+    tc = _cfg()
+    assert _raw("moe_router_expert_choice", ctypes.byref(tc), FAKE, FAKE, None, FAKE, FAKE, FAKE,
+                FAKE, FAKE, FAKE, moe.moe_workspace_size(tc), None) == moe.MOE_ERR_UNSUPPORTED
+    # forward with a token-choice output pointer
+    st = _raw("moe_forward", cp, FAKE, FAKE, None, FAKE, FAKE, FAKE, None, None, None, FAKE,
+              FAKE, None, None, None, None, FAKE, ws, None)
+    assert st == moe.MOE_ERR_INVALID_ARG
+    # missing list outputs
+    assert _raw("moe_router_expert_choice", cp, FAKE, FAKE, None, FAKE, FAKE, FAKE, None, FAKE,
+                FAKE, ws, None) == moe.MOE_ERR_INVALID_ARG
+
+
 def test_workspace_checks_before_launch():
     c = _cfg()
     cp = ctypes.byref(c)

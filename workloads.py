@@ -46,6 +46,7 @@ class Workload:
     act: str = "silu_gated"             # or "relu"
     capacity_factor: tuple | None = None  # (num, den) or None for no limit
     router_bias: bool = False
+    routing: str = "token_choice"       # or "expert_choice" (capacity_factor = experts per token)
 
     def replace(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -64,6 +65,11 @@ WORKLOADS = {
     "mixtral_decode_128": Workload("mixtral_decode_128", 4, T=128, d=4096, N=8, k=2, h=14336),
     "deepseek_fine": Workload("deepseek_fine", 5, T=8192, d=7168, N=256, k=8, h=2048,
                               h_shared=2048, gating="softmax_then_topk", act="silu_gated"),
+    # Expert Choice on the Mixtral prefill layer (same seeds, so the same inputs):
+    # every expert takes C = T * 2 / N tokens, two experts per token on average
+    "mixtral_expert_choice": Workload("mixtral_expert_choice", 3, T=4096, d=4096, N=8, k=2,
+                                      h=14336, act="silu_gated", capacity_factor=(2, 1),
+                                      routing="expert_choice"),
 }
 
 
