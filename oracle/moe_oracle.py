@@ -506,6 +506,116 @@ def forward(cfg, inp: dict, tokens=None) -> dict:
     return rt
 
 
+# ------------------------------------------------------------------------- backward
+
+def _silu_parts(A):
+    sig = 1.0 / (1.0 + np.exp(-A))
+    return A * sig, sig * (1.0 + A * (1.0 - sig))     # SiLU(A) and its derivative
+
+
+def expert_ffn_backward(X, dO, w_a, w_b, w_out, act: str):
+    """One expert's FFN backward on its rows, float64: given dO = dLoss/dO for
+    O = FFN(X), returns (dX, dW_a, dW_b, dW_out) by the chain rule through
+    O = H W_outᵀ, H = SiLU(X W_aᵀ) ⊙ (X W_bᵀ) (gated) or H = max(0, X W_aᵀ) (ReLU):
+      dH = dO W_out,  dW_out = dOᵀ H,
+      gated: dA = dH ⊙ B ⊙ SiLU'(A), dB = dH ⊙ SiLU(A), SiLU'(z) = σ(z)(1 + z(1 - σ(z)));
+      ReLU:  dA = dH ⊙ [A > 0];
+      dW_a = dAᵀ X, dW_b = dBᵀ X, dX = dA W_a + dB W_b.
+    """
+    X = np.asarray(X, np.float64)
+    wa = np.asarray(w_a, np.float64)
+    wo = np.asarray(w_out, np.float64)
+    A = X @ wa.T
+    if act == "silu_gated":
+        wb = np.asarray(w_b, np.float64)
+        B = X @ wb.T
+        sA, dsA = _silu_parts(A)
+        H = sA * B
+        dH = dO @ wo
+        dA = dH * B * dsA
+        dB = dH * sA
+        return dA @ wa + dB @ wb, dA.T @ X, dB.T @ X, dO.T @ H
+    if act == "relu":
+        H = np.maximum(A, 0.0)
+        dH = dO @ wo
+        dA = dH * (A > 0)
+        return dA @ wa, dA.T @ X, None, dO.T @ H
+    raise ValueError(act)
+
+
+def backward(cfg, inp: dict, dy, aux_coef: float = 0.0, z_coef: float = 0.0) -> dict:
+    """Gradients of  Loss = sum(dy ⊙ y) + aux_coef * aux[0] + z_coef * z  (float64).
+
+    The routing decisions (selections, capacity drops) are held fixed: they are
+    piecewise constant in the inputs. With O_r = FFN_e(x_t) the output of row r =
+    (t, j) and g_tj its gate:
+      dO_r = g_tj dy_t;  dg_tj = <dy_t, O_r> (0 for a dropped slot);
+      expert weights and dX_r from expert_ffn_backward; dx_t = dy_t + sum_j dX_r
+      + the shared expert's dx + the router's dx;
+      router: dL from the gates (softmax over the k selected logits, or the full
+      softmax at the selected experts), from the aux loss N sum_e f_e P_e (f held
+      fixed, dP_e = N f_e) and from the z-loss (d lse_t / dL = softmax p_t);
+      dW_r = xᵀ dL, db = sum_t dL_t, dx += dL W_rᵀ.
+    Returns dx [T][d], dw_r [d][N], db_r [N] (or None), dw_gate / dw_up / dw_down as
+    lists over experts (None for an expert without rows), shared-expert gradients
+    (or None), and the routing it used.
+    """
+    x32 = np.asarray(inp["x"], np.float32)
+    x = x32.astype(np.float64)
+    T, d = x.shape
+    N, k = cfg.N, cfg.k
+    dy = np.asarray(dy, np.float64)
+    rt = route(cfg, x32, inp["w_r"], inp.get("b_r"))
+    idx, kept, g = rt["topk_idx"], rt["kept"], rt["topk_gate"]
+    dx = dy.copy()
+    dg = np.zeros((T, k))
+    dwa, dwb, dwo = [None] * N, [None] * N, [None] * N
+    for e in range(N):
+        sel = [(t, j) for t in range(T) for j in range(k) if kept[t, j] and idx[t, j] == e]
+        if not sel:
+            continue
+        ts = np.array([t for t, _ in sel])
+        js = np.array([j for _, j in sel])
+        wu = None if inp.get("w_up") is None else inp["w_up"][e]
+        O = expert_ffn(x[ts], inp["w_gate"][e], wu, inp["w_down"][e], cfg.act)
+        dg[ts, js] = np.sum(dy[ts] * O, axis=1)
+        dO = g[ts, js][:, None] * dy[ts]
+        dX, dwa[e], dwb[e], dwo[e] = expert_ffn_backward(x[ts], dO, inp["w_gate"][e], wu, inp["w_down"][e],
+                                                          cfg.act)
+        np.add.at(dx, ts, dX)
+    sh = None
+    if cfg.h_shared:
+        dXs, a_, b_, o_ = expert_ffn_backward(x, dy, inp["shared_w_gate"], inp["shared_w_up"],
+                                               inp["shared_w_down"], "silu_gated")
+        dx += dXs
+        sh = dict(dw_gate=a_, dw_up=b_, dw_down=o_)
+    # router
+    L = rt["logits"].astype(np.float64)
+    p = rt["p"]
+    dL = np.zeros((T, N))
+    for t in range(T):
+        sel = idx[t]
+        if cfg.gating == GATING_TOPK_THEN_SOFTMAX:
+            gt = g[t]
+            dL[t, sel] += gt * (dg[t] - np.sum(gt * dg[t]))
+        else:
+            dp = np.zeros(N)
+            dp[sel] = dg[t]
+            dL[t] += p[t] * (dp - np.sum(p[t] * dp))
+    if aux_coef:
+        f = rt["counts_routed"].astype(np.float64) / float(T * k)
+        dp = np.broadcast_to(aux_coef * N * f / T, (T, N))
+        dL += p * (dp - np.sum(p * dp, axis=1, keepdims=True))
+    if z_coef:
+        m = L.max(axis=1, keepdims=True)
+        lse = m[:, 0] + np.log(np.exp(L - m).sum(axis=1))
+        dL += z_coef * (2.0 * lse / T)[:, None] * p
+    w_r = np.asarray(inp["w_r"], np.float64)
+    dx += dL @ w_r.T
+    return dict(dx=dx, dw_r=x.T @ dL, db_r=dL.sum(axis=0) if inp.get("b_r") is not None else None,
+                dlogits=dL, dw_gate=dwa, dw_up=dwb, dw_down=dwo, shared=sh, route=rt, dgate=dg)
+
+
 def forward_dense(cfg, inp: dict) -> np.ndarray:
     """Brute-force dense evaluation of the DeepSeekMoE equation on tiny inputs.
 

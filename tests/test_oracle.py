@@ -571,13 +571,134 @@ def pin_ec_dense_brute_force(O):
             assert np.array_equal(rt["y"][unchosen], x[unchosen])
 
 
+# ------------------------------------------------------------------------- backward
+
+def _torch_loss(cfg, inp, rt, dy, aux_coef, z_coef):
+    """The layer's loss in torch float64 with the routing of `rt` held fixed; the
+    logits take the oracle's fp32 values with the gradient of x W_r + b."""
+    T, N, k = cfg.T, cfg.N, cfg.k
+    t64 = lambda a: torch.tensor(np.asarray(a, np.float64), requires_grad=True)  # noqa: E731
+    x, w_r = t64(inp["x"]), t64(inp["w_r"])
+    b = t64(inp["b_r"]) if inp.get("b_r") is not None else None
+    lin = x @ w_r + (b if b is not None else 0.0)
+    L = torch.tensor(rt["logits"].astype(np.float64)) + (lin - lin.detach())
+    p = torch.softmax(L, dim=1)
+    idx = torch.tensor(rt["topk_idx"], dtype=torch.long)
+    if cfg.gating == O.GATING_TOPK_THEN_SOFTMAX:
+        g = torch.softmax(torch.gather(L, 1, idx), dim=1)
+    else:
+        g = torch.gather(p, 1, idx)
+    W = {n: [t64(inp[n][e]) for e in range(N)] if inp.get(n) is not None else None
+         for n in ("w_gate", "w_up", "w_down")}
+    y = x.clone()
+    for t in range(T):
+        for j in range(k):
+            if rt["kept"][t, j]:
+                e = int(idx[t, j])
+                a = W["w_gate"][e] @ x[t]
+                hdn = torch.nn.functional.silu(a) * (W["w_up"][e] @ x[t]) if cfg.act == "silu_gated" else torch.relu(a)
+                y[t] = y[t] + g[t, j] * (W["w_down"][e] @ hdn)
+    sh = None
+    if cfg.h_shared:
+        sh = [t64(inp[n]) for n in ("shared_w_gate", "shared_w_up", "shared_w_down")]
+        y = y + (torch.nn.functional.silu(x @ sh[0].T) * (x @ sh[1].T)) @ sh[2].T
+    loss = torch.sum(torch.tensor(np.asarray(dy, np.float64)) * y)
+    if aux_coef:
+        f = torch.tensor(rt["counts_routed"], dtype=torch.float64) / (T * k)
+        loss = loss + aux_coef * N * torch.sum(f * p.mean(dim=0))
+    if z_coef:
+        loss = loss + z_coef * torch.mean(torch.logsumexp(L, dim=1) ** 2)
+    loss.backward()
+    return x, w_r, b, W, sh
+
+
+def pin_backward_autograd(O):
+    """Every gradient equals torch autograd of the same loss (routing held fixed):
+    both gating conventions, SiLU-gated and ReLU experts, a shared expert, router
+    bias, capacity drops, the aux and z terms."""
+    rng = np.random.default_rng(31)
+    for kw in (dict(gating=O.GATING_TOPK_THEN_SOFTMAX, hs=5, bias=False, cf=None),
+               dict(gating=O.GATING_SOFTMAX_THEN_TOPK, hs=0, bias=True, cf=(1, 1)),
+               dict(gating=O.GATING_SOFTMAX_THEN_TOPK, hs=6, bias=False, cf=None, act="relu")):
+        act = kw.pop("act", "silu_gated")
+        cfg, inp = _rand_layer(rng, T=11, d=6, N=4, k=2, h=5, act=act, **kw)
+        dy = rng.standard_normal((cfg.T, cfg.d))
+        gb = O.backward(cfg, inp, dy, aux_coef=0.3, z_coef=0.05)
+        x, w_r, b, W, sh = _torch_loss(cfg, inp, gb["route"], dy, 0.3, 0.05)
+        close = lambda a, ref: np.allclose(a, ref.grad.numpy(), rtol=1e-9, atol=1e-11)  # noqa: E731
+        assert close(gb["dx"], x) and close(gb["dw_r"], w_r)
+        if b is not None:
+            assert close(gb["db_r"], b)
+        for e in range(cfg.N):
+            for n, key in (("w_gate", "dw_gate"), ("w_up", "dw_up"), ("w_down", "dw_down")):
+                if W[n] is None:
+                    continue
+                want = W[n][e].grad
+                got = gb[key][e]
+                if want is None:
+                    assert got is None
+                else:
+                    assert got is not None and np.allclose(got, want.numpy(), rtol=1e-9, atol=1e-11)
+        if sh is not None:
+            for tsr, key in zip(sh, ("dw_gate", "dw_up", "dw_down")):
+                assert np.allclose(gb["shared"][key], tsr.grad.numpy(), rtol=1e-9, atol=1e-11)
+
+
+def pin_backward_finite_differences(O):
+    """Central differences of the loss in float64 along expert and shared-expert
+    weight coordinates (the routing does not move with them)."""
+    rng = np.random.default_rng(32)
+    cfg, inp = _rand_layer(rng, T=9, d=5, N=3, k=2, h=4, hs=3)
+    dy = rng.standard_normal((cfg.T, cfg.d))
+    gb = O.backward(cfg, inp, dy)
+
+    def loss():
+        return float(np.sum(dy * O.forward(cfg, inp)["y"]))
+    eps = 1e-6
+    for name, key, e in (("w_gate", "dw_gate", 0), ("w_up", "dw_up", 1), ("w_down", "dw_down", 2),
+                         ("shared_w_gate", None, None), ("shared_w_down", None, None)):
+        for _ in range(3):
+            tgt = inp[name][e] if e is not None else inp[name]
+            i, j = rng.integers(tgt.shape[0]), rng.integers(tgt.shape[1])
+            keep = tgt[i, j]
+            tgt[i, j] = keep + eps
+            lp = loss()
+            tgt[i, j] = keep - eps
+            lm = loss()
+            tgt[i, j] = keep
+            fd = (lp - lm) / (2 * eps)
+            an = (gb[key][e] if e is not None else gb["shared"][name.replace("shared_", "d")])[i, j]
+            assert abs(fd - an) <= 1e-6 * max(1.0, abs(an))
+
+
+def pin_backward_special_cases(O):
+    """dy = 0 without aux or z: every gradient is zero. One expert with top-1 and
+    top-k-then-softmax: the gate is 1, so the router gets no gradient and dx is
+    dy plus the dense MLP's input gradient (torch autograd)."""
+    rng = np.random.default_rng(33)
+    cfg, inp = _rand_layer(rng, T=7, d=6, N=3, k=2, h=4, hs=2)
+    gb = O.backward(cfg, inp, np.zeros((cfg.T, cfg.d)))
+    assert not np.any(gb["dx"]) and not np.any(gb["dw_r"])
+    assert all(w is None or not np.any(w) for w in gb["dw_gate"] + gb["dw_down"])
+    cfg, inp = _rand_layer(rng, T=8, d=6, N=1, k=1, h=5)
+    dy = rng.standard_normal((cfg.T, cfg.d))
+    gb = O.backward(cfg, inp, dy)
+    assert np.allclose(gb["dlogits"], 0.0, atol=1e-15) and np.allclose(gb["dw_r"], 0.0, atol=1e-14)
+    x = torch.tensor(inp["x"].astype(np.float64), requires_grad=True)
+    wg, wu, wd = (torch.tensor(np.asarray(inp[n][0], np.float64)) for n in ("w_gate", "w_up", "w_down"))
+    y = x + (torch.nn.functional.silu(x @ wg.T) * (x @ wu.T)) @ wd.T
+    torch.sum(torch.tensor(dy) * y).backward()
+    assert np.allclose(gb["dx"], x.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
 PINS = [pin_router_logits_exact, pin_router_logits_error_bound, pin_topk_brute_force,
         pin_worked_example, pin_three_token_dispatch, pin_softmax_library, pin_aux_closed_forms,
         pin_capacity, pin_single_expert_is_dense_mlp, pin_identical_experts,
         pin_dense_brute_force, pin_dropped_tokens_are_residual, pin_noisy_logits_exact,
         pin_noisy_selection, pin_route_train_without_noise, pin_z_loss_closed_forms, pin_ec_exp,
         pin_ec_scores, pin_ec_selection_brute_force, pin_ec_dispatch_and_balance,
-        pin_ec_dense_brute_force]
+        pin_ec_dense_brute_force, pin_backward_autograd, pin_backward_finite_differences,
+        pin_backward_special_cases]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -760,6 +881,29 @@ def _mut_ec_exp_short_series(mp):
                .astype(np.float32))
 
 
+def _mut_bwd_sigmoid_for_silu_derivative(mp):
+    mp.setattr(O, "_silu_parts", lambda A: (A / (1.0 + np.exp(-A)), 1.0 / (1.0 + np.exp(-A))))
+
+
+def _mut_bwd_no_residual_gradient(mp):
+    real = O.backward
+
+    def bw(cfg, inp, dy, **kw):
+        out = real(cfg, inp, dy, **kw)
+        out["dx"] = out["dx"] - np.asarray(dy, np.float64)
+        return out
+    mp.setattr(O, "backward", bw)
+
+
+def _mut_bwd_down_grad_sign(mp):
+    real = O.expert_ffn_backward
+
+    def fb(X, dO, wa, wb, wo, act):
+        dX, da, db, do = real(X, dO, wa, wb, wo, act)
+        return dX, da, db, -do
+    mp.setattr(O, "expert_ffn_backward", fb)
+
+
 MUTATIONS = [
     (_mut_tie_high_index, pin_topk_brute_force),
     (_mut_swap_gating, pin_worked_example),
@@ -781,6 +925,9 @@ MUTATIONS = [
     (_mut_ec_select_by_logits, pin_ec_dense_brute_force),
     (_mut_ec_rows_by_score, pin_ec_dispatch_and_balance),
     (_mut_ec_exp_short_series, pin_ec_exp),
+    (_mut_bwd_sigmoid_for_silu_derivative, pin_backward_autograd),
+    (_mut_bwd_no_residual_gradient, pin_backward_special_cases),
+    (_mut_bwd_down_grad_sign, pin_backward_finite_differences),
 ]
 
 
