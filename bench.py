@@ -368,6 +368,57 @@ def measure_router_train(w, inp, cfg, ws, stream, dev, cpu_tokens: int) -> dict:
     return out
 
 
+def measure_backward(w, inp, cfg, ws, stream, dev, peaks, host_inp=None, cpu_tokens: int = 16) -> dict:
+    """moe_backward after one moe_forward on the same inputs: CUDA-event time per
+    backward, its algorithmic FLOPs against the bf16 peak, and the oracle's backward
+    timed on a token slice of the same layer."""
+    import sparse_mixture_experts_64_b300 as moe
+    T, d, N, k = w.T, w.d, w.N, w.k
+    bws = moe.backward_workspace(cfg, device=dev)
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    gate = torch.empty((T, k), device=dev)
+    y = torch.empty((T, d), dtype=inp["x"].dtype, device=dev)
+    kept = torch.empty(N, dtype=torch.int32, device=dev)
+    moe.moe_forward(cfg, inp["x"], inp["w_r"], inp["b_r"], inp["w_gate"], inp["w_up"], inp["w_down"],
+                    inp["shared_w_gate"], inp["shared_w_up"], inp["shared_w_down"], y, idx, gate, None, kept,
+                    None, ws, stream)
+    g = torch.Generator(device=dev).manual_seed(17)
+    dy = torch.randn((T, d), device=dev, generator=g).to(inp["x"].dtype)
+    e = lambda t: None if t is None else torch.empty_like(t)  # noqa: E731
+    out = [e(inp["x"]), e(inp["w_r"]), e(inp["b_r"]), e(inp["w_gate"]), e(inp["w_up"]), e(inp["w_down"]),
+           e(inp["shared_w_gate"]), e(inp["shared_w_up"]), e(inp["shared_w_down"])]
+
+    def bwd():
+        moe.moe_backward(cfg, inp["x"], inp["w_r"], inp["b_r"], inp["w_gate"], inp["w_up"], inp["w_down"],
+                         inp["shared_w_gate"], inp["shared_w_up"], inp["shared_w_down"], idx, gate, dy, 0.01, 0.001,
+                         *out, ws, bws, stream)
+    ms = _time_calls(bwd, stream, 10)
+    st = moe.moe_check_error(ws, stream)
+    if st != moe.MOE_OK:
+        raise RuntimeError("device error word: " + moe.status_str(st))
+    R = int(kept.sum().item())
+    gated = w.act == "silu_gated"
+    # recomputed pre-activations, dH, dX, and the weight gradients (each 2 R d h per matrix)
+    per = (4 + 2 + 4 + 2 + 4) if gated else (2 + 2 + 2 + 2 + 2)
+    flops = per * R * d * w.h + (16 * T * d * w.h_shared if w.h_shared else 0) + 2 * 2 * T * d * N
+    out_d = {"ms": ms, "tokens_per_s": T / (ms / 1e3), "rows": R, "algorithmic_flops": flops,
+             "achieved_tflops": flops / (ms / 1e3) / 1e12, "bound": "tensor",
+             "frac": flops / (ms / 1e3) / 1e12 / peaks["bf16"],
+             "peak": f"{peaks['source']} bf16 burst {peaks['bf16']} TFLOP/s",
+             "note": "includes the per-call transposes of the expert weights (HBM)"}
+    if host_inp is not None:
+        from oracle import moe_oracle as O
+        n = min(T, cpu_tokens)
+        wn = w.replace(T=n)
+        host = dict(host_inp, x=host_inp["x"][:n])
+        t0 = time.perf_counter()
+        O.backward(wn, host, dy[:n].float().cpu().numpy(), aux_coef=0.01, z_coef=0.001)
+        secs = time.perf_counter() - t0
+        out_d["cpu_oracle"] = {"tokens_per_s": n / secs, "sample_tokens": n, "cores": _blas_threads(),
+                               "kind": "oracle"}
+    return out_d
+
+
 # ------------------------------------------------------------------------ GPU arm
 
 def run_ours(a, w, world, rank, local):
@@ -538,13 +589,15 @@ def run_ours(a, w, world, rank, local):
     }
 
     # ---- training-time router variant (noisy top-k + z-loss), same inputs
+    cpu = rank == 0 and world == 1 and not a.no_cpu_baseline
+    host_inp = _oracle_inputs(inp, w) if cpu else None
     if not a.no_variants and not ec:
-        line["variants"] = {"router_train": measure_router_train(
-            w, inp, cfg, ws, stream, dev, 0 if (a.no_cpu_baseline or rank != 0) else 512)}
+        line["variants"] = {"router_train": measure_router_train(w, inp, cfg, ws, stream, dev, 512 if cpu else 0)}
+        if w.dtype == "bf16":
+            line["variants"]["backward"] = measure_backward(w, inp, cfg, ws, stream, dev, peaks, host_inp)
 
     # ---- CPU oracle baseline (rank 0, single process only)
-    if rank == 0 and world == 1 and not a.no_cpu_baseline:
-        host_inp = _oracle_inputs(inp, w)
+    if cpu:
         secs, n = time_oracle(w, host_inp, a.cpu_sample, 7)
         line["cpu_baseline"] = {
             "value": n / secs, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",

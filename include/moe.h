@@ -343,6 +343,36 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const float *w_r,
                        cudaStream_t stream);
 
 /*
+ * Backward of the layer (token choice, bf16): the gradients of
+ *   Loss = sum(dy * y) + aux_coef * aux[0] + z_coef * z
+ * with the routing of the preceding moe_forward held fixed (selections and capacity
+ * are piecewise constant; f_e of the aux loss is held fixed too). Chain rule through
+ * the combine ("From Router to Combine"), the experts (O = H W_outᵀ with H =
+ * SiLU(X W_gateᵀ) ⊙ X W_upᵀ, or max(0, X W1ᵀ)), the shared expert and the router
+ * (gates from the fp32 logits; aux N sum_e f_e P_e; z = mean_t (log sum_e exp L)²).
+ * Call it after moe_forward with the same inputs and the same workspace ws (it
+ * reads the saved dispatch order, rows, expert outputs and hidden activations);
+ * topk_idx / topk_gate: the buffers given to that moe_forward, or NULL if it was
+ * given NULL. bws: backward scratch of moe_backward_workspace_size(cfg) bytes.
+ *   dy [T][d] bf16 in;  dx [T][d] bf16, dw_r [d][N] fp32, db_r [N] fp32 (NULL or
+ *   ignored without a router bias), dw_gate_or_w1 / dw_up [N][h][d], dw_down
+ *   [N][d][h], dshared_* shaped like the shared weights — all bf16 outputs.
+ * The expert weights are transposed into bws for the row products; the weight
+ * gradients reduce over each expert's rows on the tensor cores. fp32 and Expert
+ * Choice configs return MOE_ERR_UNSUPPORTED.
+ */
+size_t moe_backward_workspace_size(const moe_config *cfg);
+moe_status moe_backward(const moe_config *cfg, const void *x, const float *w_r, const float *b_r,
+                        const void *w_gate_or_w1, const void *w_up, const void *w_down,
+                        const void *shared_w_gate, const void *shared_w_up,
+                        const void *shared_w_down, const int32_t *topk_idx,
+                        const float *topk_gate, const void *dy, float aux_coef, float z_coef,
+                        void *dx, float *dw_r, float *db_r, void *dw_gate_or_w1, void *dw_up,
+                        void *dw_down, void *dshared_w_gate, void *dshared_w_up,
+                        void *dshared_w_down, void *ws, size_t ws_bytes, void *bws,
+                        size_t bws_bytes, cudaStream_t stream);
+
+/*
  * moe_forward with timing instrumentation: the same launches and results, plus
  * events[0..5] recorded on `stream` before the router, after the router, after
  * dispatch, after the first expert product (hidden activations), after the second

@@ -32,7 +32,8 @@ EXPORTED = ("moe_validate_config", "moe_workspace_size", "moe_max_rows", "moe_ca
             "moe_router_topk", "moe_dispatch", "moe_grouped_ffn", "moe_combine", "moe_forward",
             "moe_forward_profiled", "moe_check_error", "moe_status_str", "moe_router_topk_noalloc",
             "moe_router_topk_train", "moe_router_shard_stats", "moe_router_shard_assign",
-            "moe_router_expert_choice", "moe_combine_expert_choice")
+            "moe_router_expert_choice", "moe_combine_expert_choice", "moe_backward",
+            "moe_backward_workspace_size")
 
 
 class moe_config(ctypes.Structure):
@@ -65,6 +66,9 @@ def _load() -> ctypes.CDLL:
         "moe_router_topk_train": (I32, [cfgp, P, P, P, P, ctypes.c_float] + [P] * 9 + [P, SZ, P]),
         "moe_router_shard_stats": (I32, [cfgp] + [P] * 7 + [P, SZ, P]),
         "moe_router_expert_choice": (I32, [cfgp] + [P] * 8 + [P, SZ, P]),
+        "moe_backward_workspace_size": (SZ, [cfgp]),
+        "moe_backward": (I32, [cfgp] + [P] * 12 + [ctypes.c_float, ctypes.c_float] + [P] * 9
+                         + [P, SZ, P, SZ, P]),
         "moe_combine_expert_choice": (I32, [cfgp] + [P] * 9 + [P, SZ, P]),
         "moe_router_shard_assign": (I32, [cfgp, P, P, I32, P, P, I64] + [P] * 5 + [P, SZ, P]),
         "moe_dispatch": (I32, [cfgp, P, P, P, P, P, SZ, P]),
@@ -219,6 +223,27 @@ def moe_combine_expert_choice(cfg, x, y_perm, token_ptr, token_rows, row_gate, s
                                           _p(shared_w_up), _p(shared_w_down), _p(y), _p(ws),
                                           ws.numel() if ws is not None else 0, _stream(stream)),
            "moe_combine_expert_choice")
+
+
+def backward_workspace(cfg, device="cuda"):
+    """Scratch for moe_backward (uint8, 256-byte aligned by the allocator)."""
+    import torch
+    return torch.empty(int(_lib.moe_backward_workspace_size(ctypes.byref(cfg))), dtype=torch.uint8, device=device)
+
+
+def moe_backward(cfg, x, w_r, b_r, w_gate_or_w1, w_up, w_down, shared_w_gate, shared_w_up,
+                 shared_w_down, topk_idx, topk_gate, dy, aux_coef, z_coef, dx, dw_r, db_r,
+                 dw_gate_or_w1, dw_up, dw_down, dshared_w_gate, dshared_w_up, dshared_w_down, ws,
+                 bws, stream=None):
+    """Gradients of sum(dy * y) + aux_coef * aux[0] + z_coef * z after moe_forward with the
+    same inputs and workspace ws; bws from backward_workspace(cfg)."""
+    _check(_lib.moe_backward(ctypes.byref(cfg), _p(x), _p(w_r), _p(b_r), _p(w_gate_or_w1), _p(w_up),
+                             _p(w_down), _p(shared_w_gate), _p(shared_w_up), _p(shared_w_down),
+                             _p(topk_idx), _p(topk_gate), _p(dy), float(aux_coef), float(z_coef),
+                             _p(dx), _p(dw_r), _p(db_r), _p(dw_gate_or_w1), _p(dw_up), _p(dw_down),
+                             _p(dshared_w_gate), _p(dshared_w_up), _p(dshared_w_down), _p(ws),
+                             ws.numel() if ws is not None else 0, _p(bws),
+                             bws.numel() if bws is not None else 0, _stream(stream)), "moe_backward")
 
 
 def moe_router_topk_noalloc(cfg, x, w_r, b_r, topk_idx, topk_gate, counts_routed, counts_kept,

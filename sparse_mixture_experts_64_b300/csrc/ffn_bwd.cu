@@ -1,0 +1,393 @@
+// Backward building blocks on the GPU: the weight-gradient GEMM of the experts and
+// the transposes that feed the K-major tensor-core kernels.
+//
+// The experts' weight gradients reduce over each expert's rows: dW_out[e] =
+// dO_eᵀ H_e, dW_a[e] = dA_eᵀ X_e, dW_b[e] = dB_eᵀ X_e (the chain rule through
+// O = H W_outᵀ, H = act(X W_aᵀ) (⊙ X W_bᵀ)). K is an expert's row count, so it varies
+// per expert. The activations are transposed into [M][Kall] with expert e's rows in
+// columns k0_e .. k0_e + R_e - 1, zero up to kp_e = R_e rounded up to 64, so that a
+// 64-wide K tile never reads another expert's rows (k_transpose_rows_padded). The
+// weight-gradient kernel (k_wgrad_tc) is the single-CTA tcgen05 structure of
+// ffn_tc.cu — TMA producer warp, one MMA-issuing thread, four epilogue warps, two
+// TMEM accumulators of 128 x 256 fp32 — with tiles (expert, m, n), K from the
+// expert's column range, and an all-zero tile for an expert without rows.
+#include <algorithm>
+#include <cstring>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc_ptx.cuh"
+#include "tc_sync.cuh"
+
+namespace moe {
+namespace {
+
+using namespace tc;
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr uint32_t A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2, STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int NUM_THREADS = 192;
+constexpr int MAX_SEG = 257;
+constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + 1024;
+
+struct WgParams {
+    CUtensorMap tmA, tmB;        // At [M][Kall] (box 64 x 128), Bt [Nn][Kall] (box 64 x 256)
+    CUtensorMap tmA_sh, tmB_sh;  // shared segment: [M][K_sh], [Nn][K_sh]
+    const int32_t *offsets;      // [n_seg + 1] rows of each expert
+    int n_seg, has_sh;
+    int a_rows;                  // offsets are clamped to it
+    int M, Nn, K_sh;
+    __nv_bfloat16 *C, *C_sh;     // [n_seg][M][Nn], [M][Nn]
+    uint32_t *err;
+};
+
+struct WgSmem {
+    uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], drain;
+    uint32_t tmem_base;
+    int abort_flag;
+    int k0[MAX_SEG], kp[MAX_SEG];  // first column and padded width of each segment's K range
+};
+
+__global__ void __launch_bounds__(NUM_THREADS, 1) k_wgrad_tc(const __grid_constant__ WgParams p) {
+    __shared__ WgSmem s;
+    extern __shared__ uint8_t dyn_smem[];
+    const uint32_t dyn_base = smem_u32(dyn_smem);
+    uint8_t *tiles = dyn_smem + (((dyn_base + 1023u) & ~1023u) - dyn_base);
+    auto smA = [&](int st) { return tiles + (size_t)st * STAGE_BYTES; };
+    auto smB = [&](int st) { return tiles + (size_t)st * STAGE_BYTES + A_BYTES; };
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nseg = p.n_seg + p.has_sh;
+    const int mt = (p.M + BM - 1) / BM, nt = (p.Nn + BN - 1) / BN;
+    const int per_seg = mt * nt;
+    const int total = nseg * per_seg;
+
+    if (warp == 0) {
+        // K ranges: kp = rows rounded up to 64, k0 = exclusive scan (routed segments)
+        constexpr int PER = (MAX_SEG + 31) / 32;
+        int kp[PER];
+        int sum = 0;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int g = lane * PER + i;
+            int v = 0;
+            if (g < p.n_seg) {
+                const int r0 = min(max(p.offsets[g], 0), p.a_rows);
+                const int r1 = min(max(p.offsets[g + 1], r0), p.a_rows);
+                v = (r1 - r0 + BK - 1) / BK * BK;
+            }
+            kp[i] = v;
+            sum += v;
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += u;
+        }
+        int run = incl - sum;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int g = lane * PER + i;
+            if (g < p.n_seg) {
+                s.k0[g] = run;
+                s.kp[g] = kp[i];
+            }
+            run += kp[i];
+        }
+        if (lane == 0 && p.has_sh) {
+            s.k0[p.n_seg] = 0;
+            s.kp[p.n_seg] = p.K_sh;
+        }
+        if (lane == 0) {
+            for (int i = 0; i < STAGES; ++i) {
+                mbar_init(&s.full[i], 1);
+                mbar_init(&s.empty[i], 1);
+            }
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(&s.tfull[i], 1);
+                mbar_init(&s.tempty[i], 128);
+            }
+            mbar_init(&s.drain, 1);
+            s.abort_flag = 0;
+            fence_mbar_init();
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc(&s.tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = s.tmem_base;
+    volatile int *abort_flag = &s.abort_flag;
+
+    if (warp == 0) {
+        // ================= TMA producer =================
+        if (lane == 0) {
+            int st = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            uint32_t issued_mask = 0, issued_par = 0;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                const int g = tile / per_seg, local = tile - g * per_seg;
+                const int m = local % mt, n = local / mt;
+                const bool sh = g >= p.n_seg;
+                const CUtensorMap *ta = sh ? &p.tmA_sh : &p.tmA;
+                const CUtensorMap *tb = sh ? &p.tmB_sh : &p.tmB;
+                const int k0 = s.k0[g];
+                for (int kb = 0; kb < s.kp[g] / BK; ++kb) {
+                    if (!wait_bar(&s.empty[st], ph ^ 1, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&s.full[st], STAGE_BYTES);
+                    tma_load_2d(smA(st), ta, k0 + kb * BK, m * BM, &s.full[st]);
+                    tma_load_2d(smB(st), tb, k0 + kb * BK, n * BN, &s.full[st]);
+                    issued_mask |= 1u << st;
+                    issued_par = (issued_par & ~(1u << st)) | (ph << st);
+                    if (++st == STAGES) {
+                        st = 0;
+                        ph ^= 1;
+                    }
+                }
+            }
+            for (int i = 0; i < STAGES; ++i)
+                if (issued_mask & (1u << i)) drain_bar(&s.full[i], (issued_par >> i) & 1u);
+        }
+    } else if (warp == 1) {
+        // ================= MMA issuer =================
+        if (lane == 0) {
+            constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+            int st = 0, acc = 0;
+            uint32_t ph = 0, aph = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                const int g = tile / per_seg;
+                if (!wait_bar(&s.tempty[acc], aph ^ 1, abort_flag, p.err)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < s.kp[g] / BK; ++kb) {
+                    if (!wait_bar(&s.full[st], ph, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = desc_sw128(smem_u32(smA(st)));
+                    const uint64_t bd = desc_sw128(smem_u32(smB(st)));
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        umma_bf16(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), IDESC,
+                                  (kb | kk) != 0 ? 1u : 0u);
+                    umma_commit(&s.empty[st]);
+                    if (++st == STAGES) {
+                        st = 0;
+                        ph ^= 1;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(&s.tfull[acc]);  // no MMA for an empty segment: the epilogue writes zeros
+                if (++acc == 2) {
+                    acc = 0;
+                    aph ^= 1;
+                }
+            }
+            umma_commit(&s.drain);
+            drain_bar(&s.drain, 0);
+        }
+    } else {
+        // ================= epilogue (warps 2..5) =================
+        const int quarter = warp & 3;
+        const int r_in_tile = quarter * 32 + lane;
+        int acc = 0;
+        uint32_t aph = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+            const int g = tile / per_seg, local = tile - g * per_seg;
+            const int m = local % mt, n = local / mt;
+            const bool sh = g >= p.n_seg;
+            if (!wait_bar(&s.tfull[acc], aph, abort_flag, p.err)) break;
+            tc_fence_after();
+            const int row = m * BM + r_in_tile;
+            const bool empty_seg = s.kp[g] == 0;
+            __nv_bfloat16 *crow = (sh ? p.C_sh : p.C + (size_t)g * p.M * p.Nn) + (size_t)row * p.Nn;
+            const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16);
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+                uint32_t v[32];
+                tmem_ld32(tbase + c, v);
+                tmem_ld_wait();
+                const int col = n * BN + c;
+                if (row < p.M && col < p.Nn) {
+                    uint32_t packed[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float f0 = empty_seg ? 0.0f : __uint_as_float(v[2 * i]);
+                        const float f1 = empty_seg ? 0.0f : __uint_as_float(v[2 * i + 1]);
+                        __nv_bfloat162 b = __floats2bfloat162_rn(f0, f1);
+                        packed[i] = *reinterpret_cast<uint32_t *>(&b);
+                    }
+                    uint4 *dst = reinterpret_cast<uint4 *>(crow + col);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive_relaxed(&s.tempty[acc]);
+            if (++acc == 2) {
+                acc = 0;
+                aph ^= 1;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
+// dst[b][c][off + r] = src[b][r][c]: a batch of R x C bf16 matrices transposed into
+// rows of stride ldd (32 x 32 tiles through shared memory).
+__global__ void __launch_bounds__(256) k_transpose_batched(const __nv_bfloat16 *__restrict__ src, int R, int C,
+                                                           __nv_bfloat16 *__restrict__ dst, int ldd, int off) {
+    __shared__ __nv_bfloat16 tile[32][34];
+    const int b = blockIdx.z;
+    const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const __nv_bfloat16 *sb = src + (size_t)b * R * C;
+    __nv_bfloat16 *db = dst + (size_t)b * C * ldd;
+    for (int i = ty; i < 32; i += 8)
+        if (r0 + i < R && c0 + tx < C) tile[i][tx] = sb[(size_t)(r0 + i) * C + c0 + tx];
+    __syncthreads();
+    for (int i = ty; i < 32; i += 8)
+        if (c0 + i < C && r0 + tx < R) db[(size_t)(c0 + i) * ldd + off + r0 + tx] = tile[tx][i];
+}
+
+// kpre[g] = sum over segments g' < g of R_g' rounded up to 64 (g = 0 .. n_seg), one CTA.
+__global__ void __launch_bounds__(256) k_pad_prefix(const int32_t *__restrict__ offsets, int n_seg, int rows,
+                                                    int32_t *__restrict__ kpre) {
+    __shared__ int w[MAX_SEG];
+    for (int g = threadIdx.x; g < n_seg; g += blockDim.x) {
+        const int a = min(max(offsets[g], 0), rows);
+        const int e = min(max(offsets[g + 1], a), rows);
+        w[g] = (e - a + 63) / 64 * 64;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int run = 0;
+        for (int g = 0; g < n_seg; ++g) {
+            kpre[g] = run;
+            run += w[g];
+        }
+        kpre[n_seg] = run;
+    }
+}
+
+// Activation rows [rows][C] (row stride C) into the padded transposed layout
+// [C][Kall]: column kpre[g] + i holds row offsets[g] + i for i < R_g, zero up to
+// kpre[g + 1] and beyond kpre[n_seg]. offsets null: one segment of `rows` rows.
+__global__ void __launch_bounds__(256) k_transpose_rows_padded(const __nv_bfloat16 *__restrict__ src, int C,
+                                                               const int32_t *__restrict__ offsets,
+                                                               const int32_t *__restrict__ kpre, int n_seg,
+                                                               int rows, int64_t Kall,
+                                                               __nv_bfloat16 *__restrict__ dst) {
+    __shared__ __nv_bfloat16 tile[32][34];
+    __shared__ int srow[32];
+    const int64_t k0 = (int64_t)blockIdx.x * 32;
+    const int c0 = blockIdx.y * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    if (ty == 0) {
+        // source row of padded column k0 + tx (-1: padding), by binary search on kpre
+        const int64_t kc = k0 + tx;
+        int r = -1;
+        if (!offsets) {
+            r = kc < rows ? (int)kc : -1;
+        } else if (kc < kpre[n_seg]) {
+            int lo = 0, hi = n_seg - 1;  // largest g with kpre[g] <= kc
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (kpre[mid] <= kc) lo = mid;
+                else hi = mid - 1;
+            }
+            const int a = min(max(offsets[lo], 0), rows);
+            const int e = min(max(offsets[lo + 1], a), rows);
+            const int64_t i = kc - kpre[lo];
+            r = i < e - a ? (int)(a + i) : -1;
+        }
+        srow[tx] = r;
+    }
+    __syncthreads();
+    for (int i = ty; i < 32; i += 8) {
+        const int r = srow[i];
+        tile[i][tx] = (r >= 0 && c0 + tx < C) ? src[(size_t)r * C + c0 + tx] : __float2bfloat16_rn(0.0f);
+    }
+    __syncthreads();
+    for (int i = ty; i < 32; i += 8)
+        if (c0 + i < C && k0 + tx < Kall) dst[(size_t)(c0 + i) * Kall + k0 + tx] = tile[tx][i];
+}
+
+}  // namespace
+
+int64_t wgrad_kall_bound(const moe_config &c) { return (max_rows(c) + 64LL * c.N + 63) / 64 * 64; }
+
+cudaError_t launch_wgrad(const int32_t *offsets, int n_seg, int64_t a_rows, const void *At, const void *Bt,
+                         int64_t Kall, int M, int Nn, void *out, const void *At_sh, const void *Bt_sh, int K_sh,
+                         void *out_sh, uint32_t *err, cudaStream_t s) {
+    WgParams p;
+    memset(&p, 0, sizeof(p));
+    p.offsets = offsets;
+    p.n_seg = n_seg;
+    p.has_sh = At_sh ? 1 : 0;
+    p.a_rows = (int)a_rows;
+    p.M = M;
+    p.Nn = Nn;
+    p.K_sh = K_sh;
+    p.C = static_cast<__nv_bfloat16 *>(out);
+    p.C_sh = static_cast<__nv_bfloat16 *>(out_sh);
+    p.err = err;
+    if (n_seg > 0) {
+        if (!encode_bf16_2d(&p.tmA, At, (uint64_t)Kall, (uint64_t)M, BM)) return cudaErrorInvalidValue;
+        if (!encode_bf16_2d(&p.tmB, Bt, (uint64_t)Kall, (uint64_t)Nn, BN)) return cudaErrorInvalidValue;
+    }
+    if (p.has_sh) {
+        if (!encode_bf16_2d(&p.tmA_sh, At_sh, (uint64_t)K_sh, (uint64_t)M, BM)) return cudaErrorInvalidValue;
+        if (!encode_bf16_2d(&p.tmB_sh, Bt_sh, (uint64_t)K_sh, (uint64_t)Nn, BN)) return cudaErrorInvalidValue;
+    }
+    const int64_t tiles = (int64_t)(n_seg + p.has_sh) * ((M + BM - 1) / BM) * ((Nn + BN - 1) / BN);
+    if (tiles == 0) return cudaSuccess;
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(k_wgrad_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, device_sm_count()));
+    k_wgrad_tc<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_batched(const void *src, int B, int R, int C, void *dst, int ldd, int off,
+                                     cudaStream_t s) {
+    dim3 grid((C + 31) / 32, (R + 31) / 32, B);
+    k_transpose_batched<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(src), R, C,
+                                             static_cast<__nv_bfloat16 *>(dst), ldd, off);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pad_prefix(const int32_t *offsets, int n_seg, int rows, int32_t *kpre, cudaStream_t s) {
+    k_pad_prefix<<<1, 256, 0, s>>>(offsets, n_seg, rows, kpre);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_rows_padded(const void *src, int C, const int32_t *offsets, const int32_t *kpre,
+                                         int n_seg, int rows, int64_t Kall, void *dst, cudaStream_t s) {
+    dim3 grid((unsigned)((Kall + 31) / 32), (unsigned)((C + 31) / 32));
+    k_transpose_rows_padded<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(src), C, offsets, kpre, n_seg,
+                                                 rows, Kall, static_cast<__nv_bfloat16 *>(dst));
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -46,7 +46,12 @@ constexpr int NUM_THREADS = 192;
 constexpr int MAX_SEG = 257;
 constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + 1024;
 
-enum { KIND_GATED = 0, KIND_RELU = 1, KIND_PLAIN = 2 };
+// KIND_PREACT: the gated product's two accumulators stored raw (no activation), gate
+// pre-activations in columns [0, n_out) and up pre-activations in [n_out, 2 n_out) of
+// a 2 n_out-wide output (the backward recomputes them).
+enum { KIND_GATED = 0, KIND_RELU = 1, KIND_PLAIN = 2, KIND_PREACT = 3 };
+template <int KIND> constexpr bool kGatedLayout = KIND == KIND_GATED || KIND == KIND_PREACT;
+template <int KIND> constexpr int kOutLd = KIND == KIND_PREACT ? 2 : 1;  // output row stride / n_out
 
 struct TcParams {
     CUtensorMap tmA, tmA_sh;       // [rows][K], box 64 x 128
@@ -93,9 +98,34 @@ __device__ __forceinline__ TileInfo decode_tile(const S &s, int nseg, int tile) 
 
 // Epilogue of one accumulator row (this thread's TMEM lane): activation, bf16,
 // 16-byte stores of the output columns [col0, col0 + BN_OUT) when row_ok.
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16 *dst, const uint32_t *v) {
+    uint32_t packed[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+        packed[i] = *reinterpret_cast<uint32_t *>(&b);
+    }
+    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) d4[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+}
+
 template <int KIND>
 __device__ __forceinline__ void epilogue_row(uint32_t tbase, __nv_bfloat16 *crow, int col0, int n_out, bool row_ok) {
-    if constexpr (KIND == KIND_GATED) {
+    if constexpr (KIND == KIND_PREACT) {
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 32) {
+            uint32_t g[32], u[32];
+            tmem_ld32(tbase + c, g);
+            tmem_ld32(tbase + 128 + c, u);
+            tmem_ld_wait();
+            const int col = col0 + c;
+            if (row_ok && col < n_out) {
+                store_bf16x32(crow + col, g);
+                store_bf16x32(crow + n_out + col, u);
+            }
+        }
+    } else if constexpr (KIND == KIND_GATED) {
 #pragma unroll 1
         for (int c = 0; c < 128; c += 32) {
             uint32_t g[32], u[32];
@@ -148,7 +178,7 @@ __device__ __forceinline__ void epilogue_row(uint32_t tbase, __nv_bfloat16 *crow
 
 template <int KIND>
 __global__ void __launch_bounds__(NUM_THREADS, 1) k_ffn_tc(const __grid_constant__ TcParams p) {
-    constexpr int BN_OUT = KIND == KIND_GATED ? 128 : 256;
+    constexpr int BN_OUT = kGatedLayout<KIND> ? 128 : 256;
     __shared__ Smem s;
     extern __shared__ uint8_t dyn_smem[];
     const uint32_t dyn_base = smem_u32(dyn_smem);
@@ -251,7 +281,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_ffn_tc(const __grid_constant
                     mbar_arrive_expect_tx(&s.full[st], STAGE_BYTES);
                     const int kc = kb * BK;
                     tma_load_2d(smA(st), ta, kc, arow, &s.full[st]);
-                    if (KIND == KIND_GATED) {
+                    if (kGatedLayout<KIND>) {
                         if (sh) {
                             tma_load_2d(smB(st), &p.tmB0_sh, kc, ti.n * 128, &s.full[st]);
                             tma_load_2d(smB(st) + B_BYTES / 2, &p.tmB1_sh, kc, ti.n * 128, &s.full[st]);
@@ -335,7 +365,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_ffn_tc(const __grid_constant
             const bool row_ok = r_in_tile < rows;
             const int64_t orow = (int64_t)s.row0[ti.seg] + ti.m * BM + r_in_tile;
             const int n_out = sh ? p.n_out_sh : p.n_out;
-            __nv_bfloat16 *crow = (sh ? p.C_sh : p.C) + orow * n_out;
+            __nv_bfloat16 *crow = (sh ? p.C_sh : p.C) + orow * n_out * kOutLd<KIND>;
             const uint32_t tbase = tmem_base + (uint32_t)(acc * ACC_COLS) + ((uint32_t)(quarter * 32) << 16);
             epilogue_row<KIND>(tbase, crow, ti.n * BN_OUT, n_out, row_ok);
             tc_fence_before();
@@ -384,7 +414,7 @@ struct Smem2 {
 template <int KIND, int NACC>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     k_ffn_tc2(const __grid_constant__ TcParams p) {
-    constexpr int BN_OUT = KIND == KIND_GATED ? 128 : 256;
+    constexpr int BN_OUT = kGatedLayout<KIND> ? 128 : 256;
     constexpr uint32_t TMEM_COLS2 = NACC * ACC_COLS;
     __shared__ Smem2 s;
     extern __shared__ uint8_t dyn_smem[];
@@ -507,7 +537,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                     if (leader) mbar_arrive_expect_tx(&s.full[st], 2 * STAGE2_BYTES);
                     const int kc = kb * BK;
                     tma_load_2d_pair(smA(st), ta, kc, arow, fb);
-                    if (KIND == KIND_GATED) {
+                    if (kGatedLayout<KIND>) {
                         // even CTA: gate rows, odd CTA: up rows -> accumulator columns 0-127 / 128-255
                         if (sh) tma_load_2d_pair(smB(st), rank == 0 ? &p.tmB0_sh : &p.tmB1_sh, kc, ti.n * 128, fb);
                         else tma_load_3d_pair(smB(st), rank == 0 ? &p.tmB0 : &p.tmB1, kc, ti.n * 128, ti.seg, fb);
@@ -590,7 +620,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             const bool row_ok = r_seg < s.rows[ti.seg];
             const int64_t orow = (int64_t)s.row0[ti.seg] + r_seg;
             const int n_out = sh ? p.n_out_sh : p.n_out;
-            __nv_bfloat16 *crow = (sh ? p.C_sh : p.C) + orow * n_out;
+            __nv_bfloat16 *crow = (sh ? p.C_sh : p.C) + orow * n_out * kOutLd<KIND>;
             const uint32_t tbase = tmem_base + (uint32_t)(acc * ACC_COLS) + ((uint32_t)(quarter * 32) << 16);
             epilogue_row<KIND>(tbase, crow, ti.n * BN_OUT, n_out, row_ok);
             tc_fence_before();
@@ -658,8 +688,8 @@ cudaError_t product(const int32_t *offsets, int n_seg, int64_t a_rows, const voi
                     const void *b1, int K, int n_out, void *out, int sh_rows, const void *a_sh,
                     const void *b0_sh, const void *b1_sh, int K_sh, int n_out_sh, void *out_sh,
                     uint32_t *err, cudaStream_t s, bool pair) {
-    constexpr int BN_OUT = KIND == KIND_GATED ? 128 : 256;
-    const uint32_t box_b = (KIND == KIND_GATED || pair) ? 128 : 256;
+    constexpr int BN_OUT = kGatedLayout<KIND> ? 128 : 256;
+    const uint32_t box_b = (kGatedLayout<KIND> || pair) ? 128 : 256;
     const int64_t tm = pair ? 2 * BM : BM;
     TcParams p;
     memset(&p, 0, sizeof(p));
@@ -678,13 +708,13 @@ cudaError_t product(const int32_t *offsets, int n_seg, int64_t a_rows, const voi
     if (n_seg > 0) {
         if (!encode_bf16_2d(&p.tmA, a, K, a_rows, BM)) return cudaErrorInvalidValue;
         if (!encode_bf16_3d(&p.tmB0, b0, K, n_out, n_seg, box_b)) return cudaErrorInvalidValue;
-        if (KIND == KIND_GATED && !encode_bf16_3d(&p.tmB1, b1, K, n_out, n_seg, box_b)) return cudaErrorInvalidValue;
+        if (kGatedLayout<KIND> && !encode_bf16_3d(&p.tmB1, b1, K, n_out, n_seg, box_b)) return cudaErrorInvalidValue;
         max_tiles += ((a_rows + tm - 1) / tm + n_seg) * ((n_out + BN_OUT - 1) / BN_OUT);
     }
     if (sh_rows > 0) {
         if (!encode_bf16_2d(&p.tmA_sh, a_sh, K_sh, sh_rows, BM)) return cudaErrorInvalidValue;
         if (!encode_bf16_2d(&p.tmB0_sh, b0_sh, K_sh, n_out_sh, box_b)) return cudaErrorInvalidValue;
-        if (KIND == KIND_GATED && !encode_bf16_2d(&p.tmB1_sh, b1_sh, K_sh, n_out_sh, box_b))
+        if (kGatedLayout<KIND> && !encode_bf16_2d(&p.tmB1_sh, b1_sh, K_sh, n_out_sh, box_b))
             return cudaErrorInvalidValue;
         max_tiles += ((int64_t)(sh_rows + tm - 1) / tm) * ((n_out_sh + BN_OUT - 1) / BN_OUT);
     }
@@ -693,6 +723,20 @@ cudaError_t product(const int32_t *offsets, int n_seg, int64_t a_rows, const voi
 }
 
 }  // namespace
+
+cudaError_t launch_gemm_rows(const moe_config &c, bool preact, const int32_t *offsets, int n_seg, int64_t a_rows,
+                             const void *a, const void *b0, const void *b1, int K, int n_out, void *out, int sh_rows,
+                             const void *a_sh, const void *b0_sh, const void *b1_sh, int K_sh, int n_out_sh,
+                             void *out_sh, uint32_t *err, cudaStream_t s) {
+    bool pair = n_seg > 0 && a_rows >= 224LL * n_seg;
+    if (c.debug_flags & MOE_DEBUG_FFN_PAIR) pair = true;
+    if (c.debug_flags & MOE_DEBUG_FFN_SINGLE) pair = false;
+    if (preact)
+        return product<KIND_PREACT>(offsets, n_seg, a_rows, a, b0, b1, K, n_out, out, sh_rows, a_sh, b0_sh, b1_sh,
+                                    K_sh, n_out_sh, out_sh, err, s, pair);
+    return product<KIND_PLAIN>(offsets, n_seg, a_rows, a, b0, nullptr, K, n_out, out, sh_rows, a_sh, b0_sh, nullptr,
+                               K_sh, n_out_sh, out_sh, err, s, pair);
+}
 
 cudaError_t launch_ffn_tc(const moe_config &c, const FfnGroup &g, uint32_t *err, cudaStream_t s) {
     if (c.debug_flags & MOE_DEBUG_FFN_SWAP) return launch_ffn_sw(c, g, err, s);

@@ -58,6 +58,23 @@ struct WsLayout {
 };
 WsLayout ws_layout(const moe_config &c);
 
+// Byte offsets of the backward workspace regions (each 256-byte aligned). W = 2h for
+// SiLU-gated experts ([A | B] pre-activations), h for ReLU experts.
+struct BwdLayout {
+    size_t dO;                   // bf16 [R_max][d]  gate-scaled dy per row
+    size_t dgate;                // f32  [T][k]      gate gradients
+    size_t AB, dH, dAB;          // bf16 [R_max][W], [R_max][h], [R_max][W]
+    size_t dX;                   // bf16 [R_max][d]
+    size_t wo_t, wab_t;          // bf16 [N][h][d] (W_outᵀ), [N][d][W] ([W_a | W_b]ᵀ)
+    size_t kpre;                 // int32 [N+1] padded column offsets of the experts' K ranges
+    size_t dO_t, H_t, dAB_t, X_t;  // bf16 transposed activations [d|h|W|d][Kall]
+    size_t AB_sh, dH_sh, dAB_sh, dX_sh, wo_sh_t, wab_sh_t;  // shared expert, rows = T
+    size_t dy_t, Hsh_t, dABsh_t, x_t;                       // shared expert, [..][ceil64(T)]
+    size_t logits, routed, dL, dxr;  // router: f32 [T][N], int32 [N], f32 [T][N], f32 [T][d]
+    size_t total;
+};
+BwdLayout bwd_layout(const moe_config &c);
+
 // ---- launchers (return cudaGetLastError() after the launch) ----
 struct RouterOut {
     int32_t *topk_idx;
@@ -85,6 +102,16 @@ cudaError_t launch_expert_choice(const moe_config &c, const float *logits, int32
 cudaError_t launch_combine_ec(const moe_config &c, const void *x, const void *y_perm, const void *s_out,
                               const int32_t *tok_ptr, const int32_t *tok_rows, const float *row_gate, void *y,
                               uint32_t *err, cudaStream_t s);
+// Backward pieces (backward.cu).
+cudaError_t launch_bwd_slots(const moe_config &c, const void *dy, const void *y_perm, const int32_t *slot_row,
+                             const float *gate, void *dO, float *dgate, uint32_t *err, cudaStream_t s);
+cudaError_t launch_act_bwd(bool gated, const void *AB, const void *dH, int64_t rows, int h, void *dAB,
+                           cudaStream_t s);
+cudaError_t launch_router_bwd(const moe_config &c, const void *x, const float *w_r, const int32_t *topk_idx,
+                              const float *topk_gate, const BwdLayout &L, uint8_t *bw, float aux_coef, float z_coef,
+                              float *dw_r, float *db_r, cudaStream_t s);
+cudaError_t launch_bwd_dx(const moe_config &c, const void *dy, const void *dX, const int32_t *slot_row,
+                          const void *dX_sh, const float *dxr, void *dx, uint32_t *err, cudaStream_t s);
 // Token-sharded router, phase 1: routing of this shard and the statistics the
 // shards exchange (selections per expert and slot, sums of the softmax).
 cudaError_t launch_router_stats(const moe_config &c, const void *x, const float *w_r, const float *b_r,
@@ -127,6 +154,32 @@ struct FfnGroup {
 cudaError_t launch_ffn_simt(const moe_config &c, const FfnGroup &g, uint32_t *err, cudaStream_t s);
 cudaError_t launch_ffn_tc(const moe_config &c, const FfnGroup &g, uint32_t *err, cudaStream_t s);
 cudaError_t launch_ffn_sw(const moe_config &c, const FfnGroup &g, uint32_t *err, cudaStream_t s);
+// One grouped product on the tensor cores (bf16): out[rows of segment g] = a[rows][K]
+// · b0[g][n_out][K]ᵀ, plain, or with preact the gated pair (b0, b1) stored raw as
+// [gate | up] rows of width 2 n_out; an optional shared segment with its own operands.
+cudaError_t launch_gemm_rows(const moe_config &c, bool preact, const int32_t *offsets, int n_seg, int64_t a_rows,
+                             const void *a, const void *b0, const void *b1, int K, int n_out, void *out, int sh_rows,
+                             const void *a_sh, const void *b0_sh, const void *b1_sh, int K_sh, int n_out_sh,
+                             void *out_sh, uint32_t *err, cudaStream_t s);
+// Weight-gradient GEMM with K running over each expert's rows: for expert e,
+// out[e] [M][Nn] = At[:, k0_e : k0_e + kp_e] · Bt[:, k0_e : k0_e + kp_e]ᵀ, where the
+// transposed activations At [M][Kall], Bt [Nn][Kall] hold expert e's rows in columns
+// k0_e .. k0_e + R_e - 1 and zeros up to kp_e = R_e rounded up to 64 (k0 = exclusive
+// scan of kp, R_e from offsets). An optional shared segment: out_sh = At_sh · Bt_shᵀ
+// over K_sh (a multiple of 64) columns.
+cudaError_t launch_wgrad(const int32_t *offsets, int n_seg, int64_t a_rows, const void *At, const void *Bt,
+                         int64_t Kall, int M, int Nn, void *out, const void *At_sh, const void *Bt_sh, int K_sh,
+                         void *out_sh, uint32_t *err, cudaStream_t s);
+// Upper bound of Kall (columns of the padded transposed layout) for a config.
+int64_t wgrad_kall_bound(const moe_config &c);
+// kpre[g] = sum over g' < g of rows of segment g' rounded up to 64 (g = 0 .. n_seg).
+cudaError_t launch_pad_prefix(const int32_t *offsets, int n_seg, int rows, int32_t *kpre, cudaStream_t s);
+// Rows [rows][C] into [C][Kall] in that padded column layout (offsets null: one segment).
+cudaError_t launch_transpose_rows_padded(const void *src, int C, const int32_t *offsets, const int32_t *kpre,
+                                         int n_seg, int rows, int64_t Kall, void *dst, cudaStream_t s);
+// dst[b][c][off + r] = src[b][r][c] for a batch of R x C bf16 matrices (dst row stride ldd).
+cudaError_t launch_transpose_batched(const void *src, int B, int R, int C, void *dst, int ldd, int off,
+                                     cudaStream_t s);
 
 int device_sm_count();
 

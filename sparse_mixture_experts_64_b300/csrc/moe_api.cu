@@ -303,6 +303,122 @@ moe_status moe_combine_expert_choice(const moe_config *cfg, const void *x, const
     return to_status(launch_combine_ec(c, x, y_perm, s_out, token_ptr, token_rows, row_gate, y, err, stream));
 }
 
+size_t moe_backward_workspace_size(const moe_config *cfg) {
+    if (validate(cfg) != MOE_OK) return 0;
+    return bwd_layout(*cfg).total;
+}
+
+moe_status moe_backward(const moe_config *cfg, const void *x, const float *w_r, const float *b_r,
+                        const void *w_gate_or_w1, const void *w_up, const void *w_down, const void *shared_w_gate,
+                        const void *shared_w_up, const void *shared_w_down, const int32_t *topk_idx,
+                        const float *topk_gate, const void *dy, float aux_coef, float z_coef, void *dx, float *dw_r,
+                        float *db_r, void *dw_gate_or_w1, void *dw_up, void *dw_down, void *dshared_w_gate,
+                        void *dshared_w_up, void *dshared_w_down, void *ws, size_t ws_bytes, void *bws,
+                        size_t bws_bytes, cudaStream_t stream) {
+    moe_status st = validate(cfg);
+    if (st != MOE_OK) return st;
+    const moe_config &c = *cfg;
+    if (c.routing != MOE_ROUTING_TOKEN_CHOICE || c.dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    const bool gated = c.act == MOE_ACT_SILU_GATED;
+    if (!x || !w_r || !w_gate_or_w1 || !w_down || !dy || !dx || !dw_r || !dw_gate_or_w1 || !dw_down)
+        return MOE_ERR_INVALID_ARG;
+    if (gated && (!w_up || !dw_up)) return MOE_ERR_INVALID_ARG;
+    if (c.has_router_bias && !b_r) return MOE_ERR_INVALID_ARG;
+    if (c.h_shared && (!shared_w_gate || !shared_w_up || !shared_w_down || !dshared_w_gate || !dshared_w_up ||
+                       !dshared_w_down))
+        return MOE_ERR_INVALID_ARG;
+    if (!std::isfinite(aux_coef) || !std::isfinite(z_coef)) return MOE_ERR_INVALID_ARG;
+    const void *must_align[] = {x, w_r, w_gate_or_w1, w_down, dy, dx, dw_gate_or_w1, dw_down};
+    for (const void *q : must_align)
+        if (!aligned16(q)) return MOE_ERR_INVALID_ARG;
+    if ((w_up && !aligned16(w_up)) || (dw_up && !aligned16(dw_up))) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(c);
+    if ((st = check_ws(ws, ws_bytes, L.total)) != MOE_OK) return st;
+    const BwdLayout B = bwd_layout(c);
+    if ((st = check_ws(bws, bws_bytes, B.total)) != MOE_OK) return st;
+
+    uint8_t *w = static_cast<uint8_t *>(ws), *bw = static_cast<uint8_t *>(bws);
+    uint32_t *err = reinterpret_cast<uint32_t *>(w + L.err);
+    const int32_t *idx = topk_idx ? topk_idx : reinterpret_cast<const int32_t *>(w + L.topk_idx);
+    const float *gate = topk_gate ? topk_gate : reinterpret_cast<const float *>(w + L.topk_gate);
+    const int32_t *offsets = reinterpret_cast<const int32_t *>(w + L.offsets);
+    const int32_t *slot_row = reinterpret_cast<const int32_t *>(w + L.slot_row);
+    const void *x_perm = w + L.x_perm, *y_perm = w + L.y_perm, *hid = w + L.hid, *hid_sh = w + L.hid_sh;
+    const int64_t R = max_rows(c);
+    const int N = c.N, d = c.d, h = c.h, hs = c.h_shared, Wd = gated ? 2 * h : h;
+    const int64_t Kall = wgrad_kall_bound(c), Tp = ((int64_t)c.T + 63) / 64 * 64;
+    void *dO = bw + B.dO, *AB = bw + B.AB, *dH = bw + B.dH, *dAB = bw + B.dAB, *dX = bw + B.dX;
+    void *wo_t = bw + B.wo_t, *wab_t = bw + B.wab_t;
+    float *dgate = reinterpret_cast<float *>(bw + B.dgate);
+    int32_t *kpre = reinterpret_cast<int32_t *>(bw + B.kpre);
+    cudaError_t e = cudaSuccess;
+    auto ok = [&](cudaError_t r) {
+        if (e == cudaSuccess) e = r;
+        return e == cudaSuccess;
+    };
+
+    // weights transposed for the row products: W_outᵀ [N][h][d], [W_a | W_b]ᵀ [N][d][Wd]
+    ok(launch_transpose_batched(w_down, N, d, h, wo_t, d, 0, stream));
+    ok(launch_transpose_batched(w_gate_or_w1, N, h, d, wab_t, Wd, 0, stream));
+    if (gated) ok(launch_transpose_batched(w_up, N, h, d, wab_t, Wd, h, stream));
+    if (hs) {
+        ok(launch_transpose_batched(shared_w_down, 1, d, hs, bw + B.wo_sh_t, d, 0, stream));
+        ok(launch_transpose_batched(shared_w_gate, 1, hs, d, bw + B.wab_sh_t, 2 * hs, 0, stream));
+        ok(launch_transpose_batched(shared_w_up, 1, hs, d, bw + B.wab_sh_t, 2 * hs, hs, stream));
+    }
+    // gate-scaled dy per row and the gate gradients
+    ok(launch_bwd_slots(c, dy, y_perm, slot_row, gate, dO, dgate, err, stream));
+    // pre-activations, recomputed: [A | B] (gated) or A (ReLU)
+    ok(launch_gemm_rows(c, gated, offsets, N, R, x_perm, w_gate_or_w1, w_up, d, h, AB, 0, nullptr, nullptr, nullptr, 0,
+                        0, nullptr, err, stream));
+    if (hs)
+        ok(launch_gemm_rows(c, true, nullptr, 0, 0, nullptr, nullptr, nullptr, 0, 0, nullptr, c.T, x, shared_w_gate,
+                            shared_w_up, d, hs, bw + B.AB_sh, err, stream));
+    // dH = dO W_out
+    ok(launch_gemm_rows(c, false, offsets, N, R, dO, wo_t, nullptr, d, h, dH, hs ? c.T : 0, dy, bw + B.wo_sh_t,
+                        nullptr, d, hs, bw + B.dH_sh, err, stream));
+    // [dA | dB] from the pre-activations
+    ok(launch_act_bwd(gated, AB, dH, R, h, dAB, stream));
+    if (hs) ok(launch_act_bwd(true, bw + B.AB_sh, bw + B.dH_sh, c.T, hs, bw + B.dAB_sh, stream));
+    // dX = [dA | dB] [W_a ; W_b]
+    ok(launch_gemm_rows(c, false, offsets, N, R, dAB, wab_t, nullptr, Wd, d, dX, hs ? c.T : 0, bw + B.dAB_sh,
+                        bw + B.wab_sh_t, nullptr, 2 * hs, d, bw + B.dX_sh, err, stream));
+    // weight gradients: transposed activations with each expert's rows padded to 64
+    ok(launch_pad_prefix(offsets, N, (int)R, kpre, stream));
+    ok(launch_transpose_rows_padded(dO, d, offsets, kpre, N, (int)R, Kall, bw + B.dO_t, stream));
+    ok(launch_transpose_rows_padded(hid, h, offsets, kpre, N, (int)R, Kall, bw + B.H_t, stream));
+    ok(launch_transpose_rows_padded(dAB, Wd, offsets, kpre, N, (int)R, Kall, bw + B.dAB_t, stream));
+    ok(launch_transpose_rows_padded(x_perm, d, offsets, kpre, N, (int)R, Kall, bw + B.X_t, stream));
+    ok(launch_wgrad(offsets, N, R, bw + B.dO_t, bw + B.H_t, Kall, d, h, dw_down, nullptr, nullptr, 0, nullptr, err,
+                    stream));
+    ok(launch_wgrad(offsets, N, R, bw + B.dAB_t, bw + B.X_t, Kall, h, d, dw_gate_or_w1, nullptr, nullptr, 0, nullptr,
+                    err, stream));
+    if (gated)
+        ok(launch_wgrad(offsets, N, R, bw + B.dAB_t + (size_t)h * Kall * 2, bw + B.X_t, Kall, h, d, dw_up, nullptr,
+                        nullptr, 0, nullptr, err, stream));
+    if (hs) {
+        ok(launch_transpose_rows_padded(dy, d, nullptr, nullptr, 1, c.T, Tp, bw + B.dy_t, stream));
+        ok(launch_transpose_rows_padded(hid_sh, hs, nullptr, nullptr, 1, c.T, Tp, bw + B.Hsh_t, stream));
+        ok(launch_transpose_rows_padded(bw + B.dAB_sh, 2 * hs, nullptr, nullptr, 1, c.T, Tp, bw + B.dABsh_t, stream));
+        ok(launch_transpose_rows_padded(x, d, nullptr, nullptr, 1, c.T, Tp, bw + B.x_t, stream));
+        ok(launch_wgrad(nullptr, 0, 0, nullptr, nullptr, 0, d, hs, nullptr, bw + B.dy_t, bw + B.Hsh_t, (int)Tp,
+                        dshared_w_down, err, stream));
+        ok(launch_wgrad(nullptr, 0, 0, nullptr, nullptr, 0, hs, d, nullptr, bw + B.dABsh_t, bw + B.x_t, (int)Tp,
+                        dshared_w_gate, err, stream));
+        ok(launch_wgrad(nullptr, 0, 0, nullptr, nullptr, 0, hs, d, nullptr, bw + B.dABsh_t + (size_t)hs * Tp * 2,
+                        bw + B.x_t, (int)Tp, dshared_w_up, err, stream));
+    }
+    // router: logits recomputed, dL, dx_router, dW_r, db
+    ok(launch_router_logits(c, x, w_r, c.has_router_bias ? b_r : nullptr, reinterpret_cast<float *>(bw + B.logits), w,
+                            stream));
+    ok(launch_router_bwd(c, x, w_r, idx, gate, B, bw, aux_coef, z_coef, dw_r, c.has_router_bias ? db_r : nullptr,
+                         stream));
+    // dx = dy + sum_j dX_r + dX_shared + dx_router
+    ok(launch_bwd_dx(c, dy, dX, slot_row, hs ? bw + B.dX_sh : nullptr, reinterpret_cast<const float *>(bw + B.dxr), dx,
+                     err, stream));
+    return to_status(e);
+}
+
 moe_status moe_dispatch(const moe_config *cfg, const void *x, const int32_t *perm_token,
                         const int32_t *expert_offsets, void *x_perm, void *ws, size_t ws_bytes,
                         cudaStream_t stream) {
