@@ -195,23 +195,31 @@ __global__ void __launch_bounds__(256) k_router_bwd(RouterBwdArgs a) {
 // C[M][Nc] (fp32) = sum_k A(m, k) B(k, n): A(m, k) = A[m * lda + k] or, transposed,
 // A[k * lda + m]; B(k, n) = B[k * ldb + n] or, transposed, B[n * ldb + k]. 64 x 64
 // tiles, 16-deep K slices through shared memory, 4 x 4 outputs per thread.
+//
+// Split K: blockIdx.z takes K range [z * kchunk, (z + 1) * kchunk) and writes its own
+// slab C + z * M * Nc (summed afterwards in slab order by k_sum_slabs).
 template <typename TA, bool TRANS_A, bool TRANS_B>
 __global__ void __launch_bounds__(256) k_simt_gemm(const TA *__restrict__ A, int lda, const float *__restrict__ B,
-                                                   int ldb, int M, int Nc, int K, float *__restrict__ C) {
+                                                   int ldb, int M, int Nc, int K, int kchunk, float *__restrict__ C) {
     __shared__ float As[16][64 + 4], Bs[16][64 + 4];
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
     const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+    const int kb = blockIdx.z * kchunk, ke = min(K, kb + kchunk);
+    C += (size_t)blockIdx.z * M * Nc;
     float acc[4][4] = {};
-    for (int k0 = 0; k0 < K; k0 += 16) {
+    for (int k0 = kb; k0 < ke; k0 += 16) {
+        // consecutive threads read consecutive addresses: along m / n when that is the
+        // contiguous dimension of the operand, along k otherwise
         for (int i = threadIdx.x; i < 16 * 64; i += 256) {
-            const int kk = i / 64, mm = i % 64;
+            const int kk = TRANS_A ? i / 64 : i % 16, mm = TRANS_A ? i % 64 : i / 16;
             const int gm = m0 + mm, gk = k0 + kk;
-            float va = 0.0f, vb = 0.0f;
-            if (gm < M && gk < K) va = to_f32(TRANS_A ? A[(size_t)gk * lda + gm] : A[(size_t)gm * lda + gk]);
-            const int gn = n0 + mm;
-            if (gn < Nc && gk < K) vb = TRANS_B ? B[(size_t)gn * ldb + gk] : B[(size_t)gk * ldb + gn];
-            As[kk][mm] = va;
-            Bs[kk][mm] = vb;
+            As[kk][mm] = (gm < M && gk < ke) ? to_f32(TRANS_A ? A[(size_t)gk * lda + gm] : A[(size_t)gm * lda + gk])
+                                             : 0.0f;
+        }
+        for (int i = threadIdx.x; i < 16 * 64; i += 256) {
+            const int kk = TRANS_B ? i % 16 : i / 64, nn = TRANS_B ? i / 16 : i % 64;
+            const int gn = n0 + nn, gk = k0 + kk;
+            Bs[kk][nn] = (gn < Nc && gk < ke) ? (TRANS_B ? B[(size_t)gn * ldb + gk] : B[(size_t)gk * ldb + gn]) : 0.0f;
         }
         __syncthreads();
 #pragma unroll
@@ -274,6 +282,14 @@ __global__ void __launch_bounds__(256) k_bwd_dx(const __nv_bfloat16 *__restrict_
     }
 }
 
+__global__ void k_sum_slabs(const float *__restrict__ slabs, int nslab, int64_t n, float *__restrict__ out) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        float s = 0.0f;
+        for (int z = 0; z < nslab; ++z) s += slabs[(size_t)z * n + i];
+        out[i] = s;
+    }
+}
+
 __global__ void k_col_sum(const float *__restrict__ a, int rows, int cols, float *__restrict__ out) {
     const int c = blockIdx.x * blockDim.x + threadIdx.x;
     if (c >= cols) return;
@@ -288,6 +304,12 @@ int grid_of(int64_t work, int threads) {
 }
 
 }  // namespace
+
+int dwr_splits(const moe_config &c) {
+    // enough CTAs for two waves of 148 SMs, at most 16 slabs
+    const int tiles = ((c.N + 63) / 64) * ((c.d + 63) / 64);
+    return std::max(1, std::min(16, (296 + tiles - 1) / tiles));
+}
 
 BwdLayout bwd_layout(const moe_config &c) {
     BwdLayout L;
@@ -327,6 +349,7 @@ BwdLayout bwd_layout(const moe_config &c) {
     L.routed = take(N * 4);
     L.dL = take(T * N * 4);
     L.dxr = take(T * d * 4);
+    L.wr_slabs = take((size_t)dwr_splits(c) * d * N * 4);
     L.total = o;
     return L;
 }
@@ -370,15 +393,21 @@ cudaError_t launch_router_bwd(const moe_config &c, const void *x, const float *w
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // dx_router [T][d] = dL [T][N] · W_rᵀ  (W_r is [d][N])
     k_simt_gemm<float, false, true><<<dim3((c.d + 63) / 64, (c.T + 63) / 64), 256, 0, s>>>(dL, c.N, w_r, c.N, c.T, c.d,
-                                                                                          c.N, dxr);
+                                                                                          c.N, c.N, dxr);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    // dW_r [d][N] = xᵀ [d][T] · dL [T][N]
+    // dW_r [d][N] = xᵀ [d][T] · dL [T][N], split over the tokens into slabs summed in order
+    const int zs = dwr_splits(c);
+    const int kchunk = ((c.T + zs - 1) / zs + 15) / 16 * 16;
+    float *slabs = reinterpret_cast<float *>(bw + L.wr_slabs);
+    const dim3 g3((c.N + 63) / 64, (c.d + 63) / 64, zs);
     if (c.dtype == MOE_BF16)
-        k_simt_gemm<__nv_bfloat16, true, false><<<dim3((c.N + 63) / 64, (c.d + 63) / 64), 256, 0, s>>>(
-            static_cast<const __nv_bfloat16 *>(x), c.d, dL, c.N, c.d, c.N, c.T, dw_r);
+        k_simt_gemm<__nv_bfloat16, true, false><<<g3, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(x), c.d, dL, c.N,
+                                                                  c.d, c.N, c.T, kchunk, slabs);
     else
-        k_simt_gemm<float, true, false><<<dim3((c.N + 63) / 64, (c.d + 63) / 64), 256, 0, s>>>(
-            static_cast<const float *>(x), c.d, dL, c.N, c.d, c.N, c.T, dw_r);
+        k_simt_gemm<float, true, false><<<g3, 256, 0, s>>>(static_cast<const float *>(x), c.d, dL, c.N, c.d, c.N, c.T,
+                                                          kchunk, slabs);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    k_sum_slabs<<<grid_of((int64_t)c.d * c.N, 256), 256, 0, s>>>(slabs, zs, (int64_t)c.d * c.N, dw_r);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (db_r) {
         k_col_sum<<<(c.N + 255) / 256, 256, 0, s>>>(dL, c.T, c.N, db_r);

@@ -250,20 +250,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_wgrad_tc(const __grid_consta
 }
 
 // dst[b][c][off + r] = src[b][r][c]: a batch of R x C bf16 matrices transposed into
-// rows of stride ldd (32 x 32 tiles through shared memory).
+// rows of stride ldd. 64 x 64 tiles through shared memory; 16-byte loads along C and
+// 16-byte stores along R (C, R, ldd and off multiples of 8).
 __global__ void __launch_bounds__(256) k_transpose_batched(const __nv_bfloat16 *__restrict__ src, int R, int C,
                                                            __nv_bfloat16 *__restrict__ dst, int ldd, int off) {
-    __shared__ __nv_bfloat16 tile[32][34];
+    __shared__ __nv_bfloat16 tile[64][64 + 2];
     const int b = blockIdx.z;
-    const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const int c0 = blockIdx.x * 64, r0 = blockIdx.y * 64;
     const __nv_bfloat16 *sb = src + (size_t)b * R * C;
     __nv_bfloat16 *db = dst + (size_t)b * C * ldd;
-    for (int i = ty; i < 32; i += 8)
-        if (r0 + i < R && c0 + tx < C) tile[i][tx] = sb[(size_t)(r0 + i) * C + c0 + tx];
+    for (int v = threadIdx.x; v < 64 * 8; v += 256) {
+        const int i = v >> 3, j = (v & 7) * 8;  // row i, columns j .. j+7 of the tile
+        uint4 q = make_uint4(0, 0, 0, 0);
+        if (r0 + i < R && c0 + j < C) q = *reinterpret_cast<const uint4 *>(sb + (size_t)(r0 + i) * C + c0 + j);
+        const __nv_bfloat16 *e = reinterpret_cast<const __nv_bfloat16 *>(&q);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) tile[i][j + u] = e[u];
+    }
     __syncthreads();
-    for (int i = ty; i < 32; i += 8)
-        if (c0 + i < C && r0 + tx < R) db[(size_t)(c0 + i) * ldd + off + r0 + tx] = tile[tx][i];
+    for (int v = threadIdx.x; v < 64 * 8; v += 256) {
+        const int i = v >> 3, j = (v & 7) * 8;  // destination row c0 + i, rows j .. j+7 of the source
+        if (c0 + i < C && r0 + j < R) {
+            __align__(16) __nv_bfloat16 e[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) e[u] = tile[j + u][i];
+            *reinterpret_cast<uint4 *>(db + (size_t)(c0 + i) * ldd + off + r0 + j) = *reinterpret_cast<const uint4 *>(e);
+        }
+    }
 }
 
 // kpre[g] = sum over segments g' < g of R_g' rounded up to 64 (g = 0 .. n_seg), one CTA.
@@ -289,19 +302,19 @@ __global__ void __launch_bounds__(256) k_pad_prefix(const int32_t *__restrict__ 
 // Activation rows [rows][C] (row stride C) into the padded transposed layout
 // [C][Kall]: column kpre[g] + i holds row offsets[g] + i for i < R_g, zero up to
 // kpre[g + 1] and beyond kpre[n_seg]. offsets null: one segment of `rows` rows.
+// 64 x 64 tiles, 16-byte loads and stores (C and Kall multiples of 8).
 __global__ void __launch_bounds__(256) k_transpose_rows_padded(const __nv_bfloat16 *__restrict__ src, int C,
                                                                const int32_t *__restrict__ offsets,
                                                                const int32_t *__restrict__ kpre, int n_seg,
                                                                int rows, int64_t Kall,
                                                                __nv_bfloat16 *__restrict__ dst) {
-    __shared__ __nv_bfloat16 tile[32][34];
-    __shared__ int srow[32];
-    const int64_t k0 = (int64_t)blockIdx.x * 32;
-    const int c0 = blockIdx.y * 32;
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    if (ty == 0) {
-        // source row of padded column k0 + tx (-1: padding), by binary search on kpre
-        const int64_t kc = k0 + tx;
+    __shared__ __nv_bfloat16 tile[64][64 + 2];
+    __shared__ int srow[64];
+    const int64_t k0 = (int64_t)blockIdx.x * 64;
+    const int c0 = blockIdx.y * 64;
+    if (threadIdx.x < 64) {
+        // source row of padded column k0 + threadIdx.x (-1: padding), by binary search on kpre
+        const int64_t kc = k0 + threadIdx.x;
         int r = -1;
         if (!offsets) {
             r = kc < rows ? (int)kc : -1;
@@ -317,16 +330,28 @@ __global__ void __launch_bounds__(256) k_transpose_rows_padded(const __nv_bfloat
             const int64_t i = kc - kpre[lo];
             r = i < e - a ? (int)(a + i) : -1;
         }
-        srow[tx] = r;
+        srow[threadIdx.x] = r;
     }
     __syncthreads();
-    for (int i = ty; i < 32; i += 8) {
+    for (int v = threadIdx.x; v < 64 * 8; v += 256) {
+        const int i = v >> 3, j = (v & 7) * 8;  // padded column k0 + i, source columns c0 + j .. + 7
         const int r = srow[i];
-        tile[i][tx] = (r >= 0 && c0 + tx < C) ? src[(size_t)r * C + c0 + tx] : __float2bfloat16_rn(0.0f);
+        uint4 q = make_uint4(0, 0, 0, 0);
+        if (r >= 0 && c0 + j < C) q = *reinterpret_cast<const uint4 *>(src + (size_t)r * C + c0 + j);
+        const __nv_bfloat16 *e = reinterpret_cast<const __nv_bfloat16 *>(&q);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) tile[i][j + u] = e[u];
     }
     __syncthreads();
-    for (int i = ty; i < 32; i += 8)
-        if (c0 + i < C && k0 + tx < Kall) dst[(size_t)(c0 + i) * Kall + k0 + tx] = tile[tx][i];
+    for (int v = threadIdx.x; v < 64 * 8; v += 256) {
+        const int i = v >> 3, j = (v & 7) * 8;  // destination row c0 + i, padded columns k0 + j .. + 7
+        if (c0 + i < C && k0 + j < Kall) {
+            __align__(16) __nv_bfloat16 e[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) e[u] = tile[j + u][i];
+            *reinterpret_cast<uint4 *>(dst + (size_t)(c0 + i) * Kall + k0 + j) = *reinterpret_cast<const uint4 *>(e);
+        }
+    }
 }
 
 }  // namespace
@@ -371,7 +396,7 @@ cudaError_t launch_wgrad(const int32_t *offsets, int n_seg, int64_t a_rows, cons
 
 cudaError_t launch_transpose_batched(const void *src, int B, int R, int C, void *dst, int ldd, int off,
                                      cudaStream_t s) {
-    dim3 grid((C + 31) / 32, (R + 31) / 32, B);
+    dim3 grid((C + 63) / 64, (R + 63) / 64, B);
     k_transpose_batched<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(src), R, C,
                                              static_cast<__nv_bfloat16 *>(dst), ldd, off);
     return cudaGetLastError();
@@ -384,7 +409,7 @@ cudaError_t launch_pad_prefix(const int32_t *offsets, int n_seg, int rows, int32
 
 cudaError_t launch_transpose_rows_padded(const void *src, int C, const int32_t *offsets, const int32_t *kpre,
                                          int n_seg, int rows, int64_t Kall, void *dst, cudaStream_t s) {
-    dim3 grid((unsigned)((Kall + 31) / 32), (unsigned)((C + 31) / 32));
+    dim3 grid((unsigned)((Kall + 63) / 64), (unsigned)((C + 63) / 64));
     k_transpose_rows_padded<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(src), C, offsets, kpre, n_seg,
                                                  rows, Kall, static_cast<__nv_bfloat16 *>(dst));
     return cudaGetLastError();

@@ -71,9 +71,11 @@ struct BwdLayout {
     size_t AB_sh, dH_sh, dAB_sh, dX_sh, wo_sh_t, wab_sh_t;  // shared expert, rows = T
     size_t dy_t, Hsh_t, dABsh_t, x_t;                       // shared expert, [..][ceil64(T)]
     size_t logits, routed, dL, dxr;  // router: f32 [T][N], int32 [N], f32 [T][N], f32 [T][d]
+    size_t wr_slabs;                 // f32 [dwr_splits][d][N] partial router-weight gradients
     size_t total;
 };
 BwdLayout bwd_layout(const moe_config &c);
+int dwr_splits(const moe_config &c);  // token splits of the router-weight gradient
 
 // ---- launchers (return cudaGetLastError() after the launch) ----
 struct RouterOut {

@@ -5,7 +5,9 @@ Usage: python sparse_mixture_experts_64_b300/profile_cases.py CASE [--config NAM
   router  moe_router_topk alone (router logits, gating, expert scan, slot assignment);
   memory  moe_router_topk, moe_dispatch and moe_combine (no shared expert) with the
           config's activation sizes: the HBM-bound kernels without the expert weights,
-          so a DeepSeek-shaped case (0.94 GB of dispatched rows) holds about 2 GB.
+          so a DeepSeek-shaped case (0.94 GB of dispatched rows) holds about 2 GB;
+  backward  one moe_forward, then moe_backward --reps times (the full layer: expert
+          weights, their gradients and the backward scratch are all on the device).
 
 Inputs are seeded synthetic tensors of the config's shapes (x ~ N(0,1), router
 weight ~ N(0, 1/d), y_perm ~ N(0,1)); every launch goes through the library.
@@ -27,11 +29,13 @@ import workloads as W  # noqa: E402
 
 def main() -> None:
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=("router", "memory"))
+    ap.add_argument("case", choices=("router", "memory", "backward"))
     ap.add_argument("--config", default="deepseek_fine", choices=sorted(W.WORKLOADS))
     ap.add_argument("--reps", type=int, default=4)
     a = ap.parse_args()
     w = W.WORKLOADS[a.config]
+    if a.case == "backward":
+        return backward_case(w, a.reps)
     if a.case == "memory":
         w = w.replace(h_shared=0)
     dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
@@ -60,6 +64,35 @@ def main() -> None:
             moe.moe_combine(cfg, x, y_perm, slot_row, gate, None, None, None, y, ws)
     st = moe.moe_check_error(ws)
     print(f"{a.case} {w.name}: status {moe.status_str(st)}, "
+          f"{torch.cuda.max_memory_allocated() / 1e9:.2f} GB allocated")
+    if st != moe.MOE_OK:
+        sys.exit(1)
+
+
+def backward_case(w, reps: int) -> None:
+    cfg = moe.make_config(T=w.T, d=w.d, N=w.N, k=w.k, h=w.h, h_shared=w.h_shared, dtype=w.dtype,
+                          gating=w.gating, act=w.act, capacity_factor=w.capacity_factor,
+                          router_bias=w.router_bias)
+    inp = W.make_inputs(w, device="cuda")
+    ws, bws = moe.workspace(cfg), moe.backward_workspace(cfg)
+    T, d, k = w.T, w.d, w.k
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    gate = torch.empty((T, k), device="cuda")
+    y = torch.empty((T, d), dtype=inp["x"].dtype, device="cuda")
+    moe.moe_forward(cfg, inp["x"], inp["w_r"], inp["b_r"], inp["w_gate"], inp["w_up"], inp["w_down"],
+                    inp["shared_w_gate"], inp["shared_w_up"], inp["shared_w_down"], y, idx, gate, None, None,
+                    None, ws)
+    g = torch.Generator(device="cuda").manual_seed(2)
+    dy = torch.randn((T, d), device="cuda", generator=g).to(inp["x"].dtype)
+    e = lambda t: None if t is None else torch.empty_like(t)  # noqa: E731
+    out = [e(inp[n]) for n in ("x", "w_r", "b_r", "w_gate", "w_up", "w_down", "shared_w_gate", "shared_w_up",
+                               "shared_w_down")]
+    for _ in range(reps):
+        moe.moe_backward(cfg, inp["x"], inp["w_r"], inp["b_r"], inp["w_gate"], inp["w_up"], inp["w_down"],
+                         inp["shared_w_gate"], inp["shared_w_up"], inp["shared_w_down"], idx, gate, dy, 0.01,
+                         0.001, *out, ws, bws)
+    st = moe.moe_check_error(ws)
+    print(f"backward {w.name}: status {moe.status_str(st)}, "
           f"{torch.cuda.max_memory_allocated() / 1e9:.2f} GB allocated")
     if st != moe.MOE_OK:
         sys.exit(1)
