@@ -194,48 +194,73 @@ __global__ void __launch_bounds__(256) k_router_bwd(RouterBwdArgs a) {
 
 // C[M][Nc] (fp32) = sum_k A(m, k) B(k, n): A(m, k) = A[m * lda + k] or, transposed,
 // A[k * lda + m]; B(k, n) = B[k * ldb + n] or, transposed, B[n * ldb + k]. 64 x 64
-// tiles, 16-deep K slices through shared memory, 4 x 4 outputs per thread.
+// tiles, 16-deep K slices through a double-buffered shared-memory slice (the next
+// slice's global loads are in flight while the current one is multiplied), 4 x 4
+// outputs per thread. Consecutive threads read consecutive addresses: along m / n
+// when that is the operand's contiguous dimension, along k otherwise.
 //
 // Split K: blockIdx.z takes K range [z * kchunk, (z + 1) * kchunk) and writes its own
 // slab C + z * M * Nc (summed afterwards in slab order by k_sum_slabs).
 template <typename TA, bool TRANS_A, bool TRANS_B>
 __global__ void __launch_bounds__(256) k_simt_gemm(const TA *__restrict__ A, int lda, const float *__restrict__ B,
                                                    int ldb, int M, int Nc, int K, int kchunk, float *__restrict__ C) {
-    __shared__ float As[16][64 + 4], Bs[16][64 + 4];
+    __shared__ float As[2][16][64 + 4], Bs[2][16][64 + 4];
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
     const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
     const int kb = blockIdx.z * kchunk, ke = min(K, kb + kchunk);
     C += (size_t)blockIdx.z * M * Nc;
+    float ra[4], rb[4];
+    auto fetch = [&](int k0) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int i = threadIdx.x + q * 256;
+            {
+                const int kk = TRANS_A ? i / 64 : i % 16, mm = TRANS_A ? i % 64 : i / 16;
+                const int gm = m0 + mm, gk = k0 + kk;
+                ra[q] = (gm < M && gk < ke) ? to_f32(TRANS_A ? A[(size_t)gk * lda + gm] : A[(size_t)gm * lda + gk])
+                                            : 0.0f;
+            }
+            {
+                const int kk = TRANS_B ? i % 16 : i / 64, nn = TRANS_B ? i / 16 : i % 64;
+                const int gn = n0 + nn, gk = k0 + kk;
+                rb[q] = (gn < Nc && gk < ke) ? (TRANS_B ? B[(size_t)gn * ldb + gk] : B[(size_t)gk * ldb + gn]) : 0.0f;
+            }
+        }
+    };
+    auto stash = [&](int buf) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int i = threadIdx.x + q * 256;
+            As[buf][TRANS_A ? i / 64 : i % 16][TRANS_A ? i % 64 : i / 16] = ra[q];
+            Bs[buf][TRANS_B ? i % 16 : i / 64][TRANS_B ? i / 16 : i % 64] = rb[q];
+        }
+    };
     float acc[4][4] = {};
+    int buf = 0;
+    if (kb < ke) {
+        fetch(kb);
+        stash(0);
+    }
+    __syncthreads();
     for (int k0 = kb; k0 < ke; k0 += 16) {
-        // consecutive threads read consecutive addresses: along m / n when that is the
-        // contiguous dimension of the operand, along k otherwise
-        for (int i = threadIdx.x; i < 16 * 64; i += 256) {
-            const int kk = TRANS_A ? i / 64 : i % 16, mm = TRANS_A ? i % 64 : i / 16;
-            const int gm = m0 + mm, gk = k0 + kk;
-            As[kk][mm] = (gm < M && gk < ke) ? to_f32(TRANS_A ? A[(size_t)gk * lda + gm] : A[(size_t)gm * lda + gk])
-                                             : 0.0f;
-        }
-        for (int i = threadIdx.x; i < 16 * 64; i += 256) {
-            const int kk = TRANS_B ? i % 16 : i / 64, nn = TRANS_B ? i / 16 : i % 64;
-            const int gn = n0 + nn, gk = k0 + kk;
-            Bs[kk][nn] = (gn < Nc && gk < ke) ? (TRANS_B ? B[(size_t)gn * ldb + gk] : B[(size_t)gk * ldb + gn]) : 0.0f;
-        }
-        __syncthreads();
+        const bool more = k0 + 16 < ke;
+        if (more) fetch(k0 + 16);
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk) {
-            float a[4], b[4];
+            float av[4], bv[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                a[i] = As[kk][ty * 4 + i];
-                b[i] = Bs[kk][tx * 4 + i];
+                av[i] = As[buf][kk][ty * 4 + i];
+                bv[i] = Bs[buf][kk][tx * 4 + i];
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = __fmaf_rn(a[i], b[j], acc[i][j]);
+                for (int j = 0; j < 4; ++j) acc[i][j] = __fmaf_rn(av[i], bv[j], acc[i][j]);
         }
+        if (more) stash(buf ^ 1);
         __syncthreads();
+        buf ^= 1;
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i)
