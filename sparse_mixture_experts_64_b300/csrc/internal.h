@@ -127,6 +127,9 @@ cudaError_t launch_router_assign(const moe_config &c, const int32_t *topk_idx, c
 
 cudaError_t launch_dispatch(const moe_config &c, const void *x, const int32_t *perm_token,
                             const int32_t *offsets, void *x_perm, uint32_t *err, cudaStream_t s);
+// Dispatch in token order from slot_row [T][k] (each token read once).
+cudaError_t launch_dispatch_tokens(const moe_config &c, const void *x, const int32_t *slot_row, void *x_perm,
+                                   uint32_t *err, cudaStream_t s);
 
 cudaError_t launch_combine(const moe_config &c, const void *x, const void *y_perm,
                            const void *s_out, const int32_t *slot_row, const float *gate,

@@ -552,7 +552,8 @@ static moe_status forward_impl(const moe_config *cfg, const void *x, const float
     if (e != cudaSuccess || mark(1) != cudaSuccess) return MOE_ERR_CUDA;
 
     void *x_perm = w + L.x_perm, *y_perm = w + L.y_perm;
-    e = launch_dispatch(c, x, o.perm_token, o.expert_offsets, x_perm, err, stream);
+    e = ec ? launch_dispatch(c, x, o.perm_token, o.expert_offsets, x_perm, err, stream)
+           : launch_dispatch_tokens(c, x, o.slot_row, x_perm, err, stream);
     if (e != cudaSuccess || mark(2) != cudaSuccess) return MOE_ERR_CUDA;
 
     FfnGroup g{};
