@@ -32,8 +32,14 @@ def main() -> None:
     ap.add_argument("case", choices=("router", "memory", "backward"))
     ap.add_argument("--config", default="deepseek_fine", choices=sorted(W.WORKLOADS))
     ap.add_argument("--reps", type=int, default=4)
+    ap.add_argument("--tokens", type=int, default=None, help="override T (smaller cases)")
+    ap.add_argument("--experts", type=int, default=None, help="override N")
+    ap.add_argument("--hidden", type=int, default=None, help="override h")
     a = ap.parse_args()
     w = W.WORKLOADS[a.config]
+    over = {k: v for k, v in (("T", a.tokens), ("N", a.experts), ("h", a.hidden)) if v}
+    if over:
+        w = w.replace(name=w.name + "_" + "_".join(f"{k}{v}" for k, v in over.items()), **over)
     if a.case == "backward":
         return backward_case(w, a.reps)
     if a.case == "memory":
