@@ -467,7 +467,30 @@ def run_ours(a, w, world, rank, local):
     counts_kept = kept.cpu().tolist()
     rows = int(sum(counts_kept))
 
-    # ---- timed region: K forwards, per-step CUDA events on the launching stream
+    # ---- one CUDA graph of the whole forward per timed step, each with its own six
+    # stage events (before the router ... after combine) captured as graph nodes, so
+    # that the step times and the stage times come from the same timed launches
+    graphs, gevs, graph_note = [], [], None
+    try:
+        for i in range(a.steps):
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+            for ev in evs:
+                ev.record(stream)
+            graphs.append(moe.moe_forward_graph_create(cfg, inp["x"], inp["w_r"], inp["b_r"], inp["w_gate"],
+                                                       inp["w_up"], inp["w_down"], inp["shared_w_gate"],
+                                                       inp["shared_w_up"], inp["shared_w_down"], y, idx, gate,
+                                                       routed, kept, aux, ws, events=evs))
+            gevs.append(evs)
+        for g_ in graphs:                   # warm-up: every graph launched once
+            g_.launch(stream)
+        torch.cuda.synchronize(dev)
+        gevs[0][0].elapsed_time(gevs[0][5])
+    except (RuntimeError, moe.MoeError) as exc:
+        graph_note = f"stream launches (graph capture failed: {exc})"
+        graphs, gevs = [], []
+    use_graph = bool(graphs)
+
+    # ---- timed region: K forwards on the launching stream
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps)]
     clocks = ClockSampler(local, enabled=not a.no_clocks)
@@ -477,33 +500,56 @@ def run_ours(a, w, world, rank, local):
     for i in range(a.steps):
         if flush is not None:
             flush.zero_()
-        starts[i].record(stream)
-        fwd()
-        ends[i].record(stream)
+        if use_graph:
+            graphs[i].launch(stream)
+        else:
+            starts[i].record(stream)
+            fwd()
+            ends[i].record(stream)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
     _barrier(world)
     clk = clocks.stop()
-    ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / a.steps
+    if use_graph:
+        ms = sum(g_[0].elapsed_time(g_[5]) for g_ in gevs) / a.steps
+        stage_ms = [sum(g_[j].elapsed_time(g_[j + 1]) for g_ in gevs) / a.steps for j in range(5)]
+    else:
+        ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / a.steps
     ms_max = _max_over_ranks(ms, world)
     value = world * T / (ms_max / 1e3)
+    st = moe.moe_check_error(ws, stream)
+    if st != moe.MOE_OK:
+        raise RuntimeError("device error word: " + moe.status_str(st))
 
-    # ---- per-stage durations (same launches, events between the stages)
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
-    for ev in evs:
-        ev.record(stream)
-    stage_ms = [0.0] * 5
-    nprof = max(10, a.steps // 2)
-    for i in range(nprof):
+    # ---- the same forwards as plain stream launches (moe_forward per step), for comparison
+    for i in range(a.steps):
         if flush is not None:
             flush.zero_()
-        moe.moe_forward_profiled(cfg, inp["x"], inp["w_r"], inp["b_r"], inp["w_gate"], inp["w_up"],
-                                 inp["w_down"], inp["shared_w_gate"], inp["shared_w_up"],
-                                 inp["shared_w_down"], y, idx, gate, routed, kept, aux, ws, evs,
-                                 stream)
-        evs[-1].synchronize()
-        for j in range(5):
-            stage_ms[j] += evs[j].elapsed_time(evs[j + 1]) / nprof
+        starts[i].record(stream)
+        fwd()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    stream_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / a.steps
+
+    if not use_graph:
+        # per-stage durations (same launches, events between the stages)
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        for ev in evs:
+            ev.record(stream)
+        stage_ms = [0.0] * 5
+        nprof = max(10, a.steps // 2)
+        for i in range(nprof):
+            if flush is not None:
+                flush.zero_()
+            moe.moe_forward_profiled(cfg, inp["x"], inp["w_r"], inp["b_r"], inp["w_gate"], inp["w_up"],
+                                     inp["w_down"], inp["shared_w_gate"], inp["shared_w_up"],
+                                     inp["shared_w_down"], y, idx, gate, routed, kept, aux, ws, evs,
+                                     stream)
+            evs[-1].synchronize()
+            for j in range(5):
+                stage_ms[j] += evs[j].elapsed_time(evs[j + 1]) / nprof
+    for g_ in graphs:
+        g_.destroy()
 
     # ---- end to end: every step copies its x from pinned host memory, runs the
     # forward and copies its y back; the copies of neighbouring steps overlap the
@@ -513,6 +559,12 @@ def run_ours(a, w, world, rank, local):
     y_host = [torch.empty_like(y, device="cpu").pin_memory() for _ in range(2)]
     x_dev = [torch.empty_like(inp["x"]) for _ in range(2)]
     y_dev = [torch.empty_like(y) for _ in range(2)]
+    e2e_graphs = []
+    if use_graph:
+        e2e_graphs = [moe.moe_forward_graph_create(cfg, x_dev[b], inp["w_r"], inp["b_r"], inp["w_gate"], inp["w_up"],
+                                                   inp["w_down"], inp["shared_w_gate"], inp["shared_w_up"],
+                                                   inp["shared_w_down"], y_dev[b], idx, gate, routed, kept, aux, ws)
+                      for b in range(2)]
     s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev = {n: [torch.cuda.Event() for _ in range(2)] for n in ("h2d", "comp", "d2h")}
     for n in ev:
@@ -528,7 +580,10 @@ def run_ours(a, w, world, rank, local):
             ev["h2d"][b].record(s_h2d)
             stream.wait_event(ev["h2d"][b])
             stream.wait_event(ev["d2h"][b])           # y_dev[b] no longer read
-            fwd(x_dev[b], y_dev[b])
+            if e2e_graphs:
+                e2e_graphs[b].launch(stream)
+            else:
+                fwd(x_dev[b], y_dev[b])
             ev["comp"][b].record(stream)
             s_d2h.wait_event(ev["comp"][b])
             with torch.cuda.stream(s_d2h):
@@ -549,6 +604,8 @@ def run_ours(a, w, world, rank, local):
     st = moe.moe_check_error(ws, stream)
     if st != moe.MOE_OK:
         raise RuntimeError("device error word: " + moe.status_str(st))
+    for g_ in e2e_graphs:
+        g_.destroy()
 
     # ---- roofline of the dominant kernel
     alg = algorithmic(w, rows, counts_kept)
@@ -600,7 +657,9 @@ def run_ours(a, w, world, rank, local):
                    "h_shared": w.h_shared, "gating": w.gating, "act": w.act,
                    "capacity_factor": w.capacity_factor, "router": "fp32",
                    "global_batch_tokens": world * T, "parallelism": f"replicas x{world}",
-                   "l2": l2_mode},
+                   "l2": l2_mode,
+                   "launch": graph_note or "one CUDA graph of the whole forward per step "
+                                           "(moe_forward_graph_launch); stage events inside the graph"},
         "roofline": roof,
         "layer_roofline": {"roofline_ms": layer_roof_ms, "frac": layer_roof_ms / ms_max,
                            "algorithmic_flops": alg["flops"], "algorithmic_bytes": alg["bytes"],
@@ -608,10 +667,12 @@ def run_ours(a, w, world, rank, local):
                            "peaks": f"{peaks['source']}: bf16 {peaks['bf16']} TFLOP/s, "
                                     f"HBM {peaks['hbm']} GB/s"},
         "stages_ms": stage, "rows_dispatched": rows,
+        "stream_launch_ms_per_step": stream_ms,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
                 "d2h_bytes_per_step": y_host[0].numel() * y_host[0].element_size(),
                 "ms_per_step": e2e_ms,
-                "pipelining": "copies of neighbouring steps overlap the forward (2 buffers, 3 streams)"},
+                "pipelining": "copies of neighbouring steps overlap the forward (2 buffers, 3 streams)",
+                "launch": "moe_forward_graph_launch" if e2e_graphs else "moe_forward"},
         "gpu_launches": launches_per_forward(w) * a.steps,
         "clocks": clk, "wall_s_timed": wall,
     }

@@ -387,6 +387,42 @@ moe_status moe_forward_profiled(const moe_config *cfg, const void *x, const floa
                                 int32_t *counts_kept, float *aux, void *ws, size_t ws_bytes,
                                 cudaStream_t stream, cudaEvent_t *events, int32_t n_events);
 
+/*
+ * The whole forward captured once as a CUDA graph and replayed (the layer's steps as
+ * in moe_forward; for small layers the host's launch work, not the GPU, bounds a
+ * stream of moe_forward calls, and one graph launch replaces its seven to ten kernel
+ * launches).
+ *
+ * moe_forward_graph_create validates its arguments exactly as moe_forward does and
+ * returns that status without capturing anything on an error; otherwise it captures
+ * one moe_forward with these arguments on a private stream and instantiates it into
+ * *out. Nothing runs on the GPU during create. Every pointer is baked into the graph:
+ * the caller keeps all buffers alive and in place until moe_forward_graph_destroy and
+ * changes inputs (x, weights) by writing into the same buffers; each launch then
+ * computes the layer from their current contents, routing included (all
+ * data-dependent sizes stay on the device). `events` is NULL (n_events 0) or six
+ * caller-created events recorded at the stages of moe_forward_profiled on every
+ * launch.
+ *
+ * moe_forward_graph_launch enqueues one forward on `stream` (any stream of the device
+ * the graph was created on); launches on one stream run in order, and two launches of
+ * one graph must not overlap (they share the workspace). Device errors go to the
+ * error word of ws as for moe_forward. moe_forward_graph_destroy frees the graph
+ * (NULL is a no-op) after the caller has synchronised with its last launch.
+ * Errors: MOE_ERR_INVALID_ARG (NULL out or graph, n_events not 0 or 6), the statuses
+ * of moe_forward, MOE_ERR_CUDA if capture or instantiation fails.
+ */
+typedef struct moe_forward_graph_s *moe_forward_graph;
+moe_status moe_forward_graph_create(const moe_config *cfg, const void *x, const float *w_r,
+                                    const float *b_r, const void *w_gate_or_w1, const void *w_up,
+                                    const void *w_down, const void *shared_w_gate,
+                                    const void *shared_w_up, const void *shared_w_down, void *y,
+                                    int32_t *topk_idx, float *topk_gate, int32_t *counts_routed,
+                                    int32_t *counts_kept, float *aux, void *ws, size_t ws_bytes,
+                                    cudaEvent_t *events, int32_t n_events, moe_forward_graph *out);
+moe_status moe_forward_graph_launch(moe_forward_graph graph, cudaStream_t stream);
+moe_status moe_forward_graph_destroy(moe_forward_graph graph);
+
 /* Synchronise `stream`, read and clear the device error word in `ws`.
  * Returns MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_FAULT or MOE_ERR_CUDA. */
 moe_status moe_check_error(void *ws, cudaStream_t stream);

@@ -33,7 +33,8 @@ EXPORTED = ("moe_validate_config", "moe_workspace_size", "moe_max_rows", "moe_ca
             "moe_forward_profiled", "moe_check_error", "moe_status_str", "moe_router_topk_noalloc",
             "moe_router_topk_train", "moe_router_shard_stats", "moe_router_shard_assign",
             "moe_router_expert_choice", "moe_combine_expert_choice", "moe_backward",
-            "moe_backward_workspace_size")
+            "moe_backward_workspace_size", "moe_forward_graph_create", "moe_forward_graph_launch",
+            "moe_forward_graph_destroy")
 
 
 class moe_config(ctypes.Structure):
@@ -76,6 +77,9 @@ def _load() -> ctypes.CDLL:
         "moe_combine": (I32, [cfgp, P, P, P, P, P, P, P, P, P, SZ, P]),
         "moe_forward": (I32, [cfgp] + [P] * 15 + [P, SZ, P]),
         "moe_forward_profiled": (I32, [cfgp] + [P] * 15 + [P, SZ, P, P, I32]),
+        "moe_forward_graph_create": (I32, [cfgp] + [P] * 15 + [P, SZ, P, I32, ctypes.POINTER(P)]),
+        "moe_forward_graph_launch": (I32, [P, P]),
+        "moe_forward_graph_destroy": (I32, [P]),
         "moe_check_error": (I32, [P, P]),
         "moe_status_str": (ctypes.c_char_p, [I32]),
     }
@@ -302,6 +306,56 @@ def moe_forward_profiled(cfg, x, w_r, b_r, w_gate_or_w1, w_up, w_down, shared_w_
                                      _p(ws), ws.numel() if ws is not None else 0,
                                      _stream(stream), handles, len(events)),
            "moe_forward_profiled")
+
+
+class ForwardGraph:
+    """Handle of a captured forward (moe_forward_graph_create). It keeps the tensors
+    baked into the graph alive until destroy(); launch() enqueues one forward."""
+
+    def __init__(self, handle, tensors, events):
+        self.handle = handle
+        self._keep = (tensors, events)
+
+    def launch(self, stream=None):
+        moe_forward_graph_launch(self, stream)
+
+    def destroy(self):
+        moe_forward_graph_destroy(self)
+
+    def __del__(self):
+        if getattr(self, "handle", None):
+            _lib.moe_forward_graph_destroy(self.handle)
+            self.handle = None
+
+
+def moe_forward_graph_create(cfg, x, w_r, b_r, w_gate_or_w1, w_up, w_down, shared_w_gate,
+                             shared_w_up, shared_w_down, y, topk_idx, topk_gate, counts_routed,
+                             counts_kept, aux, ws, events=None) -> ForwardGraph:
+    """Capture one moe_forward with these buffers into a CUDA graph. `events`: None or
+    six torch.cuda.Event recorded at the stages (each recorded once before, so that its
+    CUDA handle exists)."""
+    tensors = (x, w_r, b_r, w_gate_or_w1, w_up, w_down, shared_w_gate, shared_w_up,
+               shared_w_down, y, topk_idx, topk_gate, counts_routed, counts_kept, aux, ws)
+    handles = (ctypes.c_void_p * 6)(*[ev.cuda_event for ev in events]) if events else None
+    out = ctypes.c_void_p()
+    _check(_lib.moe_forward_graph_create(ctypes.byref(cfg), *[_p(t) for t in tensors[:-1]], _p(ws),
+                                         ws.numel() if ws is not None else 0, handles,
+                                         len(events) if events else 0, ctypes.byref(out)),
+           "moe_forward_graph_create")
+    return ForwardGraph(out.value, tensors, events)
+
+
+def moe_forward_graph_launch(graph, stream=None):
+    h = graph.handle if isinstance(graph, ForwardGraph) else graph
+    _check(_lib.moe_forward_graph_launch(h, _stream(stream)), "moe_forward_graph_launch")
+
+
+def moe_forward_graph_destroy(graph):
+    if isinstance(graph, ForwardGraph):
+        h, graph.handle = graph.handle, None
+    else:
+        h = graph
+    _check(_lib.moe_forward_graph_destroy(h), "moe_forward_graph_destroy")
 
 
 def moe_check_error(ws, stream=None) -> int:

@@ -178,7 +178,7 @@ cudaError_t run(const moe_config &c, const FfnGroup &g, cudaStream_t s) {
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if (g.mid_event && (e = cudaEventRecord(g.mid_event, s)) != cudaSuccess) return e;
+    if (g.mid_event && (e = cudaEventRecordWithFlags(g.mid_event, s, g.event_flags)) != cudaSuccess) return e;
     // product 2: out = hidden W_outᵀ
     SimtProblem<T> p2{g.offsets, g.n_seg, g.sh_rows, g.a_rows,
                       static_cast<const T *>(g.hid), static_cast<const T *>(g.sh_hid), g.h, g.h_sh,

@@ -512,7 +512,7 @@ cudaError_t launch_ffn_sw(const moe_config &c, const FfnGroup &g, uint32_t *err,
                                     g.sh_w_gate, g.sh_w_up, c.d, g.h_sh, g.sh_hid, err, s);
     }
     if (e != cudaSuccess) return e;
-    if (g.mid_event && (e = cudaEventRecord(g.mid_event, s)) != cudaSuccess) return e;
+    if (g.mid_event && (e = cudaEventRecordWithFlags(g.mid_event, s, g.event_flags)) != cudaSuccess) return e;
     // product 2: outputs
     return product<KIND_PLAIN>(g.offsets, g.n_seg, g.a_rows, g.hid, g.w_out, nullptr, g.h, c.d, g.out, g.sh_rows,
                                g.sh_hid, g.sh_w_down, nullptr, g.h_sh, c.d, g.sh_out, err, s);

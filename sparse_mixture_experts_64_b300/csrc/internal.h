@@ -155,6 +155,7 @@ struct FfnGroup {
     void *sh_out;            // [sh_rows][d]
     int h_sh;
     cudaEvent_t mid_event;   // if set: recorded between the two products
+    unsigned event_flags;    // cudaEventRecordExternal while a graph is being captured
 };
 cudaError_t launch_ffn_simt(const moe_config &c, const FfnGroup &g, uint32_t *err, cudaStream_t s);
 cudaError_t launch_ffn_tc(const moe_config &c, const FfnGroup &g, uint32_t *err, cudaStream_t s);

@@ -6,6 +6,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <new>
 
 #include "internal.h"
 
@@ -505,7 +506,8 @@ static moe_status forward_impl(const moe_config *cfg, const void *x, const float
                                const void *shared_w_gate, const void *shared_w_up,
                                const void *shared_w_down, void *y, int32_t *topk_idx, float *topk_gate,
                                int32_t *counts_routed, int32_t *counts_kept, float *aux, void *ws,
-                               size_t ws_bytes, cudaStream_t stream, cudaEvent_t *ev) {
+                               size_t ws_bytes, cudaStream_t stream, cudaEvent_t *ev,
+                               unsigned ev_flags = cudaEventRecordDefault) {
     moe_status st = validate(cfg);
     if (st != MOE_OK) return st;
     const moe_config &c = *cfg;
@@ -520,7 +522,9 @@ static moe_status forward_impl(const moe_config *cfg, const void *x, const float
     if ((st = check_ws(ws, ws_bytes, L.total)) != MOE_OK) return st;
     uint8_t *w = static_cast<uint8_t *>(ws);
     uint32_t *err = reinterpret_cast<uint32_t *>(w + L.err);
-    auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], stream) : cudaSuccess; };
+    // Under stream capture an event record only orders the capture unless it is
+    // external; external records become graph nodes that record on every launch.
+    auto mark = [&](int i) { return ev ? cudaEventRecordWithFlags(ev[i], stream, ev_flags) : cudaSuccess; };
 
     const bool ec = c.routing == MOE_ROUTING_EXPERT_CHOICE;
     if (ec && (topk_idx || topk_gate || aux)) return MOE_ERR_INVALID_ARG;  // token-choice outputs
@@ -569,6 +573,7 @@ static moe_status forward_impl(const moe_config *cfg, const void *x, const float
     g.h = c.h;
     g.act = c.act;
     g.mid_event = ev ? ev[3] : nullptr;
+    g.event_flags = ev_flags;
     if (c.h_shared) {
         g.sh_rows = c.T;
         g.sh_a = x;
@@ -614,6 +619,72 @@ moe_status moe_forward_profiled(const moe_config *cfg, const void *x, const floa
     return forward_impl(cfg, x, w_r, b_r, w_gate_or_w1, w_up, w_down, shared_w_gate, shared_w_up,
                         shared_w_down, y, topk_idx, topk_gate, counts_routed, counts_kept, aux, ws, ws_bytes,
                         stream, events);
+}
+
+struct moe_forward_graph_s {
+    cudaGraph_t graph;
+    cudaGraphExec_t exec;
+};
+
+moe_status moe_forward_graph_create(const moe_config *cfg, const void *x, const float *w_r, const float *b_r,
+                                    const void *w_gate_or_w1, const void *w_up, const void *w_down,
+                                    const void *shared_w_gate, const void *shared_w_up,
+                                    const void *shared_w_down, void *y, int32_t *topk_idx, float *topk_gate,
+                                    int32_t *counts_routed, int32_t *counts_kept, float *aux, void *ws,
+                                    size_t ws_bytes, cudaEvent_t *events, int32_t n_events,
+                                    moe_forward_graph *out) {
+    if (!out) return MOE_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (n_events != 0 && (n_events != 6 || !events)) return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i < n_events; ++i)
+        if (!events[i]) return MOE_ERR_INVALID_ARG;
+    // Config and workspace are checked before a stream or a capture exists; the pointer
+    // checks run inside forward_impl, which returns before its first launch on an error.
+    moe_status st = validate(cfg);
+    if (st != MOE_OK) return st;
+    if ((st = check_ws(ws, ws_bytes, ws_layout(*cfg).total)) != MOE_OK) return st;
+    cudaStream_t cs;
+    if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) return MOE_ERR_CUDA;
+    cudaGraph_t graph = nullptr;
+    if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed) != cudaSuccess) {
+        cudaStreamDestroy(cs);
+        return MOE_ERR_CUDA;
+    }
+    st = forward_impl(cfg, x, w_r, b_r, w_gate_or_w1, w_up, w_down, shared_w_gate, shared_w_up, shared_w_down, y,
+                      topk_idx, topk_gate, counts_routed, counts_kept, aux, ws, ws_bytes, cs,
+                      n_events ? events : nullptr, cudaEventRecordExternal);
+    const cudaError_t ce = cudaStreamEndCapture(cs, &graph);
+    cudaStreamDestroy(cs);
+    if (st == MOE_OK && ce != cudaSuccess) st = MOE_ERR_CUDA;
+    if (st != MOE_OK) {
+        if (graph) cudaGraphDestroy(graph);
+        return st;
+    }
+    cudaGraphExec_t exec = nullptr;
+    if (cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess) {
+        cudaGraphDestroy(graph);
+        return MOE_ERR_CUDA;
+    }
+    auto *g = new (std::nothrow) moe_forward_graph_s{graph, exec};
+    if (!g) {
+        cudaGraphExecDestroy(exec);
+        cudaGraphDestroy(graph);
+        return MOE_ERR_CUDA;
+    }
+    *out = g;
+    return MOE_OK;
+}
+
+moe_status moe_forward_graph_launch(moe_forward_graph graph, cudaStream_t stream) {
+    if (!graph) return MOE_ERR_INVALID_ARG;
+    return cudaGraphLaunch(graph->exec, stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status moe_forward_graph_destroy(moe_forward_graph graph) {
+    if (!graph) return MOE_OK;
+    const bool ok = cudaGraphExecDestroy(graph->exec) == cudaSuccess && cudaGraphDestroy(graph->graph) == cudaSuccess;
+    delete graph;
+    return ok ? MOE_OK : MOE_ERR_CUDA;
 }
 
 moe_status moe_check_error(void *ws, cudaStream_t stream) {

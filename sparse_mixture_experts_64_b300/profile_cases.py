@@ -7,7 +7,8 @@ Usage: python sparse_mixture_experts_64_b300/profile_cases.py CASE [--config NAM
           config's activation sizes: the HBM-bound kernels without the expert weights,
           so a DeepSeek-shaped case (0.94 GB of dispatched rows) holds about 2 GB;
   backward  one moe_forward, then moe_backward --reps times (the full layer: expert
-          weights, their gradients and the backward scratch are all on the device).
+          weights, their gradients and the backward scratch are all on the device);
+  forward  moe_forward --reps times on the config's full layer.
 
 Inputs are seeded synthetic tensors of the config's shapes (x ~ N(0,1), router
 weight ~ N(0, 1/d), y_perm ~ N(0,1)); every launch goes through the library.
@@ -29,7 +30,7 @@ import workloads as W  # noqa: E402
 
 def main() -> None:
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=("router", "memory", "backward"))
+    ap.add_argument("case", choices=("router", "memory", "backward", "forward"))
     ap.add_argument("--config", default="deepseek_fine", choices=sorted(W.WORKLOADS))
     ap.add_argument("--reps", type=int, default=4)
     ap.add_argument("--tokens", type=int, default=None, help="override T (smaller cases)")
@@ -42,6 +43,8 @@ def main() -> None:
         w = w.replace(name=w.name + "_" + "_".join(f"{k}{v}" for k, v in over.items()), **over)
     if a.case == "backward":
         return backward_case(w, a.reps)
+    if a.case == "forward":
+        return forward_case(w, a.reps)
     if a.case == "memory":
         w = w.replace(h_shared=0)
     dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
@@ -70,6 +73,28 @@ def main() -> None:
             moe.moe_combine(cfg, x, y_perm, slot_row, gate, None, None, None, y, ws)
     st = moe.moe_check_error(ws)
     print(f"{a.case} {w.name}: status {moe.status_str(st)}, "
+          f"{torch.cuda.max_memory_allocated() / 1e9:.2f} GB allocated")
+    if st != moe.MOE_OK:
+        sys.exit(1)
+
+
+def _layer_config(w):
+    return moe.make_config(T=w.T, d=w.d, N=w.N, k=w.k, h=w.h, h_shared=w.h_shared, dtype=w.dtype,
+                           gating=w.gating, act=w.act, capacity_factor=w.capacity_factor,
+                           router_bias=w.router_bias, routing=w.routing)
+
+
+def forward_case(w, reps: int) -> None:
+    cfg = _layer_config(w)
+    inp = W.make_inputs(w, device="cuda")
+    ws = moe.workspace(cfg)
+    y = torch.empty((w.T, w.d), dtype=inp["x"].dtype, device="cuda")
+    for _ in range(reps):
+        moe.moe_forward(cfg, inp["x"], inp["w_r"], inp["b_r"], inp["w_gate"], inp["w_up"], inp["w_down"],
+                        inp["shared_w_gate"], inp["shared_w_up"], inp["shared_w_down"], y, None, None, None,
+                        None, None, ws)
+    st = moe.moe_check_error(ws)
+    print(f"forward {w.name}: status {moe.status_str(st)}, "
           f"{torch.cuda.max_memory_allocated() / 1e9:.2f} GB allocated")
     if st != moe.MOE_OK:
         sys.exit(1)

@@ -196,3 +196,31 @@ def test_product_path_has_no_cpu_fallback():
             with open(os.path.join(pkg, name)) as f:
                 assert "import oracle" not in f.read() and "from oracle" not in open(
                     os.path.join(pkg, name)).read()
+
+
+def test_forward_graph_checks_before_capture():
+    """moe_forward_graph_create returns its status before any stream or capture exists
+    when the handle, the events, the config or the workspace is wrong; destroying a
+    NULL graph is a no-op and launching one is an error."""
+    lib = ctypes.CDLL(moe.library_path())
+    lib.moe_forward_graph_create.restype = ctypes.c_int32
+    P = ctypes.c_void_p
+    out = P()
+    good = _cfg()
+
+    def create(cfg, ws=0x1000, ws_bytes=1 << 40, events=None, n_events=0, out_p=ctypes.byref(out)):
+        args = [ctypes.byref(cfg)] + [P(0x100)] * 15 + [P(ws), ctypes.c_size_t(ws_bytes), events,
+                                                         ctypes.c_int32(n_events), out_p]
+        return lib.moe_forward_graph_create(*args)
+
+    assert create(good, out_p=None) == moe.MOE_ERR_INVALID_ARG
+    assert create(good, n_events=6) == moe.MOE_ERR_INVALID_ARG               # NULL events
+    three = (P * 3)(1, 2, 3)
+    assert create(good, events=three, n_events=3) == moe.MOE_ERR_INVALID_ARG
+    assert create(_cfg(T=0)) == moe.MOE_ERR_INVALID_ARG
+    assert create(_cfg(d=96)) == moe.MOE_ERR_UNSUPPORTED
+    assert create(good, ws=0) == moe.MOE_ERR_WORKSPACE
+    assert create(good, ws_bytes=16) == moe.MOE_ERR_WORKSPACE
+    assert out.value is None
+    assert lib.moe_forward_graph_destroy(None) == moe.MOE_OK
+    assert lib.moe_forward_graph_launch(None, None) == moe.MOE_ERR_INVALID_ARG
