@@ -105,10 +105,12 @@ typedef struct {
 /* debug_flags bits */
 #define MOE_DEBUG_FORCE_SIMT_FFN 1u  /* run the expert FFN on the CUDA-core kernel even for bf16 */
 #define MOE_DEBUG_FFN_PAIR 2u        /* bf16: always use the row-tile CTA-pair kernel (256-row tiles)  */
-#define MOE_DEBUG_FFN_SINGLE 4u      /* bf16: always use the row-tile single-CTA kernel (128-row tiles) */
+#define MOE_DEBUG_FFN_SINGLE 4u      /* bf16: always use the row-tile single-CTA kernel (128-row tiles),
+                                        in moe_backward also for the weight gradients */
 #define MOE_DEBUG_FFN_SWAP 8u        /* bf16: use the weights-as-M CTA-pair kernel (token tiles 32..256) */
 /* Without these flags bf16 experts run on the row-tile pair kernel when the row buffers hold at
-   least 224 rows per expert, else on the row-tile single-CTA kernel. */
+   least 224 rows per expert, else on the row-tile single-CTA kernel; the backward's weight
+   gradients run on CTA pairs when the gradient has at least 256 rows. */
 
 /* Validate a config on the host. No CUDA call is made. */
 moe_status moe_validate_config(const moe_config *cfg);

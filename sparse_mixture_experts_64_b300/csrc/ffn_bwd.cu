@@ -249,6 +249,254 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_wgrad_tc(const __grid_consta
     }
 }
 
+// ------------------------------------------------------------------ CTA-pair version
+//
+// The same tiles with 2-CTA (cta_group::2) MMAs, as the forward's pair kernel in
+// ffn_tc.cu: a cluster of two CTAs computes a 256 x 256 output tile per MMA
+// 256x256x16; each CTA stages 128 rows of At and 128 of the 256 rows of Bt per
+// k-block (a third less operand data per FLOP than the single-CTA kernel), both
+// halves complete on the even CTA's stage barrier, the even CTA issues the MMAs and
+// its commits arrive on both CTAs' barriers; each CTA's epilogue stores its 128 rows.
+constexpr int STAGES2 = 6;
+constexpr uint32_t HALF_BYTES = 128 * BK * 2;
+constexpr uint32_t STAGE2_BYTES = 2 * HALF_BYTES;
+constexpr size_t SMEM2_BYTES = (size_t)STAGES2 * STAGE2_BYTES + 1024;
+
+struct WgSmem2 {
+    uint64_t full[STAGES2], empty[STAGES2], tfull[2], tempty[2], drain;
+    uint32_t tmem_base;
+    int abort_flag;
+    int k0[MAX_SEG], kp[MAX_SEG];
+};
+
+// Tensor maps as in WgParams but with 128-row boxes for Bt (each CTA loads half).
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    k_wgrad_tc2(const __grid_constant__ WgParams p) {
+    __shared__ WgSmem2 s;
+    extern __shared__ uint8_t dyn_smem[];
+    const uint32_t dyn_base = smem_u32(dyn_smem);
+    uint8_t *tiles = dyn_smem + (((dyn_base + 1023u) & ~1023u) - dyn_base);
+    auto smA = [&](int st) { return tiles + (size_t)st * STAGE2_BYTES; };
+    auto smB = [&](int st) { return tiles + (size_t)st * STAGE2_BYTES + HALF_BYTES; };
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+    const int nseg = p.n_seg + p.has_sh;
+    const int mt = (p.M + 2 * BM - 1) / (2 * BM), nt = (p.Nn + BN - 1) / BN;
+    const int per_seg = mt * nt;
+    const int total = nseg * per_seg;
+
+    if (warp == 0) {
+        constexpr int PER = (MAX_SEG + 31) / 32;
+        int kp[PER];
+        int sum = 0;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int g = lane * PER + i;
+            int v = 0;
+            if (g < p.n_seg) {
+                const int r0 = min(max(p.offsets[g], 0), p.a_rows);
+                const int r1 = min(max(p.offsets[g + 1], r0), p.a_rows);
+                v = (r1 - r0 + BK - 1) / BK * BK;
+            }
+            kp[i] = v;
+            sum += v;
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += u;
+        }
+        int run = incl - sum;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int g = lane * PER + i;
+            if (g < p.n_seg) {
+                s.k0[g] = run;
+                s.kp[g] = kp[i];
+            }
+            run += kp[i];
+        }
+        if (lane == 0 && p.has_sh) {
+            s.k0[p.n_seg] = 0;
+            s.kp[p.n_seg] = p.K_sh;
+        }
+        if (lane == 0) {
+            for (int i = 0; i < STAGES2; ++i) {
+                mbar_init(&s.full[i], 1);
+                mbar_init(&s.empty[i], 1);
+            }
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(&s.tfull[i], 1);
+                mbar_init(&s.tempty[i], 8);  // 4 epilogue warps of each CTA
+            }
+            mbar_init(&s.drain, 1);
+            s.abort_flag = 0;
+            fence_mbar_init();
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(&s.tmem_base, 512);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // both CTAs' barriers initialised and TMEM allocated
+    tc_fence_after();
+    const uint32_t tmem_base = s.tmem_base;
+    if (tid == 0) {
+        // the pair MMA writes the same TMEM address in both CTAs
+        const uint32_t other = ld_shared_cluster_u32(map_to_rank(smem_u32(&s.tmem_base), rank ^ 1u));
+        if (other != tmem_base) {
+            s.abort_flag = 1;
+            record_error(p.err, kErrFault);
+        }
+    }
+    __syncthreads();
+    const bool run = s.abort_flag == 0;
+    volatile int *abort_flag = &s.abort_flag;
+    const uint32_t lead_tempty = map_to_rank(smem_u32(&s.tempty[0]), 0);
+
+    if (warp == 0) {
+        // ================= TMA producer (both CTAs) =================
+        if (lane == 0 && run) {
+            int st = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            uint32_t issued_mask = 0, issued_par = 0;
+            const uint32_t lead_full = map_to_rank(smem_u32(&s.full[0]), 0);
+            for (int tile = cluster; tile < total && ok; tile += nclusters) {
+                const int g = tile / per_seg, local = tile - g * per_seg;
+                const int m = local % mt, n = local / mt;
+                const bool sh = g >= p.n_seg;
+                const CUtensorMap *ta = sh ? &p.tmA_sh : &p.tmA;
+                const CUtensorMap *tb = sh ? &p.tmB_sh : &p.tmB;
+                const int k0 = s.k0[g];
+                const int arow = m * 2 * BM + (int)rank * BM, brow = n * BN + (int)rank * (BN / 2);
+                for (int kb = 0; kb < s.kp[g] / BK; ++kb) {
+                    if (!wait_bar(&s.empty[st], ph ^ 1, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = lead_full + 8u * (uint32_t)st;
+                    if (leader) mbar_arrive_expect_tx(&s.full[st], 2 * STAGE2_BYTES);
+                    tma_load_2d_pair(smA(st), ta, k0 + kb * BK, arow, fb);
+                    tma_load_2d_pair(smB(st), tb, k0 + kb * BK, brow, fb);
+                    issued_mask |= 1u << st;
+                    issued_par = (issued_par & ~(1u << st)) | (ph << st);
+                    if (++st == STAGES2) {
+                        st = 0;
+                        ph ^= 1;
+                    }
+                }
+            }
+            // loads in flight land before the CTA exits (the even CTA waits for both halves)
+            if (leader)
+                for (int i = 0; i < STAGES2; ++i)
+                    if (issued_mask & (1u << i)) drain_bar(&s.full[i], (issued_par >> i) & 1u);
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && run && leader) {
+            // ================= MMA issuer (even CTA) =================
+            constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, BN);
+            int st = 0, acc = 0;
+            uint32_t ph = 0, aph = 0;
+            bool ok = true;
+            for (int tile = cluster; tile < total && ok; tile += nclusters) {
+                const int g = tile / per_seg;
+                if (!wait_bar(&s.tempty[acc], aph ^ 1, abort_flag, p.err)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < s.kp[g] / BK; ++kb) {
+                    if (!wait_bar(&s.full[st], ph, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = desc_sw128(smem_u32(smA(st)));
+                    const uint64_t bd = desc_sw128(smem_u32(smB(st)));
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        umma_bf16_pair(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), IDESC,
+                                       (kb | kk) != 0 ? 1u : 0u);
+                    umma_commit_pair_mc(&s.empty[st], 0x3);
+                    if (++st == STAGES2) {
+                        st = 0;
+                        ph ^= 1;
+                    }
+                }
+                if (!ok) break;
+                umma_commit_pair_mc(&s.tfull[acc], 0x3);  // no MMA for an empty segment: zeros stored
+                if (++acc == 2) {
+                    acc = 0;
+                    aph ^= 1;
+                }
+            }
+            umma_commit_pair_mc(&s.drain, 0x1);
+            drain_bar(&s.drain, 0);
+        }
+    } else if (run) {
+        // ================= epilogue (warps 2..5 of both CTAs) =================
+        const int quarter = warp & 3;
+        const int r_in_tile = (int)rank * BM + quarter * 32 + lane;
+        int acc = 0;
+        uint32_t aph = 0;
+        for (int tile = cluster; tile < total; tile += nclusters) {
+            const int g = tile / per_seg, local = tile - g * per_seg;
+            const int m = local % mt, n = local / mt;
+            const bool sh = g >= p.n_seg;
+            if (!wait_bar(&s.tfull[acc], aph, abort_flag, p.err)) break;
+            tc_fence_after();
+            const int row = m * 2 * BM + r_in_tile;
+            const bool empty_seg = s.kp[g] == 0;
+            __nv_bfloat16 *crow = (sh ? p.C_sh : p.C + (size_t)g * p.M * p.Nn) + (size_t)row * p.Nn;
+            const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16);
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+                uint32_t v[32];
+                tmem_ld32(tbase + c, v);
+                tmem_ld_wait();
+                const int col = n * BN + c;
+                if (row < p.M && col < p.Nn) {
+                    uint32_t packed[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float f0 = empty_seg ? 0.0f : __uint_as_float(v[2 * i]);
+                        const float f1 = empty_seg ? 0.0f : __uint_as_float(v[2 * i + 1]);
+                        __nv_bfloat162 b = __floats2bfloat162_rn(f0, f1);
+                        packed[i] = *reinterpret_cast<uint32_t *>(&b);
+                    }
+                    uint4 *dst = reinterpret_cast<uint4 *>(crow + col);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (leader) mbar_arrive_relaxed(&s.tempty[acc]);
+                else mbar_arrive_remote_relaxed(lead_tempty + 8u * (uint32_t)acc);
+            }
+            if (++acc == 2) {
+                acc = 0;
+                aph ^= 1;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // the pair's MMAs and both epilogues are done with TMEM
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, 512);
+    }
+}
+
 // dst[b][c][off + r] = src[b][r][c]: a batch of R x C bf16 matrices transposed into
 // rows of stride ldd. 64 x 64 tiles through shared memory; 16-byte loads along C and
 // 16-byte stores along R (C, R, ldd and off multiples of 8).
@@ -360,7 +608,10 @@ int64_t wgrad_kall_bound(const moe_config &c) { return (max_rows(c) + 64LL * c.N
 
 cudaError_t launch_wgrad(const int32_t *offsets, int n_seg, int64_t a_rows, const void *At, const void *Bt,
                          int64_t Kall, int M, int Nn, void *out, const void *At_sh, const void *Bt_sh, int K_sh,
-                         void *out_sh, uint32_t *err, cudaStream_t s) {
+                         void *out_sh, uint32_t *err, cudaStream_t s, bool allow_pair) {
+    // CTA pairs once a 256-row output tile is not mostly empty
+    const bool pair = allow_pair && M >= 2 * BM;
+    const uint32_t box_b = pair ? BN / 2 : BN;
     WgParams p;
     memset(&p, 0, sizeof(p));
     p.offsets = offsets;
@@ -375,11 +626,25 @@ cudaError_t launch_wgrad(const int32_t *offsets, int n_seg, int64_t a_rows, cons
     p.err = err;
     if (n_seg > 0) {
         if (!encode_bf16_2d(&p.tmA, At, (uint64_t)Kall, (uint64_t)M, BM)) return cudaErrorInvalidValue;
-        if (!encode_bf16_2d(&p.tmB, Bt, (uint64_t)Kall, (uint64_t)Nn, BN)) return cudaErrorInvalidValue;
+        if (!encode_bf16_2d(&p.tmB, Bt, (uint64_t)Kall, (uint64_t)Nn, box_b)) return cudaErrorInvalidValue;
     }
     if (p.has_sh) {
         if (!encode_bf16_2d(&p.tmA_sh, At_sh, (uint64_t)K_sh, (uint64_t)M, BM)) return cudaErrorInvalidValue;
-        if (!encode_bf16_2d(&p.tmB_sh, Bt_sh, (uint64_t)K_sh, (uint64_t)Nn, BN)) return cudaErrorInvalidValue;
+        if (!encode_bf16_2d(&p.tmB_sh, Bt_sh, (uint64_t)K_sh, (uint64_t)Nn, box_b)) return cudaErrorInvalidValue;
+    }
+    if (pair) {
+        const int64_t tiles2 = (int64_t)(n_seg + p.has_sh) * ((M + 2 * BM - 1) / (2 * BM)) * ((Nn + BN - 1) / BN);
+        if (tiles2 == 0) return cudaSuccess;
+        static bool attr2_done = false;
+        if (!attr2_done) {
+            cudaError_t e =
+                cudaFuncSetAttribute(k_wgrad_tc2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM2_BYTES);
+            if (e != cudaSuccess) return e;
+            attr2_done = true;
+        }
+        const int clusters = (int)std::max<int64_t>(1, std::min<int64_t>(tiles2, device_sm_count() / 2));
+        k_wgrad_tc2<<<2 * clusters, NUM_THREADS, SMEM2_BYTES, s>>>(p);
+        return cudaGetLastError();
     }
     const int64_t tiles = (int64_t)(n_seg + p.has_sh) * ((M + BM - 1) / BM) * ((Nn + BN - 1) / BN);
     if (tiles == 0) return cudaSuccess;

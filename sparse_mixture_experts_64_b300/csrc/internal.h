@@ -175,7 +175,7 @@ cudaError_t launch_gemm_rows(const moe_config &c, bool preact, const int32_t *of
 // over K_sh (a multiple of 64) columns.
 cudaError_t launch_wgrad(const int32_t *offsets, int n_seg, int64_t a_rows, const void *At, const void *Bt,
                          int64_t Kall, int M, int Nn, void *out, const void *At_sh, const void *Bt_sh, int K_sh,
-                         void *out_sh, uint32_t *err, cudaStream_t s);
+                         void *out_sh, uint32_t *err, cudaStream_t s, bool allow_pair = true);
 // Upper bound of Kall (columns of the padded transposed layout) for a config.
 int64_t wgrad_kall_bound(const moe_config &c);
 // kpre[g] = sum over g' < g of rows of segment g' rounded up to 64 (g = 0 .. n_seg).

@@ -390,24 +390,25 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const float *w_r, 
     ok(launch_transpose_rows_padded(hid, h, offsets, kpre, N, (int)R, Kall, bw + B.H_t, stream));
     ok(launch_transpose_rows_padded(dAB, Wd, offsets, kpre, N, (int)R, Kall, bw + B.dAB_t, stream));
     ok(launch_transpose_rows_padded(x_perm, d, offsets, kpre, N, (int)R, Kall, bw + B.X_t, stream));
+    const bool pair_ok = !(c.debug_flags & MOE_DEBUG_FFN_SINGLE);
     ok(launch_wgrad(offsets, N, R, bw + B.dO_t, bw + B.H_t, Kall, d, h, dw_down, nullptr, nullptr, 0, nullptr, err,
-                    stream));
+                    stream, pair_ok));
     ok(launch_wgrad(offsets, N, R, bw + B.dAB_t, bw + B.X_t, Kall, h, d, dw_gate_or_w1, nullptr, nullptr, 0, nullptr,
-                    err, stream));
+                    err, stream, pair_ok));
     if (gated)
         ok(launch_wgrad(offsets, N, R, bw + B.dAB_t + (size_t)h * Kall * 2, bw + B.X_t, Kall, h, d, dw_up, nullptr,
-                        nullptr, 0, nullptr, err, stream));
+                        nullptr, 0, nullptr, err, stream, pair_ok));
     if (hs) {
         ok(launch_transpose_rows_padded(dy, d, nullptr, nullptr, 1, c.T, Tp, bw + B.dy_t, stream));
         ok(launch_transpose_rows_padded(hid_sh, hs, nullptr, nullptr, 1, c.T, Tp, bw + B.Hsh_t, stream));
         ok(launch_transpose_rows_padded(bw + B.dAB_sh, 2 * hs, nullptr, nullptr, 1, c.T, Tp, bw + B.dABsh_t, stream));
         ok(launch_transpose_rows_padded(x, d, nullptr, nullptr, 1, c.T, Tp, bw + B.x_t, stream));
         ok(launch_wgrad(nullptr, 0, 0, nullptr, nullptr, 0, d, hs, nullptr, bw + B.dy_t, bw + B.Hsh_t, (int)Tp,
-                        dshared_w_down, err, stream));
+                        dshared_w_down, err, stream, pair_ok));
         ok(launch_wgrad(nullptr, 0, 0, nullptr, nullptr, 0, hs, d, nullptr, bw + B.dABsh_t, bw + B.x_t, (int)Tp,
-                        dshared_w_gate, err, stream));
+                        dshared_w_gate, err, stream, pair_ok));
         ok(launch_wgrad(nullptr, 0, 0, nullptr, nullptr, 0, hs, d, nullptr, bw + B.dABsh_t + (size_t)hs * Tp * 2,
-                        bw + B.x_t, (int)Tp, dshared_w_up, err, stream));
+                        bw + B.x_t, (int)Tp, dshared_w_up, err, stream, pair_ok));
     }
     // router: logits recomputed, dL, dx_router, dW_r, db
     ok(launch_router_logits(c, x, w_r, c.has_router_bias ? b_r : nullptr, reinterpret_cast<float *>(bw + B.logits), w,

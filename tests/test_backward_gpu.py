@@ -51,8 +51,8 @@ CASES = [
 ]
 
 
-def _run(w, aux_coef, z_coef, seed=3):
-    cfg = cfg_of(w)
+def _run(w, aux_coef, z_coef, seed=3, debug_flags=0):
+    cfg = cfg_of(w, debug_flags=debug_flags)
     inp = W.make_inputs(w, device="cuda")
     ws = moe.workspace(cfg)
     bws = moe.backward_workspace(cfg)
@@ -84,9 +84,22 @@ def _f(t):
     return None if t is None else t.float().cpu().numpy()
 
 
+
+
 @pytest.mark.parametrize("w,aux,z", CASES, ids=[c[0].name for c in CASES])
 def test_backward_matches_oracle(w, aux, z):
-    inp, dy, out = _run(w, aux, z)
+    _check(w, aux, z, 0)
+
+
+def test_backward_single_cta_kernels():
+    """The pair-kernel shape once more with every expert product and weight gradient
+    on the single-CTA kernels."""
+    w, aux, z = CASES[4]
+    _check(w, aux, z, moe.MOE_DEBUG_FFN_SINGLE)
+
+
+def _check(w, aux, z, flags):
+    inp, dy, out = _run(w, aux, z, debug_flags=flags)
     ref = O.backward(w, oracle_inputs(inp), _f(dy), aux_coef=aux, z_coef=z)
     errs = {"dx": _errs(_f(out["dx"]), ref["dx"]), "dw_r": _errs(_f(out["dw_r"]), ref["dw_r"])}
     if out["db_r"] is not None:
