@@ -467,30 +467,29 @@ def run_ours(a, w, world, rank, local):
     counts_kept = kept.cpu().tolist()
     rows = int(sum(counts_kept))
 
-    # ---- one CUDA graph of the whole forward per timed step, each with its own six
-    # stage events (before the router ... after combine) captured as graph nodes, so
-    # that the step times and the stage times come from the same timed launches
-    graphs, gevs, graph_note = [], [], None
-    try:
-        for i in range(a.steps):
-            evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
-            for ev in evs:
-                ev.record(stream)
-            graphs.append(moe.moe_forward_graph_create(cfg, inp["x"], inp["w_r"], inp["b_r"], inp["w_gate"],
-                                                       inp["w_up"], inp["w_down"], inp["shared_w_gate"],
-                                                       inp["shared_w_up"], inp["shared_w_down"], y, idx, gate,
-                                                       routed, kept, aux, ws, events=evs))
-            gevs.append(evs)
-        for g_ in graphs:                   # warm-up: every graph launched once
-            g_.launch(stream)
-        torch.cuda.synchronize(dev)
-        gevs[0][0].elapsed_time(gevs[0][5])
-    except (RuntimeError, moe.MoeError) as exc:
-        graph_note = f"stream launches (graph capture failed: {exc})"
-        graphs, gevs = [], []
-    use_graph = bool(graphs)
+    # ---- the forward captured once as a CUDA graph (moe_forward_graph_create); the
+    # timed steps launch it. Stage times come from a second pass over graphs that
+    # also record six events at the stage boundaries (one graph per step, so that
+    # every step's events can be read afterwards); an event between two kernels
+    # orders them fully, so that pass shows each stage alone, without the
+    # programmatic-launch overlap of neighbouring kernels that the timed graph has.
+    def make_graph(events=None, x=None, y_out=None):
+        return moe.moe_forward_graph_create(cfg, inp["x"] if x is None else x, inp["w_r"], inp["b_r"], inp["w_gate"],
+                                            inp["w_up"], inp["w_down"], inp["shared_w_gate"], inp["shared_w_up"],
+                                            inp["shared_w_down"], y if y_out is None else y_out, idx, gate, routed,
+                                            kept, aux, ws, events=events)
 
-    # ---- timed region: K forwards on the launching stream
+    graph, graph_note = None, None
+    try:
+        graph = make_graph()
+        for _ in range(max(3, a.warmup)):
+            graph.launch(stream)
+        torch.cuda.synchronize(dev)
+    except (RuntimeError, moe.MoeError) as exc:
+        graph_note = f"stream launches of moe_forward (graph capture failed: {exc})"
+        graph = None
+
+    # ---- timed region: K forwards, per-step CUDA events on the launching stream
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps)]
     clocks = ClockSampler(local, enabled=not a.no_clocks)
@@ -500,21 +499,17 @@ def run_ours(a, w, world, rank, local):
     for i in range(a.steps):
         if flush is not None:
             flush.zero_()
-        if use_graph:
-            graphs[i].launch(stream)
+        starts[i].record(stream)
+        if graph is not None:
+            graph.launch(stream)
         else:
-            starts[i].record(stream)
             fwd()
-            ends[i].record(stream)
+        ends[i].record(stream)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
     _barrier(world)
     clk = clocks.stop()
-    if use_graph:
-        ms = sum(g_[0].elapsed_time(g_[5]) for g_ in gevs) / a.steps
-        stage_ms = [sum(g_[j].elapsed_time(g_[j + 1]) for g_ in gevs) / a.steps for j in range(5)]
-    else:
-        ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / a.steps
+    ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / a.steps
     ms_max = _max_over_ranks(ms, world)
     value = world * T / (ms_max / 1e3)
     st = moe.moe_check_error(ws, stream)
@@ -531,13 +526,32 @@ def run_ours(a, w, world, rank, local):
     torch.cuda.synchronize(dev)
     stream_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / a.steps
 
-    if not use_graph:
-        # per-stage durations (same launches, events between the stages)
+    # ---- per-stage durations: one pass of K graphs with stage events, after warm-up
+    nprof = a.steps
+    stage_ms = None
+    if graph is not None:
+        try:
+            pgs = []
+            for _ in range(nprof):
+                evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+                for ev in evs:
+                    ev.record(stream)
+                pgs.append((make_graph(events=evs), evs))
+            for g_, _ in pgs:
+                if flush is not None:
+                    flush.zero_()
+                g_.launch(stream)
+            torch.cuda.synchronize(dev)
+            stage_ms = [sum(e_[j].elapsed_time(e_[j + 1]) for _, e_ in pgs) / nprof for j in range(5)]
+            for g_, _ in pgs:
+                g_.destroy()
+        except (RuntimeError, moe.MoeError):
+            stage_ms = None
+    if stage_ms is None:
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
         for ev in evs:
             ev.record(stream)
         stage_ms = [0.0] * 5
-        nprof = max(10, a.steps // 2)
         for i in range(nprof):
             if flush is not None:
                 flush.zero_()
@@ -548,8 +562,9 @@ def run_ours(a, w, world, rank, local):
             evs[-1].synchronize()
             for j in range(5):
                 stage_ms[j] += evs[j].elapsed_time(evs[j + 1]) / nprof
-    for g_ in graphs:
-        g_.destroy()
+    if graph is not None:
+        graph.destroy()
+    use_graph = graph is not None
 
     # ---- end to end: every step copies its x from pinned host memory, runs the
     # forward and copies its y back; the copies of neighbouring steps overlap the
@@ -559,12 +574,7 @@ def run_ours(a, w, world, rank, local):
     y_host = [torch.empty_like(y, device="cpu").pin_memory() for _ in range(2)]
     x_dev = [torch.empty_like(inp["x"]) for _ in range(2)]
     y_dev = [torch.empty_like(y) for _ in range(2)]
-    e2e_graphs = []
-    if use_graph:
-        e2e_graphs = [moe.moe_forward_graph_create(cfg, x_dev[b], inp["w_r"], inp["b_r"], inp["w_gate"], inp["w_up"],
-                                                   inp["w_down"], inp["shared_w_gate"], inp["shared_w_up"],
-                                                   inp["shared_w_down"], y_dev[b], idx, gate, routed, kept, aux, ws)
-                      for b in range(2)]
+    e2e_graphs = [make_graph(x=x_dev[b], y_out=y_dev[b]) for b in range(2)] if use_graph else []
     s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev = {n: [torch.cuda.Event() for _ in range(2)] for n in ("h2d", "comp", "d2h")}
     for n in ev:
@@ -658,8 +668,8 @@ def run_ours(a, w, world, rank, local):
                    "capacity_factor": w.capacity_factor, "router": "fp32",
                    "global_batch_tokens": world * T, "parallelism": f"replicas x{world}",
                    "l2": l2_mode,
-                   "launch": graph_note or "one CUDA graph of the whole forward per step "
-                                           "(moe_forward_graph_launch); stage events inside the graph"},
+                   "launch": graph_note or "the forward as one CUDA graph per step (moe_forward_graph_launch); "
+                                           "stage times from a pass of graphs with stage events"},
         "roofline": roof,
         "layer_roofline": {"roofline_ms": layer_roof_ms, "frac": layer_roof_ms / ms_max,
                            "algorithmic_flops": alg["flops"], "algorithmic_bytes": alg["bytes"],

@@ -108,6 +108,8 @@ typedef struct {
 #define MOE_DEBUG_FFN_SINGLE 4u      /* bf16: always use the row-tile single-CTA kernel (128-row tiles),
                                         in moe_backward also for the weight gradients */
 #define MOE_DEBUG_FFN_SWAP 8u        /* bf16: use the weights-as-M CTA-pair kernel (token tiles 32..256) */
+#define MOE_DEBUG_NO_PDL 16u         /* moe_forward: launch every kernel only after its predecessor has
+                                        completed (no programmatic dependent launch)             */
 /* Without these flags bf16 experts run on the row-tile pair kernel when the row buffers hold at
    least 224 rows per expert, else on the row-tile single-CTA kernel; the backward's weight
    gradients run on CTA pairs when the gradient has at least 256 rows. */

@@ -27,6 +27,7 @@ MOE_DEBUG_FORCE_SIMT_FFN = 1
 MOE_DEBUG_FFN_PAIR = 2
 MOE_DEBUG_FFN_SINGLE = 4
 MOE_DEBUG_FFN_SWAP = 8
+MOE_DEBUG_NO_PDL = 16
 
 EXPORTED = ("moe_validate_config", "moe_workspace_size", "moe_max_rows", "moe_capacity",
             "moe_router_topk", "moe_dispatch", "moe_grouped_ffn", "moe_combine", "moe_forward",

@@ -53,6 +53,44 @@ template <> struct Vec16<__nv_bfloat16> {
     }
 };
 
+// Programmatic dependent launch. The forward's kernels are launched with programmatic
+// stream serialisation (launch_pdl): a kernel may be scheduled while its predecessor
+// on the stream is still running, overlapping its launch and its prologue (barrier
+// setup, TMEM allocation) with the predecessor's last wave. pdl_wait() returns once
+// the predecessor grid has completed and its memory is visible; every such kernel
+// calls it before its first access to global memory, so the chain stays ordered
+// (each kernel's predecessor waited for its own predecessor before finishing).
+// pdl_launch_dependents() lets the next kernel be scheduled once every CTA of this
+// one has issued it; it is issued after pdl_wait(), so a waiting dependent never
+// holds an SM that a not yet started CTA of this grid needs. Both are no-ops for a
+// kernel launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_enter() {
+    pdl_wait();
+    pdl_launch_dependents();
+}
+
+// Set for the duration of a call whose config carries MOE_DEBUG_NO_PDL: launch_pdl
+// then launches plainly (every kernel waits for its predecessor's completion).
+extern thread_local bool g_no_pdl;
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = g_no_pdl ? 0 : 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // SiLU(z) = z / (1 + exp(-z)), fp32.
 __device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + __expf(-z)); }
 

@@ -25,6 +25,7 @@ __global__ void __launch_bounds__(256) k_dispatch(const T *__restrict__ x, const
                                                   uint32_t *err) {
     constexpr int V = Vec16<T>::n;
     const int vpr = d / V;  // vectors per row
+    pdl_enter();
     int64_t R = offsets[N];
     if (R < 0 || R > rmax) {
         if (blockIdx.x == 0 && threadIdx.x == 0) record_error(err, kErrFault);
@@ -57,6 +58,7 @@ __global__ void __launch_bounds__(256) k_dispatch_tokens(const T *__restrict__ x
     constexpr int V = Vec16<T>::n;
     const int vpr = d / V;
     const int64_t total = (int64_t)Ttok * vpr;
+    pdl_enter();
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
         const int t = (int)(i / vpr);
@@ -85,6 +87,7 @@ __global__ void __launch_bounds__(256) k_combine(const T *__restrict__ x, const 
     constexpr int V = Vec16<T>::n;
     const int vpr = d / V;
     const int64_t total = (int64_t)Ttok * vpr;
+    pdl_enter();
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
         const int t = (int)(i / vpr);
@@ -130,60 +133,45 @@ int grid_for(int64_t work, int threads) {
 cudaError_t launch_dispatch(const moe_config &c, const void *x, const int32_t *perm_token,
                             const int32_t *offsets, void *x_perm, uint32_t *err, cudaStream_t s) {
     const int64_t rmax = max_rows(c);
-    if (c.dtype == MOE_BF16) {
-        const int grid = grid_for(rmax * (c.d / 8), 256);
-        k_dispatch<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(x), perm_token,
-                                                       offsets, c.N, c.T, c.d, rmax,
-                                                       static_cast<__nv_bfloat16 *>(x_perm), err);
-    } else {
-        const int grid = grid_for(rmax * (c.d / 4), 256);
-        k_dispatch<float><<<grid, 256, 0, s>>>(static_cast<const float *>(x), perm_token, offsets, c.N,
-                                               c.T, c.d, rmax, static_cast<float *>(x_perm), err);
-    }
-    return cudaGetLastError();
+    if (c.dtype == MOE_BF16)
+        return launch_pdl(k_dispatch<__nv_bfloat16>, dim3(grid_for(rmax * (c.d / 8), 256)), dim3(256), 0, s,
+                          static_cast<const __nv_bfloat16 *>(x), perm_token, offsets, c.N, c.T, c.d, rmax,
+                          static_cast<__nv_bfloat16 *>(x_perm), err);
+    return launch_pdl(k_dispatch<float>, dim3(grid_for(rmax * (c.d / 4), 256)), dim3(256), 0, s,
+                      static_cast<const float *>(x), perm_token, offsets, c.N, c.T, c.d, rmax,
+                      static_cast<float *>(x_perm), err);
 }
 
 cudaError_t launch_dispatch_tokens(const moe_config &c, const void *x, const int32_t *slot_row, void *x_perm,
                                    uint32_t *err, cudaStream_t s) {
     const int64_t rmax = max_rows(c);
     if (c.dtype == MOE_BF16)
-        k_dispatch_tokens<__nv_bfloat16><<<grid_for((int64_t)c.T * (c.d / 8), 256), 256, 0, s>>>(
-            static_cast<const __nv_bfloat16 *>(x), slot_row, c.T, c.k, c.d, rmax, static_cast<__nv_bfloat16 *>(x_perm),
-            err);
-    else
-        k_dispatch_tokens<float><<<grid_for((int64_t)c.T * (c.d / 4), 256), 256, 0, s>>>(
-            static_cast<const float *>(x), slot_row, c.T, c.k, c.d, rmax, static_cast<float *>(x_perm), err);
-    return cudaGetLastError();
+        return launch_pdl(k_dispatch_tokens<__nv_bfloat16>, dim3(grid_for((int64_t)c.T * (c.d / 8), 256)), dim3(256),
+                          0, s, static_cast<const __nv_bfloat16 *>(x), slot_row, c.T, c.k, c.d, rmax,
+                          static_cast<__nv_bfloat16 *>(x_perm), err);
+    return launch_pdl(k_dispatch_tokens<float>, dim3(grid_for((int64_t)c.T * (c.d / 4), 256)), dim3(256), 0, s,
+                      static_cast<const float *>(x), slot_row, c.T, c.k, c.d, rmax, static_cast<float *>(x_perm),
+                      err);
+}
+
+template <typename T>
+static cudaError_t combine_typed(const moe_config &c, const void *x, const void *y_perm, const void *s_out,
+                                 const int32_t *slot_row, const float *gate, void *y, uint32_t *err, cudaStream_t s) {
+    const dim3 grid(grid_for((int64_t)c.T * (c.d / Vec16<T>::n), 256));
+    const T *sp = static_cast<const T *>(s_out);
+    return s_out ? launch_pdl(k_combine<T, true>, grid, dim3(256), 0, s, static_cast<const T *>(x),
+                              static_cast<const T *>(y_perm), sp, slot_row, gate, c.T, c.d, c.k, max_rows(c),
+                              static_cast<T *>(y), err)
+                 : launch_pdl(k_combine<T, false>, grid, dim3(256), 0, s, static_cast<const T *>(x),
+                              static_cast<const T *>(y_perm), sp, slot_row, gate, c.T, c.d, c.k, max_rows(c),
+                              static_cast<T *>(y), err);
 }
 
 cudaError_t launch_combine(const moe_config &c, const void *x, const void *y_perm, const void *s_out,
                            const int32_t *slot_row, const float *gate, void *y, uint32_t *err,
                            cudaStream_t s) {
-    const int64_t rmax = max_rows(c);
-    if (c.dtype == MOE_BF16) {
-        using T = __nv_bfloat16;
-        const int grid = grid_for((int64_t)c.T * (c.d / 8), 256);
-        if (s_out)
-            k_combine<T, true><<<grid, 256, 0, s>>>(static_cast<const T *>(x), static_cast<const T *>(y_perm),
-                                                    static_cast<const T *>(s_out), slot_row, gate, c.T, c.d,
-                                                    c.k, rmax, static_cast<T *>(y), err);
-        else
-            k_combine<T, false><<<grid, 256, 0, s>>>(static_cast<const T *>(x), static_cast<const T *>(y_perm),
-                                                     nullptr, slot_row, gate, c.T, c.d, c.k, rmax,
-                                                     static_cast<T *>(y), err);
-    } else {
-        using T = float;
-        const int grid = grid_for((int64_t)c.T * (c.d / 4), 256);
-        if (s_out)
-            k_combine<T, true><<<grid, 256, 0, s>>>(static_cast<const T *>(x), static_cast<const T *>(y_perm),
-                                                    static_cast<const T *>(s_out), slot_row, gate, c.T, c.d,
-                                                    c.k, rmax, static_cast<T *>(y), err);
-        else
-            k_combine<T, false><<<grid, 256, 0, s>>>(static_cast<const T *>(x), static_cast<const T *>(y_perm),
-                                                     nullptr, slot_row, gate, c.T, c.d, c.k, rmax,
-                                                     static_cast<T *>(y), err);
-    }
-    return cudaGetLastError();
+    if (c.dtype == MOE_BF16) return combine_typed<__nv_bfloat16>(c, x, y_perm, s_out, slot_row, gate, y, err, s);
+    return combine_typed<float>(c, x, y_perm, s_out, slot_row, gate, y, err, s);
 }
 
 }  // namespace moe

@@ -59,6 +59,7 @@ __device__ __forceinline__ float ec_exp(float x) {
 
 __global__ void __launch_bounds__(256) k_ec_scores(const float *__restrict__ L, int T, int N,
                                                    float *__restrict__ S_t, int32_t *__restrict__ tok_cnt) {
+    pdl_enter();
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= T) return;
     const float *l = L + (size_t)t * N;
@@ -118,6 +119,7 @@ __global__ void __launch_bounds__(1024) k_ec_select(SelectArgs a) {
     __shared__ int sh[33];
     const int e = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
     const float *s = a.S_t + (size_t)e * a.T;
+    pdl_enter();
     // key: score bits (non-negative floats order like their bits) above the
     // complemented token index, so that a descending sort puts lower tokens first
     // on equal scores; padding keys are 0, below every real key
@@ -173,6 +175,7 @@ __global__ void __launch_bounds__(1024) k_ec_scan(const int32_t *__restrict__ to
     __shared__ int sh[33];
     const int tid = threadIdx.x, nt = blockDim.x;
     const int per = (T + nt - 1) / nt;
+    pdl_enter();
     const int beg = min(T, tid * per), end = min(T, beg + per);
     int c = 0;
     for (int t = beg; t < end; ++t) c += tok_cnt[t];
@@ -188,6 +191,7 @@ __global__ void __launch_bounds__(1024) k_ec_scan(const int32_t *__restrict__ to
 // One thread per token: its rows in expert order.
 __global__ void __launch_bounds__(256) k_ec_fill(const int32_t *__restrict__ ec_row, const int32_t *__restrict__ tok_ptr,
                                                  int T, int N, int32_t *__restrict__ tok_rows) {
+    pdl_enter();
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= T) return;
     int p = tok_ptr[t];
@@ -206,6 +210,7 @@ __global__ void __launch_bounds__(256) k_combine_ec(const T *__restrict__ x, con
     constexpr int V = Vec16<T>::n;
     const int vpr = d / V;
     const int64_t total = (int64_t)Ttok * vpr;
+    pdl_enter();
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
         const int t = (int)(i / vpr);
@@ -247,15 +252,13 @@ cudaError_t combine_ec_typed(const moe_config &c, const void *x, const void *y_p
     const int64_t work = (int64_t)c.T * (c.d / Vec16<T>::n);
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((work + 255) / 256, (int64_t)device_sm_count() * 8));
     const int64_t rmax = max_rows(c);
-    if (s_out)
-        k_combine_ec<T, true><<<grid, 256, 0, s>>>(static_cast<const T *>(x), static_cast<const T *>(y_perm),
-                                                  static_cast<const T *>(s_out), tok_ptr, tok_rows, row_gate, c.T,
-                                                  c.d, rmax, static_cast<T *>(y), err);
-    else
-        k_combine_ec<T, false><<<grid, 256, 0, s>>>(static_cast<const T *>(x), static_cast<const T *>(y_perm),
-                                                   nullptr, tok_ptr, tok_rows, row_gate, c.T, c.d, rmax,
-                                                   static_cast<T *>(y), err);
-    return cudaGetLastError();
+    const T *sp = static_cast<const T *>(s_out);
+    return s_out ? launch_pdl(k_combine_ec<T, true>, dim3(grid), dim3(256), 0, s, static_cast<const T *>(x),
+                              static_cast<const T *>(y_perm), sp, tok_ptr, tok_rows, row_gate, c.T, c.d, rmax,
+                              static_cast<T *>(y), err)
+                 : launch_pdl(k_combine_ec<T, false>, dim3(grid), dim3(256), 0, s, static_cast<const T *>(x),
+                              static_cast<const T *>(y_perm), sp, tok_ptr, tok_rows, row_gate, c.T, c.d, rmax,
+                              static_cast<T *>(y), err);
 }
 
 }  // namespace
@@ -267,8 +270,7 @@ cudaError_t launch_expert_choice(const moe_config &c, const float *logits, int32
     float *S_t = reinterpret_cast<float *>(ws + L.ec_scores);
     int32_t *ec_row = reinterpret_cast<int32_t *>(ws + L.ec_row);
     int32_t *tok_cnt = reinterpret_cast<int32_t *>(ws + L.ec_tok_cnt);
-    k_ec_scores<<<(c.T + 255) / 256, 256, 0, s>>>(logits, c.T, c.N, S_t, tok_cnt);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(k_ec_scores, dim3((c.T + 255) / 256), dim3(256), 0, s, logits, c.T, c.N, S_t, tok_cnt);
     if (e != cudaSuccess) return e;
     int Tpad = 1;
     while (Tpad < c.T) Tpad <<= 1;
@@ -283,12 +285,9 @@ cudaError_t launch_expert_choice(const moe_config &c, const float *logits, int32
         attr_done = true;
     }
     SelectArgs sa{S_t, c.T, Tpad, c.N, Ce, ec_row, tok_cnt, expert_offsets, perm_token, row_gate};
-    k_ec_select<<<c.N, 1024, smem, s>>>(sa);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    k_ec_scan<<<1, 1024, 0, s>>>(tok_cnt, c.T, tok_ptr);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    k_ec_fill<<<(c.T + 255) / 256, 256, 0, s>>>(ec_row, tok_ptr, c.T, c.N, tok_rows);
-    return cudaGetLastError();
+    if ((e = launch_pdl(k_ec_select, dim3(c.N), dim3(1024), smem, s, sa)) != cudaSuccess) return e;
+    if ((e = launch_pdl(k_ec_scan, dim3(1), dim3(1024), 0, s, tok_cnt, c.T, tok_ptr)) != cudaSuccess) return e;
+    return launch_pdl(k_ec_fill, dim3((c.T + 255) / 256), dim3(256), 0, s, ec_row, tok_ptr, c.T, c.N, tok_rows);
 }
 
 cudaError_t launch_combine_ec(const moe_config &c, const void *x, const void *y_perm, const void *s_out,

@@ -52,6 +52,7 @@ __global__ void __launch_bounds__(256) k_ffn_simt(SimtProblem<T> p) {
     __shared__ __align__(16) float As[BK][BM];
     __shared__ __align__(16) float Bs[TWO ? 2 : 1][BK][BN];
 
+    pdl_enter();
     // ---- locate this CTA's segment and m-tile ----
     int y = blockIdx.y, seg = -1;
     int row0 = 0, rows = 0;
@@ -163,20 +164,21 @@ cudaError_t run(const moe_config &c, const FfnGroup &g, cudaStream_t s) {
                       static_cast<T *>(g.hid), static_cast<T *>(g.sh_hid), g.h, g.h_sh};
     const int nmax1 = std::max(g.n_seg ? g.h : 0, g.sh_rows ? g.h_sh : 0);
     dim3 grid1((nmax1 + BN - 1) / BN, (unsigned)mslots);
+    cudaError_t e;
     if (g.act == MOE_ACT_RELU && g.sh_rows == 0) {
-        k_ffn_simt<T, MODE_RELU><<<grid1, 256, 0, s>>>(p1);
+        e = launch_pdl(k_ffn_simt<T, MODE_RELU>, grid1, dim3(256), 0, s, p1);
     } else if (g.act == MOE_ACT_RELU) {
         // routed ReLU experts and a gated shared expert: two launches
         SimtProblem<T> pr = p1;
         pr.sh_rows = 0;
-        k_ffn_simt<T, MODE_RELU><<<grid1, 256, 0, s>>>(pr);
+        e = launch_pdl(k_ffn_simt<T, MODE_RELU>, grid1, dim3(256), 0, s, pr);
         SimtProblem<T> ps = p1;
         ps.n_seg = 0;
-        k_ffn_simt<T, MODE_GATED><<<dim3(grid1.x, (g.sh_rows + BM - 1) / BM), 256, 0, s>>>(ps);
+        if (e == cudaSuccess)
+            e = launch_pdl(k_ffn_simt<T, MODE_GATED>, dim3(grid1.x, (g.sh_rows + BM - 1) / BM), dim3(256), 0, s, ps);
     } else {
-        k_ffn_simt<T, MODE_GATED><<<grid1, 256, 0, s>>>(p1);
+        e = launch_pdl(k_ffn_simt<T, MODE_GATED>, grid1, dim3(256), 0, s, p1);
     }
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (g.mid_event && (e = cudaEventRecordWithFlags(g.mid_event, s, g.event_flags)) != cudaSuccess) return e;
     // product 2: out = hidden W_outᵀ
@@ -186,8 +188,7 @@ cudaError_t run(const moe_config &c, const FfnGroup &g, cudaStream_t s) {
                       static_cast<const T *>(g.sh_w_down), nullptr,
                       static_cast<T *>(g.out), static_cast<T *>(g.sh_out), c.d, c.d};
     dim3 grid2((c.d + BN - 1) / BN, (unsigned)mslots);
-    k_ffn_simt<T, MODE_PLAIN><<<grid2, 256, 0, s>>>(p2);
-    return cudaGetLastError();
+    return launch_pdl(k_ffn_simt<T, MODE_PLAIN>, grid2, dim3(256), 0, s, p2);
 }
 
 }  // namespace

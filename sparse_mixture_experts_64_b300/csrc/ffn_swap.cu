@@ -228,6 +228,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1) k_ff
 
     // ---- tile table and barriers ----
     if (warp == 0) {
+        pdl_wait();  // the offsets come from the router
         constexpr int PER = (MAX_SEG + 31) / 32;
         int cnt[PER];
         int sum = 0;
@@ -296,6 +297,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1) k_ff
     __syncthreads();
     cluster_sync();  // both CTAs' barriers initialised and TMEM allocated
     tc_fence_after();
+    pdl_enter();
     const uint32_t tmem_base = s.tmem_base;
     if (tid == 0) {
         // the pair MMA writes the same TMEM address in both CTAs
@@ -451,8 +453,7 @@ cudaError_t launch_kind(const SwParams &p, int64_t max_tiles, cudaStream_t s) {
         attr_done = true;
     }
     const int clusters = (int)std::max<int64_t>(1, std::min<int64_t>(max_tiles, device_sm_count() / 2));
-    k_ffn_sw2<KIND><<<2 * clusters, NUM_THREADS, SMEM_BYTES, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(k_ffn_sw2<KIND>, dim3(2 * clusters), dim3(NUM_THREADS), SMEM_BYTES, s, p);
 }
 
 // One product over the routed segments and/or the shared segment.

@@ -208,6 +208,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_ffn_tc(const __grid_constant
 
     // ---- tile table (warp 0) and barriers (thread 0) ----
     if (warp == 0) {
+        pdl_wait();  // the offsets come from the router
         constexpr int PER = (MAX_SEG + 31) / 32;
         int cnt[PER];
         int sum = 0;
@@ -272,6 +273,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_ffn_tc(const __grid_constant
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    pdl_enter();
     const uint32_t tmem_base = s.tmem_base;
     const int total = s.base[nseg];
     volatile int *abort_flag = &s.abort_flag;
@@ -449,6 +451,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 
     // ---- tile table (pair tiles of 256 rows) and barriers ----
     if (warp == 0) {
+        pdl_wait();  // the offsets come from the router
         constexpr int PER = (MAX_SEG + 31) / 32;
         int cnt[PER];
         int sum = 0;
@@ -514,6 +517,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     __syncthreads();
     cluster_sync();  // both CTAs' barriers initialised and TMEM allocated
     tc_fence_after();
+    pdl_enter();
     const uint32_t tmem_base = s.tmem_base;
     if (tid == 0) {
         // the pair MMA writes the same TMEM address in both CTAs
@@ -674,8 +678,7 @@ cudaError_t launch_kind(const TcParams &p, int64_t max_tiles, cudaStream_t s) {
         attr_done = true;
     }
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(max_tiles, device_sm_count()));
-    k_ffn_tc<KIND><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(k_ffn_tc<KIND>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, s, p);
 }
 
 // Accumulator buffers of the pair kernel (TMEM columns = 256 per buffer).
@@ -691,8 +694,7 @@ cudaError_t launch_kind2(const TcParams &p, int64_t max_tiles, cudaStream_t s) {
         attr_done = true;
     }
     const int clusters = (int)std::max<int64_t>(1, std::min<int64_t>(max_tiles, device_sm_count() / 2));
-    k_ffn_tc2<KIND, PAIR_NACC><<<2 * clusters, NUM_THREADS, SMEM2_BYTES, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(k_ffn_tc2<KIND, PAIR_NACC>, dim3(2 * clusters), dim3(NUM_THREADS), SMEM2_BYTES, s, p);
 }
 
 // One product over the routed segments and/or the shared segment.

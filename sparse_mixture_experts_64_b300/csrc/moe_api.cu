@@ -8,9 +8,21 @@
 #include <cstring>
 #include <new>
 
+#include "common.cuh"
 #include "internal.h"
 
 namespace moe {
+
+thread_local bool g_no_pdl = false;
+
+// Programmatic launches off for one call (MOE_DEBUG_NO_PDL), restored on return.
+struct PdlScope {
+    bool saved;
+    explicit PdlScope(const moe_config *c) : saved(g_no_pdl) {
+        if (c && (c->debug_flags & MOE_DEBUG_NO_PDL)) g_no_pdl = true;
+    }
+    ~PdlScope() { g_no_pdl = saved; }
+};
 
 int64_t max_rows(const moe_config &c) {
     const int32_t C = capacity_of(c);
@@ -490,6 +502,7 @@ moe_status moe_combine(const moe_config *cfg, const void *x, const void *y_perm,
 
 // Expert Choice: every expert takes Ce = min(C, T) tokens.
 __global__ void k_fill_counts(int32_t *a, int32_t *b, int n, int32_t v) {
+    moe::pdl_enter();
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i < n) {
         if (a) a[i] = v;
@@ -498,8 +511,8 @@ __global__ void k_fill_counts(int32_t *a, int32_t *b, int n, int32_t v) {
 }
 
 static cudaError_t fill_counts(const moe_config &c, int32_t *routed, int32_t *kept, cudaStream_t s) {
-    k_fill_counts<<<(c.N + 255) / 256, 256, 0, s>>>(routed, kept, c.N, (int32_t)(max_rows(c) / c.N));
-    return cudaGetLastError();
+    return moe::launch_pdl(k_fill_counts, dim3((c.N + 255) / 256), dim3(256), 0, s, routed, kept, c.N,
+                      (int32_t)(max_rows(c) / c.N));
 }
 
 static moe_status forward_impl(const moe_config *cfg, const void *x, const float *w_r, const float *b_r,
@@ -512,6 +525,7 @@ static moe_status forward_impl(const moe_config *cfg, const void *x, const float
     moe_status st = validate(cfg);
     if (st != MOE_OK) return st;
     const moe_config &c = *cfg;
+    const PdlScope pdl(cfg);
     if (!x || !w_r || !w_gate_or_w1 || !w_down || !y) return MOE_ERR_INVALID_ARG;
     if (c.act == MOE_ACT_SILU_GATED && !w_up) return MOE_ERR_INVALID_ARG;
     if (c.has_router_bias && !b_r) return MOE_ERR_INVALID_ARG;

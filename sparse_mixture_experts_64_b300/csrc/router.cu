@@ -376,6 +376,7 @@ __global__ void __launch_bounds__(256) k_transpose_wr(const float *__restrict__ 
     __shared__ float tile[32][33];
     const int i0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    pdl_enter();
     for (int r = ty; r < 32; r += 8)
         if (i0 + r < d && e0 + tx < N) tile[r][tx] = w_r[(size_t)(i0 + r) * N + e0 + tx];
     __syncthreads();
@@ -417,6 +418,7 @@ __global__ void __launch_bounds__(160) k_router_small(const __grid_constant__ CU
 
     if (tid == 0) ring.init(NW);
     __syncthreads();
+    pdl_enter();
 
     float acc[TO][NP];
 #pragma unroll
@@ -520,6 +522,7 @@ __global__ void __launch_bounds__(544, 1) k_logits_large(const __grid_constant__
 
     if (tid == 0) ring.init(NC);
     __syncthreads();
+    pdl_enter();
 
     float acc[TO][EO];
 #pragma unroll
@@ -589,6 +592,7 @@ __global__ void __launch_bounds__(256) k_gate(const float *__restrict__ logits, 
     int *Is = reinterpret_cast<int *>(smem + TT * a.N);  // [TT][8]
     const int t0 = blockIdx.x * TT;
     const int nrows = min(TT, a.T - t0);
+    pdl_enter();
     for (int i = threadIdx.x; i < nrows * a.N; i += blockDim.x) Ls[i] = logits[(size_t)t0 * a.N + i];
     __syncthreads();
     if (a.noise || a.zpart) {
@@ -672,6 +676,7 @@ __global__ void __launch_bounds__(256) k_expert_scan(ScanArgs a) {
     __shared__ float shf[32];
     const int e = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
     const int n = a.k * a.tiles;
+    pdl_enter();
     const int32_t *ce = a.cnt + (size_t)e * n;
     int32_t *pe = a.pre + (size_t)e * n;
     const int C = a.cap > 0 ? a.cap : INT_MAX;
@@ -773,6 +778,7 @@ __global__ void __launch_bounds__(256) k_assign(AssignArgs a) {
     const int tid = threadIdx.x, nt = blockDim.x, N = a.N, k = a.k;
     const int tile = blockIdx.x, t0 = tile * a.TT;
     const int C = a.cap > 0 ? a.cap : INT_MAX;
+    pdl_enter();
 
     // expert offsets (every CTA computes them; N <= 256 <= blockDim)
     {
@@ -876,8 +882,7 @@ cudaError_t launch_small(const moe_config &c, const XT *x, const float *w_t, con
     auto kern = k_router_small<XT, NP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
     if (e != cudaSuccess) return e;
-    kern<<<ra.tiles, 160, bytes, s>>>(tmx, w_t, b_r, ra);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(ra.tiles), dim3(160), bytes, s, tmx, w_t, b_r, ra);
 }
 
 template <typename XT>
@@ -890,8 +895,8 @@ cudaError_t launch_logits_only(const moe_config &c, const XT *x, const float *w_
     const size_t lbytes = 4 * stage + 1024;
     cudaError_t e = cudaFuncSetAttribute(k_logits_large<XT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lbytes);
     if (e != cudaSuccess) return e;
-    k_logits_large<XT><<<dim3((c.N + 31) / 32, (c.T + 15) / 16), 544, lbytes, s>>>(tmx, w_t, b_r, la);
-    return cudaGetLastError();
+    return launch_pdl(k_logits_large<XT>, dim3((c.N + 31) / 32, (c.T + 15) / 16), dim3(544), lbytes, s, tmx, w_t,
+                      b_r, la);
 }
 
 template <typename XT>
@@ -902,15 +907,14 @@ cudaError_t launch_large(const moe_config &c, const XT *x, const float *w_t, con
     const size_t gbytes = ((size_t)64 * c.N + 64 * 8) * sizeof(float);
     e = cudaFuncSetAttribute(k_gate, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gbytes);
     if (e != cudaSuccess) return e;
-    k_gate<<<ra.tiles, 256, gbytes, s>>>(logits, ra);
-    return cudaGetLastError();
+    return launch_pdl(k_gate, dim3(ra.tiles), dim3(256), gbytes, s, logits, ra);
 }
 
 template <typename XT>
 cudaError_t launch_logits_gate(const moe_config &c, const XT *x, const float *w_r, const float *b_r, RouterArgs ra,
                                float *logits, float *w_t, cudaStream_t s) {
-    k_transpose_wr<<<dim3((c.d + 31) / 32, (c.N + 31) / 32), 256, 0, s>>>(w_r, w_t, c.d, c.N);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(k_transpose_wr, dim3((c.d + 31) / 32, (c.N + 31) / 32), dim3(256), 0, s, w_r, w_t, c.d,
+                               c.N);
     if (e != cudaSuccess) return e;
     if (c.N <= 4) return launch_small<XT, 4>(c, x, w_t, b_r, ra, s);
     if (c.N <= 8) return launch_small<XT, 8>(c, x, w_t, b_r, ra, s);
@@ -926,8 +930,8 @@ cudaError_t launch_router_logits(const moe_config &c, const void *x, const float
     const WsLayout L = ws_layout(c);
     uint32_t *err = reinterpret_cast<uint32_t *>(ws + L.err);
     float *w_t = reinterpret_cast<float *>(ws + L.w_t);
-    k_transpose_wr<<<dim3((c.d + 31) / 32, (c.N + 31) / 32), 256, 0, s>>>(w_r, w_t, c.d, c.N);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(k_transpose_wr, dim3((c.d + 31) / 32, (c.N + 31) / 32), dim3(256), 0, s, w_r, w_t, c.d,
+                               c.N);
     if (e != cudaSuccess) return e;
     const int hb = c.has_router_bias && b_r ? 1 : 0;
     if (c.dtype == MOE_BF16)
@@ -958,8 +962,7 @@ cudaError_t launch_router_stats(const moe_config &c, const void *x, const float 
     sa.stats_only = 1;
     sa.slot_counts = slot_counts;
     sa.prob_sums = prob_sums;
-    k_expert_scan<<<c.N, 256, 0, s>>>(sa);
-    return cudaGetLastError();
+    return launch_pdl(k_expert_scan, dim3(c.N), dim3(256), 0, s, sa);
 }
 
 cudaError_t launch_router_assign(const moe_config &c, const int32_t *topk_idx, const int32_t *slot_base, int32_t cap,
@@ -978,8 +981,7 @@ cudaError_t launch_router_assign(const moe_config &c, const int32_t *topk_idx, c
     int32_t *kept = counts_kept ? counts_kept : reinterpret_cast<int32_t *>(ws + L.kept);
     ScanArgs sa{c.T, c.N, c.k, tiles, cap, cnt, pre, kpre, psum, pmean, routed, kept};
     sa.slot_base = slot_base;
-    k_expert_scan<<<c.N, 256, 0, s>>>(sa);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(k_expert_scan, dim3(c.N), dim3(256), 0, s, sa);
     if (e != cudaSuccess) return e;
     const int TT = router_tile_tokens(c);
     AssignArgs aa{c.T, c.N, c.k, tiles, TT, cap, max_rows(c), topk_idx, pre, kpre, routed, kept,
@@ -988,8 +990,7 @@ cudaError_t launch_router_assign(const moe_config &c, const int32_t *topk_idx, c
     aa.g_psum = g_psum;
     aa.g_T = g_T;
     const size_t sbytes = (size_t)(c.N + 1 + 2 * TT * 8) * sizeof(int);
-    k_assign<<<tiles, 256, sbytes, s>>>(aa);
-    return cudaGetLastError();
+    return launch_pdl(k_assign, dim3(tiles), dim3(256), sbytes, s, aa);
 }
 
 cudaError_t launch_router(const moe_config &c, const void *x, const float *w_r, const float *b_r,
@@ -1019,15 +1020,13 @@ cudaError_t launch_router(const moe_config &c, const void *x, const float *w_r, 
 
     const int cap = capacity_of(c);
     ScanArgs sa{c.T, c.N, c.k, tiles, cap, cnt, pre, kpre, psum, pmean, routed, kept};
-    k_expert_scan<<<c.N, 256, 0, s>>>(sa);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_pdl(k_expert_scan, dim3(c.N), dim3(256), 0, s, sa)) != cudaSuccess) return e;
 
     const int TT = router_tile_tokens(c);
     AssignArgs aa{c.T, c.N, c.k, tiles, TT, cap, max_rows(c), o.topk_idx, pre, kpre, routed, kept,
                   pmean, o.expert_offsets, o.slot_row, o.perm_token, o.aux, err, zpart, o.z_loss};
     const size_t sbytes = (size_t)(c.N + 1 + 2 * TT * 8) * sizeof(int);
-    k_assign<<<tiles, 256, sbytes, s>>>(aa);
-    return cudaGetLastError();
+    return launch_pdl(k_assign, dim3(tiles), dim3(256), sbytes, s, aa);
 }
 
 }  // namespace moe
