@@ -131,8 +131,9 @@ def captured_traffic(workload: str, stage: str):
                 h.update(f.read())
         if h.hexdigest() != rec["sources_sha256"]:
             return None
-        k = rec["workloads"][workload][stage]
-        return int(k["dram_read"]) + int(k["dram_write"])
+        ks = rec["workloads"][workload][stage]
+        ks = ks if isinstance(ks, list) else [ks]  # a stage can be two launches (tail split)
+        return sum(int(k["dram_read"]) + int(k["dram_write"]) for k in ks)
     except (OSError, KeyError, ValueError):
         return None
 
@@ -143,13 +144,25 @@ def launches_per_forward(w) -> int:
     expert scan, slot assignment. Expert Choice: weight re-layout, logits, scores,
     per-expert selection, per-token list scan and fill, per-expert counts. Then
     dispatch, expert product 1 (two launches for ReLU experts with a shared expert),
-    expert product 2 and the combine."""
+    expert product 2 and the combine. With bf16 experts receiving 224 to 511 rows on
+    average (the row buffers' size over N) each product is two launches: the CTA-pair
+    kernel and a single-CTA kernel for the short last row blocks."""
     if w.routing == "expert_choice":
         router = 7
     else:
         router = 1 + (2 if w.N > 32 else 1) + 2
     p1 = 2 if (w.act == "relu" and w.h_shared) else 1
-    return router + 1 + p1 + 1 + 1
+    p2 = 1
+    if w.dtype == "bf16":
+        if w.routing == "expert_choice":
+            rows = w.N * min(-(-w.T * w.capacity_factor[0] // (w.N * w.capacity_factor[1])), w.T)
+        elif w.capacity_factor:
+            rows = min(w.T * w.k, w.N * -(-w.T * w.capacity_factor[0] // (w.N * w.capacity_factor[1])))
+        else:
+            rows = w.T * w.k
+        if 224 * w.N <= rows < 512 * w.N:
+            p1, p2 = p1 + 1, p2 + 1
+    return router + 1 + p1 + p2 + 1
 
 
 def _peaks():
