@@ -63,21 +63,18 @@ struct TcParams {
     int n_out, K, n_out_sh, K_sh;
     __nv_bfloat16 *C, *C_sh;
     uint32_t *err;
-    // Which rows of each routed segment this launch covers: all of them (0); all but
-    // a last partial 256-row block of at most 128 rows (1: the pair kernel); only that
-    // short last block (2: the single-CTA kernel, which covers it in one 128-row tile).
+    // Which routed segments this launch covers: all (0); those whose last 256-row
+    // block holds more than 128 rows or is full (1: the pair kernel); those whose
+    // last 256-row block holds 1 to 128 rows, whole (2: the single-CTA kernel, in
+    // 128-row tiles).
     int tail_mode;
 };
 
-// Rows [r0, r0 + rows) of a routed segment restricted to a launch's tail mode.
-__device__ __forceinline__ void apply_tail_mode(int mode, int &r0, int &rows) {
+// The rows of a routed segment a launch covers under its tail mode (all or none).
+__device__ __forceinline__ void apply_tail_mode(int mode, int &rows) {
     const int tail = rows & 255;
     const bool short_tail = tail > 0 && tail <= 128;
-    if (mode == 1 && short_tail) rows -= tail;
-    if (mode == 2) {
-        r0 += rows - (short_tail ? tail : 0);
-        rows = short_tail ? tail : 0;
-    }
+    if ((mode == 1 && short_tail) || (mode == 2 && !short_tail)) rows = 0;
 }
 
 struct Smem {
@@ -221,7 +218,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_ffn_tc(const __grid_constant
                 if (g < p.n_seg) {
                     r0 = min(max(p.offsets[g], 0), p.a_rows);
                     rows = min(max(p.offsets[g + 1], r0), p.a_rows) - r0;
-                    apply_tail_mode(p.tail_mode, r0, rows);
+                    apply_tail_mode(p.tail_mode, rows);
                     nt = nt_routed;
                 } else {
                     r0 = 0;
@@ -464,7 +461,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 if (g < p.n_seg) {
                     r0 = min(max(p.offsets[g], 0), p.a_rows);
                     rows = min(max(p.offsets[g + 1], r0), p.a_rows) - r0;
-                    apply_tail_mode(p.tail_mode, r0, rows);
+                    apply_tail_mode(p.tail_mode, rows);
                     nt = nt_routed;
                 } else {
                     r0 = 0;
@@ -740,11 +737,10 @@ cudaError_t product(const int32_t *offsets, int n_seg, int64_t a_rows, const voi
     if (max_tiles == 0) return cudaSuccess;
     if (!pair) return launch_kind<KIND>(p, max_tiles, s);
     // With few rows per expert (under 512 on average) a short last block is a large
-    // share of the work: the pair kernel then takes every segment's full 256-row blocks
-    // (and last blocks of more than 128 rows) and the single-CTA kernel the short last
-    // blocks, whose 128-row tiles waste less than a mostly empty pair tile. Measured
-    // A/B on B300: DeepSeek-shaped layer (256 rows per expert) 8.94 vs 9.19 ms; with
-    // 1024 rows per expert (Mixtral-shaped) the split cost 3 %.
+    // share of the work: an expert whose last 256-row block holds at most 128 rows then
+    // runs whole on the single-CTA kernel (its 128-row tiles cost half a pair tile), the
+    // others on the pair kernel, so that no expert's weights are streamed by both
+    // launches. With 1024 rows per expert (Mixtral-shaped) a split cost 3 %.
     const bool split = n_seg > 0 && a_rows < 512LL * n_seg;
     p.tail_mode = split ? 1 : 0;
     cudaError_t e = launch_kind2<KIND>(p, max_tiles, s);
@@ -753,7 +749,7 @@ cudaError_t product(const int32_t *offsets, int n_seg, int64_t a_rows, const voi
     q.tail_mode = 2;
     q.sh_rows = 0;
     if (!kGatedLayout<KIND> && !encode_bf16_3d(&q.tmB0, b0, K, n_out, n_seg, 256)) return cudaErrorInvalidValue;
-    return launch_kind<KIND>(q, (int64_t)n_seg * ((n_out + BN_OUT - 1) / BN_OUT), s);
+    return launch_kind<KIND>(q, ((a_rows + BM - 1) / BM + n_seg) * ((n_out + BN_OUT - 1) / BN_OUT), s);
 }
 
 }  // namespace

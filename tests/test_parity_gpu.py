@@ -35,6 +35,9 @@ SMALL = [
     _small("mixtral_prefill", T=300, d=256, h=384),
     _small("mixtral_prefill", T=1, d=128, h=128),
     _small("mixtral_prefill", T=129, d=192, h=320, N=3, k=3),
+    # 256 rows per expert on average: pair kernel for some experts, single-CTA for the
+    # experts whose last 256-row block holds at most 128 rows
+    _small("mixtral_prefill", T=1024, d=256, h=256),
     _small("deepseek_fine", T=200, d=256, N=16, k=4, h=128, h_shared=128),
     _small("deepseek_fine", T=130, d=128, N=256, k=8, h=128, h_shared=192),
     _small("deepseek_fine", T=96, d=128, N=100, k=6, h=192, h_shared=0,
