@@ -480,27 +480,34 @@ def run_ours(a, w, world, rank, local):
     counts_kept = kept.cpu().tolist()
     rows = int(sum(counts_kept))
 
-    # ---- the forward captured once as a CUDA graph (moe_forward_graph_create); the
-    # timed steps launch it. Stage times come from a second pass over graphs that
-    # also record six events at the stage boundaries (one graph per step, so that
-    # every step's events can be read afterwards); an event between two kernels
-    # orders them fully, so that pass shows each stage alone, without the
-    # programmatic-launch overlap of neighbouring kernels that the timed graph has.
+    # ---- the forward captured once as a CUDA graph (moe_forward_graph_create); each
+    # timed step launches it. Stage times come from graphs that also record six events
+    # at the stage boundaries, one per step, launched between the timed steps so that
+    # both run under the same clocks and power state (an event between two kernels
+    # orders them fully, so those launches show each stage alone, without the
+    # programmatic-launch overlap of neighbouring kernels that the timed graph has).
     def make_graph(events=None, x=None, y_out=None):
         return moe.moe_forward_graph_create(cfg, inp["x"] if x is None else x, inp["w_r"], inp["b_r"], inp["w_gate"],
                                             inp["w_up"], inp["w_down"], inp["shared_w_gate"], inp["shared_w_up"],
                                             inp["shared_w_down"], y if y_out is None else y_out, idx, gate, routed,
                                             kept, aux, ws, events=events)
 
-    graph, graph_note = None, None
+    graph, pgs, graph_note = None, [], None
     try:
         graph = make_graph()
+        for _ in range(a.steps):
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+            for ev in evs:
+                ev.record(stream)
+            pgs.append((make_graph(events=evs), evs))
         for _ in range(max(3, a.warmup)):
             graph.launch(stream)
+        for g_, _ in pgs[:3]:
+            g_.launch(stream)
         torch.cuda.synchronize(dev)
     except (RuntimeError, moe.MoeError) as exc:
         graph_note = f"stream launches of moe_forward (graph capture failed: {exc})"
-        graph = None
+        graph, pgs = None, []
 
     # ---- timed region: K forwards, per-step CUDA events on the launching stream
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps)]
@@ -518,6 +525,10 @@ def run_ours(a, w, world, rank, local):
         else:
             fwd()
         ends[i].record(stream)
+        if pgs:
+            if flush is not None:
+                flush.zero_()
+            pgs[i][0].launch(stream)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
     _barrier(world)
@@ -528,43 +539,16 @@ def run_ours(a, w, world, rank, local):
     st = moe.moe_check_error(ws, stream)
     if st != moe.MOE_OK:
         raise RuntimeError("device error word: " + moe.status_str(st))
-
-    # ---- the same forwards as plain stream launches (moe_forward per step), for comparison
-    for i in range(a.steps):
-        if flush is not None:
-            flush.zero_()
-        starts[i].record(stream)
-        fwd()
-        ends[i].record(stream)
-    torch.cuda.synchronize(dev)
-    stream_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / a.steps
-
-    # ---- per-stage durations: one pass of K graphs with stage events, after warm-up
-    nprof = a.steps
-    stage_ms = None
-    if graph is not None:
-        try:
-            pgs = []
-            for _ in range(nprof):
-                evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
-                for ev in evs:
-                    ev.record(stream)
-                pgs.append((make_graph(events=evs), evs))
-            for g_, _ in pgs:
-                if flush is not None:
-                    flush.zero_()
-                g_.launch(stream)
-            torch.cuda.synchronize(dev)
-            stage_ms = [sum(e_[j].elapsed_time(e_[j + 1]) for _, e_ in pgs) / nprof for j in range(5)]
-            for g_, _ in pgs:
-                g_.destroy()
-        except (RuntimeError, moe.MoeError):
-            stage_ms = None
-    if stage_ms is None:
+    if pgs:
+        stage_ms = [sum(e_[j].elapsed_time(e_[j + 1]) for _, e_ in pgs) / len(pgs) for j in range(5)]
+        for g_, _ in pgs:
+            g_.destroy()
+    else:
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
         for ev in evs:
             ev.record(stream)
         stage_ms = [0.0] * 5
+        nprof = max(10, a.steps // 2)
         for i in range(nprof):
             if flush is not None:
                 flush.zero_()
@@ -575,9 +559,18 @@ def run_ours(a, w, world, rank, local):
             evs[-1].synchronize()
             for j in range(5):
                 stage_ms[j] += evs[j].elapsed_time(evs[j + 1]) / nprof
-    if graph is not None:
-        graph.destroy()
+
+    # ---- the same forwards as plain stream launches (moe_forward per step), for comparison
+    for i in range(a.steps):
+        if flush is not None:
+            flush.zero_()
+        starts[i].record(stream)
+        fwd()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    stream_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / a.steps
     use_graph = graph is not None
+    e2e_graph_src = graph
 
     # ---- end to end: every step copies its x from pinned host memory, runs the
     # forward and copies its y back; the copies of neighbouring steps overlap the
@@ -629,6 +622,8 @@ def run_ours(a, w, world, rank, local):
         raise RuntimeError("device error word: " + moe.status_str(st))
     for g_ in e2e_graphs:
         g_.destroy()
+    if e2e_graph_src is not None:
+        e2e_graph_src.destroy()
 
     # ---- roofline of the dominant kernel
     alg = algorithmic(w, rows, counts_kept)
@@ -682,7 +677,8 @@ def run_ours(a, w, world, rank, local):
                    "global_batch_tokens": world * T, "parallelism": f"replicas x{world}",
                    "l2": l2_mode,
                    "launch": graph_note or "the forward as one CUDA graph per step (moe_forward_graph_launch); "
-                                           "stage times from a pass of graphs with stage events"},
+                                           "stage times from graphs with stage events launched between "
+                                           "the timed steps"},
         "roofline": roof,
         "layer_roofline": {"roofline_ms": layer_roof_ms, "frac": layer_roof_ms / ms_max,
                            "algorithmic_flops": alg["flops"], "algorithmic_bytes": alg["bytes"],

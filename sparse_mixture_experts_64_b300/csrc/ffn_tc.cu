@@ -77,6 +77,7 @@ __device__ __forceinline__ void apply_tail_mode(int mode, int &rows) {
     if ((mode == 1 && short_tail) || (mode == 2 && !short_tail)) rows = 0;
 }
 
+
 struct Smem {
     uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], drain;
     uint32_t tmem_base;
@@ -122,14 +123,20 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16 *dst, const uint32_t
     for (int q = 0; q < 4; ++q) d4[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
 }
 
-template <int KIND>
+// Gated layouts: SPLIT64 = false (single-CTA kernel): accumulator columns 0-127 gate,
+// 128-255 up of the tile's 128 hidden units; SPLIT64 = true (pair kernel): columns
+// 0-63 gate and 64-127 up of hidden units 0-63, 128-191 gate and 192-255 up of 64-127.
+template <bool SPLIT64> __device__ __forceinline__ int gate_col(int c) { return SPLIT64 ? (c >> 6) * 128 + (c & 63) : c; }
+template <bool SPLIT64> __device__ __forceinline__ int up_col(int c) { return gate_col<SPLIT64>(c) + (SPLIT64 ? 64 : 128); }
+
+template <int KIND, bool SPLIT64 = false>
 __device__ __forceinline__ void epilogue_row(uint32_t tbase, __nv_bfloat16 *crow, int col0, int n_out, bool row_ok) {
     if constexpr (KIND == KIND_PREACT) {
 #pragma unroll 1
         for (int c = 0; c < 128; c += 32) {
             uint32_t g[32], u[32];
-            tmem_ld32(tbase + c, g);
-            tmem_ld32(tbase + 128 + c, u);
+            tmem_ld32(tbase + gate_col<SPLIT64>(c), g);
+            tmem_ld32(tbase + up_col<SPLIT64>(c), u);
             tmem_ld_wait();
             const int col = col0 + c;
             if (row_ok && col < n_out) {
@@ -141,8 +148,8 @@ __device__ __forceinline__ void epilogue_row(uint32_t tbase, __nv_bfloat16 *crow
 #pragma unroll 1
         for (int c = 0; c < 128; c += 32) {
             uint32_t g[32], u[32];
-            tmem_ld32(tbase + c, g);
-            tmem_ld32(tbase + 128 + c, u);
+            tmem_ld32(tbase + gate_col<SPLIT64>(c), g);
+            tmem_ld32(tbase + up_col<SPLIT64>(c), u);
             tmem_ld_wait();
             const int col = col0 + c;
             if (row_ok && col < n_out) {
@@ -404,20 +411,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_ffn_tc(const __grid_constant
 //
 // Same computation with 2-CTA (cta_group::2) MMAs: a cluster of two CTAs on two
 // SMs computes a 256 x 256 tile per MMA 256x256x16. Each CTA stages its own 128
-// rows of A and 128 of the 256 B rows (gated: gate rows in the even CTA, up rows in
-// the odd CTA), so each SM moves a third less operand data per FLOP than the
-// single-CTA kernel and six 32 KB stages fit in shared memory. Both CTAs' loads
-// complete on the even CTA's stage barrier, and the even CTA issues the MMAs;
-// each CTA's TMEM holds its own 128 accumulator rows and its epilogue stores them.
-// Commits arrive on both CTAs' barriers (multicast). Tiles cover 256 rows of one
-// segment, so this kernel is chosen when experts receive many rows.
+// rows of A and 128 of the 256 B rows, so each SM moves a third less operand data
+// per FLOP than the single-CTA kernel. Gated experts: CTA r stages the gate rows and
+// then the up rows of hidden units 64r .. 64r+63 of the tile's 128, so accumulator
+// columns 0-63 / 64-127 are gate / up of units 0-63 and 128-191 / 192-255 those of
+// 64-127. Both CTAs' loads complete on the even CTA's stage barrier, the even CTA
+// issues the MMAs and its commits arrive on both CTAs' barriers (multicast); each
+// CTA's TMEM holds its own 128 accumulator rows and its epilogue stores them.
+//
+// Last blocks. A segment of r = 256 q + t rows has q full 256-row blocks and t rows
+// left. With 0 < t < 256 those t rows are not a partly empty 256-row tile but a tile
+// with the weights on the MMA's M side and the tokens on its N side,
+//   D[256 weight rows][t' tokens] = W[256][64] · X_tail[t'][64]ᵀ,  t' = t rounded up to 32,
+// whose MMAs cost t'/256 of a row tile's; the tokens are staged where a row tile's
+// token rows go (t'/2 per CTA) and the weights as for a row tile, so the tile follows
+// the segment's full blocks in the tile order and finds their weights in L2. Its
+// epilogue turns the transposed result (one lane per weight row, one column per token)
+// back into rows (gated: the up lanes hand their values to the gate lanes of the same
+// units through shared memory, bounded mbarrier handshakes).
 constexpr int STAGES2 = 6;
 constexpr uint32_t HALF_BYTES = 128 * BK * 2;            // 16 KB: 128 rows x 64 bf16
 constexpr uint32_t STAGE2_BYTES = 2 * HALF_BYTES;
-constexpr size_t SMEM2_BYTES = (size_t)STAGES2 * STAGE2_BYTES + 1024;
+constexpr int XSTRIDE2 = 33;                              // exchange buffer row stride (fp32)
+constexpr uint32_t XBUF2_BYTES = 32 * XSTRIDE2 * 4;       // one warp's 32 lanes x 32 tokens
+constexpr size_t SMEM2_BYTES = 1024 + (size_t)STAGES2 * STAGE2_BYTES + 2 * XBUF2_BYTES;
+
+enum { TILE_ROW = 0, TILE_TAIL = 1 };
 
 struct Smem2 {
     uint64_t full[STAGES2], empty[STAGES2], tfull[2], tempty[2], drain;
+    uint64_t xfull[2], xempty[2];  // gated tail exchange, per (gate warp, up warp) pair
     uint32_t tmem_base;
     int abort_flag;
     int base[MAX_SEG + 1];
@@ -425,18 +448,117 @@ struct Smem2 {
     int row0[MAX_SEG];
     int rows[MAX_SEG];
 };
+static_assert(SMEM2_BYTES + sizeof(Smem2) <= 232448, "shared memory budget of one CTA");
 
-template <int KIND, int NACC>
+struct Tile2 {
+    int seg, m, n;
+    int type;   // TILE_ROW: rows [256 m, 256 m + 256); TILE_TAIL: rows [256 q, 256 q + tail)
+    int tail;   // tail rows (TILE_TAIL)
+    int tpad;   // tail rounded up to 32: the tail MMA's N
+};
+
+// Tiles per n-tile of a segment of `rows` rows: its full blocks and a tail tile.
+__device__ __forceinline__ int pair_tiles(int rows) { return (rows >> 8) + ((rows & 255) ? 1 : 0); }
+
+__device__ __forceinline__ Tile2 decode_tile2(const Smem2 &s, int nseg, int tile) {
+    const TileInfo ti = decode_tile(s, nseg, tile);
+    Tile2 t2;
+    t2.seg = ti.seg;
+    t2.m = ti.m;
+    t2.n = ti.n;
+    const int rows = s.rows[ti.seg];
+    t2.type = ti.m == (rows >> 8) ? TILE_TAIL : TILE_ROW;
+    t2.tail = t2.type == TILE_TAIL ? rows & 255 : 0;
+    t2.tpad = (t2.tail + 31) & ~31;
+    return t2;
+}
+
+// Tail epilogue of one warp (TMEM lane quarter q of CTA `rank`): the accumulator holds
+// one weight row per lane and one tail token per column (tokens [0, tpad)).
+template <int KIND>
+__device__ __forceinline__ bool epilogue_tail(Smem2 &s, uint8_t *xbufs, uint32_t tbase, const Tile2 &t,
+                                              int64_t row_tail0, __nv_bfloat16 *out, int n_out, uint32_t rank,
+                                              int q, int lane, uint32_t &xcount, volatile int *abort_flag,
+                                              uint32_t *err) {
+    const int nchunks = t.tpad >> 5;
+    if constexpr (KIND == KIND_GATED || KIND == KIND_PREACT) {
+        // lanes of quarters 0-1: gate rows, 2-3: up rows of hidden units 64 rank + 32 (q & 1) + lane
+        const bool is_gate = q < 2;
+        const int pidx = q & 1;
+        const int hcol = t.n * 128 + (int)rank * 64 + pidx * 32 + lane;
+        const bool col_ok = hcol < n_out;
+        float *xb = reinterpret_cast<float *>(xbufs + (size_t)pidx * XBUF2_BYTES);
+#pragma unroll 1
+        for (int c = 0; c < nchunks; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tbase + (uint32_t)(c * 32), v);
+            tmem_ld_wait();
+            if constexpr (KIND == KIND_PREACT) {
+                // raw pre-activations: gate in columns [0, n_out), up in [n_out, 2 n_out)
+                const int col = hcol + (is_gate ? 0 : n_out);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int j = c * 32 + i;
+                    if (col_ok && j < t.tail)
+                        out[(row_tail0 + j) * (2 * (int64_t)n_out) + col] = __float2bfloat16_rn(__uint_as_float(v[i]));
+                }
+            } else {
+                const uint32_t ph = xcount & 1u;
+                ++xcount;
+                if (!is_gate) {
+                    // up warp: hand this chunk's values to the gate warp of the same units
+                    if (!wait_bar(&s.xempty[pidx], ph ^ 1u, abort_flag, err)) return false;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) xb[lane * XSTRIDE2 + i] = __uint_as_float(v[i]);
+                    mbar_arrive(&s.xfull[pidx]);
+                } else {
+                    if (!wait_bar(&s.xfull[pidx], ph, abort_flag, err)) return false;
+                    float u[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) u[i] = xb[lane * XSTRIDE2 + i];
+                    mbar_arrive(&s.xempty[pidx]);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int j = c * 32 + i;
+                        if (col_ok && j < t.tail)
+                            out[(row_tail0 + j) * (int64_t)n_out + hcol] =
+                                __float2bfloat16_rn(silu_f32(__uint_as_float(v[i])) * u[i]);
+                    }
+                }
+            }
+        }
+    } else {
+        // one output column per lane: 256 n + 128 rank + 32 q + lane
+        const int ocol = t.n * 256 + (int)rank * 128 + q * 32 + lane;
+        const bool col_ok = ocol < n_out;
+#pragma unroll 1
+        for (int c = 0; c < nchunks; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tbase + (uint32_t)(c * 32), v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int j = c * 32 + i;
+                float x = __uint_as_float(v[i]);
+                if (KIND == KIND_RELU) x = fmaxf(x, 0.0f);
+                if (col_ok && j < t.tail) out[(row_tail0 + j) * (int64_t)n_out + ocol] = __float2bfloat16_rn(x);
+            }
+        }
+    }
+    return true;
+}
+
+template <int KIND>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     k_ffn_tc2(const __grid_constant__ TcParams p) {
     constexpr int BN_OUT = kGatedLayout<KIND> ? 128 : 256;
-    constexpr uint32_t TMEM_COLS2 = NACC * ACC_COLS;
     __shared__ Smem2 s;
     extern __shared__ uint8_t dyn_smem[];
     const uint32_t dyn_base = smem_u32(dyn_smem);
     uint8_t *tiles = dyn_smem + (((dyn_base + 1023u) & ~1023u) - dyn_base);
     auto smA = [&](int st) { return tiles + (size_t)st * STAGE2_BYTES; };
     auto smB = [&](int st) { return tiles + (size_t)st * STAGE2_BYTES + HALF_BYTES; };
+    uint8_t *xbufs = tiles + (size_t)STAGES2 * STAGE2_BYTES;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_ctarank();
@@ -446,7 +568,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const int nt_routed = (p.n_out + BN_OUT - 1) / BN_OUT;
     const int nt_sh = (p.n_out_sh + BN_OUT - 1) / BN_OUT;
 
-    // ---- tile table (pair tiles of 256 rows) and barriers ----
+    // ---- tile table and barriers ----
     if (warp == 0) {
         pdl_wait();  // the offsets come from the router
         constexpr int PER = (MAX_SEG + 31) / 32;
@@ -469,7 +591,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                     nt = nt_sh;
                 }
                 rows = max(rows, 0);
-                const int mt = (rows + 2 * BM - 1) / (2 * BM);
+                const int mt = pair_tiles(rows);
                 s.mt[g] = max(mt, 1);
                 s.row0[g] = r0;
                 s.rows[g] = rows;
@@ -500,6 +622,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             for (int i = 0; i < 2; ++i) {
                 mbar_init(&s.tfull[i], 1);
                 mbar_init(&s.tempty[i], 8);  // 4 epilogue warps of each CTA
+                mbar_init(&s.xfull[i], 32);  // the 32 lanes of an up warp
+                mbar_init(&s.xempty[i], 32); // the 32 lanes of a gate warp
             }
             mbar_init(&s.drain, 1);
             s.abort_flag = 0;
@@ -507,7 +631,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         }
     }
     if (warp == 1) {
-        tmem_alloc_pair(&s.tmem_base, TMEM_COLS2);
+        tmem_alloc_pair(&s.tmem_base, 2 * ACC_COLS);
         tmem_relinquish_pair();
     }
     tc_fence_before();
@@ -541,10 +665,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             uint32_t issued_mask = 0, issued_par = 0;
             const uint32_t lead_full = map_to_rank(smem_u32(&s.full[0]), 0);
             for (int tile = cluster; tile < total && ok; tile += nclusters) {
-                const TileInfo ti = decode_tile(s, nseg, tile);
-                const bool sh = ti.seg >= p.n_seg;
+                const Tile2 t = decode_tile2(s, nseg, tile);
+                const bool sh = t.seg >= p.n_seg;
                 const int K = sh ? p.K_sh : p.K;
-                const int arow = s.row0[ti.seg] + ti.m * 2 * BM + (int)rank * BM;
+                // token rows of this CTA: 128 of a row tile, or t'/2 of the tail (the box
+                // loads 128; the MMA reads the first t'/2)
+                const int arow = s.row0[t.seg] + t.m * 2 * BM +
+                                 (int)rank * (t.type == TILE_TAIL ? (t.tpad >> 1) : BM);
                 const CUtensorMap *ta = sh ? &p.tmA_sh : &p.tmA;
                 for (int kb = 0; kb < K / BK; ++kb) {
                     if (!wait_bar(&s.empty[st], ph ^ 1, abort_flag, p.err)) {
@@ -556,13 +683,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                     const int kc = kb * BK;
                     tma_load_2d_pair(smA(st), ta, kc, arow, fb);
                     if (kGatedLayout<KIND>) {
-                        // even CTA: gate rows, odd CTA: up rows -> accumulator columns 0-127 / 128-255
-                        if (sh) tma_load_2d_pair(smB(st), rank == 0 ? &p.tmB0_sh : &p.tmB1_sh, kc, ti.n * 128, fb);
-                        else tma_load_3d_pair(smB(st), rank == 0 ? &p.tmB0 : &p.tmB1, kc, ti.n * 128, ti.seg, fb);
+                        // gate rows then up rows of hidden units 128 n + 64 rank .. + 63
+                        const int wrow = t.n * 128 + (int)rank * 64;
+                        if (sh) {
+                            tma_load_2d_pair(smB(st), &p.tmB0_sh, kc, wrow, fb);
+                            tma_load_2d_pair(smB(st) + HALF_BYTES / 2, &p.tmB1_sh, kc, wrow, fb);
+                        } else {
+                            tma_load_3d_pair(smB(st), &p.tmB0, kc, wrow, t.seg, fb);
+                            tma_load_3d_pair(smB(st) + HALF_BYTES / 2, &p.tmB1, kc, wrow, t.seg, fb);
+                        }
                     } else {
-                        const int brow = ti.n * 256 + (int)rank * 128;
+                        const int brow = t.n * 256 + (int)rank * 128;
                         if (sh) tma_load_2d_pair(smB(st), &p.tmB0_sh, kc, brow, fb);
-                        else tma_load_3d_pair(smB(st), &p.tmB0, kc, brow, ti.seg, fb);
+                        else tma_load_3d_pair(smB(st), &p.tmB0, kc, brow, t.seg, fb);
                     }
                     issued_mask |= 1u << st;
                     issued_par = (issued_par & ~(1u << st)) | (ph << st);
@@ -578,76 +711,82 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                     if (issued_mask & (1u << i)) drain_bar(&s.full[i], (issued_par >> i) & 1u);
         }
     } else if (warp == 1) {
-        if (lane == 0 && run) {
+        if (lane == 0 && run && leader) {
+            // ================= MMA issuer (even CTA) =================
+            constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, BN_MMA);
             int st = 0, acc = 0;
             uint32_t ph = 0, aph = 0;
             bool ok = true;
-            if (leader) {
-                // ================= MMA issuer (even CTA) =================
-                constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, BN_MMA);
-                for (int tile = cluster; tile < total && ok; tile += nclusters) {
-                    const TileInfo ti = decode_tile(s, nseg, tile);
-                    const int K = ti.seg >= p.n_seg ? p.K_sh : p.K;
-                    if (!wait_bar(&s.tempty[acc], aph ^ 1, abort_flag, p.err)) {
+            for (int tile = cluster; tile < total && ok; tile += nclusters) {
+                const Tile2 t = decode_tile2(s, nseg, tile);
+                const int K = t.seg >= p.n_seg ? p.K_sh : p.K;
+                const bool tail = t.type == TILE_TAIL;
+                // a tail tile: the weights (B stage) as the M side, the tokens as N
+                const uint32_t idesc = tail ? idesc_bf16_f32(2 * BM, t.tpad) : IDESC;
+                if (!wait_bar(&s.tempty[acc], aph ^ 1, abort_flag, p.err)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * ACC_COLS);
+                for (int kb = 0; kb < K / BK; ++kb) {
+                    if (!wait_bar(&s.full[st], ph, abort_flag, p.err)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + (uint32_t)(acc * ACC_COLS);
-                    for (int kb = 0; kb < K / BK; ++kb) {
-                        if (!wait_bar(&s.full[st], ph, abort_flag, p.err)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint64_t ad = desc_sw128(smem_u32(smA(st)));
-                        const uint64_t bd = desc_sw128(smem_u32(smB(st)));
+                    const uint64_t ad = desc_sw128(smem_u32(smA(st)));
+                    const uint64_t bd = desc_sw128(smem_u32(smB(st)));
+                    const uint64_t m_side = tail ? bd : ad, n_side = tail ? ad : bd;
 #pragma unroll
-                        for (int kk = 0; kk < BK / 16; ++kk)
-                            umma_bf16_pair(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), IDESC,
-                                           (kb | kk) != 0 ? 1u : 0u);
-                        umma_commit_pair_mc(&s.empty[st], 0x3);
-                        if (++st == STAGES2) {
-                            st = 0;
-                            ph ^= 1;
-                        }
-                    }
-                    if (!ok) break;
-                    umma_commit_pair_mc(&s.tfull[acc], 0x3);
-                    if (++acc == NACC) {
-                        acc = 0;
-                        aph ^= 1;
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        umma_bf16_pair(d_tmem, m_side + (uint64_t)(2 * kk), n_side + (uint64_t)(2 * kk), idesc,
+                                       (kb | kk) != 0 ? 1u : 0u);
+                    umma_commit_pair_mc(&s.empty[st], 0x3);
+                    if (++st == STAGES2) {
+                        st = 0;
+                        ph ^= 1;
                     }
                 }
-                umma_commit_pair_mc(&s.drain, 0x1);
-                drain_bar(&s.drain, 0);
+                if (!ok) break;
+                umma_commit_pair_mc(&s.tfull[acc], 0x3);
+                if (++acc == 2) {
+                    acc = 0;
+                    aph ^= 1;
+                }
             }
+            umma_commit_pair_mc(&s.drain, 0x1);
+            drain_bar(&s.drain, 0);
         }
     } else if (run) {
         // ================= epilogue (warps 2..5 of both CTAs) =================
         const int quarter = warp & 3;
         const int r_in_tile = quarter * 32 + lane;
         int acc = 0;
-        uint32_t aph = 0;
+        uint32_t aph = 0, xcount = 0;
         for (int tile = cluster; tile < total; tile += nclusters) {
-            const TileInfo ti = decode_tile(s, nseg, tile);
-            const bool sh = ti.seg >= p.n_seg;
+            const Tile2 t = decode_tile2(s, nseg, tile);
+            const bool sh = t.seg >= p.n_seg;
+            const int n_out = sh ? p.n_out_sh : p.n_out;
+            __nv_bfloat16 *C = sh ? p.C_sh : p.C;
             if (!wait_bar(&s.tfull[acc], aph, abort_flag, p.err)) break;
             tc_fence_after();
-            const int r_seg = ti.m * 2 * BM + (int)rank * BM + r_in_tile;  // row within the segment
-            const bool row_ok = r_seg < s.rows[ti.seg];
-            const int64_t orow = (int64_t)s.row0[ti.seg] + r_seg;
-            const int n_out = sh ? p.n_out_sh : p.n_out;
-            __nv_bfloat16 *crow = (sh ? p.C_sh : p.C) + orow * n_out * kOutLd<KIND>;
             const uint32_t tbase = tmem_base + (uint32_t)(acc * ACC_COLS) + ((uint32_t)(quarter * 32) << 16);
-            epilogue_row<KIND>(tbase, crow, ti.n * BN_OUT, n_out, row_ok);
+            if (t.type == TILE_ROW) {
+                const int r_seg = t.m * 2 * BM + (int)rank * BM + r_in_tile;  // row within the segment
+                const bool row_ok = r_seg < s.rows[t.seg];
+                const int64_t orow = (int64_t)s.row0[t.seg] + r_seg;
+                epilogue_row<KIND, true>(tbase, C + orow * n_out * kOutLd<KIND>, t.n * BN_OUT, n_out, row_ok);
+            } else {
+                const int64_t row_tail0 = (int64_t)s.row0[t.seg] + t.m * 2 * BM;
+                if (!epilogue_tail<KIND>(s, xbufs, tbase, t, row_tail0, C, n_out, rank, quarter, lane, xcount,
+                                         abort_flag, p.err))
+                    break;
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
                 if (leader) mbar_arrive_relaxed(&s.tempty[acc]);
                 else mbar_arrive_remote_relaxed(lead_tempty + 8u * (uint32_t)acc);
             }
-            if (++acc == NACC) {
+            if (++acc == 2) {
                 acc = 0;
                 aph ^= 1;
             }
@@ -659,7 +798,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     cluster_sync();  // the pair's MMAs and both epilogues are done with TMEM
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc_pair(tmem_base, TMEM_COLS2);
+        tmem_dealloc_pair(tmem_base, 2 * ACC_COLS);
     }
 }
 
@@ -678,20 +817,17 @@ cudaError_t launch_kind(const TcParams &p, int64_t max_tiles, cudaStream_t s) {
     return launch_pdl(k_ffn_tc<KIND>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, s, p);
 }
 
-// Accumulator buffers of the pair kernel (TMEM columns = 256 per buffer).
-constexpr int PAIR_NACC = 2;
-
 template <int KIND>
 cudaError_t launch_kind2(const TcParams &p, int64_t max_tiles, cudaStream_t s) {
     static bool attr_done = false;
     if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(k_ffn_tc2<KIND, PAIR_NACC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)SMEM2_BYTES);
+        cudaError_t e =
+            cudaFuncSetAttribute(k_ffn_tc2<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM2_BYTES);
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
     const int clusters = (int)std::max<int64_t>(1, std::min<int64_t>(max_tiles, device_sm_count() / 2));
-    return launch_pdl(k_ffn_tc2<KIND, PAIR_NACC>, dim3(2 * clusters), dim3(NUM_THREADS), SMEM2_BYTES, s, p);
+    return launch_pdl(k_ffn_tc2<KIND>, dim3(2 * clusters), dim3(NUM_THREADS), SMEM2_BYTES, s, p);
 }
 
 // One product over the routed segments and/or the shared segment.
@@ -705,7 +841,9 @@ cudaError_t product(const int32_t *offsets, int n_seg, int64_t a_rows, const voi
                     const void *b0_sh, const void *b1_sh, int K_sh, int n_out_sh, void *out_sh,
                     uint32_t *err, cudaStream_t s, bool pair) {
     constexpr int BN_OUT = kGatedLayout<KIND> ? 128 : 256;
-    const uint32_t box_b = (kGatedLayout<KIND> || pair) ? 128 : 256;
+    // weight rows per TMA box: the single-CTA kernel stages 256 rows (gated: 128 gate +
+    // 128 up), the pair kernel 128 per CTA (gated: 64 gate + 64 up)
+    const uint32_t box_b = kGatedLayout<KIND> ? (pair ? 64 : 128) : (pair ? 128 : 256);
     const int64_t tm = pair ? 2 * BM : BM;
     TcParams p;
     memset(&p, 0, sizeof(p));
@@ -738,9 +876,9 @@ cudaError_t product(const int32_t *offsets, int n_seg, int64_t a_rows, const voi
     if (!pair) return launch_kind<KIND>(p, max_tiles, s);
     // With few rows per expert (under 512 on average) a short last block is a large
     // share of the work: an expert whose last 256-row block holds at most 128 rows then
-    // runs whole on the single-CTA kernel (its 128-row tiles cost half a pair tile), the
-    // others on the pair kernel, so that no expert's weights are streamed by both
-    // launches. With 1024 rows per expert (Mixtral-shaped) a split cost 3 %.
+    // runs whole on the single-CTA kernel (128-row tiles), the others on the pair kernel,
+    // so that no expert's weights are streamed by both launches (measured on the
+    // DeepSeek-shaped layer against the pair kernel's tail tiles: 8.05 vs 8.20-8.32 ms).
     const bool split = n_seg > 0 && a_rows < 512LL * n_seg;
     p.tail_mode = split ? 1 : 0;
     cudaError_t e = launch_kind2<KIND>(p, max_tiles, s);
@@ -748,7 +886,8 @@ cudaError_t product(const int32_t *offsets, int n_seg, int64_t a_rows, const voi
     TcParams q = p;
     q.tail_mode = 2;
     q.sh_rows = 0;
-    if (!kGatedLayout<KIND> && !encode_bf16_3d(&q.tmB0, b0, K, n_out, n_seg, 256)) return cudaErrorInvalidValue;
+    if (!encode_bf16_3d(&q.tmB0, b0, K, n_out, n_seg, kGatedLayout<KIND> ? 128 : 256)) return cudaErrorInvalidValue;
+    if (kGatedLayout<KIND> && !encode_bf16_3d(&q.tmB1, b1, K, n_out, n_seg, 128)) return cudaErrorInvalidValue;
     return launch_kind<KIND>(q, ((a_rows + BM - 1) / BM + n_seg) * ((n_out + BN_OUT - 1) / BN_OUT), s);
 }
 

@@ -225,3 +225,25 @@ def test_full_size_parity(name, sample):
     ysel = fwd["y"] if tokens is None else fwd["y"][tokens]
     check_output(ysel, rt["y"], w.dtype)
     assert np.array_equal(fwd["y"], sep["y"])
+
+
+# One expert takes every token, so its row count is T: the pair kernel's last block
+# holds T mod 256 rows, handled as a tile with the tokens on the MMA's N side (1, 32,
+# 33, 128, 129, 255 rows), or none (T = 768); below 512 rows the experts with a short
+# last block move to the single-CTA kernel (T = 300) and the others keep the pair
+# kernel's tail tile (T = 400). Gated, ReLU and shared-expert variants.
+TAILS = [_small("mixtral_prefill", T=t, d=128, h=256, N=1, k=1) for t in (513, 544, 545, 640, 641, 767, 768,
+                                                                          300, 400)]
+TAILS += [_small("switch_top1", T=t, d=128, h=384, N=1, k=1, capacity_factor=None) for t in (545, 767)]
+TAILS += [_small("deepseek_fine", T=t, d=128, N=1, k=1, h=128, h_shared=128) for t in (545, 767)]
+
+
+@pytest.mark.parametrize("w", TAILS, ids=[w.name for w in TAILS])
+def test_pair_kernel_tail_tiles(w):
+    inp = W.make_inputs(w, device="cuda")
+    ws = moe.workspace(cfg_of(w))
+    rt = O.forward(w, oracle_inputs(inp))
+    out = host(run_forward(cfg_of(w, debug_flags=moe.MOE_DEBUG_FFN_PAIR), inp, ws))
+    assert moe.moe_check_error(ws) == moe.MOE_OK
+    check_routing(out, rt, sep=False)
+    check_output(out["y"], rt["y"], w.dtype)
