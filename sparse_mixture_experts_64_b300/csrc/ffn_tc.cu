@@ -878,7 +878,8 @@ cudaError_t product(const int32_t *offsets, int n_seg, int64_t a_rows, const voi
     // share of the work: an expert whose last 256-row block holds at most 128 rows then
     // runs whole on the single-CTA kernel (128-row tiles), the others on the pair kernel,
     // so that no expert's weights are streamed by both launches (measured on the
-    // DeepSeek-shaped layer against the pair kernel's tail tiles: 8.05 vs 8.20-8.32 ms).
+    // DeepSeek-shaped layer against the pair kernel's tail tiles alone: 7.97-8.03 vs
+    // 8.17-8.23 ms per forward).
     const bool split = n_seg > 0 && a_rows < 512LL * n_seg;
     p.tail_mode = split ? 1 : 0;
     cudaError_t e = launch_kind2<KIND>(p, max_tiles, s);
