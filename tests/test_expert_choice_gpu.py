@@ -123,3 +123,23 @@ def test_full_size_expert_choice():
     tokens = np.sort(np.random.default_rng(5).choice(w.T, size=12, replace=False))
     ref = O.layer_output_expert_choice(w, oi["x"], rt, oi["w_gate"], oi["w_up"], oi["w_down"], tokens=tokens)
     check_output(y.float().cpu().numpy()[tokens], ref, w.dtype)
+
+
+def test_largest_expert_choice_batch():
+    """T = 16384, the largest batch the Expert Choice selection sorts in shared memory,
+    over 64 experts: routing bit-exact for all tokens, outputs on a sample."""
+    w = _ec("deepseek_fine", T=16384, d=128, N=64, h=128, h_shared=0, capacity_factor=(2, 1))
+    cfg = cfg_of(w)
+    inp = W.make_inputs(w, device="cuda")
+    ws = moe.workspace(cfg)
+    g = host(_router(cfg, w, inp, ws))
+    oi = oracle_inputs(inp)
+    rt = O.route_expert_choice(w, oi["x"], oi["w_r"], oi["b_r"])
+    _check_router(g, rt)
+    y = torch.empty((w.T, w.d), dtype=inp["x"].dtype, device="cuda")
+    moe.moe_forward(cfg, inp["x"], inp["w_r"], inp["b_r"], inp["w_gate"], inp["w_up"], inp["w_down"],
+                    None, None, None, y, None, None, None, None, None, ws)
+    assert moe.moe_check_error(ws) == moe.MOE_OK
+    tokens = np.sort(np.random.default_rng(6).choice(w.T, size=16, replace=False))
+    ref = O.layer_output_expert_choice(w, oi["x"], rt, oi["w_gate"], oi["w_up"], oi["w_down"], tokens=tokens)
+    check_output(y.float().cpu().numpy()[tokens], ref, w.dtype)

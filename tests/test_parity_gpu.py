@@ -247,3 +247,29 @@ def test_pair_kernel_tail_tiles(w):
     assert moe.moe_check_error(ws) == moe.MOE_OK
     check_routing(out, rt, sep=False)
     check_output(out["y"], rt["y"], w.dtype)
+
+
+# The largest batch the library accepts (T = 65536) with the most experts and slots
+# (N = 256, top-8, a capacity that drops slots) and with the N <= 32 router: routing,
+# counts, dispatch order and drop set bit-exact for all tokens, outputs on a sample.
+MAXIMAL = [
+    _small("deepseek_fine", T=65536, d=128, N=256, k=8, h=128, h_shared=0, capacity_factor=(1, 1)),
+    _small("mixtral_prefill", T=65536, d=256, N=32, k=8, h=128),
+]
+
+
+@pytest.mark.parametrize("w", MAXIMAL, ids=[w.name for w in MAXIMAL])
+def test_maximum_batch(w):
+    inp = W.make_inputs(w, device="cuda")
+    cfg = cfg_of(w)
+    ws = moe.workspace(cfg)
+    fwd = host(run_forward(cfg, inp, ws))
+    sep = host(run_separate(cfg, inp, ws))
+    assert moe.moe_check_error(ws) == moe.MOE_OK
+    tokens = np.sort(np.random.default_rng(99).choice(w.T, size=24, replace=False))
+    rt = O.forward(w, oracle_inputs(inp), tokens=tokens)
+    check_routing(sep, rt, sep=True)
+    check_routing(fwd, rt, sep=False)
+    check_output(fwd["y"][tokens], rt["y"], w.dtype)
+    if w.capacity_factor:
+        assert int(rt["counts_kept"].sum()) < w.T * w.k  # the capacity dropped slots
