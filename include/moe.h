@@ -22,8 +22,10 @@
  * --------------------------------
  *  - Every pointer argument is a DEVICE pointer unless stated otherwise; the
  *    config is a HOST pointer. The caller owns all memory. The library never
- *    allocates, frees or synchronises (moe_check_error excepted): every call
- *    enqueues kernels on `stream` and returns.
+ *    allocates device memory and never synchronises (moe_check_error excepted):
+ *    every call enqueues kernels on `stream` and returns. Two calls hold other CUDA
+ *    objects: moe_forward_graph_create (a graph, captured on a private stream) and
+ *    moe_backward (an auxiliary stream and events for the duration of the call).
  *  - Layouts are row-major. Activations x, x_perm, y_perm, y: [rows][d].
  *    Router weight w_r: [d][N] fp32; router bias b_r: [N] fp32.
  *    Expert weights use the [out][in] (nn.Linear) layout:
@@ -362,8 +364,13 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const float *w_r,
  *   ignored without a router bias), dw_gate_or_w1 / dw_up [N][h][d], dw_down
  *   [N][d][h], dshared_* shaped like the shared weights — all bf16 outputs.
  * The expert weights are transposed into bws for the row products; the weight
- * gradients reduce over each expert's rows on the tensor cores. fp32 and Expert
- * Choice configs return MOE_ERR_UNSUPPORTED.
+ * gradients reduce over each expert's rows on the tensor cores. The weight
+ * transposes, the transposed forward activations and the recomputed router logits
+ * run on a non-blocking auxiliary stream that the call creates, joins to `stream` with
+ * events where their results are needed, and releases before returning (its work
+ * completes asynchronously, ordered before the work enqueued on `stream` after the
+ * call); if the stream cannot be created, everything runs on `stream`. fp32 and
+ * Expert Choice configs return MOE_ERR_UNSUPPORTED.
  */
 size_t moe_backward_workspace_size(const moe_config *cfg);
 moe_status moe_backward(const moe_config *cfg, const void *x, const float *w_r, const float *b_r,

@@ -370,15 +370,52 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const float *w_r, 
         return e == cudaSuccess;
     };
 
+    // Work that depends only on the inputs and the forward's saved tensors runs on an
+    // auxiliary stream beside the row products: the weight re-layouts (HBM-bound, while
+    // the recompute and dH products are tensor-bound), the padding prefix, the
+    // transposed forward activations and the router logits. Events join it where each
+    // result is first needed; without the stream (creation failed) it all runs in order
+    // on `stream`.
+    cudaStream_t aux = nullptr;
+    cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};  // fork, W_outᵀ ready, [W_a | W_b]ᵀ ready, aux done
+    bool two = cudaStreamCreateWithFlags(&aux, cudaStreamNonBlocking) == cudaSuccess;
+    for (int i = 0; i < 4 && two; ++i) two = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) == cudaSuccess;
+    if (two) two = cudaEventRecord(ev[0], stream) == cudaSuccess && cudaStreamWaitEvent(aux, ev[0], 0) == cudaSuccess;
+    const cudaStream_t sa = two ? aux : stream;
+    auto mark = [&](int i) {
+        if (two) ok(cudaEventRecord(ev[i], sa));
+    };
+    auto join = [&](int i) {
+        if (two) ok(cudaStreamWaitEvent(stream, ev[i], 0));
+    };
+
+    // -- auxiliary stream
     // weights transposed for the row products: W_outᵀ [N][h][d], [W_a | W_b]ᵀ [N][d][Wd]
-    ok(launch_transpose_batched(w_down, N, d, h, wo_t, d, 0, stream));
-    ok(launch_transpose_batched(w_gate_or_w1, N, h, d, wab_t, Wd, 0, stream));
-    if (gated) ok(launch_transpose_batched(w_up, N, h, d, wab_t, Wd, h, stream));
+    ok(launch_transpose_batched(w_down, N, d, h, wo_t, d, 0, sa));
+    if (hs) ok(launch_transpose_batched(shared_w_down, 1, d, hs, bw + B.wo_sh_t, d, 0, sa));
+    mark(1);
+    ok(launch_transpose_batched(w_gate_or_w1, N, h, d, wab_t, Wd, 0, sa));
+    if (gated) ok(launch_transpose_batched(w_up, N, h, d, wab_t, Wd, h, sa));
     if (hs) {
-        ok(launch_transpose_batched(shared_w_down, 1, d, hs, bw + B.wo_sh_t, d, 0, stream));
-        ok(launch_transpose_batched(shared_w_gate, 1, hs, d, bw + B.wab_sh_t, 2 * hs, 0, stream));
-        ok(launch_transpose_batched(shared_w_up, 1, hs, d, bw + B.wab_sh_t, 2 * hs, hs, stream));
+        ok(launch_transpose_batched(shared_w_gate, 1, hs, d, bw + B.wab_sh_t, 2 * hs, 0, sa));
+        ok(launch_transpose_batched(shared_w_up, 1, hs, d, bw + B.wab_sh_t, 2 * hs, hs, sa));
     }
+    mark(2);
+    // the weight gradients' operands that the forward left: each expert's rows padded to 64
+    ok(launch_pad_prefix(offsets, N, (int)R, kpre, sa));
+    ok(launch_transpose_rows_padded(hid, h, offsets, kpre, N, (int)R, Kall, bw + B.H_t, sa));
+    ok(launch_transpose_rows_padded(x_perm, d, offsets, kpre, N, (int)R, Kall, bw + B.X_t, sa));
+    if (hs) {
+        ok(launch_transpose_rows_padded(dy, d, nullptr, nullptr, 1, c.T, Tp, bw + B.dy_t, sa));
+        ok(launch_transpose_rows_padded(hid_sh, hs, nullptr, nullptr, 1, c.T, Tp, bw + B.Hsh_t, sa));
+        ok(launch_transpose_rows_padded(x, d, nullptr, nullptr, 1, c.T, Tp, bw + B.x_t, sa));
+    }
+    // router logits, recomputed
+    ok(launch_router_logits(c, x, w_r, c.has_router_bias ? b_r : nullptr, reinterpret_cast<float *>(bw + B.logits), w,
+                            sa));
+    mark(3);
+
+    // -- main stream
     // gate-scaled dy per row and the gate gradients
     ok(launch_bwd_slots(c, dy, y_perm, slot_row, gate, dO, dgate, err, stream));
     // pre-activations, recomputed: [A | B] (gated) or A (ReLU)
@@ -388,20 +425,20 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const float *w_r, 
         ok(launch_gemm_rows(c, true, nullptr, 0, 0, nullptr, nullptr, nullptr, 0, 0, nullptr, c.T, x, shared_w_gate,
                             shared_w_up, d, hs, bw + B.AB_sh, err, stream));
     // dH = dO W_out
+    join(1);
     ok(launch_gemm_rows(c, false, offsets, N, R, dO, wo_t, nullptr, d, h, dH, hs ? c.T : 0, dy, bw + B.wo_sh_t,
                         nullptr, d, hs, bw + B.dH_sh, err, stream));
     // [dA | dB] from the pre-activations
     ok(launch_act_bwd(gated, AB, dH, R, h, dAB, stream));
     if (hs) ok(launch_act_bwd(true, bw + B.AB_sh, bw + B.dH_sh, c.T, hs, bw + B.dAB_sh, stream));
     // dX = [dA | dB] [W_a ; W_b]
+    join(2);
     ok(launch_gemm_rows(c, false, offsets, N, R, dAB, wab_t, nullptr, Wd, d, dX, hs ? c.T : 0, bw + B.dAB_sh,
                         bw + B.wab_sh_t, nullptr, 2 * hs, d, bw + B.dX_sh, err, stream));
     // weight gradients: transposed activations with each expert's rows padded to 64
-    ok(launch_pad_prefix(offsets, N, (int)R, kpre, stream));
+    join(3);
     ok(launch_transpose_rows_padded(dO, d, offsets, kpre, N, (int)R, Kall, bw + B.dO_t, stream));
-    ok(launch_transpose_rows_padded(hid, h, offsets, kpre, N, (int)R, Kall, bw + B.H_t, stream));
     ok(launch_transpose_rows_padded(dAB, Wd, offsets, kpre, N, (int)R, Kall, bw + B.dAB_t, stream));
-    ok(launch_transpose_rows_padded(x_perm, d, offsets, kpre, N, (int)R, Kall, bw + B.X_t, stream));
     const bool pair_ok = !(c.debug_flags & MOE_DEBUG_FFN_SINGLE);
     ok(launch_wgrad(offsets, N, R, bw + B.dO_t, bw + B.H_t, Kall, d, h, dw_down, nullptr, nullptr, 0, nullptr, err,
                     stream, pair_ok));
@@ -411,10 +448,7 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const float *w_r, 
         ok(launch_wgrad(offsets, N, R, bw + B.dAB_t + (size_t)h * Kall * 2, bw + B.X_t, Kall, h, d, dw_up, nullptr,
                         nullptr, 0, nullptr, err, stream, pair_ok));
     if (hs) {
-        ok(launch_transpose_rows_padded(dy, d, nullptr, nullptr, 1, c.T, Tp, bw + B.dy_t, stream));
-        ok(launch_transpose_rows_padded(hid_sh, hs, nullptr, nullptr, 1, c.T, Tp, bw + B.Hsh_t, stream));
         ok(launch_transpose_rows_padded(bw + B.dAB_sh, 2 * hs, nullptr, nullptr, 1, c.T, Tp, bw + B.dABsh_t, stream));
-        ok(launch_transpose_rows_padded(x, d, nullptr, nullptr, 1, c.T, Tp, bw + B.x_t, stream));
         ok(launch_wgrad(nullptr, 0, 0, nullptr, nullptr, 0, d, hs, nullptr, bw + B.dy_t, bw + B.Hsh_t, (int)Tp,
                         dshared_w_down, err, stream, pair_ok));
         ok(launch_wgrad(nullptr, 0, 0, nullptr, nullptr, 0, hs, d, nullptr, bw + B.dABsh_t, bw + B.x_t, (int)Tp,
@@ -422,14 +456,16 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const float *w_r, 
         ok(launch_wgrad(nullptr, 0, 0, nullptr, nullptr, 0, hs, d, nullptr, bw + B.dABsh_t + (size_t)hs * Tp * 2,
                         bw + B.x_t, (int)Tp, dshared_w_up, err, stream, pair_ok));
     }
-    // router: logits recomputed, dL, dx_router, dW_r, db
-    ok(launch_router_logits(c, x, w_r, c.has_router_bias ? b_r : nullptr, reinterpret_cast<float *>(bw + B.logits), w,
-                            stream));
+    // router: dL, dx_router, dW_r, db
     ok(launch_router_bwd(c, x, w_r, idx, gate, B, bw, aux_coef, z_coef, dw_r, c.has_router_bias ? db_r : nullptr,
                          stream));
     // dx = dy + sum_j dX_r + dX_shared + dx_router
     ok(launch_bwd_dx(c, dy, dX, slot_row, hs ? bw + B.dX_sh : nullptr, reinterpret_cast<const float *>(bw + B.dxr), dx,
                      err, stream));
+    // the stream and events are released once their work completes
+    for (cudaEvent_t q : ev)
+        if (q) cudaEventDestroy(q);
+    if (aux) cudaStreamDestroy(aux);
     return to_status(e);
 }
 
