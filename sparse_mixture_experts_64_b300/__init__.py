@@ -324,9 +324,12 @@ class ForwardGraph:
         moe_forward_graph_destroy(self)
 
     def __del__(self):
-        if getattr(self, "handle", None):
-            _lib.moe_forward_graph_destroy(self.handle)
-            self.handle = None
+        h, self.handle = getattr(self, "handle", None), None
+        if h and _lib is not None:
+            try:
+                _lib.moe_forward_graph_destroy(h)
+            except Exception:  # interpreter shutdown: the library may already be gone
+                pass
 
 
 def moe_forward_graph_create(cfg, x, w_r, b_r, w_gate_or_w1, w_up, w_down, shared_w_gate,
