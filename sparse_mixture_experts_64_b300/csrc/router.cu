@@ -906,8 +906,12 @@ cudaError_t launch_logits_tile(const moe_config &c, const XT *x, const float *w_
 template <typename XT>
 cudaError_t launch_logits_only(const moe_config &c, const XT *x, const float *w_t, const float *b_r, int has_bias,
                                float *logits, uint32_t *err, cudaStream_t s) {
-    // 8 warps of 8 tokens x 8 experts (0.75 bytes of shared memory read per FMA):
-    // 902 us for the DeepSeek-shaped router (T = 8192, d = 7168, N = 256) against
+    // At most 8 experts (the Expert Choice router of the Mixtral-shaped layer, the
+    // backward's recomputed logits): 4 warps of 4 tokens x 8 experts, tile 16 x 8, so no
+    // warp works on absent experts and twice as many CTAs share the tokens.
+    if (c.N <= 8) return launch_logits_tile<XT, 4, 8, 4, 1>(c, x, w_t, b_r, has_bias, logits, err, s);
+    // Otherwise 8 warps of 8 tokens x 8 experts (0.75 bytes of shared memory read per
+    // FMA): 902 us for the DeepSeek-shaped router (T = 8192, d = 7168, N = 256) against
     // 995 us with 16 warps of 4 x 8 (1.25 bytes per FMA), and 982-1001 us for 6 x 8,
     // 8 x 4 and 4 x 8 tiles of 32 x 16; identical logits in every case.
     return launch_logits_tile<XT, 8, 8, 4, 2>(c, x, w_t, b_r, has_bias, logits, err, s);
