@@ -21,7 +21,9 @@
 // L2); row counts never travel to the host. Rows past a segment's end are
 // computed on whatever the A rows hold and never stored. Every wait is bounded:
 // after kTimeoutNs the kernel records MOE_ERR_TIMEOUT, drains its own copies and
-// MMAs, frees TMEM and returns.
+// MMAs, frees TMEM and returns. The CTA-pair kernel further down has the same roles
+// with 2-SM MMAs (256 x 256 tiles) and computes a segment's last partial row block
+// with the tokens on the MMA's N side.
 #include <algorithm>
 #include <cstring>
 
