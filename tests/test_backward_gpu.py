@@ -48,6 +48,7 @@ CASES = [
     (_w("switch_top1", T=150, d=192, h=128, N=4, k=2, h_shared=192, capacity_factor=None), 0.0, 0.01),
     (_w("mixtral_prefill", T=1024, d=512, h=1024, N=8, k=2), 0.0, 0.0),          # pair kernels
     (_w("deepseek_fine", T=96, d=128, N=64, k=6, h=192, h_shared=0), 0.05, 0.0),  # N > 32 router
+    (_w("deepseek_fine", T=600, d=64, N=4, k=2, h=64, h_shared=64), 0.01, 0.001),  # smallest tiles, pair
 ]
 
 

@@ -273,3 +273,25 @@ def test_maximum_batch(w):
     check_output(fwd["y"][tokens], rt["y"], w.dtype)
     if w.capacity_factor:
         assert int(rt["counts_kept"].sum()) < w.T * w.k  # the capacity dropped slots
+
+
+# The smallest shapes the tensor-core path takes: d = h = 64 (one 64-wide k-block per
+# tile, output narrower than one 128- or 256-column tile), with and without a shared
+# expert, on the pair kernel (forced) and the single-CTA kernel.
+TINY_TC = [
+    _small("mixtral_prefill", T=70, d=64, h=64, N=4, k=2),
+    _small("deepseek_fine", T=300, d=64, N=4, k=2, h=64, h_shared=64),
+    _small("switch_top1", T=600, d=64, h=64, N=2, k=1),
+]
+
+
+@pytest.mark.parametrize("w", TINY_TC, ids=[w.name for w in TINY_TC])
+@pytest.mark.parametrize("flags", [0, 2, 4], ids=["auto", "pair", "single"])
+def test_smallest_tensor_core_shapes(w, flags):
+    inp = W.make_inputs(w, device="cuda")
+    ws = moe.workspace(cfg_of(w))
+    rt = O.forward(w, oracle_inputs(inp))
+    out = host(run_forward(cfg_of(w, debug_flags=flags), inp, ws))
+    assert moe.moe_check_error(ws) == moe.MOE_OK
+    check_routing(out, rt, sep=False)
+    check_output(out["y"], rt["y"], w.dtype)
