@@ -267,8 +267,8 @@ moe_status moe_combine_expert_choice(const moe_config *cfg, const void *x, const
                                      void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
- * moe_router_topk for callers that cannot allocate device memory. The paper has
- * no counterpart to this call; it exists for hosts that forbid allocation after
+ * moe_router_topk for callers that cannot allocate device memory. The pages
+ * describe no such call; it exists for hosts that forbid allocation after
  * start-up (engines that plan all device memory ahead and call plugins from an
  * enqueue path, services with a fixed memory budget), which cannot hand over a
  * workspace on demand.
@@ -276,8 +276,8 @@ moe_status moe_combine_expert_choice(const moe_config *cfg, const void *x, const
  * workspace: the router's scratch lives in one static 32 MiB device array of the
  * library, held by every GPU that loads it until the process exits. Configs whose
  * router scratch would exceed 32 MiB are rejected with MOE_ERR_UNSUPPORTED before
- * anything is enqueued (the five reference workloads all fit). Nothing is
- * allocated and no allocating routine is called.
+ * anything is enqueued (the tiny, Switch, Mixtral and DeepSeekMoE-shaped layers
+ * all fit). Nothing is allocated and no allocating routine is called.
  * The first call on a device looks up the array's device address (make that first
  * call before any stream capture). All calls share the array: the error word in
  * it is cleared at the start of each call and is not readable through
