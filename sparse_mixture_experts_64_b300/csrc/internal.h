@@ -40,7 +40,7 @@ struct WsLayout {
     size_t zpart;                // f32   [tiles] per-tile sums of the z-loss terms
     size_t routed, kept;         // int32 [N] (used when the caller passes NULL)
     size_t logits;               // f32   [T][N]  (N > 32 only)
-    size_t w_t;                  // f32   [ceil(d/256)][N][256]  router weight, re-laid out
+    size_t w_t;                  // f32   [ceil(d/256)][N even][256]  router weight, re-laid out
     size_t offsets;              // int32 [N+1]
     size_t topk_idx, topk_gate;  // [T][k]
     size_t slot_row;             // int32 [T][k]

@@ -65,7 +65,7 @@ WsLayout ws_layout(const moe_config &c) {
     L.kept = take(N * 4);
     const bool ec = c.routing == MOE_ROUTING_EXPERT_CHOICE;
     L.logits = take(c.N > 32 || ec ? T * N * 4 : 0);
-    L.w_t = take((size_t)((c.d + 255) / 256) * 256 * N * 4);
+    L.w_t = take((size_t)((c.d + 255) / 256) * 256 * ((N + 1) & ~(size_t)1) * 4);  // N rounded up to even
     // expert / shared-expert buffers
     L.hid = take(rmax * c.h * es);
     L.hid_sh = take(c.h_shared ? T * c.h_shared * es : 0);

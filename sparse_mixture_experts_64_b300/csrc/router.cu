@@ -22,9 +22,12 @@
 //   k_router_small   N <= 32: one CTA per tile of tokens; each lane holds every
 //                    expert's partial for its tokens; gating fused (one thread per
 //                    token). Per-tile routed counts per slot and sums of p.
-//   k_transpose_wr   N > 32: router weight [d][N] -> [N][d] (workspace), so that a
-//                    lane's 8 features of one expert are contiguous.
-//   k_logits_large   N > 32: 32 tokens x 16 experts per CTA -> logits [T][N].
+//   k_transpose_wr   router weight [d][N] -> chunk-major copy in the workspace, per
+//                    expert (k_router_small) or per expert pair (k_logits_large),
+//                    so that a lane's features of a block load as 16-byte runs.
+//   k_logits_large   N > 32: 32 tokens x 16 experts per CTA -> logits [T][N]; one
+//                    packed fp32x2 fma updates two experts' partials (each half
+//                    rounds exactly like a scalar fma, so the order above holds).
 //   k_gate           N > 32: one warp per token: top-k, softmax, gates; per-tile stats.
 //   k_expert_scan    one CTA per expert: priority-order prefix of the tile counts
 //                    (slot-major, token order), capacity clamp, kept-per-tile
@@ -371,17 +374,43 @@ __device__ __forceinline__ size_t wt_index(int i, int e, int d, int N) {
     return ((size_t)c * N + e) * 256 + (r >> 2) * (nb * 4) + l * 4 + (r & 3);
 }
 
+// Expert-pair layout of k_logits_large, whose lanes update two experts with one
+// packed fp32x2 FMA: [chunk of 256 features][expert pair][512 positions] over
+// N rounded up to even (the extra expert of an odd N holds zeros). Inside a pair,
+// quarter q (features 2q and 2q+1 of every 8-feature block) comes block after
+// block, and each block's 16 bytes of the quarter hold (f = 2q: expert 2p, 2p+1;
+// f = 2q+1: expert 2p, 2p+1), so lane l's quarter-q load sits at 16*(q*nb + l)
+// bytes and one 16-byte load gives the two experts' weights of two features as
+// float pairs; every quarter-load of a warp reads one contiguous 512-byte run.
+__device__ __forceinline__ size_t wt_index_paired(int i, int e, int d, int n_even) {
+    const int c = i >> 8, p = i & 255;
+    const int nb = min(32, (d - (c << 8)) >> 3);
+    const int l = p >> 3, r = p & 7;
+    return ((size_t)c * n_even + (e & ~1)) * 256 + (r >> 1) * (nb * 4) + l * 4 + (r & 1) * 2 + (e & 1);
+}
+
+// Grid: (ceil(d/32), ceil(N'/32)) with N' = N (per-expert layout) or N rounded up
+// to even (pair layout, whose extra expert is written as zeros).
+template <bool PAIRED>
 __global__ void __launch_bounds__(256) k_transpose_wr(const float *__restrict__ w_r, float *__restrict__ w_t,
                                                       int d, int N) {
     __shared__ float tile[32][33];
     const int i0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const int n_out = PAIRED ? (N + 1) & ~1 : N;
     pdl_enter();
     for (int r = ty; r < 32; r += 8)
         if (i0 + r < d && e0 + tx < N) tile[r][tx] = w_r[(size_t)(i0 + r) * N + e0 + tx];
     __syncthreads();
-    for (int r = ty; r < 32; r += 8)
-        if (e0 + r < N && i0 + tx < d) w_t[wt_index(i0 + tx, e0 + r, d, N)] = tile[tx][r];
+    for (int r = ty; r < 32; r += 8) {
+        const int e = e0 + r, i = i0 + tx;
+        if (e >= n_out || i >= d) continue;
+        const float v = e < N ? tile[tx][r] : 0.0f;
+        if constexpr (PAIRED)
+            w_t[wt_index_paired(i, e, d, n_out)] = v;
+        else
+            w_t[wt_index(i, e, d, N)] = v;
+    }
 }
 
 // 8 weights of expert row `row` (256 floats of one chunk) for lane's block.
@@ -500,6 +529,26 @@ struct LogitsArgs {
 // features one 2D TMA copy of the token tile and one bulk copy of the tile's expert
 // weight rows, into a STAGES-slot ring. Per feature a lane loads TO x values and EO
 // weights from shared memory for TO*EO FMAs.
+// 8 consecutive features of one token, kept as loaded; dup(r) gives feature r
+// as the float pair (x, x) for a packed FMA against two experts' weights.
+template <typename XT> struct XRow8;
+template <> struct XRow8<__nv_bfloat16> {
+    uint32_t w[4];
+    __device__ __forceinline__ void load(const uint8_t *p) {
+        const uint4 q = *reinterpret_cast<const uint4 *>(p);
+        w[0] = q.x; w[1] = q.y; w[2] = q.z; w[3] = q.w;
+    }
+    __device__ __forceinline__ float2 dup(int r) const {
+        const float v = __uint_as_float((r & 1) ? (w[r >> 1] & 0xffff0000u) : (w[r >> 1] << 16));
+        return make_float2(v, v);
+    }
+};
+template <> struct XRow8<float> {
+    float f[8];
+    __device__ __forceinline__ void load(const uint8_t *p) { lds<8>(reinterpret_cast<const float *>(p), f); }
+    __device__ __forceinline__ float2 dup(int r) const { return make_float2(f[r], f[r]); }
+};
+
 template <typename XT, int TO, int EO, int TG, int EG>
 __global__ void __launch_bounds__((TG * EG + 1) * 32, 1) k_logits_large(const __grid_constant__ CUtensorMap tmx,
                                                                      const float *__restrict__ w_t,
@@ -509,16 +558,16 @@ __global__ void __launch_bounds__((TG * EG + 1) * 32, 1) k_logits_large(const __
     constexpr int ES = (int)sizeof(XT);
     constexpr int X_BYTES = TOK * KC * ES;
     constexpr int STAGE = (X_BYTES + EXP * KC * 4 + 1023) & ~1023;
-    static_assert(EO % 2 == 0, "experts are loaded in pairs");
+    static_assert(EO % 2 == 0, "experts are taken in pairs");
     extern __shared__ __align__(1024) uint8_t router_smem[];
     __shared__ Ring<STAGES> ring;
     uint8_t *sb = router_smem + ((1024 - (tc::smem_u32(router_smem) & 1023)) & 1023);
 
-    const int T = a.T, d = a.d, N = a.N;
+    const int T = a.T, d = a.d, N = a.N, n_even = (N + 1) & ~1;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int tg = warp / EG, eg = warp % EG;
     const int e0 = blockIdx.x * EXP, t0 = blockIdx.y * TOK;   // experts fastest: CTAs sharing a token tile run together
-    const int nexp = min(EXP, N - e0);
+    const int nexp = min(EXP, n_even - e0);                    // even: whole pairs
     const int nblocks = d / 8;
     const int nchunks = (nblocks + NBLK - 1) / NBLK;
 
@@ -526,11 +575,12 @@ __global__ void __launch_bounds__((TG * EG + 1) * 32, 1) k_logits_large(const __
     __syncthreads();
     pdl_enter();
 
-    float acc[TO][EO];
+    // acc[i][p] = partials of token i for experts 2p and 2p+1 of the warp's EO
+    float2 acc[TO][EO / 2];
 #pragma unroll
     for (int i = 0; i < TO; ++i)
 #pragma unroll
-        for (int j = 0; j < EO; ++j) acc[i][j] = 0.0f;
+        for (int p = 0; p < EO / 2; ++p) acc[i][p] = make_float2(0.0f, 0.0f);
 
     if (warp == NC) {
         if (lane == 0) {
@@ -542,7 +592,7 @@ __global__ void __launch_bounds__((TG * EG + 1) * 32, 1) k_logits_large(const __
                 const uint32_t wbytes = (uint32_t)(nexp * KC * 4);
                 tc::mbar_arrive_expect_tx(bar, (uint32_t)X_BYTES + wbytes);
                 tc::tma_load_2d(slot, &tmx, c * KC, t0, bar);
-                tc::bulk_copy_g2s(slot + X_BYTES, w_t + ((size_t)c * N + e0) * KC, wbytes, bar);
+                tc::bulk_copy_g2s(slot + X_BYTES, w_t + ((size_t)c * n_even + e0) * KC, wbytes, bar);
                 issued = c + 1;
             }
             ring.drain(issued);
@@ -553,21 +603,28 @@ __global__ void __launch_bounds__((TG * EG + 1) * 32, 1) k_logits_large(const __
             const uint8_t *slot = sb + (size_t)(c % STAGES) * STAGE;
             const int nb = min(NBLK, nblocks - c * NBLK);
             if (lane < nb) {
-                float xf[TO][8];
+                XRow8<XT> xr[TO];
 #pragma unroll
-                for (int i = 0; i < TO; ++i) load8<XT>(slot + ((tg * TO + i) * KC + lane * 8) * ES, xf[i]);
-                const float *wl = reinterpret_cast<const float *>(slot + X_BYTES) + (eg * EO) * KC;
+                for (int i = 0; i < TO; ++i) xr[i].load(slot + ((tg * TO + i) * KC + lane * 8) * ES);
+                // pair p of the warp's experts: 2 * KC floats per chunk
+                const float *wl = reinterpret_cast<const float *>(slot + X_BYTES) + (eg * EO) * KC + lane * 4;
 #pragma unroll
-                for (int jp = 0; jp < EO; jp += 2) {
-                    float w0[8], w1[8];
-                    load_w8(wl + jp * KC, lane, nb, w0);
-                    load_w8(wl + (jp + 1) * KC, lane, nb, w1);
+                for (int q = 0; q < 4; ++q) {
+                    float2 wp[EO / 2][2];
 #pragma unroll
-                    for (int r = 0; r < 8; ++r)
+                    for (int p = 0; p < EO / 2; ++p) {
+                        const float4 v = *reinterpret_cast<const float4 *>(wl + p * 2 * KC + q * nb * 4);
+                        wp[p][0] = make_float2(v.x, v.y);
+                        wp[p][1] = make_float2(v.z, v.w);
+                    }
+                    // features 2q, 2q+1 of the block, in increasing order for every partial
+#pragma unroll
+                    for (int f = 0; f < 2; ++f)
 #pragma unroll
                         for (int i = 0; i < TO; ++i) {
-                            acc[i][jp] = __fmaf_rn(xf[i][r], w0[r], acc[i][jp]);
-                            acc[i][jp + 1] = __fmaf_rn(xf[i][r], w1[r], acc[i][jp + 1]);
+                            const float2 xv = xr[i].dup(2 * q + f);
+#pragma unroll
+                            for (int p = 0; p < EO / 2; ++p) acc[i][p] = __ffma2_rn(xv, wp[p][f], acc[i][p]);
                         }
                 }
             }
@@ -580,7 +637,7 @@ __global__ void __launch_bounds__((TG * EG + 1) * 32, 1) k_logits_large(const __
     for (int i = 0; i < TO; ++i)
 #pragma unroll
         for (int j = 0; j < EO; ++j) {
-            const float v = butterfly32(acc[i][j]);
+            const float v = butterfly32((j & 1) ? acc[i][j >> 1].y : acc[i][j >> 1].x);
             const int t = t0 + tg * TO + i, e = e0 + eg * EO + j;
             if (lane == 0 && t < T && e < N) a.logits[(size_t)t * N + e] = a.has_bias ? __fadd_rn(v, b_r[e]) : v;
         }
@@ -887,6 +944,13 @@ cudaError_t launch_small(const moe_config &c, const XT *x, const float *w_t, con
     return launch_pdl(kern, dim3(ra.tiles), dim3(160), bytes, s, tmx, w_t, b_r, ra);
 }
 
+// Router weight -> expert-pair layout of k_logits_large (N rounded up to even).
+cudaError_t launch_transpose_paired(const moe_config &c, const float *w_r, float *w_t, cudaStream_t s) {
+    const int n_even = (c.N + 1) & ~1;
+    return launch_pdl(k_transpose_wr<true>, dim3((c.d + 31) / 32, (n_even + 31) / 32), dim3(256), 0, s, w_r, w_t, c.d,
+                      c.N);
+}
+
 template <typename XT, int TO, int EO, int TG, int EG>
 cudaError_t launch_logits_tile(const moe_config &c, const XT *x, const float *w_t, const float *b_r, int has_bias,
                                float *logits, uint32_t *err, cudaStream_t s) {
@@ -913,7 +977,9 @@ cudaError_t launch_logits_only(const moe_config &c, const XT *x, const float *w_
     // Otherwise 8 warps of 8 tokens x 8 experts (0.75 bytes of shared memory read per
     // FMA): 902 us for the DeepSeek-shaped router (T = 8192, d = 7168, N = 256) against
     // 995 us with 16 warps of 4 x 8 (1.25 bytes per FMA), and 982-1001 us for 6 x 8,
-    // 8 x 4 and 4 x 8 tiles of 32 x 16; identical logits in every case.
+    // 8 x 4 and 4 x 8 tiles of 32 x 16; identical logits in every case. Packed fp32x2
+    // FMAs over expert pairs (half the FMA instructions, one 16-byte weight load per two
+    // features of two experts) took the same router from 902.7 to 890.4 us, same bits.
     return launch_logits_tile<XT, 8, 8, 4, 2>(c, x, w_t, b_r, has_bias, logits, err, s);
 }
 
@@ -931,8 +997,9 @@ cudaError_t launch_large(const moe_config &c, const XT *x, const float *w_t, con
 template <typename XT>
 cudaError_t launch_logits_gate(const moe_config &c, const XT *x, const float *w_r, const float *b_r, RouterArgs ra,
                                float *logits, float *w_t, cudaStream_t s) {
-    cudaError_t e = launch_pdl(k_transpose_wr, dim3((c.d + 31) / 32, (c.N + 31) / 32), dim3(256), 0, s, w_r, w_t, c.d,
-                               c.N);
+    cudaError_t e = c.N > 32 ? launch_transpose_paired(c, w_r, w_t, s)
+                             : launch_pdl(k_transpose_wr<false>, dim3((c.d + 31) / 32, (c.N + 31) / 32), dim3(256), 0,
+                                          s, w_r, w_t, c.d, c.N);
     if (e != cudaSuccess) return e;
     if (c.N <= 4) return launch_small<XT, 4>(c, x, w_t, b_r, ra, s);
     if (c.N <= 8) return launch_small<XT, 8>(c, x, w_t, b_r, ra, s);
@@ -948,8 +1015,7 @@ cudaError_t launch_router_logits(const moe_config &c, const void *x, const float
     const WsLayout L = ws_layout(c);
     uint32_t *err = reinterpret_cast<uint32_t *>(ws + L.err);
     float *w_t = reinterpret_cast<float *>(ws + L.w_t);
-    cudaError_t e = launch_pdl(k_transpose_wr, dim3((c.d + 31) / 32, (c.N + 31) / 32), dim3(256), 0, s, w_r, w_t, c.d,
-                               c.N);
+    cudaError_t e = launch_transpose_paired(c, w_r, w_t, s);
     if (e != cudaSuccess) return e;
     const int hb = c.has_router_bias && b_r ? 1 : 0;
     if (c.dtype == MOE_BF16)
