@@ -49,7 +49,7 @@ namespace moe {
 static int router_np(int N) { return N <= 4 ? 4 : N <= 8 ? 8 : N <= 16 ? 16 : 32; }
 
 int router_tile_tokens(const moe_config &c) {
-    if (c.N > 32) return 64;           // k_gate: 8 warps x 8 tokens
+    if (c.N > 32) return 64;           // k_gate: 16 warps x 4 tokens
     return 4 * (32 / router_np(c.N));  // k_router_small: 4 warps x (32 / NP) tokens
 }
 
@@ -643,16 +643,42 @@ __global__ void __launch_bounds__((TG * EG + 1) * 32, 1) k_logits_large(const __
         }
 }
 
-// One CTA = 8 warps, 64 tokens: logits tile -> shared memory -> gating -> stats.
-__global__ void __launch_bounds__(256) k_gate(const float *__restrict__ logits, RouterArgs a) {
-    constexpr int TT = 64;
+// One CTA = 16 warps, 64 tokens: logits tile -> shared memory -> gating -> stats.
+// The tile is one contiguous run of logits; it is loaded as 16-byte vectors with
+// every load of a thread in flight before the first store (one round trip to L2,
+// where the logits kernel left them), then each warp gates 4 tokens.
+constexpr int kGateThreads = 512;
+__global__ void __launch_bounds__(kGateThreads) k_gate(const float *__restrict__ logits, RouterArgs a) {
+    constexpr int TT = 64, U = 8;
     extern __shared__ __align__(16) float smem[];
     float *Ls = smem;                                    // [TT][N]
     int *Is = reinterpret_cast<int *>(smem + TT * a.N);  // [TT][8]
     const int t0 = blockIdx.x * TT;
     const int nrows = min(TT, a.T - t0);
     pdl_enter();
-    for (int i = threadIdx.x; i < nrows * a.N; i += blockDim.x) Ls[i] = logits[(size_t)t0 * a.N + i];
+    const float *src = logits + (size_t)t0 * a.N;
+    const int n = nrows * a.N;
+    int done = 0;
+    if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+        const int n4 = n >> 2;
+        const float4 *src4 = reinterpret_cast<const float4 *>(src);
+        float4 *dst4 = reinterpret_cast<float4 *>(Ls);
+        for (int base = 0; base < n4; base += U * kGateThreads) {
+            float4 r[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int i = base + u * kGateThreads + (int)threadIdx.x;
+                if (i < n4) r[u] = src4[i];
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int i = base + u * kGateThreads + (int)threadIdx.x;
+                if (i < n4) dst4[i] = r[u];
+            }
+        }
+        done = n4 << 2;
+    }
+    for (int i = done + (int)threadIdx.x; i < n; i += kGateThreads) Ls[i] = src[i];
     __syncthreads();
     if (a.noise || a.zpart) {
         train_step(Ls, a, TT);
@@ -991,7 +1017,7 @@ cudaError_t launch_large(const moe_config &c, const XT *x, const float *w_t, con
     const size_t gbytes = ((size_t)64 * c.N + 64 * 8) * sizeof(float);
     e = cudaFuncSetAttribute(k_gate, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gbytes);
     if (e != cudaSuccess) return e;
-    return launch_pdl(k_gate, dim3(ra.tiles), dim3(256), gbytes, s, logits, ra);
+    return launch_pdl(k_gate, dim3(ra.tiles), dim3(kGateThreads), gbytes, s, logits, ra);
 }
 
 template <typename XT>
