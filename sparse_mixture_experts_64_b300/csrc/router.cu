@@ -25,7 +25,7 @@
 //   k_transpose_wr   router weight [d][N] -> chunk-major copy in the workspace, per
 //                    expert (k_router_small) or per expert pair (k_logits_large),
 //                    so that a lane's features of a block load as 16-byte runs.
-//   k_logits_large   N > 32: 32 tokens x 16 experts per CTA -> logits [T][N]; one
+//   k_logits_large   N > 32: 48 (bf16) or 32 (fp32) tokens x 16 experts per CTA -> logits [T][N]; one
 //                    packed fp32x2 fma updates two experts' partials (each half
 //                    rounds exactly like a scalar fma, so the order above holds).
 //   k_gate           N > 32: one warp per token: top-k, softmax, gates; per-tile stats.
@@ -1000,13 +1000,19 @@ cudaError_t launch_logits_only(const moe_config &c, const XT *x, const float *w_
     // backward's recomputed logits): 4 warps of 4 tokens x 8 experts, tile 16 x 8, so no
     // warp works on absent experts and twice as many CTAs share the tokens.
     if (c.N <= 8) return launch_logits_tile<XT, 4, 8, 4, 1>(c, x, w_t, b_r, has_bias, logits, err, s);
-    // Otherwise 8 warps of 8 tokens x 8 experts (0.75 bytes of shared memory read per
-    // FMA): 902 us for the DeepSeek-shaped router (T = 8192, d = 7168, N = 256) against
-    // 995 us with 16 warps of 4 x 8 (1.25 bytes per FMA), and 982-1001 us for 6 x 8,
-    // 8 x 4 and 4 x 8 tiles of 32 x 16; identical logits in every case. Packed fp32x2
-    // FMAs over expert pairs (half the FMA instructions, one 16-byte weight load per two
-    // features of two experts) took the same router from 902.7 to 890.4 us, same bits.
-    return launch_logits_tile<XT, 8, 8, 4, 2>(c, x, w_t, b_r, has_bias, logits, err, s);
+    // Otherwise warps of 8 tokens x 8 experts (0.75 bytes of shared memory read per FMA).
+    // With 8 warps (tile 32 x 16) this took 902 us for the DeepSeek-shaped router
+    // (T = 8192, d = 7168, N = 256) against 995 us with 16 warps of 4 x 8 (1.25 bytes per
+    // FMA) and 982-1001 us for 6 x 8, 8 x 4 and 4 x 8 warp tiles; packed fp32x2 FMAs over
+    // expert pairs then took it to 890 us. One CTA fits per SM, so its consumer warps are
+    // all the SM has: for bf16 tokens 12 warps (tile 48 tokens x 16 experts; 13 warps hold
+    // at most 128 registers a thread, a few bytes spill) run the whole router call in
+    // 795 us against 832 us with 8 (and 840 us with a 32 x 24 tile); identical logits.
+    // fp32 tokens keep 8 warps: a 48-token ring of fp32 rows does not fit in shared memory.
+    if constexpr (sizeof(XT) == 2)
+        return launch_logits_tile<XT, 8, 8, 6, 2>(c, x, w_t, b_r, has_bias, logits, err, s);
+    else
+        return launch_logits_tile<XT, 8, 8, 4, 2>(c, x, w_t, b_r, has_bias, logits, err, s);
 }
 
 template <typename XT>
