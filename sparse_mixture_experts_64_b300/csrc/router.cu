@@ -49,7 +49,7 @@ namespace moe {
 static int router_np(int N) { return N <= 4 ? 4 : N <= 8 ? 8 : N <= 16 ? 16 : 32; }
 
 int router_tile_tokens(const moe_config &c) {
-    if (c.N > 32) return 64;           // k_gate: 16 warps x 4 tokens
+    if (c.N > 32) return 64;           // k_gate: 32 warps x 2 tokens
     return 4 * (32 / router_np(c.N));  // k_router_small: 4 warps x (32 / NP) tokens
 }
 
@@ -215,20 +215,25 @@ __device__ __forceinline__ void gate_tokens_warp(float *Ls, int *Is, const Route
             const int e = lane + 32 * q;
             v[q] = e < N ? Ls[tok * N + e] : -INFINITY;
         }
-        unsigned taken = 0;
+        // Candidates still open: a copy of v with taken experts (and absent ones) at
+        // -inf. Logits are finite, so -inf never wins; a lane's experts rise with q, so
+        // keeping the first of equal values picks the lower index inside the lane, and
+        // the butterfly breaks ties between lanes by index.
+        float open[QMAX];
+#pragma unroll
+        for (int q = 0; q < QMAX; ++q) open[q] = v[q];
         float my_v = 0.0f, vmax = 0.0f;
         int my_e = 0;
         for (int s = 0; s < k; ++s) {
-            float bv = -INFINITY;
-            int bi = INT_MAX;
+            float bv = open[0];
+            int bq = 0;
 #pragma unroll
-            for (int q = 0; q < QMAX; ++q) {
-                const int e = lane + 32 * q;
-                if (e < N && !((taken >> q) & 1u) && (v[q] > bv || (v[q] == bv && e < bi))) {
-                    bv = v[q];
-                    bi = e;
+            for (int q = 1; q < QMAX; ++q)
+                if (open[q] > bv) {
+                    bv = open[q];
+                    bq = q;
                 }
-            }
+            int bi = bv == -INFINITY ? INT_MAX : lane + 32 * bq;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
                 const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
@@ -243,7 +248,9 @@ __device__ __forceinline__ void gate_tokens_warp(float *Ls, int *Is, const Route
                 my_v = bv;
                 my_e = bi;
             }
-            if (bi != INT_MAX && (bi & 31) == lane) taken |= 1u << (bi >> 5);
+            const int tq = (bi != INT_MAX && (bi & 31) == lane) ? (bi >> 5) : -1;  // taken here
+#pragma unroll
+            for (int q = 0; q < QMAX; ++q) open[q] = q == tq ? -INFINITY : open[q];
         }
         float part = 0.0f;
 #pragma unroll
@@ -643,11 +650,11 @@ __global__ void __launch_bounds__((TG * EG + 1) * 32, 1) k_logits_large(const __
         }
 }
 
-// One CTA = 16 warps, 64 tokens: logits tile -> shared memory -> gating -> stats.
+// One CTA = 32 warps, 64 tokens: logits tile -> shared memory -> gating -> stats.
 // The tile is one contiguous run of logits; it is loaded as 16-byte vectors with
 // every load of a thread in flight before the first store (one round trip to L2,
-// where the logits kernel left them), then each warp gates 4 tokens.
-constexpr int kGateThreads = 512;
+// where the logits kernel left them), then each warp gates 2 tokens.
+constexpr int kGateThreads = 1024;
 __global__ void __launch_bounds__(kGateThreads) k_gate(const float *__restrict__ logits, RouterArgs a) {
     constexpr int TT = 64, U = 8;
     extern __shared__ __align__(16) float smem[];
