@@ -13,6 +13,11 @@ Multi-GPU (torchrun, one process per GPU): every rank runs an independent replic
 of the layer on its own batch (the layer needs no exchange between replicas);
 the time is the max over ranks and `value` counts the tokens of all ranks.
 
+On one GPU the default run also measures the layer's other workloads (the
+DeepSeekMoE-shaped layer, Mixtral-shaped decode at T = 16, 64 and 128, Switch
+top-1 with capacity, tiny fp32) the same way, each under "workloads" in the same
+line, with its own oracle baseline on a bounded sample.
+
 Prints one JSON line on rank 0.
 """
 from __future__ import annotations
@@ -58,8 +63,19 @@ def _args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-variants", action="store_true",
-                    help="skip the training-router variant timing")
+                    help="skip the training-router and backward variant timing")
+    ap.add_argument("--workloads", default="auto", choices=["auto", "all", "none"],
+                    help="also measure the other workloads of the layer (auto: when the default "
+                         "workload runs on one GPU without overrides)")
+    ap.add_argument("--secondary-cpu-seconds", type=float, default=2.0,
+                    help="CPU seconds of the oracle baseline for each of the other workloads")
     return ap.parse_args()
+
+
+# The other workloads measured in the same run as the default one (one GPU): every
+# configuration the layer is specified on besides the Mixtral-shaped prefill layer.
+SECONDARY = ["deepseek_fine", "mixtral_decode_16", "mixtral_decode_64", "mixtral_decode_128",
+             "switch_top1", "tiny_fp32"]
 
 
 # --------------------------------------------------------------------------- helpers
@@ -232,11 +248,25 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def _blas_threads() -> int:
-    """Threads the oracle's float64 BLAS calls use (its C router is single-threaded)."""
+def _host_cores() -> int:
     try:
-        from threadpoolctl import threadpool_info
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+_BLAS_LIMIT = None
+
+
+def _blas_threads() -> int:
+    """Threads the oracle's float64 BLAS calls use: every host core this process may run
+    on (the oracle's C router runs on one thread)."""
+    global _BLAS_LIMIT
+    try:
+        from threadpoolctl import threadpool_info, threadpool_limits
         import numpy  # noqa: F401  (loads the BLAS so that it is listed)
+        if _BLAS_LIMIT is None:
+            _BLAS_LIMIT = threadpool_limits(limits=_host_cores(), user_api="blas")
         n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
         return max(n) if n else 1
     except Exception:
@@ -285,6 +315,57 @@ def time_oracle(w, host_inp, sample: int, seed: int) -> tuple[float, float]:
     else:
         O.forward(w, host_inp, tokens=toks)
     return time.perf_counter() - t0, n
+
+
+class _LazyExperts:
+    """Host float32 copies of the experts of a [N][...] device stack, fetched on first
+    use and kept (so that a timed oracle pass finds them already in host memory)."""
+
+    def __init__(self, t):
+        self.t, self.cache = t, {}
+
+    def __getitem__(self, e):
+        if e not in self.cache:
+            self.cache[e] = self.t[e].float().cpu().numpy()
+        return self.cache[e]
+
+
+def oracle_sample_baseline(w, inp, cpu_seconds: float) -> dict:
+    """The oracle on a bounded sample of workload `w`: a batch of the first n tokens
+    of the same layer (all of its steps: routing of the n tokens, their layer outputs),
+    n grown until one pass takes about `cpu_seconds`. The expert weights a pass needs
+    are fetched to host memory (float32) before it is timed."""
+    import numpy as np
+    from oracle import moe_oracle as O
+    threads = _blas_threads()
+    host = {"w_r": inp["w_r"].cpu().numpy(),
+            "b_r": None if inp["b_r"] is None else inp["b_r"].cpu().numpy()}
+    for nme in ("w_gate", "w_up", "w_down"):
+        host[nme] = None if inp[nme] is None else _LazyExperts(inp[nme])
+    for nme in ("shared_w_gate", "shared_w_up", "shared_w_down"):
+        host[nme] = None if inp[nme] is None else inp[nme].float().cpu().numpy()
+    x_all = inp["x"].float().cpu().numpy()
+
+    def one_pass(n):
+        wn = w.replace(T=n)
+        hn = dict(host, x=x_all[:n])
+        rt = O.route(wn, hn["x"], hn["w_r"], hn["b_r"])          # untimed: which experts to fetch
+        for e in np.unique(rt["topk_idx"]):
+            for nme in ("w_gate", "w_up", "w_down"):
+                if hn[nme] is not None:
+                    hn[nme][int(e)]
+        t0 = time.perf_counter()
+        O.forward(wn, hn)
+        return time.perf_counter() - t0
+
+    n, secs = 1, one_pass(1)
+    while secs < cpu_seconds and n < w.T:
+        n = min(w.T, max(n + 1, int(n * min(8.0, cpu_seconds / max(secs, 1e-3)))))
+        secs = one_pass(n)
+    return {"value": n / secs, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"one oracle pass over a batch of the first {n} tokens of the layer (routing and "
+                      f"layer outputs of all {n}) in {secs:.4f} s; fp32 router in C on one thread, "
+                      f"float64 numpy elsewhere on {threads} BLAS thread(s)"}
 
 
 def run_reference(a, w, world, rank):
@@ -436,7 +517,10 @@ def measure_backward(w, inp, cfg, ws, stream, dev, peaks, host_inp=None, cpu_tok
 
 # ------------------------------------------------------------------------ GPU arm
 
-def run_ours(a, w, world, rank, local):
+def measure(a, w, world, rank, local, primary: bool = True) -> dict:
+    """Time the layer forward of workload `w` (the bench contract's step) and return its
+    JSON record. primary: the headline workload, with the router/backward variants and
+    the full oracle baseline; otherwise a bounded oracle sample and no variants."""
     import sparse_mixture_experts_64_b300 as moe
 
     torch.cuda.set_device(local)
@@ -699,18 +783,22 @@ def run_ours(a, w, world, rank, local):
         # stage-event graph of the same kernels
         "gpu_launches": launches_per_forward(w) * a.steps * (2 if stage_from_graphs else 1),
         "clocks": clk, "wall_s_timed": wall,
+        # expert weights that received rows (+ shared + router) per forward, over the step time
+        "weight_stream_gbs": weight_bytes_hit(w, counts_kept) / (ms_max / 1e3) / 1e9,
     }
 
     # ---- training-time router variant (noisy top-k + z-loss), same inputs
     cpu = rank == 0 and world == 1 and not a.no_cpu_baseline
-    host_inp = _oracle_inputs(inp, w) if cpu else None
-    if not a.no_variants and not ec:
+    host_inp = _oracle_inputs(inp, w) if cpu and primary else None
+    if primary and not a.no_variants and not ec:
         line["variants"] = {"router_train": measure_router_train(w, inp, cfg, ws, stream, dev, 512 if cpu else 0)}
         if w.dtype == "bf16":
             line["variants"]["backward"] = measure_backward(w, inp, cfg, ws, stream, dev, peaks, host_inp)
 
     # ---- CPU oracle baseline (rank 0, single process only)
-    if cpu:
+    if cpu and not primary:
+        line["cpu_baseline"] = oracle_sample_baseline(w, inp, a.secondary_cpu_seconds)
+    elif cpu:
         # passes of the oracle (each: routing of all tokens, outputs of a new random
         # sample) until about --cpu-seconds of CPU time, at most 200 passes
         secs, n, passes = 0.0, 0, 0
@@ -721,7 +809,36 @@ def run_ours(a, w, world, rank, local):
             "value": n / secs, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
             "sample": f"{passes} pass(es), each routing all {T} tokens and computing the layer outputs of "
                       f"{min(a.cpu_sample, T)} random tokens: {n} outputs in {secs:.1f} s "
-                      f"(fp32 router in C, float64 numpy elsewhere)"}
+                      f"(fp32 router in C on one thread, float64 numpy elsewhere on "
+                      f"{_blas_threads()} BLAS thread(s))"}
+    return line
+
+
+def _summary(sub: dict) -> dict:
+    """The fields of a secondary workload's record kept in the headline line."""
+    keep = ("value", "unit", "ms_per_step", "dtype", "config", "layer_roofline", "stages_ms",
+            "weight_stream_gbs", "rows_dispatched", "gpu_launches", "clocks", "cpu_baseline", "e2e",
+            "stream_launch_ms_per_step")
+    out = {k: sub[k] for k in keep if k in sub}
+    r = sub["roofline"]
+    out["roofline"] = {k: r[k] for k in ("kernel", "bound", "achieved", "peak", "unit", "frac", "traffic",
+                                         "peak_source", "avg_launch_ms", "algorithmic_flops_per_launch",
+                                         "algorithmic_bytes_per_launch", "traffic_over_algorithmic")
+                       if k in r}
+    return out
+
+
+def run_ours(a, w, world, rank, local, secondary: bool):
+    line = measure(a, w, world, rank, local, primary=True)
+    if secondary:
+        import gc
+        line["workloads"] = {}
+        for name in SECONDARY:
+            if name == w.name:
+                continue
+            gc.collect()
+            torch.cuda.empty_cache()
+            line["workloads"][name] = _summary(measure(a, W.WORKLOADS[name], world, rank, local, primary=False))
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -729,6 +846,7 @@ def run_ours(a, w, world, rank, local):
 def main():
     a = _args()
     world, rank, local = _dist()
+    _blas_threads()  # the oracle's BLAS on every host core, before any oracle leg runs
     w = W.WORKLOADS[a.config]
     over = {k: v for k, v in (("T", a.tokens), ("N", a.experts), ("h", a.hidden)) if v}
     if over:
@@ -736,7 +854,11 @@ def main():
     if a.impl == "reference":
         run_reference(a, w, world, rank)
     else:
-        run_ours(a, w, world, rank, local)
+        # the other workloads join the default run on one GPU (a scaling run times the
+        # default workload alone)
+        secondary = a.workloads == "all" or (a.workloads == "auto" and a.config == "mixtral_prefill"
+                                             and not over and world == 1)
+        run_ours(a, w, world, rank, local, secondary)
     if world > 1:
         torch.distributed.destroy_process_group()
 

@@ -112,6 +112,13 @@ typedef struct {
 #define MOE_DEBUG_FFN_SWAP 8u        /* bf16: use the weights-as-M CTA-pair kernel (token tiles 32..256) */
 #define MOE_DEBUG_NO_PDL 16u         /* moe_forward: launch every kernel only after its predecessor has
                                         completed (no programmatic dependent launch)             */
+#define MOE_DEBUG_ROUTER_STALL 32u   /* exercises the timeout path of the bounded waits: the router
+                                        kernel for N <= 32 (token choice) copies nothing into its
+                                        staging ring and its waits give up after about 1 ms, so the
+                                        call records MOE_ERR_TIMEOUT (read by moe_check_error) with
+                                        no copy in flight. Every output of the call is then
+                                        meaningless (later kernels of the call still check every
+                                        index they read). Ignored for N > 32.                      */
 /* Without these flags bf16 experts run on the row-tile pair kernel when the row buffers hold at
    least 224 rows per expert, else on the row-tile single-CTA kernel; the backward's weight
    gradients run on CTA pairs when the gradient has at least 256 rows. */
@@ -123,6 +130,12 @@ moe_status moe_validate_config(const moe_config *cfg);
  * 0 when the config is invalid. No CUDA call is made. */
 size_t moe_workspace_size(const moe_config *cfg);
 
+/* Bytes of workspace the router calls need for `cfg` (moe_router_topk,
+ * moe_router_topk_train, moe_router_shard_stats / _assign): the leading part of
+ * the full workspace, smaller than moe_workspace_size(cfg). 0 when the config is
+ * invalid or uses Expert Choice routing. No CUDA call is made. */
+size_t moe_router_workspace_size(const moe_config *cfg);
+
 /* Worst-case dispatched row count R_max for `cfg` (see above); 0 if invalid. */
 int64_t moe_max_rows(const moe_config *cfg);
 
@@ -132,11 +145,21 @@ int32_t moe_capacity(const moe_config *cfg);
 /*
  * Router: logits, gating, counts, capacity and dispatch order.
  *
- * logits L[t][e] = sum_i x[t][i] * w_r[i][e] (+ b_r[e]) in fp32, accumulated from
- * 0 with one fused multiply-add per feature i in increasing order ("Noise Top-k
+ * logits L[t][e] = sum_i x[t][i] * w_r[i][e] (+ b_r[e]) in fp32 ("Noise Top-k
  * Gating" router paragraph; "Router: Selecting Experts ..." Figure 2; Switch
- * explainer "Making it work" for the fp32 router). Top-k by logit, largest first,
- * lower expert index first on equal logits. Gates per cfg->gating.
+ * explainer "Making it work" for the fp32 router), summed in one fixed order so
+ * that the routing is reproducible bit for bit:
+ *   - the features are taken in blocks of 8 (block b = features 8b .. 8b+7);
+ *   - partial sum l (l = 0 .. 31) starts at 0 and takes every block b with
+ *     b mod 32 = l, in increasing b, with one correctly rounded fused
+ *     multiply-add per feature in increasing feature order;
+ *   - the 32 partials are combined by five pairwise rounds
+ *     p_l <- p_l + p_(l xor o) for o = 16, 8, 4, 2, 1 (each sum rounded to fp32),
+ *     and the logit is p_0;
+ *   - the bias, when present, is added last (one fp32 addition).
+ * Top-k by logit, largest first, lower expert index first on equal logits (-0 and
+ * +0 are equal); a NaN logit ranks below every number and is chosen only when
+ * fewer than k experts have a numeric logit. Gates per cfg->gating.
  * Capacity (glossary capacity paragraph; Switch "Making it work"): when set, an
  * expert keeps at most C slots, chosen slot-major (every token's first choice in
  * token order, then every second choice, ...); dropped slots get slot_row = -1
@@ -275,20 +298,30 @@ moe_status moe_combine_expert_choice(const moe_config *cfg, const void *x, const
  * Same computation, arguments and outputs as moe_router_topk, without the
  * workspace: the router's scratch lives in one static 32 MiB device array of the
  * library, held by every GPU that loads it until the process exits. Configs whose
- * router scratch would exceed 32 MiB are rejected with MOE_ERR_UNSUPPORTED before
- * anything is enqueued (the tiny, Switch, Mixtral and DeepSeekMoE-shaped layers
- * all fit). Nothing is allocated and no allocating routine is called.
+ * router scratch (moe_router_workspace_size) exceeds 32 MiB are rejected with
+ * MOE_ERR_UNSUPPORTED before anything is enqueued (the tiny, Switch, Mixtral and
+ * DeepSeekMoE-shaped layers all fit). Nothing is allocated and no allocating
+ * routine is called.
  * The first call on a device looks up the array's device address (make that first
  * call before any stream capture). All calls share the array: the error word in
- * it is cleared at the start of each call and is not readable through
- * moe_check_error; calls that overlap on the GPU race on the array and must be
- * serialised by the caller.
+ * it is cleared at the start of each call and is read with
+ * moe_router_noalloc_check_error, not moe_check_error; calls that overlap on the
+ * GPU race on the array and must be serialised by the caller.
  */
 moe_status moe_router_topk_noalloc(const moe_config *cfg, const void *x, const float *w_r,
                                    const float *b_r, int32_t *topk_idx, float *topk_gate,
                                    int32_t *counts_routed, int32_t *counts_kept,
                                    int32_t *expert_offsets, int32_t *slot_row,
                                    int32_t *perm_token, float *aux, cudaStream_t stream);
+
+/*
+ * Device error word of moe_router_topk_noalloc on the current device: synchronises
+ * `stream`, reads and clears the word, and returns MOE_OK, MOE_ERR_TIMEOUT (a bounded
+ * wait ran out: that call's outputs are not written), MOE_ERR_DEVICE_FAULT or
+ * MOE_ERR_CUDA. The word covers the calls made since the last call started (each
+ * call clears it first), so read it after the call it is meant to check.
+ */
+moe_status moe_router_noalloc_check_error(cudaStream_t stream);
 
 /*
  * Dispatch: x_perm[r] = x[perm_token[r]] for r < expert_offsets[N]

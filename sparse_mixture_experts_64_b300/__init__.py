@@ -28,6 +28,7 @@ MOE_DEBUG_FFN_PAIR = 2
 MOE_DEBUG_FFN_SINGLE = 4
 MOE_DEBUG_FFN_SWAP = 8
 MOE_DEBUG_NO_PDL = 16
+MOE_DEBUG_ROUTER_STALL = 32
 
 EXPORTED = ("moe_validate_config", "moe_workspace_size", "moe_max_rows", "moe_capacity",
             "moe_router_topk", "moe_dispatch", "moe_grouped_ffn", "moe_combine", "moe_forward",
@@ -35,7 +36,8 @@ EXPORTED = ("moe_validate_config", "moe_workspace_size", "moe_max_rows", "moe_ca
             "moe_router_topk_train", "moe_router_shard_stats", "moe_router_shard_assign",
             "moe_router_expert_choice", "moe_combine_expert_choice", "moe_backward",
             "moe_backward_workspace_size", "moe_forward_graph_create", "moe_forward_graph_launch",
-            "moe_forward_graph_destroy")
+            "moe_forward_graph_destroy", "moe_router_workspace_size",
+            "moe_router_noalloc_check_error")
 
 
 class moe_config(ctypes.Structure):
@@ -61,6 +63,8 @@ def _load() -> ctypes.CDLL:
     sig = {
         "moe_validate_config": (I32, [cfgp]),
         "moe_workspace_size": (SZ, [cfgp]),
+        "moe_router_workspace_size": (SZ, [cfgp]),
+        "moe_router_noalloc_check_error": (I32, [P]),
         "moe_max_rows": (I64, [cfgp]),
         "moe_capacity": (I32, [cfgp]),
         "moe_router_topk": (I32, [cfgp] + [P] * 11 + [P, SZ, P]),
@@ -147,6 +151,10 @@ def moe_validate_config(cfg) -> int:
 
 def moe_workspace_size(cfg) -> int:
     return _lib.moe_workspace_size(ctypes.byref(cfg))
+
+
+def moe_router_workspace_size(cfg) -> int:
+    return _lib.moe_router_workspace_size(ctypes.byref(cfg))
 
 
 def moe_max_rows(cfg) -> int:
@@ -259,6 +267,12 @@ def moe_router_topk_noalloc(cfg, x, w_r, b_r, topk_idx, topk_gate, counts_routed
                                         _p(topk_gate), _p(counts_routed), _p(counts_kept),
                                         _p(expert_offsets), _p(slot_row), _p(perm_token), _p(aux),
                                         _stream(stream)), "moe_router_topk_noalloc")
+
+
+def moe_router_noalloc_check_error(stream=None) -> int:
+    """Synchronise the stream, read and clear the error word of the no-allocation router
+    on the current device (the status, not raised)."""
+    return _lib.moe_router_noalloc_check_error(_stream(stream))
 
 
 def moe_dispatch(cfg, x, perm_token, expert_offsets, x_perm, ws=None, stream=None):

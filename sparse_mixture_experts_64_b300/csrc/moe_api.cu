@@ -177,6 +177,11 @@ size_t moe_workspace_size(const moe_config *cfg) {
     return ws_layout(*cfg).total;
 }
 
+size_t moe_router_workspace_size(const moe_config *cfg) {
+    if (validate(cfg) != MOE_OK || cfg->routing != MOE_ROUTING_TOKEN_CHOICE) return 0;
+    return ws_layout(*cfg).hid;
+}
+
 int64_t moe_max_rows(const moe_config *cfg) {
     if (validate(cfg) != MOE_OK) return 0;
     return max_rows(*cfg);

@@ -69,3 +69,21 @@ extern "C" moe_status moe_router_topk_noalloc(const moe_config *cfg, const void 
     const cudaError_t e = moe::launch_router(c, x, w_r, c.has_router_bias ? b_r : nullptr, o, scratch, stream);
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
+
+// The device error word of the static array (the first word of the router's scratch
+// for every config): bounded waits that ran out and out-of-range indices of the calls
+// since the last call started. A caller without a workspace has no other way to see
+// them, and a call whose wait ran out has unwritten outputs.
+extern "C" moe_status moe_router_noalloc_check_error(cudaStream_t stream) {
+    uint8_t *scratch = nullptr;
+    moe_status st = scratch_of_current_device(&scratch);
+    if (st != MOE_OK) return st;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+    static_assert(sizeof(uint32_t) <= kNoAllocScratchBytes, "error word inside the array");
+    uint32_t word = 0;
+    if (cudaMemcpy(&word, scratch, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    if (word && cudaMemset(scratch, 0, sizeof(word)) != cudaSuccess) return MOE_ERR_CUDA;
+    if (word & moe::kErrTimeout) return MOE_ERR_TIMEOUT;
+    if (word & moe::kErrFault) return MOE_ERR_DEVICE_FAULT;
+    return MOE_OK;
+}

@@ -56,6 +56,9 @@ int router_tile_tokens(const moe_config &c) {
 namespace {
 
 constexpr uint64_t kWaitNs = 1000000000ull;  // bound of every mbarrier wait (1 s)
+// Bound of the waits of k_router_small under MOE_DEBUG_ROUTER_STALL (1 ms): its producer
+// then issues no copy, so the consumers' first wait runs out with nothing in flight.
+constexpr uint64_t kStallWaitNs = 1000000ull;
 
 struct RouterArgs {
     int T, d, N, k, gating, tiles, has_bias;
@@ -69,6 +72,7 @@ struct RouterArgs {
     const float *noise = nullptr;
     float noise_w = 0.0f;
     float *zpart = nullptr;
+    int stall = 0;  // MOE_DEBUG_ROUTER_STALL (k_router_small only)
 };
 
 // 8 consecutive features of one token as fp32 (16 bytes of bf16, 32 of fp32).
@@ -95,12 +99,13 @@ __device__ __forceinline__ float butterfly32(float v) {
 
 // Bounded wait for phase `par` of `bar`; on expiry sets *abort_flag and records
 // MOE_ERR_TIMEOUT. Returns false if the wait ran out or another thread aborted.
-__device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t par, int *abort_flag, uint32_t *err) {
+__device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t par, int *abort_flag, uint32_t *err,
+                                           uint64_t limit_ns = kWaitNs) {
     if (tc::mbar_try_wait(bar, par)) return true;
     const uint64_t t0 = tc::globaltimer_ns();
     while (!tc::mbar_try_wait(bar, par)) {
         if (*(volatile int *)abort_flag) return false;
-        if (tc::globaltimer_ns() - t0 > kWaitNs) {
+        if (tc::globaltimer_ns() - t0 > limit_ns) {
             *(volatile int *)abort_flag = 1;
             record_error(err, kErrTimeout);
             return false;
@@ -110,6 +115,25 @@ __device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t par, int *abo
 }
 
 // ------------------------------------------------------------------ gating
+
+// Selection key of a logit: the fp32 order as a signed integer, with -0 equal to +0,
+// a NaN below every number (-inf included), and taken or absent experts below that.
+// For numeric logits the larger key is the larger logit, so selecting the largest key,
+// lower expert index first on equal keys, is selection by logit; a NaN logit (a NaN in
+// the token or the router weight) is chosen only when no numeric logit is left, and
+// every token still gets k distinct experts.
+constexpr int kKeyNaN = INT_MIN + 1;
+constexpr int kKeyNone = INT_MIN;
+__device__ __forceinline__ int sel_key(float v) {
+    if (v != v) return kKeyNaN;
+    const int b = __float_as_int(__fadd_rn(v, 0.0f));  // -0 + 0 = +0
+    return b >= 0 ? b : b ^ 0x7fffffff;
+}
+// The logit of a numeric key (+0 for a zero logit), NaN for kKeyNaN.
+__device__ __forceinline__ float key_value(int key) {
+    if (key == kKeyNaN) return __int_as_float(0x7fc00000);
+    return __int_as_float(key >= 0 ? key : key ^ 0x7fffffff);
+}
 
 // Per-tile statistics from p (Ls) and the selections (Is): per expert, the sum of
 // p over the tile's tokens and the number of tokens choosing it in each slot.
@@ -146,21 +170,25 @@ __device__ __forceinline__ void gate_tokens_thread(float *Ls, int *Is, const Rou
             continue;
         }
         float Lr[NP];
+        int key[NP];
 #pragma unroll
-        for (int e = 0; e < NP; ++e) Lr[e] = e < N ? L[e] : 0.0f;
-        uint32_t taken = 0;
+        for (int e = 0; e < NP; ++e) {
+            Lr[e] = e < N ? L[e] : 0.0f;
+            key[e] = e < N ? sel_key(Lr[e]) : kKeyNone;
+        }
         float vmax = 0.0f, den = 0.0f;
         for (int s = 0; s < k; ++s) {
-            float bv = -INFINITY;
-            int bi = -1;
+            // an untaken expert of this token has a key above kKeyNone (k <= N)
+            int bk = kKeyNone, bi = 0;
 #pragma unroll
             for (int e = 0; e < NP; ++e)  // ascending e, strict '>': lowest index wins ties
-                if (e < N && !((taken >> e) & 1u) && (bi < 0 || Lr[e] > bv)) {
-                    bv = Lr[e];
+                if (key[e] > bk) {
+                    bk = key[e];
                     bi = e;
                 }
-            taken |= 1u << bi;
-            if (s == 0) vmax = bv;
+#pragma unroll
+            for (int e = 0; e < NP; ++e) key[e] = e == bi ? kKeyNone : key[e];
+            if (s == 0) vmax = key_value(bk);
             Is[tok * 8 + s] = bi;
         }
         float sum = 0.0f;
@@ -215,42 +243,44 @@ __device__ __forceinline__ void gate_tokens_warp(float *Ls, int *Is, const Route
             const int e = lane + 32 * q;
             v[q] = e < N ? Ls[tok * N + e] : -INFINITY;
         }
-        // Candidates still open: a copy of v with taken experts (and absent ones) at
-        // -inf. Logits are finite, so -inf never wins; a lane's experts rise with q, so
-        // keeping the first of equal values picks the lower index inside the lane, and
-        // the butterfly breaks ties between lanes by index.
-        float open[QMAX];
+        // Candidates still open: the selection keys of v, taken and absent experts at
+        // kKeyNone. An untaken expert's key is above kKeyNone (k <= N), so the winner
+        // is always a real expert; a lane's experts rise with q, so keeping the first
+        // of equal keys picks the lower index inside the lane, and the butterfly
+        // breaks ties between lanes by index.
+        int open[QMAX];
 #pragma unroll
-        for (int q = 0; q < QMAX; ++q) open[q] = v[q];
+        for (int q = 0; q < QMAX; ++q) open[q] = lane + 32 * q < N ? sel_key(v[q]) : kKeyNone;
         float my_v = 0.0f, vmax = 0.0f;
         int my_e = 0;
         for (int s = 0; s < k; ++s) {
-            float bv = open[0];
+            int bk = open[0];
             int bq = 0;
 #pragma unroll
             for (int q = 1; q < QMAX; ++q)
-                if (open[q] > bv) {
-                    bv = open[q];
+                if (open[q] > bk) {
+                    bk = open[q];
                     bq = q;
                 }
-            int bi = bv == -INFINITY ? INT_MAX : lane + 32 * bq;
+            int bi = bk == kKeyNone ? INT_MAX : lane + 32 * bq;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int ok = __shfl_xor_sync(0xffffffffu, bk, o);
                 const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-                if (ov > bv || (ov == bv && oi < bi)) {
-                    bv = ov;
+                if (ok > bk || (ok == bk && oi < bi)) {
+                    bk = ok;
                     bi = oi;
                 }
             }
+            const float bv = key_value(bk);
             if (s == 0) vmax = bv;
             if (lane == s) {
                 my_v = bv;
                 my_e = bi;
             }
-            const int tq = (bi != INT_MAX && (bi & 31) == lane) ? (bi >> 5) : -1;  // taken here
+            const int tq = (bi & 31) == lane ? (bi >> 5) : -1;  // taken here
 #pragma unroll
-            for (int q = 0; q < QMAX; ++q) open[q] = q == tq ? -INFINITY : open[q];
+            for (int q = 0; q < QMAX; ++q) open[q] = q == tq ? kKeyNone : open[q];
         }
         float part = 0.0f;
 #pragma unroll
@@ -347,8 +377,8 @@ struct Ring {
         return wait_phase(&empty[c % STAGES], (uint32_t)((c / STAGES - 1) & 1), &abort_flag, err);
     }
     // consumer: wait until chunk c has landed
-    __device__ bool ready(int c, uint32_t *err) {
-        return wait_phase(&full[c % STAGES], (uint32_t)((c / STAGES) & 1), &abort_flag, err);
+    __device__ bool ready(int c, uint32_t *err, uint64_t limit_ns = kWaitNs) {
+        return wait_phase(&full[c % STAGES], (uint32_t)((c / STAGES) & 1), &abort_flag, err, limit_ns);
     }
     // consumer warp: done reading chunk c
     __device__ void release(int c) {
@@ -462,9 +492,12 @@ __global__ void __launch_bounds__(160) k_router_small(const __grid_constant__ CU
 #pragma unroll
         for (int e = 0; e < NP; ++e) acc[i][e] = 0.0f;
 
+    // MOE_DEBUG_ROUTER_STALL: the producer issues nothing and the consumers' first wait
+    // gives up after kStallWaitNs (records MOE_ERR_TIMEOUT; no copy is in flight)
+    const uint64_t wait_ns = a.stall ? kStallWaitNs : kWaitNs;
     if (warp == NW) {
         // ---- producer (lane 0)
-        if (lane == 0) {
+        if (lane == 0 && !a.stall) {
             int issued = 0;
             for (int c = 0; c < nchunks; ++c) {
                 if (!ring.acquire(c, a.err)) break;
@@ -481,7 +514,7 @@ __global__ void __launch_bounds__(160) k_router_small(const __grid_constant__ CU
     } else {
         // ---- consumers
         for (int c = 0; c < nchunks; ++c) {
-            if (!ring.ready(c, a.err)) break;
+            if (!ring.ready(c, a.err, wait_ns)) break;
             const uint8_t *slot = sb + (size_t)(c % STAGES) * STAGE;
             const int nb = min(NBLK, nblocks - c * NBLK);
             if (lane < nb) {
@@ -1134,6 +1167,7 @@ cudaError_t launch_router(const moe_config &c, const void *x, const float *w_r, 
     float *zpart = o.z_loss ? reinterpret_cast<float *>(ws + L.zpart) : nullptr;
     RouterArgs ra{c.T, c.d, c.N, c.k, c.gating, tiles, c.has_router_bias ? 1 : 0,
                   o.topk_idx, o.topk_gate, cnt, psum, err, o.noise, o.noise_w, zpart};
+    ra.stall = (c.debug_flags & MOE_DEBUG_ROUTER_STALL) ? 1 : 0;
     cudaError_t e;
     if (c.dtype == MOE_BF16)
         e = launch_logits_gate<__nv_bfloat16>(c, static_cast<const __nv_bfloat16 *>(x), w_r, b_r, ra, logits, w_t, s);

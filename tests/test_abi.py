@@ -71,6 +71,13 @@ def test_valid_configs_and_sizes():
     assert moe.moe_max_rows(sw) == 4096
     sw2 = moe.make_config(T=4096, d=768, N=8, k=2, h=3072, capacity_factor=(1, 2))
     assert moe.moe_capacity(sw2) == 256 and moe.moe_max_rows(sw2) == 8 * 256
+    # the router calls need only the leading part of the workspace
+    assert 0 < moe.moe_router_workspace_size(c) < moe.moe_workspace_size(c)
+    ds = moe.make_config(T=8192, d=7168, N=256, k=8, h=2048, h_shared=2048, gating="softmax_then_topk")
+    assert moe.moe_router_workspace_size(ds) <= 32 << 20
+    ec = moe.make_config(T=64, d=128, N=8, k=2, h=256, capacity_factor=(2, 1), routing="expert_choice")
+    assert moe.moe_router_workspace_size(ec) == 0
+    assert moe.moe_router_workspace_size(_cfg(T=0)) == 0
     tiny = moe.make_config(T=256, d=64, N=4, k=2, h=128, dtype="f32")
     assert moe.moe_validate_config(tiny) == moe.MOE_OK
     assert moe.status_str(moe.MOE_ERR_TIMEOUT) == "MOE_ERR_TIMEOUT"

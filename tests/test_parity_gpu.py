@@ -1,8 +1,9 @@
 """Parity of the CUDA path (through the C ABI) with the CPU oracle.
 
 Small and ragged shapes are compared element by element on every output; the
-full-size workloads are compared bit-exactly on all routing outputs and on the
-layer output of a seeded token sample."""
+full-size workloads are compared bit-exactly on all routing outputs, on the layer
+output of a seeded token sample, and on the expert outputs of rows drawn from every
+128-row block of every expert."""
 import numpy as np
 import pytest
 import torch
@@ -202,14 +203,51 @@ def test_dispatch_rejects_out_of_range_token():
 
 # ------------------------------------------------------------ full-size workloads
 
-FULL = [("switch_top1", None), ("mixtral_decode_16", None), ("mixtral_decode_128", 24),
-        ("mixtral_prefill", 16), ("deepseek_fine", 8)]
+FULL = [("switch_top1", None), ("mixtral_decode_16", None), ("mixtral_decode_64", None),
+        ("mixtral_decode_128", 24), ("mixtral_prefill", 16), ("deepseek_fine", 8)]
+
+
+def _expert_block_rows(offsets, rng):
+    """Dispatched rows to check: one random row of every 128-row block of every
+    expert (the tiles of both tensor-core kernels: 256-row pair tiles and 128-row
+    single-CTA tiles) and every expert's last row (its last, partial block)."""
+    rows = []
+    for e in range(len(offsets) - 1):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        for b0 in range(lo, hi, 128):
+            rows.append(int(rng.integers(b0, min(b0 + 128, hi))))
+        if hi > lo:
+            rows.append(hi - 1)
+    return np.array(sorted(set(rows)), dtype=np.int64)
+
+
+def check_expert_rows(w, inp, sep, rng):
+    """Expert outputs y_perm of sampled rows of every expert against the oracle's
+    FFN_e of the row's token (the DeepSeekMoE layer equation's FFN_i for every expert
+    with a non-zero gate), element by element at the layer tolerance."""
+    oi = oracle_inputs(inp)
+    off, perm = sep["expert_offsets"], sep["perm_token"]
+    rows = _expert_block_rows(off, rng)
+    got, ref = [], []
+    for e in range(w.N):
+        r = rows[(rows >= off[e]) & (rows < off[e + 1])]
+        if r.size == 0:
+            continue
+        xr = oi["x"][perm[r]]
+        ref.append(O.expert_ffn(xr, oi["w_gate"][e], None if oi["w_up"] is None else oi["w_up"][e],
+                                oi["w_down"][e], w.act))
+        got.append(sep["y_perm"][r])
+    experts_hit = int(np.count_nonzero(np.diff(off)))
+    assert len(ref) == experts_hit
+    check_output(np.concatenate(got), np.concatenate(ref), w.dtype)
+    return rows.size, experts_hit
 
 
 @pytest.mark.parametrize("name,sample", FULL, ids=[n for n, _ in FULL])
 def test_full_size_parity(name, sample):
     """Full-size layer as the benchmark runs it (moe_forward, one call): routing,
-    counts and aux bit-exact / toleranced over all tokens; outputs on a sample."""
+    counts and aux bit-exact / toleranced over all tokens; layer outputs on a token
+    sample; expert outputs of every expert on rows drawn from each of its blocks."""
     w = W.WORKLOADS[name]
     inp = W.make_inputs(w, device="cuda")
     cfg = cfg_of(w)
@@ -225,6 +263,7 @@ def test_full_size_parity(name, sample):
     ysel = fwd["y"] if tokens is None else fwd["y"][tokens]
     check_output(ysel, rt["y"], w.dtype)
     assert np.array_equal(fwd["y"], sep["y"])
+    check_expert_rows(w, inp, sep, rng)
 
 
 # One expert takes every token, so its row count is T: the pair kernel's last block
