@@ -268,13 +268,17 @@ def test_full_size_parity(name, sample):
 
 # One expert takes every token, so its row count is T: the pair kernel's last block
 # holds T mod 256 rows, handled as a tile with the tokens on the MMA's N side (1, 32,
-# 33, 128, 129, 255 rows), or none (T = 768); below 512 rows the experts with a short
-# last block move to the single-CTA kernel (T = 300) and the others keep the pair
-# kernel's tail tile (T = 400). Gated, ReLU and shared-expert variants.
-TAILS = [_small("mixtral_prefill", T=t, d=128, h=256, N=1, k=1) for t in (513, 544, 545, 640, 641, 767, 768,
-                                                                          300, 400)]
+# 33, 49, 128, 129, 255 rows), or none (T = 768); below 512 rows the experts with a
+# short last block move to the single-CTA kernel (T = 300, 304, 305) and the others
+# keep the pair kernel's tail tile (T = 400). Gated, ReLU and shared-expert variants.
+TAILS = [_small("mixtral_prefill", T=t, d=128, h=256, N=1, k=1) for t in (513, 544, 545, 561, 640, 641, 767, 768,
+                                                                          300, 304, 305, 400)]
 TAILS += [_small("switch_top1", T=t, d=128, h=384, N=1, k=1, capacity_factor=None) for t in (545, 767)]
 TAILS += [_small("deepseek_fine", T=t, d=128, N=1, k=1, h=128, h_shared=128) for t in (545, 767)]
+# About 272 rows per expert (most experts just over one 256-row block, as in the
+# DeepSeekMoE-shaped layer): both launches of the split, several tiles per CTA pair.
+TAILS += [_small("deepseek_fine", T=4352, d=128, N=32, k=2, h=1024, h_shared=0),
+          _small("switch_top1", T=2176, d=128, h=2048, N=8, k=1, capacity_factor=None)]
 
 
 @pytest.mark.parametrize("w", TAILS, ids=[w.name for w in TAILS])
