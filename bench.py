@@ -36,6 +36,18 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+
+def _host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+# The CPU oracle's float64 numpy work runs on every core this process may use: the
+# BLAS pool size is fixed when numpy's OpenBLAS loads, so it is set before the import.
+os.environ.setdefault("OPENBLAS_NUM_THREADS", str(_host_cores()))
+
 import torch  # noqa: E402
 
 import workloads as W  # noqa: E402
@@ -248,28 +260,21 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def _host_cores() -> int:
-    try:
-        return len(os.sched_getaffinity(0))
-    except (AttributeError, OSError):
-        return os.cpu_count() or 1
-
-
-_BLAS_LIMIT = None
-
-
 def _blas_threads() -> int:
-    """Threads the oracle's float64 BLAS calls use: every host core this process may run
-    on (the oracle's C router runs on one thread)."""
-    global _BLAS_LIMIT
+    """Threads the oracle's float64 BLAS calls use (its C router runs on one thread):
+    the pool's size as threadpoolctl reports it, else the OPENBLAS_NUM_THREADS that
+    numpy's OpenBLAS read when it loaded."""
     try:
-        from threadpoolctl import threadpool_info, threadpool_limits
+        from threadpoolctl import threadpool_info
         import numpy  # noqa: F401  (loads the BLAS so that it is listed)
-        if _BLAS_LIMIT is None:
-            _BLAS_LIMIT = threadpool_limits(limits=_host_cores(), user_api="blas")
         n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
-        return max(n) if n else 1
-    except Exception:
+        if n:
+            return max(n)
+    except ImportError:
+        pass
+    try:
+        return max(1, int(os.environ.get("OPENBLAS_NUM_THREADS", "1")))
+    except ValueError:
         return 1
 
 
@@ -846,7 +851,6 @@ def run_ours(a, w, world, rank, local, secondary: bool):
 def main():
     a = _args()
     world, rank, local = _dist()
-    _blas_threads()  # the oracle's BLAS on every host core, before any oracle leg runs
     w = W.WORKLOADS[a.config]
     over = {k: v for k, v in (("T", a.tokens), ("N", a.experts), ("h", a.hidden)) if v}
     if over:
