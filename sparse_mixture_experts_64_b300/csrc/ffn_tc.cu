@@ -57,6 +57,7 @@ template <int KIND> constexpr int kOutLd = KIND == KIND_PREACT ? 2 : 1;  // outp
 
 struct TcParams {
     CUtensorMap tmA, tmA_sh;       // [rows][K], box 64 x 128
+    CUtensorMap tmA64, tmA64_sh;   // the same arrays, box 64 x 64 (single-CTA half tiles)
     CUtensorMap tmB0, tmB1;        // routed weights [n_seg][n_out][K], box 64 x (128|256) x 1
     CUtensorMap tmB0_sh, tmB1_sh;  // shared weights [n_out_sh][K_sh], box 64 x (128|256)
     const int32_t *offsets;
@@ -197,6 +198,12 @@ __device__ __forceinline__ void epilogue_row(uint32_t tbase, __nv_bfloat16 *crow
     }
 }
 
+// A single-CTA tile whose 128-row block holds at most 64 rows of its segment (a segment's
+// last block) runs one M = 64 MMA per k-step on a 64-row A tile: half the tensor work and
+// half the A bytes. The M = 64 accumulator puts row r in TMEM lane 32 (r / 16) + r % 16,
+// so epilogue warp q holds rows 16 q .. 16 q + 15 in its lanes 0-15.
+__device__ __forceinline__ bool half_tile(int rows_left) { return rows_left <= BM / 2; }
+
 template <int KIND>
 __global__ void __launch_bounds__(NUM_THREADS, 1) k_ffn_tc(const __grid_constant__ TcParams p) {
     constexpr int BN_OUT = kGatedLayout<KIND> ? 128 : 256;
@@ -296,13 +303,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_ffn_tc(const __grid_constant
                 const bool sh = ti.seg >= p.n_seg;
                 const int K = sh ? p.K_sh : p.K;
                 const int arow = s.row0[ti.seg] + ti.m * BM;
-                const CUtensorMap *ta = sh ? &p.tmA_sh : &p.tmA;
+                const bool half = half_tile(s.rows[ti.seg] - ti.m * BM);
+                const CUtensorMap *ta = half ? (sh ? &p.tmA64_sh : &p.tmA64) : (sh ? &p.tmA_sh : &p.tmA);
+                const uint32_t tx = (half ? A_BYTES / 2 : A_BYTES) + B_BYTES;
                 for (int kb = 0; kb < K / BK; ++kb) {
                     if (!wait_bar(&s.empty[st], ph ^ 1, abort_flag, p.err)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&s.full[st], STAGE_BYTES);
+                    mbar_arrive_expect_tx(&s.full[st], tx);
                     const int kc = kb * BK;
                     tma_load_2d(smA(st), ta, kc, arow, &s.full[st]);
                     if (kGatedLayout<KIND>) {
@@ -333,12 +342,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_ffn_tc(const __grid_constant
         // ================= MMA issuer =================
         if (lane == 0) {
             constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN_MMA);
+            constexpr uint32_t IDESC64 = idesc_bf16_f32(BM / 2, BN_MMA);
             int st = 0, acc = 0;
             uint32_t ph = 0, aph = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
                 const TileInfo ti = decode_tile(s, nseg, tile);
                 const int K = ti.seg >= p.n_seg ? p.K_sh : p.K;
+                const uint32_t idesc = half_tile(s.rows[ti.seg] - ti.m * BM) ? IDESC64 : IDESC;
                 if (!wait_bar(&s.tempty[acc], aph ^ 1, abort_flag, p.err)) {
                     ok = false;
                     break;
@@ -355,7 +366,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_ffn_tc(const __grid_constant
                     const uint64_t bd = desc_sw128(smem_u32(smB(st)));
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
-                        umma_bf16(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), IDESC,
+                        umma_bf16(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc,
                                   (kb | kk) != 0 ? 1u : 0u);
                     umma_commit(&s.empty[st]);
                     if (++st == STAGES) {
@@ -377,7 +388,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_ffn_tc(const __grid_constant
     } else {
         // ================= epilogue (warps 2..5) =================
         const int quarter = warp & 3;  // TMEM lanes this warp may access
-        const int r_in_tile = quarter * 32 + lane;
         int acc = 0;
         uint32_t aph = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
@@ -386,7 +396,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_ffn_tc(const __grid_constant
             if (!wait_bar(&s.tfull[acc], aph, abort_flag, p.err)) break;
             tc_fence_after();
             const int rows = s.rows[ti.seg] - ti.m * BM;
-            const bool row_ok = r_in_tile < rows;
+            const bool half = half_tile(rows);
+            const int r_in_tile = half ? quarter * 16 + lane : quarter * 32 + lane;
+            const bool row_ok = (!half || lane < 16) && r_in_tile < rows;
             const int64_t orow = (int64_t)s.row0[ti.seg] + ti.m * BM + r_in_tile;
             const int n_out = sh ? p.n_out_sh : p.n_out;
             __nv_bfloat16 *crow = (sh ? p.C_sh : p.C) + orow * n_out * kOutLd<KIND>;
@@ -863,12 +875,14 @@ cudaError_t product(const int32_t *offsets, int n_seg, int64_t a_rows, const voi
     int64_t max_tiles = 0;
     if (n_seg > 0) {
         if (!encode_bf16_2d(&p.tmA, a, K, a_rows, BM)) return cudaErrorInvalidValue;
+        if (!encode_bf16_2d(&p.tmA64, a, K, a_rows, BM / 2)) return cudaErrorInvalidValue;
         if (!encode_bf16_3d(&p.tmB0, b0, K, n_out, n_seg, box_b)) return cudaErrorInvalidValue;
         if (kGatedLayout<KIND> && !encode_bf16_3d(&p.tmB1, b1, K, n_out, n_seg, box_b)) return cudaErrorInvalidValue;
         max_tiles += ((a_rows + tm - 1) / tm + n_seg) * ((n_out + BN_OUT - 1) / BN_OUT);
     }
     if (sh_rows > 0) {
         if (!encode_bf16_2d(&p.tmA_sh, a_sh, K_sh, sh_rows, BM)) return cudaErrorInvalidValue;
+        if (!encode_bf16_2d(&p.tmA64_sh, a_sh, K_sh, sh_rows, BM / 2)) return cudaErrorInvalidValue;
         if (!encode_bf16_2d(&p.tmB0_sh, b0_sh, K_sh, n_out_sh, box_b)) return cudaErrorInvalidValue;
         if (kGatedLayout<KIND> && !encode_bf16_2d(&p.tmB1_sh, b1_sh, K_sh, n_out_sh, box_b))
             return cudaErrorInvalidValue;
