@@ -436,7 +436,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_ffn_tc(const __grid_constant
 // Last blocks. A segment of r = 256 q + t rows has q full 256-row blocks and t rows
 // left. With 0 < t < 256 those t rows are not a partly empty 256-row tile but a tile
 // with the weights on the MMA's M side and the tokens on its N side,
-//   D[256 weight rows][t' tokens] = W[256][64] · X_tail[t'][64]ᵀ,  t' = t rounded up to 32,
+//   D[256 weight rows][t' tokens] = W[256][64] · X_tail[t'][64]ᵀ,  t' = t rounded up to 16,
 // whose MMAs cost t'/256 of a row tile's; the tokens are staged where a row tile's
 // token rows go (t'/2 per CTA) and the weights as for a row tile, so the tile follows
 // the segment's full blocks in the tile order and finds their weights in L2. Its
@@ -468,7 +468,7 @@ struct Tile2 {
     int seg, m, n;
     int type;   // TILE_ROW: rows [256 m, 256 m + 256); TILE_TAIL: rows [256 q, 256 q + tail)
     int tail;   // tail rows (TILE_TAIL)
-    int tpad;   // tail rounded up to 32: the tail MMA's N
+    int tpad;   // tail rounded up to 16: the tail MMA's N (t'/2 rows per CTA, whole 8-row groups)
 };
 
 // Tiles per n-tile of a segment of `rows` rows: its full blocks and a tail tile.
@@ -483,7 +483,7 @@ __device__ __forceinline__ Tile2 decode_tile2(const Smem2 &s, int nseg, int tile
     const int rows = s.rows[ti.seg];
     t2.type = ti.m == (rows >> 8) ? TILE_TAIL : TILE_ROW;
     t2.tail = t2.type == TILE_TAIL ? rows & 255 : 0;
-    t2.tpad = (t2.tail + 31) & ~31;
+    t2.tpad = (t2.tail + 15) & ~15;
     return t2;
 }
 
@@ -494,7 +494,7 @@ __device__ __forceinline__ bool epilogue_tail(Smem2 &s, uint8_t *xbufs, uint32_t
                                               int64_t row_tail0, __nv_bfloat16 *out, int n_out, uint32_t rank,
                                               int q, int lane, uint32_t &xcount, volatile int *abort_flag,
                                               uint32_t *err) {
-    const int nchunks = t.tpad >> 5;
+    const int nchunks = (t.tpad + 31) >> 5;  // the last chunk's columns past t' are never stored
     if constexpr (KIND == KIND_GATED || KIND == KIND_PREACT) {
         // lanes of quarters 0-1: gate rows, 2-3: up rows of hidden units 64 rank + 32 (q & 1) + lane
         const bool is_gate = q < 2;
