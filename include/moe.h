@@ -396,13 +396,13 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const float *w_r,
  *   dy [T][d] bf16 in;  dx [T][d] bf16, dw_r [d][N] fp32, db_r [N] fp32 (NULL or
  *   ignored without a router bias), dw_gate_or_w1 / dw_up [N][h][d], dw_down
  *   [N][d][h], dshared_* shaped like the shared weights — all bf16 outputs.
- * The expert weights are transposed into bws for the row products; the weight
- * gradients reduce over each expert's rows on the tensor cores. The weight
- * transposes, the transposed forward activations and the recomputed router logits
- * run on a non-blocking auxiliary stream that the call creates, joins to `stream` with
- * events where their results are needed, and releases before returning (its work
- * completes asynchronously, ordered before the work enqueued on `stream` after the
- * call); if the stream cannot be created, everything runs on `stream`. fp32 and
+ * The row products read the expert weights in their own layout; the weight
+ * gradients reduce over each expert's rows on the tensor cores. The transposed forward
+ * activations and the recomputed router logits run on a non-blocking auxiliary stream
+ * that the call creates, joins to `stream` with an event where their results are
+ * needed, and releases before returning (its work completes asynchronously, ordered
+ * before the work enqueued on `stream` after the call); if the stream cannot be
+ * created, everything runs on `stream`. fp32 and
  * Expert Choice configs return MOE_ERR_UNSUPPORTED.
  */
 size_t moe_backward_workspace_size(const moe_config *cfg);

@@ -353,8 +353,6 @@ BwdLayout bwd_layout(const moe_config &c) {
     L.dH = take(R * h * 2);
     L.dAB = take(R * W * 2);
     L.dX = take(R * d * 2);
-    L.wo_t = take(N * h * d * 2);
-    L.wab_t = take(N * d * W * 2);
     L.kpre = take((N + 1) * 4);
     L.dO_t = take(d * Kall * 2);
     L.H_t = take(h * Kall * 2);
@@ -364,8 +362,6 @@ BwdLayout bwd_layout(const moe_config &c) {
     L.dH_sh = take(hs ? T * hs * 2 : 0);
     L.dAB_sh = take(hs ? T * 2 * hs * 2 : 0);
     L.dX_sh = take(hs ? T * d * 2 : 0);
-    L.wo_sh_t = take(hs ? hs * d * 2 : 0);
-    L.wab_sh_t = take(hs ? d * 2 * hs * 2 : 0);
     L.dy_t = take(hs ? d * Tp * 2 : 0);
     L.Hsh_t = take(hs ? hs * Tp * 2 : 0);
     L.dABsh_t = take(hs ? 2 * hs * Tp * 2 : 0);

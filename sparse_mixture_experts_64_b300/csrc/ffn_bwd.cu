@@ -497,36 +497,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
-// dst[b][c][off + r] = src[b][r][c]: a batch of R x C bf16 matrices transposed into
-// rows of stride ldd. 64 x 64 tiles through shared memory; 16-byte loads along C and
-// 16-byte stores along R (C, R, ldd and off multiples of 8).
-__global__ void __launch_bounds__(256) k_transpose_batched(const __nv_bfloat16 *__restrict__ src, int R, int C,
-                                                           __nv_bfloat16 *__restrict__ dst, int ldd, int off) {
-    __shared__ __nv_bfloat16 tile[64][64 + 2];
-    const int b = blockIdx.z;
-    const int c0 = blockIdx.x * 64, r0 = blockIdx.y * 64;
-    const __nv_bfloat16 *sb = src + (size_t)b * R * C;
-    __nv_bfloat16 *db = dst + (size_t)b * C * ldd;
-    for (int v = threadIdx.x; v < 64 * 8; v += 256) {
-        const int i = v >> 3, j = (v & 7) * 8;  // row i, columns j .. j+7 of the tile
-        uint4 q = make_uint4(0, 0, 0, 0);
-        if (r0 + i < R && c0 + j < C) q = *reinterpret_cast<const uint4 *>(sb + (size_t)(r0 + i) * C + c0 + j);
-        const __nv_bfloat16 *e = reinterpret_cast<const __nv_bfloat16 *>(&q);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) tile[i][j + u] = e[u];
-    }
-    __syncthreads();
-    for (int v = threadIdx.x; v < 64 * 8; v += 256) {
-        const int i = v >> 3, j = (v & 7) * 8;  // destination row c0 + i, rows j .. j+7 of the source
-        if (c0 + i < C && r0 + j < R) {
-            __align__(16) __nv_bfloat16 e[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) e[u] = tile[j + u][i];
-            *reinterpret_cast<uint4 *>(db + (size_t)(c0 + i) * ldd + off + r0 + j) = *reinterpret_cast<const uint4 *>(e);
-        }
-    }
-}
-
 // kpre[g] = sum over segments g' < g of R_g' rounded up to 64 (g = 0 .. n_seg), one CTA.
 __global__ void __launch_bounds__(256) k_pad_prefix(const int32_t *__restrict__ offsets, int n_seg, int rows,
                                                     int32_t *__restrict__ kpre) {
@@ -656,14 +626,6 @@ cudaError_t launch_wgrad(const int32_t *offsets, int n_seg, int64_t a_rows, cons
     }
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, device_sm_count()));
     k_wgrad_tc<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(p);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_transpose_batched(const void *src, int B, int R, int C, void *dst, int ldd, int off,
-                                     cudaStream_t s) {
-    dim3 grid((C + 63) / 64, (R + 63) / 64, B);
-    k_transpose_batched<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(src), R, C,
-                                             static_cast<__nv_bfloat16 *>(dst), ldd, off);
     return cudaGetLastError();
 }
 

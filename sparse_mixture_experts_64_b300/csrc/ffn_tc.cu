@@ -60,6 +60,10 @@ struct TcParams {
     CUtensorMap tmA64, tmA64_sh;   // the same arrays, box 64 x 64 (single-CTA half tiles)
     CUtensorMap tmB0, tmB1;        // routed weights [n_seg][n_out][K], box 64 x (128|256) x 1
     CUtensorMap tmB0_sh, tmB1_sh;  // shared weights [n_out_sh][K_sh], box 64 x (128|256)
+    // Plain products only: weights MN-major, maps over [n_seg][K][n_out] and [K_sh][n_out_sh]
+    // (box 64 x 64), for k < k_split from tmB0 and beyond from tmB1 at k - k_split
+    // (k_split 0: tmB0 only); likewise k_split_sh for the shared segment.
+    int b_mn, k_split, k_split_sh;
     const int32_t *offsets;
     int n_seg, sh_rows;
     int a_rows;                    // rows of the routed buffers; offsets are clamped to it
@@ -322,6 +326,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_ffn_tc(const __grid_constant
                             tma_load_3d(smB(st), &p.tmB0, kc, ti.n * 128, ti.seg, &s.full[st]);
                             tma_load_3d(smB(st) + B_BYTES / 2, &p.tmB1, kc, ti.n * 128, ti.seg, &s.full[st]);
                         }
+                    } else if (p.b_mn) {
+                        // MN-major weights: four 64-column chunks of 64 K-rows
+                        const int ks = sh ? p.k_split_sh : p.k_split;
+                        const bool hi = ks > 0 && kc >= ks;
+                        const int kq = hi ? kc - ks : kc;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            if (sh) tma_load_2d(smB(st) + j * 8192, hi ? &p.tmB1_sh : &p.tmB0_sh, ti.n * 256 + 64 * j, kq,
+                                                &s.full[st]);
+                            else tma_load_3d(smB(st) + j * 8192, hi ? &p.tmB1 : &p.tmB0, ti.n * 256 + 64 * j, kq, ti.seg,
+                                             &s.full[st]);
+                        }
                     } else {
                         if (sh) tma_load_2d(smB(st), &p.tmB0_sh, kc, ti.n * 256, &s.full[st]);
                         else tma_load_3d(smB(st), &p.tmB0, kc, ti.n * 256, ti.seg, &s.full[st]);
@@ -349,7 +365,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_ffn_tc(const __grid_constant
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
                 const TileInfo ti = decode_tile(s, nseg, tile);
                 const int K = ti.seg >= p.n_seg ? p.K_sh : p.K;
-                const uint32_t idesc = half_tile(s.rows[ti.seg] - ti.m * BM) ? IDESC64 : IDESC;
+                const uint32_t idesc =
+                    (half_tile(s.rows[ti.seg] - ti.m * BM) ? IDESC64 : IDESC) | (p.b_mn ? kIdescBMajorMN : 0u);
+                const uint64_t bstep = p.b_mn ? 128u : 2u;  // descriptor units (16 B) per K step of 16
                 if (!wait_bar(&s.tempty[acc], aph ^ 1, abort_flag, p.err)) {
                     ok = false;
                     break;
@@ -363,10 +381,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_ffn_tc(const __grid_constant
                     }
                     tc_fence_after();
                     const uint64_t ad = desc_sw128(smem_u32(smA(st)));
-                    const uint64_t bd = desc_sw128(smem_u32(smB(st)));
+                    const uint64_t bd = p.b_mn ? desc_sw128_mn(smem_u32(smB(st))) : desc_sw128(smem_u32(smB(st)));
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
-                        umma_bf16(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc,
+                        umma_bf16(d_tmem, ad + (uint64_t)(2 * kk), bd + bstep * (uint64_t)kk, idesc,
                                   (kb | kk) != 0 ? 1u : 0u);
                     umma_commit(&s.empty[st]);
                     if (++st == STAGES) {
@@ -706,6 +724,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                             tma_load_3d_pair(smB(st), &p.tmB0, kc, wrow, t.seg, fb);
                             tma_load_3d_pair(smB(st) + HALF_BYTES / 2, &p.tmB1, kc, wrow, t.seg, fb);
                         }
+                    } else if (p.b_mn) {
+                        // MN-major weights: this CTA's 128 columns as two chunks of 64 K-rows
+                        const int brow = t.n * 256 + (int)rank * 128;
+                        const int ks = sh ? p.k_split_sh : p.k_split;
+                        const bool hi = ks > 0 && kc >= ks;
+                        const int kq = hi ? kc - ks : kc;
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            if (sh) tma_load_2d_pair(smB(st) + j * 8192, hi ? &p.tmB1_sh : &p.tmB0_sh, brow + 64 * j, kq,
+                                                     fb);
+                            else tma_load_3d_pair(smB(st) + j * 8192, hi ? &p.tmB1 : &p.tmB0, brow + 64 * j, kq, t.seg,
+                                                  fb);
+                        }
                     } else {
                         const int brow = t.n * 256 + (int)rank * 128;
                         if (sh) tma_load_2d_pair(smB(st), &p.tmB0_sh, kc, brow, fb);
@@ -735,8 +766,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 const Tile2 t = decode_tile2(s, nseg, tile);
                 const int K = t.seg >= p.n_seg ? p.K_sh : p.K;
                 const bool tail = t.type == TILE_TAIL;
-                // a tail tile: the weights (B stage) as the M side, the tokens as N
-                const uint32_t idesc = tail ? idesc_bf16_f32(2 * BM, t.tpad) : IDESC;
+                // a tail tile: the weights (B stage) as the M side, the tokens as N; MN-major
+                // weights mark that side of the MMA as MN-major
+                const uint32_t idesc = (tail ? idesc_bf16_f32(2 * BM, t.tpad) : IDESC) |
+                                       (p.b_mn ? (tail ? kIdescAMajorMN : kIdescBMajorMN) : 0u);
+                const uint64_t wstep = p.b_mn ? 128u : 2u;  // descriptor units per K step of 16 (weights)
                 if (!wait_bar(&s.tempty[acc], aph ^ 1, abort_flag, p.err)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * ACC_COLS);
@@ -747,11 +781,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                     }
                     tc_fence_after();
                     const uint64_t ad = desc_sw128(smem_u32(smA(st)));
-                    const uint64_t bd = desc_sw128(smem_u32(smB(st)));
+                    const uint64_t bd = p.b_mn ? desc_sw128_mn(smem_u32(smB(st))) : desc_sw128(smem_u32(smB(st)));
                     const uint64_t m_side = tail ? bd : ad, n_side = tail ? ad : bd;
+                    const uint64_t m_step = tail ? wstep : 2u, n_step = tail ? 2u : wstep;
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
-                        umma_bf16_pair(d_tmem, m_side + (uint64_t)(2 * kk), n_side + (uint64_t)(2 * kk), idesc,
+                        umma_bf16_pair(d_tmem, m_side + m_step * (uint64_t)kk, n_side + n_step * (uint64_t)kk, idesc,
                                        (kb | kk) != 0 ? 1u : 0u);
                     umma_commit_pair_mc(&s.empty[st], 0x3);
                     if (++st == STAGES2) {
@@ -849,11 +884,16 @@ cudaError_t launch_kind2(const TcParams &p, int64_t max_tiles, cudaStream_t s) {
 //   b0,b1 / b0_sh,b1_sh: weights ([n_seg][n_out][K] / [n_out_sh][K_sh]);
 //   out / out_sh: outputs ([a_rows][n_out] / [sh_rows][n_out_sh]).
 // pair: run the CTA-pair kernel (256-row tiles) instead of the single-CTA one.
+//   b_mn (plain products only): the weights are MN-major, b0 [n_seg][K or k_split][n_out]
+//   and, with k_split > 0, b1 [n_seg][K - k_split][n_out] for k >= k_split (likewise
+//   b0_sh / b1_sh with k_split_sh).
 template <int KIND>
 cudaError_t product(const int32_t *offsets, int n_seg, int64_t a_rows, const void *a, const void *b0,
                     const void *b1, int K, int n_out, void *out, int sh_rows, const void *a_sh,
                     const void *b0_sh, const void *b1_sh, int K_sh, int n_out_sh, void *out_sh,
-                    uint32_t *err, cudaStream_t s, bool pair) {
+                    uint32_t *err, cudaStream_t s, bool pair, bool b_mn = false, int k_split = 0,
+                    int k_split_sh = 0) {
+    if (b_mn && KIND != KIND_PLAIN) return cudaErrorInvalidValue;
     constexpr int BN_OUT = kGatedLayout<KIND> ? 128 : 256;
     // weight rows per TMA box: the single-CTA kernel stages 256 rows (gated: 128 gate +
     // 128 up), the pair kernel 128 per CTA (gated: 64 gate + 64 up)
@@ -872,20 +912,49 @@ cudaError_t product(const int32_t *offsets, int n_seg, int64_t a_rows, const voi
     p.C = static_cast<__nv_bfloat16 *>(out);
     p.C_sh = static_cast<__nv_bfloat16 *>(out_sh);
     p.err = err;
+    p.b_mn = b_mn ? 1 : 0;
+    p.k_split = b_mn ? k_split : 0;
+    p.k_split_sh = b_mn ? k_split_sh : 0;
+    if (b_mn && (k_split < 0 || k_split % BK || k_split >= K || k_split_sh < 0 || k_split_sh % BK ||
+                 (sh_rows > 0 && k_split_sh >= K_sh)))
+        return cudaErrorInvalidValue;
+    // MN-major weight maps: [n_exp][rows of K][n_out], box 64 columns x 64 K-rows
+    auto mn_maps = [&](CUtensorMap *m0, CUtensorMap *m1, const void *w0, const void *w1, int Kt, int ks, int no,
+                       int nexp) {
+        const int k0 = ks > 0 ? ks : Kt;
+        if (nexp > 0) {
+            if (!encode_bf16_3d(m0, w0, no, k0, nexp, BK)) return false;
+            if (ks > 0 && !encode_bf16_3d(m1, w1, no, Kt - ks, nexp, BK)) return false;
+        } else {
+            if (!encode_bf16_2d(m0, w0, no, k0, BK)) return false;
+            if (ks > 0 && !encode_bf16_2d(m1, w1, no, Kt - ks, BK)) return false;
+        }
+        return true;
+    };
     int64_t max_tiles = 0;
     if (n_seg > 0) {
         if (!encode_bf16_2d(&p.tmA, a, K, a_rows, BM)) return cudaErrorInvalidValue;
         if (!encode_bf16_2d(&p.tmA64, a, K, a_rows, BM / 2)) return cudaErrorInvalidValue;
-        if (!encode_bf16_3d(&p.tmB0, b0, K, n_out, n_seg, box_b)) return cudaErrorInvalidValue;
-        if (kGatedLayout<KIND> && !encode_bf16_3d(&p.tmB1, b1, K, n_out, n_seg, box_b)) return cudaErrorInvalidValue;
+        if (b_mn) {
+            if (!mn_maps(&p.tmB0, &p.tmB1, b0, b1, K, k_split, n_out, n_seg)) return cudaErrorInvalidValue;
+        } else {
+            if (!encode_bf16_3d(&p.tmB0, b0, K, n_out, n_seg, box_b)) return cudaErrorInvalidValue;
+            if (kGatedLayout<KIND> && !encode_bf16_3d(&p.tmB1, b1, K, n_out, n_seg, box_b))
+                return cudaErrorInvalidValue;
+        }
         max_tiles += ((a_rows + tm - 1) / tm + n_seg) * ((n_out + BN_OUT - 1) / BN_OUT);
     }
     if (sh_rows > 0) {
         if (!encode_bf16_2d(&p.tmA_sh, a_sh, K_sh, sh_rows, BM)) return cudaErrorInvalidValue;
         if (!encode_bf16_2d(&p.tmA64_sh, a_sh, K_sh, sh_rows, BM / 2)) return cudaErrorInvalidValue;
-        if (!encode_bf16_2d(&p.tmB0_sh, b0_sh, K_sh, n_out_sh, box_b)) return cudaErrorInvalidValue;
-        if (kGatedLayout<KIND> && !encode_bf16_2d(&p.tmB1_sh, b1_sh, K_sh, n_out_sh, box_b))
-            return cudaErrorInvalidValue;
+        if (b_mn) {
+            if (!mn_maps(&p.tmB0_sh, &p.tmB1_sh, b0_sh, b1_sh, K_sh, k_split_sh, n_out_sh, 0))
+                return cudaErrorInvalidValue;
+        } else {
+            if (!encode_bf16_2d(&p.tmB0_sh, b0_sh, K_sh, n_out_sh, box_b)) return cudaErrorInvalidValue;
+            if (kGatedLayout<KIND> && !encode_bf16_2d(&p.tmB1_sh, b1_sh, K_sh, n_out_sh, box_b))
+                return cudaErrorInvalidValue;
+        }
         max_tiles += ((int64_t)(sh_rows + tm - 1) / tm) * ((n_out_sh + BN_OUT - 1) / BN_OUT);
     }
     if (max_tiles == 0) return cudaSuccess;
@@ -903,8 +972,11 @@ cudaError_t product(const int32_t *offsets, int n_seg, int64_t a_rows, const voi
     TcParams q = p;
     q.tail_mode = 2;
     q.sh_rows = 0;
-    if (!encode_bf16_3d(&q.tmB0, b0, K, n_out, n_seg, kGatedLayout<KIND> ? 128 : 256)) return cudaErrorInvalidValue;
-    if (kGatedLayout<KIND> && !encode_bf16_3d(&q.tmB1, b1, K, n_out, n_seg, 128)) return cudaErrorInvalidValue;
+    if (!b_mn) {  // the single-CTA kernel stages 256 weight rows per K-major box (MN-major maps serve both)
+        if (!encode_bf16_3d(&q.tmB0, b0, K, n_out, n_seg, kGatedLayout<KIND> ? 128 : 256))
+            return cudaErrorInvalidValue;
+        if (kGatedLayout<KIND> && !encode_bf16_3d(&q.tmB1, b1, K, n_out, n_seg, 128)) return cudaErrorInvalidValue;
+    }
     return launch_kind<KIND>(q, ((a_rows + BM - 1) / BM + n_seg) * ((n_out + BN_OUT - 1) / BN_OUT), s);
 }
 
@@ -913,15 +985,17 @@ cudaError_t product(const int32_t *offsets, int n_seg, int64_t a_rows, const voi
 cudaError_t launch_gemm_rows(const moe_config &c, bool preact, const int32_t *offsets, int n_seg, int64_t a_rows,
                              const void *a, const void *b0, const void *b1, int K, int n_out, void *out, int sh_rows,
                              const void *a_sh, const void *b0_sh, const void *b1_sh, int K_sh, int n_out_sh,
-                             void *out_sh, uint32_t *err, cudaStream_t s) {
+                             void *out_sh, uint32_t *err, cudaStream_t s, bool b_mn, int k_split, int k_split_sh) {
     bool pair = n_seg > 0 && a_rows >= 224LL * n_seg;
     if (c.debug_flags & MOE_DEBUG_FFN_PAIR) pair = true;
     if (c.debug_flags & MOE_DEBUG_FFN_SINGLE) pair = false;
-    if (preact)
+    if (preact) {
+        if (b_mn) return cudaErrorInvalidValue;
         return product<KIND_PREACT>(offsets, n_seg, a_rows, a, b0, b1, K, n_out, out, sh_rows, a_sh, b0_sh, b1_sh,
                                     K_sh, n_out_sh, out_sh, err, s, pair);
-    return product<KIND_PLAIN>(offsets, n_seg, a_rows, a, b0, nullptr, K, n_out, out, sh_rows, a_sh, b0_sh, nullptr,
-                               K_sh, n_out_sh, out_sh, err, s, pair);
+    }
+    return product<KIND_PLAIN>(offsets, n_seg, a_rows, a, b0, b1, K, n_out, out, sh_rows, a_sh, b0_sh, b1_sh, K_sh,
+                               n_out_sh, out_sh, err, s, pair, b_mn, k_split, k_split_sh);
 }
 
 cudaError_t launch_ffn_tc(const moe_config &c, const FfnGroup &g, uint32_t *err, cudaStream_t s) {

@@ -65,10 +65,9 @@ struct BwdLayout {
     size_t dgate;                // f32  [T][k]      gate gradients
     size_t AB, dH, dAB;          // bf16 [R_max][W], [R_max][h], [R_max][W]
     size_t dX;                   // bf16 [R_max][d]
-    size_t wo_t, wab_t;          // bf16 [N][h][d] (W_outᵀ), [N][d][W] ([W_a | W_b]ᵀ)
     size_t kpre;                 // int32 [N+1] padded column offsets of the experts' K ranges
     size_t dO_t, H_t, dAB_t, X_t;  // bf16 transposed activations [d|h|W|d][Kall]
-    size_t AB_sh, dH_sh, dAB_sh, dX_sh, wo_sh_t, wab_sh_t;  // shared expert, rows = T
+    size_t AB_sh, dH_sh, dAB_sh, dX_sh;  // shared expert, rows = T
     size_t dy_t, Hsh_t, dABsh_t, x_t;                       // shared expert, [..][ceil64(T)]
     size_t logits, routed, dL, dxr;  // router: f32 [T][N], int32 [N], f32 [T][N], f32 [T][d]
     size_t wr_slabs;                 // f32 [dwr_splits][d][N] partial router-weight gradients
@@ -163,10 +162,15 @@ cudaError_t launch_ffn_sw(const moe_config &c, const FfnGroup &g, uint32_t *err,
 // One grouped product on the tensor cores (bf16): out[rows of segment g] = a[rows][K]
 // · b0[g][n_out][K]ᵀ, plain, or with preact the gated pair (b0, b1) stored raw as
 // [gate | up] rows of width 2 n_out; an optional shared segment with its own operands.
+// b_mn (plain only): the weights are MN-major instead, out = a · b0[g] with b0[g]
+// [K][n_out]; with k_split > 0 the K rows are b0[g] [k_split][n_out] followed by b1[g]
+// [K - k_split][n_out] (likewise b0_sh / b1_sh with k_split_sh), so [W_gate; W_up] need
+// not be stacked.
 cudaError_t launch_gemm_rows(const moe_config &c, bool preact, const int32_t *offsets, int n_seg, int64_t a_rows,
                              const void *a, const void *b0, const void *b1, int K, int n_out, void *out, int sh_rows,
                              const void *a_sh, const void *b0_sh, const void *b1_sh, int K_sh, int n_out_sh,
-                             void *out_sh, uint32_t *err, cudaStream_t s);
+                             void *out_sh, uint32_t *err, cudaStream_t s, bool b_mn = false, int k_split = 0,
+                             int k_split_sh = 0);
 // Weight-gradient GEMM with K running over each expert's rows: for expert e,
 // out[e] [M][Nn] = At[:, k0_e : k0_e + kp_e] · Bt[:, k0_e : k0_e + kp_e]ᵀ, where the
 // transposed activations At [M][Kall], Bt [Nn][Kall] hold expert e's rows in columns
@@ -183,9 +187,6 @@ cudaError_t launch_pad_prefix(const int32_t *offsets, int n_seg, int rows, int32
 // Rows [rows][C] into [C][Kall] in that padded column layout (offsets null: one segment).
 cudaError_t launch_transpose_rows_padded(const void *src, int C, const int32_t *offsets, const int32_t *kpre,
                                          int n_seg, int rows, int64_t Kall, void *dst, cudaStream_t s);
-// dst[b][c][off + r] = src[b][r][c] for a batch of R x C bf16 matrices (dst row stride ldd).
-cudaError_t launch_transpose_batched(const void *src, int B, int R, int C, void *dst, int ldd, int off,
-                                     cudaStream_t s);
 
 int device_sm_count();
 

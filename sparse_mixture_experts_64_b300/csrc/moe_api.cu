@@ -366,7 +366,6 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const float *w_r, 
     const int N = c.N, d = c.d, h = c.h, hs = c.h_shared, Wd = gated ? 2 * h : h;
     const int64_t Kall = wgrad_kall_bound(c), Tp = ((int64_t)c.T + 63) / 64 * 64;
     void *dO = bw + B.dO, *AB = bw + B.AB, *dH = bw + B.dH, *dAB = bw + B.dAB, *dX = bw + B.dX;
-    void *wo_t = bw + B.wo_t, *wab_t = bw + B.wab_t;
     float *dgate = reinterpret_cast<float *>(bw + B.dgate);
     int32_t *kpre = reinterpret_cast<int32_t *>(bw + B.kpre);
     cudaError_t e = cudaSuccess;
@@ -376,15 +375,15 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const float *w_r, 
     };
 
     // Work that depends only on the inputs and the forward's saved tensors runs on an
-    // auxiliary stream beside the row products: the weight re-layouts (HBM-bound, while
-    // the recompute and dH products are tensor-bound), the padding prefix, the
-    // transposed forward activations and the router logits. Events join it where each
-    // result is first needed; without the stream (creation failed) it all runs in order
-    // on `stream`.
+    // auxiliary stream beside the row products: the padding prefix, the transposed forward
+    // activations (HBM-bound, while the recompute and dH products are tensor-bound) and
+    // the router logits. An event joins it where its results are first needed; without
+    // the stream (creation failed) it all runs in order on `stream`. The row products read
+    // the expert weights in their own layout (MN-major operands), so no weight is copied.
     cudaStream_t aux = nullptr;
-    cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};  // fork, W_outᵀ ready, [W_a | W_b]ᵀ ready, aux done
+    cudaEvent_t ev[2] = {nullptr, nullptr};  // fork, aux done
     bool two = cudaStreamCreateWithFlags(&aux, cudaStreamNonBlocking) == cudaSuccess;
-    for (int i = 0; i < 4 && two; ++i) two = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; i < 2 && two; ++i) two = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) == cudaSuccess;
     if (two) two = cudaEventRecord(ev[0], stream) == cudaSuccess && cudaStreamWaitEvent(aux, ev[0], 0) == cudaSuccess;
     const cudaStream_t sa = two ? aux : stream;
     auto mark = [&](int i) {
@@ -395,17 +394,6 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const float *w_r, 
     };
 
     // -- auxiliary stream
-    // weights transposed for the row products: W_outᵀ [N][h][d], [W_a | W_b]ᵀ [N][d][Wd]
-    ok(launch_transpose_batched(w_down, N, d, h, wo_t, d, 0, sa));
-    if (hs) ok(launch_transpose_batched(shared_w_down, 1, d, hs, bw + B.wo_sh_t, d, 0, sa));
-    mark(1);
-    ok(launch_transpose_batched(w_gate_or_w1, N, h, d, wab_t, Wd, 0, sa));
-    if (gated) ok(launch_transpose_batched(w_up, N, h, d, wab_t, Wd, h, sa));
-    if (hs) {
-        ok(launch_transpose_batched(shared_w_gate, 1, hs, d, bw + B.wab_sh_t, 2 * hs, 0, sa));
-        ok(launch_transpose_batched(shared_w_up, 1, hs, d, bw + B.wab_sh_t, 2 * hs, hs, sa));
-    }
-    mark(2);
     // the weight gradients' operands that the forward left: each expert's rows padded to 64
     ok(launch_pad_prefix(offsets, N, (int)R, kpre, sa));
     ok(launch_transpose_rows_padded(hid, h, offsets, kpre, N, (int)R, Kall, bw + B.H_t, sa));
@@ -418,7 +406,7 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const float *w_r, 
     // router logits, recomputed
     ok(launch_router_logits(c, x, w_r, c.has_router_bias ? b_r : nullptr, reinterpret_cast<float *>(bw + B.logits), w,
                             sa));
-    mark(3);
+    mark(1);
 
     // -- main stream
     // gate-scaled dy per row and the gate gradients
@@ -429,19 +417,18 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const float *w_r, 
     if (hs)
         ok(launch_gemm_rows(c, true, nullptr, 0, 0, nullptr, nullptr, nullptr, 0, 0, nullptr, c.T, x, shared_w_gate,
                             shared_w_up, d, hs, bw + B.AB_sh, err, stream));
-    // dH = dO W_out
-    join(1);
-    ok(launch_gemm_rows(c, false, offsets, N, R, dO, wo_t, nullptr, d, h, dH, hs ? c.T : 0, dy, bw + B.wo_sh_t,
-                        nullptr, d, hs, bw + B.dH_sh, err, stream));
+    // dH = dO W_out (W_out [d][h] per expert: MN-major, K = d)
+    ok(launch_gemm_rows(c, false, offsets, N, R, dO, w_down, nullptr, d, h, dH, hs ? c.T : 0, dy, shared_w_down,
+                        nullptr, d, hs, bw + B.dH_sh, err, stream, true, 0, 0));
     // [dA | dB] from the pre-activations
     ok(launch_act_bwd(gated, AB, dH, R, h, dAB, stream));
     if (hs) ok(launch_act_bwd(true, bw + B.AB_sh, bw + B.dH_sh, c.T, hs, bw + B.dAB_sh, stream));
-    // dX = [dA | dB] [W_a ; W_b]
-    join(2);
-    ok(launch_gemm_rows(c, false, offsets, N, R, dAB, wab_t, nullptr, Wd, d, dX, hs ? c.T : 0, bw + B.dAB_sh,
-                        bw + B.wab_sh_t, nullptr, 2 * hs, d, bw + B.dX_sh, err, stream));
+    // dX = [dA | dB] [W_a ; W_b] (W_a, W_b [h][d] per expert: MN-major, K = Wd split at h)
+    ok(launch_gemm_rows(c, false, offsets, N, R, dAB, w_gate_or_w1, gated ? w_up : nullptr, Wd, d, dX, hs ? c.T : 0,
+                        bw + B.dAB_sh, shared_w_gate, shared_w_up, 2 * hs, d, bw + B.dX_sh, err, stream, true,
+                        gated ? h : 0, hs));
     // weight gradients: transposed activations with each expert's rows padded to 64
-    join(3);
+    join(1);
     ok(launch_transpose_rows_padded(dO, d, offsets, kpre, N, (int)R, Kall, bw + B.dO_t, stream));
     ok(launch_transpose_rows_padded(dAB, Wd, offsets, kpre, N, (int)R, Kall, bw + B.dAB_t, stream));
     const bool pair_ok = !(c.debug_flags & MOE_DEBUG_FFN_SINGLE);

@@ -216,6 +216,20 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
+// Shared-memory matrix descriptor for an MN-major operand tile (M or N contiguous)
+// written by TMA with 128-byte swizzling as 64-element chunks, each 64 K-rows of 128 B
+// (8 KB apart): leading byte offset 8192 (from one 64-element chunk of M or N to the
+// next), stride byte offset 1024 (from one 8-row K group to the next); a K step of 16
+// advances the start address by 2048 bytes. Checked on one MMA against exact integer
+// products, as A and as B operand.
+__device__ __forceinline__ uint64_t desc_sw128_mn(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(8192 >> 4) << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// Instruction descriptor bits marking A / B as MN-major.
+constexpr uint32_t kIdescAMajorMN = 1u << 15;
+constexpr uint32_t kIdescBMajorMN = 1u << 16;
+
 // Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), A and B
 // bf16 (bits 7-9 = 1, bits 10-12 = 1), both K-major, N >> 3 at bit 17, M >> 4 at
 // bit 24.
