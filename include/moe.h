@@ -396,6 +396,8 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const float *w_r,
  *   dy [T][d] bf16 in;  dx [T][d] bf16, dw_r [d][N] fp32, db_r [N] fp32 (NULL or
  *   ignored without a router bias), dw_gate_or_w1 / dw_up [N][h][d], dw_down
  *   [N][d][h], dshared_* shaped like the shared weights — all bf16 outputs.
+ * x, w_r, dy, dx, the expert and shared-expert weights and their gradients must be
+ * 16-byte aligned (MOE_ERR_INVALID_ARG otherwise).
  * The row products read the expert weights in their own layout; the weight
  * gradients reduce over each expert's rows on the tensor cores. The transposed forward
  * activations and the recomputed router logits run on a non-blocking auxiliary stream

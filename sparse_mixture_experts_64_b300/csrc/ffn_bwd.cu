@@ -33,6 +33,7 @@ constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + 1024;
 struct WgParams {
     CUtensorMap tmA, tmB;        // At [M][Kall] (box 64 x 128), Bt [Nn][Kall] (box 64 x 256)
     CUtensorMap tmA_sh, tmB_sh;  // shared segment: [M][K_sh], [Nn][K_sh]
+    CUtensorMap tmC, tmC_sh;     // outputs for the pair kernel's stores: [n_seg][M][Nn], [1][M][Nn], box 64 x 32 x 1
     const int32_t *offsets;      // [n_seg + 1] rows of each expert
     int n_seg, has_sh;
     int a_rows;                  // offsets are clamped to it
@@ -257,10 +258,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_wgrad_tc(const __grid_consta
 // k-block (a third less operand data per FLOP than the single-CTA kernel), both
 // halves complete on the even CTA's stage barrier, the even CTA issues the MMAs and
 // its commits arrive on both CTAs' barriers; each CTA's epilogue stores its 128 rows.
-constexpr int STAGES2 = 6;
+// The epilogue writes through shared memory: each warp converts 32 rows x 64 columns
+// to bf16 into one of two 4 KB boxes laid out as the output map's 128-byte swizzle and
+// stores the box with one TMA tensor store, so whole 128-byte lines reach L2. With an
+// expert's few hundred rows as K, a tile's MMAs are short next to its 128 KB of
+// gradient, and per-thread 16-byte row stores (32 rows per instruction) kept L2 busy
+// with partial-line write requests.
+constexpr int STAGES2 = 5;
 constexpr uint32_t HALF_BYTES = 128 * BK * 2;
 constexpr uint32_t STAGE2_BYTES = 2 * HALF_BYTES;
-constexpr size_t SMEM2_BYTES = (size_t)STAGES2 * STAGE2_BYTES + 1024;
+constexpr uint32_t OUT_BOX_BYTES = 32 * 64 * 2;  // 32 rows x 64 bf16
+constexpr size_t SMEM2_BYTES = (size_t)STAGES2 * STAGE2_BYTES + 4 * 2 * OUT_BOX_BYTES + 1024;
 
 struct WgSmem2 {
     uint64_t full[STAGES2], empty[STAGES2], tfull[2], tempty[2], drain;
@@ -268,6 +276,8 @@ struct WgSmem2 {
     int abort_flag;
     int k0[MAX_SEG], kp[MAX_SEG];
 };
+static_assert(SMEM2_BYTES + sizeof(WgSmem2) <= 232448, "shared memory budget of one CTA");
+static_assert(STAGE2_BYTES % 1024 == 0 && OUT_BOX_BYTES % 1024 == 0, "swizzled boxes stay 1024-byte aligned");
 
 // Tensor maps as in WgParams but with 128-row boxes for Bt (each CTA loads half).
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
@@ -441,7 +451,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     } else if (run) {
         // ================= epilogue (warps 2..5 of both CTAs) =================
         const int quarter = warp & 3;
-        const int r_in_tile = (int)rank * BM + quarter * 32 + lane;
+        uint8_t *boxes = tiles + (size_t)STAGES2 * STAGE2_BYTES + (size_t)quarter * 2 * OUT_BOX_BYTES;
+        const uint32_t swz = (uint32_t)(lane & 7);  // 128-byte swizzle: 16-byte unit j of row r at j ^ (r % 8)
+        uint32_t nbox = 0;
         int acc = 0;
         uint32_t aph = 0;
         for (int tile = cluster; tile < total; tile += nclusters) {
@@ -450,29 +462,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             const bool sh = g >= p.n_seg;
             if (!wait_bar(&s.tfull[acc], aph, abort_flag, p.err)) break;
             tc_fence_after();
-            const int row = m * 2 * BM + r_in_tile;
+            const int row0 = m * 2 * BM + (int)rank * BM + quarter * 32;  // this warp's 32 rows
             const bool empty_seg = s.kp[g] == 0;
-            __nv_bfloat16 *crow = (sh ? p.C_sh : p.C + (size_t)g * p.M * p.Nn) + (size_t)row * p.Nn;
+            const CUtensorMap *cmap = sh ? &p.tmC_sh : &p.tmC;
+            const int gz = sh ? 0 : g;
             const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16);
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
-                uint32_t v[32];
+            for (int c = 0; c < BN; c += 64) {
+                uint32_t v[64];
                 tmem_ld32(tbase + c, v);
+                tmem_ld32(tbase + c + 32, v + 32);
                 tmem_ld_wait();
                 const int col = n * BN + c;
-                if (row < p.M && col < p.Nn) {
-                    uint32_t packed[16];
+                // M and Nn are multiples of 64: a box lies wholly inside the output or wholly outside
+                if (row0 < p.M && col < p.Nn) {
+                    uint8_t *box = boxes + (nbox & 1u) * OUT_BOX_BYTES;
+                    if (lane == 0) bulk_wait_group_read<1>();  // the store of two boxes ago has read this box
+                    __syncwarp();
+                    uint8_t *rowp = box + lane * 128;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float f0 = empty_seg ? 0.0f : __uint_as_float(v[2 * i]);
-                        const float f1 = empty_seg ? 0.0f : __uint_as_float(v[2 * i + 1]);
-                        __nv_bfloat162 b = __floats2bfloat162_rn(f0, f1);
-                        packed[i] = *reinterpret_cast<uint32_t *>(&b);
+                    for (int j = 0; j < 8; ++j) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            const float f0 = empty_seg ? 0.0f : __uint_as_float(v[8 * j + 2 * t]);
+                            const float f1 = empty_seg ? 0.0f : __uint_as_float(v[8 * j + 2 * t + 1]);
+                            __nv_bfloat162 b = __floats2bfloat162_rn(f0, f1);
+                            w[t] = *reinterpret_cast<uint32_t *>(&b);
+                        }
+                        *reinterpret_cast<uint4 *>(rowp + ((j ^ swz) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
                     }
-                    uint4 *dst = reinterpret_cast<uint4 *>(crow + col);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(cmap, box, col, row0, gz);
+                        bulk_commit_group();
+                    }
+                    ++nbox;
                 }
             }
             tc_fence_before();
@@ -486,6 +512,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 aph ^= 1;
             }
         }
+        if (lane == 0) bulk_wait_group<0>();  // every store of this warp done before the CTA exits
     }
 
     tc_fence_before();
@@ -597,10 +624,13 @@ cudaError_t launch_wgrad(const int32_t *offsets, int n_seg, int64_t a_rows, cons
     if (n_seg > 0) {
         if (!encode_bf16_2d(&p.tmA, At, (uint64_t)Kall, (uint64_t)M, BM)) return cudaErrorInvalidValue;
         if (!encode_bf16_2d(&p.tmB, Bt, (uint64_t)Kall, (uint64_t)Nn, box_b)) return cudaErrorInvalidValue;
+        if (pair && !encode_bf16_3d(&p.tmC, out, (uint64_t)Nn, (uint64_t)M, (uint64_t)n_seg, 32))
+            return cudaErrorInvalidValue;
     }
     if (p.has_sh) {
         if (!encode_bf16_2d(&p.tmA_sh, At_sh, (uint64_t)K_sh, (uint64_t)M, BM)) return cudaErrorInvalidValue;
         if (!encode_bf16_2d(&p.tmB_sh, Bt_sh, (uint64_t)K_sh, (uint64_t)Nn, box_b)) return cudaErrorInvalidValue;
+        if (pair && !encode_bf16_3d(&p.tmC_sh, out_sh, (uint64_t)Nn, (uint64_t)M, 1, 32)) return cudaErrorInvalidValue;
     }
     if (pair) {
         const int64_t tiles2 = (int64_t)(n_seg + p.has_sh) * ((M + 2 * BM - 1) / (2 * BM)) * ((Nn + BN - 1) / BN);

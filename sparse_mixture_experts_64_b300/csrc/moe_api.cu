@@ -350,6 +350,9 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const float *w_r, 
     for (const void *q : must_align)
         if (!aligned16(q)) return MOE_ERR_INVALID_ARG;
     if ((w_up && !aligned16(w_up)) || (dw_up && !aligned16(dw_up))) return MOE_ERR_INVALID_ARG;
+    if (c.h_shared && (!aligned16(shared_w_gate) || !aligned16(shared_w_up) || !aligned16(shared_w_down) ||
+                       !aligned16(dshared_w_gate) || !aligned16(dshared_w_up) || !aligned16(dshared_w_down)))
+        return MOE_ERR_INVALID_ARG;
     const WsLayout L = ws_layout(c);
     if ((st = check_ws(ws, ws_bytes, L.total)) != MOE_OK) return st;
     const BwdLayout B = bwd_layout(c);

@@ -49,6 +49,9 @@ CASES = [
     (_w("mixtral_prefill", T=1024, d=512, h=1024, N=8, k=2), 0.0, 0.0),          # pair kernels
     (_w("deepseek_fine", T=96, d=128, N=64, k=6, h=192, h_shared=0), 0.05, 0.0),  # N > 32 router
     (_w("deepseek_fine", T=600, d=64, N=4, k=2, h=64, h_shared=64), 0.01, 0.001),  # smallest tiles, pair
+    # 128 routed rows over 64 experts: many experts without rows on the pair
+    # weight-gradient kernel (their gradients are stored as zero boxes)
+    (_w("deepseek_fine", T=64, d=256, N=64, k=2, h=256, h_shared=256), 0.01, 0.0),
 ]
 
 
