@@ -8,11 +8,15 @@
 //
 // This file holds the kernels that are not GEMMs and the orchestration; the row
 // GEMMs run on ffn_tc.cu's kernels, the weight gradients on ffn_bwd.cu's, the two
-// router contractions (T x d x N) on a tiled fp32 CUDA-core GEMM here:
+// router contractions (T x d x N) on the weight-gradient kernel as plain products of
+// bf16-split operands (an fp32 value v = hi + lo + r with hi = bf16(v), lo = bf16(v - hi),
+// |r| <= 2^-16 |v|; bf16 products are exact in the fp32 accumulator):
 //   k_bwd_slots   per kept slot: dO_r = g dy_t (bf16) and dg = <dy_t, O_r> (fp32)
 //   k_act_bwd     dA = dH ⊙ B ⊙ SiLU'(A), dB = dH ⊙ SiLU(A) (ReLU: dA = dH ⊙ [A > 0])
 //   k_count_routed, k_router_bwd  dL per token from dg, aux and z (warp per token)
-//   k_simt_gemm   dx_router = dL W_rᵀ, dW_r = xᵀ dL
+//   k_split3, k_split_t  the split operands of dx_router = dL W_rᵀ (the hi·hi, hi·lo and
+//                 lo·hi terms, concatenated along K) and of dW_rᵀ = dLᵀ x (hi and lo
+//                 stacked along M, x exact in bf16), k_sum_hi_lo_t  dW_r from the two halves
 //   k_bwd_dx      dx = dy + sum_j dX_r + dX_shared + dx_router
 #include <algorithm>
 #include <cmath>
@@ -192,83 +196,62 @@ __global__ void __launch_bounds__(256) k_router_bwd(RouterBwdArgs a) {
     }
 }
 
-// C[M][Nc] (fp32) = sum_k A(m, k) B(k, n): A(m, k) = A[m * lda + k] or, transposed,
-// A[k * lda + m]; B(k, n) = B[k * ldb + n] or, transposed, B[n * ldb + k]. 64 x 64
-// tiles, 16-deep K slices through a double-buffered shared-memory slice (the next
-// slice's global loads are in flight while the current one is multiplied), 4 x 4
-// outputs per thread. Consecutive threads read consecutive addresses: along m / n
-// when that is the operand's contiguous dimension, along k otherwise.
-//
-// Split K: blockIdx.z takes K range [z * kchunk, (z + 1) * kchunk) and writes its own
-// slab C + z * M * Nc (summed afterwards in slab order by k_sum_slabs).
-template <typename TA, bool TRANS_A, bool TRANS_B>
-__global__ void __launch_bounds__(256) k_simt_gemm(const TA *__restrict__ A, int lda, const float *__restrict__ B,
-                                                   int ldb, int M, int Nc, int K, int kchunk, float *__restrict__ C) {
-    __shared__ float As[2][16][64 + 4], Bs[2][16][64 + 4];
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-    const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
-    const int kb = blockIdx.z * kchunk, ke = min(K, kb + kchunk);
-    C += (size_t)blockIdx.z * M * Nc;
-    float ra[4], rb[4];
-    auto fetch = [&](int k0) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int i = threadIdx.x + q * 256;
-            {
-                const int kk = TRANS_A ? i / 64 : i % 16, mm = TRANS_A ? i % 64 : i / 16;
-                const int gm = m0 + mm, gk = k0 + kk;
-                ra[q] = (gm < M && gk < ke) ? to_f32(TRANS_A ? A[(size_t)gk * lda + gm] : A[(size_t)gm * lda + gk])
-                                            : 0.0f;
-            }
-            {
-                const int kk = TRANS_B ? i % 16 : i / 64, nn = TRANS_B ? i / 16 : i % 64;
-                const int gn = n0 + nn, gk = k0 + kk;
-                rb[q] = (gn < Nc && gk < ke) ? (TRANS_B ? B[(size_t)gn * ldb + gk] : B[(size_t)gk * ldb + gn]) : 0.0f;
-            }
-        }
-    };
-    auto stash = [&](int buf) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int i = threadIdx.x + q * 256;
-            As[buf][TRANS_A ? i / 64 : i % 16][TRANS_A ? i % 64 : i / 16] = ra[q];
-            Bs[buf][TRANS_B ? i % 16 : i / 64][TRANS_B ? i / 16 : i % 64] = rb[q];
-        }
-    };
-    float acc[4][4] = {};
-    int buf = 0;
-    if (kb < ke) {
-        fetch(kb);
-        stash(0);
+__device__ __forceinline__ __nv_bfloat16 split_part(float v, int part) {
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    return part == 0 ? hi : __float2bfloat16_rn(v - __bfloat162float(hi));  // v - hi is exact
+}
+
+// src fp32 [rows][n] -> dst bf16 [rows][kp]: column q * n + j (q < 3) holds part p_q of
+// src[r][j] (0: hi, 1: lo), columns from 3n to kp are zero.
+__global__ void __launch_bounds__(256) k_split3(const float *__restrict__ src, int rows, int n, int kp, int p0,
+                                                int p1, int p2, __nv_bfloat16 *__restrict__ dst) {
+    const int64_t total = (int64_t)rows * kp;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int r = (int)(i / kp), j = (int)(i - (int64_t)r * kp);
+        const int q = j / n;
+        __nv_bfloat16 v = __float2bfloat16_rn(0.0f);
+        if (q < 3) v = split_part(src[(size_t)r * n + (j - q * n)], q == 0 ? p0 : q == 1 ? p1 : p2);
+        dst[i] = v;
+    }
+}
+
+// dL fp32 [T][N] -> dst bf16 [2N][Tp]: row e = hi(dL[:, e]), row N + e = lo(dL[:, e]),
+// zero from column T on. 32 x 32 tiles through shared memory.
+__global__ void __launch_bounds__(256) k_split_t(const float *__restrict__ dL, int T, int N, int Tp,
+                                                 __nv_bfloat16 *__restrict__ dst) {
+    __shared__ float tile[32][33];
+    const int t0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    for (int i = ty; i < 32; i += 8) {
+        const int t = t0 + i, e = e0 + tx;
+        tile[i][tx] = (t < T && e < N) ? dL[(size_t)t * N + e] : 0.0f;
     }
     __syncthreads();
-    for (int k0 = kb; k0 < ke; k0 += 16) {
-        const bool more = k0 + 16 < ke;
-        if (more) fetch(k0 + 16);
-#pragma unroll
-        for (int kk = 0; kk < 16; ++kk) {
-            float av[4], bv[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                av[i] = As[buf][kk][ty * 4 + i];
-                bv[i] = Bs[buf][kk][tx * 4 + i];
-            }
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = __fmaf_rn(av[i], bv[j], acc[i][j]);
+    for (int i = ty; i < 32; i += 8) {
+        const int e = e0 + i, t = t0 + tx;
+        if (e < N && t < Tp) {
+            const float v = tile[tx][i];
+            dst[(size_t)e * Tp + t] = split_part(v, 0);
+            dst[(size_t)(N + e) * Tp + t] = split_part(v, 1);
         }
-        if (more) stash(buf ^ 1);
-        __syncthreads();
-        buf ^= 1;
     }
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int gm = m0 + ty * 4 + i, gn = n0 + tx * 4 + j;
-            if (gm < M && gn < Nc) C[(size_t)gm * Nc + gn] = acc[i][j];
-        }
+}
+
+// dw_r [d][N] = C[e][i] + C[N + e][i] from C fp32 [2N][d] (the hi and lo halves).
+__global__ void __launch_bounds__(256) k_sum_hi_lo_t(const float *__restrict__ C, int N, int d,
+                                                     float *__restrict__ dw_r) {
+    __shared__ float tile[32][33];
+    const int i0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    for (int j = ty; j < 32; j += 8) {
+        const int e = e0 + j, i = i0 + tx;
+        tile[j][tx] = (e < N && i < d) ? C[(size_t)e * d + i] + C[(size_t)(N + e) * d + i] : 0.0f;
+    }
+    __syncthreads();
+    for (int j = ty; j < 32; j += 8) {
+        const int i = i0 + j, e = e0 + tx;
+        if (i < d && e < N) dw_r[(size_t)i * N + e] = tile[tx][j];
+    }
 }
 
 // dx = dy + sum_j dX[slot_row] + dX_sh + dx_router, per 8 features of a token.
@@ -307,14 +290,6 @@ __global__ void __launch_bounds__(256) k_bwd_dx(const __nv_bfloat16 *__restrict_
     }
 }
 
-__global__ void k_sum_slabs(const float *__restrict__ slabs, int nslab, int64_t n, float *__restrict__ out) {
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-        float s = 0.0f;
-        for (int z = 0; z < nslab; ++z) s += slabs[(size_t)z * n + i];
-        out[i] = s;
-    }
-}
-
 __global__ void k_col_sum(const float *__restrict__ a, int rows, int cols, float *__restrict__ out) {
     const int c = blockIdx.x * blockDim.x + threadIdx.x;
     if (c >= cols) return;
@@ -329,12 +304,6 @@ int grid_of(int64_t work, int threads) {
 }
 
 }  // namespace
-
-int dwr_splits(const moe_config &c) {
-    // enough CTAs for two waves of 148 SMs, at most 16 slabs
-    const int tiles = ((c.N + 63) / 64) * ((c.d + 63) / 64);
-    return std::max(1, std::min(16, (296 + tiles - 1) / tiles));
-}
 
 BwdLayout bwd_layout(const moe_config &c) {
     BwdLayout L;
@@ -365,12 +334,16 @@ BwdLayout bwd_layout(const moe_config &c) {
     L.dy_t = take(hs ? d * Tp * 2 : 0);
     L.Hsh_t = take(hs ? hs * Tp * 2 : 0);
     L.dABsh_t = take(hs ? 2 * hs * Tp * 2 : 0);
-    L.x_t = take(hs ? d * Tp * 2 : 0);
+    L.x_t = take(d * Tp * 2);
     L.logits = take(T * N * 4);
     L.routed = take(N * 4);
     L.dL = take(T * N * 4);
     L.dxr = take(T * d * 4);
-    L.wr_slabs = take((size_t)dwr_splits(c) * d * N * 4);
+    const size_t Kr = (3 * N + 63) / 64 * 64;
+    L.rA = take(T * Kr * 2);
+    L.rB = take(d * Kr * 2);
+    L.dLt = take(2 * N * Tp * 2);
+    L.wrC = take(2 * N * d * 4);
     L.total = o;
     return L;
 }
@@ -398,9 +371,9 @@ cudaError_t launch_act_bwd(bool gated, const void *AB, const void *dH, int64_t r
     return cudaGetLastError();
 }
 
-cudaError_t launch_router_bwd(const moe_config &c, const void *x, const float *w_r, const int32_t *topk_idx,
-                              const float *topk_gate, const BwdLayout &L, uint8_t *bw, float aux_coef, float z_coef,
-                              float *dw_r, float *db_r, cudaStream_t s) {
+cudaError_t launch_router_bwd(const moe_config &c, const float *w_r, const int32_t *topk_idx, const float *topk_gate,
+                              const BwdLayout &L, uint8_t *bw, float aux_coef, float z_coef, float *dw_r, float *db_r,
+                              uint32_t *err, bool allow_pair, cudaStream_t s) {
     float *logits = reinterpret_cast<float *>(bw + L.logits);
     int32_t *routed = reinterpret_cast<int32_t *>(bw + L.routed);
     float *dL = reinterpret_cast<float *>(bw + L.dL);
@@ -412,23 +385,23 @@ cudaError_t launch_router_bwd(const moe_config &c, const void *x, const float *w
                      c.k, c.gating, aux_coef, z_coef, dL};
     k_router_bwd<<<(c.T + 7) / 8, 256, 0, s>>>(ra);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    // dx_router [T][d] = dL [T][N] · W_rᵀ  (W_r is [d][N])
-    k_simt_gemm<float, false, true><<<dim3((c.d + 63) / 64, (c.T + 63) / 64), 256, 0, s>>>(dL, c.N, w_r, c.N, c.T, c.d,
-                                                                                          c.N, c.N, dxr);
+    const int Kr = (3 * c.N + 63) / 64 * 64, Tp = (c.T + 63) / 64 * 64;
+    __nv_bfloat16 *rA = reinterpret_cast<__nv_bfloat16 *>(bw + L.rA), *rB = reinterpret_cast<__nv_bfloat16 *>(bw + L.rB);
+    __nv_bfloat16 *dLt = reinterpret_cast<__nv_bfloat16 *>(bw + L.dLt);
+    // dx_router [T][d] = [dL_hi | dL_hi | dL_lo] · [W_hi | W_lo | W_hi]ᵀ  (W_r is [d][N]: K-major)
+    k_split3<<<grid_of((int64_t)c.T * Kr, 256), 256, 0, s>>>(dL, c.T, c.N, Kr, 0, 0, 1, rA);
+    k_split3<<<grid_of((int64_t)c.d * Kr, 256), 256, 0, s>>>(w_r, c.d, c.N, Kr, 0, 1, 0, rB);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    // dW_r [d][N] = xᵀ [d][T] · dL [T][N], split over the tokens into slabs summed in order
-    const int zs = dwr_splits(c);
-    const int kchunk = ((c.T + zs - 1) / zs + 15) / 16 * 16;
-    float *slabs = reinterpret_cast<float *>(bw + L.wr_slabs);
-    const dim3 g3((c.N + 63) / 64, (c.d + 63) / 64, zs);
-    if (c.dtype == MOE_BF16)
-        k_simt_gemm<__nv_bfloat16, true, false><<<g3, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(x), c.d, dL, c.N,
-                                                                  c.d, c.N, c.T, kchunk, slabs);
-    else
-        k_simt_gemm<float, true, false><<<g3, 256, 0, s>>>(static_cast<const float *>(x), c.d, dL, c.N, c.d, c.N, c.T,
-                                                          kchunk, slabs);
+    e = launch_wgrad(nullptr, 0, 0, nullptr, nullptr, 0, c.T, c.d, nullptr, rA, rB, Kr, dxr, err, s, allow_pair, true);
+    if (e != cudaSuccess) return e;
+    // dW_rᵀ halves [2N][d] = [dL_hiᵀ ; dL_loᵀ] · (xᵀ)ᵀ over the tokens (x exact in bf16, xᵀ [d][Tp])
+    k_split_t<<<dim3(Tp / 32, (c.N + 31) / 32), 256, 0, s>>>(dL, c.T, c.N, Tp, dLt);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    k_sum_slabs<<<grid_of((int64_t)c.d * c.N, 256), 256, 0, s>>>(slabs, zs, (int64_t)c.d * c.N, dw_r);
+    float *wrC = reinterpret_cast<float *>(bw + L.wrC);
+    e = launch_wgrad(nullptr, 0, 0, nullptr, nullptr, 0, 2 * c.N, c.d, nullptr, dLt, bw + L.x_t, Tp, wrC, err, s,
+                     allow_pair, true);
+    if (e != cudaSuccess) return e;
+    k_sum_hi_lo_t<<<dim3((c.d + 31) / 32, (c.N + 31) / 32), 256, 0, s>>>(wrC, c.N, c.d, dw_r);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (db_r) {
         k_col_sum<<<(c.N + 255) / 256, 256, 0, s>>>(dL, c.T, c.N, db_r);

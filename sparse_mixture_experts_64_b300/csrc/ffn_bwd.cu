@@ -33,12 +33,13 @@ constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + 1024;
 struct WgParams {
     CUtensorMap tmA, tmB;        // At [M][Kall] (box 64 x 128), Bt [Nn][Kall] (box 64 x 256)
     CUtensorMap tmA_sh, tmB_sh;  // shared segment: [M][K_sh], [Nn][K_sh]
-    CUtensorMap tmC, tmC_sh;     // outputs for the pair kernel's stores: [n_seg][M][Nn], [1][M][Nn], box 64 x 32 x 1
+    CUtensorMap tmC, tmC_sh;     // outputs for the pair kernel's stores: [n_seg][M][Nn], [1][M][Nn], box of
+                                 // 32 rows x 128 bytes (64 bf16 or 32 fp32 columns)
     const int32_t *offsets;      // [n_seg + 1] rows of each expert
     int n_seg, has_sh;
     int a_rows;                  // offsets are clamped to it
     int M, Nn, K_sh;
-    __nv_bfloat16 *C, *C_sh;     // [n_seg][M][Nn], [M][Nn]
+    void *C, *C_sh;              // [n_seg][M][Nn], [M][Nn]: bf16, or fp32 in the kernels' F32 form
     uint32_t *err;
 };
 
@@ -49,6 +50,8 @@ struct WgSmem {
     int k0[MAX_SEG], kp[MAX_SEG];  // first column and padded width of each segment's K range
 };
 
+// F32: the output is fp32 (general products of the router gradient), else bf16.
+template <bool F32>
 __global__ void __launch_bounds__(NUM_THREADS, 1) k_wgrad_tc(const __grid_constant__ WgParams p) {
     __shared__ WgSmem s;
     extern __shared__ uint8_t dyn_smem[];
@@ -211,7 +214,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_wgrad_tc(const __grid_consta
             tc_fence_after();
             const int row = m * BM + r_in_tile;
             const bool empty_seg = s.kp[g] == 0;
-            __nv_bfloat16 *crow = (sh ? p.C_sh : p.C + (size_t)g * p.M * p.Nn) + (size_t)row * p.Nn;
+            const size_t crow = ((sh ? 0 : (size_t)g * p.M) + (size_t)row) * p.Nn;  // element offset of the row
             const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16);
 #pragma unroll 1
             for (int c = 0; c < BN; c += 32) {
@@ -219,7 +222,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_wgrad_tc(const __grid_consta
                 tmem_ld32(tbase + c, v);
                 tmem_ld_wait();
                 const int col = n * BN + c;
-                if (row < p.M && col < p.Nn) {
+                if (F32 && row < p.M && col < p.Nn) {
+                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(sh ? p.C_sh : p.C) + crow + col);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        dst[q] = empty_seg ? make_float4(0.0f, 0.0f, 0.0f, 0.0f)
+                                           : make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                                         __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+                } else if (!F32 && row < p.M && col < p.Nn) {
                     uint32_t packed[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
@@ -228,7 +238,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_wgrad_tc(const __grid_consta
                         __nv_bfloat162 b = __floats2bfloat162_rn(f0, f1);
                         packed[i] = *reinterpret_cast<uint32_t *>(&b);
                     }
-                    uint4 *dst = reinterpret_cast<uint4 *>(crow + col);
+                    uint4 *dst =
+                        reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(sh ? p.C_sh : p.C) + crow + col);
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
                         dst[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
@@ -259,8 +270,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_wgrad_tc(const __grid_consta
 // halves complete on the even CTA's stage barrier, the even CTA issues the MMAs and
 // its commits arrive on both CTAs' barriers; each CTA's epilogue stores its 128 rows.
 // The epilogue writes through shared memory: each warp converts 32 rows x 64 columns
-// to bf16 into one of two 4 KB boxes laid out as the output map's 128-byte swizzle and
-// stores the box with one TMA tensor store, so whole 128-byte lines reach L2. With an
+// to bf16 (32 columns in the fp32 form) into one of two 4 KB boxes laid out as the
+// output map's 128-byte swizzle and stores the box with one TMA tensor store, so whole
+// 128-byte lines reach L2. With an
 // expert's few hundred rows as K, a tile's MMAs are short next to its 128 KB of
 // gradient, and per-thread 16-byte row stores (32 rows per instruction) kept L2 busy
 // with partial-line write requests.
@@ -280,6 +292,7 @@ static_assert(SMEM2_BYTES + sizeof(WgSmem2) <= 232448, "shared memory budget of 
 static_assert(STAGE2_BYTES % 1024 == 0 && OUT_BOX_BYTES % 1024 == 0, "swizzled boxes stay 1024-byte aligned");
 
 // Tensor maps as in WgParams but with 128-row boxes for Bt (each CTA loads half).
+template <bool F32>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     k_wgrad_tc2(const __grid_constant__ WgParams p) {
     __shared__ WgSmem2 s;
@@ -467,14 +480,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             const CUtensorMap *cmap = sh ? &p.tmC_sh : &p.tmC;
             const int gz = sh ? 0 : g;
             const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16);
+            constexpr int CW = F32 ? 32 : 64;  // columns per 128-byte box row
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 64) {
+            for (int c = 0; c < BN; c += CW) {
                 uint32_t v[64];
                 tmem_ld32(tbase + c, v);
-                tmem_ld32(tbase + c + 32, v + 32);
+                if (!F32) tmem_ld32(tbase + c + 32, v + 32);
                 tmem_ld_wait();
                 const int col = n * BN + c;
-                // M and Nn are multiples of 64: a box lies wholly inside the output or wholly outside
+                // Nn is a multiple of 64: a box's columns lie wholly inside the output or outside;
+                // rows past M (a box straddling it) are clipped by the tensor store
                 if (row0 < p.M && col < p.Nn) {
                     uint8_t *box = boxes + (nbox & 1u) * OUT_BOX_BYTES;
                     if (lane == 0) bulk_wait_group_read<1>();  // the store of two boxes ago has read this box
@@ -485,10 +500,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                         uint32_t w[4];
 #pragma unroll
                         for (int t = 0; t < 4; ++t) {
-                            const float f0 = empty_seg ? 0.0f : __uint_as_float(v[8 * j + 2 * t]);
-                            const float f1 = empty_seg ? 0.0f : __uint_as_float(v[8 * j + 2 * t + 1]);
-                            __nv_bfloat162 b = __floats2bfloat162_rn(f0, f1);
-                            w[t] = *reinterpret_cast<uint32_t *>(&b);
+                            if constexpr (F32) {
+                                w[t] = empty_seg ? 0u : v[4 * j + t];
+                            } else {
+                                const float f0 = empty_seg ? 0.0f : __uint_as_float(v[8 * j + 2 * t]);
+                                const float f1 = empty_seg ? 0.0f : __uint_as_float(v[8 * j + 2 * t + 1]);
+                                __nv_bfloat162 b = __floats2bfloat162_rn(f0, f1);
+                                w[t] = *reinterpret_cast<uint32_t *>(&b);
+                            }
                         }
                         *reinterpret_cast<uint4 *>(rowp + ((j ^ swz) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
                     }
@@ -603,12 +622,31 @@ __global__ void __launch_bounds__(256) k_transpose_rows_padded(const __nv_bfloat
 
 int64_t wgrad_kall_bound(const moe_config &c) { return (max_rows(c) + 64LL * c.N + 63) / 64 * 64; }
 
+// Output map of the pair kernel's tensor stores: [n][M][Nn] of bf16 or fp32, box of 32
+// rows x 128 bytes, 128-byte swizzle.
+static bool encode_out_map(CUtensorMap *m, void *base, int Nn, int M, int n, bool f32) {
+    const uint64_t es = f32 ? 4 : 2;
+    const uint64_t dims[3] = {(uint64_t)Nn, (uint64_t)M, (uint64_t)n};
+    const uint64_t strides[2] = {(uint64_t)Nn * es, (uint64_t)Nn * M * es};
+    const uint32_t box[3] = {(uint32_t)(128 / es), 32u, 1u};
+    return encode_tmap(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims,
+                       strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+template <typename Kern> static cudaError_t smem_attr_once(Kern kern, size_t bytes, bool &done) {
+    if (done) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) done = true;
+    return e;
+}
+
 cudaError_t launch_wgrad(const int32_t *offsets, int n_seg, int64_t a_rows, const void *At, const void *Bt,
                          int64_t Kall, int M, int Nn, void *out, const void *At_sh, const void *Bt_sh, int K_sh,
-                         void *out_sh, uint32_t *err, cudaStream_t s, bool allow_pair) {
+                         void *out_sh, uint32_t *err, cudaStream_t s, bool allow_pair, bool f32_out) {
     // CTA pairs once a 256-row output tile is not mostly empty
     const bool pair = allow_pair && M >= 2 * BM;
     const uint32_t box_b = pair ? BN / 2 : BN;
+    if (Nn % 64 != 0) return cudaErrorInvalidValue;
     WgParams p;
     memset(&p, 0, sizeof(p));
     p.offsets = offsets;
@@ -618,44 +656,41 @@ cudaError_t launch_wgrad(const int32_t *offsets, int n_seg, int64_t a_rows, cons
     p.M = M;
     p.Nn = Nn;
     p.K_sh = K_sh;
-    p.C = static_cast<__nv_bfloat16 *>(out);
-    p.C_sh = static_cast<__nv_bfloat16 *>(out_sh);
+    p.C = out;
+    p.C_sh = out_sh;
     p.err = err;
     if (n_seg > 0) {
         if (!encode_bf16_2d(&p.tmA, At, (uint64_t)Kall, (uint64_t)M, BM)) return cudaErrorInvalidValue;
         if (!encode_bf16_2d(&p.tmB, Bt, (uint64_t)Kall, (uint64_t)Nn, box_b)) return cudaErrorInvalidValue;
-        if (pair && !encode_bf16_3d(&p.tmC, out, (uint64_t)Nn, (uint64_t)M, (uint64_t)n_seg, 32))
-            return cudaErrorInvalidValue;
+        if (pair && !encode_out_map(&p.tmC, out, Nn, M, n_seg, f32_out)) return cudaErrorInvalidValue;
     }
     if (p.has_sh) {
         if (!encode_bf16_2d(&p.tmA_sh, At_sh, (uint64_t)K_sh, (uint64_t)M, BM)) return cudaErrorInvalidValue;
         if (!encode_bf16_2d(&p.tmB_sh, Bt_sh, (uint64_t)K_sh, (uint64_t)Nn, box_b)) return cudaErrorInvalidValue;
-        if (pair && !encode_bf16_3d(&p.tmC_sh, out_sh, (uint64_t)Nn, (uint64_t)M, 1, 32)) return cudaErrorInvalidValue;
+        if (pair && !encode_out_map(&p.tmC_sh, out_sh, Nn, M, 1, f32_out)) return cudaErrorInvalidValue;
     }
+    cudaError_t e;
     if (pair) {
         const int64_t tiles2 = (int64_t)(n_seg + p.has_sh) * ((M + 2 * BM - 1) / (2 * BM)) * ((Nn + BN - 1) / BN);
         if (tiles2 == 0) return cudaSuccess;
-        static bool attr2_done = false;
-        if (!attr2_done) {
-            cudaError_t e =
-                cudaFuncSetAttribute(k_wgrad_tc2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM2_BYTES);
-            if (e != cudaSuccess) return e;
-            attr2_done = true;
-        }
+        static bool done_h = false, done_f = false;
+        if ((e = f32_out ? smem_attr_once(k_wgrad_tc2<true>, SMEM2_BYTES, done_f)
+                         : smem_attr_once(k_wgrad_tc2<false>, SMEM2_BYTES, done_h)) != cudaSuccess)
+            return e;
         const int clusters = (int)std::max<int64_t>(1, std::min<int64_t>(tiles2, device_sm_count() / 2));
-        k_wgrad_tc2<<<2 * clusters, NUM_THREADS, SMEM2_BYTES, s>>>(p);
+        if (f32_out) k_wgrad_tc2<true><<<2 * clusters, NUM_THREADS, SMEM2_BYTES, s>>>(p);
+        else k_wgrad_tc2<false><<<2 * clusters, NUM_THREADS, SMEM2_BYTES, s>>>(p);
         return cudaGetLastError();
     }
     const int64_t tiles = (int64_t)(n_seg + p.has_sh) * ((M + BM - 1) / BM) * ((Nn + BN - 1) / BN);
     if (tiles == 0) return cudaSuccess;
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(k_wgrad_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
+    static bool done1_h = false, done1_f = false;
+    if ((e = f32_out ? smem_attr_once(k_wgrad_tc<true>, SMEM_BYTES, done1_f)
+                     : smem_attr_once(k_wgrad_tc<false>, SMEM_BYTES, done1_h)) != cudaSuccess)
+        return e;
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, device_sm_count()));
-    k_wgrad_tc<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(p);
+    if (f32_out) k_wgrad_tc<true><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(p);
+    else k_wgrad_tc<false><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(p);
     return cudaGetLastError();
 }
 

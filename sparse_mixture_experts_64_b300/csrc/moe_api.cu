@@ -404,8 +404,9 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const float *w_r, 
     if (hs) {
         ok(launch_transpose_rows_padded(dy, d, nullptr, nullptr, 1, c.T, Tp, bw + B.dy_t, sa));
         ok(launch_transpose_rows_padded(hid_sh, hs, nullptr, nullptr, 1, c.T, Tp, bw + B.Hsh_t, sa));
-        ok(launch_transpose_rows_padded(x, d, nullptr, nullptr, 1, c.T, Tp, bw + B.x_t, sa));
     }
+    // xᵀ: the shared expert's and the router's weight gradients
+    ok(launch_transpose_rows_padded(x, d, nullptr, nullptr, 1, c.T, Tp, bw + B.x_t, sa));
     // router logits, recomputed
     ok(launch_router_logits(c, x, w_r, c.has_router_bias ? b_r : nullptr, reinterpret_cast<float *>(bw + B.logits), w,
                             sa));
@@ -452,8 +453,8 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const float *w_r, 
                         bw + B.x_t, (int)Tp, dshared_w_up, err, stream, pair_ok));
     }
     // router: dL, dx_router, dW_r, db
-    ok(launch_router_bwd(c, x, w_r, idx, gate, B, bw, aux_coef, z_coef, dw_r, c.has_router_bias ? db_r : nullptr,
-                         stream));
+    ok(launch_router_bwd(c, w_r, idx, gate, B, bw, aux_coef, z_coef, dw_r, c.has_router_bias ? db_r : nullptr, err,
+                         pair_ok, stream));
     // dx = dy + sum_j dX_r + dX_shared + dx_router
     ok(launch_bwd_dx(c, dy, dX, slot_row, hs ? bw + B.dX_sh : nullptr, reinterpret_cast<const float *>(bw + B.dxr), dx,
                      err, stream));

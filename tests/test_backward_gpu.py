@@ -3,7 +3,9 @@ against torch autograd and finite differences).
 
 The GPU keeps dy, the gate-scaled rows dO, the hidden activations H, the recomputed
 pre-activations A and B, dH and [dA | dB] in bf16 and accumulates in fp32 (the
-router's gradients are fp32 throughout). Each of those roundings is relative
+router's gradients are fp32; its two contractions multiply bf16 hi/lo splits of the
+fp32 operands, whose products the fp32 accumulator holds exactly, within 2^-15 of the
+fp32 products). Each of those roundings is relative
 (2^-9), so a gradient element's error is proportional to its own size, and the
 gradients are heavy-tailed (elements 10-20 times their RMS occur). A float64
 simulation of exactly those roundings (and of the bf16 outputs) on these shapes gives
@@ -52,6 +54,8 @@ CASES = [
     # 128 routed rows over 64 experts: many experts without rows on the pair
     # weight-gradient kernel (their gradients are stored as zero boxes)
     (_w("deepseek_fine", T=64, d=256, N=64, k=2, h=256, h_shared=256), 0.01, 0.0),
+    # N = 128: both router-gradient products on CTA pairs (2N = 256 and T = 320 rows)
+    (_w("deepseek_fine", T=320, d=256, N=128, k=4, h=128, h_shared=0), 0.01, 0.001),
 ]
 
 
