@@ -470,43 +470,63 @@ def measure_router_train(w, inp, cfg, ws, stream, dev, cpu_tokens: int) -> dict:
 
 
 def measure_backward(w, inp, cfg, ws, stream, dev, peaks, host_inp=None, cpu_tokens: int = 16) -> dict:
-    """moe_backward after one moe_forward on the same inputs: CUDA-event time per
-    backward, its algorithmic FLOPs against the bf16 peak, and the oracle's backward
-    timed on a token slice of the same layer."""
+    """The training step's backward: moe_forward with save_preact (it keeps the experts'
+    pre-activations) and moe_backward on the same inputs. CUDA-event times of the
+    backward alone, of the keeping forward alone and of the pair back to back; the
+    backward's algorithmic FLOPs (the gradient products: dH, dX and the weight gradients
+    of the experts and the shared expert, and the router's two) against the bf16 peak;
+    the backward that recomputes the pre-activations (plain forward) for comparison; and
+    the oracle's backward timed on a token slice of the same layer."""
     import sparse_mixture_experts_64_b300 as moe
     T, d, N, k = w.T, w.d, w.N, w.k
-    bws = moe.backward_workspace(cfg, device=dev)
+    keep_cfg = moe.make_config(**{f: getattr(w, f) for f in w.__dataclass_fields__}, save_preact=True)
+    ws_keep = moe.workspace(keep_cfg, device=dev)
+    bws = moe.backward_workspace(cfg, device=dev)  # the larger one: it holds recomputed pre-activations
     idx = torch.empty((T, k), dtype=torch.int32, device=dev)
     gate = torch.empty((T, k), device=dev)
     y = torch.empty((T, d), dtype=inp["x"].dtype, device=dev)
     kept = torch.empty(N, dtype=torch.int32, device=dev)
-    moe.moe_forward(cfg, inp["x"], inp["w_r"], inp["b_r"], inp["w_gate"], inp["w_up"], inp["w_down"],
-                    inp["shared_w_gate"], inp["shared_w_up"], inp["shared_w_down"], y, idx, gate, None, kept,
-                    None, ws, stream)
+
+    def fwd(c, wsp):
+        moe.moe_forward(c, inp["x"], inp["w_r"], inp["b_r"], inp["w_gate"], inp["w_up"], inp["w_down"],
+                        inp["shared_w_gate"], inp["shared_w_up"], inp["shared_w_down"], y, idx, gate, None, kept,
+                        None, wsp, stream)
     g = torch.Generator(device=dev).manual_seed(17)
     dy = torch.randn((T, d), device=dev, generator=g).to(inp["x"].dtype)
     e = lambda t: None if t is None else torch.empty_like(t)  # noqa: E731
     out = [e(inp["x"]), e(inp["w_r"]), e(inp["b_r"]), e(inp["w_gate"]), e(inp["w_up"]), e(inp["w_down"]),
            e(inp["shared_w_gate"]), e(inp["shared_w_up"]), e(inp["shared_w_down"])]
 
-    def bwd():
-        moe.moe_backward(cfg, inp["x"], inp["w_r"], inp["b_r"], inp["w_gate"], inp["w_up"], inp["w_down"],
+    def bwd(c, wsp):
+        moe.moe_backward(c, inp["x"], inp["w_r"], inp["b_r"], inp["w_gate"], inp["w_up"], inp["w_down"],
                          inp["shared_w_gate"], inp["shared_w_up"], inp["shared_w_down"], idx, gate, dy, 0.01, 0.001,
-                         *out, ws, bws, stream)
-    ms = _time_calls(bwd, stream, 10)
-    st = moe.moe_check_error(ws, stream)
-    if st != moe.MOE_OK:
-        raise RuntimeError("device error word: " + moe.status_str(st))
+                         *out, wsp, bws, stream)
+    fwd(cfg, ws)
+    ms_recompute = _time_calls(lambda: bwd(cfg, ws), stream, 10)
+    fwd(keep_cfg, ws_keep)
+    ms = _time_calls(lambda: bwd(keep_cfg, ws_keep), stream, 10)
+    fwd_keep_ms = _time_calls(lambda: fwd(keep_cfg, ws_keep), stream, 10)
+    step_ms = _time_calls(lambda: (fwd(keep_cfg, ws_keep), bwd(keep_cfg, ws_keep)), stream, 10)
+    for wsp in (ws, ws_keep):
+        st = moe.moe_check_error(wsp, stream)
+        if st != moe.MOE_OK:
+            raise RuntimeError("device error word: " + moe.status_str(st))
     R = int(kept.sum().item())
     gated = w.act == "silu_gated"
-    # recomputed pre-activations, dH, dX, and the weight gradients (each 2 R d h per matrix)
-    per = (4 + 2 + 4 + 2 + 4) if gated else (2 + 2 + 2 + 2 + 2)
-    flops = per * R * d * w.h + (16 * T * d * w.h_shared if w.h_shared else 0) + 2 * 2 * T * d * N
+    # dH (2 R d h), dX (4 R d h gated, else 2), the weight gradients (6 or 4 R d h); the
+    # shared expert's 12 T d h_shared; the router's dx and dW_r (2 T d N each)
+    per = 12 if gated else 8
+    flops = per * R * d * w.h + (12 * T * d * w.h_shared if w.h_shared else 0) + 2 * 2 * T * d * N
+    tf = lambda m: flops / (m / 1e3) / 1e12  # noqa: E731
     out_d = {"ms": ms, "tokens_per_s": T / (ms / 1e3), "rows": R, "algorithmic_flops": flops,
-             "achieved_tflops": flops / (ms / 1e3) / 1e12, "bound": "tensor",
-             "frac": flops / (ms / 1e3) / 1e12 / peaks["bf16"],
+             "achieved_tflops": tf(ms), "bound": "tensor", "frac": tf(ms) / peaks["bf16"],
              "peak": f"{peaks['source']} bf16 burst {peaks['bf16']} TFLOP/s",
-             "note": "includes the per-call transposes of the expert weights (HBM)"}
+             "pre_activations": "kept by the forward (save_preact)",
+             "forward_keeping_ms": fwd_keep_ms, "forward_plus_backward_ms": step_ms,
+             "recompute": {"ms": ms_recompute, "achieved_tflops": tf(ms_recompute),
+                           "frac": tf(ms_recompute) / peaks["bf16"],
+                           "note": "plain forward; the backward recomputes the pre-activations "
+                                   "(not counted as algorithmic FLOPs)"}}
     if host_inp is not None:
         from oracle import moe_oracle as O
         n = min(T, cpu_tokens)

@@ -102,6 +102,9 @@ typedef struct {
     int32_t has_router_bias;  /* 1: b_r is read and added to the logits              */
     int32_t debug_flags;      /* MOE_DEBUG_* bits, 0 in normal use                   */
     int32_t routing;          /* moe_routing: token choice (top-k) or Expert Choice  */
+    int32_t save_preact;      /* 1: moe_forward also keeps the experts' pre-activations
+                                 in the workspace and moe_backward reads them instead of
+                                 recomputing them (see moe_backward); 0 or 1          */
 } moe_config;
 
 /* debug_flags bits */
@@ -135,6 +138,15 @@ size_t moe_workspace_size(const moe_config *cfg);
  * the full workspace, smaller than moe_workspace_size(cfg). 0 when the config is
  * invalid or uses Expert Choice routing. No CUDA call is made. */
 size_t moe_router_workspace_size(const moe_config *cfg);
+
+/* Byte offset in the workspace of the pre-activations moe_forward keeps when
+ * cfg->save_preact = 1 (see moe_backward): shared = 0, the routed experts' rows
+ * [R_max][W] bf16 in dispatch order (row r of expert e's range holds the token
+ * perm_token[r]; W = 2h with X W_gateᵀ in columns [0, h) and X W_upᵀ in [h, 2h), or
+ * W = h with X W1ᵀ for ReLU experts); shared = 1, the shared expert's [T][2 h_shared].
+ * Rows past the kept row count are not written. SIZE_MAX when the config keeps none
+ * (or has no shared expert). No CUDA call is made. */
+size_t moe_preact_offset(const moe_config *cfg, int32_t shared);
 
 /* Worst-case dispatched row count R_max for `cfg` (see above); 0 if invalid. */
 int64_t moe_max_rows(const moe_config *cfg);
@@ -398,7 +410,12 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const float *w_r,
  *   [N][d][h], dshared_* shaped like the shared weights — all bf16 outputs.
  * x, w_r, dy, dx, the expert and shared-expert weights and their gradients must be
  * 16-byte aligned (MOE_ERR_INVALID_ARG otherwise).
- * The row products read the expert weights in their own layout; the weight
+ * The backward needs the experts' pre-activations (X W_gateᵀ and X W_upᵀ, or X W1ᵀ, and
+ * the shared expert's): with cfg->save_preact = 1, moe_forward stores them in ws as its
+ * first product computes them (bf16 token choice on the tensor-core kernels; not with
+ * MOE_DEBUG_FORCE_SIMT_FFN or MOE_DEBUG_FFN_SWAP) and moe_backward reads them, else
+ * moe_backward recomputes them; moe_forward and moe_backward must then get the same
+ * cfg. The row products read the expert weights in their own layout; the weight
  * gradients reduce over each expert's rows on the tensor cores. The transposed forward
  * activations and the recomputed router logits run on a non-blocking auxiliary stream
  * that the call creates, joins to `stream` with an event where their results are

@@ -37,14 +37,14 @@ EXPORTED = ("moe_validate_config", "moe_workspace_size", "moe_max_rows", "moe_ca
             "moe_router_expert_choice", "moe_combine_expert_choice", "moe_backward",
             "moe_backward_workspace_size", "moe_forward_graph_create", "moe_forward_graph_launch",
             "moe_forward_graph_destroy", "moe_router_workspace_size",
-            "moe_router_noalloc_check_error")
+            "moe_router_noalloc_check_error", "moe_preact_offset")
 
 
 class moe_config(ctypes.Structure):
     """Mirror of the C struct moe_config (all fields int32)."""
     _fields_ = [(n, ctypes.c_int32) for n in (
         "T", "d", "N", "k", "h", "h_shared", "dtype", "gating", "act", "cap_num", "cap_den",
-        "has_router_bias", "debug_flags", "routing")]
+        "has_router_bias", "debug_flags", "routing", "save_preact")]
 
 
 class MoeError(RuntimeError):
@@ -64,6 +64,7 @@ def _load() -> ctypes.CDLL:
         "moe_validate_config": (I32, [cfgp]),
         "moe_workspace_size": (SZ, [cfgp]),
         "moe_router_workspace_size": (SZ, [cfgp]),
+        "moe_preact_offset": (SZ, [cfgp, I32]),
         "moe_router_noalloc_check_error": (I32, [P]),
         "moe_max_rows": (I64, [cfgp]),
         "moe_capacity": (I32, [cfgp]),
@@ -106,7 +107,7 @@ moe_status_str = status_str
 
 def make_config(T, d, N, k, h, h_shared=0, dtype="bf16", gating="topk_then_softmax",
                 act="silu_gated", capacity_factor=None, router_bias=False, debug_flags=0,
-                routing="token_choice", **_ignored) -> moe_config:
+                routing="token_choice", save_preact=False, **_ignored) -> moe_config:
     """Build a moe_config from plain fields (the names used by the workload table)."""
     c = moe_config()
     c.T, c.d, c.N, c.k, c.h, c.h_shared = T, d, N, k, h, h_shared
@@ -121,6 +122,7 @@ def make_config(T, d, N, k, h, h_shared=0, dtype="bf16", gating="topk_then_softm
     c.debug_flags = debug_flags
     c.routing = ({"token_choice": MOE_ROUTING_TOKEN_CHOICE, "expert_choice": MOE_ROUTING_EXPERT_CHOICE}[routing]
                  if isinstance(routing, str) else int(routing))
+    c.save_preact = 1 if save_preact else 0
     return c
 
 
@@ -159,6 +161,21 @@ def moe_router_workspace_size(cfg) -> int:
 
 def moe_max_rows(cfg) -> int:
     return _lib.moe_max_rows(ctypes.byref(cfg))
+
+
+def moe_preact_offset(cfg, shared=False) -> int:
+    return _lib.moe_preact_offset(ctypes.byref(cfg), 1 if shared else 0)
+
+
+def preact_view(cfg, ws, shared=False) -> torch.Tensor:
+    """The pre-activations moe_forward kept in `ws` (save_preact) as a bf16 tensor view:
+    [R_max][W] (routed, dispatch order) or [T][2 h_shared] (shared expert)."""
+    off = moe_preact_offset(cfg, shared)
+    if off == ctypes.c_size_t(-1).value:
+        raise MoeError(MOE_ERR_INVALID_ARG, "moe_preact_offset")
+    rows = cfg.T if shared else moe_max_rows(cfg)
+    width = 2 * cfg.h_shared if shared else (2 * cfg.h if cfg.act == MOE_ACT_SILU_GATED else cfg.h)
+    return ws[off:off + rows * width * 2].view(torch.bfloat16).view(rows, width)
 
 
 def moe_capacity(cfg) -> int:

@@ -318,7 +318,8 @@ BwdLayout bwd_layout(const moe_config &c) {
     };
     L.dO = take(R * d * 2);
     L.dgate = take(T * c.k * 4);
-    L.AB = take(R * W * 2);
+    const bool kept_pre = saves_preact(c);  // then the forward's workspace holds the pre-activations
+    L.AB = take(kept_pre ? 0 : R * W * 2);
     L.dH = take(R * h * 2);
     L.dAB = take(R * W * 2);
     L.dX = take(R * d * 2);
@@ -327,7 +328,7 @@ BwdLayout bwd_layout(const moe_config &c) {
     L.H_t = take(h * Kall * 2);
     L.dAB_t = take(W * Kall * 2);
     L.X_t = take(d * Kall * 2);
-    L.AB_sh = take(hs ? T * 2 * hs * 2 : 0);
+    L.AB_sh = take(hs && !kept_pre ? T * 2 * hs * 2 : 0);
     L.dH_sh = take(hs ? T * hs * 2 : 0);
     L.dAB_sh = take(hs ? T * 2 * hs * 2 : 0);
     L.dX_sh = take(hs ? T * d * 2 : 0);

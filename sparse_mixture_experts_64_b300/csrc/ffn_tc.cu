@@ -69,6 +69,9 @@ struct TcParams {
     int a_rows;                    // rows of the routed buffers; offsets are clamped to it
     int n_out, K, n_out_sh, K_sh;
     __nv_bfloat16 *C, *C_sh;
+    // Gated and ReLU products: null, or where the raw pre-activations are stored too
+    // (gated: gate in columns [0, n_out), up in [n_out, 2 n_out) of 2 n_out-wide rows)
+    __nv_bfloat16 *P, *P_sh;
     uint32_t *err;
     // Which routed segments this launch covers: all (0); those whose last 256-row
     // block holds more than 128 rows or is full (1: the pair kernel); those whose
@@ -136,8 +139,11 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16 *dst, const uint32_t
 template <bool SPLIT64> __device__ __forceinline__ int gate_col(int c) { return SPLIT64 ? (c >> 6) * 128 + (c & 63) : c; }
 template <bool SPLIT64> __device__ __forceinline__ int up_col(int c) { return gate_col<SPLIT64>(c) + (SPLIT64 ? 64 : 128); }
 
+// prow (gated and ReLU products): null, or the row of the pre-activation output, where
+// the raw accumulators are stored as well (gated: gate at col, up at n_out + col).
 template <int KIND, bool SPLIT64 = false>
-__device__ __forceinline__ void epilogue_row(uint32_t tbase, __nv_bfloat16 *crow, int col0, int n_out, bool row_ok) {
+__device__ __forceinline__ void epilogue_row(uint32_t tbase, __nv_bfloat16 *crow, int col0, int n_out, bool row_ok,
+                                             __nv_bfloat16 *prow = nullptr) {
     if constexpr (KIND == KIND_PREACT) {
 #pragma unroll 1
         for (int c = 0; c < 128; c += 32) {
@@ -159,6 +165,10 @@ __device__ __forceinline__ void epilogue_row(uint32_t tbase, __nv_bfloat16 *crow
             tmem_ld32(tbase + up_col<SPLIT64>(c), u);
             tmem_ld_wait();
             const int col = col0 + c;
+            if (prow && row_ok && col < n_out) {
+                store_bf16x32(prow + col, g);
+                store_bf16x32(prow + n_out + col, u);
+            }
             if (row_ok && col < n_out) {
                 uint32_t packed[16];
 #pragma unroll
@@ -181,6 +191,7 @@ __device__ __forceinline__ void epilogue_row(uint32_t tbase, __nv_bfloat16 *crow
             tmem_ld32(tbase + c, v);
             tmem_ld_wait();
             const int col = col0 + c;
+            if (KIND == KIND_RELU && prow && row_ok && col < n_out) store_bf16x32(prow + col, v);
             if (row_ok && col < n_out) {
                 uint32_t packed[16];
 #pragma unroll
@@ -420,8 +431,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_ffn_tc(const __grid_constant
             const int64_t orow = (int64_t)s.row0[ti.seg] + ti.m * BM + r_in_tile;
             const int n_out = sh ? p.n_out_sh : p.n_out;
             __nv_bfloat16 *crow = (sh ? p.C_sh : p.C) + orow * n_out * kOutLd<KIND>;
+            __nv_bfloat16 *P = sh ? p.P_sh : p.P;
+            __nv_bfloat16 *prow = P ? P + orow * n_out * (KIND == KIND_GATED ? 2 : 1) : nullptr;
             const uint32_t tbase = tmem_base + (uint32_t)(acc * ACC_COLS) + ((uint32_t)(quarter * 32) << 16);
-            epilogue_row<KIND>(tbase, crow, ti.n * BN_OUT, n_out, row_ok);
+            epilogue_row<KIND>(tbase, crow, ti.n * BN_OUT, n_out, row_ok, prow);
             tc_fence_before();
             mbar_arrive_relaxed(&s.tempty[acc]);
             if (++acc == 2) {
@@ -507,11 +520,13 @@ __device__ __forceinline__ Tile2 decode_tile2(const Smem2 &s, int nseg, int tile
 
 // Tail epilogue of one warp (TMEM lane quarter q of CTA `rank`): the accumulator holds
 // one weight row per lane and one tail token per column (tokens [0, tpad)).
+// pre (gated and ReLU products): null, or the pre-activation output, where the raw
+// accumulators are stored as well (gated rows 2 n_out wide: gate, then up).
 template <int KIND>
 __device__ __forceinline__ bool epilogue_tail(Smem2 &s, uint8_t *xbufs, uint32_t tbase, const Tile2 &t,
                                               int64_t row_tail0, __nv_bfloat16 *out, int n_out, uint32_t rank,
                                               int q, int lane, uint32_t &xcount, volatile int *abort_flag,
-                                              uint32_t *err) {
+                                              uint32_t *err, __nv_bfloat16 *pre = nullptr) {
     const int nchunks = (t.tpad + 31) >> 5;  // the last chunk's columns past t' are never stored
     if constexpr (KIND == KIND_GATED || KIND == KIND_PREACT) {
         // lanes of quarters 0-1: gate rows, 2-3: up rows of hidden units 64 rank + 32 (q & 1) + lane
@@ -535,6 +550,16 @@ __device__ __forceinline__ bool epilogue_tail(Smem2 &s, uint8_t *xbufs, uint32_t
                         out[(row_tail0 + j) * (2 * (int64_t)n_out) + col] = __float2bfloat16_rn(__uint_as_float(v[i]));
                 }
             } else {
+                if (pre) {
+                    // raw gate (quarters 0-1) or up (quarters 2-3) pre-activations of unit hcol
+                    const int col = hcol + (is_gate ? 0 : n_out);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int j = c * 32 + i;
+                        if (col_ok && j < t.tail)
+                            pre[(row_tail0 + j) * (2 * (int64_t)n_out) + col] = __float2bfloat16_rn(__uint_as_float(v[i]));
+                    }
+                }
                 const uint32_t ph = xcount & 1u;
                 ++xcount;
                 if (!is_gate) {
@@ -572,6 +597,8 @@ __device__ __forceinline__ bool epilogue_tail(Smem2 &s, uint8_t *xbufs, uint32_t
             for (int i = 0; i < 32; ++i) {
                 const int j = c * 32 + i;
                 float x = __uint_as_float(v[i]);
+                if (KIND == KIND_RELU && pre && col_ok && j < t.tail)
+                    pre[(row_tail0 + j) * (int64_t)n_out + ocol] = __float2bfloat16_rn(x);
                 if (KIND == KIND_RELU) x = fmaxf(x, 0.0f);
                 if (col_ok && j < t.tail) out[(row_tail0 + j) * (int64_t)n_out + ocol] = __float2bfloat16_rn(x);
             }
@@ -815,6 +842,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             const bool sh = t.seg >= p.n_seg;
             const int n_out = sh ? p.n_out_sh : p.n_out;
             __nv_bfloat16 *C = sh ? p.C_sh : p.C;
+            __nv_bfloat16 *P = sh ? p.P_sh : p.P;
             if (!wait_bar(&s.tfull[acc], aph, abort_flag, p.err)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + (uint32_t)(acc * ACC_COLS) + ((uint32_t)(quarter * 32) << 16);
@@ -822,11 +850,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
                 const int r_seg = t.m * 2 * BM + (int)rank * BM + r_in_tile;  // row within the segment
                 const bool row_ok = r_seg < s.rows[t.seg];
                 const int64_t orow = (int64_t)s.row0[t.seg] + r_seg;
-                epilogue_row<KIND, true>(tbase, C + orow * n_out * kOutLd<KIND>, t.n * BN_OUT, n_out, row_ok);
+                __nv_bfloat16 *prow = P ? P + orow * n_out * (KIND == KIND_GATED ? 2 : 1) : nullptr;
+                epilogue_row<KIND, true>(tbase, C + orow * n_out * kOutLd<KIND>, t.n * BN_OUT, n_out, row_ok, prow);
             } else {
                 const int64_t row_tail0 = (int64_t)s.row0[t.seg] + t.m * 2 * BM;
                 if (!epilogue_tail<KIND>(s, xbufs, tbase, t, row_tail0, C, n_out, rank, quarter, lane, xcount,
-                                         abort_flag, p.err))
+                                         abort_flag, p.err, P))
                     break;
             }
             tc_fence_before();
@@ -892,8 +921,9 @@ cudaError_t product(const int32_t *offsets, int n_seg, int64_t a_rows, const voi
                     const void *b1, int K, int n_out, void *out, int sh_rows, const void *a_sh,
                     const void *b0_sh, const void *b1_sh, int K_sh, int n_out_sh, void *out_sh,
                     uint32_t *err, cudaStream_t s, bool pair, bool b_mn = false, int k_split = 0,
-                    int k_split_sh = 0) {
+                    int k_split_sh = 0, void *pre = nullptr, void *pre_sh = nullptr) {
     if (b_mn && KIND != KIND_PLAIN) return cudaErrorInvalidValue;
+    if ((pre || pre_sh) && KIND != KIND_GATED && KIND != KIND_RELU) return cudaErrorInvalidValue;
     constexpr int BN_OUT = kGatedLayout<KIND> ? 128 : 256;
     // weight rows per TMA box: the single-CTA kernel stages 256 rows (gated: 128 gate +
     // 128 up), the pair kernel 128 per CTA (gated: 64 gate + 64 up)
@@ -911,6 +941,8 @@ cudaError_t product(const int32_t *offsets, int n_seg, int64_t a_rows, const voi
     p.K_sh = K_sh;
     p.C = static_cast<__nv_bfloat16 *>(out);
     p.C_sh = static_cast<__nv_bfloat16 *>(out_sh);
+    p.P = static_cast<__nv_bfloat16 *>(pre);
+    p.P_sh = static_cast<__nv_bfloat16 *>(pre_sh);
     p.err = err;
     p.b_mn = b_mn ? 1 : 0;
     p.k_split = b_mn ? k_split : 0;
@@ -1012,13 +1044,15 @@ cudaError_t launch_ffn_tc(const moe_config &c, const FfnGroup &g, uint32_t *err,
     // product 1: hidden activations
     if (g.act == MOE_ACT_SILU_GATED) {
         e = product<KIND_GATED>(g.offsets, g.n_seg, g.a_rows, g.a, g.w_a, g.w_b, c.d, g.h, g.hid, g.sh_rows,
-                                g.sh_a, g.sh_w_gate, g.sh_w_up, c.d, g.h_sh, g.sh_hid, err, s, pair);
+                                g.sh_a, g.sh_w_gate, g.sh_w_up, c.d, g.h_sh, g.sh_hid, err, s, pair, false, 0, 0,
+                                g.pre, g.sh_pre);
     } else {
         e = product<KIND_RELU>(g.offsets, g.n_seg, g.a_rows, g.a, g.w_a, nullptr, c.d, g.h, g.hid, 0, nullptr,
-                               nullptr, nullptr, 0, 0, nullptr, err, s, pair);
+                               nullptr, nullptr, 0, 0, nullptr, err, s, pair, false, 0, 0, g.pre, nullptr);
         if (e == cudaSuccess && g.sh_rows > 0)
             e = product<KIND_GATED>(nullptr, 0, 0, nullptr, nullptr, nullptr, 0, 0, nullptr, g.sh_rows, g.sh_a,
-                                    g.sh_w_gate, g.sh_w_up, c.d, g.h_sh, g.sh_hid, err, s, false);
+                                    g.sh_w_gate, g.sh_w_up, c.d, g.h_sh, g.sh_hid, err, s, false, false, 0, 0,
+                                    nullptr, g.sh_pre);
     }
     if (e != cudaSuccess) return e;
     if (g.mid_event && (e = cudaEventRecordWithFlags(g.mid_event, s, g.event_flags)) != cudaSuccess) return e;

@@ -54,9 +54,15 @@ struct WsLayout {
     size_t hid;                  // [R_max][h]
     size_t hid_sh;               // [T][h_shared]
     size_t s_out;                // [T][d]  shared expert output
+    // pre-activations kept by moe_forward for moe_backward (saves_preact): bf16 [R_max][W]
+    // (gated: gate in columns [0, h), up in [h, 2h); ReLU: W = h) and [T][2 h_shared]
+    size_t preact, preact_sh;
     size_t total;
 };
 WsLayout ws_layout(const moe_config &c);
+// moe_forward keeps the pre-activations (cfg.save_preact on the bf16 token-choice
+// tensor-core path; not with the forced CUDA-core or weights-as-M kernels).
+bool saves_preact(const moe_config &c);
 
 // Byte offsets of the backward workspace regions (each 256-byte aligned). W = 2h for
 // SiLU-gated experts ([A | B] pre-activations), h for ReLU experts.
@@ -155,6 +161,8 @@ struct FfnGroup {
     const void *sh_w_gate, *sh_w_up, *sh_w_down;
     void *sh_hid;            // [sh_rows][h_shared]
     void *sh_out;            // [sh_rows][d]
+    void *pre, *sh_pre;      // null, or where product 1 also stores its raw pre-activations
+                             // ([a_rows][2h] gated / [a_rows][h] ReLU; [sh_rows][2 h_sh])
     int h_sh;
     cudaEvent_t mid_event;   // if set: recorded between the two products
     unsigned event_flags;    // cudaEventRecordExternal while a graph is being captured

@@ -86,8 +86,17 @@ WsLayout ws_layout(const moe_config &c) {
     L.ec_tok_ptr = take(ec ? (T + 1) * 4 : 0);
     L.ec_tok_rows = take(ec ? rmax * 4 : 0);
     L.ec_row_gate = take(ec ? rmax * 4 : 0);
+    const bool keep = saves_preact(c);
+    const size_t W = c.act == MOE_ACT_SILU_GATED ? 2 * (size_t)c.h : (size_t)c.h;
+    L.preact = take(keep ? rmax * W * 2 : 0);
+    L.preact_sh = take(keep && c.h_shared ? T * 2 * (size_t)c.h_shared * 2 : 0);
     L.total = o;
     return L;
+}
+
+bool saves_preact(const moe_config &c) {
+    return c.save_preact == 1 && c.dtype == MOE_BF16 && c.routing == MOE_ROUTING_TOKEN_CHOICE &&
+           !(c.debug_flags & (MOE_DEBUG_FORCE_SIMT_FFN | MOE_DEBUG_FFN_SWAP));
 }
 
 int device_sm_count() {
@@ -122,6 +131,7 @@ static moe_status validate(const moe_config *c) {
     if (!dim_ok(c->d, c->dtype) || !dim_ok(c->h, c->dtype)) return MOE_ERR_UNSUPPORTED;
     if (c->h_shared && !dim_ok(c->h_shared, c->dtype)) return MOE_ERR_UNSUPPORTED;
     if (c->routing != MOE_ROUTING_TOKEN_CHOICE && c->routing != MOE_ROUTING_EXPERT_CHOICE) return MOE_ERR_INVALID_ARG;
+    if (c->save_preact != 0 && c->save_preact != 1) return MOE_ERR_INVALID_ARG;
     if (c->routing == MOE_ROUTING_EXPERT_CHOICE) {
         if (c->cap_num == 0) return MOE_ERR_INVALID_ARG;  // the experts' capacity is the routing
         if (c->T > kMaxExpertChoiceTokens) return MOE_ERR_UNSUPPORTED;
@@ -180,6 +190,13 @@ size_t moe_workspace_size(const moe_config *cfg) {
 size_t moe_router_workspace_size(const moe_config *cfg) {
     if (validate(cfg) != MOE_OK || cfg->routing != MOE_ROUTING_TOKEN_CHOICE) return 0;
     return ws_layout(*cfg).hid;
+}
+
+size_t moe_preact_offset(const moe_config *cfg, int32_t shared) {
+    if (validate(cfg) != MOE_OK || !saves_preact(*cfg)) return SIZE_MAX;
+    if (shared && !cfg->h_shared) return SIZE_MAX;
+    const WsLayout L = ws_layout(*cfg);
+    return shared ? L.preact_sh : L.preact;
 }
 
 int64_t moe_max_rows(const moe_config *cfg) {
@@ -368,7 +385,10 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const float *w_r, 
     const int64_t R = max_rows(c);
     const int N = c.N, d = c.d, h = c.h, hs = c.h_shared, Wd = gated ? 2 * h : h;
     const int64_t Kall = wgrad_kall_bound(c), Tp = ((int64_t)c.T + 63) / 64 * 64;
-    void *dO = bw + B.dO, *AB = bw + B.AB, *dH = bw + B.dH, *dAB = bw + B.dAB, *dX = bw + B.dX;
+    // pre-activations: kept by moe_forward (save_preact), else recomputed into the scratch
+    const bool kept_pre = saves_preact(c);
+    void *AB = kept_pre ? w + L.preact : bw + B.AB, *AB_sh = kept_pre ? w + L.preact_sh : bw + B.AB_sh;
+    void *dO = bw + B.dO, *dH = bw + B.dH, *dAB = bw + B.dAB, *dX = bw + B.dX;
     float *dgate = reinterpret_cast<float *>(bw + B.dgate);
     int32_t *kpre = reinterpret_cast<int32_t *>(bw + B.kpre);
     cudaError_t e = cudaSuccess;
@@ -415,18 +435,20 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const float *w_r, 
     // -- main stream
     // gate-scaled dy per row and the gate gradients
     ok(launch_bwd_slots(c, dy, y_perm, slot_row, gate, dO, dgate, err, stream));
-    // pre-activations, recomputed: [A | B] (gated) or A (ReLU)
-    ok(launch_gemm_rows(c, gated, offsets, N, R, x_perm, w_gate_or_w1, w_up, d, h, AB, 0, nullptr, nullptr, nullptr, 0,
-                        0, nullptr, err, stream));
-    if (hs)
-        ok(launch_gemm_rows(c, true, nullptr, 0, 0, nullptr, nullptr, nullptr, 0, 0, nullptr, c.T, x, shared_w_gate,
-                            shared_w_up, d, hs, bw + B.AB_sh, err, stream));
+    // pre-activations, recomputed unless the forward kept them: [A | B] (gated) or A (ReLU)
+    if (!kept_pre) {
+        ok(launch_gemm_rows(c, gated, offsets, N, R, x_perm, w_gate_or_w1, w_up, d, h, AB, 0, nullptr, nullptr,
+                            nullptr, 0, 0, nullptr, err, stream));
+        if (hs)
+            ok(launch_gemm_rows(c, true, nullptr, 0, 0, nullptr, nullptr, nullptr, 0, 0, nullptr, c.T, x,
+                                shared_w_gate, shared_w_up, d, hs, AB_sh, err, stream));
+    }
     // dH = dO W_out (W_out [d][h] per expert: MN-major, K = d)
     ok(launch_gemm_rows(c, false, offsets, N, R, dO, w_down, nullptr, d, h, dH, hs ? c.T : 0, dy, shared_w_down,
                         nullptr, d, hs, bw + B.dH_sh, err, stream, true, 0, 0));
     // [dA | dB] from the pre-activations
     ok(launch_act_bwd(gated, AB, dH, R, h, dAB, stream));
-    if (hs) ok(launch_act_bwd(true, bw + B.AB_sh, bw + B.dH_sh, c.T, hs, bw + B.dAB_sh, stream));
+    if (hs) ok(launch_act_bwd(true, AB_sh, bw + B.dH_sh, c.T, hs, bw + B.dAB_sh, stream));
     // dX = [dA | dB] [W_a ; W_b] (W_a, W_b [h][d] per expert: MN-major, K = Wd split at h)
     ok(launch_gemm_rows(c, false, offsets, N, R, dAB, w_gate_or_w1, gated ? w_up : nullptr, Wd, d, dX, hs ? c.T : 0,
                         bw + B.dAB_sh, shared_w_gate, shared_w_up, 2 * hs, d, bw + B.dX_sh, err, stream, true,
@@ -621,6 +643,8 @@ static moe_status forward_impl(const moe_config *cfg, const void *x, const float
     g.act = c.act;
     g.mid_event = ev ? ev[3] : nullptr;
     g.event_flags = ev_flags;
+    const bool keep = saves_preact(c);
+    g.pre = keep ? w + L.preact : nullptr;
     if (c.h_shared) {
         g.sh_rows = c.T;
         g.sh_a = x;
@@ -630,6 +654,7 @@ static moe_status forward_impl(const moe_config *cfg, const void *x, const float
         g.sh_hid = w + L.hid_sh;
         g.sh_out = w + L.s_out;
         g.h_sh = c.h_shared;
+        g.sh_pre = keep ? w + L.preact_sh : nullptr;
     }
     e = run_ffn(c, g, err, stream);
     if (e != cudaSuccess || mark(4) != cudaSuccess) return MOE_ERR_CUDA;

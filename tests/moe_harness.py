@@ -22,9 +22,9 @@ TOL_GATE = 1e-5
 TOL_AUX = 1e-4
 
 
-def cfg_of(w, debug_flags=0):
+def cfg_of(w, debug_flags=0, save_preact=False):
     f = dataclasses.asdict(w)
-    return moe.make_config(**f, debug_flags=debug_flags)
+    return moe.make_config(**f, debug_flags=debug_flags, save_preact=save_preact)
 
 
 class _ExpertsView:

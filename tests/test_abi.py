@@ -83,6 +83,44 @@ def test_valid_configs_and_sizes():
     assert moe.status_str(moe.MOE_ERR_TIMEOUT) == "MOE_ERR_TIMEOUT"
 
 
+NONE = ctypes.c_size_t(-1).value
+
+
+def test_kept_preactivation_regions():
+    """save_preact adds the pre-activation regions to the workspace (bf16, dispatch
+    order) and only where moe_forward keeps them."""
+    kw = dict(T=8192, d=7168, N=256, k=8, h=2048, h_shared=2048, gating="softmax_then_topk")
+    plain, keep = moe.make_config(**kw), moe.make_config(**kw, save_preact=True)
+    assert moe.moe_preact_offset(plain) == NONE
+    rmax = moe.moe_max_rows(keep)
+    grow = moe.moe_workspace_size(keep) - moe.moe_workspace_size(plain)
+    need = rmax * 2 * 2048 * 2 + 8192 * 2 * 2048 * 2
+    assert need - 512 <= grow <= need  # (an empty region still takes 256 bytes)
+    off, off_sh = moe.moe_preact_offset(keep), moe.moe_preact_offset(keep, shared=True)
+    assert off % 256 == 0 and off_sh >= off + rmax * 2 * 2048 * 2
+    assert off_sh + 8192 * 2 * 2048 * 2 <= moe.moe_workspace_size(keep)
+    # the router's prefix and the backward scratch (which then holds no pre-activations)
+    assert moe.moe_router_workspace_size(keep) == moe.moe_router_workspace_size(plain)
+    bws = lambda c: moe._lib.moe_backward_workspace_size(ctypes.byref(c))  # noqa: E731
+    assert (bws(plain) - bws(keep)
+            >= need - 512)
+    # ReLU experts keep X W1ᵀ only; no shared expert, no shared region
+    relu = moe.make_config(T=4096, d=768, N=8, k=1, h=3072, act="relu", save_preact=True)
+    assert moe.moe_preact_offset(relu) != NONE and moe.moe_preact_offset(relu, shared=True) == NONE
+    # nothing is kept on the fp32, forced CUDA-core, weights-as-M and Expert Choice paths
+    for c in (moe.make_config(T=256, d=64, N=4, k=2, h=128, dtype="f32", save_preact=True),
+              moe.make_config(**kw, save_preact=True, debug_flags=moe.MOE_DEBUG_FORCE_SIMT_FFN),
+              moe.make_config(**kw, save_preact=True, debug_flags=moe.MOE_DEBUG_FFN_SWAP),
+              moe.make_config(T=64, d=128, N=8, k=2, h=256, capacity_factor=(2, 1),
+                              routing="expert_choice", save_preact=True)):
+        assert moe.moe_validate_config(c) == moe.MOE_OK
+        assert moe.moe_preact_offset(c) == NONE
+    bad = moe.make_config(**kw)
+    bad.save_preact = 2
+    assert moe.moe_validate_config(bad) == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_preact_offset(bad) == NONE
+
+
 FAKE = 1 << 20          # a 256-aligned address that is never dereferenced on these paths
 
 

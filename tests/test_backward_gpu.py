@@ -59,8 +59,8 @@ CASES = [
 ]
 
 
-def _run(w, aux_coef, z_coef, seed=3, debug_flags=0):
-    cfg = cfg_of(w, debug_flags=debug_flags)
+def _run(w, aux_coef, z_coef, seed=3, debug_flags=0, save_preact=False):
+    cfg = cfg_of(w, debug_flags=debug_flags, save_preact=save_preact)
     inp = W.make_inputs(w, device="cuda")
     ws = moe.workspace(cfg)
     bws = moe.backward_workspace(cfg)
@@ -99,6 +99,23 @@ def test_backward_matches_oracle(w, aux, z):
     _check(w, aux, z, 0)
 
 
+# gated with a shared expert, ReLU with bias and drops, ReLU with a shared expert, the
+# pair kernels (with a split), and the smallest tiles
+KEPT = [CASES[i] for i in (1, 2, 3, 4, 6)]
+
+
+@pytest.mark.parametrize("w,aux,z", KEPT, ids=[c[0].name for c in KEPT])
+def test_backward_with_kept_preactivations(w, aux, z):
+    """save_preact: the forward keeps the pre-activations and the backward reads them;
+    the gradients match the oracle, and match bit for bit those of the backward that
+    recomputes them (the same products on the same kernels)."""
+    out = _check(w, aux, z, 0, save_preact=True)
+    _, _, ref = _run(w, aux, z)
+    for key, t in out.items():
+        if t is not None:
+            assert torch.equal(t, ref[key]), key
+
+
 def test_backward_single_cta_kernels():
     """The pair-kernel shape once more with every expert product and weight gradient
     on the single-CTA kernels."""
@@ -106,8 +123,8 @@ def test_backward_single_cta_kernels():
     _check(w, aux, z, moe.MOE_DEBUG_FFN_SINGLE)
 
 
-def _check(w, aux, z, flags):
-    inp, dy, out = _run(w, aux, z, debug_flags=flags)
+def _check(w, aux, z, flags, save_preact=False):
+    inp, dy, out = _run(w, aux, z, debug_flags=flags, save_preact=save_preact)
     ref = O.backward(w, oracle_inputs(inp), _f(dy), aux_coef=aux, z_coef=z)
     errs = {"dx": _errs(_f(out["dx"]), ref["dx"]), "dw_r": _errs(_f(out["dw_r"]), ref["dw_r"])}
     if out["db_r"] is not None:
@@ -128,6 +145,7 @@ def _check(w, aux, z, flags):
     print({k_: (round(a, 5), round(b, 4)) for k_, (a, b) in errs.items()})
     bad = {k_: v for k_, v in errs.items() if not (v[0] <= TOL_RMS and v[1] <= TOL_ELEM)}
     assert not bad, errs
+    return out
 
 
 def test_backward_is_deterministic():

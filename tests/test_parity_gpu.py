@@ -180,6 +180,51 @@ def test_run_to_run_determinism():
             assert np.array_equal(first[k], again[k]), k
 
 
+KEEP = [_small("mixtral_prefill", T=1024, d=256, h=256),
+        _small("deepseek_fine", T=200, d=256, N=16, k=4, h=128, h_shared=128),
+        _small("switch_top1", T=333, d=128, h=256),
+        _small("switch_top1", T=150, d=192, h=128, N=4, k=2, h_shared=192, capacity_factor=None)]
+
+
+@pytest.mark.parametrize("w", KEEP, ids=[w.name for w in KEEP])
+def test_forward_keeping_preactivations(w):
+    """save_preact only adds stores: the forward's outputs are bit for bit those of the
+    plain forward, and the kept pre-activations of every kept row and of the shared
+    expert are those of the oracle's experts (x W_gateᵀ, x W_upᵀ / x W1ᵀ)."""
+    inp = W.make_inputs(w, device="cuda")
+    plain_cfg, keep_cfg = cfg_of(w), cfg_of(w, save_preact=True)
+    ws0, ws1 = moe.workspace(plain_cfg), moe.workspace(keep_cfg)
+    assert ws1.numel() > ws0.numel()
+    a, b = host(run_forward(plain_cfg, inp, ws0)), host(run_forward(keep_cfg, inp, ws1))
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+    assert moe.moe_check_error(ws1) == moe.MOE_OK
+    # pre-activations of a sample of kept rows against the oracle's products on that token
+    oi = oracle_inputs(inp)
+    sep = host(run_separate(plain_cfg, inp, moe.workspace(plain_cfg)))
+    offs, perm = sep["expert_offsets"], sep["perm_token"]
+    gated = w.act == "silu_gated"
+    width = 2 * w.h if gated else w.h
+    rmax = moe.moe_max_rows(keep_cfg)
+    pre = moe.preact_view(keep_cfg, ws1)
+    assert tuple(pre.shape) == (rmax, width)
+    rng = np.random.default_rng(0)
+    for e in range(w.N):
+        lo, hi = int(offs[e]), int(offs[e + 1])
+        for r in sorted(set(rng.integers(lo, hi, size=min(4, hi - lo)).tolist())) if hi > lo else []:
+            xt = oi["x"][int(perm[r])].astype(np.float64)
+            want = xt @ oi["w_gate"][e].astype(np.float64).T
+            if gated:
+                want = np.concatenate([want, xt @ oi["w_up"][e].astype(np.float64).T])
+            check_output(pre[r].float().cpu().numpy(), want, "bf16")
+    if w.h_shared:
+        pre_sh = moe.preact_view(keep_cfg, ws1, shared=True)
+        xs = oi["x"].astype(np.float64)
+        want = np.concatenate([xs @ oi["shared_w_gate"].astype(np.float64).T,
+                               xs @ oi["shared_w_up"].astype(np.float64).T], axis=1)
+        check_output(pre_sh.float().cpu().numpy(), want, "bf16")
+
+
 def test_dispatch_rejects_out_of_range_token():
     """A perm_token entry outside [0, T) is skipped and reported, never followed."""
     w = _small("mixtral_prefill", T=64, d=128, h=128)
