@@ -402,7 +402,8 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const float *w_r,
  * SiLU(X W_gateᵀ) ⊙ X W_upᵀ, or max(0, X W1ᵀ)), the shared expert and the router
  * (gates from the fp32 logits; aux N sum_e f_e P_e; z = mean_t (log sum_e exp L)²).
  * Call it after moe_forward with the same inputs and the same workspace ws (it
- * reads the saved dispatch order, rows, expert outputs and hidden activations);
+ * reads the saved dispatch order, rows, expert outputs and hidden activations, and
+ * for N > 32 the router logits);
  * topk_idx / topk_gate: the buffers given to that moe_forward, or NULL if it was
  * given NULL. bws: backward scratch of moe_backward_workspace_size(cfg) bytes.
  *   dy [T][d] bf16 in;  dx [T][d] bf16, dw_r [d][N] fp32, db_r [N] fp32 (NULL or

@@ -336,7 +336,7 @@ BwdLayout bwd_layout(const moe_config &c) {
     L.Hsh_t = take(hs ? hs * Tp * 2 : 0);
     L.dABsh_t = take(hs ? 2 * hs * Tp * 2 : 0);
     L.x_t = take(d * Tp * 2);
-    L.logits = take(T * N * 4);
+    L.logits = take(N > 32 ? 0 : T * N * 4);  // N > 32: the forward's logits in its workspace serve
     L.routed = take(N * 4);
     L.dL = take(T * N * 4);
     L.dxr = take(T * d * 4);
@@ -372,10 +372,9 @@ cudaError_t launch_act_bwd(bool gated, const void *AB, const void *dH, int64_t r
     return cudaGetLastError();
 }
 
-cudaError_t launch_router_bwd(const moe_config &c, const float *w_r, const int32_t *topk_idx, const float *topk_gate,
-                              const BwdLayout &L, uint8_t *bw, float aux_coef, float z_coef, float *dw_r, float *db_r,
-                              uint32_t *err, bool allow_pair, cudaStream_t s) {
-    float *logits = reinterpret_cast<float *>(bw + L.logits);
+cudaError_t launch_router_bwd(const moe_config &c, const float *w_r, const float *logits, const int32_t *topk_idx,
+                              const float *topk_gate, const BwdLayout &L, uint8_t *bw, float aux_coef, float z_coef,
+                              float *dw_r, float *db_r, uint32_t *err, bool allow_pair, cudaStream_t s) {
     int32_t *routed = reinterpret_cast<int32_t *>(bw + L.routed);
     float *dL = reinterpret_cast<float *>(bw + L.dL);
     float *dxr = reinterpret_cast<float *>(bw + L.dxr);

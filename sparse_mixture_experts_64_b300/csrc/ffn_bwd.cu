@@ -565,7 +565,8 @@ __global__ void __launch_bounds__(256) k_pad_prefix(const int32_t *__restrict__ 
 
 // Activation rows [rows][C] (row stride C) into the padded transposed layout
 // [C][Kall]: column kpre[g] + i holds row offsets[g] + i for i < R_g, zero up to
-// kpre[g + 1] and beyond kpre[n_seg]. offsets null: one segment of `rows` rows.
+// kpre[g + 1]; 64-column blocks from kpre[n_seg] on are left unwritten (no product reads
+// them). offsets null: one segment of `rows` rows, zero up to Kall.
 // 64 x 64 tiles, 16-byte loads and stores (C and Kall multiples of 8).
 __global__ void __launch_bounds__(256) k_transpose_rows_padded(const __nv_bfloat16 *__restrict__ src, int C,
                                                                const int32_t *__restrict__ offsets,
@@ -576,6 +577,7 @@ __global__ void __launch_bounds__(256) k_transpose_rows_padded(const __nv_bfloat
     __shared__ int srow[64];
     const int64_t k0 = (int64_t)blockIdx.x * 64;
     const int c0 = blockIdx.y * 64;
+    if (offsets && k0 >= kpre[n_seg]) return;  // past the last segment: never read
     if (threadIdx.x < 64) {
         // source row of padded column k0 + threadIdx.x (-1: padding), by binary search on kpre
         const int64_t kc = k0 + threadIdx.x;

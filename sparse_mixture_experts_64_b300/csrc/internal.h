@@ -76,7 +76,7 @@ struct BwdLayout {
     size_t AB_sh, dH_sh, dAB_sh, dX_sh;  // shared expert, rows = T
     size_t dy_t, Hsh_t, dABsh_t;     // shared expert, [..][ceil64(T)]
     size_t x_t;                      // bf16 xᵀ [d][ceil64(T)] (shared expert and router weight gradients)
-    size_t logits, routed, dL, dxr;  // router: f32 [T][N], int32 [N], f32 [T][N], f32 [T][d]
+    size_t logits, routed, dL, dxr;  // router: f32 [T][N] (N <= 32: recomputed), int32 [N], f32 [T][N], f32 [T][d]
     size_t rA, rB, dLt, wrC;         // router-gradient split operands: bf16 [T][Kr], [d][Kr] (Kr = 3N
                                      // rounded up to 64), [2N][ceil64(T)]; f32 [2N][d] dW_rᵀ halves
     size_t total;
@@ -115,11 +115,11 @@ cudaError_t launch_bwd_slots(const moe_config &c, const void *dy, const void *y_
                              const float *gate, void *dO, float *dgate, uint32_t *err, cudaStream_t s);
 cudaError_t launch_act_bwd(bool gated, const void *AB, const void *dH, int64_t rows, int h, void *dAB,
                            cudaStream_t s);
-// Router backward: dL, then dx_router (into L.dxr) and dW_r on the tensor cores from
-// bf16-split operands; xᵀ (L.x_t) must be in place.
-cudaError_t launch_router_bwd(const moe_config &c, const float *w_r, const int32_t *topk_idx, const float *topk_gate,
-                              const BwdLayout &L, uint8_t *bw, float aux_coef, float z_coef, float *dw_r, float *db_r,
-                              uint32_t *err, bool allow_pair, cudaStream_t s);
+// Router backward from the fp32 logits [T][N]: dL, then dx_router (into L.dxr) and dW_r
+// on the tensor cores from bf16-split operands; xᵀ (L.x_t) must be in place.
+cudaError_t launch_router_bwd(const moe_config &c, const float *w_r, const float *logits, const int32_t *topk_idx,
+                              const float *topk_gate, const BwdLayout &L, uint8_t *bw, float aux_coef, float z_coef,
+                              float *dw_r, float *db_r, uint32_t *err, bool allow_pair, cudaStream_t s);
 cudaError_t launch_bwd_dx(const moe_config &c, const void *dy, const void *dX, const int32_t *slot_row,
                           const void *dX_sh, const float *dxr, void *dx, uint32_t *err, cudaStream_t s);
 // Token-sharded router, phase 1: routing of this shard and the statistics the

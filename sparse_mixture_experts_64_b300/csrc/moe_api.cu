@@ -397,16 +397,17 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const float *w_r, 
         return e == cudaSuccess;
     };
 
-    // Work that depends only on the inputs and the forward's saved tensors runs on an
-    // auxiliary stream beside the row products: the padding prefix, the transposed forward
-    // activations (HBM-bound, while the recompute and dH products are tensor-bound) and
-    // the router logits. An event joins it where its results are first needed; without
-    // the stream (creation failed) it all runs in order on `stream`. The row products read
-    // the expert weights in their own layout (MN-major operands), so no weight is copied.
+    // The weight gradients' transposed operands run on an auxiliary stream beside the row
+    // products (HBM-bound copies beside tensor-bound products): the padding prefix and
+    // the forward's activations from the start, the recomputed router logits, dOᵀ once the
+    // slots are done and [dA | dB]ᵀ once the activation backward is. An event joins it
+    // before the weight gradients; without the stream (creation failed) it all runs in
+    // order on `stream`. The row products read the expert weights in their own layout
+    // (MN-major operands), so no weight is copied.
     cudaStream_t aux = nullptr;
-    cudaEvent_t ev[2] = {nullptr, nullptr};  // fork, aux done
+    cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};  // fork, aux done, slots done, dA | dB done
     bool two = cudaStreamCreateWithFlags(&aux, cudaStreamNonBlocking) == cudaSuccess;
-    for (int i = 0; i < 2 && two; ++i) two = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; i < 4 && two; ++i) two = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) == cudaSuccess;
     if (two) two = cudaEventRecord(ev[0], stream) == cudaSuccess && cudaStreamWaitEvent(aux, ev[0], 0) == cudaSuccess;
     const cudaStream_t sa = two ? aux : stream;
     auto mark = [&](int i) {
@@ -414,6 +415,12 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const float *w_r, 
     };
     auto join = [&](int i) {
         if (two) ok(cudaStreamWaitEvent(stream, ev[i], 0));
+    };
+    auto signal = [&](int i) {  // main stream -> auxiliary stream
+        if (two) {
+            ok(cudaEventRecord(ev[i], stream));
+            ok(cudaStreamWaitEvent(sa, ev[i], 0));
+        }
     };
 
     // -- auxiliary stream
@@ -427,14 +434,18 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const float *w_r, 
     }
     // xᵀ: the shared expert's and the router's weight gradients
     ok(launch_transpose_rows_padded(x, d, nullptr, nullptr, 1, c.T, Tp, bw + B.x_t, sa));
-    // router logits, recomputed
-    ok(launch_router_logits(c, x, w_r, c.has_router_bias ? b_r : nullptr, reinterpret_cast<float *>(bw + B.logits), w,
-                            sa));
-    mark(1);
+    // router logits: for N > 32 the forward's router left them in ws, else recomputed
+    const bool fwd_logits = N > 32;
+    const float *logits = reinterpret_cast<const float *>(fwd_logits ? w + L.logits : bw + B.logits);
+    if (!fwd_logits)
+        ok(launch_router_logits(c, x, w_r, c.has_router_bias ? b_r : nullptr, reinterpret_cast<float *>(bw + B.logits),
+                                w, sa));
 
     // -- main stream
     // gate-scaled dy per row and the gate gradients
     ok(launch_bwd_slots(c, dy, y_perm, slot_row, gate, dO, dgate, err, stream));
+    signal(2);
+    ok(launch_transpose_rows_padded(dO, d, offsets, kpre, N, (int)R, Kall, bw + B.dO_t, sa));
     // pre-activations, recomputed unless the forward kept them: [A | B] (gated) or A (ReLU)
     if (!kept_pre) {
         ok(launch_gemm_rows(c, gated, offsets, N, R, x_perm, w_gate_or_w1, w_up, d, h, AB, 0, nullptr, nullptr,
@@ -449,14 +460,17 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const float *w_r, 
     // [dA | dB] from the pre-activations
     ok(launch_act_bwd(gated, AB, dH, R, h, dAB, stream));
     if (hs) ok(launch_act_bwd(true, AB_sh, bw + B.dH_sh, c.T, hs, bw + B.dAB_sh, stream));
+    signal(3);
+    ok(launch_transpose_rows_padded(dAB, Wd, offsets, kpre, N, (int)R, Kall, bw + B.dAB_t, sa));
+    if (hs)
+        ok(launch_transpose_rows_padded(bw + B.dAB_sh, 2 * hs, nullptr, nullptr, 1, c.T, Tp, bw + B.dABsh_t, sa));
+    mark(1);
     // dX = [dA | dB] [W_a ; W_b] (W_a, W_b [h][d] per expert: MN-major, K = Wd split at h)
     ok(launch_gemm_rows(c, false, offsets, N, R, dAB, w_gate_or_w1, gated ? w_up : nullptr, Wd, d, dX, hs ? c.T : 0,
                         bw + B.dAB_sh, shared_w_gate, shared_w_up, 2 * hs, d, bw + B.dX_sh, err, stream, true,
                         gated ? h : 0, hs));
     // weight gradients: transposed activations with each expert's rows padded to 64
     join(1);
-    ok(launch_transpose_rows_padded(dO, d, offsets, kpre, N, (int)R, Kall, bw + B.dO_t, stream));
-    ok(launch_transpose_rows_padded(dAB, Wd, offsets, kpre, N, (int)R, Kall, bw + B.dAB_t, stream));
     const bool pair_ok = !(c.debug_flags & MOE_DEBUG_FFN_SINGLE);
     ok(launch_wgrad(offsets, N, R, bw + B.dO_t, bw + B.H_t, Kall, d, h, dw_down, nullptr, nullptr, 0, nullptr, err,
                     stream, pair_ok));
@@ -466,7 +480,6 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const float *w_r, 
         ok(launch_wgrad(offsets, N, R, bw + B.dAB_t + (size_t)h * Kall * 2, bw + B.X_t, Kall, h, d, dw_up, nullptr,
                         nullptr, 0, nullptr, err, stream, pair_ok));
     if (hs) {
-        ok(launch_transpose_rows_padded(bw + B.dAB_sh, 2 * hs, nullptr, nullptr, 1, c.T, Tp, bw + B.dABsh_t, stream));
         ok(launch_wgrad(nullptr, 0, 0, nullptr, nullptr, 0, d, hs, nullptr, bw + B.dy_t, bw + B.Hsh_t, (int)Tp,
                         dshared_w_down, err, stream, pair_ok));
         ok(launch_wgrad(nullptr, 0, 0, nullptr, nullptr, 0, hs, d, nullptr, bw + B.dABsh_t, bw + B.x_t, (int)Tp,
@@ -475,8 +488,8 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const float *w_r, 
                         bw + B.x_t, (int)Tp, dshared_w_up, err, stream, pair_ok));
     }
     // router: dL, dx_router, dW_r, db
-    ok(launch_router_bwd(c, w_r, idx, gate, B, bw, aux_coef, z_coef, dw_r, c.has_router_bias ? db_r : nullptr, err,
-                         pair_ok, stream));
+    ok(launch_router_bwd(c, w_r, logits, idx, gate, B, bw, aux_coef, z_coef, dw_r, c.has_router_bias ? db_r : nullptr,
+                         err, pair_ok, stream));
     // dx = dy + sum_j dX_r + dX_shared + dx_router
     ok(launch_bwd_dx(c, dy, dX, slot_row, hs ? bw + B.dX_sh : nullptr, reinterpret_cast<const float *>(bw + B.dxr), dx,
                      err, stream));
