@@ -506,6 +506,7 @@ def measure_backward(w, inp, cfg, ws, stream, dev, peaks, host_inp=None, cpu_tok
     fwd(keep_cfg, ws_keep)
     ms = _time_calls(lambda: bwd(keep_cfg, ws_keep), stream, 10)
     fwd_keep_ms = _time_calls(lambda: fwd(keep_cfg, ws_keep), stream, 10)
+    fwd_plain_ms = _time_calls(lambda: fwd(cfg, ws), stream, 10)  # the same launches without keeping
     step_ms = _time_calls(lambda: (fwd(keep_cfg, ws_keep), bwd(keep_cfg, ws_keep)), stream, 10)
     for wsp in (ws, ws_keep):
         st = moe.moe_check_error(wsp, stream)
@@ -522,7 +523,8 @@ def measure_backward(w, inp, cfg, ws, stream, dev, peaks, host_inp=None, cpu_tok
              "achieved_tflops": tf(ms), "bound": "tensor", "frac": tf(ms) / peaks["bf16"],
              "peak": f"{peaks['source']} bf16 burst {peaks['bf16']} TFLOP/s",
              "pre_activations": "kept by the forward (save_preact)",
-             "forward_keeping_ms": fwd_keep_ms, "forward_plus_backward_ms": step_ms,
+             "forward_keeping_ms": fwd_keep_ms, "forward_plain_ms": fwd_plain_ms,
+             "forward_plus_backward_ms": step_ms,
              "recompute": {"ms": ms_recompute, "achieved_tflops": tf(ms_recompute),
                            "frac": tf(ms_recompute) / peaks["bf16"],
                            "note": "plain forward; the backward recomputes the pre-activations "
