@@ -896,8 +896,9 @@ struct AssignArgs {
 __global__ void __launch_bounds__(256) k_assign(AssignArgs a) {
     extern __shared__ int sm[];
     int *offs = sm;                       // [N+1]
-    int *Is = offs + a.N + 1;             // [TT][8]
-    int *Ks = Is + a.TT * 8;              // [TT][8]
+    int *Is = offs + a.N + 1;             // [TT][8] expert of each slot (-1 none, -2 invalid)
+    int *Ks = Is + a.TT * 8;              // [TT][8] kept
+    int *Cs = Ks + a.TT * 8;              // [9][N] running counts: per slot, then kept per expert
     __shared__ int shi[33];
     __shared__ float shf[32];
     const int tid = threadIdx.x, nt = blockDim.x, N = a.N, k = a.k;
@@ -943,44 +944,73 @@ __global__ void __launch_bounds__(256) k_assign(AssignArgs a) {
     for (int s = tid; s < a.TT * 8; s += nt) {
         const int tok = s >> 3, j = s & 7;
         const int t = t0 + tok;
-        Is[s] = (t < a.T && j < k) ? a.topk_idx[(size_t)t * k + j] : -1;
+        int e = (t < a.T && j < k) ? a.topk_idx[(size_t)t * k + j] : -1;
+        if (t < a.T && j < k && (e < 0 || e >= N)) {
+            record_error(a.err, kErrFault);
+            e = -2;  // matches no expert: neither kept nor counted
+        }
+        Is[s] = e;
         Ks[s] = 0;
     }
+    for (int i = tid; i < 9 * N; i += nt) Cs[i] = 0;
     __syncthreads();
 
-    for (int s = tid; s < a.TT * k; s += nt) {
-        const int tok = s / k, j = s % k, t = t0 + tok;
-        if (t >= a.T) continue;
-        const int e = Is[tok * 8 + j];
-        if (e < 0 || e >= N) {
-            record_error(a.err, kErrFault);
-            continue;
+    // Keep or drop each slot: its priority is the expert's selections before this tile
+    // in slot j (pre) plus this tile's earlier tokens that chose the same expert in slot
+    // j. Warp j ranks slot j's selections in token order, 32 tokens at a time: lanes with
+    // equal experts are matched, a lane's rank among them is the count of lower lanes,
+    // and a per-(slot, expert) counter carries the earlier chunks.
+    const int warp = tid >> 5, lane = tid & 31;
+    const unsigned lower = (1u << lane) - 1u;
+    if (warp < k) {
+        const int j = warp;
+        int *cj = Cs + (size_t)j * N;
+        for (int base = 0; base < a.TT; base += 32) {
+            const int tok = base + lane;
+            const int e = tok < a.TT ? Is[tok * 8 + j] : -2;
+            const unsigned peers = __match_any_sync(0xffffffffu, e);
+            const int before = e >= 0 ? cj[e] : 0;
+            __syncwarp();
+            if (e >= 0) {
+                const int r = a.pre[((size_t)e * k + j) * a.tiles + tile] + before + __popc(peers & lower);
+                Ks[tok * 8 + j] = r < C;
+                if ((peers & lower) == 0) cj[e] = before + __popc(peers);  // the group's lowest lane
+            }
+            __syncwarp();
         }
-        int local = 0;
-        for (int u = 0; u < tok; ++u) local += (Is[u * 8 + j] == e);
-        const int r = a.pre[((size_t)e * k + j) * a.tiles + tile] + local;
-        Ks[tok * 8 + j] = r < C;
     }
     __syncthreads();
 
-    for (int s = tid; s < a.TT * k; s += nt) {
-        const int tok = s / k, j = s % k, t = t0 + tok;
-        if (t >= a.T) continue;
-        const int e = Is[tok * 8 + j];
-        int row = -1;
-        if (e >= 0 && e < N && Ks[tok * 8 + j]) {
-            int pos = a.kpre[(size_t)e * a.tiles + tile];
-            for (int u = 0; u < tok; ++u)
-                for (int jj = 0; jj < k; ++jj) pos += (Is[u * 8 + jj] == e && Ks[u * 8 + jj]);
-            row = offs[e] + pos;
-            if (row < 0 || row >= a.rmax) {
-                record_error(a.err, kErrFault);
-                row = -1;
-            } else {
-                a.perm_token[row] = t;
+    // Rows: a kept slot's row is its expert's offset, plus the expert's kept slots of
+    // earlier tiles (kpre), plus this tile's kept slots of the expert in earlier tokens
+    // (a token selects an expert at most once, so earlier (token, slot) entries in
+    // token-major order). Warp 0 ranks the tile's entries 32 at a time as above.
+    if (warp == 0) {
+        int *ce = Cs + (size_t)8 * N;
+        const int n = a.TT * k;
+        for (int base = 0; base < n; base += 32) {
+            const int i = base + lane;
+            const int tok = i / k, j = i - tok * k, t = t0 + tok;
+            const bool live = i < n && t < a.T;
+            const int e = live ? Is[tok * 8 + j] : -2;
+            const bool kept = e >= 0 && Ks[tok * 8 + j];
+            const unsigned peers = __match_any_sync(0xffffffffu, kept ? e : -1);
+            const int before = kept ? ce[e] : 0;
+            __syncwarp();
+            int row = -1;
+            if (kept) {
+                row = offs[e] + a.kpre[(size_t)e * a.tiles + tile] + before + __popc(peers & lower);
+                if (row < 0 || row >= a.rmax) {
+                    record_error(a.err, kErrFault);
+                    row = -1;
+                } else {
+                    a.perm_token[row] = t;
+                }
+                if ((peers & lower) == 0) ce[e] = before + __popc(peers);
             }
+            __syncwarp();
+            if (live) a.slot_row[(size_t)t * k + j] = row;
         }
-        a.slot_row[(size_t)t * k + j] = row;
     }
 }
 
@@ -1145,7 +1175,7 @@ cudaError_t launch_router_assign(const moe_config &c, const int32_t *topk_idx, c
     aa.g_routed = g_routed;
     aa.g_psum = g_psum;
     aa.g_T = g_T;
-    const size_t sbytes = (size_t)(c.N + 1 + 2 * TT * 8) * sizeof(int);
+    const size_t sbytes = (size_t)(c.N + 1 + 2 * TT * 8 + 9 * c.N) * sizeof(int);
     return launch_pdl(k_assign, dim3(tiles), dim3(256), sbytes, s, aa);
 }
 
@@ -1182,7 +1212,7 @@ cudaError_t launch_router(const moe_config &c, const void *x, const float *w_r, 
     const int TT = router_tile_tokens(c);
     AssignArgs aa{c.T, c.N, c.k, tiles, TT, cap, max_rows(c), o.topk_idx, pre, kpre, routed, kept,
                   pmean, o.expert_offsets, o.slot_row, o.perm_token, o.aux, err, zpart, o.z_loss};
-    const size_t sbytes = (size_t)(c.N + 1 + 2 * TT * 8) * sizeof(int);
+    const size_t sbytes = (size_t)(c.N + 1 + 2 * TT * 8 + 9 * c.N) * sizeof(int);
     return launch_pdl(k_assign, dim3(tiles), dim3(256), sbytes, s, aa);
 }
 

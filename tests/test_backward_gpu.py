@@ -100,8 +100,10 @@ def test_backward_matches_oracle(w, aux, z):
 
 
 # gated with a shared expert, ReLU with bias and drops, ReLU with a shared expert, the
-# pair kernels (with a split), and the smallest tiles
-KEPT = [CASES[i] for i in (1, 2, 3, 4, 6)]
+# pair kernels (with a split), the smallest tiles, and ReLU experts on the pair kernel
+# with tail tiles
+KEPT = [CASES[i] for i in (1, 2, 3, 4, 6)] + [
+    (_w("switch_top1", T=1100, d=128, h=256, N=2, capacity_factor=None), 0.01, 0.001)]
 
 
 @pytest.mark.parametrize("w,aux,z", KEPT, ids=[c[0].name for c in KEPT])
