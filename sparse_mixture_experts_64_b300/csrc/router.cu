@@ -891,7 +891,61 @@ struct AssignArgs {
     const int32_t *g_routed = nullptr;  // [N] selections per expert, all shards
     const float *g_psum = nullptr;      // [N] sum over all tokens of softmax
     float g_T = 0.0f;                   // tokens of all shards
+    // Small problems (at most kFusedScanTiles tiles and kFusedScanMax counts): k_expert_scan is not launched and
+    // every CTA derives what it needs of it from the tile counts itself; CTA 0 writes
+    // routed, kept and the mean probabilities.
+    int fused_scan = 0;
+    const int32_t *cnt = nullptr;  // [N][k][tiles]
+    const float *psum = nullptr;   // [N][tiles]
+    int32_t *routed_out = nullptr, *kept_out = nullptr;
 };
+constexpr int kFusedScanMax = 4096, kFusedScanTiles = 32;
+
+// One warp: expert e's priority-order prefix over its (slot, tile) counts (what
+// k_expert_scan computes), reduced to what tile `tile` needs: pre for each slot of the
+// tile, kept slots of earlier tiles, and the totals.
+__device__ void scan_expert_warp(const AssignArgs &a, const int *cnt_s, int e, int tile, int C, int *pre_t,
+                                 int *kpre_t, int *routed_e, int *kept_e, float *pmean_e) {
+    const int lane = threadIdx.x & 31, n = a.k * a.tiles;
+    const int *ce = cnt_s + (size_t)e * n;
+    int run = 0, kb = 0, kt = 0;
+    for (int i0 = 0; i0 < n; i0 += 32) {
+        const int i = i0 + lane;
+        const int v = i < n ? ce[i] : 0;
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += u;
+        }
+        const int ex = run + incl - v;
+        if (i < n) {
+            const int j = i / a.tiles, tl = i - j * a.tiles;
+            const int kv = min(max(C - ex, 0), v);
+            if (tl == tile) pre_t[j] = ex;
+            if (tl < tile) kb += kv;
+            kt += kv;
+        }
+        run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        kb += __shfl_xor_sync(0xffffffffu, kb, o);
+        kt += __shfl_xor_sync(0xffffffffu, kt, o);
+    }
+    if (lane == 0) {
+        *kpre_t = kb;
+        *routed_e = run;
+        *kept_e = kt;
+    }
+    if (pmean_e) {  // mean routing probability: lane-strided tile sums, then a fixed butterfly
+        float ps = 0.0f;
+        for (int tl = lane; tl < a.tiles; tl += 32) ps += a.psum[(size_t)e * a.tiles + tl];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+        if (lane == 0) *pmean_e = ps / (float)a.T;
+    }
+}
 
 __global__ void __launch_bounds__(256) k_assign(AssignArgs a) {
     extern __shared__ int sm[];
@@ -899,6 +953,7 @@ __global__ void __launch_bounds__(256) k_assign(AssignArgs a) {
     int *Is = offs + a.N + 1;             // [TT][8] expert of each slot (-1 none, -2 invalid)
     int *Ks = Is + a.TT * 8;              // [TT][8] kept
     int *Cs = Ks + a.TT * 8;              // [9][N] running counts: per slot, then kept per expert
+    int *Fp = Cs + 9 * a.N;               // fused scan: [N][8] pre of this tile, [N] kpre, routed, kept, pmean
     __shared__ int shi[33];
     __shared__ float shf[32];
     const int tid = threadIdx.x, nt = blockDim.x, N = a.N, k = a.k;
@@ -906,9 +961,34 @@ __global__ void __launch_bounds__(256) k_assign(AssignArgs a) {
     const int C = a.cap > 0 ? a.cap : INT_MAX;
     pdl_enter();
 
+    const int32_t *kept_of = a.kept;
+    const int32_t *routed_of = a.routed;
+    if (a.fused_scan) {
+        float *pm = reinterpret_cast<float *>(Fp + 11 * N);
+        int *cnt_s = Fp + 12 * N;  // the tile counts, loaded once with every load in flight
+        const int ncnt = N * k * a.tiles;
+        for (int i = tid; i < ncnt; i += nt) cnt_s[i] = a.cnt[i];
+        __syncthreads();
+        for (int e = tid >> 5; e < N; e += nt >> 5)
+            scan_expert_warp(a, cnt_s, e, tile, C, Fp + e * 8, Fp + 8 * N + e, Fp + 9 * N + e, Fp + 10 * N + e,
+                             tile == 0 ? pm + e : nullptr);
+        __syncthreads();
+        kept_of = Fp + 10 * N;
+        routed_of = Fp + 9 * N;
+        if (tile == 0)
+            for (int e = tid; e < N; e += nt) {
+                if (a.routed_out) a.routed_out[e] = routed_of[e];
+                if (a.kept_out) a.kept_out[e] = kept_of[e];
+            }
+    }
+    auto pre_of = [&](int e, int j) {
+        return a.fused_scan ? Fp[e * 8 + j] : a.pre[((size_t)e * k + j) * a.tiles + tile];
+    };
+    auto kpre_of = [&](int e) { return a.fused_scan ? Fp[8 * N + e] : a.kpre[(size_t)e * a.tiles + tile]; };
+
     // expert offsets (every CTA computes them; N <= 256 <= blockDim)
     {
-        const int v = tid < N ? a.kept[tid] : 0;
+        const int v = tid < N ? kept_of[tid] : 0;
         int total;
         const int ex = block_exclusive_scan(v, shi, &total);
         if (tid < N) offs[tid] = ex;
@@ -923,8 +1003,15 @@ __global__ void __launch_bounds__(256) k_assign(AssignArgs a) {
         if (tid < N) {
             const bool global = a.g_routed != nullptr;
             const float Tg = global ? a.g_T : (float)a.T;
-            const float pm = global ? a.g_psum[tid] / Tg : a.pmean[tid];
-            const float routed = (float)(global ? a.g_routed[tid] : a.routed[tid]);
+            float pm;
+            if (global) {
+                pm = a.g_psum[tid] / Tg;
+            } else if (a.fused_scan) {
+                pm = reinterpret_cast<const float *>(Fp + 11 * N)[tid];
+            } else {
+                pm = a.pmean[tid];
+            }
+            const float routed = (float)(global ? a.g_routed[tid] : routed_of[tid]);
             f0 = (routed / (Tg * (float)k)) * pm;
             f1 = (pm - invN) * (pm - invN);
         }
@@ -972,7 +1059,7 @@ __global__ void __launch_bounds__(256) k_assign(AssignArgs a) {
             const int before = e >= 0 ? cj[e] : 0;
             __syncwarp();
             if (e >= 0) {
-                const int r = a.pre[((size_t)e * k + j) * a.tiles + tile] + before + __popc(peers & lower);
+                const int r = pre_of(e, j) + before + __popc(peers & lower);
                 Ks[tok * 8 + j] = r < C;
                 if ((peers & lower) == 0) cj[e] = before + __popc(peers);  // the group's lowest lane
             }
@@ -999,7 +1086,7 @@ __global__ void __launch_bounds__(256) k_assign(AssignArgs a) {
             __syncwarp();
             int row = -1;
             if (kept) {
-                row = offs[e] + a.kpre[(size_t)e * a.tiles + tile] + before + __popc(peers & lower);
+                row = offs[e] + kpre_of(e) + before + __popc(peers & lower);
                 if (row < 0 || row >= a.rmax) {
                     record_error(a.err, kErrFault);
                     row = -1;
@@ -1206,13 +1293,27 @@ cudaError_t launch_router(const moe_config &c, const void *x, const float *w_r, 
     if (e != cudaSuccess) return e;
 
     const int cap = capacity_of(c);
-    ScanArgs sa{c.T, c.N, c.k, tiles, cap, cnt, pre, kpre, psum, pmean, routed, kept};
-    if ((e = launch_pdl(k_expert_scan, dim3(c.N), dim3(256), 0, s, sa)) != cudaSuccess) return e;
+    // every CTA scans all the counts again: worth a launch only with few tiles (measured:
+    // tiny and decode layers 1-2.5 us faster, 256-tile Switch and Mixtral routers 3 and 15 us
+    // slower)
+    const bool fused = tiles <= kFusedScanTiles && (int64_t)c.N * c.k * tiles <= kFusedScanMax;
+    if (!fused) {
+        ScanArgs sa{c.T, c.N, c.k, tiles, cap, cnt, pre, kpre, psum, pmean, routed, kept};
+        if ((e = launch_pdl(k_expert_scan, dim3(c.N), dim3(256), 0, s, sa)) != cudaSuccess) return e;
+    }
 
     const int TT = router_tile_tokens(c);
     AssignArgs aa{c.T, c.N, c.k, tiles, TT, cap, max_rows(c), o.topk_idx, pre, kpre, routed, kept,
                   pmean, o.expert_offsets, o.slot_row, o.perm_token, o.aux, err, zpart, o.z_loss};
-    const size_t sbytes = (size_t)(c.N + 1 + 2 * TT * 8 + 9 * c.N) * sizeof(int);
+    if (fused) {
+        aa.fused_scan = 1;
+        aa.cnt = cnt;
+        aa.psum = psum;
+        aa.routed_out = routed;
+        aa.kept_out = kept;
+    }
+    const size_t sbytes =
+        (size_t)(c.N + 1 + 2 * TT * 8 + 9 * c.N + (fused ? 12 * c.N + c.N * c.k * tiles : 0)) * sizeof(int);
     return launch_pdl(k_assign, dim3(tiles), dim3(256), sbytes, s, aa);
 }
 
