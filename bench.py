@@ -168,19 +168,28 @@ def captured_traffic(workload: str, stage: str):
         return None
 
 
+def router_np(N: int) -> int:
+    """Experts per lane group of the N <= 32 router kernel (4, 8, 16 or 32)."""
+    return 4 if N <= 4 else 8 if N <= 8 else 16 if N <= 16 else 32
+
+
 def launches_per_forward(w) -> int:
     """Kernels one moe_forward launches. Token choice: router weight re-layout,
     logits with gating (one kernel for N <= 32, logits and gating kernels above),
-    expert scan, slot assignment. Expert Choice: weight re-layout, logits, scores,
-    per-expert selection, per-token list scan and fill, per-expert counts. Then
+    expert scan (folded into the slot assignment when the router has at most 32 tiles
+    and N·k·tiles <= 4096 counts), slot assignment. Expert Choice: weight re-layout, logits, scores,
+    per-expert selection, per-token list scan and fill. Then
     dispatch, expert product 1 (two launches for ReLU experts with a shared expert),
     expert product 2 and the combine. With bf16 experts receiving 224 to 511 rows on
     average (the row buffers' size over N) each product is two launches: the CTA-pair
     kernel and a single-CTA kernel for the short last row blocks."""
     if w.routing == "expert_choice":
-        router = 7
+        router = 6
     else:
-        router = 1 + (2 if w.N > 32 else 1) + 2
+        tt = 64 if w.N > 32 else 4 * (32 // router_np(w.N))  # tokens per router tile
+        tiles = -(-w.T // tt)
+        fused_scan = tiles <= 32 and w.N * w.k * tiles <= 4096
+        router = 1 + (2 if w.N > 32 else 1) + (1 if fused_scan else 2)
     p1 = 2 if (w.act == "relu" and w.h_shared) else 1
     p2 = 1
     if w.dtype == "bf16":
