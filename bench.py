@@ -178,13 +178,14 @@ def launches_per_forward(w) -> int:
     logits with gating (one kernel for N <= 32, logits and gating kernels above),
     expert scan (folded into the slot assignment when the router has at most 32 tiles
     and N·k·tiles <= 4096 counts), slot assignment. Expert Choice: weight re-layout, logits, scores,
-    per-expert selection, per-token list scan and fill. Then
+    per-expert selection, per-token list scan and fill, and the per-expert counts (the
+    benchmark asks for them). Then
     dispatch, expert product 1 (two launches for ReLU experts with a shared expert),
     expert product 2 and the combine. With bf16 experts receiving 224 to 511 rows on
     average (the row buffers' size over N) each product is two launches: the CTA-pair
     kernel and a single-CTA kernel for the short last row blocks."""
     if w.routing == "expert_choice":
-        router = 6
+        router = 7
     else:
         tt = 64 if w.N > 32 else 4 * (32 // router_np(w.N))  # tokens per router tile
         tiles = -(-w.T // tt)

@@ -49,11 +49,14 @@ def test_kernels_per_forward(w):
     ec = w.routing == "expert_choice"
     idx = None if ec else torch.empty((T, k), dtype=torch.int32, device="cuda")
     gate = None if ec else torch.empty((T, k), device="cuda")
+    # the outputs the benchmark asks for: per-expert counts too
+    routed = torch.empty(w.N, dtype=torch.int32, device="cuda")
+    kept = torch.empty(w.N, dtype=torch.int32, device="cuda")
     s = torch.cuda.Stream()
 
     def fwd():
         moe.moe_forward(cfg, inp["x"], inp["w_r"], inp["b_r"], inp["w_gate"], inp["w_up"], inp["w_down"],
-                        inp["shared_w_gate"], inp["shared_w_up"], inp["shared_w_down"], y, idx, gate, None, None,
+                        inp["shared_w_gate"], inp["shared_w_up"], inp["shared_w_down"], y, idx, gate, routed, kept,
                         None, ws, s)
     fwd()  # first call: one-time kernel attributes outside the capture
     torch.cuda.synchronize()
