@@ -118,6 +118,46 @@ def test_backward_with_kept_preactivations(w, aux, z):
             assert torch.equal(t, ref[key]), key
 
 
+def test_kept_preactivations_on_single_cta_kernels():
+    """The pair-kernel shape with every product on the single-CTA kernel, whose row
+    epilogue (half tiles included) then keeps the pre-activations."""
+    w, aux, z = CASES[4]
+    _check(w, aux, z, moe.MOE_DEBUG_FFN_SINGLE, save_preact=True)
+
+
+def test_kept_preactivations_through_the_forward_graph():
+    """A keeping forward captured as a CUDA graph leaves what moe_backward reads: the
+    gradients equal bit for bit those after the stream-launched keeping forward."""
+    w, aux, z = CASES[1]
+    _, _, ref = _run(w, aux, z, save_preact=True)
+    cfg = cfg_of(w, save_preact=True)
+    inp = W.make_inputs(w, device="cuda")
+    ws = moe.workspace(cfg)
+    bws = moe.backward_workspace(cfg)
+    T, d, k = w.T, w.d, w.k
+    y = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    gate = torch.empty((T, k), device="cuda")
+    g = moe.moe_forward_graph_create(cfg, inp["x"], inp["w_r"], inp["b_r"], inp["w_gate"], inp["w_up"],
+                                     inp["w_down"], inp["shared_w_gate"], inp["shared_w_up"],
+                                     inp["shared_w_down"], y, idx, gate, None, None, None, ws)
+    try:
+        g.launch()
+    finally:
+        g.destroy()
+    gen = torch.Generator(device="cuda").manual_seed(3)
+    dy = torch.randn((T, d), device="cuda", generator=gen).to(torch.bfloat16)
+    out = {key: None if t is None else torch.empty_like(t) for key, t in ref.items()}
+    moe.moe_backward(cfg, inp["x"], inp["w_r"], inp["b_r"], inp["w_gate"], inp["w_up"], inp["w_down"],
+                     inp["shared_w_gate"], inp["shared_w_up"], inp["shared_w_down"], idx, gate, dy, aux, z,
+                     out["dx"], out["dw_r"], out["db_r"], out["dw_gate"], out["dw_up"], out["dw_down"],
+                     out["dshared_w_gate"], out["dshared_w_up"], out["dshared_w_down"], ws, bws)
+    assert moe.moe_check_error(ws) == moe.MOE_OK
+    for key, t in ref.items():
+        if t is not None:
+            assert torch.equal(out[key], t), key
+
+
 def test_backward_single_cta_kernels():
     """The pair-kernel shape once more with every expert product and weight gradient
     on the single-CTA kernels."""
