@@ -103,7 +103,10 @@ def test_backward_matches_oracle(w, aux, z):
 # pair kernels (with a split), the smallest tiles, and ReLU experts on the pair kernel
 # with tail tiles
 KEPT = [CASES[i] for i in (1, 2, 3, 4, 6)] + [
-    (_w("switch_top1", T=1100, d=128, h=256, N=2, capacity_factor=None), 0.01, 0.001)]
+    (_w("switch_top1", T=1100, d=128, h=256, N=2, capacity_factor=None), 0.01, 0.001),
+    # the shared expert as a segment of the forward's pair launch, its 1100 rows ending
+    # in a tail tile
+    (_w("deepseek_fine", T=1100, d=256, N=8, k=2, h=128, h_shared=128), 0.01, 0.001)]
 
 
 @pytest.mark.parametrize("w,aux,z", KEPT, ids=[c[0].name for c in KEPT])

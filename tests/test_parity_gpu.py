@@ -185,7 +185,9 @@ KEEP = [_small("mixtral_prefill", T=1024, d=256, h=256),
         _small("switch_top1", T=333, d=128, h=256),
         _small("switch_top1", T=150, d=192, h=128, N=4, k=2, h_shared=192, capacity_factor=None),
         # ReLU experts of ~550 rows on the pair kernel, whose last blocks are tail tiles
-        _small("switch_top1", T=1100, d=128, h=256, N=2, capacity_factor=None)]
+        _small("switch_top1", T=1100, d=128, h=256, N=2, capacity_factor=None),
+        # the pair kernel with the shared expert's segment (1100 rows: a 76-row tail tile)
+        _small("deepseek_fine", T=1100, d=256, N=8, k=2, h=128, h_shared=128)]
 
 
 @pytest.mark.parametrize("w", KEEP, ids=[w.name for w in KEEP])
