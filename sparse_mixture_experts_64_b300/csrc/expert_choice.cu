@@ -5,9 +5,9 @@
 //   k_ec_scores  one thread per token: the scores S = softmax over experts, in the
 //                fixed fp32 steps below, written transposed (S_t [N][T]) so that an
 //                expert's column is contiguous;
-//   k_ec_select  one CTA per expert: sorts the expert's T (score, token) keys in
-//                shared memory (bitonic network, descending; on equal scores the
-//                lower token first), keeps the first Ce = min(C, T), and writes them
+//   k_ec_select  one CTA per expert: chooses the expert's first Ce = min(C, T) tokens
+//                by (score descending, token ascending) with a radix selection of the
+//                score bits in shared memory, and writes them
 //                in ascending token order as rows e*Ce .. e*Ce + Ce - 1 (perm_token,
 //                row_gate = the score), plus the row of every (expert, token) pair
 //                (-1 if not chosen) and, per token, how many experts chose it;
@@ -104,7 +104,7 @@ __device__ int block_scan(int v, int *sh, int *total) {
 
 struct SelectArgs {
     const float *S_t;  // [N][T]
-    int T, Tpad, N, Ce;
+    int T, N, Ce;
     int32_t *ec_row;   // [N][T]
     int32_t *tok_cnt;  // [T]
     int32_t *offsets;  // [N+1]
@@ -114,36 +114,78 @@ struct SelectArgs {
 
 __global__ void __launch_bounds__(1024) k_ec_select(SelectArgs a) {
     extern __shared__ __align__(16) uint8_t sm[];
-    uint64_t *key = reinterpret_cast<uint64_t *>(sm);          // [Tpad]
-    uint8_t *flag = reinterpret_cast<uint8_t *>(key + a.Tpad);  // [Tpad]
+    uint32_t *bits = reinterpret_cast<uint32_t *>(sm);        // [T] score bits
+    uint8_t *flag = reinterpret_cast<uint8_t *>(bits + a.T);  // [T]
     __shared__ int sh[33];
+    __shared__ int hist[256];
+    __shared__ uint32_t s_prefix;
+    __shared__ int s_need;
     const int e = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
+    const int lane = tid & 31, warp = tid >> 5;
     const float *s = a.S_t + (size_t)e * a.T;
     pdl_enter();
-    // key: score bits (non-negative floats order like their bits) above the
-    // complemented token index, so that a descending sort puts lower tokens first
-    // on equal scores; padding keys are 0, below every real key
-    for (int i = tid; i < a.Tpad; i += nt) {
-        key[i] = i < a.T ? ((uint64_t)__float_as_uint(s[i]) << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)i) : 0ull;
+    // Non-negative floats order like their bits (a NaN's bits above every number), so
+    // the expert's first Ce tokens by (score descending, token ascending) are: every
+    // token whose score bits exceed the Ce-th largest score's bits P, and of the tokens
+    // at P the lowest `need`. P is found a byte at a time from the top (radix selection):
+    // a histogram of the next byte over the tokens that match P's bytes so far, then the
+    // byte where the count from the top reaches the number still to choose.
+    for (int i = tid; i < a.T; i += nt) {
+        bits[i] = __float_as_uint(s[i]);
         flag[i] = 0;
     }
-    __syncthreads();
-    for (int size = 2; size <= a.Tpad; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int i = tid; i < (a.Tpad >> 1); i += nt) {
-                const int lo = 2 * i - (i & (stride - 1));
-                const int hi = lo + stride;
-                const bool desc = (lo & size) == 0;
-                const uint64_t x = key[lo], y = key[hi];
-                if ((x < y) == desc) {
-                    key[lo] = y;
-                    key[hi] = x;
-                }
+    uint32_t prefix = 0;
+    int need = a.Ce;
+    for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+        for (int i = tid; i < 256; i += nt) hist[i] = 0;
+        __syncthreads();
+        for (int i = tid; i < a.T; i += nt) {
+            const uint32_t u = bits[i];
+            if (pass == 0 || (u >> (shift + 8)) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1);
+        }
+        __syncthreads();
+        if (warp == 0) {
+            // lane l holds bytes 255 - 8l .. 248 - 8l (from the top): counts from the top
+            int c[8], sum = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                c[j] = hist[255 - 8 * lane - j];
+                sum += c[j];
             }
-            __syncthreads();
+            int incl = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += u;
+            }
+            const int before = incl - sum;  // tokens in higher bytes than this lane's
+            const unsigned hit = __ballot_sync(0xffffffffu, before < need && incl >= need);
+            if (lane == __ffs(hit) - 1) {
+                int cum = before, j = 0;
+                while (cum + c[j] < need) cum += c[j++];
+                s_prefix = (prefix << 8) | (uint32_t)(255 - 8 * lane - j);
+                s_need = need - cum;
+            }
+        }
+        __syncthreads();
+        prefix = s_prefix;
+        need = s_need;
+    }
+    // flags: above P, or at P among the lowest `need` tokens (token order)
+    {
+        const int per = (a.T + nt - 1) / nt;
+        const int beg = min(a.T, tid * per), end = min(a.T, beg + per);
+        int eq = 0;
+        for (int t = beg; t < end; ++t) eq += bits[t] == prefix;
+        int total_eq;
+        int rank = block_scan(eq, sh, &total_eq);
+        for (int t = beg; t < end; ++t) {
+            const uint32_t u = bits[t];
+            if (u > prefix) flag[t] = 1;
+            else if (u == prefix) flag[t] = rank++ < need ? 1 : 0;
         }
     }
-    for (int i = tid; i < a.Ce; i += nt) flag[0xFFFFFFFFu - (uint32_t)key[i]] = 1;
     __syncthreads();
     // rows of the chosen tokens in ascending token order
     const int per = (a.T + nt - 1) / nt;
@@ -272,19 +314,16 @@ cudaError_t launch_expert_choice(const moe_config &c, const float *logits, int32
     int32_t *tok_cnt = reinterpret_cast<int32_t *>(ws + L.ec_tok_cnt);
     cudaError_t e = launch_pdl(k_ec_scores, dim3((c.T + 255) / 256), dim3(256), 0, s, logits, c.T, c.N, S_t, tok_cnt);
     if (e != cudaSuccess) return e;
-    int Tpad = 1;
-    while (Tpad < c.T) Tpad <<= 1;
-    if (Tpad < 2) Tpad = 2;
     const int Ce = (int)(max_rows(c) / c.N);
-    const size_t smem = (size_t)Tpad * 9;
+    const size_t smem = (size_t)c.T * 5;  // score bits and flags
     static bool attr_done = false;
     if (!attr_done) {
         e = cudaFuncSetAttribute(k_ec_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)((size_t)kMaxExpertChoiceTokens * 9));
+                                 (int)((size_t)kMaxExpertChoiceTokens * 5));
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    SelectArgs sa{S_t, c.T, Tpad, c.N, Ce, ec_row, tok_cnt, expert_offsets, perm_token, row_gate};
+    SelectArgs sa{S_t, c.T, c.N, Ce, ec_row, tok_cnt, expert_offsets, perm_token, row_gate};
     if ((e = launch_pdl(k_ec_select, dim3(c.N), dim3(1024), smem, s, sa)) != cudaSuccess) return e;
     if ((e = launch_pdl(k_ec_scan, dim3(1), dim3(1024), 0, s, tok_cnt, c.T, tok_ptr)) != cudaSuccess) return e;
     return launch_pdl(k_ec_fill, dim3((c.T + 255) / 256), dim3(256), 0, s, ec_row, tok_ptr, c.T, c.N, tok_rows);
