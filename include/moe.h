@@ -140,7 +140,10 @@ size_t moe_workspace_size(const moe_config *cfg);
 size_t moe_router_workspace_size(const moe_config *cfg);
 
 /* Byte offset in the workspace of the pre-activations moe_forward keeps when
- * cfg->save_preact = 1 (see moe_backward): shared = 0, the routed experts' rows
+ * cfg->save_preact = 1 for the backward (router and experts learn together by
+ * backpropagation, "Mixture of Experts (MoE)" glossary; the expert products of "MoE:
+ * Choosing Which MLPs to Use for Each Token", "Dense MLP and MoE"; see moe_backward):
+ * shared = 0, the routed experts' rows
  * [R_max][W] bf16 in dispatch order (row r of expert e's range holds the token
  * perm_token[r]; W = 2h with X W_gateᵀ in columns [0, h) and X W_upᵀ in [h, 2h), or
  * W = h with X W1ᵀ for ReLU experts); shared = 1, the shared expert's [T][2 h_shared].
