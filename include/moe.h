@@ -419,13 +419,13 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const float *w_r,
  * first product computes them (bf16 token choice on the tensor-core kernels; not with
  * MOE_DEBUG_FORCE_SIMT_FFN or MOE_DEBUG_FFN_SWAP) and moe_backward reads them, else
  * moe_backward recomputes them; moe_forward and moe_backward must then get the same
- * cfg. The row products read the expert weights in their own layout; the weight
- * gradients reduce over each expert's rows on the tensor cores. The transposed forward
- * activations and the recomputed router logits run on a non-blocking auxiliary stream
- * that the call creates, joins to `stream` with an event where their results are
- * needed, and releases before returning (its work completes asynchronously, ordered
- * before the work enqueued on `stream` after the call); if the stream cannot be
- * created, everything runs on `stream`. fp32 and
+ * cfg. The row products read the expert weights, and the weight gradients (which
+ * reduce over each expert's rows on the tensor cores) the activations, in their own
+ * layouts: nothing is transposed or copied. For N <= 32 the router logits are
+ * recomputed on a non-blocking auxiliary stream that the call creates, joins to
+ * `stream` with an event before the router's backward, and releases before returning
+ * (its work completes asynchronously, ordered before the work enqueued on `stream`
+ * after the call); if the stream cannot be created, everything runs on `stream`. fp32 and
  * Expert Choice configs return MOE_ERR_UNSUPPORTED.
  */
 size_t moe_backward_workspace_size(const moe_config *cfg);

@@ -309,7 +309,7 @@ BwdLayout bwd_layout(const moe_config &c) {
     BwdLayout L;
     const size_t R = (size_t)max_rows(c), T = c.T, d = c.d, h = c.h, hs = c.h_shared, N = c.N;
     const size_t W = c.act == MOE_ACT_SILU_GATED ? 2 * h : h;  // [A | B] or A
-    const size_t Kall = (size_t)wgrad_kall_bound(c), Tp = (T + 63) / 64 * 64;
+    const size_t Tp = (T + 63) / 64 * 64;
     size_t o = 0;
     auto take = [&](size_t bytes) {
         const size_t at = o;
@@ -323,19 +323,10 @@ BwdLayout bwd_layout(const moe_config &c) {
     L.dH = take(R * h * 2);
     L.dAB = take(R * W * 2);
     L.dX = take(R * d * 2);
-    L.kpre = take((N + 1) * 4);
-    L.dO_t = take(d * Kall * 2);
-    L.H_t = take(h * Kall * 2);
-    L.dAB_t = take(W * Kall * 2);
-    L.X_t = take(d * Kall * 2);
     L.AB_sh = take(hs && !kept_pre ? T * 2 * hs * 2 : 0);
     L.dH_sh = take(hs ? T * hs * 2 : 0);
     L.dAB_sh = take(hs ? T * 2 * hs * 2 : 0);
     L.dX_sh = take(hs ? T * d * 2 : 0);
-    L.dy_t = take(hs ? d * Tp * 2 : 0);
-    L.Hsh_t = take(hs ? hs * Tp * 2 : 0);
-    L.dABsh_t = take(hs ? 2 * hs * Tp * 2 : 0);
-    L.x_t = take(d * Tp * 2);
     L.logits = take(N > 32 ? 0 : T * N * 4);  // N > 32: the forward's logits in its workspace serve
     L.routed = take(N * 4);
     L.dL = take(T * N * 4);
@@ -372,9 +363,10 @@ cudaError_t launch_act_bwd(bool gated, const void *AB, const void *dH, int64_t r
     return cudaGetLastError();
 }
 
-cudaError_t launch_router_bwd(const moe_config &c, const float *w_r, const float *logits, const int32_t *topk_idx,
-                              const float *topk_gate, const BwdLayout &L, uint8_t *bw, float aux_coef, float z_coef,
-                              float *dw_r, float *db_r, uint32_t *err, bool allow_pair, cudaStream_t s) {
+cudaError_t launch_router_bwd(const moe_config &c, const void *x, const float *w_r, const float *logits,
+                              const int32_t *topk_idx, const float *topk_gate, const BwdLayout &L, uint8_t *bw,
+                              float aux_coef, float z_coef, float *dw_r, float *db_r, uint32_t *err, bool allow_pair,
+                              cudaStream_t s) {
     int32_t *routed = reinterpret_cast<int32_t *>(bw + L.routed);
     float *dL = reinterpret_cast<float *>(bw + L.dL);
     float *dxr = reinterpret_cast<float *>(bw + L.dxr);
@@ -392,14 +384,17 @@ cudaError_t launch_router_bwd(const moe_config &c, const float *w_r, const float
     k_split3<<<grid_of((int64_t)c.T * Kr, 256), 256, 0, s>>>(dL, c.T, c.N, Kr, 0, 0, 1, rA);
     k_split3<<<grid_of((int64_t)c.d * Kr, 256), 256, 0, s>>>(w_r, c.d, c.N, Kr, 0, 1, 0, rB);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    e = launch_wgrad(nullptr, 0, 0, nullptr, nullptr, 0, c.T, c.d, nullptr, rA, rB, Kr, dxr, err, s, allow_pair, true);
+    const WgOperand none{nullptr, 0, 0, false};
+    e = launch_wgrad(nullptr, 0, 0, none, none, c.T, c.d, nullptr, WgOperand{rA, Kr, 0, false},
+                     WgOperand{rB, Kr, 0, false}, Kr, dxr, err, s, allow_pair, true);
     if (e != cudaSuccess) return e;
-    // dW_rᵀ halves [2N][d] = [dL_hiᵀ ; dL_loᵀ] · (xᵀ)ᵀ over the tokens (x exact in bf16, xᵀ [d][Tp])
+    // dW_rᵀ halves [2N][d] = [dL_hiᵀ ; dL_loᵀ] · x over the tokens (x exact in bf16, read
+    // in its own layout [T][d] as the MN-major operand; tokens past T read as zero)
     k_split_t<<<dim3(Tp / 32, (c.N + 31) / 32), 256, 0, s>>>(dL, c.T, c.N, Tp, dLt);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     float *wrC = reinterpret_cast<float *>(bw + L.wrC);
-    e = launch_wgrad(nullptr, 0, 0, nullptr, nullptr, 0, 2 * c.N, c.d, nullptr, dLt, bw + L.x_t, Tp, wrC, err, s,
-                     allow_pair, true);
+    e = launch_wgrad(nullptr, 0, 0, none, none, 2 * c.N, c.d, nullptr, WgOperand{dLt, Tp, 0, false},
+                     WgOperand{x, c.d, c.T, true}, Tp, wrC, err, s, allow_pair, true);
     if (e != cudaSuccess) return e;
     k_sum_hi_lo_t<<<dim3((c.d + 31) / 32, (c.N + 31) / 32), 256, 0, s>>>(wrC, c.N, c.d, dw_r);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -1,16 +1,22 @@
-// Backward building blocks on the GPU: the weight-gradient GEMM of the experts and
-// the transposes that feed the K-major tensor-core kernels.
+// Weight-gradient GEMM of the experts on the tensor cores.
 //
 // The experts' weight gradients reduce over each expert's rows: dW_out[e] =
 // dO_eᵀ H_e, dW_a[e] = dA_eᵀ X_e, dW_b[e] = dB_eᵀ X_e (the chain rule through
 // O = H W_outᵀ, H = act(X W_aᵀ) (⊙ X W_bᵀ)). K is an expert's row count, so it varies
-// per expert. The activations are transposed into [M][Kall] with expert e's rows in
-// columns k0_e .. k0_e + R_e - 1, zero up to kp_e = R_e rounded up to 64, so that a
-// 64-wide K tile never reads another expert's rows (k_transpose_rows_padded). The
-// weight-gradient kernel (k_wgrad_tc) is the single-CTA tcgen05 structure of
-// ffn_tc.cu — TMA producer warp, one MMA-issuing thread, four epilogue warps, two
-// TMEM accumulators of 128 x 256 fp32 — with tiles (expert, m, n), K from the
-// expert's column range, and an all-zero tile for an expert without rows.
+// per expert. Both operands are read where the forward and the row products left them,
+// [rows][columns] with the rows grouped by expert: for these products that is the
+// MN-major layout (M or N contiguous), staged as 64-column chunks of 64 K-rows under the
+// 128-byte swizzle. Expert e's k-blocks start at its first row; when its row count is
+// not a multiple of 64 its last k-block reaches into the next expert's rows (or past the
+// rows in use), and those K-rows are zeroed in shared memory before the MMAs read the
+// stage: in this layout K-row i of a chunk is its 128-byte line i, so that is the tail of
+// each 8 KB chunk. The kernels — a TMA producer warp, an MMA-issuing warp, four epilogue
+// warps, a fixup warp that does that zeroing as soon as such a stage lands, two TMEM
+// accumulators — take tiles (expert, m, n) and store an all-zero tile for an expert
+// without rows. An optional shared segment (the shared expert, or with no
+// routed segment a plain product such as the router's gradients) reduces over K_sh,
+// with either operand MN-major ([K_sh][..], rows past K_sh read as zero by the copy) or
+// K-major ([M|Nn][K_sh], zero-padded to a multiple of 64).
 #include <algorithm>
 #include <cstring>
 
@@ -26,29 +32,84 @@ using namespace tc;
 
 constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
 constexpr uint32_t A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2, STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int NUM_THREADS = 192;
+constexpr uint32_t CHUNK_BYTES = 64 * BK * 2;  // MN-major: 64 columns x 64 K-rows
+constexpr int NUM_THREADS = 224;  // 7 warps (roles below)
 constexpr int MAX_SEG = 257;
 constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + 1024;
 
 struct WgParams {
-    CUtensorMap tmA, tmB;        // At [M][Kall] (box 64 x 128), Bt [Nn][Kall] (box 64 x 256)
-    CUtensorMap tmA_sh, tmB_sh;  // shared segment: [M][K_sh], [Nn][K_sh]
+    CUtensorMap tmA, tmB;        // routed segments: MN-major maps over [a_rows][M], [a_rows][Nn] seen as
+                                 // (64 columns, rows, 64-column chunks): one box stages a CTA's chunks
+    CUtensorMap tmA_sh, tmB_sh;  // shared segment: MN-major as above over K_sh rows, or K-major over
+                                 // [M|Nn][K_sh] with a box of 64 x the rows one CTA stages
     CUtensorMap tmC, tmC_sh;     // outputs for the pair kernel's stores: [n_seg][M][Nn], [1][M][Nn], box of
                                  // 32 rows x 128 bytes (64 bf16 or 32 fp32 columns)
     const int32_t *offsets;      // [n_seg + 1] rows of each expert
     int n_seg, has_sh;
     int a_rows;                  // offsets are clamped to it
     int M, Nn, K_sh;
+    int a_mn_sh, b_mn_sh;        // the shared segment's operands MN-major (routed ones always are)
     void *C, *C_sh;              // [n_seg][M][Nn], [M][Nn]: bf16, or fp32 in the kernels' F32 form
     uint32_t *err;
 };
 
+// Per segment: first K-row, k-blocks, and the valid rows of a partial last k-block (0: none).
+struct SegK {
+    int k0[MAX_SEG], nk[MAX_SEG], kv[MAX_SEG];
+};
+
+__device__ __forceinline__ void seg_k_ranges(const WgParams &p, SegK &s, int lane) {
+    for (int g = lane; g < p.n_seg; g += 32) {
+        const int r0 = min(max(p.offsets[g], 0), p.a_rows);
+        const int r1 = min(max(p.offsets[g + 1], r0), p.a_rows);
+        s.k0[g] = r0;
+        s.nk[g] = (r1 - r0 + BK - 1) / BK;
+        s.kv[g] = (r1 - r0) % BK;
+    }
+    if (lane == 0 && p.has_sh) {
+        s.k0[p.n_seg] = 0;
+        s.nk[p.n_seg] = (p.K_sh + BK - 1) / BK;
+        s.kv[p.n_seg] = 0;  // MN-major: rows past K_sh are outside the map (zero); K-major: zero-padded
+    }
+}
+
+// Zero K-rows kv .. 63 of `chunks` consecutive MN-major chunks (lines kv .. 63 of each
+// 8 KB chunk; a line keeps its 16-byte units whatever the swizzle). One warp.
+__device__ __forceinline__ void zero_k_tail(uint8_t *base, int chunks, int kv, int lane) {
+    for (int c = 0; c < chunks; ++c) {
+        uint4 *q = reinterpret_cast<uint4 *>(base + (size_t)c * CHUNK_BYTES);
+        for (int u = kv * 8 + lane; u < (int)(CHUNK_BYTES / 16); u += 32) q[u] = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+// Instruction-descriptor bits and descriptor steps (16-byte units per K step of 16) of a
+// segment's operands.
+struct SegMajor {
+    bool a_mn, b_mn;
+    __device__ uint32_t idesc_bits() const { return (a_mn ? kIdescAMajorMN : 0u) | (b_mn ? kIdescBMajorMN : 0u); }
+    __device__ uint64_t a_step() const { return a_mn ? 128u : 2u; }  // MN-major: 16 K-rows of 128 bytes
+    __device__ uint64_t b_step() const { return b_mn ? 128u : 2u; }
+    __device__ uint64_t a_desc(uint32_t addr) const { return a_mn ? desc_sw128_mn(addr) : desc_sw128(addr); }
+    __device__ uint64_t b_desc(uint32_t addr) const { return b_mn ? desc_sw128_mn(addr) : desc_sw128(addr); }
+};
+__device__ __forceinline__ SegMajor seg_major(const WgParams &p, int g) {
+    const bool sh = g >= p.n_seg;
+    return {!sh || p.a_mn_sh != 0, !sh || p.b_mn_sh != 0};
+}
+
 struct WgSmem {
     uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], drain;
+    uint64_t bfull[STAGES];  // a segment's partial last k-block landed (only those complete it)
+    uint64_t fixed[STAGES];  // ... and the fixup warp zeroed its rows past the segment
     uint32_t tmem_base;
     int abort_flag;
-    int k0[MAX_SEG], kp[MAX_SEG];  // first column and padded width of each segment's K range
+    SegK seg;
 };
+
+// Warp roles of both kernels: 0 TMA producer, 1 MMA issuer (one thread), 2-5 epilogue,
+// 6 fixup (zeroes the rows past a segment in a partial last k-block as soon as it lands,
+// beside the MMAs of the stages before it).
+constexpr int FIXUP_WARP = 6;
 
 // F32: the output is fp32 (general products of the router gradient), else bf16.
 template <bool F32>
@@ -67,46 +128,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_wgrad_tc(const __grid_consta
     const int total = nseg * per_seg;
 
     if (warp == 0) {
-        // K ranges: kp = rows rounded up to 64, k0 = exclusive scan (routed segments)
-        constexpr int PER = (MAX_SEG + 31) / 32;
-        int kp[PER];
-        int sum = 0;
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            const int g = lane * PER + i;
-            int v = 0;
-            if (g < p.n_seg) {
-                const int r0 = min(max(p.offsets[g], 0), p.a_rows);
-                const int r1 = min(max(p.offsets[g + 1], r0), p.a_rows);
-                v = (r1 - r0 + BK - 1) / BK * BK;
-            }
-            kp[i] = v;
-            sum += v;
-        }
-        int incl = sum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int u = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += u;
-        }
-        int run = incl - sum;
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            const int g = lane * PER + i;
-            if (g < p.n_seg) {
-                s.k0[g] = run;
-                s.kp[g] = kp[i];
-            }
-            run += kp[i];
-        }
-        if (lane == 0 && p.has_sh) {
-            s.k0[p.n_seg] = 0;
-            s.kp[p.n_seg] = p.K_sh;
-        }
+        seg_k_ranges(p, s.seg, lane);
         if (lane == 0) {
             for (int i = 0; i < STAGES; ++i) {
                 mbar_init(&s.full[i], 1);
                 mbar_init(&s.empty[i], 1);
+                mbar_init(&s.bfull[i], 1);
+                mbar_init(&s.fixed[i], 1);
             }
             for (int i = 0; i < 2; ++i) {
                 mbar_init(&s.tfull[i], 1);
@@ -129,66 +157,86 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_wgrad_tc(const __grid_consta
 
     if (warp == 0) {
         // ================= TMA producer =================
+        // A stage completes full[], or bfull[] when it is a segment's partial last k-block.
         if (lane == 0) {
             int st = 0;
             uint32_t ph = 0;
             bool ok = true;
-            uint32_t issued_mask = 0, issued_par = 0;
+            uint32_t issued_mask = 0, issued_par = 0, fcount = 0;    // full[]: parity of each stage's uses
+            uint32_t bissued_mask = 0, bissued_par = 0, bcount = 0;  // bfull[]
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
                 const int g = tile / per_seg, local = tile - g * per_seg;
                 const int m = local % mt, n = local / mt;
                 const bool sh = g >= p.n_seg;
+                const SegMajor mj = seg_major(p, g);
                 const CUtensorMap *ta = sh ? &p.tmA_sh : &p.tmA;
                 const CUtensorMap *tb = sh ? &p.tmB_sh : &p.tmB;
-                const int k0 = s.k0[g];
-                for (int kb = 0; kb < s.kp[g] / BK; ++kb) {
+                const int k0 = s.seg.k0[g], nk = s.seg.nk[g], kv = s.seg.kv[g];
+                for (int kb = 0; kb < nk; ++kb) {
                     if (!wait_bar(&s.empty[st], ph ^ 1, abort_flag, p.err)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&s.full[st], STAGE_BYTES);
-                    tma_load_2d(smA(st), ta, k0 + kb * BK, m * BM, &s.full[st]);
-                    tma_load_2d(smB(st), tb, k0 + kb * BK, n * BN, &s.full[st]);
-                    issued_mask |= 1u << st;
-                    issued_par = (issued_par & ~(1u << st)) | (ph << st);
+                    const uint32_t bit = 1u << st;
+                    const bool edge = kb == nk - 1 && kv != 0;
+                    uint64_t *bar = edge ? &s.bfull[st] : &s.full[st];
+                    mbar_arrive_expect_tx(bar, STAGE_BYTES);
+                    const int kc = k0 + kb * BK;
+                    if (mj.a_mn) tma_load_3d(smA(st), ta, 0, kc, m * (BM / 64), bar);
+                    else tma_load_2d(smA(st), ta, kc, m * BM, bar);
+                    if (mj.b_mn) tma_load_3d(smB(st), tb, 0, kc, n * (BN / 64), bar);
+                    else tma_load_2d(smB(st), tb, kc, n * BN, bar);
+                    if (edge) {
+                        bissued_mask |= bit;
+                        bissued_par = (bissued_par & ~bit) | (bcount & bit);
+                        bcount ^= bit;
+                    } else {
+                        issued_mask |= bit;
+                        issued_par = (issued_par & ~bit) | (fcount & bit);
+                        fcount ^= bit;
+                    }
                     if (++st == STAGES) {
                         st = 0;
                         ph ^= 1;
                     }
                 }
             }
-            for (int i = 0; i < STAGES; ++i)
+            for (int i = 0; i < STAGES; ++i) {
                 if (issued_mask & (1u << i)) drain_bar(&s.full[i], (issued_par >> i) & 1u);
+                if (bissued_mask & (1u << i)) drain_bar(&s.bfull[i], (bissued_par >> i) & 1u);
+            }
         }
     } else if (warp == 1) {
         // ================= MMA issuer =================
         if (lane == 0) {
-            constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
             int st = 0, acc = 0;
-            uint32_t ph = 0, aph = 0;
+            uint32_t aph = 0, fpar = 0, xpar = 0;  // per-stage parities of full[] and fixed[] uses
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
                 const int g = tile / per_seg;
+                const SegMajor mj = seg_major(p, g);
+                const uint32_t idesc = idesc_bf16_f32(BM, BN) | mj.idesc_bits();
                 if (!wait_bar(&s.tempty[acc], aph ^ 1, abort_flag, p.err)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-                for (int kb = 0; kb < s.kp[g] / BK; ++kb) {
-                    if (!wait_bar(&s.full[st], ph, abort_flag, p.err)) {
+                const int nk = s.seg.nk[g], kv = s.seg.kv[g];
+                for (int kb = 0; kb < nk; ++kb) {
+                    const uint32_t bit = 1u << st;
+                    const bool edge = kb == nk - 1 && kv != 0;
+                    if (!(edge ? wait_bar(&s.fixed[st], (xpar >> st) & 1u, abort_flag, p.err)
+                               : wait_bar(&s.full[st], (fpar >> st) & 1u, abort_flag, p.err))) {
                         ok = false;
                         break;
                     }
+                    if (edge) xpar ^= bit;
+                    else fpar ^= bit;
                     tc_fence_after();
-                    const uint64_t ad = desc_sw128(smem_u32(smA(st)));
-                    const uint64_t bd = desc_sw128(smem_u32(smB(st)));
+                    const uint64_t ad = mj.a_desc(smem_u32(smA(st))), bd = mj.b_desc(smem_u32(smB(st)));
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
-                        umma_bf16(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), IDESC,
-                                  (kb | kk) != 0 ? 1u : 0u);
+                        umma_bf16(d_tmem, ad + mj.a_step() * kk, bd + mj.b_step() * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
                     umma_commit(&s.empty[st]);
-                    if (++st == STAGES) {
-                        st = 0;
-                        ph ^= 1;
-                    }
+                    if (++st == STAGES) st = 0;
                 }
                 if (!ok) break;
                 umma_commit(&s.tfull[acc]);  // no MMA for an empty segment: the epilogue writes zeros
@@ -199,6 +247,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_wgrad_tc(const __grid_consta
             }
             umma_commit(&s.drain);
             drain_bar(&s.drain, 0);
+        }
+    } else if (warp == FIXUP_WARP) {
+        // ================= fixup: rows past a segment in its partial last k-block =================
+        int st = 0;
+        uint32_t bpar = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+            const int g = tile / per_seg;
+            const int nk = s.seg.nk[g], kv = s.seg.kv[g];
+            for (int kb = 0; kb < nk; ++kb) {
+                if (kb == nk - 1 && kv != 0) {
+                    if (!__all_sync(0xffffffffu, wait_bar(&s.bfull[st], (bpar >> st) & 1u, abort_flag, p.err))) {
+                        ok = false;
+                        break;
+                    }
+                    bpar ^= 1u << st;
+                    zero_k_tail(smA(st), BM / 64, kv, lane);  // routed segments: both operands MN-major
+                    zero_k_tail(smB(st), BN / 64, kv, lane);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&s.fixed[st]);
+                }
+                if (++st == STAGES) st = 0;
+            }
         }
     } else {
         // ================= epilogue (warps 2..5) =================
@@ -213,7 +285,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_wgrad_tc(const __grid_consta
             if (!wait_bar(&s.tfull[acc], aph, abort_flag, p.err)) break;
             tc_fence_after();
             const int row = m * BM + r_in_tile;
-            const bool empty_seg = s.kp[g] == 0;
+            const bool empty_seg = s.seg.nk[g] == 0;
             const size_t crow = ((sh ? 0 : (size_t)g * p.M) + (size_t)row) * p.Nn;  // element offset of the row
             const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16);
 #pragma unroll 1
@@ -265,10 +337,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_wgrad_tc(const __grid_consta
 //
 // The same tiles with 2-CTA (cta_group::2) MMAs, as the forward's pair kernel in
 // ffn_tc.cu: a cluster of two CTAs computes a 256 x 256 output tile per MMA
-// 256x256x16; each CTA stages 128 rows of At and 128 of the 256 rows of Bt per
-// k-block (a third less operand data per FLOP than the single-CTA kernel), both
+// 256x256x16; each CTA stages 128 of the 256 A columns (M) and 128 of the 256 B columns
+// (N) per k-block (a third less operand data per FLOP than the single-CTA kernel), both
 // halves complete on the even CTA's stage barrier, the even CTA issues the MMAs and
 // its commits arrive on both CTAs' barriers; each CTA's epilogue stores its 128 rows.
+// A segment's partial last k-block is the exception: each CTA's half lands on that CTA's
+// own bfull[] barrier, each CTA's fixup warp zeroes the rows past the segment in its half
+// and arrives on the even CTA's fixed[] barrier (two arrivals), and the MMA issuer waits
+// for fixed[] instead of full[] before that k-block's MMAs.
 // The epilogue writes through shared memory: each warp converts 32 rows x 64 columns
 // to bf16 (32 columns in the fp32 form) into one of two 4 KB boxes laid out as the
 // output map's 128-byte swizzle and stores the box with one TMA tensor store, so whole
@@ -284,14 +360,15 @@ constexpr size_t SMEM2_BYTES = (size_t)STAGES2 * STAGE2_BYTES + 4 * 2 * OUT_BOX_
 
 struct WgSmem2 {
     uint64_t full[STAGES2], empty[STAGES2], tfull[2], tempty[2], drain;
+    uint64_t bfull[STAGES2];  // this CTA's half of a partial last k-block landed
+    uint64_t fixed[STAGES2];  // even CTA: both halves of that k-block zeroed past the segment
     uint32_t tmem_base;
     int abort_flag;
-    int k0[MAX_SEG], kp[MAX_SEG];
+    SegK seg;
 };
 static_assert(SMEM2_BYTES + sizeof(WgSmem2) <= 232448, "shared memory budget of one CTA");
 static_assert(STAGE2_BYTES % 1024 == 0 && OUT_BOX_BYTES % 1024 == 0, "swizzled boxes stay 1024-byte aligned");
 
-// Tensor maps as in WgParams but with 128-row boxes for Bt (each CTA loads half).
 template <bool F32>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     k_wgrad_tc2(const __grid_constant__ WgParams p) {
@@ -312,45 +389,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const int total = nseg * per_seg;
 
     if (warp == 0) {
-        constexpr int PER = (MAX_SEG + 31) / 32;
-        int kp[PER];
-        int sum = 0;
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            const int g = lane * PER + i;
-            int v = 0;
-            if (g < p.n_seg) {
-                const int r0 = min(max(p.offsets[g], 0), p.a_rows);
-                const int r1 = min(max(p.offsets[g + 1], r0), p.a_rows);
-                v = (r1 - r0 + BK - 1) / BK * BK;
-            }
-            kp[i] = v;
-            sum += v;
-        }
-        int incl = sum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int u = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += u;
-        }
-        int run = incl - sum;
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            const int g = lane * PER + i;
-            if (g < p.n_seg) {
-                s.k0[g] = run;
-                s.kp[g] = kp[i];
-            }
-            run += kp[i];
-        }
-        if (lane == 0 && p.has_sh) {
-            s.k0[p.n_seg] = 0;
-            s.kp[p.n_seg] = p.K_sh;
-        }
+        seg_k_ranges(p, s.seg, lane);
         if (lane == 0) {
             for (int i = 0; i < STAGES2; ++i) {
                 mbar_init(&s.full[i], 1);
                 mbar_init(&s.empty[i], 1);
+                mbar_init(&s.bfull[i], 1);
+                mbar_init(&s.fixed[i], 2);  // the fixup warps of both CTAs
             }
             for (int i = 0; i < 2; ++i) {
                 mbar_init(&s.tfull[i], 1);
@@ -382,74 +427,102 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const bool run = s.abort_flag == 0;
     volatile int *abort_flag = &s.abort_flag;
     const uint32_t lead_tempty = map_to_rank(smem_u32(&s.tempty[0]), 0);
+    const uint32_t lead_fixed = map_to_rank(smem_u32(&s.fixed[0]), 0);
 
     if (warp == 0) {
         // ================= TMA producer (both CTAs) =================
+        // Both CTAs' loads complete on the even CTA's full[] barrier, which the even
+        // CTA's producer arms with the bytes of both halves; in a partial last k-block
+        // each CTA's half lands on its own bfull[] instead.
         if (lane == 0 && run) {
             int st = 0;
             uint32_t ph = 0;
             bool ok = true;
-            uint32_t issued_mask = 0, issued_par = 0;
+            uint32_t issued_mask = 0, issued_par = 0, fcount = 0;    // full[] (even CTA)
+            uint32_t bissued_mask = 0, bissued_par = 0, bcount = 0;  // bfull[] (each CTA)
             const uint32_t lead_full = map_to_rank(smem_u32(&s.full[0]), 0);
             for (int tile = cluster; tile < total && ok; tile += nclusters) {
                 const int g = tile / per_seg, local = tile - g * per_seg;
                 const int m = local % mt, n = local / mt;
                 const bool sh = g >= p.n_seg;
+                const SegMajor mj = seg_major(p, g);
                 const CUtensorMap *ta = sh ? &p.tmA_sh : &p.tmA;
                 const CUtensorMap *tb = sh ? &p.tmB_sh : &p.tmB;
-                const int k0 = s.k0[g];
-                const int arow = m * 2 * BM + (int)rank * BM, brow = n * BN + (int)rank * (BN / 2);
-                for (int kb = 0; kb < s.kp[g] / BK; ++kb) {
+                const int k0 = s.seg.k0[g], nk = s.seg.nk[g], kv = s.seg.kv[g];
+                const int acol = m * 2 * BM + (int)rank * BM, bcol = n * BN + (int)rank * (BN / 2);
+                for (int kb = 0; kb < nk; ++kb) {
                     if (!wait_bar(&s.empty[st], ph ^ 1, abort_flag, p.err)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t fb = lead_full + 8u * (uint32_t)st;
-                    if (leader) mbar_arrive_expect_tx(&s.full[st], 2 * STAGE2_BYTES);
-                    tma_load_2d_pair(smA(st), ta, k0 + kb * BK, arow, fb);
-                    tma_load_2d_pair(smB(st), tb, k0 + kb * BK, brow, fb);
-                    issued_mask |= 1u << st;
-                    issued_par = (issued_par & ~(1u << st)) | (ph << st);
+                    const uint32_t bit = 1u << st;
+                    const bool edge = kb == nk - 1 && kv != 0;
+                    const int kc = k0 + kb * BK;
+                    if (edge) {
+                        // routed segment (MN-major): this CTA's half, plain copies into its own stage
+                        mbar_arrive_expect_tx(&s.bfull[st], STAGE2_BYTES);
+                        tma_load_3d(smA(st), ta, 0, kc, acol / 64, &s.bfull[st]);
+                        tma_load_3d(smB(st), tb, 0, kc, bcol / 64, &s.bfull[st]);
+                        bissued_mask |= bit;
+                        bissued_par = (bissued_par & ~bit) | (bcount & bit);
+                        bcount ^= bit;
+                    } else {
+                        const uint32_t fb = lead_full + 8u * (uint32_t)st;
+                        if (leader) mbar_arrive_expect_tx(&s.full[st], 2 * STAGE2_BYTES);
+                        if (mj.a_mn) tma_load_3d_pair(smA(st), ta, 0, kc, acol / 64, fb);
+                        else tma_load_2d_pair(smA(st), ta, kc, acol, fb);
+                        if (mj.b_mn) tma_load_3d_pair(smB(st), tb, 0, kc, bcol / 64, fb);
+                        else tma_load_2d_pair(smB(st), tb, kc, bcol, fb);
+                        issued_mask |= bit;
+                        issued_par = (issued_par & ~bit) | (fcount & bit);
+                        fcount ^= bit;
+                    }
                     if (++st == STAGES2) {
                         st = 0;
                         ph ^= 1;
                     }
                 }
             }
-            // loads in flight land before the CTA exits (the even CTA waits for both halves)
-            if (leader)
-                for (int i = 0; i < STAGES2; ++i)
-                    if (issued_mask & (1u << i)) drain_bar(&s.full[i], (issued_par >> i) & 1u);
+            // loads in flight land before the CTA exits (the even CTA waits for both halves
+            // on full[], each CTA for its own half on bfull[])
+            for (int i = 0; i < STAGES2; ++i) {
+                if (leader && (issued_mask & (1u << i))) drain_bar(&s.full[i], (issued_par >> i) & 1u);
+                if (bissued_mask & (1u << i)) drain_bar(&s.bfull[i], (bissued_par >> i) & 1u);
+            }
         }
     } else if (warp == 1) {
         if (lane == 0 && run && leader) {
             // ================= MMA issuer (even CTA) =================
-            constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, BN);
             int st = 0, acc = 0;
-            uint32_t ph = 0, aph = 0;
+            uint32_t aph = 0, fpar = 0, xpar = 0;  // per-stage parities of full[] and fixed[] uses
             bool ok = true;
             for (int tile = cluster; tile < total && ok; tile += nclusters) {
                 const int g = tile / per_seg;
+                const SegMajor mj = seg_major(p, g);
+                const uint32_t idesc = idesc_bf16_f32(2 * BM, BN) | mj.idesc_bits();
                 if (!wait_bar(&s.tempty[acc], aph ^ 1, abort_flag, p.err)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-                for (int kb = 0; kb < s.kp[g] / BK; ++kb) {
-                    if (!wait_bar(&s.full[st], ph, abort_flag, p.err)) {
+                const int nk = s.seg.nk[g], kv = s.seg.kv[g];
+                for (int kb = 0; kb < nk; ++kb) {
+                    const uint32_t bit = 1u << st;
+                    const bool edge = kb == nk - 1 && kv != 0;
+                    // fixed[] gets the odd CTA's fixup arrival from across the cluster
+                    if (!(edge ? wait_bar_cluster(&s.fixed[st], (xpar >> st) & 1u, abort_flag, p.err)
+                               : wait_bar(&s.full[st], (fpar >> st) & 1u, abort_flag, p.err))) {
                         ok = false;
                         break;
                     }
+                    if (edge) xpar ^= bit;
+                    else fpar ^= bit;
                     tc_fence_after();
-                    const uint64_t ad = desc_sw128(smem_u32(smA(st)));
-                    const uint64_t bd = desc_sw128(smem_u32(smB(st)));
+                    const uint64_t ad = mj.a_desc(smem_u32(smA(st))), bd = mj.b_desc(smem_u32(smB(st)));
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
-                        umma_bf16_pair(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), IDESC,
+                        umma_bf16_pair(d_tmem, ad + mj.a_step() * kk, bd + mj.b_step() * kk, idesc,
                                        (kb | kk) != 0 ? 1u : 0u);
                     umma_commit_pair_mc(&s.empty[st], 0x3);
-                    if (++st == STAGES2) {
-                        st = 0;
-                        ph ^= 1;
-                    }
+                    if (++st == STAGES2) st = 0;
                 }
                 if (!ok) break;
                 umma_commit_pair_mc(&s.tfull[acc], 0x3);  // no MMA for an empty segment: zeros stored
@@ -460,6 +533,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             }
             umma_commit_pair_mc(&s.drain, 0x1);
             drain_bar(&s.drain, 0);
+        }
+    } else if (warp == FIXUP_WARP) {
+        if (run) {
+            // ================= fixup (both CTAs): rows past a segment in this CTA's half ==========
+            int st = 0;
+            uint32_t bpar = 0;
+            bool ok = true;
+            for (int tile = cluster; tile < total && ok; tile += nclusters) {
+                const int g = tile / per_seg;
+                const int nk = s.seg.nk[g], kv = s.seg.kv[g];
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (kb == nk - 1 && kv != 0) {
+                        if (!__all_sync(0xffffffffu, wait_bar(&s.bfull[st], (bpar >> st) & 1u, abort_flag, p.err))) {
+                            ok = false;
+                            break;
+                        }
+                        bpar ^= 1u << st;
+                        zero_k_tail(smA(st), 2, kv, lane);
+                        zero_k_tail(smB(st), 2, kv, lane);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if (leader) mbar_arrive(&s.fixed[st]);
+                            else mbar_arrive_remote(lead_fixed + 8u * (uint32_t)st);
+                        }
+                    }
+                    if (++st == STAGES2) st = 0;
+                }
+            }
         }
     } else if (run) {
         // ================= epilogue (warps 2..5 of both CTAs) =================
@@ -476,7 +578,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
             if (!wait_bar(&s.tfull[acc], aph, abort_flag, p.err)) break;
             tc_fence_after();
             const int row0 = m * 2 * BM + (int)rank * BM + quarter * 32;  // this warp's 32 rows
-            const bool empty_seg = s.kp[g] == 0;
+            const bool empty_seg = s.seg.nk[g] == 0;
             const CUtensorMap *cmap = sh ? &p.tmC_sh : &p.tmC;
             const int gz = sh ? 0 : g;
             const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16);
@@ -543,86 +645,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
-// kpre[g] = sum over segments g' < g of R_g' rounded up to 64 (g = 0 .. n_seg), one CTA.
-__global__ void __launch_bounds__(256) k_pad_prefix(const int32_t *__restrict__ offsets, int n_seg, int rows,
-                                                    int32_t *__restrict__ kpre) {
-    __shared__ int w[MAX_SEG];
-    for (int g = threadIdx.x; g < n_seg; g += blockDim.x) {
-        const int a = min(max(offsets[g], 0), rows);
-        const int e = min(max(offsets[g + 1], a), rows);
-        w[g] = (e - a + 63) / 64 * 64;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int run = 0;
-        for (int g = 0; g < n_seg; ++g) {
-            kpre[g] = run;
-            run += w[g];
-        }
-        kpre[n_seg] = run;
-    }
-}
-
-// Activation rows [rows][C] (row stride C) into the padded transposed layout
-// [C][Kall]: column kpre[g] + i holds row offsets[g] + i for i < R_g, zero up to
-// kpre[g + 1]; 64-column blocks from kpre[n_seg] on are left unwritten (no product reads
-// them). offsets null: one segment of `rows` rows, zero up to Kall.
-// 64 x 64 tiles, 16-byte loads and stores (C and Kall multiples of 8).
-__global__ void __launch_bounds__(256) k_transpose_rows_padded(const __nv_bfloat16 *__restrict__ src, int C,
-                                                               const int32_t *__restrict__ offsets,
-                                                               const int32_t *__restrict__ kpre, int n_seg,
-                                                               int rows, int64_t Kall,
-                                                               __nv_bfloat16 *__restrict__ dst) {
-    __shared__ __nv_bfloat16 tile[64][64 + 2];
-    __shared__ int srow[64];
-    const int64_t k0 = (int64_t)blockIdx.x * 64;
-    const int c0 = blockIdx.y * 64;
-    if (offsets && k0 >= kpre[n_seg]) return;  // past the last segment: never read
-    if (threadIdx.x < 64) {
-        // source row of padded column k0 + threadIdx.x (-1: padding), by binary search on kpre
-        const int64_t kc = k0 + threadIdx.x;
-        int r = -1;
-        if (!offsets) {
-            r = kc < rows ? (int)kc : -1;
-        } else if (kc < kpre[n_seg]) {
-            int lo = 0, hi = n_seg - 1;  // largest g with kpre[g] <= kc
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (kpre[mid] <= kc) lo = mid;
-                else hi = mid - 1;
-            }
-            const int a = min(max(offsets[lo], 0), rows);
-            const int e = min(max(offsets[lo + 1], a), rows);
-            const int64_t i = kc - kpre[lo];
-            r = i < e - a ? (int)(a + i) : -1;
-        }
-        srow[threadIdx.x] = r;
-    }
-    __syncthreads();
-    for (int v = threadIdx.x; v < 64 * 8; v += 256) {
-        const int i = v >> 3, j = (v & 7) * 8;  // padded column k0 + i, source columns c0 + j .. + 7
-        const int r = srow[i];
-        uint4 q = make_uint4(0, 0, 0, 0);
-        if (r >= 0 && c0 + j < C) q = *reinterpret_cast<const uint4 *>(src + (size_t)r * C + c0 + j);
-        const __nv_bfloat16 *e = reinterpret_cast<const __nv_bfloat16 *>(&q);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) tile[i][j + u] = e[u];
-    }
-    __syncthreads();
-    for (int v = threadIdx.x; v < 64 * 8; v += 256) {
-        const int i = v >> 3, j = (v & 7) * 8;  // destination row c0 + i, padded columns k0 + j .. + 7
-        if (c0 + i < C && k0 + j < Kall) {
-            __align__(16) __nv_bfloat16 e[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) e[u] = tile[j + u][i];
-            *reinterpret_cast<uint4 *>(dst + (size_t)(c0 + i) * Kall + k0 + j) = *reinterpret_cast<const uint4 *>(e);
-        }
-    }
-}
-
 }  // namespace
-
-int64_t wgrad_kall_bound(const moe_config &c) { return (max_rows(c) + 64LL * c.N + 63) / 64 * 64; }
 
 // Output map of the pair kernel's tensor stores: [n][M][Nn] of bf16 or fp32, box of 32
 // rows x 128 bytes, 128-byte swizzle.
@@ -635,6 +658,27 @@ static bool encode_out_map(CUtensorMap *m, void *base, int Nn, int M, int n, boo
                        strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// An operand's map. MN-major: [o.rows][o.ld] (cols columns used, a multiple of 64) seen
+// as (64 columns, rows, cols / 64 chunks) with the chunks 128 bytes apart, box 64 x 64 x
+// box_k / 64: one copy stages box_k columns of 64 K-rows as consecutive 8 KB chunks (K-rows
+// past o.rows read as zero). K-major: [cols][o.ld] (K = o.ld), box 64 x box_k.
+static bool encode_operand(CUtensorMap *m, const WgOperand &o, uint64_t cols, uint32_t box_k) {
+    if (!o.p || o.ld <= 0 || (o.ld * 2) % 16 != 0 || box_k % 64 != 0 ||
+        (o.mn && (o.rows <= 0 || cols % 64 != 0 || cols > (uint64_t)o.ld)))
+        return false;
+    if (o.mn) {
+        const uint64_t dims[3] = {64u, (uint64_t)o.rows, cols / 64};
+        const uint64_t strides[2] = {(uint64_t)o.ld * 2, 128u};
+        const uint32_t box[3] = {64u, 64u, box_k / 64};
+        return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, o.p, dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
+    }
+    const uint64_t dims[2] = {(uint64_t)o.ld, cols};
+    const uint64_t strides[1] = {(uint64_t)o.ld * 2};
+    const uint32_t box[2] = {64u, box_k};
+    return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, o.p, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 template <typename Kern> static cudaError_t smem_attr_once(Kern kern, size_t bytes, bool &done) {
     if (done) return cudaSuccess;
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
@@ -642,33 +686,41 @@ template <typename Kern> static cudaError_t smem_attr_once(Kern kern, size_t byt
     return e;
 }
 
-cudaError_t launch_wgrad(const int32_t *offsets, int n_seg, int64_t a_rows, const void *At, const void *Bt,
-                         int64_t Kall, int M, int Nn, void *out, const void *At_sh, const void *Bt_sh, int K_sh,
-                         void *out_sh, uint32_t *err, cudaStream_t s, bool allow_pair, bool f32_out) {
+cudaError_t launch_wgrad(const int32_t *offsets, int n_seg, int64_t a_rows, WgOperand A, WgOperand B, int M, int Nn,
+                         void *out, WgOperand A_sh, WgOperand B_sh, int K_sh, void *out_sh, uint32_t *err,
+                         cudaStream_t s, bool allow_pair, bool f32_out) {
     // CTA pairs once a 256-row output tile is not mostly empty
     const bool pair = allow_pair && M >= 2 * BM;
-    const uint32_t box_b = pair ? BN / 2 : BN;
-    if (Nn % 64 != 0) return cudaErrorInvalidValue;
+    if (Nn % 64 != 0 || M <= 0 || n_seg < 0 || n_seg >= MAX_SEG) return cudaErrorInvalidValue;
     WgParams p;
     memset(&p, 0, sizeof(p));
     p.offsets = offsets;
     p.n_seg = n_seg;
-    p.has_sh = At_sh ? 1 : 0;
+    p.has_sh = A_sh.p ? 1 : 0;
     p.a_rows = (int)a_rows;
     p.M = M;
     p.Nn = Nn;
     p.K_sh = K_sh;
+    p.a_mn_sh = A_sh.mn ? 1 : 0;
+    p.b_mn_sh = B_sh.mn ? 1 : 0;
     p.C = out;
     p.C_sh = out_sh;
     p.err = err;
     if (n_seg > 0) {
-        if (!encode_bf16_2d(&p.tmA, At, (uint64_t)Kall, (uint64_t)M, BM)) return cudaErrorInvalidValue;
-        if (!encode_bf16_2d(&p.tmB, Bt, (uint64_t)Kall, (uint64_t)Nn, box_b)) return cudaErrorInvalidValue;
+        // the routed segments' operands are the activations in their own layout
+        if (!A.mn || !B.mn || !offsets) return cudaErrorInvalidValue;
+        if (A.rows != a_rows || B.rows != a_rows || !encode_operand(&p.tmA, A, (uint64_t)M, BM) ||
+            !encode_operand(&p.tmB, B, (uint64_t)Nn, pair ? BN / 2 : BN))
+            return cudaErrorInvalidValue;
         if (pair && !encode_out_map(&p.tmC, out, Nn, M, n_seg, f32_out)) return cudaErrorInvalidValue;
     }
     if (p.has_sh) {
-        if (!encode_bf16_2d(&p.tmA_sh, At_sh, (uint64_t)K_sh, (uint64_t)M, BM)) return cudaErrorInvalidValue;
-        if (!encode_bf16_2d(&p.tmB_sh, Bt_sh, (uint64_t)K_sh, (uint64_t)Nn, box_b)) return cudaErrorInvalidValue;
+        // K-major operands hold K_sh (zero-padded to a multiple of 64) per row
+        if ((!A_sh.mn && (A_sh.ld != K_sh || K_sh % BK)) || (!B_sh.mn && (B_sh.ld != K_sh || K_sh % BK)))
+            return cudaErrorInvalidValue;
+        if (K_sh <= 0 || !encode_operand(&p.tmA_sh, A_sh, (uint64_t)M, BM) ||
+            !encode_operand(&p.tmB_sh, B_sh, (uint64_t)Nn, pair ? BN / 2 : BN))
+            return cudaErrorInvalidValue;
         if (pair && !encode_out_map(&p.tmC_sh, out_sh, Nn, M, 1, f32_out)) return cudaErrorInvalidValue;
     }
     cudaError_t e;
@@ -693,19 +745,6 @@ cudaError_t launch_wgrad(const int32_t *offsets, int n_seg, int64_t a_rows, cons
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, device_sm_count()));
     if (f32_out) k_wgrad_tc<true><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(p);
     else k_wgrad_tc<false><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(p);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_pad_prefix(const int32_t *offsets, int n_seg, int rows, int32_t *kpre, cudaStream_t s) {
-    k_pad_prefix<<<1, 256, 0, s>>>(offsets, n_seg, rows, kpre);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_transpose_rows_padded(const void *src, int C, const int32_t *offsets, const int32_t *kpre,
-                                         int n_seg, int rows, int64_t Kall, void *dst, cudaStream_t s) {
-    dim3 grid((unsigned)((Kall + 63) / 64), (unsigned)((C + 63) / 64));
-    k_transpose_rows_padded<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(src), C, offsets, kpre, n_seg,
-                                                 rows, Kall, static_cast<__nv_bfloat16 *>(dst));
     return cudaGetLastError();
 }
 

@@ -71,11 +71,7 @@ struct BwdLayout {
     size_t dgate;                // f32  [T][k]      gate gradients
     size_t AB, dH, dAB;          // bf16 [R_max][W], [R_max][h], [R_max][W]
     size_t dX;                   // bf16 [R_max][d]
-    size_t kpre;                 // int32 [N+1] padded column offsets of the experts' K ranges
-    size_t dO_t, H_t, dAB_t, X_t;  // bf16 transposed activations [d|h|W|d][Kall]
     size_t AB_sh, dH_sh, dAB_sh, dX_sh;  // shared expert, rows = T
-    size_t dy_t, Hsh_t, dABsh_t;     // shared expert, [..][ceil64(T)]
-    size_t x_t;                      // bf16 xᵀ [d][ceil64(T)] (shared expert and router weight gradients)
     size_t logits, routed, dL, dxr;  // router: f32 [T][N] (N <= 32: recomputed), int32 [N], f32 [T][N], f32 [T][d]
     size_t rA, rB, dLt, wrC;         // router-gradient split operands: bf16 [T][Kr], [d][Kr] (Kr = 3N
                                      // rounded up to 64), [2N][ceil64(T)]; f32 [2N][d] dW_rᵀ halves
@@ -116,10 +112,11 @@ cudaError_t launch_bwd_slots(const moe_config &c, const void *dy, const void *y_
 cudaError_t launch_act_bwd(bool gated, const void *AB, const void *dH, int64_t rows, int h, void *dAB,
                            cudaStream_t s);
 // Router backward from the fp32 logits [T][N]: dL, then dx_router (into L.dxr) and dW_r
-// on the tensor cores from bf16-split operands; xᵀ (L.x_t) must be in place.
-cudaError_t launch_router_bwd(const moe_config &c, const float *w_r, const float *logits, const int32_t *topk_idx,
-                              const float *topk_gate, const BwdLayout &L, uint8_t *bw, float aux_coef, float z_coef,
-                              float *dw_r, float *db_r, uint32_t *err, bool allow_pair, cudaStream_t s);
+// on the tensor cores from bf16-split operands and the tokens x [T][d].
+cudaError_t launch_router_bwd(const moe_config &c, const void *x, const float *w_r, const float *logits,
+                              const int32_t *topk_idx, const float *topk_gate, const BwdLayout &L, uint8_t *bw,
+                              float aux_coef, float z_coef, float *dw_r, float *db_r, uint32_t *err, bool allow_pair,
+                              cudaStream_t s);
 cudaError_t launch_bwd_dx(const moe_config &c, const void *dy, const void *dX, const int32_t *slot_row,
                           const void *dX_sh, const float *dxr, void *dx, uint32_t *err, cudaStream_t s);
 // Token-sharded router, phase 1: routing of this shard and the statistics the
@@ -182,23 +179,25 @@ cudaError_t launch_gemm_rows(const moe_config &c, bool preact, const int32_t *of
                              const void *a_sh, const void *b0_sh, const void *b1_sh, int K_sh, int n_out_sh,
                              void *out_sh, uint32_t *err, cudaStream_t s, bool b_mn = false, int k_split = 0,
                              int k_split_sh = 0);
-// Weight-gradient GEMM with K running over each expert's rows: for expert e,
-// out[e] [M][Nn] = At[:, k0_e : k0_e + kp_e] · Bt[:, k0_e : k0_e + kp_e]ᵀ, where the
-// transposed activations At [M][Kall], Bt [Nn][Kall] hold expert e's rows in columns
-// k0_e .. k0_e + R_e - 1 and zeros up to kp_e = R_e rounded up to 64 (k0 = exclusive
-// scan of kp, R_e from offsets). An optional shared segment: out_sh = At_sh · Bt_shᵀ
-// over K_sh (a multiple of 64) columns; with n_seg = 0 that is a plain product. Outputs
-// are bf16, or fp32 with f32_out. Nn must be a multiple of 64; M is any row count.
-cudaError_t launch_wgrad(const int32_t *offsets, int n_seg, int64_t a_rows, const void *At, const void *Bt,
-                         int64_t Kall, int M, int Nn, void *out, const void *At_sh, const void *Bt_sh, int K_sh,
-                         void *out_sh, uint32_t *err, cudaStream_t s, bool allow_pair = true, bool f32_out = false);
-// Upper bound of Kall (columns of the padded transposed layout) for a config.
-int64_t wgrad_kall_bound(const moe_config &c);
-// kpre[g] = sum over g' < g of rows of segment g' rounded up to 64 (g = 0 .. n_seg).
-cudaError_t launch_pad_prefix(const int32_t *offsets, int n_seg, int rows, int32_t *kpre, cudaStream_t s);
-// Rows [rows][C] into [C][Kall] in that padded column layout (offsets null: one segment).
-cudaError_t launch_transpose_rows_padded(const void *src, int C, const int32_t *offsets, const int32_t *kpre,
-                                         int n_seg, int rows, int64_t Kall, void *dst, cudaStream_t s);
+// An operand of the weight-gradient GEMM. MN-major (mn): an activation array
+// [rows][ld] whose first M (or Nn) columns are the operand, its rows the reduction
+// index; K-rows at or past `rows` read as zero. K-major: [M|Nn][ld] with K = ld along
+// each row (zero-padded to a multiple of 64).
+struct WgOperand {
+    const void *p;
+    int64_t ld, rows;
+    bool mn;
+};
+// Weight-gradient GEMM with K running over each expert's rows: for expert e with rows
+// [r0, r1) of `offsets` (clamped to a_rows), out[e] [M][Nn] = A[r0:r1]ᵀ · B[r0:r1] with A
+// and B MN-major over the a_rows rows of the routed buffers. An optional shared segment:
+// out_sh [M][Nn] = Aᵀ B over K_sh K-rows, either operand MN-major or K-major (then ld =
+// K_sh, a multiple of 64); with n_seg = 0 that is a plain product. Outputs are bf16, or
+// fp32 with f32_out. Nn must be a multiple of 64; M is any row count; ld × 2 bytes and
+// the operand addresses must be multiples of 16.
+cudaError_t launch_wgrad(const int32_t *offsets, int n_seg, int64_t a_rows, WgOperand A, WgOperand B, int M, int Nn,
+                         void *out, WgOperand A_sh, WgOperand B_sh, int K_sh, void *out_sh, uint32_t *err,
+                         cudaStream_t s, bool allow_pair = true, bool f32_out = false);
 
 int device_sm_count();
 

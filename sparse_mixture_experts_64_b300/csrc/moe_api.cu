@@ -384,68 +384,39 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const float *w_r, 
     const void *x_perm = w + L.x_perm, *y_perm = w + L.y_perm, *hid = w + L.hid, *hid_sh = w + L.hid_sh;
     const int64_t R = max_rows(c);
     const int N = c.N, d = c.d, h = c.h, hs = c.h_shared, Wd = gated ? 2 * h : h;
-    const int64_t Kall = wgrad_kall_bound(c), Tp = ((int64_t)c.T + 63) / 64 * 64;
     // pre-activations: kept by moe_forward (save_preact), else recomputed into the scratch
     const bool kept_pre = saves_preact(c);
     void *AB = kept_pre ? w + L.preact : bw + B.AB, *AB_sh = kept_pre ? w + L.preact_sh : bw + B.AB_sh;
     void *dO = bw + B.dO, *dH = bw + B.dH, *dAB = bw + B.dAB, *dX = bw + B.dX;
     float *dgate = reinterpret_cast<float *>(bw + B.dgate);
-    int32_t *kpre = reinterpret_cast<int32_t *>(bw + B.kpre);
     cudaError_t e = cudaSuccess;
     auto ok = [&](cudaError_t r) {
         if (e == cudaSuccess) e = r;
         return e == cudaSuccess;
     };
 
-    // The weight gradients' transposed operands run on an auxiliary stream beside the row
-    // products (HBM-bound copies beside tensor-bound products): the padding prefix and
-    // the forward's activations from the start, the recomputed router logits, dOᵀ once the
-    // slots are done and [dA | dB]ᵀ once the activation backward is. An event joins it
-    // before the weight gradients; without the stream (creation failed) it all runs in
-    // order on `stream`. The row products read the expert weights in their own layout
-    // (MN-major operands), so no weight is copied.
-    cudaStream_t aux = nullptr;
-    cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};  // fork, aux done, slots done, dA | dB done
-    bool two = cudaStreamCreateWithFlags(&aux, cudaStreamNonBlocking) == cudaSuccess;
-    for (int i = 0; i < 4 && two; ++i) two = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) == cudaSuccess;
-    if (two) two = cudaEventRecord(ev[0], stream) == cudaSuccess && cudaStreamWaitEvent(aux, ev[0], 0) == cudaSuccess;
-    const cudaStream_t sa = two ? aux : stream;
-    auto mark = [&](int i) {
-        if (two) ok(cudaEventRecord(ev[i], sa));
-    };
-    auto join = [&](int i) {
-        if (two) ok(cudaStreamWaitEvent(stream, ev[i], 0));
-    };
-    auto signal = [&](int i) {  // main stream -> auxiliary stream
-        if (two) {
-            ok(cudaEventRecord(ev[i], stream));
-            ok(cudaStreamWaitEvent(sa, ev[i], 0));
-        }
-    };
-
-    // -- auxiliary stream
-    // the weight gradients' operands that the forward left: each expert's rows padded to 64
-    ok(launch_pad_prefix(offsets, N, (int)R, kpre, sa));
-    ok(launch_transpose_rows_padded(hid, h, offsets, kpre, N, (int)R, Kall, bw + B.H_t, sa));
-    ok(launch_transpose_rows_padded(x_perm, d, offsets, kpre, N, (int)R, Kall, bw + B.X_t, sa));
-    if (hs) {
-        ok(launch_transpose_rows_padded(dy, d, nullptr, nullptr, 1, c.T, Tp, bw + B.dy_t, sa));
-        ok(launch_transpose_rows_padded(hid_sh, hs, nullptr, nullptr, 1, c.T, Tp, bw + B.Hsh_t, sa));
-    }
-    // xᵀ: the shared expert's and the router's weight gradients
-    ok(launch_transpose_rows_padded(x, d, nullptr, nullptr, 1, c.T, Tp, bw + B.x_t, sa));
-    // router logits: for N > 32 the forward's router left them in ws, else recomputed
+    // For N <= 32 the router logits are recomputed on an auxiliary stream beside the
+    // expert products (FMA-bound beside tensor-bound work), joined before the router
+    // backward; without the stream (creation failed) they run in order on `stream`. For
+    // N > 32 the forward left them in its workspace. Every other operand is read where
+    // the forward and the earlier steps left it: the row products take the expert weights
+    // and the weight gradients the activations in their own layouts (MN-major operands).
     const bool fwd_logits = N > 32;
     const float *logits = reinterpret_cast<const float *>(fwd_logits ? w + L.logits : bw + B.logits);
-    if (!fwd_logits)
+    cudaStream_t aux = nullptr;
+    cudaEvent_t ev[2] = {nullptr, nullptr};  // fork, logits done
+    bool two = !fwd_logits && cudaStreamCreateWithFlags(&aux, cudaStreamNonBlocking) == cudaSuccess;
+    for (int i = 0; i < 2 && two; ++i) two = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming) == cudaSuccess;
+    if (two) two = cudaEventRecord(ev[0], stream) == cudaSuccess && cudaStreamWaitEvent(aux, ev[0], 0) == cudaSuccess;
+    const cudaStream_t sa = two ? aux : stream;
+    if (!fwd_logits) {
         ok(launch_router_logits(c, x, w_r, c.has_router_bias ? b_r : nullptr, reinterpret_cast<float *>(bw + B.logits),
                                 w, sa));
+        if (two) ok(cudaEventRecord(ev[1], sa));
+    }
 
-    // -- main stream
     // gate-scaled dy per row and the gate gradients
     ok(launch_bwd_slots(c, dy, y_perm, slot_row, gate, dO, dgate, err, stream));
-    signal(2);
-    ok(launch_transpose_rows_padded(dO, d, offsets, kpre, N, (int)R, Kall, bw + B.dO_t, sa));
     // pre-activations, recomputed unless the forward kept them: [A | B] (gated) or A (ReLU)
     if (!kept_pre) {
         ok(launch_gemm_rows(c, gated, offsets, N, R, x_perm, w_gate_or_w1, w_up, d, h, AB, 0, nullptr, nullptr,
@@ -460,35 +431,35 @@ moe_status moe_backward(const moe_config *cfg, const void *x, const float *w_r, 
     // [dA | dB] from the pre-activations
     ok(launch_act_bwd(gated, AB, dH, R, h, dAB, stream));
     if (hs) ok(launch_act_bwd(true, AB_sh, bw + B.dH_sh, c.T, hs, bw + B.dAB_sh, stream));
-    signal(3);
-    ok(launch_transpose_rows_padded(dAB, Wd, offsets, kpre, N, (int)R, Kall, bw + B.dAB_t, sa));
-    if (hs)
-        ok(launch_transpose_rows_padded(bw + B.dAB_sh, 2 * hs, nullptr, nullptr, 1, c.T, Tp, bw + B.dABsh_t, sa));
-    mark(1);
     // dX = [dA | dB] [W_a ; W_b] (W_a, W_b [h][d] per expert: MN-major, K = Wd split at h)
     ok(launch_gemm_rows(c, false, offsets, N, R, dAB, w_gate_or_w1, gated ? w_up : nullptr, Wd, d, dX, hs ? c.T : 0,
                         bw + B.dAB_sh, shared_w_gate, shared_w_up, 2 * hs, d, bw + B.dX_sh, err, stream, true,
                         gated ? h : 0, hs));
-    // weight gradients: transposed activations with each expert's rows padded to 64
-    join(1);
+    // weight gradients over each expert's rows, the activations [rows][..] as MN-major operands
     const bool pair_ok = !(c.debug_flags & MOE_DEBUG_FFN_SINGLE);
-    ok(launch_wgrad(offsets, N, R, bw + B.dO_t, bw + B.H_t, Kall, d, h, dw_down, nullptr, nullptr, 0, nullptr, err,
+    const auto rows_op = [&](const void *q, int64_t ld) { return WgOperand{q, ld, R, true}; };
+    const auto tok_op = [&](const void *q, int64_t ld) { return WgOperand{q, ld, c.T, true}; };
+    const WgOperand none{nullptr, 0, 0, false};
+    const char *dAB_up = static_cast<const char *>(dAB) + (size_t)h * 2;
+    ok(launch_wgrad(offsets, N, R, rows_op(dO, d), rows_op(hid, h), d, h, dw_down, none, none, 0, nullptr, err,
                     stream, pair_ok));
-    ok(launch_wgrad(offsets, N, R, bw + B.dAB_t, bw + B.X_t, Kall, h, d, dw_gate_or_w1, nullptr, nullptr, 0, nullptr,
+    ok(launch_wgrad(offsets, N, R, rows_op(dAB, Wd), rows_op(x_perm, d), h, d, dw_gate_or_w1, none, none, 0, nullptr,
                     err, stream, pair_ok));
     if (gated)
-        ok(launch_wgrad(offsets, N, R, bw + B.dAB_t + (size_t)h * Kall * 2, bw + B.X_t, Kall, h, d, dw_up, nullptr,
-                        nullptr, 0, nullptr, err, stream, pair_ok));
+        ok(launch_wgrad(offsets, N, R, rows_op(dAB_up, Wd), rows_op(x_perm, d), h, d, dw_up, none, none, 0, nullptr,
+                        err, stream, pair_ok));
     if (hs) {
-        ok(launch_wgrad(nullptr, 0, 0, nullptr, nullptr, 0, d, hs, nullptr, bw + B.dy_t, bw + B.Hsh_t, (int)Tp,
+        const char *dABsh = reinterpret_cast<const char *>(bw + B.dAB_sh);
+        ok(launch_wgrad(nullptr, 0, 0, none, none, d, hs, nullptr, tok_op(dy, d), tok_op(hid_sh, hs), c.T,
                         dshared_w_down, err, stream, pair_ok));
-        ok(launch_wgrad(nullptr, 0, 0, nullptr, nullptr, 0, hs, d, nullptr, bw + B.dABsh_t, bw + B.x_t, (int)Tp,
+        ok(launch_wgrad(nullptr, 0, 0, none, none, hs, d, nullptr, tok_op(dABsh, 2 * hs), tok_op(x, d), c.T,
                         dshared_w_gate, err, stream, pair_ok));
-        ok(launch_wgrad(nullptr, 0, 0, nullptr, nullptr, 0, hs, d, nullptr, bw + B.dABsh_t + (size_t)hs * Tp * 2,
-                        bw + B.x_t, (int)Tp, dshared_w_up, err, stream, pair_ok));
+        ok(launch_wgrad(nullptr, 0, 0, none, none, hs, d, nullptr, tok_op(dABsh + (size_t)hs * 2, 2 * hs),
+                        tok_op(x, d), c.T, dshared_w_up, err, stream, pair_ok));
     }
     // router: dL, dx_router, dW_r, db
-    ok(launch_router_bwd(c, w_r, logits, idx, gate, B, bw, aux_coef, z_coef, dw_r, c.has_router_bias ? db_r : nullptr,
+    if (two) ok(cudaStreamWaitEvent(stream, ev[1], 0));
+    ok(launch_router_bwd(c, x, w_r, logits, idx, gate, B, bw, aux_coef, z_coef, dw_r, c.has_router_bias ? db_r : nullptr,
                          err, pair_ok, stream));
     // dx = dy + sum_j dX_r + dX_shared + dx_router
     ok(launch_bwd_dx(c, dy, dX, slot_row, hs ? bw + B.dX_sh : nullptr, reinterpret_cast<const float *>(bw + B.dxr), dx,

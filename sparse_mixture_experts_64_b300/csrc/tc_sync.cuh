@@ -33,6 +33,23 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatil
     }
 }
 
+// wait_bar for a barrier completed by a release arrival from the other CTA of the
+// cluster (acquire at cluster scope).
+__device__ __forceinline__ bool wait_bar_cluster(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                                 uint32_t *err) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > kTimeoutNs) {
+            *abort_flag = 1;
+            record_error(err, kErrTimeout);
+            return false;
+        }
+    }
+}
+
 // Wait without honouring the abort flag (used to drain work already in flight).
 __device__ __forceinline__ void drain_bar(uint64_t *bar, uint32_t parity) {
     const uint64_t t0 = globaltimer_ns();

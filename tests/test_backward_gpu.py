@@ -168,6 +168,24 @@ def test_backward_single_cta_kernels():
     _check(w, aux, z, moe.MOE_DEBUG_FFN_SINGLE)
 
 
+# every row product over several rounds of the persistent schedule (each CTA or CTA
+# pair takes several tiles in turn): 128-256 tiles on the 74 CTA pairs, 256-512 on the
+# 148 single CTAs
+ROUNDS = (_w("mixtral_prefill", T=2048, d=2048, h=2048, N=8, k=2), 0.01, 0.001)
+
+
+@pytest.mark.parametrize("kernel", ["pair", "single", "pair_kept"])
+def test_backward_over_several_rounds(kernel):
+    w, aux, z = ROUNDS
+    flags = moe.MOE_DEBUG_FFN_SINGLE if kernel == "single" else 0
+    out = _check(w, aux, z, flags, save_preact=kernel == "pair_kept")
+    if kernel == "pair_kept":
+        _, _, ref = _run(w, aux, z)
+        for key, t in out.items():
+            if t is not None:
+                assert torch.equal(t, ref[key]), key
+
+
 def _check(w, aux, z, flags, save_preact=False):
     inp, dy, out = _run(w, aux, z, debug_flags=flags, save_preact=save_preact)
     ref = O.backward(w, oracle_inputs(inp), _f(dy), aux_coef=aux, z_coef=z)

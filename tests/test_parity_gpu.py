@@ -103,6 +103,29 @@ def test_all_tensor_core_ffn_kernels(w):
     assert rel_max_err(outs["swap"]["y"], outs["single"]["y"]) <= 2e-2
 
 
+# every product over several rounds of the persistent schedule: 256 and 128 tiles on the
+# 74 CTA pairs, 512 and 256 on the 148 single CTAs
+ROUNDS = _small("mixtral_prefill", T=2048, d=2048, h=2048, N=8, k=2)
+
+
+@pytest.mark.parametrize("kernel", ["pair", "single"])
+def test_products_over_several_rounds(kernel):
+    """Each CTA (pair) of the persistent kernels takes several tiles in turn, with the
+    operand ring and both accumulators carried from tile to tile: the layer output and
+    the expert outputs of rows from every expert and 256-row block match the oracle."""
+    w = ROUNDS
+    flags = moe.MOE_DEBUG_FFN_PAIR if kernel == "pair" else moe.MOE_DEBUG_FFN_SINGLE
+    inp = W.make_inputs(w, device="cuda")
+    cfg = cfg_of(w, debug_flags=flags)
+    ws = moe.workspace(cfg)
+    sep = host(run_separate(cfg, inp, ws))
+    assert moe.moe_check_error(ws) == moe.MOE_OK
+    check_expert_rows(w, inp, sep, np.random.default_rng(5))
+    rt = O.forward(w, oracle_inputs(inp))
+    check_routing(sep, rt, sep=True)
+    check_output(sep["y"], rt["y"], w.dtype)
+
+
 @pytest.mark.parametrize("name", ["mixtral_prefill", "deepseek_fine"])
 def test_simt_and_tensor_core_ffn_agree(name):
     w = _small(name, T=160, d=256, h=256, N=8, k=2, h_shared=128 if name == "deepseek_fine" else 0)
