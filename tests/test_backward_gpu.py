@@ -59,11 +59,16 @@ CASES = [
 ]
 
 
-def _run(w, aux_coef, z_coef, seed=3, debug_flags=0, save_preact=False):
+def _run(w, aux_coef, z_coef, seed=3, debug_flags=0, save_preact=False, stale=False):
     cfg = cfg_of(w, debug_flags=debug_flags, save_preact=save_preact)
     inp = W.make_inputs(w, device="cuda")
     ws = moe.workspace(cfg)
     bws = moe.backward_workspace(cfg)
+    if stale:
+        # every byte 0xFF (NaN in bf16 and fp32) but the error word's region
+        ws.fill_(255)
+        ws[:256] = 0
+        bws.fill_(255)
     T, d, N, k = w.T, w.d, w.N, w.k
     y = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
     idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
@@ -186,8 +191,27 @@ def test_backward_over_several_rounds(kernel):
                 assert torch.equal(t, ref[key]), key
 
 
-def _check(w, aux, z, flags, save_preact=False):
-    inp, dy, out = _run(w, aux, z, debug_flags=flags, save_preact=save_preact)
+# capacity limits: the row buffers (N x capacity rows) are longer than the rows kept
+STALE = [(_w("switch_top1", T=333, d=128, h=256), 0.01, 0.001),
+         (_w("mixtral_prefill", T=600, d=256, h=384, N=8, k=2, capacity_factor=(5, 4)), 0.01, 0.001)]
+
+
+@pytest.mark.parametrize("kernel", ["pair", "single"])
+@pytest.mark.parametrize("w,aux,z", STALE, ids=[c[0].name for c in STALE])
+def test_backward_with_stale_workspaces(w, aux, z, kernel):
+    """Workspaces left with NaN bit patterns (every byte 0xFF but the error word): the
+    rows past the kept ones, which an expert's partial last k-block of the weight
+    gradients reaches into, then hold NaN unless zeroed on the way to the MMAs. The
+    forward and the gradients still match the oracle and hold no NaN."""
+    flags = moe.MOE_DEBUG_FFN_SINGLE if kernel == "single" else 0
+    out = _check(w, aux, z, flags, stale=True)
+    for key, t in out.items():
+        if t is not None:
+            assert not torch.isnan(t.float()).any(), key
+
+
+def _check(w, aux, z, flags, save_preact=False, stale=False):
+    inp, dy, out = _run(w, aux, z, debug_flags=flags, save_preact=save_preact, stale=stale)
     ref = O.backward(w, oracle_inputs(inp), _f(dy), aux_coef=aux, z_coef=z)
     errs = {"dx": _errs(_f(out["dx"]), ref["dx"]), "dw_r": _errs(_f(out["dw_r"]), ref["dw_r"])}
     if out["db_r"] is not None:
