@@ -15,8 +15,8 @@
 // accumulators — take tiles (expert, m, n) and store an all-zero tile for an expert
 // without rows. An optional shared segment (the shared expert, or with no
 // routed segment a plain product such as the router's gradients) reduces over K_sh,
-// with either operand MN-major ([K_sh][..], rows past K_sh read as zero by the copy) or
-// K-major ([M|Nn][K_sh], zero-padded to a multiple of 64).
+// with either operand MN-major ([rows][..], K-rows past its rows read as zero by the
+// copy) or K-major ([M|Nn][K_sh], zero-padded to a multiple of 64).
 #include <algorithm>
 #include <cstring>
 
@@ -69,7 +69,8 @@ __device__ __forceinline__ void seg_k_ranges(const WgParams &p, SegK &s, int lan
     if (lane == 0 && p.has_sh) {
         s.k0[p.n_seg] = 0;
         s.nk[p.n_seg] = (p.K_sh + BK - 1) / BK;
-        s.kv[p.n_seg] = 0;  // MN-major: rows past K_sh are outside the map (zero); K-major: zero-padded
+        s.kv[p.n_seg] = 0;  // MN-major: K-rows past the operand's rows are outside its map (zero);
+                            // K-major: zero-padded
     }
 }
 
