@@ -56,6 +56,9 @@ CASES = [
     (_w("deepseek_fine", T=64, d=256, N=64, k=2, h=256, h_shared=256), 0.01, 0.0),
     # N = 128: both router-gradient products on CTA pairs (2N = 256 and T = 320 rows)
     (_w("deepseek_fine", T=320, d=256, N=128, k=4, h=128, h_shared=0), 0.01, 0.001),
+    # the DeepSeekMoE structure: 256 experts, top-8 and a shared expert (257 segments in
+    # the row products, about 16 rows per expert, partial k-blocks everywhere)
+    (_w("deepseek_fine", T=512, d=128, N=256, k=8, h=128, h_shared=128), 0.01, 0.001),
 ]
 
 
