@@ -75,7 +75,7 @@ def _args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-variants", action="store_true",
-                    help="skip the training-router and backward variant timing")
+                    help="skip the training-router, sharded-router and backward variant timing")
     ap.add_argument("--workloads", default="auto", choices=["auto", "all", "none"],
                     help="also measure the other workloads of the layer (auto: when the default "
                          "workload runs on one GPU without overrides)")
@@ -479,6 +479,106 @@ def measure_router_train(w, inp, cfg, ws, stream, dev, cpu_tokens: int) -> dict:
     return out
 
 
+def measure_router_sharded(w, inp, stream, dev, cpu_tokens: int, shards: int = 2, capacity_factor=(5, 4)) -> dict:
+    """GShard-style top-k with one capacity for the whole batch (factor 1.25) over the
+    batch split into `shards` token shards in token order, as that many ranks would hold
+    it, the shards run one after another on this GPU: phase 1 (moe_router_shard_stats:
+    routing and the per-(expert, slot) statistics) per shard, the exchange's host step
+    (the statistics copied to the host, the global priorities and the rank-order sums,
+    the results copied back: on ranks, an all-gather), phase 2 (moe_router_shard_assign:
+    the capacity decisions at the global priorities) per shard. Against moe_router_topk on
+    the whole batch with the same capacity, whose kept counts the shards' must add up to
+    bit for bit; the logits' share of the fp32 FMA peak; the oracle's routing timed on a
+    token sample of the host cores."""
+    import numpy as np
+
+    import sparse_mixture_experts_64_b300 as moe
+    from sparse_mixture_experts_64_b300 import sharded
+    wg = w.replace(capacity_factor=capacity_factor)
+    T, k, N = wg.T, wg.k, wg.N
+    i32 = dict(dtype=torch.int32, device=dev)
+    cfg_of = lambda ww: moe.make_config(**{f: getattr(ww, f) for f in ww.__dataclass_fields__})  # noqa: E731
+    cuts = [T * r // shards for r in range(shards + 1)]
+    sh = []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        c = cfg_of(wg.replace(T=b - a, capacity_factor=None))
+        sh.append(dict(a=a, b=b, cfg=c, ws=moe.workspace(c, device=dev), x=inp["x"][a:b],
+                       idx=torch.empty((b - a, k), **i32), gate=torch.empty((b - a, k), device=dev),
+                       cnt=torch.empty((N, k), **i32), psum=torch.empty(N, device=dev),
+                       kept=torch.empty(N, **i32), off=torch.empty(N + 1, **i32),
+                       slot_row=torch.empty((b - a, k), **i32),
+                       perm=torch.empty(moe.moe_max_rows(c), **i32), aux=torch.empty(2, device=dev)))
+    C = sharded.global_capacity(T, N, capacity_factor)
+    glob = {}
+
+    def phase1():
+        for s in sh:
+            moe.moe_router_shard_stats(s["cfg"], s["x"], inp["w_r"], inp["b_r"], s["idx"], s["gate"], s["cnt"],
+                                       s["psum"], s["ws"], stream)
+
+    def exchange():
+        counts = np.stack([s["cnt"].cpu().numpy() for s in sh])
+        bases = sharded.slot_bases(counts)
+        psum = np.zeros(N, np.float32)
+        for s in sh:  # rank order
+            psum = (psum + s["psum"].cpu().numpy()).astype(np.float32)
+        glob["routed"] = torch.as_tensor(counts.sum(axis=(0, 2)), dtype=torch.int32).to(dev)
+        glob["psum"] = torch.as_tensor(psum).to(dev)
+        for r, s in enumerate(sh):
+            s["base"] = torch.as_tensor(bases[r], dtype=torch.int32).to(dev)
+        torch.cuda.synchronize()
+
+    def phase2():
+        for s in sh:
+            moe.moe_router_shard_assign(s["cfg"], s["idx"], s["base"], C, glob["routed"], glob["psum"], T, s["kept"],
+                                        s["off"], s["slot_row"], s["perm"], s["aux"], s["ws"], stream)
+    iters = 20
+    ms1 = _time_calls(phase1, stream, iters) / shards
+    torch.cuda.synchronize()
+    host = []
+    for _ in range(iters):
+        t0 = time.perf_counter()
+        exchange()
+        host.append((time.perf_counter() - t0) * 1e3)
+    ms2 = _time_calls(phase2, stream, iters) / shards
+    # the whole batch with the same capacity on one router call
+    cw = cfg_of(wg)
+    ws_w = moe.workspace(cw, device=dev)
+    o = [torch.empty((T, k), **i32), torch.empty((T, k), device=dev), torch.empty(N, **i32), torch.empty(N, **i32),
+         torch.empty(N + 1, **i32), torch.empty((T, k), **i32), torch.empty(moe.moe_max_rows(cw), **i32),
+         torch.empty(2, device=dev)]
+    ms_w = _time_calls(lambda: moe.moe_router_topk(cw, inp["x"], inp["w_r"], inp["b_r"], *o, ws_w, stream),
+                       stream, iters)
+    for s in sh + [dict(ws=ws_w)]:
+        st = moe.moe_check_error(s["ws"], stream)
+        if st != moe.MOE_OK:
+            raise RuntimeError("device error word: " + moe.status_str(st))
+    kept_shards = sum(s["kept"].cpu().numpy().astype(np.int64) for s in sh)
+    if not np.array_equal(kept_shards, o[3].cpu().numpy()):
+        raise RuntimeError("sharded capacity decisions differ from the whole batch's")
+    ms_x = statistics.median(host)
+    fma_peak = 148 * 128 * 2 * 2.032e9
+    flops = 2.0 * (T // shards) * w.d * N
+    out = {"shards": shards, "capacity_factor": list(capacity_factor), "capacity": C, "top_k": k,
+           "phase1_ms_per_shard": ms1, "exchange_host_ms": ms_x, "phase2_ms_per_shard": ms2,
+           "rank_ms": ms1 + ms_x + ms2, "tokens_per_s_per_rank": (T / shards) / ((ms1 + ms_x + ms2) / 1e3),
+           "whole_batch_router_ms": ms_w, "kept_counts_equal_whole_batch": True,
+           "dropped_slots": int(T * k - int(kept_shards.sum())), "bound": "alu",
+           "frac": flops / (ms1 / 1e3) / fma_peak,
+           "peak": "148 SMs x 128 FP32 lanes x 2 x 2032 MHz (fp32 FMA, phase 1's logits)",
+           "exchange": "host step standing in for the all-gather of N x k counts and N sums per rank"}
+    if cpu_tokens > 0:
+        from oracle import moe_oracle as O
+        n = min(T, cpu_tokens)
+        xs = inp["x"][:n].float().cpu().numpy()
+        t0 = time.perf_counter()
+        O.route(wg.replace(T=n), xs, inp["w_r"].cpu().numpy(),
+                None if inp["b_r"] is None else inp["b_r"].cpu().numpy())
+        secs = time.perf_counter() - t0
+        out["cpu_oracle"] = {"tokens_per_s": n / secs, "sample_tokens": n, "cores": 1, "kind": "oracle"}
+    return out
+
+
 def measure_backward(w, inp, cfg, ws, stream, dev, peaks, host_inp=None, cpu_tokens: int = 16) -> dict:
     """The training step's backward: moe_forward with save_preact (it keeps the experts'
     pre-activations) and moe_backward on the same inputs. CUDA-event times of the
@@ -828,7 +928,8 @@ def measure(a, w, world, rank, local, primary: bool = True) -> dict:
     cpu = rank == 0 and world == 1 and not a.no_cpu_baseline
     host_inp = _oracle_inputs(inp, w) if cpu and primary else None
     if primary and not a.no_variants and not ec:
-        line["variants"] = {"router_train": measure_router_train(w, inp, cfg, ws, stream, dev, 512 if cpu else 0)}
+        line["variants"] = {"router_train": measure_router_train(w, inp, cfg, ws, stream, dev, 512 if cpu else 0),
+                            "router_sharded": measure_router_sharded(w, inp, stream, dev, 512 if cpu else 0)}
         if w.dtype == "bf16":
             line["variants"]["backward"] = measure_backward(w, inp, cfg, ws, stream, dev, peaks, host_inp)
 
