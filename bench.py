@@ -15,8 +15,9 @@ the time is the max over ranks and `value` counts the tokens of all ranks.
 
 On one GPU the default run also measures the layer's other workloads (the
 DeepSeekMoE-shaped layer, Mixtral-shaped decode at T = 16, 64 and 128, Switch
-top-1 with capacity, tiny fp32) the same way, each under "workloads" in the same
-line, with its own oracle baseline on a bounded sample.
+top-1 with capacity, tiny fp32, Expert Choice routing of the Mixtral-shaped layer)
+the same way, each under "workloads" in the same line, with its own oracle baseline
+on a bounded sample.
 
 Prints one JSON line on rank 0.
 """
@@ -85,9 +86,10 @@ def _args():
 
 
 # The other workloads measured in the same run as the default one (one GPU): every
-# configuration the layer is specified on besides the Mixtral-shaped prefill layer.
+# configuration the layer is specified on besides the Mixtral-shaped prefill layer, and
+# Expert Choice routing of that layer.
 SECONDARY = ["deepseek_fine", "mixtral_decode_16", "mixtral_decode_64", "mixtral_decode_128",
-             "switch_top1", "tiny_fp32"]
+             "switch_top1", "tiny_fp32", "mixtral_expert_choice"]
 
 
 # --------------------------------------------------------------------------- helpers
@@ -361,16 +363,21 @@ def oracle_sample_baseline(w, inp, cpu_seconds: float) -> dict:
         host[nme] = None if inp[nme] is None else inp[nme].float().cpu().numpy()
     x_all = inp["x"].float().cpu().numpy()
 
+    ec = w.routing == "expert_choice"
+
     def one_pass(n):
         wn = w.replace(T=n)
         hn = dict(host, x=x_all[:n])
-        rt = O.route(wn, hn["x"], hn["w_r"], hn["b_r"])          # untimed: which experts to fetch
-        for e in np.unique(rt["topk_idx"]):
+        if ec:  # every expert takes its top tokens
+            experts = range(w.N)
+        else:   # untimed: which experts to fetch
+            experts = np.unique(O.route(wn, hn["x"], hn["w_r"], hn["b_r"])["topk_idx"])
+        for e in experts:
             for nme in ("w_gate", "w_up", "w_down"):
                 if hn[nme] is not None:
                     hn[nme][int(e)]
         t0 = time.perf_counter()
-        O.forward(wn, hn)
+        (O.forward_expert_choice if ec else O.forward)(wn, hn)
         return time.perf_counter() - t0
 
     n, secs = 1, one_pass(1)
