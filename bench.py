@@ -939,6 +939,9 @@ def measure(a, w, world, rank, local, primary: bool = True) -> dict:
                             "router_sharded": measure_router_sharded(w, inp, stream, dev, 512 if cpu else 0)}
         if w.dtype == "bf16":
             line["variants"]["backward"] = measure_backward(w, inp, cfg, ws, stream, dev, peaks, host_inp)
+    elif not primary and not a.no_variants and w.name == "deepseek_fine":
+        # the backward of the fine-grained layer as well (its oracle too slow to time beside it)
+        line["variants"] = {"backward": measure_backward(w, inp, cfg, ws, stream, dev, peaks, None)}
 
     # ---- CPU oracle baseline (rank 0, single process only)
     if cpu and not primary:
@@ -963,7 +966,7 @@ def _summary(sub: dict) -> dict:
     """The fields of a secondary workload's record kept in the headline line."""
     keep = ("value", "unit", "ms_per_step", "dtype", "config", "layer_roofline", "stages_ms",
             "weight_stream_gbs", "rows_dispatched", "gpu_launches", "clocks", "cpu_baseline", "e2e",
-            "stream_launch_ms_per_step")
+            "stream_launch_ms_per_step", "variants")
     out = {k: sub[k] for k in keep if k in sub}
     r = sub["roofline"]
     out["roofline"] = {k: r[k] for k in ("kernel", "bound", "achieved", "peak", "unit", "frac", "traffic",
